@@ -1,0 +1,234 @@
+"""ORACLE -- test infrastructure only.
+
+A plain CPU restatement of the ONNX ``MatMul`` operator used to check the CUDA
+library.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` may import it; the product package never does, and this
+package imports nothing from the product.
+
+Two halves:
+
+* ``oracle.c`` (compiled on first use with gcc into ``oracle/_build``): the
+  2-D product with the pages' accumulation rules and the binary16 / bfloat16
+  encode and decode.
+* this module: the shape rules and the batch loop.
+
+Shape rules (MatMul Kernel Design, section "Shape and plan model"; Gemm and
+MatMul Performance Roadmap, section "Phase 4: complete MatMul"):
+
+1. a rank-one A ``[K]`` is read as ``[1, K]`` and a rank-one B ``[K]`` as
+   ``[K, 1]``; the promoted dimension is dropped from the output;
+2. the leading (batch) dimensions of the two operands are aligned on the
+   right and broadcast: equal extents stay, an extent of 1 stretches to the
+   other operand's extent, anything else is an error;
+3. every output batch item ``b`` multiplies the A matrix and the B matrix that
+   ``b`` selects, where an operand's index along a dimension it broadcasts
+   (extent 1) is 0;
+4. an output with no elements is returned without reading the inputs.
+
+Readings where the pages are silent (each is listed in the design doc): rank-0
+operands are rejected; broadcasting an extent 0 against 1 gives 0 and against
+n > 1 is an error; K == 0 with a non-empty output gives zeros; two rank-one
+operands give a rank-0 (one element) output.
+
+Values are passed as numpy arrays: float32 / float64 for FLOAT / DOUBLE, and
+uint16 bit patterns for FLOAT16 / BFLOAT16 (numpy has no bfloat16).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import itertools
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD_DIR, "liboracle.so")
+_SRC = os.path.join(_HERE, "oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+DTYPES = ("float32", "float64", "float16", "bfloat16")
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_SO)
+            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+        return _SO
+    tmp = _SO + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        for name in ("oracle_gemm_f32", "oracle_gemm_f64", "oracle_gemm_f16", "oracle_gemm_bf16"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i64, i64, i64, p, p, p, i64, p, p]
+            fn.restype = None
+        for name in ("oracle_decode_f16", "oracle_decode_bf16", "oracle_encode_f16",
+                     "oracle_encode_bf16"):
+            fn = getattr(lib, name)
+            fn.argtypes = [p, p, i64]
+            fn.restype = None
+        lib.oracle_threads.argtypes = []
+        lib.oracle_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def threads() -> int:
+    """Host threads the oracle's parallel loops use."""
+    return int(_load().oracle_threads())
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# --------------------------------------------------------------------------
+# binary16 / bfloat16 bit patterns <-> float32
+
+def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """uint16 patterns of ``dtype`` ("float16" / "bfloat16") -> exact float32."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, np.float32)
+    fn = _load().oracle_decode_f16 if dtype == "float16" else _load().oracle_decode_bf16
+    fn(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def encode(values: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 -> uint16 patterns of ``dtype``, round to nearest even."""
+    values = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(values.shape, np.uint16)
+    fn = _load().oracle_encode_f16 if dtype == "float16" else _load().oracle_encode_bf16
+    fn(_ptr(values), _ptr(out), values.size)
+    return out
+
+
+# --------------------------------------------------------------------------
+# shape rules
+
+class ShapeError(ValueError):
+    """The operand shapes have no MatMul product."""
+
+
+def output_shape(a_shape, b_shape):
+    """Output shape of MatMul(A, B), following the promote / broadcast /
+    squeeze rules above.  Raises ShapeError for shapes with no product."""
+    a_shape, b_shape = [int(d) for d in a_shape], [int(d) for d in b_shape]
+    if len(a_shape) == 0 or len(b_shape) == 0:
+        raise ShapeError("rank-0 operand")
+    if any(d < 0 for d in a_shape + b_shape):
+        raise ShapeError("negative dimension")
+    a2 = [1] + a_shape if len(a_shape) == 1 else a_shape
+    b2 = b_shape + [1] if len(b_shape) == 1 else b_shape
+    m, ka = a2[-2], a2[-1]
+    kb, n = b2[-2], b2[-1]
+    if ka != kb:
+        raise ShapeError("inner dimensions differ: %d vs %d" % (ka, kb))
+    batch = _broadcast(a2[:-2], b2[:-2])
+    out = list(batch)
+    if len(a_shape) > 1:
+        out.append(m)
+    if len(b_shape) > 1:
+        out.append(n)
+    return tuple(out)
+
+
+def _broadcast(a_batch, b_batch):
+    """Right-aligned multidirectional broadcast of two batch shapes."""
+    r = max(len(a_batch), len(b_batch))
+    a = [1] * (r - len(a_batch)) + list(a_batch)
+    b = [1] * (r - len(b_batch)) + list(b_batch)
+    out = []
+    for da, db in zip(a, b):
+        if da == db:
+            out.append(da)
+        elif da == 1:
+            out.append(db)
+        elif db == 1:
+            out.append(da)
+        else:
+            raise ShapeError("batch dimensions %d and %d do not broadcast" % (da, db))
+    return out
+
+
+# --------------------------------------------------------------------------
+# the product
+
+def gemm2d(a: np.ndarray, b: np.ndarray, dtype: str, rows=None):
+    """One 2-D product A[M, K] @ B[K, N] with the accumulation rules of
+    ``dtype``.  ``rows``: optional list of output rows to compute.  Returns
+    (Y, S) with Y in the storage type of ``dtype`` and S = sum |a||b| (float64),
+    both [len(rows) or M, N]."""
+    lib = _load()
+    store = {"float32": np.float32, "float64": np.float64,
+             "float16": np.uint16, "bfloat16": np.uint16}[dtype]
+    a = np.ascontiguousarray(a, dtype=store)
+    b = np.ascontiguousarray(b, dtype=store)
+    m, k = a.shape
+    k2, n = b.shape
+    assert k == k2
+    if rows is None:
+        rows_arr, nrows, rows_p = None, m, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        assert rows_arr.size == 0 or (rows_arr.min() >= 0 and rows_arr.max() < m)
+        nrows, rows_p = rows_arr.size, _ptr(rows_arr)
+    y = np.zeros((nrows, n), store)
+    s = np.zeros((nrows, n), np.float64)
+    if nrows == 0 or n == 0:
+        return y, s
+    fn = {"float32": lib.oracle_gemm_f32, "float64": lib.oracle_gemm_f64,
+          "float16": lib.oracle_gemm_f16, "bfloat16": lib.oracle_gemm_bf16}[dtype]
+    fn(m, n, k, _ptr(a), _ptr(b), rows_p, nrows, _ptr(y), _ptr(s))
+    return y, s
+
+
+def matmul(a: np.ndarray, b: np.ndarray, dtype: str):
+    """ONNX MatMul of two dense row-major arrays.  Returns (Y, S), both of the
+    output shape; Y in the storage type of ``dtype``, S = sum |a||b| per
+    output element (float64)."""
+    if dtype not in DTYPES:
+        raise ValueError("unsupported dtype %r" % dtype)
+    out_shape = output_shape(a.shape, b.shape)
+    store = {"float32": np.float32, "float64": np.float64,
+             "float16": np.uint16, "bfloat16": np.uint16}[dtype]
+    a2 = a.reshape((1,) + a.shape) if a.ndim == 1 else a
+    b2 = b.reshape(b.shape + (1,)) if b.ndim == 1 else b
+    m, n = a2.shape[-2], b2.shape[-1]
+    batch = _broadcast(a2.shape[:-2], b2.shape[:-2])
+    r = len(batch)
+    a_batch = [1] * (r - (a2.ndim - 2)) + list(a2.shape[:-2])
+    b_batch = [1] * (r - (b2.ndim - 2)) + list(b2.shape[:-2])
+    a3 = a2.reshape(a_batch + [m, a2.shape[-1]])
+    b3 = b2.reshape(b_batch + [b2.shape[-2], n])
+    y = np.zeros(batch + [m, n], store)
+    s = np.zeros(batch + [m, n], np.float64)
+    for idx in itertools.product(*[range(d) for d in batch]):
+        ia = tuple(0 if da == 1 else i for i, da in zip(idx, a_batch))
+        ib = tuple(0 if db == 1 else i for i, db in zip(idx, b_batch))
+        y[idx], s[idx] = gemm2d(a3[ia], b3[ib], dtype)
+    return y.reshape(out_shape), s.reshape(out_shape)
+
+
+def to_float64(y: np.ndarray, dtype: str) -> np.ndarray:
+    """Values of a result array as float64 (16-bit patterns decoded)."""
+    if dtype in ("float16", "bfloat16"):
+        return decode(y, dtype).astype(np.float64)
+    return y.astype(np.float64)
