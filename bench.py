@@ -1,0 +1,556 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 ONNX MatMul library; prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-secondary] [--no-cpu-baseline]
+
+A step is one pass over every product of the workload (default: the BF16
+transformer projections [8,2048,4096]x[4096,4096], [8,2048,4096]x[4096,14336]
+and [8,2048,14336]x[14336,4096]) with the operands already resident in HBM.
+`value` is the whole job's TFLOP/s (GB/s for the bandwidth-bound workloads):
+the flops all ranks computed divided by the slowest rank's timed region.
+With N > 1 (torchrun), every rank runs its own copy of the workload on its own
+GPU (independent problems, no data-path collective; weak scaling).
+
+`--impl reference` times the CPU oracle on a bounded row sample of the same
+workload instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MatMul TFLOP/s (BF16/FP16/FP32/FP64) and skinny GB/s, % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dense tensor-core ratio of FP16 to BF16 (equal) and the FP32/FP64 SIMT
+# peaks derived from unit counts and the maximum SM clock
+SM_COUNT_GB300 = 152
+FP32_LANES_PER_SM = 128
+FP64_FLOPS_PER_SM_PER_CLK = 4.0   # ~1.25 TFLOP/s at 2.07 GHz over 152 SMs, FMA = 2 flops
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# workload accounting
+
+
+def _out_shape(a_shape, b_shape):
+    a2 = (1,) + tuple(a_shape) if len(a_shape) == 1 else tuple(a_shape)
+    b2 = tuple(b_shape) + (1,) if len(b_shape) == 1 else tuple(b_shape)
+    import numpy as np
+    batch = np.broadcast_shapes(a2[:-2], b2[:-2])
+    return batch, a2[-2], a2[-1], b2[-1]
+
+
+def work_of(a_shape, b_shape, dtype):
+    from gemm_matmulplan_broadcast_gb300.synth import ELEMENT_BYTES
+    import numpy as np
+    batch, m, k, n = _out_shape(a_shape, b_shape)
+    items = int(np.prod(batch, dtype=np.int64)) if len(batch) else 1
+    eb = ELEMENT_BYTES[dtype]
+    flop = 2.0 * m * n * k * items
+    byts = eb * (int(np.prod(a_shape)) + int(np.prod(b_shape)) + items * m * n)
+    return flop, float(byts)
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) >= 9:
+                    rows.append([c.strip() for c in r])
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = []
+        for i, nm in enumerate(names):
+            if any(r[5 + i].lower().startswith("active") for r in rows):
+                reasons.append(nm)
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------
+# multi-rank aggregation (also exercised by the gloo tests)
+
+
+def aggregate(local_seconds: float, local_units: float, group=None):
+    """(max seconds over ranks, sum of units over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_seconds, local_units
+    backend = dist.get_backend(group)
+    dev = "cuda" if backend == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# traffic figures from committed ncu summaries
+
+
+def committed_traffic(kernel_key: str):
+    """Per-launch DRAM bytes recorded from an ncu capture, if the kernel's
+    source is unchanged since (source hash recorded with the figure)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = table.get(kernel_key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    if h != ent.get("sha256"):
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# our implementation
+
+
+def build_inputs(workload, device):
+    """Per product: (A, B, Y) device tensors and the plan."""
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import Plan
+    items = []
+    for prod in workload.products:
+        a, b = prod.draw()
+        plan = Plan(prod.a_shape, prod.b_shape, prod.dtype)
+        A = a.to(device)
+        B = b.to(device)
+        Y = torch.empty(plan.output_shape, dtype=a.dtype, device=device)
+        flop, byts = work_of(prod.a_shape, prod.b_shape, prod.dtype)
+        items.append({"name": prod.name, "plan": plan, "A": A, "B": B, "Y": Y, "a": a, "b": b,
+                      "flop": flop, "bytes": byts, "dtype": prod.dtype})
+    return items
+
+
+def rotate_sets(items, min_total_bytes, device):
+    """Extra copies of the operands so that consecutive executes of the same
+    product touch different memory (inputs larger than L2 in total)."""
+    import torch
+    for it in items:
+        per = it["bytes"]
+        n = 1
+        while per * n < min_total_bytes and n < 16:
+            n += 1
+        sets = [(it["A"], it["B"], it["Y"])]
+        for _ in range(n - 1):
+            sets.append((it["A"].clone(), it["B"].clone(), torch.empty_like(it["Y"])))
+        it["sets"] = sets
+
+
+def time_steps(items, steps, stream):
+    """Run `steps` steps; returns (total seconds by the outer events,
+    per-product list of per-launch milliseconds)."""
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)] for _ in items]
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for s in range(steps):
+            for i, it in enumerate(items):
+                A, B, Y = it["sets"][s % len(it["sets"])]
+                e0, e1 = evs[i][s]
+                e0.record(stream)
+                it["plan"].execute(A, B, Y, stream=stream)
+                e1.record(stream)
+        end.record(stream)
+    end.synchronize()
+    total = start.elapsed_time(end) / 1e3
+    per = [[e0.elapsed_time(e1) for (e0, e1) in evs[i]] for i in range(len(items))]
+    return total, per
+
+
+def time_e2e(items, steps, stream):
+    """End to end through olc_matmul_execute_host: pinned host inputs copied
+    in, kernels, result copied out, every step."""
+    import torch
+    host = []
+    for it in items:
+        ah = it["a"].pin_memory()
+        bh = it["b"].pin_memory()
+        yh = torch.empty(tuple(it["Y"].shape), dtype=it["Y"].dtype).pin_memory()
+        host.append((ah, bh, yh))
+    h2d = sum(h[0].numel() * h[0].element_size() + h[1].numel() * h[1].element_size()
+              for h in host)
+    d2h = sum(h[2].numel() * h[2].element_size() for h in host)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+
+    def one_step():
+        for it, (ah, bh, yh) in zip(items, host):
+            it["plan"].execute_host(ah, bh, yh, it["A"], it["B"], it["Y"], stream=stream)
+
+    one_step()
+    stream.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        one_step()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3, h2d, d2h
+
+
+def cpu_oracle_sample(workload, target_seconds: float, items=None):
+    """Time the oracle on a seeded row sample of every product, sized so the
+    whole sample takes about `target_seconds`.  Returns (flops, seconds,
+    threads, description)."""
+    import numpy as np
+    import oracle
+    from gemm_matmulplan_broadcast_gb300 import synth
+    prods = []
+    for prod in workload.products:
+        if items is not None:
+            it = next(x for x in items if x["name"] == prod.name)
+            a, b = it["a"], it["b"]
+        else:
+            a, b = prod.draw()
+        batch, m, k, n = _out_shape(prod.a_shape, prod.b_shape)
+        if len(batch) and int(np.prod(batch)) == 0 or m * n == 0:
+            continue
+        an = synth.to_numpy_storage(a)
+        bn = synth.to_numpy_storage(b)
+        # timing sample: A's rows (all batch items stacked) against one B matrix
+        an = an.reshape((1, k) if an.ndim == 1 else (-1, k))
+        bn = bn.reshape((k, 1)) if bn.ndim == 1 else bn.reshape((-1, k, n))[0]
+        prods.append((prod, an, np.ascontiguousarray(bn), n, k))
+    # calibrate with one row of each product
+    rows = 1
+    t0 = time.perf_counter()
+    for prod, an, bn, n, k in prods:
+        oracle.gemm2d(an, bn, prod.dtype, rows=[0])
+    t1 = time.perf_counter() - t0
+    per_row = max(t1, 1e-6)
+    rows = int(max(1, min(4096, target_seconds / per_row)))
+    rng = np.random.default_rng(0)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for prod, an, bn, n, k in prods:
+        r = min(rows, an.shape[0])
+        sel = np.sort(rng.choice(an.shape[0], size=r, replace=False))
+        oracle.gemm2d(an, bn, prod.dtype, rows=sel)
+        flops += 2.0 * r * n * k
+    secs = time.perf_counter() - t0
+    desc = "%d rows of each of %d products (all N columns, full K), oracle C triple loop" % (
+        rows, len(prods))
+    return flops, secs, oracle.threads(), desc
+
+
+def roofline_for(item, ms_per_launch, peaks, long_region: bool):
+    """Roofline entry for one product's kernel."""
+    dt = item["dtype"]
+    algo = item["plan"].algorithm
+    if algo in ("skinny_m", "skinny_n", "split_k"):
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        achieved = item["bytes"] / (ms_per_launch / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+    if dt in ("bfloat16", "float16"):
+        key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+        peak = peaks.get(key, FALLBACK_PEAKS[key])   # fp16 dense rate equals bf16
+        achieved = item["flop"] / (ms_per_launch / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    clk = peaks.get("sm_max_mhz", 2070.0) * 1e6
+    if dt == "float32":
+        peak = SM_COUNT_GB300 * FP32_LANES_PER_SM * 2 * clk / 1e12
+    else:
+        peak = SM_COUNT_GB300 * FP64_FLOPS_PER_SM_PER_CLK * clk / 1e12
+    achieved = item["flop"] / (ms_per_launch / 1e3) / 1e12
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak}
+
+
+def kernel_key(item):
+    return "%s:%s:%s" % (item["plan"].algorithm, item["dtype"], item["name"])
+
+
+def measure_workload(workload, steps, warmup, device, peaks, l2_bytes):
+    import torch
+    items = build_inputs(workload, device)
+    rotate_sets(items, 2 * l2_bytes, device)
+    stream = torch.cuda.Stream()
+    for _ in range(warmup):
+        time_steps(items, 1, stream)
+    torch.cuda.synchronize()
+    return items, stream
+
+
+def run_ours(args):
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import load, synth
+    rank, world, local = dist_setup(args)
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    load()
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 129 * 1024 * 1024) or 129 * 1024 * 1024
+
+    workload = synth.workload(args.workload)
+    items, stream = measure_workload(workload, args.steps, args.warmup, device, peaks, l2)
+    flop_step = sum(it["flop"] for it in items)
+    byte_step = sum(it["bytes"] for it in items)
+    bw_bound = all(it["plan"].algorithm in ("skinny_m", "skinny_n", "split_k") for it in items)
+
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    total, per = time_steps(items, args.steps, stream)
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    barrier()
+    secs, units = aggregate(total, (byte_step if bw_bound else flop_step) * args.steps)
+    value = units / secs / (1e9 if bw_bound else 1e12)
+    unit = "GB/s" if bw_bound else "TFLOP/s"
+
+    # dominant kernel: the product with the largest total time
+    means = [statistics.mean(p) for p in per]
+    dom = max(range(len(items)), key=lambda i: means[i])
+    long_region = total > 1.0
+    roof = roofline_for(items[dom], means[dom], peaks, long_region)
+    roof["kernel"] = kernel_key(items[dom])
+    roof["traffic"] = committed_traffic(kernel_key(items[dom]))
+    roof["peak_source"] = peak_src + (" sustained" if (roof["bound"] == "tensor" and long_region)
+                                      else " burst" if roof["bound"] == "tensor" else "")
+    breakdown = []
+    for i, it in enumerate(items):
+        r = roofline_for(it, means[i], peaks, long_region)
+        breakdown.append({"product": it["name"], "algorithm": it["plan"].algorithm,
+                          "ms_per_launch": means[i], "achieved": r["achieved"], "unit": r["unit"],
+                          "frac": r["frac"], "bound": r["bound"],
+                          "p10_ms": sorted(per[i])[len(per[i]) // 10],
+                          "p90_ms": sorted(per[i])[(len(per[i]) * 9) // 10]})
+
+    # end to end through the host-buffer entry point
+    e2e_secs, h2d, d2h = time_e2e(items, max(1, min(args.steps, 5)), stream)
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_secs_all, e2e_units = aggregate(e2e_secs, (byte_step if bw_bound else flop_step) * e2e_steps)
+    e2e = {"value": e2e_units / e2e_secs_all / (1e9 if bw_bound else 1e12), "unit": unit,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    secondary = {}
+    if not args.no_secondary and args.workload == "bf16_transformer_projection":
+        for wname in ("fp16_skinny_splitk",):
+            w2 = synth.workload(wname)
+            its2, st2 = measure_workload(w2, 20, 3, device, peaks, l2)
+            _, per2 = time_steps(its2, 20, st2)
+            res = []
+            for i, it in enumerate(its2):
+                ms = statistics.median(per2[i])
+                r = roofline_for(it, ms, peaks, False)
+                res.append({"product": it["name"], "algorithm": it["plan"].algorithm,
+                            "ms_per_launch": ms, "achieved": r["achieved"], "unit": r["unit"],
+                            "frac": r["frac"], "bound": r["bound"]})
+            secondary[wname] = res
+            del its2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        fl, cs, cores, desc = cpu_oracle_sample(workload, args.cpu_seconds, items)
+        cpu = {"value": fl / cs / (1e12 if not bw_bound else 1.0), "unit": unit if not bw_bound else "flop/s",
+               "cores": cores, "kind": "oracle", "sample": desc, "seconds": cs}
+
+    launches = sum(it["plan"].launches for it in items) * args.steps
+    dtypes = sorted({it["dtype"] for it in items})
+    short = {"bfloat16": "bf16", "float16": "f16", "float32": "f32", "float64": "f64"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "+".join(short[d] for d in dtypes),
+        "data": "synthetic (seeded torch CPU generator, cast RNE; see DESIGN.md input recipe)",
+        "config": {
+            "workload": workload.name,
+            "description": workload.description,
+            "products": [{"a": list(p.a_shape), "b": list(p.b_shape), "dtype": p.dtype}
+                         for p in workload.products],
+            "l2": "inputs larger than L2: each product rotates over operand sets totalling "
+                  ">= 2x L2 (%d MB)" % (l2 // (1 << 20)),
+            "parallelism": "independent replicas per GPU" if world > 1 else "single GPU",
+        },
+        "roofline": roof,
+        "breakdown": breakdown,
+        "secondary": secondary,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "gpu": props.name,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for it in items:
+        it["plan"].close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle
+
+
+def run_reference(args):
+    from gemm_matmulplan_broadcast_gb300 import synth
+    rank, world, _ = dist_setup(args)
+    if rank != 0:
+        return
+    workload = synth.workload(args.workload)
+    bw_bound = args.workload == "fp16_skinny_splitk"
+    per_step = max(0.5, args.ref_step_seconds)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(workload, per_step / 4)
+    flops = secs = 0.0
+    cores, desc = 1, ""
+    for _ in range(args.steps):
+        f, s, cores, desc = cpu_oracle_sample(workload, per_step)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    unit = "TFLOP/s"
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "cpu oracle", "data": "synthetic",
+        "config": {"workload": workload.name, "description": workload.description},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    if bw_bound:
+        line["note"] = "bandwidth workload reported in TFLOP/s for the CPU oracle"
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="bf16_transformer_projection")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,568 @@
+// Host side of the library: MatMulPlan (shape resolution, broadcast batch
+// strides, batch collapse and folding), GemmPlan (algorithm choice, splits,
+// workspace) and the exported C ABI.
+//
+// "MatMul Kernel Design", section "Shape and plan model": the plan resolves
+// the whole output shape up front -- promoted M, N, K, the broadcast batch
+// shape, per-operand batch strides with zeros for broadcast dimensions -- and
+// embeds the GEMM plan that runs once per broadcast batch item.
+// "Gemm and MatMul Performance Roadmap", section "Phase 4: complete MatMul":
+// normalise rank-one inputs, compute zero-stride broadcast strides, collapse
+// contiguous batch dimensions, dispatch the batches through the same
+// scheduler, pick dedicated kernels for small M or N, and restore the output
+// rank without copying.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "olc_internal.h"
+
+using namespace olc;
+
+struct olc_matmul_plan {
+    olc_dtype dtype;
+    int a_rank, b_rank;
+    int64_t a_shape[OLC_MAX_RANK], b_shape[OLC_MAX_RANK];
+    // resolved shape
+    int out_rank;
+    int64_t out_shape[OLC_MAX_RANK];
+    int64_t M, N, K;
+    int64_t batch;               // number of broadcast batch items
+    int batch_rank;
+    int64_t batch_shape[OLC_MAX_RANK];
+    int64_t a_bstride[OLC_MAX_RANK], b_bstride[OLC_MAX_RANK];
+    // launch geometry after collapse / fold
+    int64_t rows;                // M times the folded batch
+    int64_t items;               // batch items a launch walks
+    BatchMap map;
+    // GEMM plan
+    int algo;
+    bool forced;
+    int splits;                  // SPLIT_K slices or SKINNY_M K-slices
+    int device;                  // -1: planned without a device
+    int sm_count;
+    void* workspace;
+    size_t ws_bytes;
+    size_t partial_bytes;
+    size_t counter_count;
+};
+
+namespace {
+
+constexpr int kDefaultSmCount = 152;   // GB300; used only when no device is visible
+
+int64_t elem_bytes(olc_dtype dt) {
+    switch (dt) {
+        case OLC_FLOAT: return 4;
+        case OLC_DOUBLE: return 8;
+        case OLC_FLOAT16:
+        case OLC_BFLOAT16: return 2;
+    }
+    return 0;
+}
+
+bool valid_dtype(int dt) {
+    return dt == OLC_FLOAT || dt == OLC_DOUBLE || dt == OLC_FLOAT16 || dt == OLC_BFLOAT16;
+}
+
+bool is_half(olc_dtype dt) { return dt == OLC_FLOAT16 || dt == OLC_BFLOAT16; }
+
+int64_t out_numel(const olc_matmul_plan* p) {
+    int64_t n = 1;
+    for (int i = 0; i < p->out_rank; ++i) n *= p->out_shape[i];
+    return n;
+}
+
+int64_t numel(const int64_t* s, int r) {
+    int64_t n = 1;
+    for (int i = 0; i < r; ++i) n *= s[i];
+    return n;
+}
+
+Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, void* Y) {
+    Problem pr;
+    pr.A = A;
+    pr.B = B;
+    pr.Y = Y;
+    pr.M = p->rows;
+    pr.N = p->N;
+    pr.K = p->K;
+    pr.items = p->items;
+    pr.map = p->map;
+    return pr;
+}
+
+// Collapse the broadcast batch dimensions: drop extent-1 dimensions, then
+// merge neighbours whose strides chain for both operands (the output is dense,
+// so its strides always chain).  Then fold: when B is shared by every item
+// and A's items are consecutive matrices, the items become extra rows of one
+// GEMM (M' = items * M).
+void collapse_and_fold(olc_matmul_plan* p) {
+    BatchMap m;
+    std::memset(&m, 0, sizeof m);
+    for (int d = 0; d < p->batch_rank; ++d) {
+        if (p->batch_shape[d] == 1) continue;
+        const int64_t e = p->batch_shape[d];
+        const int64_t sa = p->a_bstride[d], sb = p->b_bstride[d];
+        if (m.rank > 0) {
+            const int q = m.rank - 1;
+            if (m.a_stride[q] == sa * e && m.b_stride[q] == sb * e) {
+                m.dims[q] *= e;
+                m.a_stride[q] = sa;
+                m.b_stride[q] = sb;
+                continue;
+            }
+        }
+        m.dims[m.rank] = e;
+        m.a_stride[m.rank] = sa;
+        m.b_stride[m.rank] = sb;
+        ++m.rank;
+    }
+    p->rows = p->M;
+    p->items = p->batch;
+    if (m.rank == 1 && m.b_stride[0] == 0 && m.a_stride[0] == p->M * p->K) {
+        p->rows = p->M * m.dims[0];
+        p->items = 1;
+        m.rank = 0;
+    }
+    p->map = m;
+}
+
+// Shapes each algorithm can take (dtype, N, K; pointer alignment is checked
+// at execute time).
+bool feasible(const olc_matmul_plan* p, int algo) {
+    const int64_t rows = p->rows, N = p->N, K = p->K;
+    const int64_t n = out_numel(p);
+    switch (algo) {
+        case OLC_ALGO_EMPTY: return n == 0;
+        case OLC_ALGO_ZERO_FILL: return n > 0 && K == 0;
+        case OLC_ALGO_DIRECT:
+        case OLC_ALGO_GENERAL_SIMT: return n > 0 && K > 0;
+        case OLC_ALGO_SKINNY_M:
+            return n > 0 && K > 0 && rows <= skinny_m_max_rows() &&
+                   (N * elem_bytes(p->dtype)) % 16 == 0;
+        case OLC_ALGO_SKINNY_N:
+            return n > 0 && K > 0 && N <= skinny_n_max_cols() &&
+                   (K * elem_bytes(p->dtype)) % 16 == 0;
+        case OLC_ALGO_SPLIT_K:
+            return n > 0 && K > 0 && (K * elem_bytes(p->dtype)) % 16 == 0 &&
+                   (N * elem_bytes(p->dtype)) % 16 == 0;
+        case OLC_ALGO_GENERAL_TC: return n > 0 && K > 0 && is_half(p->dtype) && tc_shape_ok(p->dtype, N, K);
+    }
+    return false;
+}
+
+int choose_algorithm(const olc_matmul_plan* p) {
+    if (out_numel(p) == 0) return OLC_ALGO_EMPTY;
+    if (p->K == 0) return OLC_ALGO_ZERO_FILL;
+    const int64_t rows = p->rows, N = p->N, K = p->K, items = p->items;
+    const double macs = (double)rows * (double)N * (double)K * (double)items;
+    if (rows <= skinny_m_max_rows() && N >= 256 && feasible(p, OLC_ALGO_SKINNY_M))
+        return OLC_ALGO_SKINNY_M;
+    if (N <= skinny_n_max_cols() && rows >= 256 && feasible(p, OLC_ALGO_SKINNY_N))
+        return OLC_ALGO_SKINNY_N;
+    if (macs < 4.0 * 1024 * 1024) return OLC_ALGO_DIRECT;
+    // Split-K only for the guarded corner: too few output tiles (counting the
+    // batch, which takes priority) to fill half the SMs, and a long K.
+    const int64_t tiles = ((rows + 127) / 128) * ((N + 127) / 128) * items;
+    if (tiles * 2 <= p->sm_count && K >= 8 * 1024 && feasible(p, OLC_ALGO_SPLIT_K))
+        return OLC_ALGO_SPLIT_K;
+    if (is_half(p->dtype) && feasible(p, OLC_ALGO_GENERAL_TC)) return OLC_ALGO_GENERAL_TC;
+    return is_half(p->dtype) ? OLC_ALGO_DIRECT : OLC_ALGO_GENERAL_SIMT;
+}
+
+void free_workspace(olc_matmul_plan* p) {
+    if (p->workspace) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (p->device >= 0 && cur != p->device) cudaSetDevice(p->device);
+        cudaFree(p->workspace);
+        if (p->device >= 0 && cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    }
+    p->workspace = nullptr;
+    p->ws_bytes = 0;
+    p->partial_bytes = 0;
+    p->counter_count = 0;
+}
+
+// Size (and, with a device, allocate) the workspace for the current choice.
+olc_status prepare_algorithm(olc_matmul_plan* p) {
+    free_workspace(p);
+    p->splits = 1;
+    Problem pr = make_problem(p, nullptr, nullptr, nullptr);
+    const olc_dtype dt = p->dtype;
+    if (p->algo == OLC_ALGO_SPLIT_K) {
+        p->splits = split_k_pick(dt, pr, p->sm_count);
+        p->partial_bytes = split_k_partial_bytes(dt, pr, p->splits);
+        p->counter_count = split_k_counter_count(dt, pr, p->splits);
+    } else if (p->algo == OLC_ALGO_SKINNY_M) {
+        p->splits = skinny_m_pick_split(dt, pr, p->sm_count);
+        if (p->splits > 1) {
+            p->partial_bytes = skinny_m_partial_bytes(dt, pr, p->splits);
+            p->counter_count = skinny_m_counter_count(dt, pr, p->splits);
+        }
+    }
+    if (p->partial_bytes == 0) return OLC_OK;
+    const size_t counters_off = (p->partial_bytes + 255) / 256 * 256;
+    p->ws_bytes = counters_off + p->counter_count * sizeof(unsigned int);
+    if (p->device < 0) return OLC_OK;   // allocated at the first execute
+    void* ws = nullptr;
+    if (cudaMalloc(&ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        p->ws_bytes = 0;
+        return OLC_ERR_OOM;
+    }
+    if (cudaMemset(ws, 0, p->ws_bytes) != cudaSuccess) {
+        cudaFree(ws);
+        p->ws_bytes = 0;
+        return OLC_ERR_CUDA;
+    }
+    p->workspace = ws;
+    return OLC_OK;
+}
+
+Workspace workspace_of(const olc_matmul_plan* p) {
+    Workspace w;
+    const size_t counters_off = (p->partial_bytes + 255) / 256 * 256;
+    w.partials = p->workspace;
+    w.partial_bytes = p->partial_bytes;
+    w.counters = p->workspace ? reinterpret_cast<unsigned int*>(
+                                    static_cast<char*>(p->workspace) + counters_off)
+                              : nullptr;
+    w.counter_count = p->counter_count;
+    return w;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+olc_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return OLC_OK;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? OLC_ERR_OOM : OLC_ERR_CUDA;
+}
+
+olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, cudaStream_t s) {
+    const int64_t n = out_numel(p);
+    if (p->algo == OLC_ALGO_EMPTY || n == 0) return OLC_OK;
+    if (!Y) return OLC_ERR_NULL;
+    if (p->algo == OLC_ALGO_ZERO_FILL) return from_cuda(launch_zero_fill(Y, n * elem_bytes(p->dtype), s));
+    if (!A || !B) return OLC_ERR_NULL;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return from_cuda(cudaErrorNoDevice);
+    if (p->device >= 0 && cur != p->device) return OLC_ERR_WRONG_DEVICE;
+    olc_matmul_plan* mp = const_cast<olc_matmul_plan*>(p);
+    if (p->device < 0) {
+        // planned on a machine view without a device: bind now
+        mp->device = cur;
+        if (p->partial_bytes > 0 && !p->workspace) {
+            olc_status st = prepare_algorithm(mp);
+            if (st != OLC_OK) return st;
+        }
+    }
+    Problem pr = make_problem(p, A, B, Y);
+    const olc_dtype dt = p->dtype;
+    const bool al = aligned16(A) && aligned16(B) && aligned16(Y);
+    int algo = p->algo;
+    if (!al && algo != OLC_ALGO_DIRECT && algo != OLC_ALGO_GENERAL_SIMT) algo = OLC_ALGO_DIRECT;
+    cudaError_t e = cudaSuccess;
+    switch (algo) {
+        case OLC_ALGO_DIRECT: e = launch_direct(dt, pr, s); break;
+        case OLC_ALGO_GENERAL_SIMT: e = launch_general_simt(dt, pr, s); break;
+        case OLC_ALGO_SKINNY_M: e = launch_skinny_m(dt, pr, p->splits, workspace_of(p), s); break;
+        case OLC_ALGO_SKINNY_N: e = launch_skinny_n(dt, pr, p->sm_count, s); break;
+        case OLC_ALGO_SPLIT_K: e = launch_split_k(dt, pr, p->splits, workspace_of(p), s); break;
+        case OLC_ALGO_GENERAL_TC: e = launch_general_tc(dt, pr, p->sm_count, s); break;
+        default: return OLC_ERR_INVALID;
+    }
+    return from_cuda(e);
+}
+
+}  // namespace
+
+// ===========================================================================
+// exported ABI
+
+extern "C" {
+
+olc_status olc_matmul_plan_create(const int64_t* a_shape, int a_rank, const int64_t* b_shape,
+                                  int b_rank, olc_dtype dtype, olc_matmul_plan** out) {
+    if (!out) return OLC_ERR_NULL;
+    *out = nullptr;
+    if ((!a_shape && a_rank > 0) || (!b_shape && b_rank > 0)) return OLC_ERR_NULL;
+    if (a_rank < 1 || b_rank < 1 || a_rank > OLC_MAX_RANK || b_rank > OLC_MAX_RANK)
+        return OLC_ERR_RANK;
+    if (!valid_dtype(dtype)) return OLC_ERR_DTYPE;
+    for (int i = 0; i < a_rank; ++i)
+        if (a_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
+    for (int i = 0; i < b_rank; ++i)
+        if (b_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
+
+    olc_matmul_plan* p = new (std::nothrow) olc_matmul_plan;
+    if (!p) return OLC_ERR_OOM;
+    std::memset(p, 0, sizeof *p);
+    p->dtype = dtype;
+    p->a_rank = a_rank;
+    p->b_rank = b_rank;
+    std::memcpy(p->a_shape, a_shape, sizeof(int64_t) * a_rank);
+    std::memcpy(p->b_shape, b_shape, sizeof(int64_t) * b_rank);
+    p->device = -1;
+
+    // 1. rank-one promotion: A [K] -> [1, K], B [K] -> [K, 1]
+    int64_t a2[OLC_MAX_RANK + 1], b2[OLC_MAX_RANK + 1];
+    int ra2 = a_rank, rb2 = b_rank;
+    if (a_rank == 1) { a2[0] = 1; a2[1] = a_shape[0]; ra2 = 2; }
+    else std::memcpy(a2, a_shape, sizeof(int64_t) * a_rank);
+    if (b_rank == 1) { b2[0] = b_shape[0]; b2[1] = 1; rb2 = 2; }
+    else std::memcpy(b2, b_shape, sizeof(int64_t) * b_rank);
+    p->M = a2[ra2 - 2];
+    p->K = a2[ra2 - 1];
+    p->N = b2[rb2 - 1];
+    if (b2[rb2 - 2] != p->K) { delete p; return OLC_ERR_K_MISMATCH; }
+
+    // 2. multidirectional broadcast of the batch dimensions (right-aligned)
+    const int ba = ra2 - 2, bb = rb2 - 2;
+    const int r = std::max(ba, bb);
+    // each operand's own contiguous batch strides
+    int64_t a_own[OLC_MAX_RANK], b_own[OLC_MAX_RANK];
+    {
+        int64_t s = p->M * p->K;
+        for (int d = ba - 1; d >= 0; --d) { a_own[d] = s; s *= a2[d]; }
+        s = p->K * p->N;
+        for (int d = bb - 1; d >= 0; --d) { b_own[d] = s; s *= b2[d]; }
+    }
+    p->batch_rank = r;
+    p->batch = 1;
+    for (int d = 0; d < r; ++d) {
+        const int ia = d - (r - ba), ib = d - (r - bb);
+        const int64_t da = ia >= 0 ? a2[ia] : 1;
+        const int64_t db = ib >= 0 ? b2[ib] : 1;
+        int64_t e;
+        if (da == db) e = da;
+        else if (da == 1) e = db;
+        else if (db == 1) e = da;
+        else { delete p; return OLC_ERR_BATCH_MISMATCH; }
+        p->batch_shape[d] = e;
+        // stride 0 wherever the operand's extent is 1 (broadcast or trivial)
+        p->a_bstride[d] = (ia >= 0 && da != 1) ? a_own[ia] : 0;
+        p->b_bstride[d] = (ib >= 0 && db != 1) ? b_own[ib] : 0;
+        p->batch *= e;
+    }
+
+    // 3. output shape: batch + [M] (unless A was rank one) + [N] (unless B was)
+    p->out_rank = 0;
+    for (int d = 0; d < r; ++d) p->out_shape[p->out_rank++] = p->batch_shape[d];
+    if (a_rank > 1) p->out_shape[p->out_rank++] = p->M;
+    if (b_rank > 1) p->out_shape[p->out_rank++] = p->N;
+    if (p->out_rank > OLC_MAX_RANK) { delete p; return OLC_ERR_RANK; }
+
+    // 4. collapse and fold the batch, then choose the algorithm
+    collapse_and_fold(p);
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            sms > 0) {
+            p->device = dev;
+            p->sm_count = sms;
+        }
+    }
+    cudaGetLastError();
+    if (p->sm_count <= 0) p->sm_count = kDefaultSmCount;
+    p->algo = choose_algorithm(p);
+    p->forced = false;
+    olc_status st = prepare_algorithm(p);
+    if (st != OLC_OK) { delete p; return st; }
+    *out = p;
+    return OLC_OK;
+}
+
+void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
+    if (!plan) return;
+    free_workspace(plan);
+    delete plan;
+}
+
+olc_status olc_matmul_execute(const olc_matmul_plan* plan, const void* A, const void* B, void* Y,
+                              void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    return run(plan, A, B, Y, static_cast<cudaStream_t>(stream));
+}
+
+olc_status olc_matmul_execute_checked(const olc_matmul_plan* plan, const void* A, int64_t a_numel,
+                                      const void* B, int64_t b_numel, void* Y, int64_t y_numel,
+                                      void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    const int64_t n = out_numel(plan);
+    if (n > 0) {
+        if (y_numel < n) return OLC_ERR_BUFFER_TOO_SMALL;
+        if (plan->K > 0) {
+            if (a_numel < numel(plan->a_shape, plan->a_rank)) return OLC_ERR_BUFFER_TOO_SMALL;
+            if (b_numel < numel(plan->b_shape, plan->b_rank)) return OLC_ERR_BUFFER_TOO_SMALL;
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    olc_status st = run(plan, A, B, Y, s);
+    if (st != OLC_OK || n == 0) return st;
+    unsigned int flags = 0;
+    cudaError_t e = read_and_clear_device_error(&flags, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return flags ? OLC_ERR_DEVICE_TIMEOUT : OLC_OK;
+}
+
+olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_host,
+                                   const void* B_host, void* Y_host, void* A_dev, void* B_dev,
+                                   void* Y_dev, void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    const int64_t n = out_numel(plan);
+    if (n == 0) return OLC_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t eb = elem_bytes(plan->dtype);
+    if (!Y_host || !Y_dev) return OLC_ERR_NULL;
+    if (plan->K > 0) {
+        if (!A_host || !B_host || !A_dev || !B_dev) return OLC_ERR_NULL;
+        cudaError_t e = cudaMemcpyAsync(A_dev, A_host, numel(plan->a_shape, plan->a_rank) * eb,
+                                        cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(B_dev, B_host, numel(plan->b_shape, plan->b_rank) * eb,
+                                cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    olc_status st = run(plan, A_dev, B_dev, Y_dev, s);
+    if (st != OLC_OK) return st;
+    return from_cuda(cudaMemcpyAsync(Y_host, Y_dev, n * eb, cudaMemcpyDeviceToHost, s));
+}
+
+olc_status olc_matmul_plan_output_shape(const olc_matmul_plan* plan, int64_t* shape, int capacity,
+                                        int* rank) {
+    if (!plan || !rank || (!shape && plan->out_rank > 0)) return OLC_ERR_NULL;
+    if (capacity < plan->out_rank) return OLC_ERR_INVALID;
+    for (int i = 0; i < plan->out_rank; ++i) shape[i] = plan->out_shape[i];
+    *rank = plan->out_rank;
+    return OLC_OK;
+}
+
+olc_status olc_matmul_plan_dims(const olc_matmul_plan* plan, int64_t* M, int64_t* N, int64_t* K,
+                                int64_t* batch) {
+    if (!plan) return OLC_ERR_NULL;
+    if (M) *M = plan->M;
+    if (N) *N = plan->N;
+    if (K) *K = plan->K;
+    if (batch) *batch = plan->batch;
+    return OLC_OK;
+}
+
+olc_status olc_matmul_plan_batch(const olc_matmul_plan* plan, int* batch_rank,
+                                 int64_t* batch_shape, int64_t* a_strides, int64_t* b_strides) {
+    if (!plan) return OLC_ERR_NULL;
+    if (batch_rank) *batch_rank = plan->batch_rank;
+    for (int d = 0; d < plan->batch_rank; ++d) {
+        if (batch_shape) batch_shape[d] = plan->batch_shape[d];
+        if (a_strides) a_strides[d] = plan->a_bstride[d];
+        if (b_strides) b_strides[d] = plan->b_bstride[d];
+    }
+    return OLC_OK;
+}
+
+olc_status olc_matmul_plan_launch_shape(const olc_matmul_plan* plan, int64_t* rows,
+                                        int64_t* items, int* collapsed_rank) {
+    if (!plan) return OLC_ERR_NULL;
+    if (rows) *rows = plan->rows;
+    if (items) *items = plan->items;
+    if (collapsed_rank) *collapsed_rank = plan->map.rank;
+    return OLC_OK;
+}
+
+int olc_matmul_plan_algorithm(const olc_matmul_plan* plan) { return plan ? plan->algo : -1; }
+
+olc_status olc_matmul_plan_force_algorithm(olc_matmul_plan* plan, int algo) {
+    if (!plan) return OLC_ERR_NULL;
+    if (algo == OLC_ALGO_AUTO) {
+        plan->algo = choose_algorithm(plan);
+        plan->forced = false;
+        return prepare_algorithm(plan);
+    }
+    if (algo < OLC_ALGO_EMPTY || algo > OLC_ALGO_GENERAL_SIMT) return OLC_ERR_INVALID;
+    const int n = (int)(out_numel(plan) > 0);
+    if (!n || plan->K == 0) {
+        if (algo != choose_algorithm(plan)) return OLC_ERR_ALIGNMENT;
+    } else if (!feasible(plan, algo)) {
+        return OLC_ERR_ALIGNMENT;
+    }
+    plan->algo = algo;
+    plan->forced = true;
+    return prepare_algorithm(plan);
+}
+
+int olc_matmul_plan_launches(const olc_matmul_plan* plan) {
+    if (!plan) return -1;
+    switch (plan->algo) {
+        case OLC_ALGO_EMPTY: return 0;
+        default: return 1;
+    }
+}
+
+size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan) {
+    return plan ? plan->ws_bytes : 0;
+}
+
+int olc_matmul_plan_describe(const olc_matmul_plan* plan, char* buf, size_t cap) {
+    if (!plan) return -1;
+    char tmp[512];
+    int n = std::snprintf(tmp, sizeof tmp,
+                          "algo=%s dtype=%d M=%lld N=%lld K=%lld batch=%lld rows=%lld items=%lld "
+                          "collapsed_rank=%d splits=%d ws=%zu sms=%d%s",
+                          olc_algorithm_name(plan->algo), (int)plan->dtype, (long long)plan->M,
+                          (long long)plan->N, (long long)plan->K, (long long)plan->batch,
+                          (long long)plan->rows, (long long)plan->items, plan->map.rank,
+                          plan->splits, plan->ws_bytes, plan->sm_count,
+                          plan->forced ? " forced" : "");
+    if (buf && cap > 0) {
+        std::strncpy(buf, tmp, cap - 1);
+        buf[cap - 1] = '\0';
+    }
+    return n;
+}
+
+const char* olc_status_string(int status) {
+    switch (status) {
+        case OLC_OK: return "ok";
+        case OLC_ERR_NULL: return "null pointer argument";
+        case OLC_ERR_RANK: return "rank out of range (1..8)";
+        case OLC_ERR_NEGATIVE_DIM: return "negative dimension";
+        case OLC_ERR_K_MISMATCH: return "inner dimensions differ";
+        case OLC_ERR_BATCH_MISMATCH: return "batch dimensions do not broadcast";
+        case OLC_ERR_DTYPE: return "unsupported element type";
+        case OLC_ERR_ALIGNMENT: return "algorithm cannot take this shape or type";
+        case OLC_ERR_BUFFER_TOO_SMALL: return "buffer smaller than the planned tensor";
+        case OLC_ERR_NO_CONSTANT_B: return "plan owns no constant B";
+        case OLC_ERR_CUDA: return "CUDA runtime error";
+        case OLC_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case OLC_ERR_OOM: return "out of memory";
+        case OLC_ERR_INVALID: return "invalid argument";
+        case OLC_ERR_WRONG_DEVICE: return "current device is not the plan's device";
+    }
+    return "unknown status";
+}
+
+const char* olc_algorithm_name(int algo) {
+    switch (algo) {
+        case OLC_ALGO_AUTO: return "auto";
+        case OLC_ALGO_EMPTY: return "empty";
+        case OLC_ALGO_ZERO_FILL: return "zero_fill";
+        case OLC_ALGO_DIRECT: return "direct";
+        case OLC_ALGO_SKINNY_M: return "skinny_m";
+        case OLC_ALGO_SKINNY_N: return "skinny_n";
+        case OLC_ALGO_SPLIT_K: return "split_k";
+        case OLC_ALGO_GENERAL_TC: return "general_tc";
+        case OLC_ALGO_GENERAL_SIMT: return "general_simt";
+    }
+    return "unknown";
+}
+
+int olc_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+// Device helpers shared by the kernel files: element types, the batch map
+// walk, and the device error word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "olc_internal.h"
+
+namespace olc {
+
+// Element traits: accumulator type and the load / narrowing store.  FP16 and
+// BF16 accumulate in float32 and narrow once with round-to-nearest-even.
+template <typename T>
+struct Num;
+
+template <>
+struct Num<float> {
+    using acc_t = float;
+    static __device__ __forceinline__ float to_acc(float v) { return v; }
+    static __device__ __forceinline__ float from_acc(float v) { return v; }
+};
+template <>
+struct Num<double> {
+    using acc_t = double;
+    static __device__ __forceinline__ double to_acc(double v) { return v; }
+    static __device__ __forceinline__ double from_acc(double v) { return v; }
+};
+template <>
+struct Num<__half> {
+    using acc_t = float;
+    static __device__ __forceinline__ float to_acc(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half from_acc(float v) { return __float2half_rn(v); }
+};
+template <>
+struct Num<__nv_bfloat16> {
+    using acc_t = float;
+    static __device__ __forceinline__ float to_acc(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_acc(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Operand element offsets of output batch item z.
+__device__ __forceinline__ void batch_offsets(const BatchMap& m, int64_t z, int64_t& a_off,
+                                              int64_t& b_off) {
+    a_off = 0;
+    b_off = 0;
+#pragma unroll 1
+    for (int d = m.rank - 1; d >= 0; --d) {
+        const int64_t e = m.dims[d];
+        const int64_t i = z % e;
+        z /= e;
+        a_off += i * m.a_stride[d];
+        b_off += i * m.b_stride[d];
+    }
+}
+
+// Device error word: bit flags set by kernels whose bounded waits ran out.
+// Kernels receive its address (device_error_word()) as an argument.
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+__device__ __forceinline__ void raise_device_error(unsigned int* word, unsigned int bits) {
+    if (word) atomicOr(word, bits);
+}
+
+template <typename F>
+inline cudaError_t dispatch_dtype(olc_dtype dt, F&& f) {
+    switch (dt) {
+        case OLC_FLOAT: return f(float{});
+        case OLC_DOUBLE: return f(double{});
+        case OLC_FLOAT16: return f(__half{});
+        case OLC_BFLOAT16: return f(__nv_bfloat16{});
+    }
+    return cudaErrorInvalidValue;
+}
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+}  // namespace olc

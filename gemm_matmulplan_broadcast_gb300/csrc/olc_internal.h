@@ -1,0 +1,87 @@
+// Internal interface between the host plan (api.cpp) and the kernel files.
+// Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "olc_matmul.h"
+
+namespace olc {
+
+constexpr int kMaxBatchRank = OLC_MAX_RANK;
+
+// Output batch item -> operand element offsets.  `dims` are the collapsed
+// batch extents (outermost first); an operand's stride is 0 along a dimension
+// it broadcasts.  The output itself is dense: item z starts at z * M * N.
+struct BatchMap {
+    int rank;
+    int64_t dims[kMaxBatchRank];
+    int64_t a_stride[kMaxBatchRank];
+    int64_t b_stride[kMaxBatchRank];
+};
+
+// One launch's worth of work: `items` independent products
+// [M, K] @ [K, N] -> [M, N] with operand offsets from `map`.
+struct Problem {
+    const void* A;
+    const void* B;
+    void* Y;
+    int64_t M, N, K;
+    int64_t items;
+    BatchMap map;
+};
+
+// Workspace handed to the split reductions: `partials` holds fp32/fp64
+// partial results, `counters` one arrival counter per output tile (zero
+// between launches; the last arriving block resets its counter).
+struct Workspace {
+    void* partials;
+    size_t partial_bytes;
+    unsigned int* counters;
+    size_t counter_count;
+};
+
+// Device error word (bounded waits that ran out set it).  Defined in
+// simt.cu; device_error_word() is its device address on the current device.
+cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream);
+unsigned int* device_error_word();
+
+// ---- launchers: every one returns the launch's cudaError_t -------------
+
+cudaError_t launch_zero_fill(void* Y, int64_t bytes, cudaStream_t stream);
+
+// DIRECT: small tiles, scalar loads, any shape and alignment.
+cudaError_t launch_direct(olc_dtype dt, const Problem& p, cudaStream_t stream);
+
+// GENERAL_SIMT: FP32 FFMA / FP64 DFMA register-tiled kernel (any dtype works;
+// the plan routes FLOAT and DOUBLE here).
+cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t stream);
+bool general_simt_vectorizable(olc_dtype dt, int64_t N, int64_t K);
+
+// SKINNY_M: M <= 16.  `ksplit` slices of K, reduced in fixed order.
+int skinny_m_max_rows();
+cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, const Workspace& ws,
+                            cudaStream_t stream);
+size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit);
+size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit);
+int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count);
+
+// SKINNY_N: N <= 16.
+int skinny_n_max_cols();
+cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+
+// SPLIT_K: tiny output, long K.  Partials in fixed-order reduction.
+cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
+                           cudaStream_t stream);
+size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits);
+size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits);
+int split_k_pick(olc_dtype dt, const Problem& p, int sm_count);
+
+// GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
+bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
+cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+
+}  // namespace olc

@@ -1,0 +1,371 @@
+// Skinny kernels: SKINNY_M (few output rows) and SKINNY_N (few output
+// columns), plus the GENERAL_SIMT launcher that routes by vectorisability.
+//
+// "Gemm and MatMul Performance Roadmap", section "Target computation
+// algorithm", the algorithm-by-shape table: for M == 1 or very small M a
+// GEMV/skinny-M kernel that streams B once and vectorises across N; for
+// N == 1 or very small N a dot/GEMV kernel that vectorises the K reduction.
+// Both are bound by HBM bandwidth (arithmetic intensity of a few flop/byte),
+// so the kernels are built around wide coalesced loads and enough loads in
+// flight, not around arithmetic.
+#include "common.cuh"
+
+namespace olc {
+
+cudaError_t launch_general_simt_generic(olc_dtype dt, const Problem& p, cudaStream_t stream);
+cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream);
+bool general_simt_fast_ok(olc_dtype dt, int64_t N, int64_t K);
+
+bool general_simt_vectorizable(olc_dtype dt, int64_t N, int64_t K) {
+    return general_simt_fast_ok(dt, N, K);
+}
+
+cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t stream) {
+    if (general_simt_fast_ok(dt, p.N, p.K)) return launch_general_simt_fast(dt, p, stream);
+    return launch_general_simt_generic(dt, p, stream);
+}
+
+// ===========================================================================
+// SKINNY_M
+//
+// Block = KW warps.  Lane l of every warp owns VEC consecutive output columns
+// (one 16-byte vector of each B row); the block covers 32 * VEC columns.  The
+// KW warps split the block's K range; within its range a warp walks k in
+// ascending order, loading B[k][cols] as one 16-byte vector per lane and the
+// MR values A[i][k] (the same address for all lanes, so one broadcast load),
+// and keeps an MR x VEC accumulator tile in registers.  The warps' tiles are
+// summed in shared memory in warp order.  With ksplit > 1 the grid also
+// splits K across blocks: each block writes its partial tile to the
+// workspace, and the last block to arrive for a column group (counted with an
+// atomic) adds the partials in split order 0..ksplit-1 -- the same order
+// whichever block arrives last, so results are reproducible run to run.
+
+constexpr int kSkinnyMMax = 16;
+
+int skinny_m_max_rows() { return kSkinnyMMax; }
+
+template <typename T>
+struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+};
+
+template <int MR>
+struct SkinnyMConfig {
+    static constexpr int KW = MR <= 4 ? 8 : (MR <= 8 ? 4 : 2);   // warps splitting K
+};
+
+template <typename T, int MR>
+__global__ void __launch_bounds__(SkinnyMConfig<MR>::KW * 32)
+skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws) {
+    using acc_t = typename Num<T>::acc_t;
+    constexpr int VEC = Vec16<T>::N;
+    constexpr int KW = SkinnyMConfig<MR>::KW;
+    constexpr int COLS = 32 * VEC;
+    __shared__ acc_t red[KW][MR][COLS];
+    __shared__ unsigned int am_last;
+
+    const int64_t per_item = col_groups * ksplit;
+    const int64_t item = blockIdx.x / per_item;
+    const int64_t rem = blockIdx.x % per_item;
+    const int split = (int)(rem / col_groups);
+    const int64_t cg = rem % col_groups;
+    int64_t a_off, b_off;
+    batch_offsets(p.map, item, a_off, b_off);
+    const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
+    const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
+    T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
+    const int64_t M = p.M, N = p.N, K = p.K;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t col0 = cg * COLS + (int64_t)lane * VEC;
+    const bool col_ok = col0 < N;   // N is a multiple of VEC
+    // this block's K range, then this warp's share of it
+    const int64_t kb0 = (int64_t)split * kslice;
+    const int64_t kb1 = min64(K, kb0 + kslice);
+    const int64_t wlen = ceil_div(max64(kb1 - kb0, 0), KW);
+    const int64_t k0 = kb0 + warp * wlen;
+    const int64_t k1 = min64(kb1, k0 + wlen);
+
+    acc_t acc[MR][VEC];
+#pragma unroll
+    for (int i = 0; i < MR; ++i)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[i][v] = acc_t(0);
+
+    if (col_ok) {
+        const T* bp = B + col0;
+        constexpr int KU = 4;   // B vectors in flight per lane
+        int64_t k = k0;
+        for (; k + KU <= k1; k += KU) {
+            uint4 bv[KU];
+#pragma unroll
+            for (int u = 0; u < KU; ++u)
+                bv[u] = __ldg(reinterpret_cast<const uint4*>(bp + (k + u) * N));
+#pragma unroll
+            for (int u = 0; u < KU; ++u) {
+                const T* be = reinterpret_cast<const T*>(&bv[u]);
+                acc_t b[VEC];
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) b[v] = Num<T>::to_acc(be[v]);
+#pragma unroll
+                for (int i = 0; i < MR; ++i) {
+                    const acc_t a = i < M ? Num<T>::to_acc(__ldg(A + i * K + k + u)) : acc_t(0);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a, b[v], acc[i][v]);
+                }
+            }
+        }
+        for (; k < k1; ++k) {
+            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bp + k * N));
+            const T* be = reinterpret_cast<const T*>(&bv);
+#pragma unroll
+            for (int i = 0; i < MR; ++i) {
+                const acc_t a = i < M ? Num<T>::to_acc(__ldg(A + i * K + k)) : acc_t(0);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a, Num<T>::to_acc(be[v]), acc[i][v]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < MR; ++i)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) red[warp][i][lane * VEC + v] = acc[i][v];
+    __syncthreads();
+
+    // sum the warps' tiles in warp order: thread t owns entries t, t + NT, ...
+    constexpr int NT = KW * 32;
+    constexpr int ENTRIES = MR * COLS;
+    constexpr int Q = (ENTRIES + NT - 1) / NT;
+    acc_t part[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int e = threadIdx.x + q * NT;
+        acc_t s = acc_t(0);
+        if (e < ENTRIES) {
+            const int i = e / COLS, c = e % COLS;
+            s = red[0][i][c];
+#pragma unroll
+            for (int w = 1; w < KW; ++w) s += red[w][i][c];
+        }
+        part[q] = s;
+    }
+
+    if (ksplit == 1) {
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const int e = threadIdx.x + q * NT;
+            if (e >= ENTRIES) continue;
+            const int i = e / COLS, c = e % COLS;
+            const int64_t col = cg * COLS + c;
+            if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(part[q]);
+        }
+        return;
+    }
+
+    // cross-block split: partial tile -> workspace, last arrival reduces
+    acc_t* P = static_cast<acc_t*>(ws.partials);
+    const int64_t tile = item * col_groups + cg;
+    acc_t* mine = P + (tile * ksplit + split) * ENTRIES;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int e = threadIdx.x + q * NT;
+        if (e < ENTRIES) mine[e] = part[q];
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int prev = atomicAdd(ws.counters + tile, 1u);
+        am_last = (prev == (unsigned int)ksplit - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+    const acc_t* all = P + tile * ksplit * ENTRIES;
+    for (int e = threadIdx.x; e < ENTRIES; e += NT) {
+        acc_t s = __ldcg(all + e);
+        for (int t = 1; t < ksplit; ++t) s += __ldcg(all + (int64_t)t * ENTRIES + e);
+        const int i = e / COLS, c = e % COLS;
+        const int64_t col = cg * COLS + c;
+        if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(s);
+    }
+    if (threadIdx.x == 0) ws.counters[tile] = 0u;   // ready for the next launch
+}
+
+static int round_rows(int64_t m) {
+    return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
+}
+
+static int64_t skinny_m_col_groups(olc_dtype dt, int64_t N) {
+    const int64_t vec = 16 / (dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2);
+    return ceil_div(N, 32 * vec);
+}
+
+int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
+    const int64_t groups = skinny_m_col_groups(dt, p.N) * p.items;
+    // aim for about four blocks per SM; every split keeps at least 256 k
+    int64_t want = ceil_div(4LL * sm_count, groups);
+    const int64_t kmax = max64(1, p.K / 256);
+    if (want > kmax) want = kmax;
+    if (want > 64) want = 64;
+    if (want < 1) want = 1;
+    return (int)want;
+}
+
+size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit) {
+    const int64_t vec = 16 / (dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2);
+    const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
+    const int64_t entries = round_rows(p.M) * 32 * vec;
+    return (size_t)(skinny_m_col_groups(dt, p.N) * p.items * ksplit * entries * acc);
+}
+
+size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit) {
+    (void)ksplit;
+    return (size_t)(skinny_m_col_groups(dt, p.N) * p.items);
+}
+
+template <typename T, int MR>
+static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspace& ws,
+                                     cudaStream_t s) {
+    constexpr int VEC = Vec16<T>::N;
+    const int64_t groups = ceil_div(p.N, 32 * VEC);
+    const int64_t kslice = ceil_div(p.K, ksplit);
+    const int64_t blocks = groups * ksplit * p.items;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (ksplit > 1 && (!ws.partials || !ws.counters)) return cudaErrorInvalidValue;
+    skinny_m_kernel<T, MR><<<(unsigned)blocks, SkinnyMConfig<MR>::KW * 32, 0, s>>>(
+        p, groups, ksplit, kslice, ws);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, const Workspace& ws,
+                            cudaStream_t s) {
+    const int mr = round_rows(p.M);
+    return dispatch_dtype(dt, [&](auto tag) {
+        using T = decltype(tag);
+        switch (mr) {
+            case 1: return launch_skinny_m_t<T, 1>(p, ksplit, ws, s);
+            case 2: return launch_skinny_m_t<T, 2>(p, ksplit, ws, s);
+            case 4: return launch_skinny_m_t<T, 4>(p, ksplit, ws, s);
+            case 8: return launch_skinny_m_t<T, 8>(p, ksplit, ws, s);
+            default: return launch_skinny_m_t<T, 16>(p, ksplit, ws, s);
+        }
+    });
+}
+
+// ===========================================================================
+// SKINNY_N
+//
+// Block = 8 warps, each warp owns RW consecutive output rows; the block
+// stages a KC-long chunk of B in shared memory, transposed (Bs[n][k]) and
+// widened, so that lane l reading Bs[n][k0 + l] hits 32 distinct banks.  Lane
+// l handles k = l, l + 32, ... of the chunk (coalesced A loads), keeps RW x NC
+// partial sums and reuses each B value across the RW rows.  At the end the
+// partial sums are reduced across the warp with shuffles (a fixed tree).
+
+constexpr int kSkinnyNMax = 16;
+int skinny_n_max_cols() { return kSkinnyNMax; }
+
+template <typename T, int NC>
+struct SkinnyNConfig {
+    static constexpr int RW = 4;                       // rows per warp
+    static constexpr int WARPS = 8;
+    static constexpr int KC = (sizeof(typename Num<T>::acc_t) * NC * 1024 <= 64 * 1024) ? 1024 : 512;
+};
+
+template <typename T, int NC>
+__global__ void __launch_bounds__(256)
+skinny_n_kernel(Problem p, int64_t row_groups) {
+    using acc_t = typename Num<T>::acc_t;
+    using Cfg = SkinnyNConfig<T, NC>;
+    constexpr int RW = Cfg::RW, KC = Cfg::KC, WARPS = Cfg::WARPS;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    acc_t* Bs = reinterpret_cast<acc_t*>(smem_raw);   // [NC][KC]
+
+    const int64_t item = blockIdx.x / row_groups;
+    const int64_t rg = blockIdx.x % row_groups;
+    int64_t a_off, b_off;
+    batch_offsets(p.map, item, a_off, b_off);
+    const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
+    const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
+    T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
+    const int64_t M = p.M, N = p.N, K = p.K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row0 = (rg * WARPS + warp) * RW;
+
+    acc_t acc[RW][NC];
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int n = 0; n < NC; ++n) acc[r][n] = acc_t(0);
+
+    for (int64_t kc = 0; kc < K; kc += KC) {
+        const int klen = (int)min64(KC, K - kc);
+        __syncthreads();
+        for (int e = threadIdx.x; e < KC * NC; e += blockDim.x) {
+            const int k = e / NC, n = e % NC;
+            Bs[n * KC + k] = (k < klen && n < N) ? Num<T>::to_acc(B[(kc + k) * N + n]) : acc_t(0);
+        }
+        __syncthreads();
+        for (int k = lane; k < klen; k += 32) {
+            acc_t a[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+                a[r] = (row0 + r < M) ? Num<T>::to_acc(__ldg(A + (row0 + r) * K + kc + k)) : acc_t(0);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const acc_t b = Bs[n * KC + k];
+#pragma unroll
+                for (int r = 0; r < RW; ++r) acc[r][n] = fma(a[r], b, acc[r][n]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int n = 0; n < NC; ++n) {
+            acc_t v = acc[r][n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[r][n] = v;
+        }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            if (row0 + r >= M) continue;
+#pragma unroll
+            for (int n = 0; n < NC; ++n)
+                if (n < N) Y[(row0 + r) * N + n] = Num<T>::from_acc(acc[r][n]);
+        }
+    }
+}
+
+template <typename T, int NC>
+static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
+    using Cfg = SkinnyNConfig<T, NC>;
+    const int64_t rows_per_block = Cfg::RW * Cfg::WARPS;
+    const int64_t groups = ceil_div(p.M, rows_per_block);
+    const int64_t blocks = groups * p.items;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const size_t smem = sizeof(typename Num<T>::acc_t) * NC * Cfg::KC;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(skinny_n_kernel<T, NC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    skinny_n_kernel<T, NC><<<(unsigned)blocks, 256, smem, s>>>(p, groups);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t s) {
+    (void)sm_count;
+    return dispatch_dtype(dt, [&](auto tag) {
+        using T = decltype(tag);
+        if (p.N <= 1) return launch_skinny_n_t<T, 1>(p, s);
+        if (p.N <= 2) return launch_skinny_n_t<T, 2>(p, s);
+        if (p.N <= 4) return launch_skinny_n_t<T, 4>(p, s);
+        if (p.N <= 8) return launch_skinny_n_t<T, 8>(p, s);
+        return launch_skinny_n_t<T, 16>(p, s);
+    });
+}
+
+}  // namespace olc

@@ -1,0 +1,143 @@
+// SPLIT_K: tiny output, long reduction.
+//
+// "Gemm and MatMul Performance Roadmap", section "Parallel execution": when
+// the whole M x N task grid cannot occupy the machine, K is partitioned into
+// slices K0 | K1 | ..., each slice produces a partial product P_s with the
+// same kernels, and a controlled reduction combines them
+// (Y = P_0 + P_1 + ...).  Independent batches take priority over split-K (the
+// plan only picks this path when tiles * batch items underfill the SMs).
+//
+// Here one launch does both passes.  Block (tile, s) accumulates its slice of
+// K for a TM x TN output tile and writes the partial tile to the workspace;
+// the last block to arrive for a tile (atomic counter) sums the partials in
+// slice order s = 0, 1, ..., S-1 and writes the narrowed result.  The order of
+// the final sum does not depend on which block arrives last, so the result is
+// bit-reproducible run to run.
+#include "common.cuh"
+
+namespace olc {
+
+template <typename T>
+struct SplitCfg {
+    static constexpr int TM = 32, TN = 32, BK = 32;
+    static constexpr int THREADS = 256;   // 2 x 2 outputs per thread
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+split_k_kernel(Problem p, int64_t tiles_m, int64_t tiles_n, int splits, int64_t kslice,
+               Workspace ws) {
+    using acc_t = typename Num<T>::acc_t;
+    constexpr int TM = SplitCfg<T>::TM, TN = SplitCfg<T>::TN, BK = SplitCfg<T>::BK;
+    __shared__ acc_t As[BK][TM + 1];
+    __shared__ acc_t Bs[BK][TN];
+    __shared__ unsigned int am_last;
+
+    const int64_t tiles = tiles_m * tiles_n;
+    const int64_t per_item = tiles * splits;
+    const int64_t item = blockIdx.x / per_item;
+    const int64_t rem = blockIdx.x % per_item;
+    const int s = (int)(rem / tiles);
+    const int64_t t = rem % tiles;
+    const int64_t m0 = (t / tiles_n) * TM, n0 = (t % tiles_n) * TN;
+    int64_t a_off, b_off;
+    batch_offsets(p.map, item, a_off, b_off);
+    const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
+    const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
+    T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
+    const int64_t M = p.M, N = p.N, K = p.K;
+    const int64_t kb0 = (int64_t)s * kslice;
+    const int64_t kb1 = min64(K, kb0 + kslice);
+
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    acc_t acc[2][2] = {{acc_t(0), acc_t(0)}, {acc_t(0), acc_t(0)}};
+    for (int64_t k0 = kb0; k0 < kb1; k0 += BK) {
+        for (int e = threadIdx.x; e < TM * BK; e += 256) {
+            const int r = e / BK, c = e % BK;
+            const int64_t gm = m0 + r, gk = k0 + c;
+            As[c][r] = (gm < M && gk < kb1) ? Num<T>::to_acc(A[gm * K + gk]) : acc_t(0);
+        }
+        for (int e = threadIdx.x; e < BK * TN; e += 256) {
+            const int r = e / TN, c = e % TN;
+            const int64_t gk = k0 + r, gn = n0 + c;
+            Bs[r][c] = (gk < kb1 && gn < N) ? Num<T>::to_acc(B[gk * N + gn]) : acc_t(0);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            const acc_t a0 = As[kk][ty], a1 = As[kk][ty + 16];
+            const acc_t b0 = Bs[kk][tx], b1 = Bs[kk][tx + 16];
+            acc[0][0] = fma(a0, b0, acc[0][0]);
+            acc[0][1] = fma(a0, b1, acc[0][1]);
+            acc[1][0] = fma(a1, b0, acc[1][0]);
+            acc[1][1] = fma(a1, b1, acc[1][1]);
+        }
+        __syncthreads();
+    }
+
+    constexpr int ENTRIES = TM * TN;
+    acc_t* P = static_cast<acc_t*>(ws.partials);
+    const int64_t tile_id = item * tiles + t;
+    acc_t* mine = P + (tile_id * splits + s) * ENTRIES;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) mine[(ty + 16 * i) * TN + tx + 16 * j] = acc[i][j];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int prev = atomicAdd(ws.counters + tile_id, 1u);
+        am_last = (prev == (unsigned int)splits - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+    const acc_t* all = P + tile_id * splits * ENTRIES;
+    for (int e = threadIdx.x; e < ENTRIES; e += 256) {
+        acc_t v = __ldcg(all + e);
+        for (int q = 1; q < splits; ++q) v += __ldcg(all + (int64_t)q * ENTRIES + e);
+        const int64_t gm = m0 + e / TN, gn = n0 + e % TN;
+        if (gm < M && gn < N) Y[gm * N + gn] = Num<T>::from_acc(v);
+    }
+    if (threadIdx.x == 0) ws.counters[tile_id] = 0u;
+}
+
+static int64_t acc_bytes(olc_dtype dt) { return dt == OLC_DOUBLE ? 8 : 4; }
+
+int split_k_pick(olc_dtype dt, const Problem& p, int sm_count) {
+    (void)dt;
+    const int64_t tiles = ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items;
+    // about two blocks per SM, each slice at least 256 long
+    int64_t s = ceil_div(2LL * sm_count, tiles);
+    const int64_t smax = max64(1, p.K / 256);
+    if (s > smax) s = smax;
+    if (s > 1024) s = 1024;
+    return (int)max64(s, 1);
+}
+
+size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits) {
+    const int64_t tiles = ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items;
+    return (size_t)(tiles * splits * 32 * 32 * acc_bytes(dt));
+}
+
+size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits) {
+    (void)dt;
+    (void)splits;
+    return (size_t)(ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items);
+}
+
+cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
+                           cudaStream_t s) {
+    if (!ws.partials || !ws.counters) return cudaErrorInvalidValue;
+    const int64_t tm = ceil_div(p.M, 32), tn = ceil_div(p.N, 32);
+    const int64_t kslice = ceil_div(ceil_div(p.K, splits), 32) * 32;
+    const int64_t blocks = tm * tn * splits * p.items;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    return dispatch_dtype(dt, [&](auto tag) {
+        using T = decltype(tag);
+        split_k_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn, splits, kslice, ws);
+        return cudaGetLastError();
+    });
+}
+
+}  // namespace olc

@@ -1,0 +1,232 @@
+/*
+ * olc_matmul.h -- C ABI of the GB300 ONNX MatMul library (libolc_matmul.so).
+ *
+ * The operator is ONNX MatMul: vector, matrix and batched matrix products with
+ * NumPy-style batch broadcasting ("MatMul Kernel Design", introduction and
+ * section "Shape and plan model").  A plan is built once from the two operand
+ * shapes and the element type; executing it enqueues CUDA kernels on the
+ * caller's stream.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are dense and row-major (C-contiguous).  A, B and Y are device
+ *    pointers owned by the caller; the library never frees them.
+ *  - A and B have the same element type (olc_dtype); Y has it too.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Execution is asynchronous: a return of OLC_OK means the work
+ *    was enqueued.
+ *  - Every shape or type error is reported by olc_matmul_plan_create, before
+ *    any device work ("Types and algorithm selection": dynamic negative
+ *    dimensions, mixed or unsupported types and incompatible matrix or batch
+ *    dimensions fail before compute).
+ *  - Functions returning olc_status never abort the process.
+ *  - A plan is bound to the CUDA device that was current when it was created.
+ *    It may be executed on any stream of that device, but not concurrently
+ *    from two host threads or on two streams at once when it holds a split
+ *    reduction workspace (olc_matmul_plan_workspace_bytes > 0).
+ */
+#ifndef OLC_MATMUL_H
+#define OLC_MATMUL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types, numbered as ONNX TensorProto data types.  FLOAT and DOUBLE
+ * accumulate natively; FLOAT16 and BFLOAT16 accumulate in float32 and narrow
+ * the result once with round-to-nearest-even ("Types and algorithm
+ * selection"; "Gemm and MatMul Performance Roadmap", section "Scope and type
+ * matrix"). */
+typedef enum {
+    OLC_FLOAT = 1,
+    OLC_FLOAT16 = 10,
+    OLC_DOUBLE = 11,
+    OLC_BFLOAT16 = 16
+} olc_dtype;
+
+typedef enum {
+    OLC_OK = 0,
+    OLC_ERR_NULL = 1,             /* a required pointer argument is NULL           */
+    OLC_ERR_RANK = 2,             /* rank 0, or rank above OLC_MAX_RANK            */
+    OLC_ERR_NEGATIVE_DIM = 3,     /* a dimension is negative                       */
+    OLC_ERR_K_MISMATCH = 4,       /* A's last dim differs from B's contraction dim */
+    OLC_ERR_BATCH_MISMATCH = 5,   /* batch extents neither equal nor 1             */
+    OLC_ERR_DTYPE = 6,            /* element type not supported                    */
+    OLC_ERR_ALIGNMENT = 7,        /* a forced algorithm cannot take these shapes   */
+    OLC_ERR_BUFFER_TOO_SMALL = 8, /* a checked execute got a buffer too small      */
+    OLC_ERR_NO_CONSTANT_B = 9,    /* reserved for the constant-B execute           */
+    OLC_ERR_CUDA = 10,            /* a CUDA runtime call failed                    */
+    OLC_ERR_DEVICE_TIMEOUT = 11,  /* a bounded device-side wait ran out            */
+    OLC_ERR_OOM = 12,             /* workspace allocation failed                   */
+    OLC_ERR_INVALID = 13,         /* an argument is out of its documented range    */
+    OLC_ERR_WRONG_DEVICE = 14     /* current device differs from the plan's        */
+} olc_status;
+
+/* The algorithm a plan runs ("MatMul Kernel Design", section "Types and
+ * algorithm selection": direct execution for small reductions, skinny-M or
+ * skinny-N kernels when one output dimension underfills the ordinary tile,
+ * split-K for the tiny-output long-reduction corner, the general tiled engine
+ * otherwise).  EMPTY and ZERO_FILL cover outputs with no elements and K == 0. */
+typedef enum {
+    OLC_ALGO_AUTO = -1,       /* only as an argument: restore automatic choice */
+    OLC_ALGO_EMPTY = 0,       /* output has no elements: nothing is launched    */
+    OLC_ALGO_ZERO_FILL = 1,   /* K == 0: Y is set to zero, A and B are not read */
+    OLC_ALGO_DIRECT = 2,      /* small SIMT tile kernel, any shape or alignment */
+    OLC_ALGO_SKINNY_M = 3,    /* M <= 16: stream B once, vectorised along N     */
+    OLC_ALGO_SKINNY_N = 4,    /* N <= 16: stream A once, vectorised along K     */
+    OLC_ALGO_SPLIT_K = 5,     /* K partitioned, fixed-order reduction           */
+    OLC_ALGO_GENERAL_TC = 6,  /* FLOAT16/BFLOAT16: tcgen05 tensor-core tiles    */
+    OLC_ALGO_GENERAL_SIMT = 7 /* FLOAT/DOUBLE: FFMA / DFMA register tiles       */
+} olc_algorithm;
+
+#define OLC_MAX_RANK 8
+
+typedef struct olc_matmul_plan olc_matmul_plan;
+
+/*
+ * Build a plan for Y = MatMul(A, B).
+ *
+ * "MatMul Kernel Design", section "Shape and plan model": the plan resolves
+ * the complete output shape before execution -- a rank-one A [K] is promoted
+ * to [1, K] and a rank-one B [K] to [K, 1] and the promoted dimension is
+ * squeezed from the output; the leading batch dimensions are broadcast
+ * multidirectionally (aligned on the right; equal, or one side 1); each
+ * operand gets per-dimension batch strides in elements, 0 where it is
+ * broadcast; then one GEMM is planned per broadcast batch item ("Gemm and
+ * MatMul Performance Roadmap", section "Phase 4: complete MatMul", steps 1-6,
+ * including the collapse of contiguous batch dimensions).
+ *
+ *  a_shape[a_rank], b_shape[b_rank]: operand shapes, 1 <= rank <= OLC_MAX_RANK.
+ *      An extent 0 is allowed; it broadcasts against 1 (giving 0) and is an
+ *      error against an extent > 1.
+ *  dtype: the common element type of A, B and Y.
+ *  out: receives the new plan (owned by the caller; free with
+ *      olc_matmul_plan_destroy).  Set to NULL on error.
+ *
+ * Errors: OLC_ERR_NULL, OLC_ERR_RANK, OLC_ERR_NEGATIVE_DIM, OLC_ERR_K_MISMATCH,
+ * OLC_ERR_BATCH_MISMATCH, OLC_ERR_DTYPE, OLC_ERR_OOM (host or workspace
+ * allocation), OLC_ERR_CUDA.  If a CUDA device is present and the chosen
+ * algorithm needs a split reduction workspace, it is allocated here
+ * (cudaMalloc on the current device) and owned by the plan.
+ */
+olc_status olc_matmul_plan_create(const int64_t* a_shape, int a_rank,
+                                  const int64_t* b_shape, int b_rank,
+                                  olc_dtype dtype, olc_matmul_plan** out);
+
+/* Free a plan and its workspace.  NULL is accepted.  The caller must make sure
+ * no execute of this plan is still running on the device. */
+void olc_matmul_plan_destroy(olc_matmul_plan* plan);
+
+/*
+ * Enqueue Y = MatMul(A, B) on `stream`.
+ *
+ * "MatMul Kernel Design", sections "Shape and plan model" and "Scheduling
+ * and invariants": one GEMM per broadcast batch item, run as one launch over
+ * all items (the batch index is part of the grid); broadcast operands are read
+ * through zero batch strides, never copied.  Y must hold every batch item's
+ * complete M x N matrix: prod(output shape) elements.
+ *
+ *  A: prod(a_shape) elements, B: prod(b_shape) elements, Y: prod(out shape)
+ *     elements, all device pointers of the plan's dtype.
+ *  An output with no elements returns OLC_OK without launching anything and
+ *     without reading A, B or Y (they may be NULL).  With K == 0 and a
+ *     non-empty output, Y is filled with zeros and A and B are not read.
+ *  The tensor-core, skinny and split-K paths need 16-byte aligned A, B and Y;
+ *     with pointers that are not, the execute runs the DIRECT kernel instead.
+ *
+ * Errors: OLC_ERR_NULL (plan, or a data pointer of a non-empty product),
+ * OLC_ERR_WRONG_DEVICE, OLC_ERR_CUDA (a launch failed), OLC_ERR_OOM.
+ * Device-side failures are not seen here; use olc_matmul_execute_checked.
+ */
+olc_status olc_matmul_execute(const olc_matmul_plan* plan, const void* A, const void* B,
+                              void* Y, void* stream);
+
+/*
+ * olc_matmul_execute plus validation of the buffer sizes ("Scheduling and
+ * invariants": the output buffer must cover every broadcast batch item and
+ * its complete M x N matrix), then a synchronisation of `stream` and a read of
+ * the device error word that the library's bounded waits set.
+ *
+ *  a_numel, b_numel, y_numel: elements available behind A, B and Y.
+ * Errors: as olc_matmul_execute, plus OLC_ERR_BUFFER_TOO_SMALL (before any
+ * launch) and OLC_ERR_DEVICE_TIMEOUT (a kernel gave up waiting; Y is then
+ * unspecified).  The device error word is cleared by this call.
+ */
+olc_status olc_matmul_execute_checked(const olc_matmul_plan* plan,
+                                      const void* A, int64_t a_numel,
+                                      const void* B, int64_t b_numel,
+                                      void* Y, int64_t y_numel, void* stream);
+
+/*
+ * The same product from host buffers: copies A and B from host memory into
+ * the caller's device buffers, runs the plan, and copies Y back, all enqueued
+ * on `stream` (use pinned host memory for asynchronous copies).  Nothing is
+ * allocated.  A_host/B_host/Y_host: host pointers; A_dev/B_dev/Y_dev: device
+ * buffers of the same sizes.  Returns after enqueueing; synchronise `stream`
+ * before reading Y_host.  Errors: as olc_matmul_execute.
+ */
+olc_status olc_matmul_execute_host(const olc_matmul_plan* plan,
+                                   const void* A_host, const void* B_host, void* Y_host,
+                                   void* A_dev, void* B_dev, void* Y_dev, void* stream);
+
+/* ---- queries ----------------------------------------------------------- */
+
+/* Output shape: writes up to `capacity` extents into shape[] and the rank
+ * into *rank (0 = a scalar with one element, from two rank-one operands).
+ * Errors: OLC_ERR_NULL, OLC_ERR_INVALID (capacity too small). */
+olc_status olc_matmul_plan_output_shape(const olc_matmul_plan* plan, int64_t* shape,
+                                        int capacity, int* rank);
+
+/* Promoted matrix sizes and the number of broadcast batch items, before any
+ * folding: the product is batch x ([M, K] @ [K, N]).  NULL outputs skipped. */
+olc_status olc_matmul_plan_dims(const olc_matmul_plan* plan, int64_t* M, int64_t* N,
+                                int64_t* K, int64_t* batch);
+
+/* The broadcast batch shape (rank *batch_rank) and each operand's batch
+ * strides in elements, 0 where the operand is broadcast ("each input receives
+ * precomputed batch strides, including zero strides for broadcast
+ * dimensions").  Arrays need OLC_MAX_RANK entries; NULL arrays skipped. */
+olc_status olc_matmul_plan_batch(const olc_matmul_plan* plan, int* batch_rank,
+                                 int64_t* batch_shape, int64_t* a_strides,
+                                 int64_t* b_strides);
+
+/* The launch geometry after batch collapse and folding: GEMM rows M' (M times
+ * the folded batch), the number of batch items one launch walks, and the
+ * number of collapsed batch dimensions.  NULL outputs skipped. */
+olc_status olc_matmul_plan_launch_shape(const olc_matmul_plan* plan, int64_t* rows,
+                                        int64_t* items, int* collapsed_rank);
+
+/* Selected algorithm (an olc_algorithm value), or -1 for a NULL plan. */
+int olc_matmul_plan_algorithm(const olc_matmul_plan* plan);
+
+/* Force an algorithm (testing and tuning sweeps); OLC_ALGO_AUTO restores the
+ * automatic choice.  Errors: OLC_ERR_NULL, OLC_ERR_INVALID (unknown value),
+ * OLC_ERR_ALIGNMENT (the algorithm cannot take this shape or type),
+ * OLC_ERR_OOM / OLC_ERR_CUDA (workspace).  EMPTY and ZERO_FILL plans accept
+ * only themselves or AUTO. */
+olc_status olc_matmul_plan_force_algorithm(olc_matmul_plan* plan, int algo);
+
+/* Kernel launches one execute of this plan makes (0 for EMPTY). */
+int olc_matmul_plan_launches(const olc_matmul_plan* plan);
+
+/* Bytes of device workspace the plan owns (split reductions), 0 if none. */
+size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan);
+
+/* One-line description of the plan (algorithm, tile, grid, splits) written
+ * into buf (NUL-terminated, truncated to cap).  Returns the full length. */
+int olc_matmul_plan_describe(const olc_matmul_plan* plan, char* buf, size_t cap);
+
+/* Static strings; never NULL. */
+const char* olc_status_string(int status);
+const char* olc_algorithm_name(int algo);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int olc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OLC_MATMUL_H */

@@ -1,0 +1,188 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched): the
+library loads and exports every function the header declares; plans resolve
+shapes, batch strides and errors as the shape rules say; the algorithm choice
+and its feasibility rules; workspace sizing."""
+
+import ctypes
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from gemm_matmulplan_broadcast_gb300 import Plan, binding
+from gemm_matmulplan_broadcast_gb300.binding import OlcError
+
+from test_oracle_pins import _golden_shapes
+
+
+def test_library_exports_every_declared_function():
+    lib = binding.load()
+    names = binding.header_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(lib, name), name
+    assert lib.olc_version() >= 100
+
+
+def test_status_and_algorithm_strings():
+    lib = binding.load()
+    for code in binding.STATUS:
+        assert lib.olc_status_string(code)
+    assert lib.olc_status_string(999) == b"unknown status"
+    for name, code in binding.ALGORITHMS.items():
+        assert lib.olc_algorithm_name(code).decode() == name
+
+
+@pytest.mark.parametrize("a_shape,b_shape,want", _golden_shapes())
+def test_plan_output_shape_matches_golden_table(a_shape, b_shape, want):
+    if want is None:
+        with pytest.raises(OlcError):
+            Plan(a_shape, b_shape, "float32")
+    else:
+        with Plan(a_shape, b_shape, "float32") as p:
+            assert p.output_shape == want
+            assert p.output_shape == oracle.output_shape(a_shape, b_shape)
+
+
+def _numpy_batch_strides(a_shape, b_shape):
+    """Reference batch strides: numpy's broadcast_to view of each operand's
+    matrix index array (stride 0 along broadcast dimensions)."""
+    a2 = (1,) + tuple(a_shape) if len(a_shape) == 1 else tuple(a_shape)
+    b2 = tuple(b_shape) + (1,) if len(b_shape) == 1 else tuple(b_shape)
+    batch = np.broadcast_shapes(a2[:-2], b2[:-2])
+    out = []
+    for op in (a2, b2):
+        mat = op[-2] * op[-1]
+        idx = np.arange(int(np.prod(op[:-2], dtype=np.int64)) if len(op) > 2 else 1,
+                        dtype=np.int64).reshape(op[:-2])
+        view = np.broadcast_to(idx, batch)
+        out.append(tuple(s // 8 * mat for s in view.strides))
+    return batch, out[0], out[1]
+
+
+STRIDE_CASES = [
+    ((8, 1, 128, 256), (1, 4, 256, 64)),
+    ((2, 1, 3, 1, 4, 5), (7, 1, 6, 5, 2)),
+    ((1, 1, 4, 5), (3, 5, 6)),
+    ((256,), (4, 256, 64)),
+    ((4, 32, 256), (256,)),
+    ((3, 2, 4, 5), (2, 5, 6)),
+    ((5, 6), (2, 3, 6, 7)),
+]
+
+
+@pytest.mark.parametrize("a_shape,b_shape", STRIDE_CASES)
+def test_batch_strides_match_numpy_broadcast_views(a_shape, b_shape):
+    batch, sa_ref, sb_ref = _numpy_batch_strides(a_shape, b_shape)
+    with Plan(a_shape, b_shape, "float32") as p:
+        shape, sa, sb = p.batch()
+        assert shape == tuple(batch)
+        for d, e in enumerate(batch):
+            if e > 1:   # strides of extent-1 dimensions are never used
+                assert sa[d] == sa_ref[d] and sb[d] == sb_ref[d]
+            else:
+                assert sa[d] == 0 and sb[d] == 0
+        m, n, k, nb = p.dims()
+        assert nb == int(np.prod(batch, dtype=np.int64))
+
+
+def test_batch_collapse_and_fold():
+    # B shared by every item and A's items consecutive: folded into rows
+    with Plan((8, 2048, 64), (64, 32), "float32") as p:
+        assert p.launch_shape() == (8 * 2048, 1, 0)
+    with Plan((2, 3, 16, 8), (8, 4), "float32") as p:
+        assert p.launch_shape() == (2 * 3 * 16, 1, 0)
+    # rank-2 A with rank-one B: folds too (B shared)
+    with Plan((4, 32, 256), (256,), "float32") as p:
+        assert p.launch_shape() == (128, 1, 0)
+    # both sides broadcast along different dims: two collapsed dims, 32 items
+    with Plan((8, 1, 128, 256), (1, 4, 256, 64), "float32") as p:
+        assert p.launch_shape() == (128, 32, 2)
+    # contiguous batch dims on both sides collapse into one
+    with Plan((2, 3, 4, 5), (2, 3, 5, 6), "float32") as p:
+        assert p.launch_shape() == (4, 6, 1)
+    # extent-1 dims drop out
+    with Plan((1, 3, 1, 4, 5), (1, 1, 5, 6), "float32") as p:
+        assert p.launch_shape() == (12, 1, 0)
+    # B broadcast but A too: cannot fold
+    with Plan((1, 4, 5), (3, 5, 6), "float32") as p:
+        assert p.launch_shape() == (4, 3, 1)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (((2, 3), (4, 5)), "OLC_ERR_K_MISMATCH"),
+    (((2, 3, 4), (3, 4, 5)), "OLC_ERR_BATCH_MISMATCH"),
+    (((-1, 3), (3, 4)), "OLC_ERR_NEGATIVE_DIM"),
+    (((1,) * 9, (1, 1)), "OLC_ERR_RANK"),
+])
+def test_create_errors(bad, status):
+    with pytest.raises(OlcError) as ei:
+        Plan(bad[0], bad[1], "float32")
+    assert ei.value.name == status
+
+
+def test_create_rejects_rank0_null_and_bad_dtype():
+    lib = binding.load()
+    h = ctypes.c_void_p()
+    a = (ctypes.c_int64 * 2)(3, 4)
+    assert lib.olc_matmul_plan_create(a, 0, a, 2, 1, ctypes.byref(h)) == 2    # rank 0
+    assert lib.olc_matmul_plan_create(a, 2, a, 2, 7, ctypes.byref(h)) == 6    # dtype 7
+    assert lib.olc_matmul_plan_create(None, 2, a, 2, 1, ctypes.byref(h)) == 1
+    assert lib.olc_matmul_plan_create(a, 2, a, 2, 1, None) == 1
+    assert h.value is None
+    lib.olc_matmul_plan_destroy(None)   # NULL is accepted
+    assert lib.olc_matmul_plan_algorithm(None) == -1
+
+
+def test_algorithm_choice_for_named_shapes():
+    cases = [
+        ((64, 128), (128, 96), "float32", "direct"),
+        ((8, 1, 128, 256), (1, 4, 256, 64), "float32", "general_simt"),
+        ((0, 16, 32), (32, 8), "float32", "empty"),
+        ((5, 0), (0, 7), "float32", "zero_fill"),
+        ((4, 8192), (8192, 28672), "float16", "skinny_m"),
+        ((16384, 4096), (4096, 8), "float16", "skinny_n"),
+        ((32, 131072), (131072, 32), "float16", "split_k"),
+        ((4096, 4096), (4096, 4096), "float32", "general_simt"),
+        ((4096, 4096), (4096, 4096), "float64", "general_simt"),
+    ]
+    for a, b, dt, want in cases:
+        with Plan(a, b, dt) as p:
+            assert p.algorithm == want, (a, b, dt, p.describe())
+
+
+def test_force_algorithm_feasibility():
+    with Plan((40, 24), (24, 20), "float16") as p:
+        p.force("direct")
+        assert p.algorithm == "direct"
+        p.force("general_simt")
+        with pytest.raises(OlcError):
+            p.force("skinny_m")          # 40 rows > 16
+        with pytest.raises(OlcError):
+            p.force("empty")
+        p.force("auto")
+    with Plan((3, 24), (24, 20), "float16") as p:
+        with pytest.raises(OlcError):
+            p.force("skinny_m")          # N * 2 bytes not a multiple of 16
+    with Plan((3, 24), (24, 24), "float16") as p:
+        p.force("skinny_m")
+    with Plan((0, 4), (4, 4), "float32") as p:
+        assert p.algorithm == "empty"
+        with pytest.raises(OlcError):
+            p.force("direct")
+        p.force("empty")
+    with Plan((2, 0), (0, 4), "float32") as p:
+        assert p.algorithm == "zero_fill"
+        p.force("zero_fill")
+
+
+def test_workspace_and_launch_counts():
+    with Plan((32, 131072), (131072, 32), "float16") as p:
+        assert p.algorithm == "split_k"
+        assert p.workspace_bytes > 0 and p.launches == 1
+    with Plan((0, 16, 32), (32, 8), "float32") as p:
+        assert p.launches == 0 and p.workspace_bytes == 0
+    with Plan((64, 128), (128, 96), "float32") as p:
+        assert p.workspace_bytes == 0 and p.launches == 1
+        assert "direct" in p.describe()

@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle on the same
+seeded inputs, for every named workload, every algorithm on small ragged
+shapes, and the edge cases (empty outputs, K == 0, rank-one operands,
+broadcast batches, unaligned pointers, buffer checks)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_matmulplan_broadcast_gb300 import OlcError, Plan, synth
+from parity import TOL, check_product, compare, gpu_matmul, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["float32", "float64", "float16", "bfloat16"]
+
+
+# --------------------------------------------------------------------------
+# the named workloads at their own sizes
+
+
+def test_fp32_64x128x96_uniform_and_exact_integers():
+    w = synth.workload("fp32_64x128x96")
+    for prod in w.products:
+        a, b = prod.draw()
+        check_product(a, b, prod.dtype, exact=(prod.name == "small_int"))
+
+
+def test_fp32_broadcast_batch_and_rank_one_and_empty():
+    w = synth.workload("fp32_broadcast_batch")
+    for prod in w.products:
+        a, b = prod.draw()
+        y, algo = check_product(a, b, prod.dtype)
+        assert y.shape == oracle.output_shape(prod.a_shape, prod.b_shape)
+        if prod.name == "empty_batch":
+            assert algo == "empty" and y.numel() == 0
+
+
+@pytest.mark.parametrize("algorithm", [None, "direct", "general_simt"])
+def test_broadcast_equals_explicit_repeat_bit_exact(algorithm):
+    a, b = synth.operands((8, 1, 128, 256), (1, 4, 256, 64), "float32", synth.UNIFORM,
+                          synth.UNIFORM, seed=1)
+    y_bc, _ = gpu_matmul(a, b, "float32", algorithm)
+    ar = a.expand(8, 4, 128, 256).contiguous()
+    br = b.expand(8, 4, 256, 64).contiguous()
+    y_rep, _ = gpu_matmul(ar, br, "float32", algorithm)
+    assert torch.equal(y_bc, y_rep)
+
+
+def test_bf16_transformer_projection_sampled_rows():
+    w = synth.workload("bf16_transformer_projection")
+    for prod in w.products:
+        a, b = prod.draw()
+        y, algo = gpu_matmul(a, b, prod.dtype, checked=True, guard=16)
+        k = prod.a_shape[-1]
+        a2 = synth.to_numpy_storage(a).reshape(-1, k)
+        rows = sample_rows(a2.shape[0], seed=len(prod.name))
+        y_ref, s = oracle.gemm2d(a2, synth.to_numpy_storage(b), prod.dtype, rows=rows)
+        y2 = y.reshape(-1, prod.b_shape[-1])[rows]
+        compare(y2, y_ref, s, prod.dtype)
+
+
+def test_fp16_skinny_and_split_k_full():
+    w = synth.workload("fp16_skinny_splitk")
+    want = {"skinny_m": "skinny_m", "skinny_n": "skinny_n", "split_k": "split_k"}
+    for prod in w.products:
+        a, b = prod.draw()
+        y, algo = check_product(a, b, prod.dtype)
+        assert algo == want[prod.name]
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float64"])
+def test_square_sweep_and_chain(dtype):
+    w = synth.workload("%s_square_chain" % dtype)
+    for prod in w.products:
+        a, b = prod.draw()
+        y, _ = gpu_matmul(a, b, dtype, guard=16)
+        rows = None if prod.a_shape[0] <= 1024 else sample_rows(prod.a_shape[0], extra=64)
+        y_ref, s = oracle.gemm2d(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype,
+                                 rows=rows)
+        compare(y if rows is None else y[rows], y_ref, s, dtype)
+    # the chain: every stage on the GPU feeds the next; the oracle runs its
+    # own chain on the sampled rows (row i of each stage depends only on row i
+    # of the previous one).  The bound adds the previous stage's propagated
+    # tolerance: tol * (S_prev @ |W|).
+    (chain,) = w.chains
+    xs = chain.draw()
+    cur = xs[0].cuda()
+    rows = sample_rows(chain.shapes[0][0], extra=64)
+    ref = synth.to_numpy_storage(xs[0])[rows]
+    prev_bound = np.zeros(ref.shape)
+    for wt in xs[1:]:
+        with Plan(tuple(cur.shape), tuple(wt.shape), dtype) as p:
+            out = torch.empty(p.output_shape, dtype=cur.dtype, device="cuda")
+            p.execute(cur, wt.cuda(), out)
+        cur = out
+        wn = synth.to_numpy_storage(wt)
+        ref, s = oracle.gemm2d(ref, wn, dtype)
+        bound = TOL[dtype] * s + prev_bound @ np.abs(wn)
+        yg = cur.cpu().numpy()[rows].astype(np.float64)
+        err = np.abs(yg - ref)
+        assert np.all(err <= bound), float((err / bound).max())
+        prev_bound = bound
+
+
+# --------------------------------------------------------------------------
+# every algorithm on small ragged shapes
+
+ALGOS = ["direct", "general_simt", "skinny_m", "skinny_n", "split_k", "general_tc"]
+
+SMALL_SHAPES = [
+    ((1, 8), (8, 16)),
+    ((3, 40), (40, 24)),
+    ((16, 72), (72, 64)),
+    ((17, 65), (65, 255)),
+    ((127, 129), (129, 33)),
+    ((129, 64), (64, 257)),
+    ((200, 3000), (3000, 8)),
+    ((33, 9000), (9000, 40)),
+    ((2, 3, 5, 16), (3, 16, 24)),
+    ((5, 1, 7, 40), (1, 3, 40, 16)),
+    ((64,), (64, 48)),
+    ((3, 80, 64), (64,)),
+]
+
+
+def _feasible(a_shape, b_shape, dtype, algo):
+    try:
+        with Plan(a_shape, b_shape, dtype) as p:
+            p.force(algo)
+        return True
+    except OlcError:
+        return False
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shapes", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_every_algorithm_uniform(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.UNIFORM, synth.UNIFORM, seed=7)
+    ran = 0
+    for algo in ALGOS:
+        if _feasible(a_shape, b_shape, dtype, algo):
+            check_product(a, b, dtype, algorithm=algo)
+            ran += 1
+    assert ran >= 2
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shapes", SMALL_SHAPES[:9], ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_every_algorithm_integers_bit_exact(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=8)
+    for algo in ALGOS:
+        if _feasible(a_shape, b_shape, dtype, algo):
+            check_product(a, b, dtype, algorithm=algo, exact=True)
+
+
+@pytest.mark.parametrize("algo,shapes", [
+    ("split_k", ((32, 131072), (131072, 32))),
+    ("skinny_m", ((4, 8192), (8192, 28672))),
+])
+def test_split_reductions_are_reproducible(algo, shapes):
+    a, b = synth.operands(shapes[0], shapes[1], "float16", synth.normal(1.0), synth.normal(0.02),
+                          seed=3)
+    y1, _ = gpu_matmul(a, b, "float16", algo)
+    y2, _ = gpu_matmul(a, b, "float16", algo)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+# --------------------------------------------------------------------------
+# edge cases
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_k_zero_fills_zeros(dtype):
+    a = torch.empty((5, 0), dtype=synth.TORCH_DTYPES[dtype])
+    b = torch.empty((0, 7), dtype=synth.TORCH_DTYPES[dtype])
+    y, algo = gpu_matmul(a, b, dtype)
+    assert algo == "zero_fill" and y.shape == (5, 7) and bool((y == 0).all())
+
+
+def test_empty_outputs_launch_nothing_and_accept_null():
+    for a_shape, b_shape in [((0, 16, 32), (32, 8)), ((4, 5), (5, 0)), ((0, 1, 2, 3), (1, 5, 3, 4))]:
+        with Plan(a_shape, b_shape, "float32") as p:
+            assert p.algorithm == "empty" and p.launches == 0
+            st = p.lib.olc_matmul_execute(p.handle, None, None, None, None)
+            assert st == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_unaligned_pointers_still_correct(dtype):
+    # operands that start one element into their buffers
+    a, b = synth.operands((16, 64), (64, 256), dtype, synth.UNIFORM, synth.UNIFORM, seed=5)
+    tdt = synth.TORCH_DTYPES[dtype]
+    abuf = torch.zeros(a.numel() + 1, dtype=tdt, device="cuda")
+    bbuf = torch.zeros(b.numel() + 1, dtype=tdt, device="cuda")
+    ybuf = torch.zeros(16 * 256 + 1, dtype=tdt, device="cuda")
+    A = abuf[1:].view(16, 64)
+    B = bbuf[1:].view(64, 256)
+    Y = ybuf[1:].view(16, 256)
+    A.copy_(a.cuda())
+    B.copy_(b.cuda())
+    with Plan((16, 64), (64, 256), dtype) as p:
+        p.execute_checked(A, B, Y)
+    y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+    compare(Y.cpu(), y_ref, s, dtype)
+
+
+def test_checked_execute_rejects_small_buffers():
+    with Plan((8, 16), (16, 4), "float32") as p:
+        A = torch.zeros(8, 16, device="cuda")
+        B = torch.zeros(16, 4, device="cuda")
+        Y = torch.zeros(8, 4, device="cuda")
+        lib = p.lib
+        assert lib.olc_matmul_execute_checked(p.handle, A.data_ptr(), 127, B.data_ptr(), 64,
+                                              Y.data_ptr(), 32, None) == 8
+        assert lib.olc_matmul_execute_checked(p.handle, A.data_ptr(), 128, B.data_ptr(), 64,
+                                              Y.data_ptr(), 31, None) == 8
+        assert lib.olc_matmul_execute_checked(p.handle, A.data_ptr(), 128, B.data_ptr(), 64,
+                                              Y.data_ptr(), 32, None) == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_execute_host_round_trip(dtype):
+    a, b = synth.operands((3, 40, 64), (64, 48), dtype, synth.UNIFORM, synth.UNIFORM, seed=6)
+    tdt = synth.TORCH_DTYPES[dtype]
+    with Plan(a.shape, b.shape, dtype) as p:
+        ah, bh = a.pin_memory(), b.pin_memory()
+        yh = torch.empty(p.output_shape, dtype=tdt).pin_memory()
+        ad = torch.empty_like(a, device="cuda")
+        bd = torch.empty_like(b, device="cuda")
+        yd = torch.empty(p.output_shape, dtype=tdt, device="cuda")
+        p.execute_host(ah, bh, yh, ad, bd, yd)
+        torch.cuda.synchronize()
+    y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+    compare(yh, y_ref, s, dtype)
+
+
+def test_plan_reuse_across_streams_and_inputs():
+    with Plan((64, 96), (96, 80), "float32") as p:
+        s = torch.cuda.Stream()
+        for seed in range(3):
+            a, b = synth.operands((64, 96), (96, 80), "float32", synth.UNIFORM, synth.UNIFORM, seed)
+            A, B = a.cuda(), b.cuda()
+            Y = torch.empty(64, 80, device="cuda")
+            with torch.cuda.stream(s):
+                p.execute(A, B, Y, stream=s)
+            s.synchronize()
+            y_ref, sm = oracle.matmul(a.numpy(), b.numpy(), "float32")
+            compare(Y.cpu(), y_ref, sm, "float32")
