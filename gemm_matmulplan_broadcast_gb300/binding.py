@@ -30,7 +30,7 @@ STATUS = {
     4: "OLC_ERR_K_MISMATCH", 5: "OLC_ERR_BATCH_MISMATCH", 6: "OLC_ERR_DTYPE",
     7: "OLC_ERR_ALIGNMENT", 8: "OLC_ERR_BUFFER_TOO_SMALL", 9: "OLC_ERR_NO_CONSTANT_B",
     10: "OLC_ERR_CUDA", 11: "OLC_ERR_DEVICE_TIMEOUT", 12: "OLC_ERR_OOM",
-    13: "OLC_ERR_INVALID", 14: "OLC_ERR_WRONG_DEVICE",
+    13: "OLC_ERR_INVALID", 14: "OLC_ERR_WRONG_DEVICE", 15: "OLC_ERR_SCRATCH_LIMIT",
 }
 MAX_RANK = 8
 

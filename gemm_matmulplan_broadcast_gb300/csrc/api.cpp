@@ -544,6 +544,7 @@ const char* olc_status_string(int status) {
         case OLC_ERR_OOM: return "out of memory";
         case OLC_ERR_INVALID: return "invalid argument";
         case OLC_ERR_WRONG_DEVICE: return "current device is not the plan's device";
+        case OLC_ERR_SCRATCH_LIMIT: return "problem needs more than the static scratch array";
     }
     return "unknown status";
 }

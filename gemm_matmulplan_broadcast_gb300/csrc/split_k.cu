@@ -13,6 +13,9 @@
 // slice order s = 0, 1, ..., S-1 and writes the narrowed result.  The order of
 // the final sum does not depend on which block arrives last, so the result is
 // bit-reproducible run to run.
+#include <cstring>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace olc {
@@ -141,3 +144,108 @@ cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, const Wor
 }
 
 }  // namespace olc
+
+// ===========================================================================
+// Allocation-free split-K: the same kernel, with its partial tiles and arrival
+// counters in a file-scope device array instead of a cudaMalloc'd workspace,
+// for callers that must not allocate device memory while they run.
+
+namespace olc {
+namespace {
+
+constexpr size_t kStaticScratchBytes = OLC_SPLIT_K_STATIC_SCRATCH_BYTES;
+constexpr size_t kStaticCounterBytes = 16 * 1024;   // 4096 counters
+constexpr size_t kStaticPartialBytes = kStaticScratchBytes - kStaticCounterBytes;
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_split_k_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per
+// device.  In host code the array's name is only a host-side stand-in.
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_split_k_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace olc
+
+extern "C" olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, const void* B,
+                                                void* Y, int64_t M, int64_t N, int64_t K,
+                                                void* stream) {
+    using namespace olc;
+    if (dtype != OLC_FLOAT && dtype != OLC_DOUBLE && dtype != OLC_FLOAT16 &&
+        dtype != OLC_BFLOAT16)
+        return OLC_ERR_DTYPE;
+    if (M < 0 || N < 0 || K < 0) return OLC_ERR_NEGATIVE_DIM;
+    if (M == 0 || N == 0) return OLC_OK;
+    if (!Y) return OLC_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t eb = dtype == OLC_DOUBLE ? 8 : dtype == OLC_FLOAT ? 4 : 2;
+    if (K == 0) {
+        return launch_zero_fill(Y, M * N * eb, s) == cudaSuccess ? OLC_OK : OLC_ERR_CUDA;
+    }
+    if (!A || !B) return OLC_ERR_NULL;
+
+    Problem p;
+    std::memset(&p, 0, sizeof p);
+    p.A = A;
+    p.B = B;
+    p.Y = Y;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.items = 1;
+    const int64_t tiles = ceil_div(M, 32) * ceil_div(N, 32);
+    const int64_t tile_bytes = 32 * 32 * acc_bytes(dtype);
+    if (tiles * (int64_t)sizeof(unsigned int) > (int64_t)kStaticCounterBytes ||
+        tiles * tile_bytes > (int64_t)kStaticPartialBytes)
+        return OLC_ERR_SCRATCH_LIMIT;
+
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return OLC_ERR_CUDA;
+    }
+    int splits = split_k_pick(dtype, p, sms);
+    const int64_t fit = (int64_t)kStaticPartialBytes / (tiles * tile_bytes);
+    if (splits > fit) splits = (int)fit;
+    if (splits < 1) splits = 1;
+
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) {
+        cudaGetLastError();
+        return OLC_ERR_CUDA;
+    }
+    Workspace ws;
+    ws.counters = static_cast<unsigned int*>(base);
+    ws.counter_count = (size_t)tiles;
+    ws.partials = static_cast<unsigned char*>(base) + kStaticCounterBytes;
+    ws.partial_bytes = (size_t)(tiles * splits * tile_bytes);
+    // the counters must start at zero for this launch, whatever an earlier
+    // call left behind
+    if (cudaMemsetAsync(ws.counters, 0, (size_t)tiles * sizeof(unsigned int), s) != cudaSuccess) {
+        cudaGetLastError();
+        return OLC_ERR_CUDA;
+    }
+    if (launch_split_k(dtype, p, splits, ws, s) != cudaSuccess) {
+        cudaGetLastError();
+        return OLC_ERR_CUDA;
+    }
+    return OLC_OK;
+}

@@ -61,7 +61,8 @@ typedef enum {
     OLC_ERR_DEVICE_TIMEOUT = 11,  /* a bounded device-side wait ran out            */
     OLC_ERR_OOM = 12,             /* workspace allocation failed                   */
     OLC_ERR_INVALID = 13,         /* an argument is out of its documented range    */
-    OLC_ERR_WRONG_DEVICE = 14     /* current device differs from the plan's        */
+    OLC_ERR_WRONG_DEVICE = 14,    /* current device differs from the plan's        */
+    OLC_ERR_SCRATCH_LIMIT = 15    /* needs more than the static scratch array      */
 } olc_status;
 
 /* The algorithm a plan runs ("MatMul Kernel Design", section "Types and
@@ -224,6 +225,55 @@ const char* olc_algorithm_name(int algo);
 
 /* Library version, as major * 10000 + minor * 100 + patch. */
 int olc_version(void);
+
+/* ---- allocation-free split-K ------------------------------------------- */
+
+/* Size of the device array behind olc_matmul_split_k_static: 4 MiB, held by
+ * every GPU that loads this library until the process exits. */
+#define OLC_SPLIT_K_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/*
+ * Split-K product Y[M, N] = A[M, K] @ B[K, N] (dense row-major device
+ * buffers, one element type) that allocates nothing.  The pages have no
+ * counterpart for this entry point: it exists for callers that must not
+ * allocate device memory while they run, such as a host framework whose
+ * memory pool owns the whole device and forbids raw cudaMalloc, or a
+ * latency-bound serving loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The plan path allocates its split-K workspace with
+ * cudaMalloc at olc_matmul_plan_create; this entry point instead keeps the
+ * partial tiles and arrival counters in one file-scope device array of
+ * OLC_SPLIT_K_STATIC_SCRATCH_BYTES bytes inside the library.
+ *
+ * It runs the same split-K kernel as the plan path (partials per K slice,
+ * summed by the last-arriving block in slice order) with the number of slices
+ * capped so the partials fit the array.
+ *
+ *  dtype: OLC_FLOAT, OLC_DOUBLE, OLC_FLOAT16 or OLC_BFLOAT16.
+ *  A, B, Y: caller-owned device pointers (M*K, K*N and M*N elements).
+ *  M, N, K >= 0.  M*N == 0 returns OLC_OK with nothing launched; K == 0
+ *  fills Y with zeros.
+ *  stream: cudaStream_t as void* (NULL = legacy default stream).
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture on that device.  Every call clears the arrival counters
+ * with cudaMemsetAsync on `stream` before its kernel, so a call never depends
+ * on what the previous one left in the array; but all calls share the one
+ * array, so calls whose executions overlap on the GPU (other streams, other
+ * host threads) race and must be serialised by the caller.
+ *
+ * Layout of the array: the first 16 KiB hold up to 4096 arrival counters,
+ * the rest holds the partial tiles (32 x 32 accumulators per output tile and
+ * K slice).  So ceil(M/32) * ceil(N/32) may be at most 1020 for FLOAT,
+ * FLOAT16 and BFLOAT16 (float32 partials) and at most 510 for DOUBLE.
+ *
+ * Errors: OLC_ERR_DTYPE, OLC_ERR_NULL (a pointer of a non-empty product),
+ * OLC_ERR_NEGATIVE_DIM, OLC_ERR_SCRATCH_LIMIT (more output tiles than the
+ * limits above), OLC_ERR_CUDA (the address lookup, memset or launch failed).
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, const void* B, void* Y,
+                                     int64_t M, int64_t N, int64_t K, void* stream);
 
 #ifdef __cplusplus
 }
