@@ -226,6 +226,15 @@ const char* olc_algorithm_name(int algo);
 /* Library version, as major * 10000 + minor * 100 + patch. */
 int olc_version(void);
 
+/* ---- testing hooks ------------------------------------------------------ */
+
+/* The 64-bit shared-memory matrix descriptor and the 32-bit instruction
+ * descriptor the tensor-core kernel hands to tcgen05.mma (PTX ISA, tcgen05
+ * "shared memory descriptor" and "instruction descriptor" for kind::f16),
+ * exported so a host test can check the bit layout.  Pure functions. */
+uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo);
+uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int b_mn_major);
+
 /* ---- allocation-free split-K ------------------------------------------- */
 
 /* Size of the device array behind olc_matmul_split_k_static: 4 MiB, held by

@@ -186,3 +186,42 @@ def test_workspace_and_launch_counts():
     with Plan((64, 128), (128, 96), "float32") as p:
         assert p.workspace_bytes == 0 and p.launches == 1
         assert "direct" in p.describe()
+
+
+def _field(v, lo, hi):
+    return (v >> lo) & ((1 << (hi - lo + 1)) - 1)
+
+
+def test_tcgen05_descriptor_bit_layout():
+    """Field-by-field check of the descriptors the tensor-core kernel builds,
+    against the PTX ISA tables (tcgen05 shared memory descriptor; instruction
+    descriptor for kind::f16)."""
+    lib = binding.load()
+    lib.olc_debug_tc_smem_desc.argtypes = [ctypes.c_uint32] * 3
+    lib.olc_debug_tc_smem_desc.restype = ctypes.c_uint64
+    lib.olc_debug_tc_instr_desc.argtypes = [ctypes.c_int] * 4
+    lib.olc_debug_tc_instr_desc.restype = ctypes.c_uint32
+    d = lib.olc_debug_tc_smem_desc(0x1A400, 8192, 1024)
+    assert _field(d, 0, 13) == 0x1A400 >> 4      # start address >> 4
+    assert _field(d, 14, 15) == 0
+    assert _field(d, 16, 29) == 8192 >> 4        # leading byte offset >> 4
+    assert _field(d, 32, 45) == 1024 >> 4        # stride byte offset >> 4
+    assert _field(d, 46, 47) == 1                # fixed 0b01 for tcgen05
+    assert _field(d, 49, 51) == 0                # base offset
+    assert _field(d, 52, 52) == 0                # relative LBO mode
+    assert _field(d, 61, 63) == 2                # 128-byte swizzle
+    # the address field keeps 18 bits of byte address (256 KiB window)
+    assert _field(lib.olc_debug_tc_smem_desc(0x3FFF0, 16, 1024), 0, 13) == 0x3FFF
+    for bf16 in (0, 1):
+        i = lib.olc_debug_tc_instr_desc(bf16, 128, 256, 1)
+        assert _field(i, 0, 3) == 0                  # dense, no saturate
+        assert _field(i, 4, 5) == 1                  # D = F32
+        assert _field(i, 7, 9) == bf16               # A: 0 F16, 1 BF16
+        assert _field(i, 10, 12) == bf16             # B
+        assert _field(i, 13, 14) == 0                # no negation
+        assert _field(i, 15, 15) == 0                # A K-major
+        assert _field(i, 16, 16) == 1                # B MN-major
+        assert _field(i, 17, 22) == 256 >> 3         # N
+        assert _field(i, 23, 23) == 0
+        assert _field(i, 24, 28) == 128 >> 4         # M
+        assert _field(i, 29, 31) == 0

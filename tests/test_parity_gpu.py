@@ -170,6 +170,51 @@ def test_split_reductions_are_reproducible(algo, shapes):
 
 
 # --------------------------------------------------------------------------
+# the tensor-core path: one tile first, then tails, batches, many tiles
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+def test_tc_single_tile(dtype):
+    a, b = synth.operands((128, 64), (64, 256), dtype, synth.SMALL_INT, synth.SMALL_INT, seed=1)
+    y, algo = check_product(a, b, dtype, algorithm="general_tc", exact=True)
+    assert algo == "general_tc"
+
+
+TC_SHAPES = [
+    ((128, 128), (128, 256)),
+    ((300, 520), (520, 264)),        # M, N and K tails
+    ((1, 8), (8, 8)),
+    ((129, 4104), (4104, 520)),
+    ((3, 1, 130, 64), (1, 2, 64, 136)),   # broadcast batch through 3-D tensor maps
+    ((2, 3, 40, 32), (3, 32, 24)),
+    ((64,), (64, 48)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("shapes", TC_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_tc_shapes(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=9)
+    check_product(a, b, dtype, algorithm="general_tc")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=9)
+    check_product(ai, bi, dtype, algorithm="general_tc", exact=True)
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+def test_tc_many_tiles_per_cta_sampled(dtype):
+    # 32 x 8 = 256 tiles of 128 x 256: more than one tile per CTA, both TMEM
+    # accumulators in use
+    a, b = synth.operands((4096, 1024), (1024, 2048), dtype, synth.normal(1.0),
+                          synth.normal(0.02), seed=10)
+    y, algo = gpu_matmul(a, b, dtype, "general_tc")
+    rows = sample_rows(4096, extra=128)
+    y_ref, s = oracle.gemm2d(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype,
+                             rows=rows)
+    compare(y[rows], y_ref, s, dtype)
+
+
+# --------------------------------------------------------------------------
 # edge cases
 
 
