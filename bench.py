@@ -97,10 +97,22 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi holds driver locks while it starts; do not time anything
+        # until it has written its first sample
+        t0 = time.time()
+        while time.time() - t0 < 10.0:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.05)
+        time.sleep(0.2)
 
     def stop(self):
         if self.proc is None:
@@ -311,23 +323,30 @@ def cpu_oracle_sample(workload, target_seconds: float, items=None):
         an = an.reshape((1, k) if an.ndim == 1 else (-1, k))
         bn = bn.reshape((k, 1)) if bn.ndim == 1 else bn.reshape((-1, k, n))[0]
         prods.append((prod, an, np.ascontiguousarray(bn), n, k))
-    # calibrate with one row of each product
-    rows = 1
-    t0 = time.perf_counter()
-    for prod, an, bn, n, k in prods:
-        oracle.gemm2d(an, bn, prod.dtype, rows=[0])
-    t1 = time.perf_counter() - t0
-    per_row = max(t1, 1e-6)
-    rows = int(max(1, min(4096, target_seconds / per_row)))
+    # size the sample: grow the row count until one pass takes a quarter of
+    # the target, then scale to the target
     rng = np.random.default_rng(0)
-    flops = 0.0
-    t0 = time.perf_counter()
-    for prod, an, bn, n, k in prods:
-        r = min(rows, an.shape[0])
-        sel = np.sort(rng.choice(an.shape[0], size=r, replace=False))
-        oracle.gemm2d(an, bn, prod.dtype, rows=sel)
-        flops += 2.0 * r * n * k
-    secs = time.perf_counter() - t0
+
+    def one_pass(rows):
+        fl = 0.0
+        t0 = time.perf_counter()
+        for prod, an, bn, n, k in prods:
+            r = min(rows, an.shape[0])
+            sel = np.sort(rng.choice(an.shape[0], size=r, replace=False))
+            oracle.gemm2d(an, bn, prod.dtype, rows=sel)
+            fl += 2.0 * r * n * k
+        return fl, time.perf_counter() - t0
+
+    max_rows = max(an.shape[0] for _, an, _, _, _ in prods)
+    rows = 8
+    fl, el = one_pass(rows)
+    while el < target_seconds / 4 and rows < max_rows:
+        rows = int(min(max_rows, max(rows * 2, rows * (target_seconds / 2) / max(el, 1e-3))))
+        fl, el = one_pass(rows)
+    if el < target_seconds * 0.6 and rows < max_rows:
+        rows = int(min(max_rows, rows * target_seconds / max(el, 1e-3)))
+        fl, el = one_pass(rows)
+    flops, secs = fl, el
     desc = "%d rows of each of %d products (all N columns, full K), oracle C triple loop" % (
         rows, len(prods))
     return flops, secs, oracle.threads(), desc
@@ -373,6 +392,44 @@ def measure_workload(workload, steps, warmup, device, peaks, l2_bytes):
     return items, stream
 
 
+def measure_secondary(workload, device, peaks, l2):
+    """Median per-launch time and roofline of every product of a workload (and
+    of each chain stage), after 3 warm-up launches; about 1 s per product."""
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import Plan
+    items = build_inputs(workload, device)
+    for ch in workload.chains:
+        xs = ch.draw()
+        cur_shape = tuple(xs[0].shape)
+        cur = xs[0].to(device)
+        for j, w in enumerate(xs[1:]):
+            plan = Plan(cur_shape, tuple(w.shape), ch.dtype)
+            W = w.to(device)
+            Y = torch.empty(plan.output_shape, dtype=W.dtype, device=device)
+            flop, byts = work_of(cur_shape, tuple(w.shape), ch.dtype)
+            items.append({"name": "%s_%d" % (ch.name, j + 1), "plan": plan, "A": cur, "B": W,
+                          "Y": Y, "flop": flop, "bytes": byts, "dtype": ch.dtype})
+            cur, cur_shape = Y, tuple(Y.shape)
+    rotate_sets(items, 2 * l2, device)
+    stream = torch.cuda.Stream()
+    time_steps(items, 3, stream)
+    _, probe = time_steps(items, 1, stream)
+    res = []
+    for i, it in enumerate(items):
+        n = int(max(3, min(50, 1000.0 / max(probe[i][0], 1e-3))))
+        one = [it]
+        _, per = time_steps(one, n, stream)
+        ms = statistics.median(per[0])
+        r = roofline_for(it, ms, peaks, False)
+        res.append({"product": it["name"], "algorithm": it["plan"].algorithm,
+                    "ms_per_launch": ms, "launches": n, "achieved": r["achieved"],
+                    "unit": r["unit"], "frac": r["frac"], "bound": r["bound"],
+                    "peak": r["peak"]})
+    for it in items:
+        it["plan"].close()
+    return res
+
+
 def run_ours(args):
     import torch
     from gemm_matmulplan_broadcast_gb300 import load, synth
@@ -395,8 +452,9 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    host_t0 = time.perf_counter()
     total, per = time_steps(items, args.steps, stream)
+    host_enqueue_s = time.perf_counter() - host_t0
     clocks = sampler.stop()
     torch.cuda.synchronize()
     barrier()
@@ -431,19 +489,11 @@ def run_ours(args):
 
     secondary = {}
     if not args.no_secondary and args.workload == "bf16_transformer_projection":
-        for wname in ("fp16_skinny_splitk",):
-            w2 = synth.workload(wname)
-            its2, st2 = measure_workload(w2, 20, 3, device, peaks, l2)
-            _, per2 = time_steps(its2, 20, st2)
-            res = []
-            for i, it in enumerate(its2):
-                ms = statistics.median(per2[i])
-                r = roofline_for(it, ms, peaks, False)
-                res.append({"product": it["name"], "algorithm": it["plan"].algorithm,
-                            "ms_per_launch": ms, "achieved": r["achieved"], "unit": r["unit"],
-                            "frac": r["frac"], "bound": r["bound"]})
-            secondary[wname] = res
-            del its2
+        names = ["fp16_skinny_splitk", "float32_square_chain"]
+        if args.full_secondary:
+            names.append("float64_square_chain")
+        for wname in names:
+            secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -483,6 +533,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
+        "host_enqueue_s": host_enqueue_s,
         "gpu": props.name,
     }
     if rank == 0:
@@ -535,11 +586,13 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="bf16_transformer_projection")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--full-secondary", action="store_true",
+                    help="also time the FP64 square/chain workload (slow)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
