@@ -74,6 +74,17 @@ inline cudaError_t dispatch_dtype(olc_dtype dt, F&& f) {
     return cudaErrorInvalidValue;
 }
 
+template <typename F>
+inline int dispatch_int(olc_dtype dt, F&& f) {
+    switch (dt) {
+        case OLC_FLOAT: return f(float{});
+        case OLC_DOUBLE: return f(double{});
+        case OLC_FLOAT16: return f(__half{});
+        case OLC_BFLOAT16: return f(__nv_bfloat16{});
+    }
+    return 0;
+}
+
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }

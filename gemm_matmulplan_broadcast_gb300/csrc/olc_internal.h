@@ -73,15 +73,30 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count);
 int skinny_n_max_cols();
 cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
 
-// SPLIT_K: tiny output, long K.  Partials in fixed-order reduction.
-cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
-                           cudaStream_t stream);
-size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits);
-size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits);
+// SPLIT_K: tiny output, long K.  Partials in fixed-order reduction.  FLOAT16 /
+// BFLOAT16 shapes with 16-byte row strides run on the tensor cores, the rest
+// on the SIMT kernel.
+cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, int sm_count,
+                           const Workspace& ws, cudaStream_t stream);
+size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits, int sm_count);
+size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits, int sm_count);
 int split_k_pick(olc_dtype dt, const Problem& p, int sm_count);
+// the SIMT split-K kernel alone (32 x 32 tiles, one partial per slice)
+cudaError_t launch_split_k_simt(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
+                                cudaStream_t stream);
+int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count);
 
 // GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+// the same kernel with 16-column tiles (N <= 16): the tensor-core skinny-N
+cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+// the same kernel in split-K mode (K slices per tile, two-level fixed-order
+// reduction of float32 partial tiles)
+int tc_split_pick(const Problem& p, int sm_count);
+size_t tc_split_partial_bytes(const Problem& p, int sm_count);
+size_t tc_split_counter_count(const Problem& p, int sm_count);
+cudaError_t launch_tc_split(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
+                            cudaStream_t stream);
 
 }  // namespace olc

@@ -56,11 +56,14 @@ struct SkinnyMConfig {
 
 template <typename T, int MR>
 __global__ void __launch_bounds__(SkinnyMConfig<MR>::KW * 32)
-skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws) {
+skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws,
+                int a_vec_ok) {
     using acc_t = typename Num<T>::acc_t;
     constexpr int VEC = Vec16<T>::N;
     constexpr int KW = SkinnyMConfig<MR>::KW;
     constexpr int COLS = 32 * VEC;
+    constexpr int KU = 8;                    // k rows per step: 8 B vectors in flight per lane
+    constexpr int AV = (KU * (int)sizeof(T) + 15) / 16;   // 16-byte A vectors per row per step
     __shared__ acc_t red[KW][MR][COLS];
     __shared__ unsigned int am_last;
 
@@ -79,11 +82,12 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t col0 = cg * COLS + (int64_t)lane * VEC;
     const bool col_ok = col0 < N;   // N is a multiple of VEC
-    // this block's K range, then this warp's share of it
+    // this block's K range (kslice is a multiple of KU), then this warp's
+    // share of it, also a multiple of KU
     const int64_t kb0 = (int64_t)split * kslice;
     const int64_t kb1 = min64(K, kb0 + kslice);
-    const int64_t wlen = ceil_div(max64(kb1 - kb0, 0), KW);
-    const int64_t k0 = kb0 + warp * wlen;
+    const int64_t wlen = ceil_div(ceil_div(max64(kb1 - kb0, 0), KW), KU) * KU;
+    const int64_t k0 = min64(kb1, kb0 + warp * wlen);
     const int64_t k1 = min64(kb1, k0 + wlen);
 
     acc_t acc[MR][VEC];
@@ -94,13 +98,33 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
 
     if (col_ok) {
         const T* bp = B + col0;
-        constexpr int KU = 4;   // B vectors in flight per lane
         int64_t k = k0;
         for (; k + KU <= k1; k += KU) {
             uint4 bv[KU];
 #pragma unroll
             for (int u = 0; u < KU; ++u)
                 bv[u] = __ldg(reinterpret_cast<const uint4*>(bp + (k + u) * N));
+            acc_t a[MR][KU];
+#pragma unroll
+            for (int i = 0; i < MR; ++i) {
+                if (i < M) {
+                    if (a_vec_ok) {
+                        uint4 av[AV];
+#pragma unroll
+                        for (int q = 0; q < AV; ++q)
+                            av[q] = __ldg(reinterpret_cast<const uint4*>(A + i * K + k) + q);
+                        const T* ae = reinterpret_cast<const T*>(av);
+#pragma unroll
+                        for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ae[u]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(__ldg(A + i * K + k + u));
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < KU; ++u) a[i][u] = acc_t(0);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < KU; ++u) {
                 const T* be = reinterpret_cast<const T*>(&bv[u]);
@@ -108,11 +132,9 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) b[v] = Num<T>::to_acc(be[v]);
 #pragma unroll
-                for (int i = 0; i < MR; ++i) {
-                    const acc_t a = i < M ? Num<T>::to_acc(__ldg(A + i * K + k + u)) : acc_t(0);
+                for (int i = 0; i < MR; ++i)
 #pragma unroll
-                    for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a, b[v], acc[i][v]);
-                }
+                    for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a[i][u], b[v], acc[i][v]);
             }
         }
         for (; k < k1; ++k) {
@@ -200,15 +222,56 @@ static int64_t skinny_m_col_groups(olc_dtype dt, int64_t N) {
     return ceil_div(N, 32 * vec);
 }
 
+template <typename T, int MR>
+static int skinny_m_occupancy() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, skinny_m_kernel<T, MR>,
+                                                      SkinnyMConfig<MR>::KW * 32, 0) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    return n > 0 ? n : 4;   // no device visible: assume four resident blocks
+}
+
+static int skinny_m_blocks_per_sm(olc_dtype dt, int64_t M) {
+    const int mr = round_rows(M);
+    return dispatch_int(dt, [&](auto tag) {
+        using T = decltype(tag);
+        switch (mr) {
+            case 1: return skinny_m_occupancy<T, 1>();
+            case 2: return skinny_m_occupancy<T, 2>();
+            case 4: return skinny_m_occupancy<T, 4>();
+            case 8: return skinny_m_occupancy<T, 8>();
+            default: return skinny_m_occupancy<T, 16>();
+        }
+    });
+}
+
+// Number of K slices across blocks.  The grid is groups * splits blocks and
+// runs in waves of sm_count * (resident blocks per SM); a last wave that is
+// mostly empty costs as much as a full one, so pick the split with the best
+// wave fill, discounted by the extra partial-tile traffic it causes.
 int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
     const int64_t groups = skinny_m_col_groups(dt, p.N) * p.items;
-    // aim for about four blocks per SM; every split keeps at least 256 k
-    int64_t want = ceil_div(4LL * sm_count, groups);
-    const int64_t kmax = max64(1, p.K / 256);
-    if (want > kmax) want = kmax;
-    if (want > 64) want = 64;
-    if (want < 1) want = 1;
-    return (int)want;
+    const int64_t slots = (int64_t)sm_count * skinny_m_blocks_per_sm(dt, p.M);
+    const int64_t eb = dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2;
+    const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
+    const double stream_bytes = (double)p.K * p.N * eb * p.items;
+    const int64_t smax = min64(64, max64(1, p.K / 256));
+    int best = 1;
+    double best_score = -1.0;
+    for (int64_t s = 1; s <= smax; ++s) {
+        const int64_t blocks = groups * s;
+        const int64_t waves = ceil_div(blocks, slots);
+        const double fill = (double)blocks / (double)(waves * slots);
+        const double extra = s > 1 ? 2.0 * (double)s * round_rows(p.M) * p.N * acc * p.items : 0.0;
+        const double score = fill * stream_bytes / (stream_bytes + extra);
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = (int)s;
+        }
+    }
+    return best;
 }
 
 size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit) {
@@ -228,12 +291,17 @@ static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspa
                                      cudaStream_t s) {
     constexpr int VEC = Vec16<T>::N;
     const int64_t groups = ceil_div(p.N, 32 * VEC);
-    const int64_t kslice = ceil_div(p.K, ksplit);
+    const int64_t kslice = ceil_div(ceil_div(p.K, ksplit), 8) * 8;
     const int64_t blocks = groups * ksplit * p.items;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (ksplit > 1 && (!ws.partials || !ws.counters)) return cudaErrorInvalidValue;
+    // 16-byte A loads need every A row (and each operand item) 16-byte aligned
+    bool a_vec_ok = (p.K * (int64_t)sizeof(T)) % 16 == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.A) & 15) == 0;
+    for (int d = 0; d < p.map.rank; ++d)
+        if ((p.map.a_stride[d] * (int64_t)sizeof(T)) % 16 != 0) a_vec_ok = false;
     skinny_m_kernel<T, MR><<<(unsigned)blocks, SkinnyMConfig<MR>::KW * 32, 0, s>>>(
-        p, groups, ksplit, kslice, ws);
+        p, groups, ksplit, kslice, ws, a_vec_ok ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -357,7 +425,11 @@ static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
 }
 
 cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t s) {
-    (void)sm_count;
+    // FLOAT16 / BFLOAT16 with 16-byte row strides: stream A through the
+    // tensor cores with 16-column tiles (8 FMAs per A element would need most
+    // of the SIMT FMA rate at full HBM bandwidth)
+    if ((dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K))
+        return launch_skinny_n_tc(dt, p, sm_count, s);
     return dispatch_dtype(dt, [&](auto tag) {
         using T = decltype(tag);
         if (p.N <= 1) return launch_skinny_n_t<T, 1>(p, s);

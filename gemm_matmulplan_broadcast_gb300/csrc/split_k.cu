@@ -97,8 +97,17 @@ split_k_kernel(Problem p, int64_t tiles_m, int64_t tiles_n, int splits, int64_t 
     __threadfence();
     const acc_t* all = P + tile_id * splits * ENTRIES;
     for (int e = threadIdx.x; e < ENTRIES; e += 256) {
-        acc_t v = __ldcg(all + e);
-        for (int q = 1; q < splits; ++q) v += __ldcg(all + (int64_t)q * ENTRIES + e);
+        // slice order 0, 1, ..., loads issued eight at a time
+        acc_t v = acc_t(0);
+        for (int q0 = 0; q0 < splits; q0 += 8) {
+            acc_t t[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (q0 + j < splits) t[j] = __ldcg(all + (int64_t)(q0 + j) * ENTRIES + e);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (q0 + j < splits) v += t[j];
+        }
         const int64_t gm = m0 + e / TN, gn = n0 + e % TN;
         if (gm < M && gn < N) Y[gm * N + gn] = Num<T>::from_acc(v);
     }
@@ -107,7 +116,7 @@ split_k_kernel(Problem p, int64_t tiles_m, int64_t tiles_n, int splits, int64_t 
 
 static int64_t acc_bytes(olc_dtype dt) { return dt == OLC_DOUBLE ? 8 : 4; }
 
-int split_k_pick(olc_dtype dt, const Problem& p, int sm_count) {
+int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count) {
     (void)dt;
     const int64_t tiles = ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items;
     // about two blocks per SM, each slice at least 256 long
@@ -118,19 +127,17 @@ int split_k_pick(olc_dtype dt, const Problem& p, int sm_count) {
     return (int)max64(s, 1);
 }
 
-size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits) {
+static size_t simt_partial_bytes(olc_dtype dt, const Problem& p, int splits) {
     const int64_t tiles = ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items;
     return (size_t)(tiles * splits * 32 * 32 * acc_bytes(dt));
 }
 
-size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits) {
-    (void)dt;
-    (void)splits;
+static size_t simt_counter_count(const Problem& p) {
     return (size_t)(ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items);
 }
 
-cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
-                           cudaStream_t s) {
+cudaError_t launch_split_k_simt(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
+                                cudaStream_t s) {
     if (!ws.partials || !ws.counters) return cudaErrorInvalidValue;
     const int64_t tm = ceil_div(p.M, 32), tn = ceil_div(p.N, 32);
     const int64_t kslice = ceil_div(ceil_div(p.K, splits), 32) * 32;
@@ -141,6 +148,32 @@ cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, const Wor
         split_k_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn, splits, kslice, ws);
         return cudaGetLastError();
     });
+}
+
+// FLOAT16 / BFLOAT16 with 16-byte row strides: the tensor-core kernel's
+// split-K mode; everything else: the SIMT kernel above.
+static bool split_on_tc(olc_dtype dt, const Problem& p) {
+    return (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K);
+}
+
+int split_k_pick(olc_dtype dt, const Problem& p, int sm_count) {
+    return split_on_tc(dt, p) ? tc_split_pick(p, sm_count) : split_k_simt_pick(dt, p, sm_count);
+}
+
+size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits, int sm_count) {
+    return split_on_tc(dt, p) ? tc_split_partial_bytes(p, sm_count)
+                              : simt_partial_bytes(dt, p, splits);
+}
+
+size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits, int sm_count) {
+    (void)splits;
+    return split_on_tc(dt, p) ? tc_split_counter_count(p, sm_count) : simt_counter_count(p);
+}
+
+cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, int sm_count,
+                           const Workspace& ws, cudaStream_t s) {
+    if (split_on_tc(dt, p)) return launch_tc_split(dt, p, sm_count, ws, s);
+    return launch_split_k_simt(dt, p, splits, ws, s);
 }
 
 }  // namespace olc
@@ -222,7 +255,7 @@ extern "C" olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, 
         cudaGetLastError();
         return OLC_ERR_CUDA;
     }
-    int splits = split_k_pick(dtype, p, sms);
+    int splits = split_k_simt_pick(dtype, p, sms);
     const int64_t fit = (int64_t)kStaticPartialBytes / (tiles * tile_bytes);
     if (splits > fit) splits = (int)fit;
     if (splits < 1) splits = 1;
@@ -243,7 +276,7 @@ extern "C" olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, 
         cudaGetLastError();
         return OLC_ERR_CUDA;
     }
-    if (launch_split_k(dtype, p, splits, ws, s) != cudaSuccess) {
+    if (launch_split_k_simt(dtype, p, splits, ws, s) != cudaSuccess) {
         cudaGetLastError();
         return OLC_ERR_CUDA;
     }

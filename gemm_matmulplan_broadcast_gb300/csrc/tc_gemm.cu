@@ -49,42 +49,70 @@ namespace olc {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;               // one 128-byte swizzle span of 16-bit elements
-constexpr int STAGES = 4;
+constexpr int BK = 64;               // one 128-byte swizzle span of 16-bit A elements
 constexpr int UMMA_K = 16;
 constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;       // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int ACC_COLS = BN;                     // float32 columns per accumulator
-constexpr int TMEM_COLS = 2 * ACC_COLS;          // 512: double buffer
+constexpr int STAGE_BUDGET = 192 * 1024;         // shared memory for the stage ring
+constexpr int MAX_STAGES = 12;
 constexpr int THREADS = 192;
+constexpr int EPI_THREADS = 128;                 // warps 2..5
 constexpr int GROUP_M = 16;                      // tile raster: 16 M-blocks per group
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
 
+// Per tile width BN: how B (MN-major, N contiguous) is staged.  A 64-deep
+// stage of B is cut into boxes BLK_COLS columns wide whose rows are one
+// swizzle span: 128-byte swizzle with 64-column boxes for BN >= 64, 64-byte
+// swizzle for BN = 32, 32-byte swizzle for BN = 16.
+template <int BN>
+struct Cfg {
+    static constexpr int SW = BN >= 64 ? 128 : BN * 2;        // swizzle span in bytes
+    static constexpr int BLK_COLS = SW / 2;
+    static constexpr int NBLK = BN / BLK_COLS;
+    static constexpr int B_BLK_BYTES = BK * SW;               // one box: BK rows of SW bytes
+    static constexpr int B_STAGE_BYTES = NBLK * B_BLK_BYTES;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int STAGES =
+        STAGE_BUDGET / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : STAGE_BUDGET / STAGE_BYTES;
+    static constexpr uint32_t LAYOUT = SW == 128 ? 2u : (SW == 64 ? 4u : 6u);   // descriptor code
+    static constexpr int ACC_COLS = BN;
+    static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 512;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+    static_assert(BN % BLK_COLS == 0, "tile width must be whole boxes");
+};
+
 struct Smem {
     // stage buffers come first (1024-byte aligned), barriers after
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int last_flag;
 };
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256;
 
 struct Params {
     int64_t M, N, K;          // per batch item
     int64_t items;
     int64_t tiles_m, tiles_n, tiles_per_item, total_tiles;
-    int64_t k_blocks;
+    int64_t k_blocks;         // BK-deep blocks of the whole K
     int64_t a_item_elems;     // M * K: A matrix size (for the TMA batch coordinate)
     int64_t b_item_elems;     // K * N
     BatchMap map;
     void* Y;
     unsigned int* err;
     int is_bf16;
+    // split-K (splits == 1 and null pointers otherwise)
+    int splits;               // K slices per tile
+    int group;                // slices per first-level reduction group
+    int groups;               // ceil(splits / group)
+    int64_t kb_per_split;     // k-blocks per slice
+    float* part1;             // [tiles][splits][BM][BN] float32 partial tiles
+    float* part2;             // [tiles][groups][BM][BN] group sums
+    unsigned int* cnt1;       // [tiles][groups] arrivals per group
+    unsigned int* cnt2;       // [tiles] arrivals of group sums
 };
 
 // ---------------------------------------------------------------------------
@@ -212,6 +240,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// the four epilogue warps only (named barrier 1)
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // descriptors (host and device agree on these encodings; the host unit test
 // checks them bit by bit)
@@ -219,10 +263,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 // Shared-memory matrix descriptor for tcgen05: start address >> 4 in bits
 // 0-13, leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45,
 // the fixed value 1 in bits 46-47, base offset 0 in 49-51, relative LBO mode
-// (bit 52 = 0), swizzle mode in 61-63 (2 = 128-byte swizzle).
-__host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// (bit 52 = 0), swizzle mode in 61-63 (2 = 128-byte, 4 = 64-byte, 6 = 32-byte).
+__host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                                 uint32_t layout) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+           ((uint64_t)(layout & 7u) << 61);
 }
 
 // Instruction descriptor for kind::f16: float32 accumulator (bits 4-5 = 1),
@@ -250,16 +296,63 @@ __device__ __forceinline__ void tile_coords(const Params& p, int64_t t, int64_t&
     nb = in / gm;
 }
 
+// A work unit is one K slice of one output tile (one slice per tile unless
+// split-K): unit u -> tile u / splits, slice u % splits.
+__device__ __forceinline__ void unit_range(const Params& p, int64_t u, int64_t& tile,
+                                           int& slice, int64_t& kb0, int64_t& kb1) {
+    tile = u / p.splits;
+    slice = (int)(u % p.splits);
+    kb0 = (int64_t)slice * p.kb_per_split;
+    kb1 = min64(p.k_blocks, kb0 + p.kb_per_split);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
+    if (is_bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Sum `count` float32 partial tiles (stride `stride` floats apart) in order
+// 0, 1, ... for the float4 at index e4; loads are issued eight at a time.
+__device__ __forceinline__ float4 ordered_sum4(const float* base, int64_t stride, int count,
+                                               int64_t e4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < count; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < count)
+                v[j] = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(s0 + j) * stride) + e4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < count) {
+                acc.x += v[j].x;
+                acc.y += v[j].y;
+                acc.z += v[j].z;
+                acc.w += v[j].w;
+            }
+    }
+    return acc;
+}
+
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    using C = Cfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int CH = BN < 32 ? BN : 32;             // accumulator columns per tcgen05.ld
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte aligned stage buffers (the 128-byte swizzle pattern repeats
-    // every 1024 bytes and the descriptors assume an aligned base)
+    // 1024-byte aligned stage buffers (every swizzle pattern repeats within
+    // 1024 bytes and the descriptors assume an aligned base)
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem* s = reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+    Smem* s = reinterpret_cast<Smem*>(base + STAGES * C::STAGE_BYTES);
     volatile int* abort_flag = &s->abort_flag;
+    const int64_t total_units = p.total_tiles * p.splits;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -275,10 +368,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
         mbar_init(&s->drain, 1);
         s->abort_flag = 0;
+        s->last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(&s->tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_alloc(&s->tmem_base, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -292,27 +386,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             bool armed[STAGES];
             for (int i = 0; i < STAGES; ++i) armed[i] = false;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            for (int64_t u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                int64_t tile, kb0, kb1;
+                int slice;
+                unit_range(p, u, tile, slice, kb0, kb1);
                 int64_t item, mb, nb;
-                tile_coords(p, t, item, mb, nb);
+                tile_coords(p, tile, item, mb, nb);
                 int64_t a_off, b_off;
                 batch_offsets(p.map, item, a_off, b_off);
                 const int a_item = (int)(a_off / p.a_item_elems);
                 const int b_item = (int)(b_off / p.b_item_elems);
                 const int m0 = (int)(mb * BM), n0 = (int)(nb * BN);
-                for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
+                for (int64_t kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    unsigned char* sa = base + stage * STAGE_BYTES;
+                    unsigned char* sa = base + stage * C::STAGE_BYTES;
                     unsigned char* sb = sa + A_STAGE_BYTES;
-                    mbar_arrive_expect_tx(&s->full[stage], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&s->full[stage], C::STAGE_BYTES);
                     armed[stage] = true;
                     armed_parity[stage] = phase;
                     const int k0 = (int)(kb * BK);
                     tma_load_3d(sa, &tmap_a, &s->full[stage], k0, m0, a_item);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_3d(sb + j * (64 * BK * 2), &tmap_b, &s->full[stage], n0 + 64 * j,
-                                    k0, b_item);
+                    for (int j = 0; j < C::NBLK; ++j)
+                        tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, &s->full[stage],
+                                    n0 + C::BLK_COLS * j, k0, b_item);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -328,23 +425,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const uint32_t idesc = instr_desc(p.is_bf16, BM, BN, 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            for (int64_t u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                int64_t tile, kb0, kb1;
+                int slice;
+                unit_range(p, u, tile, slice, kb0, kb1);
                 if (!mbar_wait(&s->acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
+                const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+                for (int64_t kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(base + stage * STAGE_BYTES);
+                    const uint32_t a_addr = smem_u32(base + stage * C::STAGE_BYTES);
                     const uint32_t b_addr = a_addr + A_STAGE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // A: K-major, advance 16 elements = 32 bytes inside the swizzle row
-                        const uint64_t ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024);
-                        // B: MN-major, advance 16 K-rows = 2048 bytes; 64-column
-                        // blocks 8192 bytes apart (LBO), 8-row groups 1024 (SBO)
-                        const uint64_t bd = smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024);
-                        mma_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        // A: K-major, 128-byte swizzle; advance 16 elements = 32
+                        // bytes inside the swizzle row; 8-row groups 1024 apart
+                        const uint64_t ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
+                        // B: MN-major; advance 16 K-rows of SW bytes; boxes of
+                        // BLK_COLS columns B_BLK_BYTES apart (LBO), 8-row groups
+                        // 8 * SW apart (SBO)
+                        const uint64_t bd = smem_desc(b_addr + kk * UMMA_K * C::SW,
+                                                      C::B_BLK_BYTES, 8 * C::SW, C::LAYOUT);
+                        mma_f16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&s->empty[stage]);   // stage free once these MMAs finish
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -361,54 +464,138 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // ------------------------------------------------------------ epilogue
         const int lane_group = warp & 3;          // TMEM lanes this warp may access
         const int row_in_tile = lane_group * 32 + lane;
+        const int etid = threadIdx.x - 64;        // 0..127 across the epilogue warps
         uint32_t acc = 0, acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+            int64_t tile, kb0, kb1;
+            int slice;
+            unit_range(p, u, tile, slice, kb0, kb1);
             int64_t item, mb, nb;
-            tile_coords(p, t, item, mb, nb);
+            tile_coords(p, tile, item, mb, nb);
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
             tc_fence_after();
             const int64_t row = mb * BM + row_in_tile;
             const bool row_ok = row < p.M;
-            const uint32_t t_base = tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * ACC_COLS;
-            unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
-                                  ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
+            const uint32_t t_base =
+                tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * C::ACC_COLS;
+            if (!SPLIT) {
+                unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
+                                      ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_base + c, r);
-                const int64_t col = nb * BN + c;
-                if (row_ok && col < p.N) {
-                    uint32_t packed[16];
+                for (int c = 0; c < BN; c += CH) {
+                    uint32_t r[32];
+                    if (CH == 32) tmem_ld_32x32b_x32(t_base + c, r);
+                    else tmem_ld_32x32b_x16(t_base + c, r);
+                    const int64_t col = nb * BN + c;
+                    if (row_ok && col < p.N) {
+                        uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float lo = __uint_as_float(r[2 * i]);
-                        const float hi = __uint_as_float(r[2 * i + 1]);
-                        if (p.is_bf16) {
-                            __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-                            packed[i] = *reinterpret_cast<uint32_t*>(&v);
-                        } else {
-                            __half2 v = __floats2half2_rn(lo, hi);
-                            packed[i] = *reinterpret_cast<uint32_t*>(&v);
-                        }
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
-                    if (col + 32 <= p.N) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                                                packed[4 * q + 3]);
-                    } else {
+                        for (int i = 0; i < CH / 2; ++i)
+                            packed[i] = pack2(__uint_as_float(r[2 * i]),
+                                              __uint_as_float(r[2 * i + 1]), p.is_bf16);
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                         // N is a multiple of 8: whole 16-byte groups only
-                        const int groups = (int)((p.N - col) / 8);
-                        for (int q = 0; q < groups; ++q)
-                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                                                packed[4 * q + 3]);
+                        const int64_t left = (p.N - col) / 8;
+                        const int groups = (int)(left < CH / 8 ? left : CH / 8);
+#pragma unroll
+                        for (int q = 0; q < CH / 8; ++q)
+                            if (q < groups)
+                                dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                    packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
+            } else {
+                // float32 partial tile of this slice -> part1[tile][slice]
+                float* mine = p.part1 + ((tile * p.splits + slice) * BM) * (int64_t)BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += CH) {
+                    uint32_t r[32];
+                    if (CH == 32) tmem_ld_32x32b_x32(t_base + c, r);
+                    else tmem_ld_32x32b_x16(t_base + c, r);
+                    if (row_ok) {
+                        float4* dst = reinterpret_cast<float4*>(mine + (int64_t)row_in_tile * BN + c);
+#pragma unroll
+                        for (int q = 0; q < CH / 4; ++q)
+                            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                 __uint_as_float(r[4 * q + 2]),
+                                                 __uint_as_float(r[4 * q + 3]));
+                    }
+                }
+                // the accumulator can be refilled while the reduction runs
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
+
+                // fixed two-level reduction tree: slices of one group summed
+                // in slice order by the group's last arrival, then the group
+                // sums in group order by the last group
+                const int g = slice / p.group;
+                const int gsize = min(p.group, p.splits - g * p.group);
+                const int64_t rows_valid = min64(BM, p.M - mb * BM);
+                const int64_t e4_count = rows_valid * BN / 4;
+                const int64_t tile_floats = (int64_t)BM * BN;
+                __threadfence();
+                epi_sync();
+                if (etid == 0) {
+                    const unsigned int prev = atomicAdd(p.cnt1 + tile * p.groups + g, 1u);
+                    s->last_flag = (prev == (unsigned int)gsize - 1) ? 1 : 0;
+                }
+                epi_sync();
+                const int last1 = s->last_flag;
+                epi_sync();
+                if (last1) {
+                    __threadfence();
+                    const float* first = p.part1 + (tile * p.splits + g * p.group) * tile_floats;
+                    if (p.groups == 1) {
+                        for (int64_t e4 = etid; e4 < e4_count; e4 += EPI_THREADS) {
+                            const float4 v = ordered_sum4(first, tile_floats, gsize, e4);
+                            const int64_t r = (e4 * 4) / BN, cc = (e4 * 4) % BN;
+                            const int64_t col = nb * BN + cc;
+                            if (col < p.N) {
+                                uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
+                                *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) +
+                                                          ((item * p.M + mb * BM + r) * p.N + col) * 2) = o;
+                            }
+                        }
+                        if (etid == 0) p.cnt1[tile * p.groups + g] = 0u;
+                    } else {
+                        float* gsum = p.part2 + (tile * p.groups + g) * tile_floats;
+                        for (int64_t e4 = etid; e4 < e4_count; e4 += EPI_THREADS)
+                            reinterpret_cast<float4*>(gsum)[e4] =
+                                ordered_sum4(first, tile_floats, gsize, e4);
+                        __threadfence();
+                        epi_sync();
+                        if (etid == 0) {
+                            p.cnt1[tile * p.groups + g] = 0u;
+                            const unsigned int prev = atomicAdd(p.cnt2 + tile, 1u);
+                            s->last_flag = (prev == (unsigned int)p.groups - 1) ? 1 : 0;
+                        }
+                        epi_sync();
+                        const int last2 = s->last_flag;
+                        epi_sync();
+                        if (last2) {
+                            __threadfence();
+                            const float* g0 = p.part2 + tile * p.groups * tile_floats;
+                            for (int64_t e4 = etid; e4 < e4_count; e4 += EPI_THREADS) {
+                                const float4 v = ordered_sum4(g0, tile_floats, p.groups, e4);
+                                const int64_t r = (e4 * 4) / BN, cc = (e4 * 4) % BN;
+                                const int64_t col = nb * BN + cc;
+                                if (col < p.N) {
+                                    uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16),
+                                                         pack2(v.z, v.w, p.is_bf16));
+                                    *reinterpret_cast<uint2*>(
+                                        static_cast<unsigned char*>(p.Y) +
+                                        ((item * p.M + mb * BM + r) * p.N + col) * 2) = o;
+                                }
+                            }
+                            if (etid == 0) p.cnt2[tile] = 0u;
+                        }
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
@@ -416,7 +603,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -438,9 +625,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // rank-3 map over [items][rows][cols] (cols innermost), 16-bit elements,
-// 128-byte swizzle, box {box_cols, box_rows, 1}
+// box {box_cols, box_rows, 1} with the given swizzle
 static bool encode_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t cols,
-                      uint64_t rows, uint64_t items, uint32_t box_cols, uint32_t box_rows) {
+                      uint64_t rows, uint64_t items, uint32_t box_cols, uint32_t box_rows,
+                      CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {cols, rows, items};
@@ -449,35 +637,71 @@ static bool encode_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t 
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-}  // namespace tc
-
-bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K) {
-    if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;
-    // TMA needs 16-byte row strides; coordinates fit in int32
-    return N % 8 == 0 && K % 8 == 0 && N < (1LL << 31) && K < (1LL << 31);
+template <int BN>
+static CUtensorMapSwizzle b_swizzle() {
+    return Cfg<BN>::SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : (Cfg<BN>::SW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
-    using namespace tc;
+// Shape of a split-K launch: slices, group size, workspace layout.
+struct SplitPlan {
+    int splits = 1, group = 1, groups = 1;
+    int64_t kb_per_split = 0;
+    int64_t tiles = 0;
+    size_t part1_bytes = 0, part2_bytes = 0, counters = 0;
+};
+
+template <int BN>
+static SplitPlan split_plan(const Problem& pr, int sm_count) {
+    SplitPlan sp;
+    const int64_t tiles = ceil_div(pr.M, BM) * ceil_div(pr.N, BN) * pr.items;
+    const int64_t kbs = ceil_div(pr.K, BK);
+    // about one unit per SM, at least 2 K blocks per slice
+    int64_t want = max64(1, sm_count / max64(tiles, 1));
+    want = min64(want, max64(1, kbs / 2));
+    const int64_t per = ceil_div(kbs, want);
+    sp.kb_per_split = per;
+    sp.splits = (int)ceil_div(kbs, per);      // every slice non-empty
+    int g = 1;
+    while ((int64_t)g * g < sp.splits) ++g;   // ~sqrt(splits) slices per group
+    sp.group = g;
+    sp.groups = (int)ceil_div(sp.splits, g);
+    sp.tiles = tiles;
+    const int64_t tile_bytes = (int64_t)BM * BN * 4;
+    sp.part1_bytes = (size_t)(tiles * sp.splits * tile_bytes);
+    sp.part2_bytes = sp.groups > 1 ? (size_t)(tiles * sp.groups * tile_bytes) : 0;
+    sp.counters = (size_t)(tiles * sp.groups + tiles);
+    return sp;
+}
+
+template <int BN, bool SPLIT>
+static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
+                             const SplitPlan* sp, const Workspace* ws) {
+    using C = Cfg<BN>;
     if (!tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31)) return cudaErrorInvalidValue;
     // the operands' batch extents: every item offset is a multiple of the
     // matrix size (dense operands), so offset / size is the TMA batch index
     int64_t a_items = 1, b_items = 1;
     for (int d = 0; d < pr.map.rank; ++d) {
-        if (pr.map.a_stride[d]) a_items = max64(a_items, pr.map.a_stride[d] / (pr.M * pr.K) * pr.map.dims[d]);
-        if (pr.map.b_stride[d]) b_items = max64(b_items, pr.map.b_stride[d] / (pr.K * pr.N) * pr.map.dims[d]);
+        if (pr.map.a_stride[d])
+            a_items = max64(a_items, pr.map.a_stride[d] / (pr.M * pr.K) * pr.map.dims[d]);
+        if (pr.map.b_stride[d])
+            b_items = max64(b_items, pr.map.b_stride[d] / (pr.K * pr.N) * pr.map.dims[d]);
     }
     CUtensorMap ma, mb;
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
     const int bf = dt == OLC_BFLOAT16;
-    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, BM)) return cudaErrorInvalidValue;
-    if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK)) return cudaErrorInvalidValue;
+    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>()))
+        return cudaErrorInvalidValue;
 
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -496,24 +720,94 @@ cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cud
     p.Y = pr.Y;
     p.err = device_error_word();
     p.is_bf16 = bf;
+    p.splits = 1;
+    p.group = 1;
+    p.groups = 1;
+    p.kb_per_split = p.k_blocks;
+    if (SPLIT) {
+        if (!sp || !ws || !ws->partials || !ws->counters) return cudaErrorInvalidValue;
+        p.splits = sp->splits;
+        p.group = sp->group;
+        p.groups = sp->groups;
+        p.kb_per_split = sp->kb_per_split;
+        p.part1 = static_cast<float*>(ws->partials);
+        p.part2 = sp->groups > 1
+                      ? reinterpret_cast<float*>(static_cast<char*>(ws->partials) + sp->part1_bytes)
+                      : nullptr;
+        p.cnt1 = ws->counters;
+        p.cnt2 = ws->counters + sp->tiles * sp->groups;
+    }
     if (p.total_tiles <= 0) return cudaSuccess;
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, SPLIT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const int64_t grid = min64(p.total_tiles, (int64_t)sm_count);
-    tc_gemm_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+    const int64_t units = p.total_tiles * p.splits;
+    const int64_t grid = min64(units, (int64_t)sm_count);
+    tc_gemm_kernel<BN, SPLIT><<<(unsigned)grid, THREADS, C::SMEM_BYTES, s>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+}  // namespace tc
+
+bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K) {
+    if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;
+    // TMA needs 16-byte row strides; coordinates fit in int32
+    return N % 8 == 0 && K % 8 == 0 && N < (1LL << 31) && K < (1LL << 31);
+}
+
+cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
+    return tc::launch_tc<256, false>(dt, pr, sm_count, s, nullptr, nullptr);
+}
+
+cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
+    if (pr.N > 16) return cudaErrorInvalidValue;
+    return tc::launch_tc<16, false>(dt, pr, sm_count, s, nullptr, nullptr);
+}
+
+// split-K on the tensor cores: tile width by N
+static int tc_split_bn(int64_t N) { return N <= 16 ? 16 : (N <= 32 ? 32 : 256); }
+
+static tc::SplitPlan tc_split_plan(const Problem& pr, int sm_count) {
+    switch (tc_split_bn(pr.N)) {
+        case 16: return tc::split_plan<16>(pr, sm_count);
+        case 32: return tc::split_plan<32>(pr, sm_count);
+        default: return tc::split_plan<256>(pr, sm_count);
+    }
+}
+
+int tc_split_pick(const Problem& pr, int sm_count) { return tc_split_plan(pr, sm_count).splits; }
+
+size_t tc_split_partial_bytes(const Problem& pr, int sm_count) {
+    const tc::SplitPlan sp = tc_split_plan(pr, sm_count);
+    return sp.part1_bytes + sp.part2_bytes;
+}
+
+size_t tc_split_counter_count(const Problem& pr, int sm_count) {
+    return tc_split_plan(pr, sm_count).counters;
+}
+
+cudaError_t launch_tc_split(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
+                            cudaStream_t s) {
+    const tc::SplitPlan sp = tc_split_plan(pr, sm_count);
+    if (ws.partial_bytes < sp.part1_bytes + sp.part2_bytes || ws.counter_count < sp.counters)
+        return cudaErrorInvalidValue;
+    switch (tc_split_bn(pr.N)) {
+        case 16: return tc::launch_tc<16, true>(dt, pr, sm_count, s, &sp, &ws);
+        case 32: return tc::launch_tc<32, true>(dt, pr, sm_count, s, &sp, &ws);
+        default: return tc::launch_tc<256, true>(dt, pr, sm_count, s, &sp, &ws);
+    }
 }
 
 }  // namespace olc
 
-extern "C" uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return olc::tc::smem_desc(addr, lbo, sbo);
+extern "C" uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                           uint32_t layout) {
+    return olc::tc::smem_desc(addr, lbo, sbo, layout);
 }
 extern "C" uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int b_mn_major) {
     return olc::tc::instr_desc(is_bf16, m, n, b_mn_major);

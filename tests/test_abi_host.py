@@ -197,11 +197,11 @@ def test_tcgen05_descriptor_bit_layout():
     against the PTX ISA tables (tcgen05 shared memory descriptor; instruction
     descriptor for kind::f16)."""
     lib = binding.load()
-    lib.olc_debug_tc_smem_desc.argtypes = [ctypes.c_uint32] * 3
+    lib.olc_debug_tc_smem_desc.argtypes = [ctypes.c_uint32] * 4
     lib.olc_debug_tc_smem_desc.restype = ctypes.c_uint64
     lib.olc_debug_tc_instr_desc.argtypes = [ctypes.c_int] * 4
     lib.olc_debug_tc_instr_desc.restype = ctypes.c_uint32
-    d = lib.olc_debug_tc_smem_desc(0x1A400, 8192, 1024)
+    d = lib.olc_debug_tc_smem_desc(0x1A400, 8192, 1024, 2)
     assert _field(d, 0, 13) == 0x1A400 >> 4      # start address >> 4
     assert _field(d, 14, 15) == 0
     assert _field(d, 16, 29) == 8192 >> 4        # leading byte offset >> 4
@@ -211,7 +211,10 @@ def test_tcgen05_descriptor_bit_layout():
     assert _field(d, 52, 52) == 0                # relative LBO mode
     assert _field(d, 61, 63) == 2                # 128-byte swizzle
     # the address field keeps 18 bits of byte address (256 KiB window)
-    assert _field(lib.olc_debug_tc_smem_desc(0x3FFF0, 16, 1024), 0, 13) == 0x3FFF
+    assert _field(lib.olc_debug_tc_smem_desc(0x3FFF0, 16, 1024, 2), 0, 13) == 0x3FFF
+    for layout in (4, 6):   # 64-byte and 32-byte swizzle codes
+        d = lib.olc_debug_tc_smem_desc(0x2000, 4096, 512, layout)
+        assert _field(d, 61, 63) == layout and _field(d, 32, 45) == 512 >> 4
     for bf16 in (0, 1):
         i = lib.olc_debug_tc_instr_desc(bf16, 128, 256, 1)
         assert _field(i, 0, 3) == 0                  # dense, no saturate

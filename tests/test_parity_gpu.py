@@ -214,6 +214,45 @@ def test_tc_many_tiles_per_cta_sampled(dtype):
     compare(y[rows], y_ref, s, dtype)
 
 
+TC_SPLIT_SHAPES = [
+    ((32, 4096), (4096, 32)),          # 32-column tiles
+    ((40, 20000), (20000, 24)),        # 32-column tiles, N tail
+    ((16, 9000), (9000, 16)),          # 16-column tiles
+    ((8, 3000), (3000, 8)),
+    ((300, 5000), (5000, 264)),        # 256-column tiles, several tiles
+    ((2, 24, 2048), (2048, 40)),       # folded batch
+    ((3, 24, 1024), (3, 1024, 32)),    # batched B
+]
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("shapes", TC_SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_tc_split_k(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=12)
+    check_product(a, b, dtype, algorithm="split_k")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=12)
+    check_product(ai, bi, dtype, algorithm="split_k", exact=True)
+
+
+TC_SKINNY_N_SHAPES = [
+    ((256, 1024), (1024, 8)),
+    ((1000, 520), (520, 16)),
+    ((3, 200, 64), (64, 8)),
+    ((2, 130, 72), (2, 72, 16)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("shapes", TC_SKINNY_N_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_tc_skinny_n(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=13)
+    check_product(a, b, dtype, algorithm="skinny_n")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=13)
+    check_product(ai, bi, dtype, algorithm="skinny_n", exact=True)
+
+
 # --------------------------------------------------------------------------
 # edge cases
 
