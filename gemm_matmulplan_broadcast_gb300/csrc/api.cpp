@@ -200,8 +200,8 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
     } else if (p->algo == OLC_ALGO_SKINNY_M) {
         p->splits = skinny_m_pick_split(dt, pr, p->sm_count);
         if (p->splits > 1) {
-            p->partial_bytes = skinny_m_partial_bytes(dt, pr, p->splits);
-            p->counter_count = skinny_m_counter_count(dt, pr, p->splits);
+            p->partial_bytes = skinny_m_partial_bytes(dt, pr, p->splits, p->sm_count);
+            p->counter_count = skinny_m_counter_count(dt, pr, p->splits, p->sm_count);
         }
     }
     if (p->partial_bytes == 0) return OLC_OK;
@@ -270,7 +270,9 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     switch (algo) {
         case OLC_ALGO_DIRECT: e = launch_direct(dt, pr, s); break;
         case OLC_ALGO_GENERAL_SIMT: e = launch_general_simt(dt, pr, s); break;
-        case OLC_ALGO_SKINNY_M: e = launch_skinny_m(dt, pr, p->splits, workspace_of(p), s); break;
+        case OLC_ALGO_SKINNY_M:
+            e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
+            break;
         case OLC_ALGO_SKINNY_N: e = launch_skinny_n(dt, pr, p->sm_count, s); break;
         case OLC_ALGO_SPLIT_K:
             e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);

@@ -63,10 +63,10 @@ bool general_simt_vectorizable(olc_dtype dt, int64_t N, int64_t K);
 
 // SKINNY_M: M <= 16.  `ksplit` slices of K, reduced in fixed order.
 int skinny_m_max_rows();
-cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, const Workspace& ws,
-                            cudaStream_t stream);
-size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit);
-size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit);
+cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_count,
+                            const Workspace& ws, cudaStream_t stream);
+size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count);
+size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit, int sm_count);
 int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count);
 
 // SKINNY_N: N <= 16.
@@ -98,5 +98,12 @@ size_t tc_split_partial_bytes(const Problem& p, int sm_count);
 size_t tc_split_counter_count(const Problem& p, int sm_count);
 cudaError_t launch_tc_split(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
                             cudaStream_t stream);
+// the same kernel with swapped operands for M <= 16 (Y^T = B^T A^T): the
+// tensor-core skinny-M, split over K when that fills the SMs better
+int tc_skinny_m_pick(const Problem& p, int sm_count);
+size_t tc_skinny_m_partial_bytes(const Problem& p, int sm_count);
+size_t tc_skinny_m_counter_count(const Problem& p, int sm_count);
+cudaError_t launch_tc_skinny_m(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
+                               cudaStream_t stream);
 
 }  // namespace olc

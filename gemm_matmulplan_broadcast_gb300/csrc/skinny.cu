@@ -251,7 +251,20 @@ static int skinny_m_blocks_per_sm(olc_dtype dt, int64_t M) {
 // runs in waves of sm_count * (resident blocks per SM); a last wave that is
 // mostly empty costs as much as a full one, so pick the split with the best
 // wave fill, discounted by the extra partial-tile traffic it causes.
+// FLOAT16 / BFLOAT16 with 16-byte row strides: the tensor-core kernel with
+// swapped operands streams B through its TMA ring; the rest: the SIMT kernel.
+static bool skinny_m_on_tc(olc_dtype dt, const Problem& p) {
+    return (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K) && p.M <= 16;
+}
+
+static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count);
+
 int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
+    return skinny_m_on_tc(dt, p) ? tc_skinny_m_pick(p, sm_count)
+                                 : skinny_m_simt_split(dt, p, sm_count);
+}
+
+static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
     const int64_t groups = skinny_m_col_groups(dt, p.N) * p.items;
     const int64_t slots = (int64_t)sm_count * skinny_m_blocks_per_sm(dt, p.M);
     const int64_t eb = dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2;
@@ -274,15 +287,17 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
     return best;
 }
 
-size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit) {
+size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
+    if (skinny_m_on_tc(dt, p)) return tc_skinny_m_partial_bytes(p, sm_count);
     const int64_t vec = 16 / (dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
     const int64_t entries = round_rows(p.M) * 32 * vec;
     return (size_t)(skinny_m_col_groups(dt, p.N) * p.items * ksplit * entries * acc);
 }
 
-size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit) {
+size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
     (void)ksplit;
+    if (skinny_m_on_tc(dt, p)) return tc_skinny_m_counter_count(p, sm_count);
     return (size_t)(skinny_m_col_groups(dt, p.N) * p.items);
 }
 
@@ -305,8 +320,9 @@ static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspa
     return cudaGetLastError();
 }
 
-cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, const Workspace& ws,
-                            cudaStream_t s) {
+cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_count,
+                            const Workspace& ws, cudaStream_t s) {
+    if (skinny_m_on_tc(dt, p)) return launch_tc_skinny_m(dt, p, sm_count, ws, s);
     const int mr = round_rows(p.M);
     return dispatch_dtype(dt, [&](auto tag) {
         using T = decltype(tag);

@@ -58,6 +58,7 @@ constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;                 // warps 2..5
 constexpr int GROUP_M = 16;                      // tile raster: 16 M-blocks per group
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+constexpr int SUM_BATCH = 12;                    // partials loaded per reduction round trip
 
 // Per tile width BN: how B (MN-major, N contiguous) is staged.  A 64-deep
 // stage of B is cut into boxes BLK_COLS columns wide whose rows are one
@@ -272,11 +273,14 @@ __host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, ui
 }
 
 // Instruction descriptor for kind::f16: float32 accumulator (bits 4-5 = 1),
-// A and B type in bits 7-9 / 10-12 (0 = F16, 1 = BF16), A K-major (bit 15 =
-// 0), B MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t instr_desc(int is_bf16, int m, int n, int b_mn_major) {
+// A and B type in bits 7-9 / 10-12 (0 = F16, 1 = BF16), A major-ness in bit 15
+// and B major-ness in bit 16 (0 = K-major, 1 = MN-major), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t instr_desc(int is_bf16, int m, int n, int a_mn_major,
+                                                  int b_mn_major) {
     return (1u << 4) | ((uint32_t)is_bf16 << 7) | ((uint32_t)is_bf16 << 10) |
-           ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+           ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -315,30 +319,61 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Sum `count` float32 partial tiles (stride `stride` floats apart) in order
-// 0, 1, ... for the float4 at index e4; loads are issued eight at a time.
-__device__ __forceinline__ float4 ordered_sum4(const float* base, int64_t stride, int count,
-                                               int64_t e4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < count; s0 += 8) {
-        float4 v[8];
+// Sum `count` float32 partial tiles (`stride` floats apart) in order 0, 1,
+// ... for the float4s at indices e0 and e1 (e1 < 0: only e0).  All loads of
+// a batch of up to SUM_BATCH partials are issued before any is added, so a
+// group costs one round trip to L2 instead of one per partial.
+__device__ __noinline__ void ordered_sum4x2(const float* base, int64_t stride, int count,
+                                            int64_t e0, int64_t e1, float4& r0, float4& r1) {
+    const int64_t e1c = e1 >= 0 ? e1 : e0;   // branch-free loads; r1 unused when e1 < 0
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 a1 = a0;
+    for (int s0 = 0; s0 < count; s0 += SUM_BATCH) {
+        const int n = count - s0 < SUM_BATCH ? count - s0 : SUM_BATCH;
+        float4 v0[SUM_BATCH], v1[SUM_BATCH];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (s0 + j < count)
-                v[j] = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(s0 + j) * stride) + e4);
+        for (int j = 0; j < SUM_BATCH; ++j) {
+            const int jj = j < n ? j : 0;
+            const float4* src = reinterpret_cast<const float4*>(base + (int64_t)(s0 + jj) * stride);
+            v0[j] = __ldcg(src + e0);
+            v1[j] = __ldcg(src + e1c);
+        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (s0 + j < count) {
-                acc.x += v[j].x;
-                acc.y += v[j].y;
-                acc.z += v[j].z;
-                acc.w += v[j].w;
+        for (int j = 0; j < SUM_BATCH; ++j) {
+            if (j < n) {
+                a0.x += v0[j].x; a0.y += v0[j].y; a0.z += v0[j].z; a0.w += v0[j].w;
+                a1.x += v1[j].x; a1.y += v1[j].y; a1.z += v1[j].z; a1.w += v1[j].w;
             }
+        }
     }
-    return acc;
+    r0 = a0;
+    r1 = a1;
 }
 
-template <int BN, bool SPLIT>
+// Narrow four float32 sums and store them at output row r, column col of
+// the tile (col < N checked by the caller).
+__device__ __forceinline__ void store4(const Params& p, int64_t item, int64_t row, int64_t col,
+                                       float4 v) {
+    uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) + ((item * p.M + row) * p.N + col) * 2) = o;
+}
+
+// Swapped operands: the tile holds Y^T (TMEM lane = output column n, TMEM
+// column = output row m); store four consecutive rows m0..m0+3 of column n.
+__device__ __forceinline__ void store4_t(const Params& p, int64_t item, int64_t n, int64_t m0,
+                                         float4 v) {
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    unsigned short* y = static_cast<unsigned short*>(p.Y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (m0 + i < p.M) {
+            const uint32_t h = pack2(f[i], 0.f, p.is_bf16);
+            y[(item * p.M + m0 + i) * p.N + n] = (unsigned short)(h & 0xFFFFu);
+        }
+    }
+}
+
+template <int BN, bool SPLIT, bool SWAP>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -378,6 +413,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     tc_fence_after();
     const uint32_t tmem_base = s->tmem_base;
 
+    // one reduced float4 of a tile (entries e4*4 .. e4*4+3 of the BM x BN
+    // partial layout) to Y
+    auto store_sum = [&](int64_t item, int64_t mb, int64_t nb, int64_t e4, float4 v) {
+        const int64_t r = (e4 * 4) / BN, cc = (e4 * 4) % BN;
+        if constexpr (SWAP) {
+            store4_t(p, item, mb * BM + r, cc, v);
+        } else {
+            if (nb * BN + cc < p.N) store4(p, item, mb * BM + r, nb * BN + cc, v);
+        }
+    };
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -405,11 +451,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     armed[stage] = true;
                     armed_parity[stage] = phase;
                     const int k0 = (int)(kb * BK);
-                    tma_load_3d(sa, &tmap_a, &s->full[stage], k0, m0, a_item);
+                    if constexpr (!SWAP) {
+                        tma_load_3d(sa, &tmap_a, &s->full[stage], k0, m0, a_item);
 #pragma unroll
-                    for (int j = 0; j < C::NBLK; ++j)
-                        tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, &s->full[stage],
-                                    n0 + C::BLK_COLS * j, k0, b_item);
+                        for (int j = 0; j < C::NBLK; ++j)
+                            tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, &s->full[stage],
+                                        n0 + C::BLK_COLS * j, k0, b_item);
+                    } else {
+                        // MMA operand A = 128 columns of the problem's B (two
+                        // 64-column MN-major boxes); operand B = the problem's
+                        // A rows (K-major, rows past M read as zeros)
+                        tma_load_3d(sa, &tmap_a, &s->full[stage], m0, k0, b_item);
+                        tma_load_3d(sa + 64 * BK * 2, &tmap_a, &s->full[stage], m0 + 64, k0, b_item);
+                        tma_load_3d(sb, &tmap_b, &s->full[stage], k0, 0, a_item);
+                        (void)n0;
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -422,7 +478,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(p.is_bf16, BM, BN, 1);
+            const uint32_t idesc = SWAP ? instr_desc(p.is_bf16, BM, BN, 1, 0)
+                                        : instr_desc(p.is_bf16, BM, BN, 0, 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
@@ -441,12 +498,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // A: K-major, 128-byte swizzle; advance 16 elements = 32
                         // bytes inside the swizzle row; 8-row groups 1024 apart
-                        const uint64_t ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
-                        // B: MN-major; advance 16 K-rows of SW bytes; boxes of
-                        // BLK_COLS columns B_BLK_BYTES apart (LBO), 8-row groups
-                        // 8 * SW apart (SBO)
-                        const uint64_t bd = smem_desc(b_addr + kk * UMMA_K * C::SW,
-                                                      C::B_BLK_BYTES, 8 * C::SW, C::LAYOUT);
+                        uint64_t ad, bd;
+                        if constexpr (!SWAP) {
+                            ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
+                            // B: MN-major; advance 16 K-rows of SW bytes; boxes of
+                            // BLK_COLS columns B_BLK_BYTES apart (LBO), 8-row
+                            // groups 8 * SW apart (SBO)
+                            bd = smem_desc(b_addr + kk * UMMA_K * C::SW, C::B_BLK_BYTES, 8 * C::SW,
+                                           C::LAYOUT);
+                        } else {
+                            // A: MN-major, 128-byte swizzle; advance 16 K-rows of
+                            // 128 bytes; the two 64-column boxes 8192 bytes apart
+                            ad = smem_desc(a_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
+                            // B: K-major, 128-byte swizzle, rows of 64 K-elements
+                            bd = smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u);
+                        }
                         mma_f16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&s->empty[stage]);   // stage free once these MMAs finish
@@ -475,10 +541,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
             tc_fence_after();
             const int64_t row = mb * BM + row_in_tile;
-            const bool row_ok = row < p.M;
+            const int64_t rows_total = SWAP ? p.N : p.M;    // extent of the TMEM-lane dimension
+            const bool row_ok = row < rows_total;
             const uint32_t t_base =
                 tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * C::ACC_COLS;
-            if (!SPLIT) {
+            if (!SPLIT && SWAP) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x16(t_base, r);
+                if (row_ok) {
+                    unsigned short* y = static_cast<unsigned short*>(p.Y);
+#pragma unroll
+                    for (int m = 0; m < BN; ++m)
+                        if (m < p.M)
+                            y[(item * p.M + m) * p.N + row] =
+                                (unsigned short)(pack2(__uint_as_float(r[m]), 0.f, p.is_bf16) & 0xFFFFu);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
+            } else if (!SPLIT) {
                 unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
                                       ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
 #pragma unroll 1
@@ -534,7 +615,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 // sums in group order by the last group
                 const int g = slice / p.group;
                 const int gsize = min(p.group, p.splits - g * p.group);
-                const int64_t rows_valid = min64(BM, p.M - mb * BM);
+                const int64_t rows_valid = min64(BM, rows_total - mb * BM);
                 const int64_t e4_count = rows_valid * BN / 4;
                 const int64_t tile_floats = (int64_t)BM * BN;
                 __threadfence();
@@ -550,22 +631,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     __threadfence();
                     const float* first = p.part1 + (tile * p.splits + g * p.group) * tile_floats;
                     if (p.groups == 1) {
-                        for (int64_t e4 = etid; e4 < e4_count; e4 += EPI_THREADS) {
-                            const float4 v = ordered_sum4(first, tile_floats, gsize, e4);
-                            const int64_t r = (e4 * 4) / BN, cc = (e4 * 4) % BN;
-                            const int64_t col = nb * BN + cc;
-                            if (col < p.N) {
-                                uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
-                                *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) +
-                                                          ((item * p.M + mb * BM + r) * p.N + col) * 2) = o;
-                            }
+                        for (int64_t e4 = etid; e4 < e4_count; e4 += 2 * EPI_THREADS) {
+                            const int64_t e4b = e4 + EPI_THREADS < e4_count ? e4 + EPI_THREADS : -1;
+                            float4 v0, v1;
+                            ordered_sum4x2(first, tile_floats, gsize, e4, e4b, v0, v1);
+                            store_sum(item, mb, nb, e4, v0);
+                            if (e4b >= 0) store_sum(item, mb, nb, e4b, v1);
                         }
                         if (etid == 0) p.cnt1[tile * p.groups + g] = 0u;
                     } else {
                         float* gsum = p.part2 + (tile * p.groups + g) * tile_floats;
-                        for (int64_t e4 = etid; e4 < e4_count; e4 += EPI_THREADS)
-                            reinterpret_cast<float4*>(gsum)[e4] =
-                                ordered_sum4(first, tile_floats, gsize, e4);
+                        for (int64_t e4 = etid; e4 < e4_count; e4 += 2 * EPI_THREADS) {
+                            const int64_t e4b = e4 + EPI_THREADS < e4_count ? e4 + EPI_THREADS : -1;
+                            float4 v0, v1;
+                            ordered_sum4x2(first, tile_floats, gsize, e4, e4b, v0, v1);
+                            reinterpret_cast<float4*>(gsum)[e4] = v0;
+                            if (e4b >= 0) reinterpret_cast<float4*>(gsum)[e4b] = v1;
+                        }
                         __threadfence();
                         epi_sync();
                         if (etid == 0) {
@@ -579,17 +661,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         if (last2) {
                             __threadfence();
                             const float* g0 = p.part2 + tile * p.groups * tile_floats;
-                            for (int64_t e4 = etid; e4 < e4_count; e4 += EPI_THREADS) {
-                                const float4 v = ordered_sum4(g0, tile_floats, p.groups, e4);
-                                const int64_t r = (e4 * 4) / BN, cc = (e4 * 4) % BN;
-                                const int64_t col = nb * BN + cc;
-                                if (col < p.N) {
-                                    uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16),
-                                                         pack2(v.z, v.w, p.is_bf16));
-                                    *reinterpret_cast<uint2*>(
-                                        static_cast<unsigned char*>(p.Y) +
-                                        ((item * p.M + mb * BM + r) * p.N + col) * 2) = o;
-                                }
+                            for (int64_t e4 = etid; e4 < e4_count; e4 += 2 * EPI_THREADS) {
+                                const int64_t e4b =
+                                    e4 + EPI_THREADS < e4_count ? e4 + EPI_THREADS : -1;
+                                float4 v0, v1;
+                                ordered_sum4x2(g0, tile_floats, p.groups, e4, e4b, v0, v1);
+                                store_sum(item, mb, nb, e4, v0);
+                                if (e4b >= 0) store_sum(item, mb, nb, e4b, v1);
                             }
                             if (etid == 0) p.cnt2[tile] = 0u;
                         }
@@ -657,34 +735,54 @@ struct SplitPlan {
     size_t part1_bytes = 0, part2_bytes = 0, counters = 0;
 };
 
+// K slices per tile.  Units (tile, slice) run one per SM at a time; pick the
+// slice count whose units fill the last wave best, discounted by the extra
+// traffic of the float32 partial tiles relative to the operand stream.  At
+// most SUM_BATCH^2 slices (both reduction levels then take one load batch),
+// at least 2 K blocks per slice.
 template <int BN>
-static SplitPlan split_plan(const Problem& pr, int sm_count) {
+static SplitPlan split_plan(int64_t tiles, int64_t k_blocks, double stream_bytes, int sm_count,
+                            bool force_split) {
     SplitPlan sp;
-    const int64_t tiles = ceil_div(pr.M, BM) * ceil_div(pr.N, BN) * pr.items;
-    const int64_t kbs = ceil_div(pr.K, BK);
-    // about one unit per SM, at least 2 K blocks per slice
-    int64_t want = max64(1, sm_count / max64(tiles, 1));
-    want = min64(want, max64(1, kbs / 2));
-    const int64_t per = ceil_div(kbs, want);
-    sp.kb_per_split = per;
-    sp.splits = (int)ceil_div(kbs, per);      // every slice non-empty
+    const int64_t smax = min64((int64_t)SUM_BATCH * SUM_BATCH, max64(1, k_blocks / 2));
+    double best = -1.0;
+    int64_t best_s = 1;
+    for (int64_t sl = force_split ? 2 : 1; sl <= max64(smax, force_split ? 2 : 1); ++sl) {
+        const int64_t per = ceil_div(k_blocks, sl);
+        const int64_t real = ceil_div(k_blocks, per);          // non-empty slices
+        const int64_t units = tiles * real;
+        const int64_t waves = ceil_div(units, sm_count);
+        const double fill = (double)units / (double)(waves * sm_count);
+        const double extra = real > 1 ? 2.0 * (double)units * BM * BN * 4 : 0.0;
+        const double score = fill * stream_bytes / (stream_bytes + extra);
+        if (score > best + 1e-9) {
+            best = score;
+            best_s = real;
+        }
+        if (sl >= smax) break;
+    }
+    sp.kb_per_split = ceil_div(k_blocks, best_s);
+    sp.splits = (int)ceil_div(k_blocks, sp.kb_per_split);
     int g = 1;
-    while ((int64_t)g * g < sp.splits) ++g;   // ~sqrt(splits) slices per group
-    sp.group = g;
-    sp.groups = (int)ceil_div(sp.splits, g);
+    while ((int64_t)g * g < sp.splits) ++g;
+    sp.group = g < SUM_BATCH ? g : SUM_BATCH;
+    sp.groups = (int)ceil_div(sp.splits, sp.group);
     sp.tiles = tiles;
     const int64_t tile_bytes = (int64_t)BM * BN * 4;
-    sp.part1_bytes = (size_t)(tiles * sp.splits * tile_bytes);
-    sp.part2_bytes = sp.groups > 1 ? (size_t)(tiles * sp.groups * tile_bytes) : 0;
-    sp.counters = (size_t)(tiles * sp.groups + tiles);
+    if (sp.splits > 1) {
+        sp.part1_bytes = (size_t)(tiles * sp.splits * tile_bytes);
+        sp.part2_bytes = sp.groups > 1 ? (size_t)(tiles * sp.groups * tile_bytes) : 0;
+        sp.counters = (size_t)(tiles * sp.groups + tiles);
+    }
     return sp;
 }
 
-template <int BN, bool SPLIT>
+template <int BN, bool SPLIT, bool SWAP>
 static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
                              const SplitPlan* sp, const Workspace* ws) {
     using C = Cfg<BN>;
     if (!tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31)) return cudaErrorInvalidValue;
+    if (SWAP && pr.M > BN) return cudaErrorInvalidValue;
     // the operands' batch extents: every item offset is a multiple of the
     // matrix size (dense operands), so offset / size is the TMA batch index
     int64_t a_items = 1, b_items = 1;
@@ -698,10 +796,19 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
     const int bf = dt == OLC_BFLOAT16;
-    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>()))
-        return cudaErrorInvalidValue;
+    if (!SWAP) {
+        if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>()))
+            return cudaErrorInvalidValue;
+    } else {
+        // MMA operand A from the problem's B (64-column MN-major boxes), MMA
+        // operand B from the problem's A (BN rows, K-major)
+        if (!encode_3d(&ma, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        if (!encode_3d(&mb, pr.A, bf, pr.K, pr.M, a_items, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
 
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -709,8 +816,8 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     p.N = pr.N;
     p.K = pr.K;
     p.items = pr.items;
-    p.tiles_m = ceil_div(pr.M, BM);
-    p.tiles_n = ceil_div(pr.N, BN);
+    p.tiles_m = SWAP ? ceil_div(pr.N, BM) : ceil_div(pr.M, BM);
+    p.tiles_n = SWAP ? 1 : ceil_div(pr.N, BN);
     p.tiles_per_item = p.tiles_m * p.tiles_n;
     p.total_tiles = p.tiles_per_item * pr.items;
     p.k_blocks = ceil_div(pr.K, BK);
@@ -725,7 +832,8 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     p.groups = 1;
     p.kb_per_split = p.k_blocks;
     if (SPLIT) {
-        if (!sp || !ws || !ws->partials || !ws->counters) return cudaErrorInvalidValue;
+        if (!sp || !ws || !ws->partials || !ws->counters || sp->splits < 2)
+            return cudaErrorInvalidValue;
         p.splits = sp->splits;
         p.group = sp->group;
         p.groups = sp->groups;
@@ -742,14 +850,19 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, SPLIT>,
+        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, SPLIT, SWAP>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t units = p.total_tiles * p.splits;
     const int64_t grid = min64(units, (int64_t)sm_count);
-    tc_gemm_kernel<BN, SPLIT><<<(unsigned)grid, THREADS, C::SMEM_BYTES, s>>>(ma, mb, p);
+    tc_gemm_kernel<BN, SPLIT, SWAP><<<(unsigned)grid, THREADS, C::SMEM_BYTES, s>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+static double operand_bytes(const Problem& pr) {
+    // A and B streamed once per item (upper bound for broadcast operands)
+    return 2.0 * (double)(pr.M * pr.K + pr.K * pr.N) * (double)pr.items;
 }
 
 }  // namespace tc
@@ -761,22 +874,26 @@ bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
-    return tc::launch_tc<256, false>(dt, pr, sm_count, s, nullptr, nullptr);
+    return tc::launch_tc<256, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
 }
 
 cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
     if (pr.N > 16) return cudaErrorInvalidValue;
-    return tc::launch_tc<16, false>(dt, pr, sm_count, s, nullptr, nullptr);
+    return tc::launch_tc<16, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
 }
 
-// split-K on the tensor cores: tile width by N
+// ---- split-K on the tensor cores: tile width by N
 static int tc_split_bn(int64_t N) { return N <= 16 ? 16 : (N <= 32 ? 32 : 256); }
 
 static tc::SplitPlan tc_split_plan(const Problem& pr, int sm_count) {
-    switch (tc_split_bn(pr.N)) {
-        case 16: return tc::split_plan<16>(pr, sm_count);
-        case 32: return tc::split_plan<32>(pr, sm_count);
-        default: return tc::split_plan<256>(pr, sm_count);
+    const int bn = tc_split_bn(pr.N);
+    const int64_t tiles = ceil_div(pr.M, tc::BM) * ceil_div(pr.N, bn) * pr.items;
+    const int64_t kbs = ceil_div(pr.K, tc::BK);
+    const double bytes = tc::operand_bytes(pr);
+    switch (bn) {
+        case 16: return tc::split_plan<16>(tiles, kbs, bytes, sm_count, true);
+        case 32: return tc::split_plan<32>(tiles, kbs, bytes, sm_count, true);
+        default: return tc::split_plan<256>(tiles, kbs, bytes, sm_count, true);
     }
 }
 
@@ -794,13 +911,50 @@ size_t tc_split_counter_count(const Problem& pr, int sm_count) {
 cudaError_t launch_tc_split(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
                             cudaStream_t s) {
     const tc::SplitPlan sp = tc_split_plan(pr, sm_count);
+    if (sp.splits < 2) {
+        // a K too short to split: the plain tile kernel of the same width
+        switch (tc_split_bn(pr.N)) {
+            case 16: return tc::launch_tc<16, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
+            case 32: return tc::launch_tc<32, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
+            default: return tc::launch_tc<256, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
+        }
+    }
     if (ws.partial_bytes < sp.part1_bytes + sp.part2_bytes || ws.counter_count < sp.counters)
         return cudaErrorInvalidValue;
     switch (tc_split_bn(pr.N)) {
-        case 16: return tc::launch_tc<16, true>(dt, pr, sm_count, s, &sp, &ws);
-        case 32: return tc::launch_tc<32, true>(dt, pr, sm_count, s, &sp, &ws);
-        default: return tc::launch_tc<256, true>(dt, pr, sm_count, s, &sp, &ws);
+        case 16: return tc::launch_tc<16, true, false>(dt, pr, sm_count, s, &sp, &ws);
+        case 32: return tc::launch_tc<32, true, false>(dt, pr, sm_count, s, &sp, &ws);
+        default: return tc::launch_tc<256, true, false>(dt, pr, sm_count, s, &sp, &ws);
     }
+}
+
+// ---- skinny-M on the tensor cores: Y^T = B^T A^T, 128 output columns per
+// tile along the MMA's M side, the (at most 16) output rows along its N side
+static tc::SplitPlan tc_skinny_m_plan(const Problem& pr, int sm_count) {
+    const int64_t tiles = ceil_div(pr.N, tc::BM) * pr.items;
+    return tc::split_plan<16>(tiles, ceil_div(pr.K, tc::BK), tc::operand_bytes(pr), sm_count,
+                              false);
+}
+
+int tc_skinny_m_pick(const Problem& pr, int sm_count) { return tc_skinny_m_plan(pr, sm_count).splits; }
+
+size_t tc_skinny_m_partial_bytes(const Problem& pr, int sm_count) {
+    const tc::SplitPlan sp = tc_skinny_m_plan(pr, sm_count);
+    return sp.part1_bytes + sp.part2_bytes;
+}
+
+size_t tc_skinny_m_counter_count(const Problem& pr, int sm_count) {
+    return tc_skinny_m_plan(pr, sm_count).counters;
+}
+
+cudaError_t launch_tc_skinny_m(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
+                               cudaStream_t s) {
+    if (pr.M > 16) return cudaErrorInvalidValue;
+    const tc::SplitPlan sp = tc_skinny_m_plan(pr, sm_count);
+    if (sp.splits < 2) return tc::launch_tc<16, false, true>(dt, pr, sm_count, s, nullptr, nullptr);
+    if (ws.partial_bytes < sp.part1_bytes + sp.part2_bytes || ws.counter_count < sp.counters)
+        return cudaErrorInvalidValue;
+    return tc::launch_tc<16, true, true>(dt, pr, sm_count, s, &sp, &ws);
 }
 
 }  // namespace olc
@@ -809,6 +963,7 @@ extern "C" uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t
                                            uint32_t layout) {
     return olc::tc::smem_desc(addr, lbo, sbo, layout);
 }
-extern "C" uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int b_mn_major) {
-    return olc::tc::instr_desc(is_bf16, m, n, b_mn_major);
+extern "C" uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int a_mn_major,
+                                            int b_mn_major) {
+    return olc::tc::instr_desc(is_bf16, m, n, a_mn_major, b_mn_major);
 }

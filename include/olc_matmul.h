@@ -233,7 +233,7 @@ int olc_version(void);
  * "shared memory descriptor" and "instruction descriptor" for kind::f16),
  * exported so a host test can check the bit layout.  Pure functions. */
 uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout);
-uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int b_mn_major);
+uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int a_mn_major, int b_mn_major);
 
 /* ---- allocation-free split-K ------------------------------------------- */
 

@@ -199,7 +199,7 @@ def test_tcgen05_descriptor_bit_layout():
     lib = binding.load()
     lib.olc_debug_tc_smem_desc.argtypes = [ctypes.c_uint32] * 4
     lib.olc_debug_tc_smem_desc.restype = ctypes.c_uint64
-    lib.olc_debug_tc_instr_desc.argtypes = [ctypes.c_int] * 4
+    lib.olc_debug_tc_instr_desc.argtypes = [ctypes.c_int] * 5
     lib.olc_debug_tc_instr_desc.restype = ctypes.c_uint32
     d = lib.olc_debug_tc_smem_desc(0x1A400, 8192, 1024, 2)
     assert _field(d, 0, 13) == 0x1A400 >> 4      # start address >> 4
@@ -216,7 +216,7 @@ def test_tcgen05_descriptor_bit_layout():
         d = lib.olc_debug_tc_smem_desc(0x2000, 4096, 512, layout)
         assert _field(d, 61, 63) == layout and _field(d, 32, 45) == 512 >> 4
     for bf16 in (0, 1):
-        i = lib.olc_debug_tc_instr_desc(bf16, 128, 256, 1)
+        i = lib.olc_debug_tc_instr_desc(bf16, 128, 256, 0, 1)
         assert _field(i, 0, 3) == 0                  # dense, no saturate
         assert _field(i, 4, 5) == 1                  # D = F32
         assert _field(i, 7, 9) == bf16               # A: 0 F16, 1 BF16
@@ -228,3 +228,7 @@ def test_tcgen05_descriptor_bit_layout():
         assert _field(i, 23, 23) == 0
         assert _field(i, 24, 28) == 128 >> 4         # M
         assert _field(i, 29, 31) == 0
+    # swapped operands: A MN-major, B K-major, N = 16
+    i = lib.olc_debug_tc_instr_desc(0, 128, 16, 1, 0)
+    assert _field(i, 15, 15) == 1 and _field(i, 16, 16) == 0
+    assert _field(i, 17, 22) == 16 >> 3 and _field(i, 24, 28) == 128 >> 4

@@ -253,6 +253,26 @@ def test_tc_skinny_n(dtype, shapes):
     check_product(ai, bi, dtype, algorithm="skinny_n", exact=True)
 
 
+TC_SKINNY_M_SHAPES = [
+    ((1, 64), (64, 256)),
+    ((16, 520), (520, 136)),           # N tail inside the second 128-column tile
+    ((4, 8192), (8192, 2048)),         # long K: split over K
+    ((3, 2, 5, 64), (2, 64, 384)),     # broadcast batch
+    ((64,), (64, 48)),                 # rank-one A
+    ((2, 16, 1024), (2, 1024, 264)),   # batched B: 2 items of 16 rows
+]
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("shapes", TC_SKINNY_M_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_tc_skinny_m(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=14)
+    check_product(a, b, dtype, algorithm="skinny_m")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=14)
+    check_product(ai, bi, dtype, algorithm="skinny_m", exact=True)
+
+
 # --------------------------------------------------------------------------
 # edge cases
 
