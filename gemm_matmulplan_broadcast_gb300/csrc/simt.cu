@@ -161,11 +161,187 @@ cudaError_t launch_general_simt_generic(olc_dtype dt, const Problem& p, cudaStre
 }  // namespace olc
 
 namespace olc {
+
+// ---------------------------------------------------------------------------
+// GENERAL_SIMT fast path: FP32 FFMA / FP64 DFMA register tiles
+//
+// Block tile BM x BN, BK-deep slices, 256 threads in a 16 x 16 grid; each
+// thread owns a TM x TN register tile split into two halves in each
+// direction (rows ty*TM/2 + i and BM/2 + ty*TM/2 + i, the same for columns),
+// so that the shared-memory reads of a warp are broadcasts (A) or one
+// contiguous run (B).  A's slice is stored transposed (As[k][m]) so a thread
+// reads its rows as 16-byte vectors.  The next slice is loaded from global
+// memory into registers while the current one is multiplied (two
+// shared-memory buffers, one barrier per slice).  Every output sums its K
+// products in ascending k with fused multiply-adds in the element type.
+// Needs K and N multiples of the 16-byte vector width and 16-byte aligned
+// operands; other shapes take the generic tile kernel above.
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<float> {
+    using type = float4;
+    static constexpr int W = 4;
+};
+template <>
+struct Vec<double> {
+    using type = double2;
+    static constexpr int W = 2;
+};
+
+template <typename T, int BM, int BN, int BK, int TM, int TN>
+__global__ void __launch_bounds__(256)
+simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
+    using V = typename Vec<T>::type;
+    constexpr int W = Vec<T>::W;
+    constexpr int PAD = W;
+    constexpr int HM = TM / 2, HN = TN / 2;
+    static_assert(BM == 16 * TM && BN == 16 * TN, "16 x 16 threads");
+    static_assert((BM * BK) / W == 256 && (BK * BN) / W == 256, "one vector per thread per slice");
+    static_assert(HM % W == 0 && HN % W == 0, "half tiles are whole vectors");
+    __shared__ __align__(16) T As[2][BK][BM + PAD];
+    __shared__ __align__(16) T Bs[2][BK][BN];
+
+    const int64_t per_item = tiles_m * tiles_n;
+    const int64_t item = blockIdx.x / per_item;
+    const int64_t rem = blockIdx.x % per_item;
+    const int64_t m0 = (rem / tiles_n) * BM;
+    const int64_t n0 = (rem % tiles_n) * BN;
+    int64_t a_off, b_off;
+    batch_offsets(p.map, item, a_off, b_off);
+    const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
+    const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
+    T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
+    const int64_t M = p.M, N = p.N, K = p.K;
+
+    const int t = threadIdx.x;
+    const int tx = t % 16, ty = t / 16;
+    // global -> register staging: one vector of A and one of B per thread
+    constexpr int AVR = BK / W;                   // vectors per A row slice
+    const int a_row = t / AVR, a_k = (t % AVR) * W;
+    constexpr int BVR = BN / W;                   // vectors per B row
+    const int b_row = t / BVR, b_col = (t % BVR) * W;
+    const int64_t ga_row = m0 + a_row;
+    const int64_t gb_col = n0 + b_col;
+
+    auto load_a = [&](int64_t k0, V& v) {
+        const int64_t k = k0 + a_k;
+        if (ga_row < M && k < K) v = *reinterpret_cast<const V*>(A + ga_row * K + k);
+        else v = V{};
+    };
+    auto load_b = [&](int64_t k0, V& v) {
+        const int64_t k = k0 + b_row;
+        if (k < K && gb_col < N) v = *reinterpret_cast<const V*>(B + k * N + gb_col);
+        else v = V{};
+    };
+    auto store_stage = [&](int buf, const V& va, const V& vb) {
+        const T* ae = reinterpret_cast<const T*>(&va);
+#pragma unroll
+        for (int i = 0; i < W; ++i) As[buf][a_k + i][a_row] = ae[i];
+        *reinterpret_cast<V*>(&Bs[buf][b_row][b_col]) = vb;
+    };
+
+    T acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = T(0);
+
+    V va, vb;
+    load_a(0, va);
+    load_b(0, vb);
+    store_stage(0, va, vb);
+    __syncthreads();
+    int buf = 0;
+    for (int64_t k0 = 0; k0 < K; k0 += BK) {
+        const bool more = k0 + BK < K;
+        if (more) {
+            load_a(k0 + BK, va);
+            load_b(k0 + BK, vb);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            T a[TM], b[TN];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int q = 0; q < HM / W; ++q) {
+                    const V v = *reinterpret_cast<const V*>(&As[buf][kk][h * (BM / 2) + ty * HM + q * W]);
+                    const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+                    for (int i = 0; i < W; ++i) a[h * HM + q * W + i] = e[i];
+                }
+#pragma unroll
+                for (int q = 0; q < HN / W; ++q) {
+                    const V v = *reinterpret_cast<const V*>(&Bs[buf][kk][h * (BN / 2) + tx * HN + q * W]);
+                    const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+                    for (int i = 0; i < W; ++i) b[h * HN + q * W + i] = e[i];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fma(a[i], b[j], acc[i][j]);
+        }
+        if (more) {
+            store_stage(buf ^ 1, va, vb);
+            __syncthreads();
+            buf ^= 1;
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int64_t gm = m0 + (i / HM) * (BM / 2) + ty * HM + (i % HM);
+        if (gm >= M) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int q = 0; q < HN / W; ++q) {
+                const int64_t gn = n0 + h * (BN / 2) + tx * HN + q * W;
+                if (gn < N) {   // N is a multiple of W: the whole vector is inside
+                    V v;
+                    T* e = reinterpret_cast<T*>(&v);
+#pragma unroll
+                    for (int j = 0; j < W; ++j) e[j] = acc[i][h * HN + q * W + j];
+                    *reinterpret_cast<V*>(Y + gm * N + gn) = v;
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int BM, int BN, int BK, int TM, int TN>
+static cudaError_t launch_fast(const Problem& p, cudaStream_t stream) {
+    const int64_t tm = ceil_div(p.M, BM), tn = ceil_div(p.N, BN);
+    const int64_t blocks = tm * tn * p.items;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    simt_fast_kernel<T, BM, BN, BK, TM, TN><<<(unsigned)blocks, 256, 0, stream>>>(p, tm, tn);
+    return cudaGetLastError();
+}
+
 bool general_simt_fast_ok(olc_dtype dt, int64_t N, int64_t K) {
-    (void)dt; (void)N; (void)K;
+    if (dt == OLC_FLOAT) return N % 4 == 0 && K % 4 == 0;
+    if (dt == OLC_DOUBLE) return N % 2 == 0 && K % 2 == 0;
     return false;
 }
+
+static bool aligned_items(const Problem& p, int64_t elem) {
+    if ((reinterpret_cast<uintptr_t>(p.A) | reinterpret_cast<uintptr_t>(p.B) |
+         reinterpret_cast<uintptr_t>(p.Y)) & 15)
+        return false;
+    for (int d = 0; d < p.map.rank; ++d)
+        if (((p.map.a_stride[d] | p.map.b_stride[d]) * elem) % 16 != 0) return false;
+    return ((p.M * p.N) * elem) % 16 == 0;
+}
+
 cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream) {
+    if (dt == OLC_FLOAT && aligned_items(p, 4)) return launch_fast<float, 128, 128, 8, 8, 8>(p, stream);
+    if (dt == OLC_DOUBLE && aligned_items(p, 8)) return launch_fast<double, 64, 64, 8, 4, 4>(p, stream);
     return launch_general_simt_generic(dt, p, stream);
 }
+
 }  // namespace olc
