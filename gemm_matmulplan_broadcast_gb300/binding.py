@@ -87,6 +87,8 @@ def load():
             "olc_matmul_plan_algorithm": ([vp], ctypes.c_int),
             "olc_matmul_plan_force_algorithm": ([vp, ctypes.c_int], ctypes.c_int),
             "olc_matmul_plan_launches": ([vp], ctypes.c_int),
+            "olc_matmul_plan_set_splits": ([vp, ctypes.c_int], ctypes.c_int),
+            "olc_matmul_plan_splits": ([vp], ctypes.c_int),
             "olc_matmul_plan_workspace_bytes": ([vp], ctypes.c_size_t),
             "olc_matmul_plan_describe": ([vp, ctypes.c_char_p, ctypes.c_size_t], ctypes.c_int),
             "olc_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -206,6 +208,15 @@ class Plan:
         _check(self.lib.olc_matmul_plan_force_algorithm(self._h, ALGORITHMS[algorithm]),
                "olc_matmul_plan_force_algorithm(%s)" % algorithm)
         return self
+
+    def set_splits(self, splits: int):
+        """Tuning override of the K-slice count (0 = automatic)."""
+        _check(self.lib.olc_matmul_plan_set_splits(self._h, int(splits)), "set_splits")
+        return self
+
+    @property
+    def splits(self) -> int:
+        return int(self.lib.olc_matmul_plan_splits(self._h))
 
     @property
     def launches(self) -> int:

@@ -41,6 +41,7 @@ struct olc_matmul_plan {
     int algo;
     bool forced;
     int splits;                  // SPLIT_K slices or SKINNY_M K-slices
+    int split_hint;              // tuning override of the slice count (0 = automatic)
     int device;                  // -1: planned without a device
     int sm_count;
     void* workspace;
@@ -91,6 +92,7 @@ Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, voi
     pr.K = p->K;
     pr.items = p->items;
     pr.map = p->map;
+    pr.split_hint = p->split_hint;
     return pr;
 }
 
@@ -500,6 +502,15 @@ olc_status olc_matmul_plan_force_algorithm(olc_matmul_plan* plan, int algo) {
     plan->forced = true;
     return prepare_algorithm(plan);
 }
+
+olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits) {
+    if (!plan) return OLC_ERR_NULL;
+    if (splits < 0 || splits > 4096) return OLC_ERR_INVALID;
+    plan->split_hint = splits;
+    return prepare_algorithm(plan);
+}
+
+int olc_matmul_plan_splits(const olc_matmul_plan* plan) { return plan ? plan->splits : -1; }
 
 int olc_matmul_plan_launches(const olc_matmul_plan* plan) {
     if (!plan) return -1;

@@ -32,6 +32,7 @@ struct Problem {
     int64_t M, N, K;
     int64_t items;
     BatchMap map;
+    int split_hint;   // > 0: K slices requested by a tuning override, 0: automatic
 };
 
 // Workspace handed to the split reductions: `partials` holds fp32/fp64

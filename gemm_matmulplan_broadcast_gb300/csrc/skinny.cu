@@ -265,6 +265,7 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
 }
 
 static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
+    if (p.split_hint > 0) return (int)min64(p.split_hint, max64(1, p.K / 8));
     const int64_t groups = skinny_m_col_groups(dt, p.N) * p.items;
     const int64_t slots = (int64_t)sm_count * skinny_m_blocks_per_sm(dt, p.M);
     const int64_t eb = dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2;

@@ -118,6 +118,7 @@ static int64_t acc_bytes(olc_dtype dt) { return dt == OLC_DOUBLE ? 8 : 4; }
 
 int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count) {
     (void)dt;
+    if (p.split_hint > 0) return (int)min64(p.split_hint, max64(1, ceil_div(p.K, 32)));
     const int64_t tiles = ceil_div(p.M, 32) * ceil_div(p.N, 32) * p.items;
     // about two blocks per SM, each slice at least 256 long
     int64_t s = ceil_div(2LL * sm_count, tiles);
@@ -243,6 +244,7 @@ extern "C" olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, 
     p.N = N;
     p.K = K;
     p.items = 1;
+    p.split_hint = 0;
     const int64_t tiles = ceil_div(M, 32) * ceil_div(N, 32);
     const int64_t tile_bytes = 32 * 32 * acc_bytes(dtype);
     if (tiles * (int64_t)sizeof(unsigned int) > (int64_t)kStaticCounterBytes ||

@@ -57,7 +57,7 @@ constexpr int MAX_STAGES = 12;
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;                 // warps 2..5
 constexpr int GROUP_M = 16;                      // tile raster: 16 M-blocks per group
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // default bound of every wait
 constexpr int SUM_BATCH = 12;                    // partials loaded per reduction round trip
 
 // Per tile width BN: how B (MN-major, N contiguous) is staged.  A 64-deep
@@ -155,15 +155,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: returns false when the wait ran out or another role aborted.
+// Bounded wait: returns false when the wait ran out (after `limit_ns` of
+// %globaltimer; the error word gets kErrWaitTimeout) or another role aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err) {
+                                          unsigned int* err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             *abort_flag = 1;
             raise_device_error(err, kErrWaitTimeout);
             return false;
@@ -742,7 +744,7 @@ struct SplitPlan {
 // at least 2 K blocks per slice.
 template <int BN>
 static SplitPlan split_plan(int64_t tiles, int64_t k_blocks, double stream_bytes, int sm_count,
-                            bool force_split) {
+                            bool force_split, int hint = 0) {
     SplitPlan sp;
     const int64_t smax = min64((int64_t)SUM_BATCH * SUM_BATCH, max64(1, k_blocks / 2));
     double best = -1.0;
@@ -761,6 +763,7 @@ static SplitPlan split_plan(int64_t tiles, int64_t k_blocks, double stream_bytes
         }
         if (sl >= smax) break;
     }
+    if (hint > 0) best_s = min64(hint, min64(k_blocks, (int64_t)SUM_BATCH * SUM_BATCH));
     sp.kb_per_split = ceil_div(k_blocks, best_s);
     sp.splits = (int)ceil_div(k_blocks, sp.kb_per_split);
     int g = 1;
@@ -891,9 +894,9 @@ static tc::SplitPlan tc_split_plan(const Problem& pr, int sm_count) {
     const int64_t kbs = ceil_div(pr.K, tc::BK);
     const double bytes = tc::operand_bytes(pr);
     switch (bn) {
-        case 16: return tc::split_plan<16>(tiles, kbs, bytes, sm_count, true);
-        case 32: return tc::split_plan<32>(tiles, kbs, bytes, sm_count, true);
-        default: return tc::split_plan<256>(tiles, kbs, bytes, sm_count, true);
+        case 16: return tc::split_plan<16>(tiles, kbs, bytes, sm_count, true, pr.split_hint);
+        case 32: return tc::split_plan<32>(tiles, kbs, bytes, sm_count, true, pr.split_hint);
+        default: return tc::split_plan<256>(tiles, kbs, bytes, sm_count, true, pr.split_hint);
     }
 }
 
@@ -933,7 +936,7 @@ cudaError_t launch_tc_split(olc_dtype dt, const Problem& pr, int sm_count, const
 static tc::SplitPlan tc_skinny_m_plan(const Problem& pr, int sm_count) {
     const int64_t tiles = ceil_div(pr.N, tc::BM) * pr.items;
     return tc::split_plan<16>(tiles, ceil_div(pr.K, tc::BK), tc::operand_bytes(pr), sm_count,
-                              false);
+                              false, pr.split_hint);
 }
 
 int tc_skinny_m_pick(const Problem& pr, int sm_count) { return tc_skinny_m_plan(pr, sm_count).splits; }
@@ -958,6 +961,37 @@ cudaError_t launch_tc_skinny_m(olc_dtype dt, const Problem& pr, int sm_count, co
 }
 
 }  // namespace olc
+
+namespace olc {
+namespace tc {
+
+// One thread: an mbarrier that expects one arrival, which is made only when
+// `arrive` is set; then the same bounded wait the GEMM kernel uses.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int arrive, unsigned int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (arrive) mbar_arrive(&bar);
+    mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+}
+
+}  // namespace tc
+}  // namespace olc
+
+extern "C" olc_status olc_debug_wait_selftest(uint64_t limit_ns, int arrive, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    olc::tc::wait_selftest_kernel<<<1, 1, 0, s>>>((unsigned long long)limit_ns, arrive,
+                                                  olc::device_error_word());
+    if (cudaGetLastError() != cudaSuccess) return OLC_ERR_CUDA;
+    unsigned int flags = 0;
+    if (olc::read_and_clear_device_error(&flags, s) != cudaSuccess) {
+        cudaGetLastError();
+        return OLC_ERR_CUDA;
+    }
+    return flags ? OLC_ERR_DEVICE_TIMEOUT : OLC_OK;
+}
 
 extern "C" uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                            uint32_t layout) {

@@ -209,6 +209,15 @@ int olc_matmul_plan_algorithm(const olc_matmul_plan* plan);
  * only themselves or AUTO. */
 olc_status olc_matmul_plan_force_algorithm(olc_matmul_plan* plan, int algo);
 
+/* Tuning override of the number of K slices of SPLIT_K and SKINNY_M plans
+ * (0 = automatic choice from the SM count; values are clamped to what the
+ * shape allows).  Re-sizes the workspace.  Errors: OLC_ERR_NULL,
+ * OLC_ERR_INVALID (negative or above 4096), OLC_ERR_OOM, OLC_ERR_CUDA. */
+olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits);
+
+/* K slices the plan currently uses (1 when it does not split). */
+int olc_matmul_plan_splits(const olc_matmul_plan* plan);
+
 /* Kernel launches one execute of this plan makes (0 for EMPTY). */
 int olc_matmul_plan_launches(const olc_matmul_plan* plan);
 
@@ -234,6 +243,14 @@ int olc_version(void);
  * exported so a host test can check the bit layout.  Pure functions. */
 uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout);
 uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int a_mn_major, int b_mn_major);
+
+/* Self-test of the bounded device-side wait the tensor-core kernel uses on
+ * every mbarrier: one thread waits for an mbarrier phase that completes only
+ * if `arrive` is non-zero, giving up after `limit_ns` nanoseconds of
+ * %globaltimer.  Synchronises `stream`.  Returns OLC_OK when the wait
+ * succeeded and OLC_ERR_DEVICE_TIMEOUT when it ran out (the device error word
+ * is read and cleared); the CUDA context stays usable either way. */
+olc_status olc_debug_wait_selftest(uint64_t limit_ns, int arrive, void* stream);
 
 /* ---- allocation-free split-K ------------------------------------------- */
 
