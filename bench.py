@@ -392,9 +392,43 @@ def measure_workload(workload, steps, warmup, device, peaks, l2_bytes):
     return items, stream
 
 
+def graph_time_per_launch(it, stream, reps=20, launches=None):
+    """Per-launch device time of one product, free of host launch gaps:
+    `launches` executes (rotating over the operand sets) captured into one
+    CUDA graph, the graph replayed `reps` times between CUDA events on the
+    capture stream.  Returns the list of per-launch milliseconds, one per
+    replay."""
+    import torch
+    n = launches or max(4, len(it["sets"]))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            A, B, Y = it["sets"][i % len(it["sets"])]
+            it["plan"].execute(A, B, Y, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                A, B, Y = it["sets"][i % len(it["sets"])]
+                it["plan"].execute(A, B, Y, stream=stream)
+        g.replay()
+        stream.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+    stream.synchronize()
+    out = [e0.elapsed_time(e1) / n for e0, e1 in evs]
+    del g
+    return out
+
+
 def measure_secondary(workload, device, peaks, l2):
     """Median per-launch time and roofline of every product of a workload (and
-    of each chain stage), after 3 warm-up launches; about 1 s per product."""
+    of each chain stage).  Short kernels are timed through CUDA graphs of
+    back-to-back launches so host launch gaps do not count; long ones
+    (> 2 ms) with per-launch events."""
     import torch
     from gemm_matmulplan_broadcast_gb300 import Plan
     items = build_inputs(workload, device)
@@ -416,13 +450,18 @@ def measure_secondary(workload, device, peaks, l2):
     _, probe = time_steps(items, 1, stream)
     res = []
     for i, it in enumerate(items):
-        n = int(max(3, min(50, 1000.0 / max(probe[i][0], 1e-3))))
-        one = [it]
-        _, per = time_steps(one, n, stream)
-        ms = statistics.median(per[0])
+        if probe[i][0] < 2.0:
+            per = graph_time_per_launch(it, stream)
+            how = "cuda graph of %d launches x %d replays" % (max(4, len(it["sets"])), len(per))
+        else:
+            n = int(max(3, min(20, 1000.0 / max(probe[i][0], 1e-3))))
+            _, per2 = time_steps([it], n, stream)
+            per = per2[0]
+            how = "%d launches, events per launch" % n
+        ms = statistics.median(per)
         r = roofline_for(it, ms, peaks, False)
         res.append({"product": it["name"], "algorithm": it["plan"].algorithm,
-                    "ms_per_launch": ms, "launches": n, "achieved": r["achieved"],
+                    "ms_per_launch": ms, "timing": how, "achieved": r["achieved"],
                     "unit": r["unit"], "frac": r["frac"], "bound": r["bound"],
                     "peak": r["peak"]})
     for it in items:

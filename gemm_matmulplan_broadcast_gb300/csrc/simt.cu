@@ -9,19 +9,34 @@
 // keeps a TM x TN register tile.  Every output sums its K products in
 // ascending k with fused multiply-adds in the accumulator type (float32 for
 // FLOAT/FLOAT16/BFLOAT16, float64 for DOUBLE).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace olc {
 
 __device__ unsigned int g_device_error = 0;
 
+// Looked up once per device (not on every launch, so launches can be
+// captured into CUDA graphs without runtime symbol queries).
 unsigned int* device_error_word() {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) {
+    static std::mutex mu;
+    static void* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         return nullptr;
     }
-    return static_cast<unsigned int*>(ptr);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = ptr;
+    }
+    return static_cast<unsigned int*>(cache[dev]);
 }
 
 cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream) {

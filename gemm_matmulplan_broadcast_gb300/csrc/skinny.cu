@@ -8,6 +8,8 @@
 // Both are bound by HBM bandwidth (arithmetic intensity of a few flop/byte),
 // so the kernels are built around wide coalesced loads and enough loads in
 // flight, not around arithmetic.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace olc {
@@ -433,9 +435,13 @@ static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const size_t smem = sizeof(typename Num<T>::acc_t) * NC * Cfg::KC;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(skinny_n_kernel<T, NC>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        static std::once_flag once;
+        static cudaError_t attr = cudaSuccess;
+        std::call_once(once, [&] {
+            attr = cudaFuncSetAttribute(skinny_n_kernel<T, NC>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        });
+        if (attr != cudaSuccess) return attr;
     }
     skinny_n_kernel<T, NC><<<(unsigned)blocks, 256, smem, s>>>(p, groups);
     return cudaGetLastError();

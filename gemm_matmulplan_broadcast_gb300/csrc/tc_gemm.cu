@@ -110,6 +110,7 @@ struct Params {
     int group;                // slices per first-level reduction group
     int groups;               // ceil(splits / group)
     int64_t kb_per_split;     // k-blocks per slice
+    uint32_t stage_tx_bytes;  // bytes the TMA loads of one stage deliver
     float* part1;             // [tiles][splits][BM][BN] float32 partial tiles
     float* part2;             // [tiles][groups][BM][BN] group sums
     unsigned int* cnt1;       // [tiles][groups] arrivals per group
@@ -429,6 +430,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
             uint32_t stage = 0, phase = 0;
             uint32_t armed_parity[STAGES];
             bool armed[STAGES];
@@ -449,7 +452,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     unsigned char* sa = base + stage * C::STAGE_BYTES;
                     unsigned char* sb = sa + A_STAGE_BYTES;
-                    mbar_arrive_expect_tx(&s->full[stage], C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(&s->full[stage], p.stage_tx_bytes);
                     armed[stage] = true;
                     armed_parity[stage] = phase;
                     const int k0 = (int)(kb * BK);
@@ -799,8 +802,12 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
     const int bf = dt == OLC_BFLOAT16;
+    // A with fewer rows than one tile: load only its rows (rounded up to a
+    // whole 8-row swizzle group); the MMA's remaining rows of the stage hold
+    // stale data and feed only output rows that are never stored
+    const uint32_t a_box_rows = (!SWAP && pr.M < BM) ? (uint32_t)ceil_div(pr.M, 8) * 8 : BM;
     if (!SWAP) {
-        if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>()))
             return cudaErrorInvalidValue;
@@ -834,6 +841,8 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     p.group = 1;
     p.groups = 1;
     p.kb_per_split = p.k_blocks;
+    p.stage_tx_bytes = SWAP ? (uint32_t)(A_STAGE_BYTES + BN * BK * 2)
+                            : (uint32_t)(a_box_rows * BK * 2 + C::B_STAGE_BYTES);
     if (SPLIT) {
         if (!sp || !ws || !ws->partials || !ws->counters || sp->splits < 2)
             return cudaErrorInvalidValue;
