@@ -89,6 +89,7 @@ def load():
             "olc_matmul_plan_launches": ([vp], ctypes.c_int),
             "olc_matmul_plan_set_splits": ([vp, ctypes.c_int], ctypes.c_int),
             "olc_matmul_plan_splits": ([vp], ctypes.c_int),
+            "olc_matmul_plan_set_tc_variant": ([vp, ctypes.c_int], ctypes.c_int),
             "olc_matmul_plan_workspace_bytes": ([vp], ctypes.c_size_t),
             "olc_matmul_plan_describe": ([vp, ctypes.c_char_p, ctypes.c_size_t], ctypes.c_int),
             "olc_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -212,6 +213,12 @@ class Plan:
     def set_splits(self, splits: int):
         """Tuning override of the K-slice count (0 = automatic)."""
         _check(self.lib.olc_matmul_plan_set_splits(self._h, int(splits)), "set_splits")
+        return self
+
+    def set_tc_variant(self, variant: int):
+        """Tuning override of the tensor-core tiling: 0 automatic, 1 one CTA
+        per 128 x 256 tile, 2 CTA pairs with 256 x 256 tiles."""
+        _check(self.lib.olc_matmul_plan_set_tc_variant(self._h, int(variant)), "set_tc_variant")
         return self
 
     @property

@@ -42,6 +42,7 @@ struct olc_matmul_plan {
     bool forced;
     int splits;                  // SPLIT_K slices or SKINNY_M K-slices
     int split_hint;              // tuning override of the slice count (0 = automatic)
+    int tc_variant;              // tuning override of the tensor-core tiling (0 = automatic)
     int device;                  // -1: planned without a device
     int sm_count;
     void* workspace;
@@ -279,7 +280,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         case OLC_ALGO_SPLIT_K:
             e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
             break;
-        case OLC_ALGO_GENERAL_TC: e = launch_general_tc(dt, pr, p->sm_count, s); break;
+        case OLC_ALGO_GENERAL_TC: e = launch_general_tc(dt, pr, p->sm_count, s, p->tc_variant); break;
         default: return OLC_ERR_INVALID;
     }
     return from_cuda(e);
@@ -511,6 +512,13 @@ olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits) {
 }
 
 int olc_matmul_plan_splits(const olc_matmul_plan* plan) { return plan ? plan->splits : -1; }
+
+olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant) {
+    if (!plan) return OLC_ERR_NULL;
+    if (variant < 0 || variant > 2) return OLC_ERR_INVALID;
+    plan->tc_variant = variant;
+    return OLC_OK;
+}
 
 int olc_matmul_plan_launches(const olc_matmul_plan* plan) {
     if (!plan) return -1;

@@ -89,7 +89,10 @@ int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count);
 
 // GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
-cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+// variant: 0 automatic, 1 one CTA per 128 x 256 tile, 2 CTA pairs (cta_group::2)
+// with 256 x 256 tiles
+cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream,
+                              int variant);
 // the same kernel with 16-column tiles (N <= 16): the tensor-core skinny-N
 cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
 // the same kernel in split-K mode (K slices per tile, two-level fixed-order

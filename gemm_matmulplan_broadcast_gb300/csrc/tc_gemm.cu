@@ -410,11 +410,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(&s->tmem_base, C::TMEM_COLS);
-    tc_fence_before();
+    // barriers visible to every warp; the producer starts loading right away
+    // while warp 1 allocates TMEM and hands the address to the epilogue warps
+    // through named barrier 2 (warps 1..5)
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = s->tmem_base;
+    uint32_t tmem_base = 0;
+    if (warp == 1) tmem_alloc(&s->tmem_base, C::TMEM_COLS);
+    if (warp >= 1) {
+        tc_fence_before();
+        asm volatile("bar.sync 2, %0;" ::"n"(THREADS - 32) : "memory");
+        tc_fence_after();
+        tmem_base = s->tmem_base;
+    }
 
     // one reduced float4 of a tile (entries e4*4 .. e4*4+3 of the BM x BN
     // partial layout) to Y
@@ -690,6 +697,278 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 }
 
 // ---------------------------------------------------------------------------
+// 2-CTA variant (cta_group::2) for large FLOAT16 / BFLOAT16 products.
+//
+// A cluster of two CTAs on one TPC computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256): CTA rank r stages A rows
+// m0 + 128 r .. +127 and B columns n0 + 128 r .. +127 in its own shared
+// memory, the leader (rank 0) issues the MMAs that read both CTAs' halves,
+// and each CTA's TMEM receives its own 128 rows x 256 columns.  Per SM that
+// is 32 KB of operands per 64-deep K block instead of 48 KB, so 6 stages fit
+// where the 1-CTA kernel has 4.
+//
+// Synchronisation: both CTAs' TMA loads complete on the leader's full[s]
+// barrier (armed once by the leader with both CTAs' bytes); the leader's MMA
+// commits multicast to empty[s] and acc_full[b] in both CTAs; both CTAs'
+// epilogue warps arrive on the leader's acc_empty[b] (8 arrivals).  Both
+// CTAs allocate and free TMEM with .cta_group::2, and meet at a cluster
+// barrier before exiting so no remote arrival targets a finished CTA.
+
+namespace pair {
+
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;               // this CTA's 128 rows of A
+constexpr int B_BYTES = 128 * BK * 2;               // this CTA's 128 columns of B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 32 KiB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
+constexpr int TMEM_COLS = 512;                       // two 256-column accumulators
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of `local` in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t map_to(const void* local, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// TMA load into this CTA's shared memory, completing on an mbarrier that may
+// be in the peer CTA (shared::cluster address)
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst_smem, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void mma2_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on the barrier at this offset in both CTAs of the pair once the
+// MMAs issued so far have completed
+__device__ __forceinline__ void commit2_both(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"((unsigned short)0x3)
+        : "memory");
+}
+
+// arrive on this CTA's own barrier once the MMAs issued so far have completed
+__device__ __forceinline__ void commit2_local(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+               const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem* s = reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+    volatile int* abort_flag = &s->abort_flag;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // pair tiles: 256 rows x 256 columns, persistent over the clusters
+    const int64_t ptm = ceil_div(p.M, 256), ptn = ceil_div(p.N, 256);
+    const int64_t per_item = ptm * ptn;
+    const int64_t total = per_item * p.items;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&s->full[i], 1);
+            mbar_init(&s->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s->acc_full[i], 1);
+            mbar_init(&s->acc_empty[i], 8);   // 4 epilogue warps in each CTA
+        }
+        mbar_init(&s->drain, 1);
+        s->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc2(&s->tmem_base, TMEM_COLS);
+    tc_fence_before();
+    cluster_sync();          // both CTAs' barriers initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = s->tmem_base;
+
+    auto coords = [&](int64_t t, int64_t& item, int64_t& mb, int64_t& nb) {
+        item = t / per_item;
+        const int64_t r = t % per_item;
+        const int64_t group_span = (int64_t)8 * ptn;      // 8 pair rows per raster group
+        const int64_t g = r / group_span;
+        const int64_t first = g * 8;
+        const int64_t gm = min64(ptm - first, 8);
+        const int64_t in = r % group_span;
+        mb = first + in % gm;
+        nb = in / gm;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_parity[STAGES];
+            bool armed[STAGES];
+            for (int i = 0; i < STAGES; ++i) armed[i] = false;
+            bool ok = true;
+            for (int64_t t = cluster_id(); t < total && ok; t += cluster_count()) {
+                int64_t item, mb, nb;
+                coords(t, item, mb, nb);
+                int64_t a_off, b_off;
+                batch_offsets(p.map, item, a_off, b_off);
+                const int a_item = (int)(a_off / p.a_item_elems);
+                const int b_item = (int)(b_off / p.b_item_elems);
+                const int m0 = (int)(mb * 256 + rank * 128), n0 = (int)(nb * 256 + rank * 128);
+                for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    unsigned char* sa = base + stage * STAGE_BYTES;
+                    unsigned char* sb = sa + A_BYTES;
+                    const uint32_t full_leader = map_to(&s->full[stage], 0);
+                    if (leader) {
+                        mbar_arrive_expect_tx(&s->full[stage], 2 * STAGE_BYTES);
+                        armed[stage] = true;
+                        armed_parity[stage] = phase;
+                    }
+                    const int k0 = (int)(kb * BK);
+                    tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
+                    tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
+                    tma_load_3d_pair(sb + 64 * BK * 2, &tmap_b, full_leader, n0 + 64, k0, b_item);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (*abort_flag && leader) {
+                for (int i = 0; i < STAGES; ++i)
+                    if (armed[i]) mbar_wait_drain(&s->full[i], armed_parity[i]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = instr_desc(p.is_bf16, 256, 256, 0, 1);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t t = cluster_id(); t < total && ok; t += cluster_count()) {
+                if (!mbar_wait(&s->acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * 256;
+                for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(base + stage * STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
+                        const uint64_t bd = smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
+                        mma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    commit2_both(&s->empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                commit2_both(&s->acc_full[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            commit2_local(&s->drain);
+            mbar_wait_drain(&s->drain, 0);
+        }
+    } else {
+        const int lane_group = warp & 3;
+        const int row_in_tile = lane_group * 32 + lane;
+        const uint32_t acc_empty_leader[2] = {map_to(&s->acc_empty[0], 0), map_to(&s->acc_empty[1], 0)};
+        uint32_t acc = 0, acc_phase = 0;
+        for (int64_t t = cluster_id(); t < total; t += cluster_count()) {
+            int64_t item, mb, nb;
+            coords(t, item, mb, nb);
+            if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
+            tc_fence_after();
+            const int64_t row = mb * 256 + rank * 128 + row_in_tile;
+            const bool row_ok = row < p.M;
+            const uint32_t t_base = tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * 256;
+            unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
+                                  ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
+#pragma unroll 1
+            for (int c = 0; c < 256; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + c, r);
+                const int64_t col = nb * 256 + c;
+                if (row_ok && col < p.N) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        packed[i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.is_bf16);
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
+                    const int64_t left = (p.N - col) / 8;
+                    const int groups = (int)(left < 4 ? left : 4);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q < groups)
+                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                                packed[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) remote_arrive(acc_empty_leader[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();          // no remote arrival may target a CTA that has left
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc2(tmem_base, TMEM_COLS);
+}
+
+}  // namespace pair
+
+// ---------------------------------------------------------------------------
 // host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -872,6 +1151,62 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     return cudaGetLastError();
 }
 
+static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
+    if (!tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31)) return cudaErrorInvalidValue;
+    int64_t a_items = 1, b_items = 1;
+    for (int d = 0; d < pr.map.rank; ++d) {
+        if (pr.map.a_stride[d])
+            a_items = max64(a_items, pr.map.a_stride[d] / (pr.M * pr.K) * pr.map.dims[d]);
+        if (pr.map.b_stride[d])
+            b_items = max64(b_items, pr.map.b_stride[d] / (pr.K * pr.N) * pr.map.dims[d]);
+    }
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof ma);
+    std::memset(&mb, 0, sizeof mb);
+    const int bf = dt == OLC_BFLOAT16;
+    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.M = pr.M;
+    p.N = pr.N;
+    p.K = pr.K;
+    p.items = pr.items;
+    p.k_blocks = ceil_div(pr.K, BK);
+    p.a_item_elems = pr.M * pr.K;
+    p.b_item_elems = pr.K * pr.N;
+    p.map = pr.map;
+    p.Y = pr.Y;
+    p.err = device_error_word();
+    p.is_bf16 = bf;
+    const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.items;
+    if (pairs <= 0) return cudaSuccess;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(pair::tc_pair_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel, ma, mb, p);
+}
+
 static double operand_bytes(const Problem& pr) {
     // A and B streamed once per item (upper bound for broadcast operands)
     return 2.0 * (double)(pr.M * pr.K + pr.K * pr.N) * (double)pr.items;
@@ -885,7 +1220,12 @@ bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K) {
     return N % 8 == 0 && K % 8 == 0 && N < (1LL << 31) && K < (1LL << 31);
 }
 
-cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
+cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
+                              int variant) {
+    // variant 2: CTA pairs with 256 x 256 tiles; 1: one CTA per 128 x 256
+    // tile; 0 (automatic): pairs when the product holds a full pair tile
+    const bool pair = variant == 2 || (variant == 0 && pr.M >= 256 && pr.N >= 256);
+    if (pair && sm_count >= 2) return tc::launch_pair(dt, pr, sm_count, s);
     return tc::launch_tc<256, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
 }
 

@@ -202,12 +202,19 @@ def test_tc_shapes(dtype, shapes):
 
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
-def test_tc_many_tiles_per_cta_sampled(dtype):
-    # 32 x 8 = 256 tiles of 128 x 256: more than one tile per CTA, both TMEM
-    # accumulators in use
+@pytest.mark.parametrize("variant", [1, 2])
+def test_tc_many_tiles_per_cta_sampled(dtype, variant):
+    # 32 x 8 = 256 tiles of 128 x 256 (128 pair tiles): more than one tile per
+    # CTA or CTA pair, both TMEM accumulators in use
     a, b = synth.operands((4096, 1024), (1024, 2048), dtype, synth.normal(1.0),
                           synth.normal(0.02), seed=10)
-    y, algo = gpu_matmul(a, b, dtype, "general_tc")
+    A, B = a.cuda(), b.cuda()
+    with Plan(a.shape, b.shape, dtype) as p:
+        p.force("general_tc")
+        p.set_tc_variant(variant)
+        Y = torch.empty(p.output_shape, dtype=A.dtype, device="cuda")
+        p.execute_checked(A, B, Y)
+    y = Y.cpu()
     rows = sample_rows(4096, extra=128)
     y_ref, s = oracle.gemm2d(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype,
                              rows=rows)
@@ -271,6 +278,47 @@ def test_tc_skinny_m(dtype, shapes):
     check_product(a, b, dtype, algorithm="skinny_m")
     ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=14)
     check_product(ai, bi, dtype, algorithm="skinny_m", exact=True)
+
+
+def _pair_product(a, b, dtype, exact=False):
+    """The product through the CTA-pair (cta_group::2) tensor-core kernel."""
+    A, B = a.cuda(), b.cuda()
+    with Plan(a.shape, b.shape, dtype) as p:
+        p.force("general_tc")
+        p.set_tc_variant(2)
+        n = int(np.prod(p.output_shape))
+        buf = torch.full((n + 64,), float("nan"), dtype=A.dtype, device="cuda")
+        Y = buf[:n].view(p.output_shape)
+        p.execute_checked(A, B, Y)
+        torch.cuda.synchronize()
+        assert torch.isnan(buf[n:].float()).all()
+    y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+    compare(Y.cpu(), y_ref, s, dtype, exact=exact)
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+def test_tc_pair_single_tile(dtype):
+    a, b = synth.operands((256, 64), (64, 256), dtype, synth.SMALL_INT, synth.SMALL_INT, seed=2)
+    _pair_product(a, b, dtype, exact=True)
+
+
+TC_PAIR_SHAPES = [
+    ((256, 128), (128, 512)),
+    ((300, 520), (520, 264)),          # M, N, K tails inside a pair tile
+    ((130, 64), (64, 136)),            # the peer CTA's rows and columns out of range
+    ((3, 1, 260, 64), (1, 2, 64, 264)),
+    ((1024, 2048), (2048, 1024)),      # several pair tiles per cluster
+]
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("shapes", TC_PAIR_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_tc_pair_shapes(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=15)
+    _pair_product(a, b, dtype)
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=15)
+    _pair_product(ai, bi, dtype, exact=True)
 
 
 # --------------------------------------------------------------------------
