@@ -200,6 +200,9 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
         p->splits = split_k_pick(dt, pr, p->sm_count);
         p->partial_bytes = split_k_partial_bytes(dt, pr, p->splits, p->sm_count);
         p->counter_count = split_k_counter_count(dt, pr, p->splits, p->sm_count);
+    } else if (p->algo == OLC_ALGO_SKINNY_N) {
+        p->partial_bytes = skinny_n_partial_bytes(dt, pr, p->sm_count);
+        p->counter_count = skinny_n_counter_count(dt, pr, p->sm_count);
     } else if (p->algo == OLC_ALGO_SKINNY_M) {
         p->splits = skinny_m_pick_split(dt, pr, p->sm_count);
         if (p->splits > 1) {
@@ -276,7 +279,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         case OLC_ALGO_SKINNY_M:
             e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
             break;
-        case OLC_ALGO_SKINNY_N: e = launch_skinny_n(dt, pr, p->sm_count, s); break;
+        case OLC_ALGO_SKINNY_N: e = launch_skinny_n(dt, pr, p->sm_count, workspace_of(p), s); break;
         case OLC_ALGO_SPLIT_K:
             e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
             break;

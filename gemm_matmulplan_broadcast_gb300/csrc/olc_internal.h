@@ -72,7 +72,10 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count);
 
 // SKINNY_N: N <= 16.
 int skinny_n_max_cols();
-cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
+                            cudaStream_t stream);
+size_t skinny_n_partial_bytes(olc_dtype dt, const Problem& p, int sm_count);
+size_t skinny_n_counter_count(olc_dtype dt, const Problem& p, int sm_count);
 
 // SPLIT_K: tiny output, long K.  Partials in fixed-order reduction.  FLOAT16 /
 // BFLOAT16 shapes with 16-byte row strides run on the tensor cores, the rest
@@ -93,8 +96,12 @@ bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
 // with 256 x 256 tiles
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream,
                               int variant);
-// the same kernel with 16-column tiles (N <= 16): the tensor-core skinny-N
-cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream);
+// the same kernel with 16-column tiles (N <= 16): the tensor-core skinny-N,
+// in stream-K shares when the row tiles alone leave SMs idle
+size_t tc_skinny_n_partial_bytes(const Problem& p, int sm_count);
+size_t tc_skinny_n_counter_count(const Problem& p, int sm_count);
+cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
+                               cudaStream_t stream);
 // the same kernel in split-K mode (K slices per tile, two-level fixed-order
 // reduction of float32 partial tiles)
 int tc_split_pick(const Problem& p, int sm_count);

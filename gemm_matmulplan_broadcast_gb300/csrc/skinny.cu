@@ -447,12 +447,24 @@ static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t s) {
+static bool skinny_n_on_tc(olc_dtype dt, const Problem& p) {
+    return (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K);
+}
+
+size_t skinny_n_partial_bytes(olc_dtype dt, const Problem& p, int sm_count) {
+    return skinny_n_on_tc(dt, p) ? tc_skinny_n_partial_bytes(p, sm_count) : 0;
+}
+
+size_t skinny_n_counter_count(olc_dtype dt, const Problem& p, int sm_count) {
+    return skinny_n_on_tc(dt, p) ? tc_skinny_n_counter_count(p, sm_count) : 0;
+}
+
+cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
+                            cudaStream_t s) {
     // FLOAT16 / BFLOAT16 with 16-byte row strides: stream A through the
     // tensor cores with 16-column tiles (8 FMAs per A element would need most
     // of the SIMT FMA rate at full HBM bandwidth)
-    if ((dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K))
-        return launch_skinny_n_tc(dt, p, sm_count, s);
+    if (skinny_n_on_tc(dt, p)) return launch_skinny_n_tc(dt, p, sm_count, ws, s);
     return dispatch_dtype(dt, [&](auto tag) {
         using T = decltype(tag);
         if (p.N <= 1) return launch_skinny_n_t<T, 1>(p, s);

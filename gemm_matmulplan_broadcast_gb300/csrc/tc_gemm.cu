@@ -111,6 +111,8 @@ struct Params {
     int groups;               // ceil(splits / group)
     int64_t kb_per_split;     // k-blocks per slice
     uint32_t stage_tx_bytes;  // bytes the TMA loads of one stage deliver
+    int stream;               // 1: stream-K shares (split instantiation only)
+    int64_t iterations;       // stream-K: total (tile, K block) iterations
     float* part1;             // [tiles][splits][BM][BN] float32 partial tiles
     float* part2;             // [tiles][groups][BM][BN] group sums
     unsigned int* cnt1;       // [tiles][groups] arrivals per group
@@ -303,14 +305,59 @@ __device__ __forceinline__ void tile_coords(const Params& p, int64_t t, int64_t&
     nb = in / gm;
 }
 
-// A work unit is one K slice of one output tile (one slice per tile unless
-// split-K): unit u -> tile u / splits, slice u % splits.
-__device__ __forceinline__ void unit_range(const Params& p, int64_t u, int64_t& tile,
-                                           int& slice, int64_t& kb0, int64_t& kb1) {
-    tile = u / p.splits;
-    slice = (int)(u % p.splits);
-    kb0 = (int64_t)slice * p.kb_per_split;
-    kb1 = min64(p.k_blocks, kb0 + p.kb_per_split);
+// The work of one CTA as a sequence of pieces (tile, K blocks kb0..kb1-1).
+// Unit mode: unit u = tile u / splits, slice u % splits, units dealt round
+// robin over the CTAs.  Stream-K mode: the tiles' K blocks laid end to end
+// form `iterations` steps; CTA c takes steps [c*I/G, (c+1)*I/G) and cuts them
+// at tile boundaries.  A tile cut between CTAs has `parts` contributors;
+// `slice` is this CTA's position among them (in K order).
+struct Cursor {
+    int64_t u;
+    int64_t it, it_end;
+};
+
+__device__ __forceinline__ int64_t share_begin(const Params& p, int64_t c) {
+    return c * p.iterations / (int64_t)gridDim.x;
+}
+
+// the CTA whose share holds step i
+__device__ __forceinline__ int64_t owner_of(const Params& p, int64_t i) {
+    int64_t c = i * (int64_t)gridDim.x / p.iterations;
+    while (c + 1 < (int64_t)gridDim.x && share_begin(p, c + 1) <= i) ++c;
+    while (c > 0 && share_begin(p, c) > i) --c;
+    return c;
+}
+
+__device__ __forceinline__ Cursor cursor_begin(const Params& p) {
+    Cursor c;
+    c.u = blockIdx.x;
+    c.it = p.stream ? share_begin(p, blockIdx.x) : 0;
+    c.it_end = p.stream ? share_begin(p, blockIdx.x + 1) : 0;
+    return c;
+}
+
+__device__ __forceinline__ bool cursor_next(const Params& p, Cursor& c, int64_t& tile, int& slice,
+                                            int64_t& kb0, int64_t& kb1, int& parts) {
+    if (!p.stream) {
+        if (c.u >= p.total_tiles * p.splits) return false;
+        tile = c.u / p.splits;
+        slice = (int)(c.u % p.splits);
+        kb0 = (int64_t)slice * p.kb_per_split;
+        kb1 = min64(p.k_blocks, kb0 + p.kb_per_split);
+        parts = p.splits;
+        c.u += gridDim.x;
+        return true;
+    }
+    if (c.it >= c.it_end) return false;
+    tile = c.it / p.k_blocks;
+    kb0 = c.it % p.k_blocks;
+    kb1 = min64(p.k_blocks, kb0 + (c.it_end - c.it));
+    c.it += kb1 - kb0;
+    const int64_t first = owner_of(p, tile * p.k_blocks);
+    const int64_t last = owner_of(p, (tile + 1) * p.k_blocks - 1);
+    slice = (int)(blockIdx.x - first);
+    parts = (int)(last - first + 1);
+    return true;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
@@ -390,7 +437,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem* s = reinterpret_cast<Smem*>(base + STAGES * C::STAGE_BYTES);
     volatile int* abort_flag = &s->abort_flag;
-    const int64_t total_units = p.total_tiles * p.splits;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -444,10 +490,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             bool armed[STAGES];
             for (int i = 0; i < STAGES; ++i) armed[i] = false;
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                int64_t tile, kb0, kb1;
-                int slice;
-                unit_range(p, u, tile, slice, kb0, kb1);
+            Cursor cur = cursor_begin(p);
+            int64_t tile, kb0, kb1;
+            int slice, parts;
+            while (ok && cursor_next(p, cur, tile, slice, kb0, kb1, parts)) {
                 int64_t item, mb, nb;
                 tile_coords(p, tile, item, mb, nb);
                 int64_t a_off, b_off;
@@ -494,10 +540,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                         : instr_desc(p.is_bf16, BM, BN, 0, 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                int64_t tile, kb0, kb1;
-                int slice;
-                unit_range(p, u, tile, slice, kb0, kb1);
+            Cursor cur = cursor_begin(p);
+            int64_t tile, kb0, kb1;
+            int slice, parts;
+            while (ok && cursor_next(p, cur, tile, slice, kb0, kb1, parts)) {
                 if (!mbar_wait(&s->acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
@@ -544,10 +590,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int row_in_tile = lane_group * 32 + lane;
         const int etid = threadIdx.x - 64;        // 0..127 across the epilogue warps
         uint32_t acc = 0, acc_phase = 0;
-        for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-            int64_t tile, kb0, kb1;
-            int slice;
-            unit_range(p, u, tile, slice, kb0, kb1);
+        Cursor cur = cursor_begin(p);
+        int64_t tile, kb0, kb1;
+        int slice, parts;
+        while (cursor_next(p, cur, tile, slice, kb0, kb1, parts)) {
             int64_t item, mb, nb;
             tile_coords(p, tile, item, mb, nb);
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
@@ -557,49 +603,52 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const bool row_ok = row < rows_total;
             const uint32_t t_base =
                 tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * C::ACC_COLS;
-            if (!SPLIT && SWAP) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x16(t_base, r);
-                if (row_ok) {
-                    unsigned short* y = static_cast<unsigned short*>(p.Y);
-#pragma unroll
-                    for (int m = 0; m < BN; ++m)
-                        if (m < p.M)
-                            y[(item * p.M + m) * p.N + row] =
-                                (unsigned short)(pack2(__uint_as_float(r[m]), 0.f, p.is_bf16) & 0xFFFFu);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
-            } else if (!SPLIT) {
-                unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
-                                      ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
-#pragma unroll 1
-                for (int c = 0; c < BN; c += CH) {
+            // the whole tile in this piece: narrow and store straight from TMEM
+            auto store_direct = [&]() {
+                if constexpr (SWAP) {
                     uint32_t r[32];
-                    if (CH == 32) tmem_ld_32x32b_x32(t_base + c, r);
-                    else tmem_ld_32x32b_x16(t_base + c, r);
-                    const int64_t col = nb * BN + c;
-                    if (row_ok && col < p.N) {
-                        uint32_t packed[16];
+                    tmem_ld_32x32b_x16(t_base, r);
+                    if (row_ok) {
+                        unsigned short* y = static_cast<unsigned short*>(p.Y);
 #pragma unroll
-                        for (int i = 0; i < CH / 2; ++i)
-                            packed[i] = pack2(__uint_as_float(r[2 * i]),
-                                              __uint_as_float(r[2 * i + 1]), p.is_bf16);
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
-                        // N is a multiple of 8: whole 16-byte groups only
-                        const int64_t left = (p.N - col) / 8;
-                        const int groups = (int)(left < CH / 8 ? left : CH / 8);
+                        for (int m = 0; m < BN; ++m)
+                            if (m < p.M)
+                                y[(item * p.M + m) * p.N + row] = (unsigned short)(
+                                    pack2(__uint_as_float(r[m]), 0.f, p.is_bf16) & 0xFFFFu);
+                    }
+                } else {
+                    unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
+                                          ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += CH) {
+                        uint32_t r[32];
+                        if (CH == 32) tmem_ld_32x32b_x32(t_base + c, r);
+                        else tmem_ld_32x32b_x16(t_base + c, r);
+                        const int64_t col = nb * BN + c;
+                        if (row_ok && col < p.N) {
+                            uint32_t packed[16];
 #pragma unroll
-                        for (int q = 0; q < CH / 8; ++q)
-                            if (q < groups)
-                                dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
-                                                    packed[4 * q + 2], packed[4 * q + 3]);
+                            for (int i = 0; i < CH / 2; ++i)
+                                packed[i] = pack2(__uint_as_float(r[2 * i]),
+                                                  __uint_as_float(r[2 * i + 1]), p.is_bf16);
+                            uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
+                            // N is a multiple of 8: whole 16-byte groups only
+                            const int64_t left = (p.N - col) / 8;
+                            const int groups = (int)(left < CH / 8 ? left : CH / 8);
+#pragma unroll
+                            for (int q = 0; q < CH / 8; ++q)
+                                if (q < groups)
+                                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                        packed[4 * q + 2], packed[4 * q + 3]);
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
+            };
+            if (!SPLIT || parts == 1) {
+                store_direct();
             } else {
                 // float32 partial tile of this slice -> part1[tile][slice]
                 float* mine = p.part1 + ((tile * p.splits + slice) * BM) * (int64_t)BN;
@@ -625,8 +674,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 // fixed two-level reduction tree: slices of one group summed
                 // in slice order by the group's last arrival, then the group
                 // sums in group order by the last group
-                const int g = slice / p.group;
-                const int gsize = min(p.group, p.splits - g * p.group);
+                // stream-K: one group holding the tile's contributors
+                const int g = p.stream ? 0 : slice / p.group;
+                const int gsize = p.stream ? parts : min(p.group, p.splits - g * p.group);
                 const int64_t rows_valid = min64(BM, rows_total - mb * BM);
                 const int64_t e4_count = rows_valid * BN / 4;
                 const int64_t tile_floats = (int64_t)BM * BN;
@@ -1017,7 +1067,41 @@ struct SplitPlan {
     int64_t kb_per_split = 0;
     int64_t tiles = 0;
     size_t part1_bytes = 0, part2_bytes = 0, counters = 0;
+    bool stream = false;       // stream-K shares instead of equal slices
+    int64_t grid = 0;          // stream-K: CTAs (one share each)
 };
+
+// Stream-K: `grid` CTAs share the tiles' K blocks equally; a tile cut
+// between CTAs has at most `splits` contributors, summed in K order by the
+// last one (one load batch, so at most SUM_BATCH contributors).
+template <int BN>
+static SplitPlan stream_plan(int64_t tiles, int64_t k_blocks, int sm_count) {
+    SplitPlan sp;
+    const int64_t iters = tiles * k_blocks;
+    const int64_t g = min64(sm_count, iters);
+    auto begin = [&](int64_t c) { return c * iters / g; };
+    auto owner = [&](int64_t i) {
+        int64_t c = i * g / iters;
+        while (c + 1 < g && begin(c + 1) <= i) ++c;
+        while (c > 0 && begin(c) > i) --c;
+        return c;
+    };
+    int64_t maxc = 1;
+    for (int64_t t = 0; t < tiles; ++t)
+        maxc = max64(maxc, owner((t + 1) * k_blocks - 1) - owner(t * k_blocks) + 1);
+    sp.stream = true;
+    sp.grid = g;
+    sp.splits = (int)maxc;
+    sp.group = (int)maxc;
+    sp.groups = 1;
+    sp.kb_per_split = k_blocks;
+    sp.tiles = tiles;
+    if (maxc > 1) {
+        sp.part1_bytes = (size_t)(tiles * maxc * (int64_t)BM * BN * 4);
+        sp.counters = (size_t)(tiles + tiles);
+    }
+    return sp;
+}
 
 // K slices per tile.  Units (tile, slice) run one per SM at a time; pick the
 // slice count whose units fill the last wave best, discounted by the extra
@@ -1123,7 +1207,7 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     p.stage_tx_bytes = SWAP ? (uint32_t)(A_STAGE_BYTES + BN * BK * 2)
                             : (uint32_t)(a_box_rows * BK * 2 + C::B_STAGE_BYTES);
     if (SPLIT) {
-        if (!sp || !ws || !ws->partials || !ws->counters || sp->splits < 2)
+        if (!sp || !ws || !ws->partials || !ws->counters || (sp->splits < 2 && !sp->stream))
             return cudaErrorInvalidValue;
         p.splits = sp->splits;
         p.group = sp->group;
@@ -1135,6 +1219,8 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
                       : nullptr;
         p.cnt1 = ws->counters;
         p.cnt2 = ws->counters + sp->tiles * sp->groups;
+        p.stream = sp->stream ? 1 : 0;
+        p.iterations = p.total_tiles * p.k_blocks;
     }
     if (p.total_tiles <= 0) return cudaSuccess;
 
@@ -1146,7 +1232,7 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t units = p.total_tiles * p.splits;
-    const int64_t grid = min64(units, (int64_t)sm_count);
+    const int64_t grid = p.stream ? sp->grid : min64(units, (int64_t)sm_count);
     tc_gemm_kernel<BN, SPLIT, SWAP><<<(unsigned)grid, THREADS, C::SMEM_BYTES, s>>>(ma, mb, p);
     return cudaGetLastError();
 }
@@ -1229,9 +1315,45 @@ cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cud
     return tc::launch_tc<256, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
 }
 
-cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
+// skinny-N: 16-column tiles; when the row tiles leave most SMs idle,
+// stream-K shares of the K blocks keep every SM streaming A
+static tc::SplitPlan tc_skinny_n_plan(const Problem& pr, int sm_count) {
+    const int64_t tiles = ceil_div(pr.M, tc::BM) * pr.items;
+    const int64_t kbs = ceil_div(pr.K, tc::BK);
+    // stream-K only when the row tiles fill at most half the SMs: with more
+    // tiles the stream is bound by DRAM, not by idle SMs, and the partials
+    // only add traffic
+    if (pr.split_hint == 1 || 2 * tiles > (int64_t)sm_count || kbs < 2) {
+        tc::SplitPlan none;
+        none.tiles = tiles;
+        return none;
+    }
+    tc::SplitPlan sp = tc::stream_plan<16>(tiles, kbs, sm_count);
+    if (sp.splits > tc::SUM_BATCH) {
+        tc::SplitPlan none;
+        none.tiles = tiles;
+        return none;
+    }
+    return sp;
+}
+
+size_t tc_skinny_n_partial_bytes(const Problem& pr, int sm_count) {
+    return tc_skinny_n_plan(pr, sm_count).part1_bytes;
+}
+
+size_t tc_skinny_n_counter_count(const Problem& pr, int sm_count) {
+    return tc_skinny_n_plan(pr, sm_count).counters;
+}
+
+cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
+                               cudaStream_t s) {
     if (pr.N > 16) return cudaErrorInvalidValue;
-    return tc::launch_tc<16, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
+    const tc::SplitPlan sp = tc_skinny_n_plan(pr, sm_count);
+    if (!sp.stream || sp.part1_bytes == 0)
+        return tc::launch_tc<16, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
+    if (ws.partial_bytes < sp.part1_bytes || ws.counter_count < sp.counters)
+        return cudaErrorInvalidValue;
+    return tc::launch_tc<16, true, false>(dt, pr, sm_count, s, &sp, &ws);
 }
 
 // ---- split-K on the tensor cores: tile width by N

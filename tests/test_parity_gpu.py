@@ -243,6 +243,8 @@ def test_tc_split_k(dtype, shapes):
 
 
 TC_SKINNY_N_SHAPES = [
+    ((4096, 1024), (1024, 8)),         # 32 row tiles: stream-K shares over the SMs
+    ((2, 2048, 512), (512, 16)),       # folded batch, stream-K
     ((256, 1024), (1024, 8)),
     ((1000, 520), (520, 16)),
     ((3, 200, 64), (64, 8)),
