@@ -205,16 +205,34 @@ struct Vec<double> {
     static constexpr int W = 2;
 };
 
+// Paired FP32 multiply-add (Blackwell fma.rn.f32x2): d = a * b + d on two
+// lanes of packed floats, one issue slot for two FMAs.
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f2(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void fma_f2(unsigned long long& d, unsigned long long a,
+                                       unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 template <typename T, int BM, int BN, int BK, int TM, int TN>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     using V = typename Vec<T>::type;
     constexpr int W = Vec<T>::W;
     constexpr int PAD = W;
     constexpr int HM = TM / 2, HN = TN / 2;
+    constexpr bool PAIRED = sizeof(T) == 4;      // FP32: accumulate with f32x2 FMAs
     static_assert(BM == 16 * TM && BN == 16 * TN, "16 x 16 threads");
-    static_assert((BM * BK) / W == 256 && (BK * BN) / W == 256, "one vector per thread per slice");
     static_assert(HM % W == 0 && HN % W == 0, "half tiles are whole vectors");
+    constexpr int AV = (BM * BK) / W / 256;      // A vectors per thread per slice
+    constexpr int BV = (BK * BN) / W / 256;      // B vectors per thread per slice
+    static_assert(AV * W * 256 == BM * BK && BV * W * 256 == BK * BN, "whole vectors per thread");
     __shared__ __align__(16) T As[2][BK][BM + PAD];
     __shared__ __align__(16) T Bs[2][BK][BN];
 
@@ -232,38 +250,54 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
 
     const int t = threadIdx.x;
     const int tx = t % 16, ty = t / 16;
-    // global -> register staging: one vector of A and one of B per thread
     constexpr int AVR = BK / W;                   // vectors per A row slice
-    const int a_row = t / AVR, a_k = (t % AVR) * W;
     constexpr int BVR = BN / W;                   // vectors per B row
-    const int b_row = t / BVR, b_col = (t % BVR) * W;
-    const int64_t ga_row = m0 + a_row;
-    const int64_t gb_col = n0 + b_col;
 
-    auto load_a = [&](int64_t k0, V& v) {
-        const int64_t k = k0 + a_k;
-        if (ga_row < M && k < K) v = *reinterpret_cast<const V*>(A + ga_row * K + k);
-        else v = V{};
-    };
-    auto load_b = [&](int64_t k0, V& v) {
-        const int64_t k = k0 + b_row;
-        if (k < K && gb_col < N) v = *reinterpret_cast<const V*>(B + k * N + gb_col);
-        else v = V{};
-    };
-    auto store_stage = [&](int buf, const V& va, const V& vb) {
-        const T* ae = reinterpret_cast<const T*>(&va);
+    auto load_a = [&](int64_t k0, V (&v)[AV]) {
 #pragma unroll
-        for (int i = 0; i < W; ++i) As[buf][a_k + i][a_row] = ae[i];
-        *reinterpret_cast<V*>(&Bs[buf][b_row][b_col]) = vb;
+        for (int q = 0; q < AV; ++q) {
+            const int e = t + q * 256;
+            const int64_t row = m0 + e / AVR, k = k0 + (e % AVR) * W;
+            if (row < M && k < K) v[q] = *reinterpret_cast<const V*>(A + row * K + k);
+            else v[q] = V{};
+        }
+    };
+    auto load_b = [&](int64_t k0, V (&v)[BV]) {
+#pragma unroll
+        for (int q = 0; q < BV; ++q) {
+            const int e = t + q * 256;
+            const int64_t k = k0 + e / BVR, col = n0 + (e % BVR) * W;
+            if (k < K && col < N) v[q] = *reinterpret_cast<const V*>(B + k * N + col);
+            else v[q] = V{};
+        }
+    };
+    auto store_stage = [&](int buf, const V (&va)[AV], const V (&vb)[BV]) {
+#pragma unroll
+        for (int q = 0; q < AV; ++q) {
+            const int e = t + q * 256;
+            const int row = e / AVR, kk = (e % AVR) * W;
+            const T* ae = reinterpret_cast<const T*>(&va[q]);
+#pragma unroll
+            for (int i = 0; i < W; ++i) As[buf][kk + i][row] = ae[i];
+        }
+#pragma unroll
+        for (int q = 0; q < BV; ++q) {
+            const int e = t + q * 256;
+            *reinterpret_cast<V*>(&Bs[buf][e / BVR][(e % BVR) * W]) = vb[q];
+        }
     };
 
     T acc[TM][TN];
+    unsigned long long acc2[TM][TN / 2];
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
+    for (int i = 0; i < TM; ++i) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = T(0);
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) acc2[i][j] = 0ull;   // +0.0f, +0.0f
+    }
 
-    V va, vb;
+    V va[AV], vb[BV];
     load_a(0, va);
     load_b(0, vb);
     store_stage(0, va, vb);
@@ -295,16 +329,39 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
                     for (int i = 0; i < W; ++i) b[h * HN + q * W + i] = e[i];
                 }
             }
+            if constexpr (PAIRED) {
+                unsigned long long b2[TN / 2];
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+                for (int j = 0; j < TN / 2; ++j) b2[j] = pack_f2(b[2 * j], b[2 * j + 1]);
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fma(a[i], b[j], acc[i][j]);
+                for (int i = 0; i < TM; ++i) {
+                    const unsigned long long a2 = pack_f2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < TN / 2; ++j) fma_f2(acc2[i][j], a2, b2[j]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fma(a[i], b[j], acc[i][j]);
+            }
         }
         if (more) {
             store_stage(buf ^ 1, va, vb);
             __syncthreads();
             buf ^= 1;
         }
+    }
+    if constexpr (PAIRED) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j) {
+                float lo, hi;
+                unpack_f2(acc2[i][j], lo, hi);
+                acc[i][2 * j] = lo;
+                acc[i][2 * j + 1] = hi;
+            }
     }
 
 #pragma unroll
@@ -354,7 +411,7 @@ static bool aligned_items(const Problem& p, int64_t elem) {
 }
 
 cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream) {
-    if (dt == OLC_FLOAT && aligned_items(p, 4)) return launch_fast<float, 128, 128, 8, 8, 8>(p, stream);
+    if (dt == OLC_FLOAT && aligned_items(p, 4)) return launch_fast<float, 128, 128, 16, 8, 8>(p, stream);
     if (dt == OLC_DOUBLE && aligned_items(p, 8)) return launch_fast<double, 64, 64, 8, 4, 4>(p, stream);
     return launch_general_simt_generic(dt, p, stream);
 }
