@@ -596,12 +596,17 @@ def run_reference(args):
     workload = synth.workload(args.workload)
     bw_bound = args.workload == "fp16_skinny_splitk"
     per_step = max(0.5, args.ref_step_seconds)
+    # operands drawn once (the same seeded inputs as the GPU arm)
+    drawn = []
+    for prod in workload.products:
+        a, b = prod.draw()
+        drawn.append({"name": prod.name, "a": a, "b": b})
     for _ in range(args.warmup):
-        cpu_oracle_sample(workload, per_step / 4)
+        cpu_oracle_sample(workload, per_step / 4, drawn)
     flops = secs = 0.0
     cores, desc = 1, ""
     for _ in range(args.steps):
-        f, s, cores, desc = cpu_oracle_sample(workload, per_step)
+        f, s, cores, desc = cpu_oracle_sample(workload, per_step, drawn)
         flops += f
         secs += s
     value = flops / secs / 1e12
