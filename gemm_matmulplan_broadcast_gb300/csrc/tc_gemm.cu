@@ -1019,6 +1019,239 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 }  // namespace pair
 
 // ---------------------------------------------------------------------------
+// Split-K for tiny outputs (M <= 32, N <= 32, FP16/BF16).
+//
+// A 128-row tcgen05 MMA would leave 3/4 of its rows idle here and its cost
+// per instruction does not shrink with N, so this kernel keeps the TMA
+// staging but multiplies with warp-level mma.sync.m16n8k16 (float32
+// accumulation): CTA s owns K slice s, one producer lane streams the
+// slice's 64-deep chunks (A: 32 rows x 128 bytes, 128-byte swizzle; B: 64
+// K-rows x 64 bytes, 64-byte swizzle) through a ring of full/empty
+// mbarriers, and four MMA warps each take one 16-deep step of every chunk
+// (ldmatrix on the swizzled layouts, ldmatrix.trans for B).  The four warps'
+// 32 x 32 sums are added in warp order, and the slices are reduced by the
+// same fixed two-level tree as the tensor-core split-K (slices of a group in
+// order by the group's last arrival, then the groups in order).
+
+namespace tiny {
+
+constexpr int ROWS = 32, COLS = 32;
+constexpr int A_CHUNK = ROWS * BK * 2;             // 4 KiB
+constexpr int B_CHUNK = BK * COLS * 2;             // 4 KiB
+constexpr int CHUNK = A_CHUNK + B_CHUNK;
+constexpr int STAGES = 24;
+constexpr int MMA_WARPS = 4;
+constexpr int THREADS_T = (MMA_WARPS + 1) * 32;    // + one producer warp
+constexpr int SMEM_BYTES = STAGES * CHUNK + MMA_WARPS * ROWS * (COLS + 1) * 4 + 1024 + 512;
+
+struct Bars {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    int abort_flag;
+    int last_flag;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, int is_bf16) {
+    if (is_bf16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(THREADS_T, 1)
+splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* red = reinterpret_cast<float*>(base + STAGES * CHUNK);      // [4][32][33]
+    Bars* s = reinterpret_cast<Bars*>(base + STAGES * CHUNK + MMA_WARPS * ROWS * (COLS + 1) * 4);
+    volatile int* abort_flag = &s->abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slice = blockIdx.x;
+    const int64_t kb0 = (int64_t)slice * p.kb_per_split;
+    const int64_t kb1 = min64(p.k_blocks, kb0 + p.kb_per_split);
+    const int nchunks = (int)(kb1 - kb0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&s->full[i], 1);
+            mbar_init(&s->empty[i], MMA_WARPS);
+        }
+        s->abort_flag = 0;
+        s->last_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == MMA_WARPS) {
+        // producer: one lane issues every chunk's two TMA loads
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            uint32_t armed_parity[STAGES];
+            bool armed[STAGES];
+            for (int i = 0; i < STAGES; ++i) armed[i] = false;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c % STAGES;
+                const uint32_t ph = (uint32_t)(c / STAGES) & 1u;
+                if (!mbar_wait(&s->empty[st], ph ^ 1, abort_flag, p.err)) break;
+                unsigned char* sa = base + st * CHUNK;
+                mbar_arrive_expect_tx(&s->full[st], CHUNK);
+                armed[st] = true;
+                armed_parity[st] = ph;
+                const int k0 = (int)((kb0 + c) * BK);
+                tma_load_3d(sa, &tmap_a, &s->full[st], k0, 0, 0);
+                tma_load_3d(sa + A_CHUNK, &tmap_b, &s->full[st], 0, k0, 0);
+            }
+            if (*abort_flag)
+                for (int i = 0; i < STAGES; ++i)
+                    if (armed[i]) mbar_wait_drain(&s->full[i], armed_parity[i]);
+        }
+    } else {
+        // MMA warps: warp w takes the 16-deep step w of every chunk
+        float acc[2][4][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
+        const int q = lane >> 3, r8 = lane & 7;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % STAGES;
+            const uint32_t ph = (uint32_t)(c / STAGES) & 1u;
+            if (!mbar_wait(&s->full[st], ph, abort_flag, p.err)) break;
+            const uint32_t a_base = smem_u32(base + st * CHUNK);
+            const uint32_t b_base = a_base + A_CHUNK;
+            uint32_t a[2][4], b[2][4];
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+                // rows mb*16 + (q&1)*8 + r8, 16-byte chunk 2*warp + (q>>1); 128-byte swizzle
+                const int r = mb * 16 + (q & 1) * 8 + r8;
+                const int kc = warp * 2 + (q >> 1);
+                ldsm_x4(a_base + r * 128 + ((kc ^ (r & 7)) << 4), a[mb]);
+            }
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                // K rows warp*16 + (q&1)*8 + r8, 16-byte chunk 2*np + (q>>1); 64-byte swizzle
+                const int kr = warp * 16 + (q & 1) * 8 + r8;
+                const int nc = np * 2 + (q >> 1);
+                ldsm_x4_t(b_base + kr * 64 + ((nc ^ ((kr >> 1) & 3)) << 4), b[np]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s->empty[st]);
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                for (int nb = 0; nb < 4; ++nb)
+                    mma16816(acc[mb][nb], a[mb], b[nb >> 1][(nb & 1) * 2], b[nb >> 1][(nb & 1) * 2 + 1],
+                             p.is_bf16);
+        }
+        // this warp's 32 x 32 sums -> red[warp]
+        float* mine = red + warp * ROWS * (COLS + 1);
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int nb = 0; nb < 4; ++nb) {
+                const int row = mb * 16 + (lane >> 2), col = nb * 8 + 2 * (lane & 3);
+                mine[row * (COLS + 1) + col] = acc[mb][nb][0];
+                mine[row * (COLS + 1) + col + 1] = acc[mb][nb][1];
+                mine[(row + 8) * (COLS + 1) + col] = acc[mb][nb][2];
+                mine[(row + 8) * (COLS + 1) + col + 1] = acc[mb][nb][3];
+            }
+        epi_sync();
+        // slice sum in warp order -> part1[slice]
+        const int tid = threadIdx.x;                  // 0..127
+        float* P = p.part1 + (int64_t)slice * ROWS * COLS;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + e * 128;
+            const int row = idx / COLS, col = idx % COLS;
+            float v = red[row * (COLS + 1) + col];
+#pragma unroll
+            for (int w = 1; w < MMA_WARPS; ++w) v += red[w * ROWS * (COLS + 1) + row * (COLS + 1) + col];
+            P[idx] = v;
+        }
+        // two-level fixed-order reduction over the slices
+        const int g = slice / p.group;
+        const int gsize = min(p.group, p.splits - g * p.group);
+        const int64_t tile_floats = (int64_t)ROWS * COLS;
+        const int64_t e4 = tid, e4b = tid + 128;      // 256 float4s per partial
+        auto store_y = [&](int64_t e, float4 v) {
+            const int row = (int)((e * 4) / COLS), col = (int)((e * 4) % COLS);
+            if (row < p.M && col < p.N) {
+                uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
+                *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) + ((int64_t)row * p.N + col) * 2) = o;
+            }
+        };
+        __threadfence();
+        epi_sync();
+        if (tid == 0) {
+            const unsigned int prev = atomicAdd(p.cnt1 + g, 1u);
+            s->last_flag = (prev == (unsigned int)gsize - 1) ? 1 : 0;
+        }
+        epi_sync();
+        const int last1 = s->last_flag;
+        epi_sync();
+        if (last1) {
+            __threadfence();
+            const float* first = p.part1 + (int64_t)g * p.group * tile_floats;
+            float4 v0, v1;
+            ordered_sum4x2(first, tile_floats, gsize, e4, e4b, v0, v1);
+            if (p.groups == 1) {
+                store_y(e4, v0);
+                store_y(e4b, v1);
+                if (tid == 0) p.cnt1[g] = 0u;
+            } else {
+                float* gsum = p.part2 + (int64_t)g * tile_floats;
+                reinterpret_cast<float4*>(gsum)[e4] = v0;
+                reinterpret_cast<float4*>(gsum)[e4b] = v1;
+                __threadfence();
+                epi_sync();
+                if (tid == 0) {
+                    p.cnt1[g] = 0u;
+                    const unsigned int prev = atomicAdd(p.cnt2, 1u);
+                    s->last_flag = (prev == (unsigned int)p.groups - 1) ? 1 : 0;
+                }
+                epi_sync();
+                const int last2 = s->last_flag;
+                epi_sync();
+                if (last2) {
+                    __threadfence();
+                    ordered_sum4x2(p.part2, tile_floats, p.groups, e4, e4b, v0, v1);
+                    store_y(e4, v0);
+                    store_y(e4b, v1);
+                    if (tid == 0) p.cnt2[0] = 0u;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace tiny
+
+// ---------------------------------------------------------------------------
 // host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1293,6 +1526,73 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel, ma, mb, p);
 }
 
+// Split-K plan and launch for tiny outputs: one slice per CTA, about one
+// CTA per SM, at most SUM_BATCH^2 slices, slices of at least 2 chunks.
+static SplitPlan tiny_plan(const Problem& pr, int sm_count) {
+    SplitPlan sp;
+    const int64_t kbs = ceil_div(pr.K, BK);
+    int64_t want = min64((int64_t)sm_count, (int64_t)SUM_BATCH * SUM_BATCH);
+    want = min64(want, max64(1, kbs / 2));
+    if (pr.split_hint > 0) want = min64(pr.split_hint, min64(kbs, (int64_t)SUM_BATCH * SUM_BATCH));
+    sp.kb_per_split = ceil_div(kbs, want);
+    sp.splits = (int)ceil_div(kbs, sp.kb_per_split);
+    int g = 1;
+    while ((int64_t)g * g < sp.splits) ++g;
+    sp.group = g < SUM_BATCH ? g : SUM_BATCH;
+    sp.groups = (int)ceil_div(sp.splits, sp.group);
+    sp.tiles = 1;
+    const int64_t tile_bytes = (int64_t)tiny::ROWS * tiny::COLS * 4;
+    sp.part1_bytes = (size_t)(sp.splits * tile_bytes);
+    sp.part2_bytes = sp.groups > 1 ? (size_t)(sp.groups * tile_bytes) : 0;
+    sp.counters = (size_t)(sp.groups + 1);
+    return sp;
+}
+
+static cudaError_t launch_tiny(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
+                               cudaStream_t s) {
+    const SplitPlan sp = tiny_plan(pr, sm_count);
+    if (ws.partial_bytes < sp.part1_bytes + sp.part2_bytes || ws.counter_count < sp.counters ||
+        !ws.partials || !ws.counters)
+        return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof ma);
+    std::memset(&mb, 0, sizeof mb);
+    const int bf = dt == OLC_BFLOAT16;
+    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, 1, BK, tiny::ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, 1, tiny::COLS, BK, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.M = pr.M;
+    p.N = pr.N;
+    p.K = pr.K;
+    p.items = 1;
+    p.k_blocks = ceil_div(pr.K, BK);
+    p.Y = pr.Y;
+    p.err = device_error_word();
+    p.is_bf16 = bf;
+    p.splits = sp.splits;
+    p.group = sp.group;
+    p.groups = sp.groups;
+    p.kb_per_split = sp.kb_per_split;
+    p.part1 = static_cast<float*>(ws.partials);
+    p.part2 = sp.groups > 1
+                  ? reinterpret_cast<float*>(static_cast<char*>(ws.partials) + sp.part1_bytes)
+                  : nullptr;
+    p.cnt1 = ws.counters;
+    p.cnt2 = ws.counters + sp.groups;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(tiny::splitk_tiny_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tiny::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    tiny::splitk_tiny_kernel<<<sp.splits, tiny::THREADS_T, tiny::SMEM_BYTES, s>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
 static double operand_bytes(const Problem& pr) {
     // A and B streamed once per item (upper bound for broadcast operands)
     return 2.0 * (double)(pr.M * pr.K + pr.K * pr.N) * (double)pr.items;
@@ -1359,7 +1659,11 @@ cudaError_t launch_skinny_n_tc(olc_dtype dt, const Problem& pr, int sm_count, co
 // ---- split-K on the tensor cores: tile width by N
 static int tc_split_bn(int64_t N) { return N <= 16 ? 16 : (N <= 32 ? 32 : 256); }
 
+// outputs of at most 32 x 32 (one item): the mma.sync split-K kernel
+static bool tc_split_tiny(const Problem& pr) { return pr.M <= 32 && pr.N <= 32 && pr.items == 1; }
+
 static tc::SplitPlan tc_split_plan(const Problem& pr, int sm_count) {
+    if (tc_split_tiny(pr)) return tc::tiny_plan(pr, sm_count);
     const int bn = tc_split_bn(pr.N);
     const int64_t tiles = ceil_div(pr.M, tc::BM) * ceil_div(pr.N, bn) * pr.items;
     const int64_t kbs = ceil_div(pr.K, tc::BK);
@@ -1384,6 +1688,7 @@ size_t tc_split_counter_count(const Problem& pr, int sm_count) {
 
 cudaError_t launch_tc_split(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
                             cudaStream_t s) {
+    if (tc_split_tiny(pr)) return tc::launch_tiny(dt, pr, sm_count, ws, s);
     const tc::SplitPlan sp = tc_split_plan(pr, sm_count);
     if (sp.splits < 2) {
         // a K too short to split: the plain tile kernel of the same width
