@@ -75,7 +75,8 @@ def _load():
             return _lib
         lib = ctypes.CDLL(build())
         i64, p = ctypes.c_int64, ctypes.c_void_p
-        for name in ("oracle_gemm_f32", "oracle_gemm_f64", "oracle_gemm_f16", "oracle_gemm_bf16"):
+        for name in ("oracle_gemm_f32", "oracle_gemm_f64", "oracle_gemm_f16", "oracle_gemm_bf16",
+                     "oracle_gemm_f16_acc", "oracle_gemm_bf16_acc"):
             fn = getattr(lib, name)
             fn.argtypes = [i64, i64, i64, p, p, p, i64, p, p]
             fn.restype = None
@@ -232,3 +233,71 @@ def to_float64(y: np.ndarray, dtype: str) -> np.ndarray:
     if dtype in ("float16", "bfloat16"):
         return decode(y, dtype).astype(np.float64)
     return y.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# the Gemm operator (rank-2, transA / transB, alpha, beta, broadcast C)
+#
+# "Gemm and MatMul Performance Roadmap", section "Scope and type matrix":
+# Gemm handles rank-2 inputs, alpha, beta, an optional broadcast bias and
+# transA / transB, on the same engine as MatMul.  It computes
+#     Y = alpha * A' B' + beta * C,   A' = A^T if transA else A,  B' likewise,
+# with C broadcast unidirectionally to [M, N] (absent C: no bias term).
+# Reading where the page is silent: the epilogue alpha * acc + beta * c is
+# evaluated in the accumulator type (float32 for FLOAT, FLOAT16, BFLOAT16;
+# float64 for DOUBLE), each operation rounded, and FLOAT16 / BFLOAT16 are
+# narrowed once at the end.
+
+
+def gemm_output_shape(a_shape, b_shape, trans_a, trans_b, c_shape=None):
+    """(M, N, K) of Gemm, or ShapeError."""
+    if len(a_shape) != 2 or len(b_shape) != 2:
+        raise ShapeError("Gemm takes rank-2 A and B")
+    if any(int(d) < 0 for d in tuple(a_shape) + tuple(b_shape)):
+        raise ShapeError("negative dimension")
+    m, ka = (a_shape[1], a_shape[0]) if trans_a else (a_shape[0], a_shape[1])
+    kb, n = (b_shape[1], b_shape[0]) if trans_b else (b_shape[0], b_shape[1])
+    if ka != kb:
+        raise ShapeError("inner dimensions differ: %d vs %d" % (ka, kb))
+    if c_shape is not None:
+        c = [int(d) for d in c_shape]
+        if len(c) > 2:
+            raise ShapeError("C has rank > 2")
+        c = [1] * (2 - len(c)) + c
+        if not (c[0] in (1, m) and c[1] in (1, n)):
+            raise ShapeError("C %s does not broadcast to [%d, %d]" % (tuple(c_shape), m, n))
+    return int(m), int(n), int(ka)
+
+
+def gemm_op(a, b, dtype, c=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=False):
+    """ONNX Gemm.  Returns (Y, S) with S = |alpha| sum|a||b| + |beta| |c|
+    (float64), the tolerance scale."""
+    m, n, k = gemm_output_shape(a.shape, b.shape, trans_a, trans_b,
+                                None if c is None else c.shape)
+    ap = np.ascontiguousarray(a.T if trans_a else a)
+    bp = np.ascontiguousarray(b.T if trans_b else b)
+    lib = _load()
+    half = dtype in ("float16", "bfloat16")
+    wide = np.float64 if dtype == "float64" else np.float32
+    if half:
+        acc = np.zeros((m, n), np.float32)
+        s = np.zeros((m, n), np.float64)
+        if m and n:
+            fn = lib.oracle_gemm_f16_acc if dtype == "float16" else lib.oracle_gemm_bf16_acc
+            ap16 = np.ascontiguousarray(ap, np.uint16)
+            bp16 = np.ascontiguousarray(bp, np.uint16)
+            fn(m, n, k, _ptr(ap16), _ptr(bp16), None, m, _ptr(acc), _ptr(s))
+    else:
+        acc, s = gemm2d(ap, bp, dtype)
+        acc = acc.astype(wide)
+    y = wide(alpha) * acc
+    scale = abs(float(alpha)) * s
+    if c is not None:
+        cv = to_float64(np.asarray(c), dtype).astype(wide) if half else np.asarray(c, wide)
+        cb = np.broadcast_to(cv.reshape([1] * (2 - cv.ndim) + list(cv.shape)), (m, n))
+        y = y + wide(beta) * cb
+        scale = scale + abs(float(beta)) * np.abs(cb.astype(np.float64))
+    y = np.asarray(y, wide)
+    if half:
+        return encode(y.astype(np.float32), dtype), scale
+    return y, scale

@@ -203,9 +203,11 @@ void oracle_gemm_f64(int64_t M, int64_t N, int64_t K, const double* A, const dou
 }
 
 /* Shared body of the two 16-bit products: widen, accumulate in float32,
- * narrow once.  `kind` 0 = binary16, 1 = bfloat16. */
+ * narrow once.  `kind` 0 = binary16, 1 = bfloat16.  With Y == NULL the
+ * float32 accumulators are returned in Yacc instead (not narrowed), for the
+ * Gemm operator, which narrows only after its alpha/beta epilogue. */
 static void gemm_half(int kind, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
-                      const int64_t* rows, int64_t nrows, uint16_t* Y, double* S) {
+                      const int64_t* rows, int64_t nrows, uint16_t* Y, double* S, float* Yacc) {
     float (*widen)(uint16_t) = kind ? oracle_bf16_to_f32 : oracle_f16_to_f32;
     uint16_t (*narrow)(float) = kind ? oracle_f32_to_bf16 : oracle_f32_to_f16;
     /* B widened once; widening is exact, so this is the same B. */
@@ -228,7 +230,10 @@ static void gemm_half(int kind, int64_t N, int64_t K, const uint16_t* A, const u
                     s[j] += fabs((double)a) * fabs((double)brow[j]);
                 }
             }
-            for (int64_t j = 0; j < N; ++j) Y[r * N + j] = narrow(acc[j]);
+            for (int64_t j = 0; j < N; ++j) {
+                if (Y) Y[r * N + j] = narrow(acc[j]);
+                else Yacc[r * N + j] = acc[j];
+            }
         }
         free(acc);
     }
@@ -238,11 +243,24 @@ static void gemm_half(int kind, int64_t N, int64_t K, const uint16_t* A, const u
 void oracle_gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
                      const int64_t* rows, int64_t nrows, uint16_t* Y, double* S) {
     (void)M;
-    gemm_half(0, N, K, A, B, rows, nrows, Y, S);
+    gemm_half(0, N, K, A, B, rows, nrows, Y, S, NULL);
 }
 
 void oracle_gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
                       const int64_t* rows, int64_t nrows, uint16_t* Y, double* S) {
     (void)M;
-    gemm_half(1, N, K, A, B, rows, nrows, Y, S);
+    gemm_half(1, N, K, A, B, rows, nrows, Y, S, NULL);
+}
+
+/* The 16-bit products' float32 accumulators, not narrowed (Gemm epilogue). */
+void oracle_gemm_f16_acc(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                         const int64_t* rows, int64_t nrows, float* Yacc, double* S) {
+    (void)M;
+    gemm_half(0, N, K, A, B, rows, nrows, NULL, S, Yacc);
+}
+
+void oracle_gemm_bf16_acc(int64_t M, int64_t N, int64_t K, const uint16_t* A, const uint16_t* B,
+                          const int64_t* rows, int64_t nrows, float* Yacc, double* S) {
+    (void)M;
+    gemm_half(1, N, K, A, B, rows, nrows, NULL, S, Yacc);
 }
