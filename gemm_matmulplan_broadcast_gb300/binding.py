@@ -73,6 +73,10 @@ def load():
             "olc_matmul_plan_create": ([i64p, ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(vp)], ctypes.c_int),
             "olc_matmul_plan_destroy": ([vp], None),
+            "olc_gemm_plan_create": ([i64p, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                      ctypes.c_double, i64p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(vp)], ctypes.c_int),
+            "olc_gemm_execute": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute_checked": ([vp, vp, ctypes.c_int64, vp, ctypes.c_int64, vp,
                                             ctypes.c_int64, vp], ctypes.c_int),
@@ -289,6 +293,52 @@ class Plan:
         if out is None:
             out = torch.empty(self.output_shape, dtype=A.dtype, device=A.device)
         return self.execute(A, B, out, stream)
+
+
+class GemmPlan(Plan):
+    """A Gemm plan: Y = alpha * A' B' + beta * C (rank-2, transA / transB,
+    C broadcast to [M, N]; c_shape None = no C)."""
+
+    def __init__(self, a_shape, b_shape, dtype: str, trans_a=False, trans_b=False, alpha=1.0,
+                 beta=1.0, c_shape=None):
+        self.lib = load()
+        self.a_shape = tuple(int(d) for d in a_shape)
+        self.b_shape = tuple(int(d) for d in b_shape)
+        if dtype not in DTYPE_CODES:
+            raise ValueError("unsupported dtype %r" % (dtype,))
+        if len(self.a_shape) != 2 or len(self.b_shape) != 2:
+            raise ValueError("Gemm takes rank-2 A and B")
+        self.dtype = dtype
+        self.trans_a, self.trans_b = bool(trans_a), bool(trans_b)
+        self.c_shape = None if c_shape is None else tuple(int(d) for d in c_shape)
+        h = ctypes.c_void_p()
+        c_rank = -1 if self.c_shape is None else len(self.c_shape)
+        st = self.lib.olc_gemm_plan_create(
+            _shape_arr(self.a_shape), _shape_arr(self.b_shape), int(self.trans_a),
+            int(self.trans_b), float(alpha), float(beta),
+            _shape_arr(self.c_shape or ()), c_rank, DTYPE_CODES[dtype], ctypes.byref(h))
+        _check(st, "olc_gemm_plan_create")
+        self._h = h
+
+    def execute(self, A, B, Y, stream=None, C=None):
+        """Enqueue the Gemm (device tensors) on ``stream``."""
+        self._check_tensors(A, B, Y)
+        st = self.lib.olc_gemm_execute(self._h, _ptr(A), _ptr(B), _ptr(C), _ptr(Y),
+                                       _stream_handle(stream))
+        _check(st, "olc_gemm_execute")
+        return Y
+
+
+def gemm(A, B, C=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=False, out=None, stream=None):
+    """ONNX Gemm of CUDA tensors through a fresh plan."""
+    import torch
+    from .synth import TORCH_DTYPES
+    inv = {v: k for k, v in TORCH_DTYPES.items()}
+    with GemmPlan(A.shape, B.shape, inv[A.dtype], trans_a, trans_b, alpha, beta,
+                  None if C is None else C.shape) as plan:
+        if out is None:
+            out = torch.empty(plan.output_shape, dtype=A.dtype, device=A.device)
+        return plan.execute(A, B, out, stream=stream, C=C)
 
 
 def matmul(A, B, out=None, stream=None, algorithm: Optional[str] = None):

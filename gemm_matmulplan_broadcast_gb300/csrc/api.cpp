@@ -43,6 +43,13 @@ struct olc_matmul_plan {
     int splits;                  // SPLIT_K slices or SKINNY_M K-slices
     int split_hint;              // tuning override of the slice count (0 = automatic)
     int tc_variant;              // tuning override of the tensor-core tiling (0 = automatic)
+    // Gemm operator (rank-2, transA / transB, alpha, beta, broadcast C)
+    int is_gemm;
+    int trans_a, trans_b;
+    double alpha, beta;
+    int c_rank;                  // -1: no C
+    int64_t c_shape[2];
+    int64_t c_rs, c_cs;          // element strides of C over [M, N] (0 = broadcast)
     int device;                  // -1: planned without a device
     int sm_count;
     void* workspace;
@@ -83,8 +90,10 @@ int64_t numel(const int64_t* s, int r) {
     return n;
 }
 
-Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, void* Y) {
+Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, void* Y,
+                     const void* C = nullptr) {
     Problem pr;
+    std::memset(&pr, 0, sizeof pr);
     pr.A = A;
     pr.B = B;
     pr.Y = Y;
@@ -94,6 +103,20 @@ Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, voi
     pr.items = p->items;
     pr.map = p->map;
     pr.split_hint = p->split_hint;
+    pr.a_trans = p->trans_a;
+    pr.b_trans = p->trans_b;
+    // Gemm: alpha * acc + beta * C; the plain product when alpha is 1 and
+    // there is no C (the same results, without the epilogue's work)
+    if (p->is_gemm && (p->alpha != 1.0 || p->c_rank >= 0)) {
+        pr.epi.mode = 1;
+        pr.epi.alpha_f = (float)p->alpha;
+        pr.epi.beta_f = (float)p->beta;
+        pr.epi.alpha_d = p->alpha;
+        pr.epi.beta_d = p->beta;
+        pr.epi.C = p->c_rank >= 0 ? C : nullptr;
+        pr.epi.c_rs = p->c_rs;
+        pr.epi.c_cs = p->c_cs;
+    }
     return pr;
 }
 
@@ -138,6 +161,11 @@ void collapse_and_fold(olc_matmul_plan* p) {
 bool feasible(const olc_matmul_plan* p, int algo) {
     const int64_t rows = p->rows, N = p->N, K = p->K;
     const int64_t n = out_numel(p);
+    const bool trans = p->trans_a || p->trans_b;
+    if (trans && (algo == OLC_ALGO_SKINNY_M || algo == OLC_ALGO_SKINNY_N || algo == OLC_ALGO_SPLIT_K))
+        return false;   // transposed operands: general and direct kernels only
+    if (algo == OLC_ALGO_GENERAL_TC && p->trans_a && (p->M * elem_bytes(p->dtype)) % 16 != 0)
+        return false;   // A stored [K, M] needs 16-byte rows for TMA
     switch (algo) {
         case OLC_ALGO_EMPTY: return n == 0;
         case OLC_ALGO_ZERO_FILL: return n > 0 && K == 0;
@@ -249,11 +277,17 @@ olc_status from_cuda(cudaError_t e) {
     return e == cudaErrorMemoryAllocation ? OLC_ERR_OOM : OLC_ERR_CUDA;
 }
 
-olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, cudaStream_t s) {
+olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, cudaStream_t s,
+               const void* C = nullptr) {
     const int64_t n = out_numel(p);
     if (p->algo == OLC_ALGO_EMPTY || n == 0) return OLC_OK;
     if (!Y) return OLC_ERR_NULL;
-    if (p->algo == OLC_ALGO_ZERO_FILL) return from_cuda(launch_zero_fill(Y, n * elem_bytes(p->dtype), s));
+    if (p->is_gemm && p->c_rank >= 0 && !C) return OLC_ERR_NULL;
+    if (p->algo == OLC_ALGO_ZERO_FILL) {
+        Problem zp = make_problem(p, A, B, Y, C);
+        if (zp.epi.mode) return from_cuda(launch_epilogue_fill(p->dtype, zp, s));
+        return from_cuda(launch_zero_fill(Y, n * elem_bytes(p->dtype), s));
+    }
     if (!A || !B) return OLC_ERR_NULL;
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return from_cuda(cudaErrorNoDevice);
@@ -267,7 +301,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
             if (st != OLC_OK) return st;
         }
     }
-    Problem pr = make_problem(p, A, B, Y);
+    Problem pr = make_problem(p, A, B, Y, C);
     const olc_dtype dt = p->dtype;
     const bool al = aligned16(A) && aligned16(B) && aligned16(Y);
     int algo = p->algo;
@@ -388,6 +422,83 @@ olc_status olc_matmul_plan_create(const int64_t* a_shape, int a_rank, const int6
     if (st != OLC_OK) { delete p; return st; }
     *out = p;
     return OLC_OK;
+}
+
+olc_status olc_gemm_plan_create(const int64_t* a_shape, const int64_t* b_shape, int trans_a,
+                                int trans_b, double alpha, double beta, const int64_t* c_shape,
+                                int c_rank, olc_dtype dtype, olc_matmul_plan** out) {
+    if (!out) return OLC_ERR_NULL;
+    *out = nullptr;
+    if (!a_shape || !b_shape || (c_rank > 0 && !c_shape)) return OLC_ERR_NULL;
+    if (c_rank < -1 || c_rank > 2) return OLC_ERR_RANK;
+    if (!valid_dtype(dtype)) return OLC_ERR_DTYPE;
+    for (int i = 0; i < 2; ++i)
+        if (a_shape[i] < 0 || b_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
+    for (int i = 0; i < c_rank; ++i)
+        if (c_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
+    const int64_t M = trans_a ? a_shape[1] : a_shape[0];
+    const int64_t K = trans_a ? a_shape[0] : a_shape[1];
+    const int64_t Kb = trans_b ? b_shape[1] : b_shape[0];
+    const int64_t N = trans_b ? b_shape[0] : b_shape[1];
+    if (K != Kb) return OLC_ERR_K_MISMATCH;
+    int64_t c2[2] = {1, 1};
+    if (c_rank >= 1) c2[1] = c_shape[c_rank - 1];
+    if (c_rank == 2) c2[0] = c_shape[0];
+    if (c_rank >= 0 && (!(c2[0] == 1 || c2[0] == M) || !(c2[1] == 1 || c2[1] == N)))
+        return OLC_ERR_BATCH_MISMATCH;   // C does not broadcast to [M, N]
+
+    olc_matmul_plan* p = new (std::nothrow) olc_matmul_plan;
+    if (!p) return OLC_ERR_OOM;
+    std::memset(p, 0, sizeof *p);
+    p->dtype = dtype;
+    p->a_rank = p->b_rank = 2;
+    std::memcpy(p->a_shape, a_shape, sizeof(int64_t) * 2);
+    std::memcpy(p->b_shape, b_shape, sizeof(int64_t) * 2);
+    p->device = -1;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->batch = 1;
+    p->batch_rank = 0;
+    p->out_rank = 2;
+    p->out_shape[0] = M;
+    p->out_shape[1] = N;
+    p->rows = M;
+    p->items = 1;
+    p->is_gemm = 1;
+    p->trans_a = trans_a ? 1 : 0;
+    p->trans_b = trans_b ? 1 : 0;
+    p->alpha = alpha;
+    p->beta = beta;
+    p->c_rank = c_rank;
+    p->c_shape[0] = c2[0];
+    p->c_shape[1] = c2[1];
+    p->c_rs = (c2[0] == 1) ? 0 : c2[1];
+    p->c_cs = (c2[1] == 1) ? 0 : 1;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            sms > 0) {
+            p->device = dev;
+            p->sm_count = sms;
+        }
+    }
+    cudaGetLastError();
+    if (p->sm_count <= 0) p->sm_count = kDefaultSmCount;
+    p->algo = choose_algorithm(p);
+    olc_status st = prepare_algorithm(p);
+    if (st != OLC_OK) { delete p; return st; }
+    *out = p;
+    return OLC_OK;
+}
+
+olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const void* B,
+                            const void* C, void* Y, void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    return run(plan, A, B, Y, static_cast<cudaStream_t>(stream), C);
 }
 
 void olc_matmul_plan_destroy(olc_matmul_plan* plan) {

@@ -40,6 +40,31 @@ struct Num<__nv_bfloat16> {
     static __device__ __forceinline__ __nv_bfloat16 from_acc(float v) { return __float2bfloat16_rn(v); }
 };
 
+// Gemm epilogue on one accumulator (see Epilogue).  The two products and the
+// sum are rounded separately (no contraction), in the accumulator type.
+template <typename T>
+__device__ __forceinline__ typename Num<T>::acc_t apply_epilogue(const Epilogue& e,
+                                                                 typename Num<T>::acc_t acc,
+                                                                 int64_t i, int64_t j) {
+    using acc_t = typename Num<T>::acc_t;
+    if (e.mode == 0) return acc;
+    if constexpr (sizeof(acc_t) == 8) {
+        double y = __dmul_rn(e.alpha_d, acc);
+        if (e.C) {
+            const double c = Num<T>::to_acc(static_cast<const T*>(e.C)[i * e.c_rs + j * e.c_cs]);
+            y = __dadd_rn(y, __dmul_rn(e.beta_d, c));
+        }
+        return y;
+    } else {
+        float y = __fmul_rn(e.alpha_f, acc);
+        if (e.C) {
+            const float c = Num<T>::to_acc(__ldg(static_cast<const T*>(e.C) + i * e.c_rs + j * e.c_cs));
+            y = __fadd_rn(y, __fmul_rn(e.beta_f, c));
+        }
+        return y;
+    }
+}
+
 // Operand element offsets of output batch item z.
 __device__ __forceinline__ void batch_offsets(const BatchMap& m, int64_t z, int64_t& a_off,
                                               int64_t& b_off) {

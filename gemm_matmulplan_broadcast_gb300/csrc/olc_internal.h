@@ -23,8 +23,22 @@ struct BatchMap {
     int64_t b_stride[kMaxBatchRank];
 };
 
+// Gemm epilogue: y = alpha * acc + beta * C[i * c_rs + j * c_cs] (C of the
+// output type, strides 0 along broadcast dimensions).  mode 0 = plain
+// product (y = acc, MatMul), 1 = alpha/beta/C applied.  C may be NULL (no
+// bias term).
+struct Epilogue {
+    int mode;
+    float alpha_f, beta_f;
+    double alpha_d, beta_d;
+    const void* C;
+    int64_t c_rs, c_cs;
+};
+
 // One launch's worth of work: `items` independent products
-// [M, K] @ [K, N] -> [M, N] with operand offsets from `map`.
+// [M, K] @ [K, N] -> [M, N] with operand offsets from `map`.  With a_trans
+// A is stored [K, M] (row-major), with b_trans B is stored [N, K] (Gemm's
+// transA / transB; rank-2 products only).
 struct Problem {
     const void* A;
     const void* B;
@@ -33,6 +47,8 @@ struct Problem {
     int64_t items;
     BatchMap map;
     int split_hint;   // > 0: K slices requested by a tuning override, 0: automatic
+    int a_trans, b_trans;
+    Epilogue epi;
 };
 
 // Workspace handed to the split reductions: `partials` holds fp32/fp64
@@ -53,6 +69,8 @@ unsigned int* device_error_word();
 // ---- launchers: every one returns the launch's cudaError_t -------------
 
 cudaError_t launch_zero_fill(void* Y, int64_t bytes, cudaStream_t stream);
+// K == 0 with a Gemm epilogue: Y = beta * C (the product term is empty)
+cudaError_t launch_epilogue_fill(olc_dtype dt, const Problem& p, cudaStream_t stream);
 
 // DIRECT: small tiles, scalar loads, any shape and alignment.
 cudaError_t launch_direct(olc_dtype dt, const Problem& p, cudaStream_t stream);

@@ -77,6 +77,29 @@ cudaError_t launch_zero_fill(void* Y, int64_t bytes, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Gemm with K == 0: Y = beta * C (or 0 without C), elementwise
+template <typename T>
+__global__ void epilogue_fill_kernel(Problem p) {
+    using acc_t = typename Num<T>::acc_t;
+    const int64_t n = p.M * p.N;
+    T* Y = static_cast<T*>(p.Y);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x)
+        Y[e] = Num<T>::from_acc(apply_epilogue<T>(p.epi, acc_t(0), e / p.N, e % p.N));
+}
+
+cudaError_t launch_epilogue_fill(olc_dtype dt, const Problem& p, cudaStream_t stream) {
+    const int64_t n = p.M * p.N;
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = ceil_div(n, 256);
+    if (blocks > 4096) blocks = 4096;
+    return dispatch_dtype(dt, [&](auto tag) {
+        using T = decltype(tag);
+        epilogue_fill_kernel<T><<<(unsigned)blocks, 256, 0, stream>>>(p);
+        return cudaGetLastError();
+    });
+}
+
 // ---------------------------------------------------------------------------
 // the tile kernel
 
@@ -114,12 +137,16 @@ tile_gemm_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
         for (int e = threadIdx.x; e < BM * BK; e += NT) {
             const int r = e / BK, c = e % BK;
             const int64_t gm = m0 + r, gk = k0 + c;
-            As[c][r] = (gm < M && gk < K) ? Num<T>::to_acc(A[gm * K + gk]) : acc_t(0);
+            As[c][r] = (gm < M && gk < K)
+                           ? Num<T>::to_acc(p.a_trans ? A[gk * M + gm] : A[gm * K + gk])
+                           : acc_t(0);
         }
         for (int e = threadIdx.x; e < BK * BN; e += NT) {
             const int r = e / BN, c = e % BN;
             const int64_t gk = k0 + r, gn = n0 + c;
-            Bs[r][c] = (gk < K && gn < N) ? Num<T>::to_acc(B[gk * N + gn]) : acc_t(0);
+            Bs[r][c] = (gk < K && gn < N)
+                           ? Num<T>::to_acc(p.b_trans ? B[gn * K + gk] : B[gk * N + gn])
+                           : acc_t(0);
         }
         __syncthreads();
 #pragma unroll
@@ -143,7 +170,7 @@ tile_gemm_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
             const int64_t gn = n0 + tx + j * TX;
-            if (gn < N) Y[gm * N + gn] = Num<T>::from_acc(acc[i][j]);
+            if (gn < N) Y[gm * N + gn] = Num<T>::from_acc(apply_epilogue<T>(p.epi, acc[i][j], gm, gn));
         }
     }
 }
@@ -220,7 +247,7 @@ __device__ __forceinline__ void fma_f2(unsigned long long& d, unsigned long long
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
-template <typename T, int BM, int BN, int BK, int TM, int TN>
+template <typename T, int BM, int BN, int BK, int TM, int TN, bool AT, bool BT>
 __global__ void __launch_bounds__(256, 2)
 simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     using V = typename Vec<T>::type;
@@ -253,37 +280,67 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     constexpr int AVR = BK / W;                   // vectors per A row slice
     constexpr int BVR = BN / W;                   // vectors per B row
 
+    // A stored [M, K]: vectors along K, stored transposed into As[k][m];
+    // A stored [K, M] (Gemm transA): vectors along M, stored as they are.
+    // B stored [K, N]: vectors along N; B stored [N, K] (transB): vectors
+    // along K, stored transposed into Bs[k][n].
+    constexpr int AMR = BM / W;                   // vectors per A k-row (transposed A)
+    constexpr int BKR = BK / W;                   // vectors per B n-row (transposed B)
+    constexpr bool at = AT, bt = BT;
     auto load_a = [&](int64_t k0, V (&v)[AV]) {
 #pragma unroll
         for (int q = 0; q < AV; ++q) {
             const int e = t + q * 256;
-            const int64_t row = m0 + e / AVR, k = k0 + (e % AVR) * W;
-            if (row < M && k < K) v[q] = *reinterpret_cast<const V*>(A + row * K + k);
-            else v[q] = V{};
+            if (!at) {
+                const int64_t row = m0 + e / AVR, k = k0 + (e % AVR) * W;
+                if (row < M && k < K) v[q] = *reinterpret_cast<const V*>(A + row * K + k);
+                else v[q] = V{};
+            } else {
+                const int64_t k = k0 + e / AMR, row = m0 + (e % AMR) * W;
+                if (k < K && row < M) v[q] = *reinterpret_cast<const V*>(A + k * M + row);
+                else v[q] = V{};
+            }
         }
     };
     auto load_b = [&](int64_t k0, V (&v)[BV]) {
 #pragma unroll
         for (int q = 0; q < BV; ++q) {
             const int e = t + q * 256;
-            const int64_t k = k0 + e / BVR, col = n0 + (e % BVR) * W;
-            if (k < K && col < N) v[q] = *reinterpret_cast<const V*>(B + k * N + col);
-            else v[q] = V{};
+            if (!bt) {
+                const int64_t k = k0 + e / BVR, col = n0 + (e % BVR) * W;
+                if (k < K && col < N) v[q] = *reinterpret_cast<const V*>(B + k * N + col);
+                else v[q] = V{};
+            } else {
+                const int64_t col = n0 + e / BKR, k = k0 + (e % BKR) * W;
+                if (col < N && k < K) v[q] = *reinterpret_cast<const V*>(B + col * K + k);
+                else v[q] = V{};
+            }
         }
     };
     auto store_stage = [&](int buf, const V (&va)[AV], const V (&vb)[BV]) {
 #pragma unroll
         for (int q = 0; q < AV; ++q) {
             const int e = t + q * 256;
-            const int row = e / AVR, kk = (e % AVR) * W;
-            const T* ae = reinterpret_cast<const T*>(&va[q]);
+            if (!at) {
+                const int row = e / AVR, kk = (e % AVR) * W;
+                const T* ae = reinterpret_cast<const T*>(&va[q]);
 #pragma unroll
-            for (int i = 0; i < W; ++i) As[buf][kk + i][row] = ae[i];
+                for (int i = 0; i < W; ++i) As[buf][kk + i][row] = ae[i];
+            } else {
+                *reinterpret_cast<V*>(&As[buf][e / AMR][(e % AMR) * W]) = va[q];
+            }
         }
 #pragma unroll
         for (int q = 0; q < BV; ++q) {
             const int e = t + q * 256;
-            *reinterpret_cast<V*>(&Bs[buf][e / BVR][(e % BVR) * W]) = vb[q];
+            if (!bt) {
+                *reinterpret_cast<V*>(&Bs[buf][e / BVR][(e % BVR) * W]) = vb[q];
+            } else {
+                const int col = e / BKR, kk = (e % BKR) * W;
+                const T* be = reinterpret_cast<const T*>(&vb[q]);
+#pragma unroll
+                for (int i = 0; i < W; ++i) Bs[buf][kk + i][col] = be[i];
+            }
         }
     };
 
@@ -377,7 +434,8 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
                     V v;
                     T* e = reinterpret_cast<T*>(&v);
 #pragma unroll
-                    for (int j = 0; j < W; ++j) e[j] = acc[i][h * HN + q * W + j];
+                    for (int j = 0; j < W; ++j)
+                        e[j] = apply_epilogue<T>(p.epi, acc[i][h * HN + q * W + j], gm, gn + j);
                     *reinterpret_cast<V*>(Y + gm * N + gn) = v;
                 }
             }
@@ -391,7 +449,15 @@ static cudaError_t launch_fast(const Problem& p, cudaStream_t stream) {
     const int64_t blocks = tm * tn * p.items;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    simt_fast_kernel<T, BM, BN, BK, TM, TN><<<(unsigned)blocks, 256, 0, stream>>>(p, tm, tn);
+    const unsigned g = (unsigned)blocks;
+    if (!p.a_trans && !p.b_trans)
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, false, false><<<g, 256, 0, stream>>>(p, tm, tn);
+    else if (p.a_trans && !p.b_trans)
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, true, false><<<g, 256, 0, stream>>>(p, tm, tn);
+    else if (!p.a_trans && p.b_trans)
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, false, true><<<g, 256, 0, stream>>>(p, tm, tn);
+    else
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, true, true><<<g, 256, 0, stream>>>(p, tm, tn);
     return cudaGetLastError();
 }
 
@@ -399,6 +465,11 @@ bool general_simt_fast_ok(olc_dtype dt, int64_t N, int64_t K) {
     if (dt == OLC_FLOAT) return N % 4 == 0 && K % 4 == 0;
     if (dt == OLC_DOUBLE) return N % 2 == 0 && K % 2 == 0;
     return false;
+}
+
+static bool fast_shape_ok(olc_dtype dt, const Problem& p) {
+    const int64_t w = dt == OLC_FLOAT ? 4 : 2;
+    return general_simt_fast_ok(dt, p.N, p.K) && (!p.a_trans || p.M % w == 0);
 }
 
 static bool aligned_items(const Problem& p, int64_t elem) {
@@ -411,6 +482,7 @@ static bool aligned_items(const Problem& p, int64_t elem) {
 }
 
 cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream) {
+    if (!fast_shape_ok(dt, p)) return launch_general_simt_generic(dt, p, stream);
     if (dt == OLC_FLOAT && aligned_items(p, 4)) return launch_fast<float, 128, 128, 16, 8, 8>(p, stream);
     if (dt == OLC_DOUBLE && aligned_items(p, 8)) return launch_fast<double, 64, 64, 8, 4, 4>(p, stream);
     return launch_general_simt_generic(dt, p, stream);

@@ -112,6 +112,9 @@ struct Params {
     int64_t kb_per_split;     // k-blocks per slice
     uint32_t stage_tx_bytes;  // bytes the TMA loads of one stage deliver
     int stream;               // 1: stream-K shares (split instantiation only)
+    int a_mn;                 // A stored [K, M] (Gemm transA): MN-major A operand
+    int b_k;                  // B stored [N, K] (Gemm transB): K-major B operand
+    Epilogue epi;
     int64_t iterations;       // stream-K: total (tile, K block) iterations
     float* part1;             // [tiles][splits][BM][BN] float32 partial tiles
     float* part2;             // [tiles][groups][BM][BN] group sums
@@ -369,6 +372,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Gemm epilogue on one float32 accumulator of output (i, j) within its item:
+// alpha * acc + beta * C (C of the 16-bit output type); the plain product
+// when epi.mode == 0.
+__device__ __forceinline__ float tc_epi(const Params& p, float acc, int64_t i, int64_t j) {
+    if (p.epi.mode == 0) return acc;
+    float y = __fmul_rn(p.epi.alpha_f, acc);
+    if (p.epi.C) {
+        const unsigned short bits =
+            __ldg(static_cast<const unsigned short*>(p.epi.C) + i * p.epi.c_rs + j * p.epi.c_cs);
+        const float c = p.is_bf16 ? __uint_as_float((unsigned)bits << 16)
+                                  : __half2float(__ushort_as_half(bits));
+        y = __fadd_rn(y, __fmul_rn(p.epi.beta_f, c));
+    }
+    return y;
+}
+
 // Sum `count` float32 partial tiles (`stride` floats apart) in order 0, 1,
 // ... for the float4s at indices e0 and e1 (e1 < 0: only e0).  All loads of
 // a batch of up to SUM_BATCH partials are issued before any is added, so a
@@ -404,6 +423,10 @@ __device__ __noinline__ void ordered_sum4x2(const float* base, int64_t stride, i
 // the tile (col < N checked by the caller).
 __device__ __forceinline__ void store4(const Params& p, int64_t item, int64_t row, int64_t col,
                                        float4 v) {
+    v.x = tc_epi(p, v.x, row, col);
+    v.y = tc_epi(p, v.y, row, col + 1);
+    v.z = tc_epi(p, v.z, row, col + 2);
+    v.w = tc_epi(p, v.w, row, col + 3);
     uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
     *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) + ((item * p.M + row) * p.N + col) * 2) = o;
 }
@@ -417,7 +440,7 @@ __device__ __forceinline__ void store4_t(const Params& p, int64_t item, int64_t 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         if (m0 + i < p.M) {
-            const uint32_t h = pack2(f[i], 0.f, p.is_bf16);
+            const uint32_t h = pack2(tc_epi(p, f[i], m0 + i, n), 0.f, p.is_bf16);
             y[(item * p.M + m0 + i) * p.N + n] = (unsigned short)(h & 0xFFFFu);
         }
     }
@@ -510,11 +533,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     armed_parity[stage] = phase;
                     const int k0 = (int)(kb * BK);
                     if constexpr (!SWAP) {
-                        tma_load_3d(sa, &tmap_a, &s->full[stage], k0, m0, a_item);
+                        if (!p.a_mn) {
+                            tma_load_3d(sa, &tmap_a, &s->full[stage], k0, m0, a_item);
+                        } else {
+                            // A stored [K, M]: two MN-major 64-row boxes
+                            tma_load_3d(sa, &tmap_a, &s->full[stage], m0, k0, a_item);
+                            tma_load_3d(sa + 64 * BK * 2, &tmap_a, &s->full[stage], m0 + 64, k0, a_item);
+                        }
+                        if (!p.b_k) {
 #pragma unroll
-                        for (int j = 0; j < C::NBLK; ++j)
-                            tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, &s->full[stage],
-                                        n0 + C::BLK_COLS * j, k0, b_item);
+                            for (int j = 0; j < C::NBLK; ++j)
+                                tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, &s->full[stage],
+                                            n0 + C::BLK_COLS * j, k0, b_item);
+                        } else {
+                            // B stored [N, K]: one K-major box of BN rows
+                            tma_load_3d(sb, &tmap_b, &s->full[stage], k0, n0, b_item);
+                        }
                     } else {
                         // MMA operand A = 128 columns of the problem's B (two
                         // 64-column MN-major boxes); operand B = the problem's
@@ -537,7 +571,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = SWAP ? instr_desc(p.is_bf16, BM, BN, 1, 0)
-                                        : instr_desc(p.is_bf16, BM, BN, 0, 1);
+                                        : instr_desc(p.is_bf16, BM, BN, p.a_mn, p.b_k ? 0 : 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             Cursor cur = cursor_begin(p);
@@ -558,12 +592,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         // bytes inside the swizzle row; 8-row groups 1024 apart
                         uint64_t ad, bd;
                         if constexpr (!SWAP) {
-                            ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
+                            ad = p.a_mn ? smem_desc(a_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u)
+                                        : smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
                             // B: MN-major; advance 16 K-rows of SW bytes; boxes of
                             // BLK_COLS columns B_BLK_BYTES apart (LBO), 8-row
-                            // groups 8 * SW apart (SBO)
-                            bd = smem_desc(b_addr + kk * UMMA_K * C::SW, C::B_BLK_BYTES, 8 * C::SW,
-                                           C::LAYOUT);
+                            // groups 8 * SW apart (SBO).  K-major (transB): rows
+                            // of 64 K-elements, 128-byte swizzle
+                            bd = p.b_k ? smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u)
+                                       : smem_desc(b_addr + kk * UMMA_K * C::SW, C::B_BLK_BYTES,
+                                                   8 * C::SW, C::LAYOUT);
                         } else {
                             // A: MN-major, 128-byte swizzle; advance 16 K-rows of
                             // 128 bytes; the two 64-column boxes 8192 bytes apart
@@ -614,7 +651,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         for (int m = 0; m < BN; ++m)
                             if (m < p.M)
                                 y[(item * p.M + m) * p.N + row] = (unsigned short)(
-                                    pack2(__uint_as_float(r[m]), 0.f, p.is_bf16) & 0xFFFFu);
+                                    pack2(tc_epi(p, __uint_as_float(r[m]), m, row), 0.f, p.is_bf16) &
+                                    0xFFFFu);
                     }
                 } else {
                     unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
@@ -629,8 +667,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                             uint32_t packed[16];
 #pragma unroll
                             for (int i = 0; i < CH / 2; ++i)
-                                packed[i] = pack2(__uint_as_float(r[2 * i]),
-                                                  __uint_as_float(r[2 * i + 1]), p.is_bf16);
+                                packed[i] = pack2(tc_epi(p, __uint_as_float(r[2 * i]), row, col + 2 * i),
+                                                  tc_epi(p, __uint_as_float(r[2 * i + 1]), row, col + 2 * i + 1),
+                                                  p.is_bf16);
                             uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                             // N is a multiple of 8: whole 16-byte groups only
                             const int64_t left = (p.N - col) / 8;
@@ -926,9 +965,18 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         armed_parity[stage] = phase;
                     }
                     const int k0 = (int)(kb * BK);
-                    tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
-                    tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
-                    tma_load_3d_pair(sb + 64 * BK * 2, &tmap_b, full_leader, n0 + 64, k0, b_item);
+                    if (!p.a_mn) {
+                        tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
+                    } else {
+                        tma_load_3d_pair(sa, &tmap_a, full_leader, m0, k0, a_item);
+                        tma_load_3d_pair(sa + 64 * BK * 2, &tmap_a, full_leader, m0 + 64, k0, a_item);
+                    }
+                    if (!p.b_k) {
+                        tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
+                        tma_load_3d_pair(sb + 64 * BK * 2, &tmap_b, full_leader, n0 + 64, k0, b_item);
+                    } else {
+                        tma_load_3d_pair(sb, &tmap_b, full_leader, k0, n0, b_item);
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -939,7 +987,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc = instr_desc(p.is_bf16, 256, 256, 0, 1);
+            const uint32_t idesc = instr_desc(p.is_bf16, 256, 256, p.a_mn, p.b_k ? 0 : 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t t = cluster_id(); t < total && ok; t += cluster_count()) {
@@ -953,8 +1001,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
-                        const uint64_t bd = smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
+                        const uint64_t ad = p.a_mn ? smem_desc(a_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u)
+                                                   : smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
+                        const uint64_t bd = p.b_k ? smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u)
+                                                  : smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
                         mma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     commit2_both(&s->empty[stage]);
@@ -991,7 +1041,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     uint32_t packed[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        packed[i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.is_bf16);
+                        packed[i] = pack2(tc_epi(p, __uint_as_float(r[2 * i]), row, col + 2 * i),
+                                          tc_epi(p, __uint_as_float(r[2 * i + 1]), row, col + 2 * i + 1),
+                                          p.is_bf16);
                     uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                     const int64_t left = (p.N - col) / 8;
                     const int groups = (int)(left < 4 ? left : 4);
@@ -1200,10 +1252,7 @@ splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int64_t e4 = tid, e4b = tid + 128;      // 256 float4s per partial
         auto store_y = [&](int64_t e, float4 v) {
             const int row = (int)((e * 4) / COLS), col = (int)((e * 4) % COLS);
-            if (row < p.M && col < p.N) {
-                uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
-                *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) + ((int64_t)row * p.N + col) * 2) = o;
-            }
+            if (row < p.M && col < p.N) store4(p, 0, row, col, v);
         };
         __threadfence();
         epi_sync();
@@ -1403,10 +1452,20 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     // stale data and feed only output rows that are never stored
     const uint32_t a_box_rows = (!SWAP && pr.M < BM) ? (uint32_t)ceil_div(pr.M, 8) * 8 : BM;
     if (!SWAP) {
-        if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (pr.a_trans) {
+            if (!encode_3d(&ma, pr.A, bf, pr.M, pr.K, a_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+        } else if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, a_box_rows,
+                              CU_TENSOR_MAP_SWIZZLE_128B)) {
             return cudaErrorInvalidValue;
-        if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>()))
+        }
+        if (pr.b_trans) {
+            if (BN != 256) return cudaErrorInvalidValue;
+            if (!encode_3d(&mb, pr.B, bf, pr.K, pr.N, b_items, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+        } else if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>())) {
             return cudaErrorInvalidValue;
+        }
     } else {
         // MMA operand A from the problem's B (64-column MN-major boxes), MMA
         // operand B from the problem's A (BN rows, K-major)
@@ -1438,7 +1497,11 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     p.groups = 1;
     p.kb_per_split = p.k_blocks;
     p.stage_tx_bytes = SWAP ? (uint32_t)(A_STAGE_BYTES + BN * BK * 2)
-                            : (uint32_t)(a_box_rows * BK * 2 + C::B_STAGE_BYTES);
+                            : (uint32_t)((pr.a_trans ? BM : a_box_rows) * BK * 2 + C::B_STAGE_BYTES);
+    p.a_mn = pr.a_trans;
+    p.b_k = pr.b_trans;
+    p.epi = pr.epi;
+    if ((pr.a_trans || pr.b_trans) && (SWAP || SPLIT)) return cudaErrorInvalidValue;
     if (SPLIT) {
         if (!sp || !ws || !ws->partials || !ws->counters || (sp->splits < 2 && !sp->stream))
             return cudaErrorInvalidValue;
@@ -1483,9 +1546,12 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
     const int bf = dt == OLC_BFLOAT16;
-    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    const bool at = pr.a_trans != 0, bt = pr.b_trans != 0;
+    if (!(at ? encode_3d(&ma, pr.A, bf, pr.M, pr.K, a_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)
+             : encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
         return cudaErrorInvalidValue;
-    if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!(bt ? encode_3d(&mb, pr.B, bf, pr.K, pr.N, b_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+             : encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)))
         return cudaErrorInvalidValue;
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -1500,6 +1566,9 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     p.Y = pr.Y;
     p.err = device_error_word();
     p.is_bf16 = bf;
+    p.a_mn = at;
+    p.b_k = bt;
+    p.epi = pr.epi;
     const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.items;
     if (pairs <= 0) return cudaSuccess;
     static std::once_flag attr_once;
@@ -1572,6 +1641,7 @@ static cudaError_t launch_tiny(olc_dtype dt, const Problem& pr, int sm_count, co
     p.Y = pr.Y;
     p.err = device_error_word();
     p.is_bf16 = bf;
+    p.epi = pr.epi;
     p.splits = sp.splits;
     p.group = sp.group;
     p.groups = sp.groups;

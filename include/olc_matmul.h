@@ -172,6 +172,42 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan,
                                    const void* A_host, const void* B_host, void* Y_host,
                                    void* A_dev, void* B_dev, void* Y_dev, void* stream);
 
+/* ---- the Gemm operator ------------------------------------------------- */
+
+/*
+ * Build a plan for ONNX Gemm: Y = alpha * A' B' + beta * C, on the same GEMM
+ * engine ("Gemm and MatMul Performance Roadmap", section "Scope and type
+ * matrix": Gemm handles rank-2 inputs, alpha, beta, an optional broadcast
+ * bias and transA / transB).
+ *
+ *  a_shape[2]: A as stored: [M, K], or [K, M] with trans_a != 0.
+ *  b_shape[2]: B as stored: [K, N], or [N, K] with trans_b != 0.
+ *  alpha, beta: scalars (applied in the accumulator type: float32 for FLOAT,
+ *      FLOAT16, BFLOAT16; float64 for DOUBLE).
+ *  c_shape[c_rank]: C's shape, unidirectionally broadcast to [M, N]: rank 0
+ *      (scalar), [N], [1, N], [M, 1], [M, N] ...; c_rank = -1: no C (the bias
+ *      term is absent and beta is unused).
+ *  dtype: the element type of A, B, C and Y.
+ * Y is [M, N].  FLOAT16 / BFLOAT16 accumulate in float32, apply the
+ * epilogue in float32 and narrow once.  With K == 0, Y = beta * C.
+ * Errors: OLC_ERR_NULL, OLC_ERR_RANK (c_rank outside -1..2),
+ * OLC_ERR_NEGATIVE_DIM, OLC_ERR_K_MISMATCH, OLC_ERR_BATCH_MISMATCH (C does
+ * not broadcast to [M, N]), OLC_ERR_DTYPE, OLC_ERR_OOM, OLC_ERR_CUDA.
+ * Free with olc_matmul_plan_destroy; the query functions below apply.
+ */
+olc_status olc_gemm_plan_create(const int64_t* a_shape, const int64_t* b_shape, int trans_a,
+                                int trans_b, double alpha, double beta, const int64_t* c_shape,
+                                int c_rank, olc_dtype dtype, olc_matmul_plan** out);
+
+/*
+ * Enqueue the Gemm on `stream`.  A, B, C, Y: device pointers of the plan's
+ * dtype, dense row-major as described at creation (C may be NULL only if the
+ * plan has no C).  The same execution rules as olc_matmul_execute.
+ * Errors: OLC_ERR_NULL, OLC_ERR_WRONG_DEVICE, OLC_ERR_CUDA, OLC_ERR_OOM.
+ */
+olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const void* B,
+                            const void* C, void* Y, void* stream);
+
 /* ---- queries ----------------------------------------------------------- */
 
 /* Output shape: writes up to `capacity` extents into shape[] and the rank
