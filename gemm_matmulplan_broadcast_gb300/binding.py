@@ -77,6 +77,10 @@ def load():
                                       ctypes.c_double, i64p, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(vp)], ctypes.c_int),
             "olc_gemm_execute": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "olc_matmul_plan_set_constant_b": ([vp, vp, ctypes.c_int64, vp], ctypes.c_int),
+            "olc_matmul_plan_has_constant_b": ([vp], ctypes.c_int),
+            "olc_matmul_execute_constant": ([vp, vp, vp, vp], ctypes.c_int),
+            "olc_gemm_execute_constant": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute_checked": ([vp, vp, ctypes.c_int64, vp, ctypes.c_int64, vp,
                                             ctypes.c_int64, vp], ctypes.c_int),
@@ -288,6 +292,25 @@ class Plan:
         _check(st, "olc_matmul_execute_host")
         return Y_host
 
+    def set_constant_b(self, B, stream=None):
+        """Copy B (host or device tensor of the planned shape) into storage
+        the plan owns; later executes may omit B."""
+        st = self.lib.olc_matmul_plan_set_constant_b(self._h, _ptr(B), B.numel(),
+                                                     _stream_handle(stream))
+        _check(st, "olc_matmul_plan_set_constant_b")
+        return self
+
+    @property
+    def has_constant_b(self) -> bool:
+        return bool(self.lib.olc_matmul_plan_has_constant_b(self._h))
+
+    def execute_constant(self, A, Y, stream=None):
+        """Y = MatMul(A, plan-owned B)."""
+        self._check_tensors(A, None, Y)
+        st = self.lib.olc_matmul_execute_constant(self._h, _ptr(A), _ptr(Y), _stream_handle(stream))
+        _check(st, "olc_matmul_execute_constant")
+        return Y
+
     def __call__(self, A, B, out=None, stream=None):
         import torch
         if out is None:
@@ -326,6 +349,14 @@ class GemmPlan(Plan):
         st = self.lib.olc_gemm_execute(self._h, _ptr(A), _ptr(B), _ptr(C), _ptr(Y),
                                        _stream_handle(stream))
         _check(st, "olc_gemm_execute")
+        return Y
+
+    def execute_constant(self, A, Y, stream=None, C=None):
+        """The Gemm with the plan-owned B."""
+        self._check_tensors(A, None, Y)
+        st = self.lib.olc_gemm_execute_constant(self._h, _ptr(A), _ptr(C), _ptr(Y),
+                                                _stream_handle(stream))
+        _check(st, "olc_gemm_execute_constant")
         return Y
 
 

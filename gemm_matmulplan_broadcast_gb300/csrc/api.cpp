@@ -50,6 +50,10 @@ struct olc_matmul_plan {
     int c_rank;                  // -1: no C
     int64_t c_shape[2];
     int64_t c_rs, c_cs;          // element strides of C over [M, N] (0 = broadcast)
+    // plan-owned constant B (device copy on the plan's device)
+    void* const_b;
+    size_t const_b_bytes;
+    int const_b_set;
     int device;                  // -1: planned without a device
     int sm_count;
     void* workspace;
@@ -504,7 +508,77 @@ olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const vo
 void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
     if (!plan) return;
     free_workspace(plan);
+    if (plan->const_b) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (plan->device >= 0 && cur != plan->device) cudaSetDevice(plan->device);
+        cudaFree(plan->const_b);
+        if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
+        cudaGetLastError();
+    }
     delete plan;
+}
+
+olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, int64_t b_numel,
+                                          void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    const int64_t want = numel(plan->b_shape, plan->b_rank);
+    if (b_numel != want) return OLC_ERR_BUFFER_TOO_SMALL;   // must be exactly the planned B
+    if (want > 0 && !B) return OLC_ERR_NULL;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return from_cuda(cudaErrorNoDevice);
+    if (plan->device >= 0 && cur != plan->device) return OLC_ERR_WRONG_DEVICE;
+    if (plan->device < 0) {
+        plan->device = cur;
+        if (plan->partial_bytes > 0 && !plan->workspace) {
+            olc_status st = prepare_algorithm(plan);
+            if (st != OLC_OK) return st;
+        }
+    }
+    const size_t bytes = (size_t)(want * elem_bytes(plan->dtype));
+    if (!plan->const_b || plan->const_b_bytes != bytes) {
+        if (plan->const_b) cudaFree(plan->const_b);
+        plan->const_b = nullptr;
+        plan->const_b_bytes = 0;
+        if (bytes > 0) {
+            void* mem = nullptr;
+            if (cudaMalloc(&mem, bytes) != cudaSuccess) {
+                cudaGetLastError();
+                return OLC_ERR_OOM;
+            }
+            plan->const_b = mem;
+        }
+        plan->const_b_bytes = bytes;
+    }
+    plan->const_b_set = 0;
+    if (bytes > 0) {
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        // host or device source (unified addressing); the copy has completed
+        // when this call returns, so the caller may free or reuse its buffer
+        cudaError_t e = cudaMemcpyAsync(plan->const_b, B, bytes, cudaMemcpyDefault, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    plan->const_b_set = 1;
+    return OLC_OK;
+}
+
+int olc_matmul_plan_has_constant_b(const olc_matmul_plan* plan) {
+    return plan && plan->const_b_set ? 1 : 0;
+}
+
+olc_status olc_matmul_execute_constant(const olc_matmul_plan* plan, const void* A, void* Y,
+                                       void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    if (!plan->const_b_set) return OLC_ERR_NO_CONSTANT_B;
+    return run(plan, A, plan->const_b, Y, static_cast<cudaStream_t>(stream));
+}
+
+olc_status olc_gemm_execute_constant(const olc_matmul_plan* plan, const void* A, const void* C,
+                                     void* Y, void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    if (!plan->const_b_set) return OLC_ERR_NO_CONSTANT_B;
+    return run(plan, A, plan->const_b, Y, static_cast<cudaStream_t>(stream), C);
 }
 
 olc_status olc_matmul_execute(const olc_matmul_plan* plan, const void* A, const void* B, void* Y,

@@ -208,6 +208,39 @@ olc_status olc_gemm_plan_create(const int64_t* a_shape, const int64_t* b_shape, 
 olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const void* B,
                             const void* C, void* Y, void* stream);
 
+/* ---- plan-owned constant B ---------------------------------------------- */
+
+/*
+ * Give the plan its own copy of a constant B ("MatMul Kernel Design",
+ * section "Shape and plan model": the library plan can own a constant B with
+ * a lifetime independent of the source buffer; section "Scheduling and
+ * invariants": the constant-B storage must contain exactly the planned
+ * matrix).  B: host or device pointer to b_numel elements of the plan's
+ * dtype, laid out as planned (for Gemm, as stored: [K, N] or [N, K]); the
+ * copy is made on `stream` and has completed when the call returns, so the
+ * caller may free or overwrite its buffer.  Device memory is allocated once
+ * (cudaMalloc on the plan's device) and freed with the plan; calling again
+ * replaces the contents.  No repacking is done: the kernels read B's layout
+ * directly.  Errors: OLC_ERR_NULL, OLC_ERR_BUFFER_TOO_SMALL (b_numel is not
+ * the planned size), OLC_ERR_WRONG_DEVICE, OLC_ERR_OOM, OLC_ERR_CUDA.
+ */
+olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, int64_t b_numel,
+                                          void* stream);
+
+/* 1 if the plan owns a constant B, 0 otherwise (also for NULL). */
+int olc_matmul_plan_has_constant_b(const olc_matmul_plan* plan);
+
+/* Y = MatMul(A, B) with the plan-owned B.  Rejected with OLC_ERR_NO_CONSTANT_B
+ * when the plan owns no B ("Scheduling and invariants": the constant-only
+ * Execute is rejected when the plan does not own B).  Otherwise as
+ * olc_matmul_execute. */
+olc_status olc_matmul_execute_constant(const olc_matmul_plan* plan, const void* A, void* Y,
+                                       void* stream);
+
+/* The Gemm with the plan-owned B; as olc_gemm_execute otherwise. */
+olc_status olc_gemm_execute_constant(const olc_matmul_plan* plan, const void* A, const void* C,
+                                     void* Y, void* stream);
+
 /* ---- queries ----------------------------------------------------------- */
 
 /* Output shape: writes up to `capacity` extents into shape[] and the rank

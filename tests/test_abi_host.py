@@ -232,3 +232,21 @@ def test_tcgen05_descriptor_bit_layout():
     i = lib.olc_debug_tc_instr_desc(0, 128, 16, 1, 0)
     assert _field(i, 15, 15) == 1 and _field(i, 16, 16) == 0
     assert _field(i, 17, 22) == 16 >> 3 and _field(i, 24, 28) == 128 >> 4
+
+
+def test_constant_b_host_rejections():
+    """No kernel runs: a plan without an owned B rejects the B-less execute,
+    NULL plans are rejected, and a wrong-size B is refused before any copy."""
+    lib = binding.load()
+    assert lib.olc_matmul_plan_has_constant_b(None) == 0
+    assert binding.STATUS[lib.olc_matmul_plan_set_constant_b(None, None, 0, None)] == "OLC_ERR_NULL"
+    assert binding.STATUS[lib.olc_matmul_execute_constant(None, None, None, None)] == "OLC_ERR_NULL"
+    with Plan((16, 32), (32, 24), "float32") as p:
+        assert not p.has_constant_b
+        st = lib.olc_matmul_execute_constant(p._h, None, None, None)
+        assert binding.STATUS[st] == "OLC_ERR_NO_CONSTANT_B"
+        st = lib.olc_gemm_execute_constant(p._h, None, None, None, None)
+        assert binding.STATUS[st] == "OLC_ERR_NO_CONSTANT_B"
+        st = lib.olc_matmul_plan_set_constant_b(p._h, None, 32 * 23, None)
+        assert binding.STATUS[st] in ("OLC_ERR_BUFFER_TOO_SMALL", "OLC_ERR_NULL")
+        assert not p.has_constant_b
