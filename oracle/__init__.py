@@ -38,6 +38,7 @@ from __future__ import annotations
 
 import ctypes
 import itertools
+import math
 import os
 import subprocess
 import threading
@@ -269,35 +270,137 @@ def gemm_output_shape(a_shape, b_shape, trans_a, trans_b, c_shape=None):
     return int(m), int(n), int(ka)
 
 
-def gemm_op(a, b, dtype, c=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=False):
-    """ONNX Gemm.  Returns (Y, S) with S = |alpha| sum|a||b| + |beta| |c|
-    (float64), the tolerance scale."""
+def _acc2d(a, b, dtype):
+    """The accumulator of one 2-D product before narrowing: float32 for
+    FLOAT / FLOAT16 / BFLOAT16, float64 for DOUBLE; plus S = sum |a||b|."""
+    if dtype in ("float16", "bfloat16"):
+        m, k = a.shape
+        n = b.shape[1]
+        acc = np.zeros((m, n), np.float32)
+        s = np.zeros((m, n), np.float64)
+        if m and n:
+            lib = _load()
+            fn = lib.oracle_gemm_f16_acc if dtype == "float16" else lib.oracle_gemm_bf16_acc
+            a16 = np.ascontiguousarray(a, np.uint16)
+            b16 = np.ascontiguousarray(b, np.uint16)
+            fn(m, n, k, _ptr(a16), _ptr(b16), None, m, _ptr(acc), _ptr(s))
+        return acc, s
+    acc, s = gemm2d(a, b, dtype)
+    return acc.astype(np.float64 if dtype == "float64" else np.float32), s
+
+
+def _wide(dtype):
+    return np.float64 if dtype == "float64" else np.float32
+
+
+def _values(x, dtype):
+    """Operand values in the accumulator type (16-bit patterns decoded)."""
+    x = np.asarray(x)
+    if dtype in ("float16", "bfloat16"):
+        return to_float64(x, dtype).astype(np.float32)
+    return x.astype(_wide(dtype))
+
+
+def gemm_op(a, b, dtype, c=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=False,
+            residual=None, act="none"):
+    """ONNX Gemm, optionally followed by the fused residual and activation
+    (see ``fused_epilogue``).  Returns (Y, S) with S the tolerance scale
+    L * (|alpha| sum|a||b| + |beta| |c| + |r|) (float64), L the activation's
+    Lipschitz constant."""
     m, n, k = gemm_output_shape(a.shape, b.shape, trans_a, trans_b,
                                 None if c is None else c.shape)
     ap = np.ascontiguousarray(a.T if trans_a else a)
     bp = np.ascontiguousarray(b.T if trans_b else b)
-    lib = _load()
-    half = dtype in ("float16", "bfloat16")
-    wide = np.float64 if dtype == "float64" else np.float32
-    if half:
-        acc = np.zeros((m, n), np.float32)
-        s = np.zeros((m, n), np.float64)
-        if m and n:
-            fn = lib.oracle_gemm_f16_acc if dtype == "float16" else lib.oracle_gemm_bf16_acc
-            ap16 = np.ascontiguousarray(ap, np.uint16)
-            bp16 = np.ascontiguousarray(bp, np.uint16)
-            fn(m, n, k, _ptr(ap16), _ptr(bp16), None, m, _ptr(acc), _ptr(s))
-    else:
-        acc, s = gemm2d(ap, bp, dtype)
-        acc = acc.astype(wide)
+    wide = _wide(dtype)
+    acc, s = _acc2d(ap, bp, dtype)
     y = wide(alpha) * acc
     scale = abs(float(alpha)) * s
     if c is not None:
-        cv = to_float64(np.asarray(c), dtype).astype(wide) if half else np.asarray(c, wide)
+        cv = _values(c, dtype)
         cb = np.broadcast_to(cv.reshape([1] * (2 - cv.ndim) + list(cv.shape)), (m, n))
         y = y + wide(beta) * cb
         scale = scale + abs(float(beta)) * np.abs(cb.astype(np.float64))
-    y = np.asarray(y, wide)
-    if half:
-        return encode(y.astype(np.float32), dtype), scale
-    return y, scale
+    return fused_epilogue(np.asarray(y, wide), scale, dtype, residual, act)
+
+
+# --------------------------------------------------------------------------
+# the fused epilogue (bias, residual, activation, narrowing)
+#
+# "Gemm and MatMul Performance Roadmap": the fused-epilogue row of its
+# opportunity table (each following elementwise operator fused into the
+# product saves one read and one write of the output) and the broadcast /
+# fused epilogue item of its plan (bias, residual, activation and output
+# conversion in one typed epilogue, no intermediate tensor).  Readings where
+# the page is silent: the steps run in the order the page lists them --
+# bias, then residual, then activation, then narrowing; the residual has the
+# output's shape and type; the activations are ReLU, max(v, 0), and the exact
+# GELU, v * Phi(v) = v / 2 * (1 + erf(v / sqrt 2)); the residual sum is
+# rounded in the accumulator type, the activation is evaluated in float64
+# and rounded to the accumulator type, and the result is narrowed once.
+
+ACTIVATIONS = ("none", "relu", "gelu")
+# max over v of |d/dv (v Phi(v))| = Phi(sqrt 2) + sqrt 2 phi(sqrt 2)
+GELU_LIPSCHITZ = 1.12891   # 1.1289041..., rounded up
+
+
+def activation(v: np.ndarray, act: str) -> np.ndarray:
+    """The activation on float64 values (NaN stays NaN)."""
+    v = np.asarray(v, np.float64)
+    if act == "none":
+        return v.copy()
+    if act == "relu":
+        return np.where(v < 0, 0.0, v)
+    if act == "gelu":
+        erf = np.vectorize(math.erf, otypes=[np.float64])
+        return 0.5 * v * (1.0 + erf(v / math.sqrt(2.0)))
+    raise ValueError("unknown activation %r" % act)
+
+
+def fused_epilogue(v, scale, dtype, residual=None, act="none"):
+    """From the accumulator-type values v (after alpha and the bias) to the
+    stored output: v + r, then the activation, then narrowing.  Returns
+    (Y, S) with S widened by |r| and by the activation's Lipschitz constant."""
+    wide = _wide(dtype)
+    v = np.asarray(v, wide)
+    scale = np.asarray(scale, np.float64)
+    if residual is not None:
+        rv = _values(residual, dtype)
+        if rv.shape != v.shape:
+            raise ShapeError("residual %s is not the output shape %s" % (rv.shape, v.shape))
+        v = (v + rv).astype(wide)
+        scale = scale + np.abs(rv.astype(np.float64))
+    if act != "none":
+        v = activation(v, act).astype(wide)
+        if act == "gelu":
+            scale = scale * GELU_LIPSCHITZ
+    if dtype in ("float16", "bfloat16"):
+        return encode(v.astype(np.float32), dtype), scale
+    return v, scale
+
+
+def matmul_acc(a: np.ndarray, b: np.ndarray, dtype: str):
+    """MatMul's accumulators before narrowing (float32, or float64 for
+    DOUBLE), with the same shape rules and batch loop as ``matmul``."""
+    out_shape = output_shape(a.shape, b.shape)
+    a2 = a.reshape((1,) + a.shape) if a.ndim == 1 else a
+    b2 = b.reshape(b.shape + (1,)) if b.ndim == 1 else b
+    m, n = a2.shape[-2], b2.shape[-1]
+    batch = _broadcast(a2.shape[:-2], b2.shape[:-2])
+    r = len(batch)
+    a_batch = [1] * (r - (a2.ndim - 2)) + list(a2.shape[:-2])
+    b_batch = [1] * (r - (b2.ndim - 2)) + list(b2.shape[:-2])
+    a3 = a2.reshape(a_batch + [m, a2.shape[-1]])
+    b3 = b2.reshape(b_batch + [b2.shape[-2], n])
+    acc = np.zeros(batch + [m, n], _wide(dtype))
+    s = np.zeros(batch + [m, n], np.float64)
+    for idx in itertools.product(*[range(d) for d in batch]):
+        ia = tuple(0 if da == 1 else i for i, da in zip(idx, a_batch))
+        ib = tuple(0 if db == 1 else i for i, db in zip(idx, b_batch))
+        acc[idx], s[idx] = _acc2d(a3[ia], b3[ib], dtype)
+    return acc.reshape(out_shape), s.reshape(out_shape)
+
+
+def matmul_fused(a, b, dtype, residual=None, act="none"):
+    """MatMul followed by the fused residual and activation.  Returns (Y, S)."""
+    acc, s = matmul_acc(a, b, dtype)
+    return fused_epilogue(acc, s, dtype, residual, act)
