@@ -31,7 +31,9 @@ STATUS = {
     7: "OLC_ERR_ALIGNMENT", 8: "OLC_ERR_BUFFER_TOO_SMALL", 9: "OLC_ERR_NO_CONSTANT_B",
     10: "OLC_ERR_CUDA", 11: "OLC_ERR_DEVICE_TIMEOUT", 12: "OLC_ERR_OOM",
     13: "OLC_ERR_INVALID", 14: "OLC_ERR_WRONG_DEVICE", 15: "OLC_ERR_SCRATCH_LIMIT",
+    16: "OLC_ERR_NEEDS_RESIDUAL",
 }
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
 MAX_RANK = 8
 
 _lock = threading.Lock()
@@ -80,6 +82,8 @@ def load():
             "olc_matmul_plan_set_constant_b": ([vp, vp, ctypes.c_int64, vp], ctypes.c_int),
             "olc_matmul_plan_has_constant_b": ([vp], ctypes.c_int),
             "olc_matmul_execute_constant": ([vp, vp, vp, vp], ctypes.c_int),
+            "olc_matmul_plan_set_epilogue": ([vp, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+            "olc_matmul_execute_fused": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_gemm_execute_constant": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute_checked": ([vp, vp, ctypes.c_int64, vp, ctypes.c_int64, vp,
@@ -309,6 +313,25 @@ class Plan:
         self._check_tensors(A, None, Y)
         st = self.lib.olc_matmul_execute_constant(self._h, _ptr(A), _ptr(Y), _stream_handle(stream))
         _check(st, "olc_matmul_execute_constant")
+        return Y
+
+    def set_epilogue(self, act: str = "none", residual: bool = False):
+        """Fuse a residual add and an activation into the product's store."""
+        if act not in ACTIVATIONS:
+            raise ValueError("activation must be one of %s" % sorted(ACTIVATIONS))
+        st = self.lib.olc_matmul_plan_set_epilogue(self._h, ACTIVATIONS[act], int(bool(residual)))
+        _check(st, "olc_matmul_plan_set_epilogue")
+        self.epilogue = (act, bool(residual))
+        return self
+
+    def execute_fused(self, A, B, Y, R=None, C=None, stream=None):
+        """Y = act(product (+ bias) + R); B None = the plan-owned B."""
+        self._check_tensors(A, B, Y)
+        if R is not None:
+            self._check_tensors(None, None, R)
+        st = self.lib.olc_matmul_execute_fused(self._h, _ptr(A), _ptr(B), _ptr(C), _ptr(R),
+                                               _ptr(Y), _stream_handle(stream))
+        _check(st, "olc_matmul_execute_fused")
         return Y
 
     def __call__(self, A, B, out=None, stream=None):

@@ -54,6 +54,9 @@ struct olc_matmul_plan {
     void* const_b;
     size_t const_b_bytes;
     int const_b_set;
+    // fused epilogue: activation, and a residual in the output's layout
+    int act;
+    int residual;
     int device;                  // -1: planned without a device
     int sm_count;
     void* workspace;
@@ -95,7 +98,7 @@ int64_t numel(const int64_t* s, int r) {
 }
 
 Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, void* Y,
-                     const void* C = nullptr) {
+                     const void* C = nullptr, const void* R = nullptr) {
     Problem pr;
     std::memset(&pr, 0, sizeof pr);
     pr.A = A;
@@ -109,17 +112,26 @@ Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, voi
     pr.split_hint = p->split_hint;
     pr.a_trans = p->trans_a;
     pr.b_trans = p->trans_b;
-    // Gemm: alpha * acc + beta * C; the plain product when alpha is 1 and
-    // there is no C (the same results, without the epilogue's work)
-    if (p->is_gemm && (p->alpha != 1.0 || p->c_rank >= 0)) {
+    // Gemm: alpha * acc + beta * C, then the fused residual and activation;
+    // the plain product when alpha is 1 and nothing else is asked for (the
+    // same results, without the epilogue's work)
+    const bool gemm_epi = p->is_gemm && (p->alpha != 1.0 || p->c_rank >= 0);
+    if (gemm_epi || p->act != OLC_ACT_NONE || p->residual) {
+        const double alpha = p->is_gemm ? p->alpha : 1.0;
+        const double beta = p->is_gemm ? p->beta : 0.0;
         pr.epi.mode = 1;
-        pr.epi.alpha_f = (float)p->alpha;
-        pr.epi.beta_f = (float)p->beta;
-        pr.epi.alpha_d = p->alpha;
-        pr.epi.beta_d = p->beta;
-        pr.epi.C = p->c_rank >= 0 ? C : nullptr;
+        pr.epi.alpha_f = (float)alpha;
+        pr.epi.beta_f = (float)beta;
+        pr.epi.alpha_d = alpha;
+        pr.epi.beta_d = beta;
+        pr.epi.C = p->is_gemm && p->c_rank >= 0 ? C : nullptr;
         pr.epi.c_rs = p->c_rs;
         pr.epi.c_cs = p->c_cs;
+        pr.epi.R = p->residual ? R : nullptr;
+        pr.epi.r_delta = p->residual ? (int64_t)(reinterpret_cast<intptr_t>(R) -
+                                                 reinterpret_cast<intptr_t>(Y))
+                                     : 0;
+        pr.epi.act = p->act;
     }
     return pr;
 }
@@ -282,13 +294,14 @@ olc_status from_cuda(cudaError_t e) {
 }
 
 olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, cudaStream_t s,
-               const void* C = nullptr) {
+               const void* C = nullptr, const void* R = nullptr) {
     const int64_t n = out_numel(p);
     if (p->algo == OLC_ALGO_EMPTY || n == 0) return OLC_OK;
     if (!Y) return OLC_ERR_NULL;
     if (p->is_gemm && p->c_rank >= 0 && !C) return OLC_ERR_NULL;
+    if (p->residual && !R) return OLC_ERR_NEEDS_RESIDUAL;
     if (p->algo == OLC_ALGO_ZERO_FILL) {
-        Problem zp = make_problem(p, A, B, Y, C);
+        Problem zp = make_problem(p, A, B, Y, C, R);
         if (zp.epi.mode) return from_cuda(launch_epilogue_fill(p->dtype, zp, s));
         return from_cuda(launch_zero_fill(Y, n * elem_bytes(p->dtype), s));
     }
@@ -305,9 +318,10 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
             if (st != OLC_OK) return st;
         }
     }
-    Problem pr = make_problem(p, A, B, Y, C);
+    Problem pr = make_problem(p, A, B, Y, C, R);
     const olc_dtype dt = p->dtype;
-    const bool al = aligned16(A) && aligned16(B) && aligned16(Y);
+    // the residual is read with the same vector widths as Y is written
+    const bool al = aligned16(A) && aligned16(B) && aligned16(Y) && (!R || aligned16(R));
     int algo = p->algo;
     if (!al && algo != OLC_ALGO_DIRECT && algo != OLC_ALGO_GENERAL_SIMT) algo = OLC_ALGO_DIRECT;
     cudaError_t e = cudaSuccess;
@@ -581,6 +595,26 @@ olc_status olc_gemm_execute_constant(const olc_matmul_plan* plan, const void* A,
     return run(plan, A, plan->const_b, Y, static_cast<cudaStream_t>(stream), C);
 }
 
+olc_status olc_matmul_plan_set_epilogue(olc_matmul_plan* plan, int activation, int residual) {
+    if (!plan) return OLC_ERR_NULL;
+    if (activation < OLC_ACT_NONE || activation > OLC_ACT_GELU || residual < 0 || residual > 1)
+        return OLC_ERR_INVALID;
+    plan->act = activation;
+    plan->residual = residual;
+    return OLC_OK;
+}
+
+olc_status olc_matmul_execute_fused(const olc_matmul_plan* plan, const void* A, const void* B,
+                                    const void* C, const void* R, void* Y, void* stream) {
+    if (!plan) return OLC_ERR_NULL;
+    if (!B && numel(plan->b_shape, plan->b_rank) > 0) {
+        if (!plan->const_b_set) return OLC_ERR_NO_CONSTANT_B;
+        B = plan->const_b;
+    }
+    if (plan->residual && !R && out_numel(plan) > 0) return OLC_ERR_NULL;
+    return run(plan, A, B, Y, static_cast<cudaStream_t>(stream), C, R);
+}
+
 olc_status olc_matmul_execute(const olc_matmul_plan* plan, const void* A, const void* B, void* Y,
                               void* stream) {
     if (!plan) return OLC_ERR_NULL;
@@ -756,6 +790,7 @@ const char* olc_status_string(int status) {
         case OLC_ERR_INVALID: return "invalid argument";
         case OLC_ERR_WRONG_DEVICE: return "current device is not the plan's device";
         case OLC_ERR_SCRATCH_LIMIT: return "problem needs more than the static scratch array";
+        case OLC_ERR_NEEDS_RESIDUAL: return "plan fuses a residual: execute with olc_matmul_execute_fused";
     }
     return "unknown status";
 }

@@ -40,28 +40,51 @@ struct Num<__nv_bfloat16> {
     static __device__ __forceinline__ __nv_bfloat16 from_acc(float v) { return __float2bfloat16_rn(v); }
 };
 
-// Gemm epilogue on one accumulator (see Epilogue).  The two products and the
-// sum are rounded separately (no contraction), in the accumulator type.
+// The fused epilogue's activation, in the accumulator type.
+__device__ __forceinline__ float activate(int act, float y) {
+    if (act == OLC_ACT_RELU) return y < 0.f ? 0.f : y;    // NaN fails the test: stays NaN
+    if (act == OLC_ACT_GELU) return __fmul_rn(__fmul_rn(0.5f, y), __fadd_rn(1.f, erff(__fmul_rn(y, 0.70710678118654752f))));
+    return y;
+}
+__device__ __forceinline__ double activate(int act, double y) {
+    if (act == OLC_ACT_RELU) return y < 0.0 ? 0.0 : y;
+    if (act == OLC_ACT_GELU) return __dmul_rn(__dmul_rn(0.5, y), __dadd_rn(1.0, erf(__dmul_rn(y, 0.70710678118654752440))));
+    return y;
+}
+
+// Where the residual of the output element at y sits (R has Y's layout).
+template <typename T>
+__device__ __forceinline__ const T* residual_at(const Epilogue& e, const T* y) {
+    return reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(y) + e.r_delta);
+}
+
+// The epilogue on one accumulator of output (i, j) (within its item), to be
+// stored at y: alpha * acc + beta * C, plus the residual, then the
+// activation.  Each product and sum is rounded separately (no contraction),
+// in the accumulator type.
 template <typename T>
 __device__ __forceinline__ typename Num<T>::acc_t apply_epilogue(const Epilogue& e,
                                                                  typename Num<T>::acc_t acc,
-                                                                 int64_t i, int64_t j) {
+                                                                 int64_t i, int64_t j,
+                                                                 const T* y) {
     using acc_t = typename Num<T>::acc_t;
     if (e.mode == 0) return acc;
     if constexpr (sizeof(acc_t) == 8) {
-        double y = __dmul_rn(e.alpha_d, acc);
+        double v = __dmul_rn(e.alpha_d, acc);
         if (e.C) {
             const double c = Num<T>::to_acc(static_cast<const T*>(e.C)[i * e.c_rs + j * e.c_cs]);
-            y = __dadd_rn(y, __dmul_rn(e.beta_d, c));
+            v = __dadd_rn(v, __dmul_rn(e.beta_d, c));
         }
-        return y;
+        if (e.R) v = __dadd_rn(v, Num<T>::to_acc(*residual_at(e, y)));
+        return activate(e.act, v);
     } else {
-        float y = __fmul_rn(e.alpha_f, acc);
+        float v = __fmul_rn(e.alpha_f, acc);
         if (e.C) {
             const float c = Num<T>::to_acc(__ldg(static_cast<const T*>(e.C) + i * e.c_rs + j * e.c_cs));
-            y = __fadd_rn(y, __fmul_rn(e.beta_f, c));
+            v = __fadd_rn(v, __fmul_rn(e.beta_f, c));
         }
-        return y;
+        if (e.R) v = __fadd_rn(v, Num<T>::to_acc(__ldg(residual_at(e, y))));
+        return activate(e.act, v);
     }
 }
 

@@ -28,11 +28,14 @@ struct BatchMap {
 // product (y = acc, MatMul), 1 = alpha/beta/C applied.  C may be NULL (no
 // bias term).
 struct Epilogue {
-    int mode;
+    int mode;                  // 0: Y = acc; 1: the steps below
     float alpha_f, beta_f;
     double alpha_d, beta_d;
-    const void* C;
+    const void* C;             // bias, broadcast through (c_rs, c_cs); may be null
     int64_t c_rs, c_cs;
+    const void* R;             // residual in Y's layout; may be null
+    int64_t r_delta;           // byte distance R - Y: residual of *y is at y + r_delta
+    int act;                   // olc_activation
 };
 
 // One launch's worth of work: `items` independent products

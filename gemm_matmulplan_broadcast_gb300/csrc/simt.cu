@@ -85,7 +85,7 @@ __global__ void epilogue_fill_kernel(Problem p) {
     T* Y = static_cast<T*>(p.Y);
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x)
-        Y[e] = Num<T>::from_acc(apply_epilogue<T>(p.epi, acc_t(0), e / p.N, e % p.N));
+        Y[e] = Num<T>::from_acc(apply_epilogue<T>(p.epi, acc_t(0), e / p.N, e % p.N, Y + e));
 }
 
 cudaError_t launch_epilogue_fill(olc_dtype dt, const Problem& p, cudaStream_t stream) {
@@ -170,7 +170,7 @@ tile_gemm_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
             const int64_t gn = n0 + tx + j * TX;
-            if (gn < N) Y[gm * N + gn] = Num<T>::from_acc(apply_epilogue<T>(p.epi, acc[i][j], gm, gn));
+            if (gn < N) Y[gm * N + gn] = Num<T>::from_acc(apply_epilogue<T>(p.epi, acc[i][j], gm, gn, Y + gm * N + gn));
         }
     }
 }
@@ -435,7 +435,8 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
                     T* e = reinterpret_cast<T*>(&v);
 #pragma unroll
                     for (int j = 0; j < W; ++j)
-                        e[j] = apply_epilogue<T>(p.epi, acc[i][h * HN + q * W + j], gm, gn + j);
+                        e[j] = apply_epilogue<T>(p.epi, acc[i][h * HN + q * W + j], gm, gn + j,
+                                                        Y + gm * N + gn + j);
                     *reinterpret_cast<V*>(Y + gm * N + gn) = v;
                 }
             }

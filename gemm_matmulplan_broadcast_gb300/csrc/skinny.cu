@@ -181,7 +181,7 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
             if (e >= ENTRIES) continue;
             const int i = e / COLS, c = e % COLS;
             const int64_t col = cg * COLS + c;
-            if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(apply_epilogue<T>(p.epi, part[q], i, col));
+            if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(apply_epilogue<T>(p.epi, part[q], i, col, Y + i * N + col));
         }
         return;
     }
@@ -210,7 +210,7 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
         for (int t = 1; t < ksplit; ++t) s += __ldcg(all + (int64_t)t * ENTRIES + e);
         const int i = e / COLS, c = e % COLS;
         const int64_t col = cg * COLS + c;
-        if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(apply_epilogue<T>(p.epi, s, i, col));
+        if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(apply_epilogue<T>(p.epi, s, i, col, Y + i * N + col));
     }
     if (threadIdx.x == 0) ws.counters[tile] = 0u;   // ready for the next launch
 }
@@ -423,7 +423,7 @@ skinny_n_kernel(Problem p, int64_t row_groups) {
             for (int n = 0; n < NC; ++n)
                 if (n < N)
                     Y[(row0 + r) * N + n] =
-                        Num<T>::from_acc(apply_epilogue<T>(p.epi, acc[r][n], row0 + r, n));
+                        Num<T>::from_acc(apply_epilogue<T>(p.epi, acc[r][n], row0 + r, n, Y + (row0 + r) * N + n));
         }
     }
 }

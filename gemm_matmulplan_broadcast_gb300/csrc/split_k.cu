@@ -109,7 +109,7 @@ split_k_kernel(Problem p, int64_t tiles_m, int64_t tiles_n, int splits, int64_t 
                 if (q0 + j < splits) v += t[j];
         }
         const int64_t gm = m0 + e / TN, gn = n0 + e % TN;
-        if (gm < M && gn < N) Y[gm * N + gn] = Num<T>::from_acc(apply_epilogue<T>(p.epi, v, gm, gn));
+        if (gm < M && gn < N) Y[gm * N + gn] = Num<T>::from_acc(apply_epilogue<T>(p.epi, v, gm, gn, Y + gm * N + gn));
     }
     if (threadIdx.x == 0) ws.counters[tile_id] = 0u;
 }

@@ -372,20 +372,64 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Gemm epilogue on one float32 accumulator of output (i, j) within its item:
-// alpha * acc + beta * C (C of the 16-bit output type); the plain product
-// when epi.mode == 0.
-__device__ __forceinline__ float tc_epi(const Params& p, float acc, int64_t i, int64_t j) {
+__device__ __forceinline__ float widen16(unsigned bits, bool is_bf16) {
+    bits &= 0xFFFFu;
+    return is_bf16 ? __uint_as_float(bits << 16) : __half2float(__ushort_as_half((unsigned short)bits));
+}
+
+// The epilogue on one float32 accumulator of output (i, j) within its item:
+// alpha * acc + beta * C (C of the 16-bit output type), plus the residual
+// whose 16-bit pattern is `rbits` (used when epi.R is set), then the
+// activation; the plain product when epi.mode == 0.
+__device__ __forceinline__ float tc_epi(const Params& p, float acc, int64_t i, int64_t j,
+                                        unsigned rbits = 0) {
     if (p.epi.mode == 0) return acc;
     float y = __fmul_rn(p.epi.alpha_f, acc);
     if (p.epi.C) {
         const unsigned short bits =
             __ldg(static_cast<const unsigned short*>(p.epi.C) + i * p.epi.c_rs + j * p.epi.c_cs);
-        const float c = p.is_bf16 ? __uint_as_float((unsigned)bits << 16)
-                                  : __half2float(__ushort_as_half(bits));
-        y = __fadd_rn(y, __fmul_rn(p.epi.beta_f, c));
+        y = __fadd_rn(y, __fmul_rn(p.epi.beta_f, widen16(bits, p.is_bf16)));
     }
-    return y;
+    if (p.epi.R) y = __fadd_rn(y, widen16(rbits, p.is_bf16));
+    return activate(p.epi.act, y);
+}
+
+// Residual pattern of the 16-bit output element at y (0 without a residual).
+__device__ __forceinline__ unsigned resid16(const Params& p, const unsigned short* y) {
+    return p.epi.R ? (unsigned)__ldg(residual_at(p.epi, y)) : 0u;
+}
+
+// The epilogue over one run of 2*NP accumulators (raw float32 bits in r) of
+// output row `row`, columns col.., narrowed into NP packed pairs.  `dst` is
+// the run's address in Y; the residual is read from the same offset in R,
+// in the `groups` 16-byte groups the store will write.
+template <int NP>
+__device__ __forceinline__ void epi_run(const Params& p, const uint32_t* r, int64_t row,
+                                        int64_t col, const unsigned char* dst, int groups,
+                                        uint32_t* packed) {
+    if (p.epi.mode == 0) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i)
+            packed[i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.is_bf16);
+        return;
+    }
+    uint32_t rr[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) rr[i] = 0u;
+    if (p.epi.R) {
+        const uint4* src = reinterpret_cast<const uint4*>(dst + p.epi.r_delta);
+#pragma unroll
+        for (int q = 0; q < NP / 4; ++q)
+            if (q < groups) {
+                const uint4 v = __ldg(src + q);
+                rr[4 * q] = v.x; rr[4 * q + 1] = v.y; rr[4 * q + 2] = v.z; rr[4 * q + 3] = v.w;
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+        packed[i] = pack2(tc_epi(p, __uint_as_float(r[2 * i]), row, col + 2 * i, rr[i]),
+                          tc_epi(p, __uint_as_float(r[2 * i + 1]), row, col + 2 * i + 1, rr[i] >> 16),
+                          p.is_bf16);
 }
 
 // Sum `count` float32 partial tiles (`stride` floats apart) in order 0, 1,
@@ -423,12 +467,14 @@ __device__ __noinline__ void ordered_sum4x2(const float* base, int64_t stride, i
 // the tile (col < N checked by the caller).
 __device__ __forceinline__ void store4(const Params& p, int64_t item, int64_t row, int64_t col,
                                        float4 v) {
-    v.x = tc_epi(p, v.x, row, col);
-    v.y = tc_epi(p, v.y, row, col + 1);
-    v.z = tc_epi(p, v.z, row, col + 2);
-    v.w = tc_epi(p, v.w, row, col + 3);
-    uint2 o = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
-    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.Y) + ((item * p.M + row) * p.N + col) * 2) = o;
+    unsigned short* y = static_cast<unsigned short*>(p.Y) + (item * p.M + row) * p.N + col;
+    uint2 rr = make_uint2(0u, 0u);
+    if (p.epi.R) rr = __ldg(reinterpret_cast<const uint2*>(residual_at(p.epi, y)));
+    v.x = tc_epi(p, v.x, row, col, rr.x);
+    v.y = tc_epi(p, v.y, row, col + 1, rr.x >> 16);
+    v.z = tc_epi(p, v.z, row, col + 2, rr.y);
+    v.w = tc_epi(p, v.w, row, col + 3, rr.y >> 16);
+    *reinterpret_cast<uint2*>(y) = make_uint2(pack2(v.x, v.y, p.is_bf16), pack2(v.z, v.w, p.is_bf16));
 }
 
 // Swapped operands: the tile holds Y^T (TMEM lane = output column n, TMEM
@@ -440,8 +486,9 @@ __device__ __forceinline__ void store4_t(const Params& p, int64_t item, int64_t 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         if (m0 + i < p.M) {
-            const uint32_t h = pack2(tc_epi(p, f[i], m0 + i, n), 0.f, p.is_bf16);
-            y[(item * p.M + m0 + i) * p.N + n] = (unsigned short)(h & 0xFFFFu);
+            unsigned short* yp = y + (item * p.M + m0 + i) * p.N + n;
+            const uint32_t h = pack2(tc_epi(p, f[i], m0 + i, n, resid16(p, yp)), 0.f, p.is_bf16);
+            *yp = (unsigned short)(h & 0xFFFFu);
         }
     }
 }
@@ -649,10 +696,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         unsigned short* y = static_cast<unsigned short*>(p.Y);
 #pragma unroll
                         for (int m = 0; m < BN; ++m)
-                            if (m < p.M)
-                                y[(item * p.M + m) * p.N + row] = (unsigned short)(
-                                    pack2(tc_epi(p, __uint_as_float(r[m]), m, row), 0.f, p.is_bf16) &
-                                    0xFFFFu);
+                            if (m < p.M) {
+                                unsigned short* yp = y + (item * p.M + m) * p.N + row;
+                                *yp = (unsigned short)(pack2(tc_epi(p, __uint_as_float(r[m]), m, row,
+                                                                    resid16(p, yp)),
+                                                             0.f, p.is_bf16) &
+                                                       0xFFFFu);
+                            }
                     }
                 } else {
                     unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
@@ -664,16 +714,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         else tmem_ld_32x32b_x16(t_base + c, r);
                         const int64_t col = nb * BN + c;
                         if (row_ok && col < p.N) {
-                            uint32_t packed[16];
-#pragma unroll
-                            for (int i = 0; i < CH / 2; ++i)
-                                packed[i] = pack2(tc_epi(p, __uint_as_float(r[2 * i]), row, col + 2 * i),
-                                                  tc_epi(p, __uint_as_float(r[2 * i + 1]), row, col + 2 * i + 1),
-                                                  p.is_bf16);
                             uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                             // N is a multiple of 8: whole 16-byte groups only
                             const int64_t left = (p.N - col) / 8;
                             const int groups = (int)(left < CH / 8 ? left : CH / 8);
+                            uint32_t packed[16];
+                            epi_run<CH / 2>(p, r, row, col, yrow + col * 2, groups, packed);
 #pragma unroll
                             for (int q = 0; q < CH / 8; ++q)
                                 if (q < groups)
@@ -1038,15 +1084,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 tmem_ld_32x32b_x32(t_base + c, r);
                 const int64_t col = nb * 256 + c;
                 if (row_ok && col < p.N) {
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        packed[i] = pack2(tc_epi(p, __uint_as_float(r[2 * i]), row, col + 2 * i),
-                                          tc_epi(p, __uint_as_float(r[2 * i + 1]), row, col + 2 * i + 1),
-                                          p.is_bf16);
                     uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                     const int64_t left = (p.N - col) / 8;
                     const int groups = (int)(left < 4 ? left : 4);
+                    uint32_t packed[16];
+                    epi_run<16>(p, r, row, col, yrow + col * 2, groups, packed);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         if (q < groups)

@@ -56,14 +56,23 @@ typedef enum {
     OLC_ERR_DTYPE = 6,            /* element type not supported                    */
     OLC_ERR_ALIGNMENT = 7,        /* a forced algorithm cannot take these shapes   */
     OLC_ERR_BUFFER_TOO_SMALL = 8, /* a checked execute got a buffer too small      */
-    OLC_ERR_NO_CONSTANT_B = 9,    /* reserved for the constant-B execute           */
+    OLC_ERR_NO_CONSTANT_B = 9,    /* a B-less execute on a plan that owns no B     */
     OLC_ERR_CUDA = 10,            /* a CUDA runtime call failed                    */
     OLC_ERR_DEVICE_TIMEOUT = 11,  /* a bounded device-side wait ran out            */
     OLC_ERR_OOM = 12,             /* workspace allocation failed                   */
     OLC_ERR_INVALID = 13,         /* an argument is out of its documented range    */
     OLC_ERR_WRONG_DEVICE = 14,    /* current device differs from the plan's        */
-    OLC_ERR_SCRATCH_LIMIT = 15    /* needs more than the static scratch array      */
+    OLC_ERR_SCRATCH_LIMIT = 15,   /* needs more than the static scratch array      */
+    OLC_ERR_NEEDS_RESIDUAL = 16   /* the plan fuses a residual: use the fused call */
 } olc_status;
+
+/* Activation of the fused epilogue (applied after bias and residual, before
+ * narrowing).  GELU is the exact form x * Phi(x) = x / 2 * (1 + erf(x / sqrt 2)). */
+typedef enum {
+    OLC_ACT_NONE = 0,
+    OLC_ACT_RELU = 1,             /* max(x, 0); NaN stays NaN                      */
+    OLC_ACT_GELU = 2
+} olc_activation;
 
 /* The algorithm a plan runs ("MatMul Kernel Design", section "Types and
  * algorithm selection": direct execution for small reductions, skinny-M or
@@ -240,6 +249,42 @@ olc_status olc_matmul_execute_constant(const olc_matmul_plan* plan, const void* 
 /* The Gemm with the plan-owned B; as olc_gemm_execute otherwise. */
 olc_status olc_gemm_execute_constant(const olc_matmul_plan* plan, const void* A, const void* C,
                                      void* Y, void* stream);
+
+/* ---- fused epilogue ----------------------------------------------------- */
+
+/*
+ * Fuse elementwise work into the product's store ("Gemm and MatMul
+ * Performance Roadmap", the fused-epilogue row of its opportunity table and
+ * the broadcast / fused epilogue item of its plan: bias, residual, activation
+ * and output conversion in one typed epilogue, with no intermediate tensor).
+ * Per output element, in the accumulator type (float32 for FP16/BF16/FP32,
+ * float64 for FP64), each step rounded on its own:
+ *     v = alpha * acc + beta * C      (Gemm plans; acc for MatMul plans)
+ *     v = v + R                       (residual != 0)
+ *     v = act(v)                      (activation, olc_activation)
+ * then v is narrowed to the output type once.  R has the output's shape,
+ * dtype and dense row-major layout (the full broadcast output for batched
+ * MatMul plans).  activation: OLC_ACT_NONE / RELU / GELU; residual: 0 or 1.
+ * Errors: OLC_ERR_NULL, OLC_ERR_INVALID (value out of range).  A plan with a
+ * residual must be run through olc_matmul_execute_fused; the other execute
+ * calls return OLC_ERR_NEEDS_RESIDUAL for it.  An activation alone applies
+ * to every execute call.
+ */
+olc_status olc_matmul_plan_set_epilogue(olc_matmul_plan* plan, int activation, int residual);
+
+/*
+ * Execute with the fused epilogue.  B: device pointer, or NULL to use the
+ * plan-owned constant B (OLC_ERR_NO_CONSTANT_B when the plan owns none).
+ * C: the Gemm bias (required when the Gemm plan has one, ignored otherwise).
+ * R: residual, device pointer, required when the plan fuses a residual
+ * (OLC_ERR_NULL otherwise); it may not overlap Y unless R == Y exactly
+ * (each element's residual is read by the thread that then writes it).
+ * Pointers the fast kernels read with 16-byte vectors (A, B, Y, R) that are
+ * not 16-byte aligned send the product to the DIRECT kernel.  Asynchronous
+ * on `stream`, as olc_matmul_execute.
+ */
+olc_status olc_matmul_execute_fused(const olc_matmul_plan* plan, const void* A, const void* B,
+                                    const void* C, const void* R, void* Y, void* stream);
 
 /* ---- queries ----------------------------------------------------------- */
 
