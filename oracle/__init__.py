@@ -334,7 +334,8 @@ def gemm_op(a, b, dtype, c=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=Fal
 # the page is silent: the steps run in the order the page lists them --
 # bias, then residual, then activation, then narrowing; the residual has the
 # output's shape and type; the activations are ReLU, max(v, 0), and the exact
-# GELU, v * Phi(v) = v / 2 * (1 + erf(v / sqrt 2)); the residual sum is
+# GELU, v * Phi(v) = v / 2 * (1 + erf(v / sqrt 2)) = v / 2 * erfc(-v / sqrt 2)
+# (the erfc form is the one evaluated); the residual sum is
 # rounded in the accumulator type, the activation is evaluated in float64
 # and rounded to the accumulator type, and the result is narrowed once.
 
@@ -351,8 +352,10 @@ def activation(v: np.ndarray, act: str) -> np.ndarray:
     if act == "relu":
         return np.where(v < 0, 0.0, v)
     if act == "gelu":
-        erf = np.vectorize(math.erf, otypes=[np.float64])
-        return 0.5 * v * (1.0 + erf(v / math.sqrt(2.0)))
+        # Phi(v) = (1 + erf(v / sqrt 2)) / 2 = erfc(-v / sqrt 2) / 2; the erfc
+        # form keeps its relative accuracy for negative v, where 1 + erf cancels
+        erfc = np.vectorize(math.erfc, otypes=[np.float64])
+        return 0.5 * v * erfc(-v / math.sqrt(2.0))
     raise ValueError("unknown activation %r" % act)
 
 
