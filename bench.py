@@ -469,6 +469,101 @@ def measure_secondary(workload, device, peaks, l2):
     return res
 
 
+def graph_time(fn, nsets, stream, reps=10, launches=None):
+    """Per-launch device milliseconds of fn(i) (one launch sequence on
+    operand set i % nsets), captured `launches` times into a CUDA graph and
+    replayed `reps` times between events on the capture stream."""
+    import torch
+    n = launches or max(4, nsets)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fn(i % nsets)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i % nsets)
+        g.replay()
+        stream.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+    stream.synchronize()
+    out = [e0.elapsed_time(e1) / n for e0, e1 in evs]
+    del g
+    return out
+
+
+def measure_fused(device, peaks, l2):
+    """The fused epilogue on the two transformer projections where it
+    belongs: GELU on the up projection [16384, 4096] x [4096, 14336] and a
+    residual add on the down projection [16384, 14336] x [14336, 4096]
+    (BF16).  Each is timed three ways: the plain product, the product with
+    the epilogue fused into its store, and the plain product followed by a
+    separate elementwise pass (torch's own kernel, as the unfused
+    comparison).  The fusion's saving is one read and one write of the
+    output per fused operator."""
+    import torch
+    import numpy as np
+    import torch.nn.functional as F
+    from gemm_matmulplan_broadcast_gb300 import Plan, synth
+    cases = [("up_gelu", (8, 2048, 4096), (4096, 14336), "gelu", False),
+             ("down_residual", (8, 2048, 14336), (14336, 4096), "none", True)]
+    out = []
+    stream = torch.cuda.Stream()
+    for name, a_shape, b_shape, act, resid in cases:
+        a, b = synth.operands(a_shape, b_shape, "bfloat16", synth.normal(1.0), synth.normal(0.02), 2)
+        plain = Plan(a_shape, b_shape, "bfloat16")
+        fused = Plan(a_shape, b_shape, "bfloat16").set_epilogue(act, resid)
+        flop, byts = work_of(a_shape, b_shape, "bfloat16")
+        y_bytes = 2 * int(np.prod(plain.output_shape))
+        nsets = max(2, int(np.ceil(2 * l2 / (byts + y_bytes))))
+        sets = []
+        for i in range(nsets):
+            A = a.to(device) if i == 0 else sets[0][0].clone()
+            B = b.to(device) if i == 0 else sets[0][1].clone()
+            Y = torch.empty(plain.output_shape, dtype=torch.bfloat16, device=device)
+            R = torch.randn(plain.output_shape, dtype=torch.bfloat16, device=device) if resid else None
+            sets.append((A, B, Y, R))
+
+        def run_plain(i):
+            A, B, Y, _ = sets[i]
+            plain.execute(A, B, Y, stream=stream)
+
+        def run_fused(i):
+            A, B, Y, R = sets[i]
+            fused.execute_fused(A, B, Y, R=R, stream=stream)
+
+        def run_unfused(i):
+            A, B, Y, R = sets[i]
+            plain.execute(A, B, Y, stream=stream)
+            if resid:
+                Y.add_(R)
+            else:
+                Y.copy_(F.gelu(Y))
+
+        t = {}
+        for label, fn in (("plain", run_plain), ("fused", run_fused), ("unfused", run_unfused)):
+            t[label] = statistics.median(graph_time(fn, nsets, stream))
+        out.append({
+            "product": name, "a": list(a_shape), "b": list(b_shape),
+            "epilogue": ("residual" if resid else act),
+            "ms_plain": t["plain"], "ms_fused": t["fused"], "ms_unfused": t["unfused"],
+            "tflops_fused": flop / (t["fused"] * 1e-3) / 1e12,
+            "fused_cost_pct": 100.0 * (t["fused"] / t["plain"] - 1.0),
+            "unfused_cost_pct": 100.0 * (t["unfused"] / t["plain"] - 1.0),
+            "timing": "cuda graph of %d launches x 10 replays, %d operand sets" % (max(4, nsets), nsets),
+        })
+        plain.close()
+        fused.close()
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     from gemm_matmulplan_broadcast_gb300 import load, synth
@@ -533,6 +628,7 @@ def run_ours(args):
             names.append("float64_square_chain")
         for wname in names:
             secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
+        secondary["fused_epilogue"] = measure_fused(device, peaks, l2)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -40,15 +40,37 @@ struct Num<__nv_bfloat16> {
     static __device__ __forceinline__ __nv_bfloat16 from_acc(float v) { return __float2bfloat16_rn(v); }
 };
 
+// GELU in float32: y Phi(y) = y / 2 (1 + erf(z)), z = y / sqrt 2, with
+// erfc(|z|) from the rational approximation of Abramowitz and Stegun,
+// Handbook of Mathematical Functions, formula 7.1.26 (absolute error at
+// most 1.5e-7): erfc(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
+// t = 1 / (1 + p x), x >= 0.  Then 1 + erf(z) is 2 - erfc(|z|) for z >= 0 and
+// erfc(|z|) for z < 0, which avoids cancellation on the negative side.  The
+// body is short because the epilogue inlines it once per accumulator
+// register of its unrolled store loop.
+__device__ __forceinline__ float gelu_f32(float y) {
+    const float z = y * 0.70710678118654752f;
+    const float az = fabsf(z);
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, az, 1.0f));
+    float q = fmaf(1.061405429f, t, -1.453152027f);
+    q = fmaf(q, t, 1.421413741f);
+    q = fmaf(q, t, -0.284496736f);
+    q = fmaf(q, t, 0.254829592f);
+    const float c = q * t * __expf(-az * az);            // erfc(|z|)
+    const float one_plus_erf = z >= 0.f ? 2.0f - c : c;  // NaN takes the second arm
+    return 0.5f * y * one_plus_erf;
+}
+
 // The fused epilogue's activation, in the accumulator type.
 __device__ __forceinline__ float activate(int act, float y) {
     if (act == OLC_ACT_RELU) return y < 0.f ? 0.f : y;    // NaN fails the test: stays NaN
-    if (act == OLC_ACT_GELU) return __fmul_rn(__fmul_rn(0.5f, y), __fadd_rn(1.f, erff(__fmul_rn(y, 0.70710678118654752f))));
+    if (act == OLC_ACT_GELU) return gelu_f32(y);
     return y;
 }
 __device__ __forceinline__ double activate(int act, double y) {
     if (act == OLC_ACT_RELU) return y < 0.0 ? 0.0 : y;
-    if (act == OLC_ACT_GELU) return __dmul_rn(__dmul_rn(0.5, y), __dadd_rn(1.0, erf(__dmul_rn(y, 0.70710678118654752440))));
+    // 1 + erf(z) = erfc(-z): no cancellation for negative y
+    if (act == OLC_ACT_GELU) return 0.5 * y * erfc(-y * 0.70710678118654752440);
     return y;
 }
 

@@ -402,34 +402,65 @@ __device__ __forceinline__ unsigned resid16(const Params& p, const unsigned shor
 // The epilogue over one run of 2*NP accumulators (raw float32 bits in r) of
 // output row `row`, columns col.., narrowed into NP packed pairs.  `dst` is
 // the run's address in Y; the residual is read from the same offset in R,
-// in the `groups` 16-byte groups the store will write.
+// in the `groups` 16-byte groups the store will write.  Each step is one
+// loop over the run behind a uniform test, so only the steps a plan uses
+// are executed and the unrolled code stays small.
 template <int NP>
 __device__ __forceinline__ void epi_run(const Params& p, const uint32_t* r, int64_t row,
                                         int64_t col, const unsigned char* dst, int groups,
                                         uint32_t* packed) {
-    if (p.epi.mode == 0) {
+    float v[2 * NP];
 #pragma unroll
-        for (int i = 0; i < NP; ++i)
-            packed[i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.is_bf16);
-        return;
-    }
-    uint32_t rr[NP];
+    for (int i = 0; i < 2 * NP; ++i) v[i] = __uint_as_float(r[i]);
+    if (p.epi.mode != 0) {
+        const float alpha = p.epi.alpha_f;
+        if (alpha != 1.0f) {
 #pragma unroll
-    for (int i = 0; i < NP; ++i) rr[i] = 0u;
-    if (p.epi.R) {
-        const uint4* src = reinterpret_cast<const uint4*>(dst + p.epi.r_delta);
+            for (int i = 0; i < 2 * NP; ++i) v[i] = __fmul_rn(alpha, v[i]);
+        }
+        if (p.epi.C) {
+            const unsigned short* c = static_cast<const unsigned short*>(p.epi.C) + row * p.epi.c_rs;
+            const float beta = p.epi.beta_f;
 #pragma unroll
-        for (int q = 0; q < NP / 4; ++q)
-            if (q < groups) {
-                const uint4 v = __ldg(src + q);
-                rr[4 * q] = v.x; rr[4 * q + 1] = v.y; rr[4 * q + 2] = v.z; rr[4 * q + 3] = v.w;
+            for (int i = 0; i < 2 * NP; ++i)
+                v[i] = __fadd_rn(v[i], __fmul_rn(beta, widen16(__ldg(c + (col + i) * p.epi.c_cs), p.is_bf16)));
+        }
+        if (p.epi.R) {
+            const uint4* src = reinterpret_cast<const uint4*>(dst + p.epi.r_delta);
+            uint32_t rr[NP];
+#pragma unroll
+            for (int q = 0; q < NP / 4; ++q) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (q < groups) w = __ldg(src + q);
+                rr[4 * q] = w.x; rr[4 * q + 1] = w.y; rr[4 * q + 2] = w.z; rr[4 * q + 3] = w.w;
             }
+#pragma unroll
+            for (int i = 0; i < 2 * NP; ++i)
+                v[i] = __fadd_rn(v[i], widen16(rr[i >> 1] >> (16 * (i & 1)), p.is_bf16));
+        }
+        if (p.epi.act == OLC_ACT_RELU) {
+#pragma unroll
+            for (int i = 0; i < 2 * NP; ++i) v[i] = v[i] < 0.f ? 0.f : v[i];
+        } else if (p.epi.act == OLC_ACT_GELU) {
+#pragma unroll
+            for (int i = 0; i < 2 * NP; ++i) v[i] = gelu_f32(v[i]);
+        }
     }
 #pragma unroll
-    for (int i = 0; i < NP; ++i)
-        packed[i] = pack2(tc_epi(p, __uint_as_float(r[2 * i]), row, col + 2 * i, rr[i]),
-                          tc_epi(p, __uint_as_float(r[2 * i + 1]), row, col + 2 * i + 1, rr[i] >> 16),
-                          p.is_bf16);
+    for (int i = 0; i < NP; ++i) packed[i] = pack2(v[2 * i], v[2 * i + 1], p.is_bf16);
+}
+
+// Ask L2 for the residual of one output row run (cols columns from (row,
+// col0) of item `item`), so the epilogue's residual loads hit L2.  The run
+// starts on a 16-byte boundary and is a whole number of 16-byte groups
+// (N is a multiple of 8 on the tensor-core path).
+__device__ __forceinline__ void prefetch_residual(const Params& p, int64_t item, int64_t row,
+                                                  int64_t col0, int64_t cols) {
+    if (!p.epi.R || cols <= 0) return;
+    const unsigned char* src = static_cast<const unsigned char*>(p.epi.R) +
+                               ((item * p.M + row) * p.N + col0) * 2;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)(cols * 2))
+                 : "memory");
 }
 
 // Sum `count` float32 partial tiles (`stride` floats apart) in order 0, 1,
@@ -680,6 +711,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         while (cursor_next(p, cur, tile, slice, kb0, kb1, parts)) {
             int64_t item, mb, nb;
             tile_coords(p, tile, item, mb, nb);
+            if (!SWAP && (!SPLIT || parts == 1) && mb * BM + row_in_tile < p.M)
+                prefetch_residual(p, item, mb * BM + row_in_tile, nb * BN, min64(BN, p.N - nb * BN));
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
             tc_fence_after();
             const int64_t row = mb * BM + row_in_tile;
@@ -1071,6 +1104,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int64_t t = cluster_id(); t < total; t += cluster_count()) {
             int64_t item, mb, nb;
             coords(t, item, mb, nb);
+            if (mb * 256 + rank * 128 + row_in_tile < p.M)
+                prefetch_residual(p, item, mb * 256 + rank * 128 + row_in_tile, nb * 256,
+                                  min64(256, p.N - nb * 256));
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
             tc_fence_after();
             const int64_t row = mb * 256 + rank * 128 + row_in_tile;

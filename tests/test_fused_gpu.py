@@ -174,3 +174,34 @@ def test_fused_with_constant_b_and_errors():
     ref, s = oracle.matmul_fused(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype,
                                  synth.to_numpy_storage(r), "relu")
     compare(Y1.cpu(), ref, s, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float64"])
+def test_device_gelu_within_its_error_bound(dtype):
+    """GELU alone (K = 1, B = [[1]], so the accumulator is x exactly) against
+    the exact x Phi(x).  FLOAT uses erfc from Abramowitz and Stegun 7.1.26,
+    absolute error at most 1.5e-7, so |gelu - exact| <= |x| / 2 (1.5e-7 +
+    float32 evaluation rounding); the test allows |x| / 2 * 1e-6.  DOUBLE
+    uses the library erfc (x / 2 * erfc(-x / sqrt 2)): a few units in the last
+    place, times erfc's condition number for the argument's rounding."""
+    xs = np.concatenate([np.linspace(-12, 12, 20001), [0.0, -0.0, 1e-30, -1e-30, 40.0, -40.0,
+                                                       1e6, -1e6]])
+    np_t = np.float32 if dtype == "float32" else np.float64
+    x = xs.astype(np_t)
+    a = torch.from_numpy(x.reshape(-1, 1).copy())
+    b = torch.ones(1, 1, dtype=a.dtype)
+    y, _, _, _ = _fused(a, b, None, dtype, "gelu")
+    y = y.numpy().reshape(-1).astype(np.float64)
+    exact = oracle.activation(x.astype(np.float64), "gelu")
+    err = np.abs(y - exact)
+    if dtype == "float32":
+        bound = 0.5 * np.abs(x.astype(np.float64)) * 1e-6 + 1e-38
+    else:
+        # erfc(u) has condition number about 2 u^2: the argument's own rounding
+        # (x / sqrt 2 here, multiplied by 1 / sqrt 2 there) moves it by that
+        xd = x.astype(np.float64)
+        bound = np.abs(exact) * 2 * (xd * xd + 16) * 2.3e-16 + 1e-300   # both sides
+    worst = int(np.argmax(err - bound))
+    assert np.all(err <= bound), "x=%r gpu %r exact %r" % (x[worst], y[worst], exact[worst])
+    nan = _fused(torch.tensor([[float("nan")]], dtype=a.dtype), b, None, dtype, "gelu")[0]
+    assert torch.isnan(nan).all()
