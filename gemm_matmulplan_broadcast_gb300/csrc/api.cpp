@@ -110,6 +110,7 @@ Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, voi
     pr.items = p->items;
     pr.map = p->map;
     pr.split_hint = p->split_hint;
+    pr.variant = p->tc_variant;
     pr.a_trans = p->trans_a;
     pr.b_trans = p->trans_b;
     // Gemm: alpha * acc + beta * C, then the fused residual and activation;
@@ -254,7 +255,7 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
             p->counter_count = skinny_m_counter_count(dt, pr, p->splits, p->sm_count);
         }
     }
-    if (p->partial_bytes == 0) return OLC_OK;
+    if (p->partial_bytes == 0 && p->counter_count == 0) return OLC_OK;
     const size_t counters_off = (p->partial_bytes + 255) / 256 * 256;
     p->ws_bytes = counters_off + p->counter_count * sizeof(unsigned int);
     if (p->device < 0) return OLC_OK;   // allocated at the first execute
@@ -313,7 +314,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     if (p->device < 0) {
         // planned on a machine view without a device: bind now
         mp->device = cur;
-        if (p->partial_bytes > 0 && !p->workspace) {
+        if ((p->partial_bytes > 0 || p->counter_count > 0) && !p->workspace) {
             olc_status st = prepare_algorithm(mp);
             if (st != OLC_OK) return st;
         }
@@ -544,7 +545,7 @@ olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, 
     if (plan->device >= 0 && cur != plan->device) return OLC_ERR_WRONG_DEVICE;
     if (plan->device < 0) {
         plan->device = cur;
-        if (plan->partial_bytes > 0 && !plan->workspace) {
+        if ((plan->partial_bytes > 0 || plan->counter_count > 0) && !plan->workspace) {
             olc_status st = prepare_algorithm(plan);
             if (st != OLC_OK) return st;
         }

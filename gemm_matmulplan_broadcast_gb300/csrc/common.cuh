@@ -110,6 +110,12 @@ __device__ __forceinline__ typename Num<T>::acc_t apply_epilogue(const Epilogue&
     }
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Operand element offsets of output batch item z.
 __device__ __forceinline__ void batch_offsets(const BatchMap& m, int64_t z, int64_t& a_off,
                                               int64_t& b_off) {

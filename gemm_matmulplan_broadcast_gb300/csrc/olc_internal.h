@@ -50,6 +50,7 @@ struct Problem {
     int64_t items;
     BatchMap map;
     int split_hint;   // > 0: K slices requested by a tuning override, 0: automatic
+    int variant;      // kernel-family override (0: automatic; see olc_matmul_plan_set_tc_variant)
     int a_trans, b_trans;
     Epilogue epi;
 };

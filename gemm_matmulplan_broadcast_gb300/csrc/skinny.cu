@@ -8,7 +8,9 @@
 // Both are bound by HBM bandwidth (arithmetic intensity of a few flop/byte),
 // so the kernels are built around wide coalesced loads and enough loads in
 // flight, not around arithmetic.
+#include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -449,6 +451,315 @@ static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// SKINNY_N for FLOAT16 / BFLOAT16: A streamed with 16-byte loads straight
+// into registers, the products on the tensor cores with mma.sync.m16n8k16
+// (float32 accumulation), B in shared memory.
+//
+// A unit is 16 rows of A (all K); one persistent block per SM owns every
+// gridDim-th unit, and its 16 warps each take one sixteenth of K of every
+// unit.  The warps run independently through the block's units: a warp
+// writes its 16 x 8 (or 16 x 16) float32 partial tile to one of kSnSlots
+// shared-memory slots and counts itself in; the sixteenth warp to arrive
+// sums the sixteen partials in K-range order (a fixed order: the result does
+// not depend on timing), applies the epilogue and stores the rows, then
+// frees the slot.  No block-wide barrier stops the loads, so while some
+// warps reduce or wait, the others keep their 16-byte loads in flight.
+// Register loads are used instead of TMA tiles: 512 threads per SM with
+// sixteen 16-byte loads each stream A at close to the HBM rate, where 2-D
+// tensor boxes of 128-byte rows did not.
+//
+// Thread (g = lane / 4, t = lane % 4) loads A[row g][k0 + 8t .. 8t + 7] and
+// A[row g + 8][...] (16 bytes each) for every 32-wide K chunk k0.  The MMA's
+// K positions are relabelled so that these are exactly the thread's A
+// fragment of two m16n8k16 products: the first takes physical k = 8t + {0,
+// 1} and 8t + {2, 3} for its logical k = 2t + {0, 1} and 2t + 8 + {0, 1},
+// the second 8t + {4 .. 7}.  Relabelling the terms of a dot product does
+// not change which products are summed, so each output is still the full
+// dot product.  The B fragments under the same relabelling come from one
+// ldmatrix.x4.trans per chunk: B sits in shared memory as 16-byte rows (8
+// columns, one plane per 8 columns), and the lanes hand ldmatrix the row
+// addresses in the relabelled order (matrix i, row r: k = k0 + 8 (r / 2) +
+// 2i + r % 2), so the transposed 8 x 8 matrices land as exactly the b
+// registers of the two products.  Rows are placed with an XOR swizzle (row
+// k at 16-byte slot k ^ (((k >> 3) & 3) << 1)) so that the eight rows of
+// each matrix fall in eight different bank groups.
+
+constexpr int kSnWarps = 16;
+constexpr int kSnSlots = 4;
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1, bool bf16) {
+    if (bf16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+__device__ __forceinline__ uint4 ldmatrix_x4_trans(uint32_t addr) {
+    uint4 r;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+// 16-byte slot of B row k in its plane
+__device__ __forceinline__ int64_t sn_slot(int64_t k) { return k ^ (((k >> 3) & 3) << 1); }
+
+// K per warp (whole 32-wide chunks) and the rows of a B plane (every warp's
+// range; rows at or past K hold zeros).
+static int64_t sn_k_per_warp(int64_t K) { return ceil_div(ceil_div(K, kSnWarps), 32) * 32; }
+static int64_t sn_rows(int64_t K) { return sn_k_per_warp(K) * kSnWarps; }
+
+template <int NB>
+struct SnShared {
+    float red[kSnSlots][kSnWarps][16][NB * 8 + 1];   // partial tiles (+1: no bank conflicts)
+    int arrived[kSnSlots];                          // warps counted into the slot's unit
+    int uses[kSnSlots];                             // reductions completed in the slot
+    int abort;
+};
+
+template <typename T, int NB>
+__global__ void __launch_bounds__(kSnWarps * 32, 1)
+skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int* err) {
+    constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int R = 8;                                   // K chunks in flight per thread
+    extern __shared__ __align__(16) uint4 bs[];            // [NB planes][rows] 16-byte B rows
+    __shared__ SnShared<NB> sh;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t M = p.M, N = p.N, K = p.K;
+    // K range of this warp: rotated by the block index, so that at the
+    // start the blocks ask L2 for different lines of B instead of all for
+    // the same ones (the partials are still summed in K-range order)
+    const int krange = (warp + (int)(blockIdx.x % kSnWarps)) % kSnWarps;
+    const int64_t kbeg = (int64_t)krange * kw;
+    const unsigned short* A = static_cast<const unsigned short*>(p.A);
+
+    // This warp's work is one sequence of 32-wide K chunks: chunk c of its K
+    // range for each of the block's units in turn.  A ring of R register
+    // slots keeps R chunks (2 x 16 bytes per thread each) in flight: chunk
+    // i + R is requested as soon as chunk i has been multiplied.
+    const int cpu = kw / 32;                               // chunks per unit
+    const int my_units = (int)((units - blockIdx.x + gridDim.x - 1) / gridDim.x);
+    // the next chunk to request: unit index (within this block) and chunk
+    int lu = 0, lc = 0;
+    auto load = [&](uint4& va, uint4& vb) {
+        va = make_uint4(0u, 0u, 0u, 0u);
+        vb = va;
+        if (lu < my_units) {
+            const int64_t r0 = (blockIdx.x + (int64_t)lu * gridDim.x) * 16;
+            const int64_t k = kbeg + lc * 32 + 8 * t;      // K is a multiple of 8
+            const int64_t ra = r0 + g, rb = r0 + g + 8;
+            if (k < K && ra < M) va = __ldcs(reinterpret_cast<const uint4*>(A + ra * K + k));
+            if (k < K && rb < M) vb = __ldcs(reinterpret_cast<const uint4*>(A + rb * K + k));
+        }
+        if (++lc == cpu) { lc = 0; ++lu; }
+    };
+    if (threadIdx.x < kSnSlots) {
+        sh.arrived[threadIdx.x] = 0;
+        sh.uses[threadIdx.x] = 0;
+    }
+    if (threadIdx.x == 0) sh.abort = 0;
+    __syncthreads();   // slot counters initialised before any warp arrives
+
+    // Each warp stages only the B rows of its own K range, so it never waits
+    // for the others.  With N == 8 or 16 every 16-byte vector of B is one
+    // row of one plane and is stored as it is; other N are padded to 8
+    // columns element by element.  Rows at or past K are zero.
+    {
+        const int64_t kend = min64(K, kbeg + kw);
+        if (N == 8 * NB) {
+            const uint4* B4 = static_cast<const uint4*>(p.B);
+            for (int v0 = lane; v0 < kw * NB; v0 += 4 * 32) {
+                uint4 w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int v = v0 + q * 32;
+                    const int64_t k = kbeg + v / NB;
+                    w[q] = (v < kw * NB && k < kend) ? __ldg(B4 + k * NB + v % NB)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int v = v0 + q * 32;
+                    if (v < kw * NB) bs[(v % NB) * rows + sn_slot(kbeg + v / NB)] = w[q];
+                }
+            }
+        } else {
+            const unsigned short* B = static_cast<const unsigned short*>(p.B);
+            for (int v = lane; v < kw * NB; v += 32) {
+                const int j = v % NB;
+                const int64_t k = kbeg + v / NB;
+                uint32_t h[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int64_t n = j * 8 + c;
+                    const uint32_t e = (k < kend && n < N) ? (uint32_t)B[k * N + n] : 0u;
+                    h[c >> 1] |= e << (16 * (c & 1));
+                }
+                bs[j * rows + sn_slot(k)] = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+        }
+        __syncwarp();
+    }
+    uint4 va[R], vb[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) load(va[q], vb[q]);
+
+    // ldmatrix row address of this lane for chunk base k0: matrix i = lane /
+    // 8, row r = lane % 8 -> k = k0 + 8 (r / 2) + 2 i + r % 2
+    const int mi = lane >> 3, mr = lane & 7;
+    const int koff = 8 * (mr >> 1) + 2 * mi + (mr & 1);
+    const uint32_t bs_base = static_cast<uint32_t>(__cvta_generic_to_shared(bs));
+
+    T* Y = static_cast<T*>(p.Y);
+    volatile int* uses = sh.uses;
+    volatile int* abort_flag = &sh.abort;
+    // two accumulator chains per n-block (the two MMAs of a chunk), summed
+    // when the unit is done
+    float d0[NB][4], d1[NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d0[j][e] = d1[j][e] = 0.f;
+
+    // one unit's partial tile -> its slot; the sixteenth warp reduces
+    auto flush = [&](int ui) -> bool {
+        const int64_t r0 = ((int64_t)blockIdx.x + (int64_t)ui * gridDim.x) * 16;
+        const int slot = (int)(ui % kSnSlots);
+        const int use = (int)(ui / kSnSlots);
+        int ok = 1;
+        if (lane == 0 && uses[slot] != use) {              // bounded wait for the slot
+            const uint64_t t0 = globaltimer_ns();
+            while (uses[slot] != use) {
+                if (*abort_flag || globaltimer_ns() - t0 > 2000000000ull) {
+                    if (!*abort_flag) {
+                        *abort_flag = 1;
+                        raise_device_error(err, kErrWaitTimeout);
+                    }
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        // row g: elements 0, 1 (columns 2t, 2t + 1); row g + 8: elements 2, 3;
+        // partials are filed by K range
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            sh.red[slot][krange][g][j * 8 + 2 * t] = d0[j][0] + d1[j][0];
+            sh.red[slot][krange][g][j * 8 + 2 * t + 1] = d0[j][1] + d1[j][1];
+            sh.red[slot][krange][g + 8][j * 8 + 2 * t] = d0[j][2] + d1[j][2];
+            sh.red[slot][krange][g + 8][j * 8 + 2 * t + 1] = d0[j][3] + d1[j][3];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d0[j][e] = d1[j][e] = 0.f;
+        }
+        __threadfence_block();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&sh.arrived[slot], 1) == kSnWarps - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence_block();
+            for (int e = lane; e < 16 * NB * 8; e += 32) {
+                const int r = e / (NB * 8), c = e % (NB * 8);
+                const int64_t row = r0 + r;
+                if (row >= M || c >= N) continue;
+                float v = sh.red[slot][0][r][c];
+#pragma unroll
+                for (int w = 1; w < kSnWarps; ++w) v += sh.red[slot][w][r][c];
+                Y[row * N + c] = Num<T>::from_acc(apply_epilogue<T>(p.epi, v, row, c, Y + row * N + c));
+            }
+            __syncwarp();
+            if (lane == 0) {
+                sh.arrived[slot] = 0;
+                __threadfence_block();
+                uses[slot] = use + 1;
+            }
+        }
+        return true;
+    };
+
+    // the chunk being multiplied: unit index (within this block) and chunk
+    int cu = 0, cc = 0;
+    while (cu < my_units) {
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            if (cu >= my_units) break;
+            const int64_t krow = sn_slot(kbeg + cc * 32 + koff);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const uint4 b = ldmatrix_x4_trans(bs_base + (uint32_t)((j * rows + krow) * 16));
+                mma_16816(d0[j], va[q].x, vb[q].x, va[q].y, vb[q].y, b.x, b.y, BF16);
+                mma_16816(d1[j], va[q].z, vb[q].z, va[q].w, vb[q].w, b.z, b.w, BF16);
+            }
+            load(va[q], vb[q]);
+            if (++cc == cpu) {
+                if (!flush(cu)) return;
+                cc = 0;
+                ++cu;
+            }
+        }
+    }
+}
+
+// Largest B (bytes, 16-byte rows per 8 columns) the streaming kernel keeps
+// in shared memory (one block per SM, next to the partial-tile slots).
+constexpr int64_t kSnMaxBtBytes = 150 * 1024;
+static_assert(kSnMaxBtBytes + sizeof(SnShared<2>) <= 227 * 1024, "shared memory of one block");
+
+bool skinny_n_mma_ok(olc_dtype dt, const Problem& p) {
+    if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;
+    if (p.N > 16 || (p.K % 8) != 0) return false;
+    // one B for every unit: a single item, or items folded into rows
+    if (p.items != 1) return false;
+    // above 8 columns the tcgen05 16-column kernel is faster (two mma.sync
+    // per 8 columns cost more than one 128 x 16 tcgen05 MMA)
+    if (p.N > 8 && p.variant != 2) return false;
+    const int nb = p.N <= 8 ? 1 : 2;                       // 8-column planes
+    return (int64_t)nb * sn_rows(p.K) * 16 <= kSnMaxBtBytes;
+}
+
+template <typename T, int NB>
+static cudaError_t launch_skinny_n_mma_t(const Problem& p, int sm_count, cudaStream_t s) {
+    const int64_t units = ceil_div(p.M, 16);
+    const int kw = (int)sn_k_per_warp(p.K);
+    const int64_t rows = sn_rows(p.K);
+    const size_t smem = (size_t)NB * rows * 16;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [&] {
+        attr = cudaFuncSetAttribute(skinny_n_mma_kernel<T, NB>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSnMaxBtBytes);
+    });
+    if (attr != cudaSuccess) return attr;
+    const int64_t grid = min64(units, (int64_t)sm_count);
+    skinny_n_mma_kernel<T, NB><<<(unsigned)grid, kSnWarps * 32, smem, s>>>(p, units, kw, rows,
+                                                                            device_error_word());
+    return cudaGetLastError();
+}
+
+static cudaError_t launch_skinny_n_mma(olc_dtype dt, const Problem& p, int sm_count,
+                                       cudaStream_t s) {
+    if (dt == OLC_FLOAT16)
+        return p.N <= 8 ? launch_skinny_n_mma_t<__half, 1>(p, sm_count, s)
+                        : launch_skinny_n_mma_t<__half, 2>(p, sm_count, s);
+    return p.N <= 8 ? launch_skinny_n_mma_t<__nv_bfloat16, 1>(p, sm_count, s)
+                    : launch_skinny_n_mma_t<__nv_bfloat16, 2>(p, sm_count, s);
+}
+
 static bool skinny_n_on_tc(olc_dtype dt, const Problem& p) {
     return (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K);
 }
@@ -466,6 +777,7 @@ cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, const 
     // FLOAT16 / BFLOAT16 with 16-byte row strides: stream A through the
     // tensor cores with 16-column tiles (8 FMAs per A element would need most
     // of the SIMT FMA rate at full HBM bandwidth)
+    if (p.variant != 1 && skinny_n_mma_ok(dt, p)) return launch_skinny_n_mma(dt, p, sm_count, s);
     if (skinny_n_on_tc(dt, p)) return launch_skinny_n_tc(dt, p, sm_count, ws, s);
     return dispatch_dtype(dt, [&](auto tag) {
         using T = decltype(tag);

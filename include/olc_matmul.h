@@ -332,10 +332,14 @@ olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits);
 /* K slices the plan currently uses (1 when it does not split). */
 int olc_matmul_plan_splits(const olc_matmul_plan* plan);
 
-/* Tuning override of the GENERAL_TC tiling: 0 = automatic, 1 = one CTA per
- * 128 x 256 output tile, 2 = pairs of CTAs on one TPC sharing a 256 x 256
- * tile (tcgen05 cta_group::2).  Results are identical within the parity
- * tolerance either way.  Errors: OLC_ERR_NULL, OLC_ERR_INVALID. */
+/* Tuning override of the kernel family.  GENERAL_TC plans: 0 = automatic,
+ * 1 = one CTA per 128 x 256 output tile, 2 = pairs of CTAs on one TPC
+ * sharing a 256 x 256 tile (tcgen05 cta_group::2).  SKINNY_N plans of
+ * FLOAT16 / BFLOAT16: 0 = automatic, 1 = the tcgen05 16-column kernel,
+ * 2 = the register-streaming mma.sync kernel wherever it applies (one B for
+ * all rows, K a multiple of 8, B^T within its shared-memory budget).
+ * Results are identical within the parity tolerance either way.  Errors:
+ * OLC_ERR_NULL, OLC_ERR_INVALID. */
 olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant);
 
 /* Kernel launches one execute of this plan makes (0 for EMPTY). */

@@ -244,6 +244,10 @@ def test_tc_split_k(dtype, shapes):
 
 TC_SKINNY_N_SHAPES = [
     ((4096, 1024), (1024, 8)),         # 32 row tiles: stream-K shares over the SMs
+    ((16384, 4096), (4096, 8)),        # the FP16 corner's skinny-N product
+    ((1000, 6144), (6144, 5)),         # widest K whose transposed B fits; row tail; N < 8
+    ((777, 8200), (8200, 12)),         # K too long for the staged B: tcgen05 kernel
+    ((3, 50, 40), (40, 3)),            # K not a multiple of 32, tiny rows per item
     ((2, 2048, 512), (512, 16)),       # folded batch, stream-K
     ((256, 1024), (1024, 8)),
     ((1000, 520), (520, 16)),
@@ -254,12 +258,27 @@ TC_SKINNY_N_SHAPES = [
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
 @pytest.mark.parametrize("shapes", TC_SKINNY_N_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
-def test_tc_skinny_n(dtype, shapes):
+@pytest.mark.parametrize("variant", [0, 1, 2], ids=["auto", "tcgen05", "mma_sync_stream"])
+def test_tc_skinny_n(dtype, shapes, variant):
+    """Both FLOAT16 / BFLOAT16 skinny-N kernels: the register-streaming
+    mma.sync kernel (the automatic choice up to 8 columns; forced with
+    variant 2 up to 16) and the tcgen05 16-column kernel (variant 1)."""
     a_shape, b_shape = shapes
-    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=13)
-    check_product(a, b, dtype, algorithm="skinny_n")
-    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=13)
-    check_product(ai, bi, dtype, algorithm="skinny_n", exact=True)
+    for dist, seed, exact in ((synth.normal(1.0), 13, False), (synth.SMALL_INT, 13, True)):
+        a, b = synth.operands(a_shape, b_shape, dtype, dist,
+                              synth.normal(0.02) if not exact else synth.SMALL_INT, seed=seed)
+        A, B = a.cuda(), b.cuda()
+        with Plan(a.shape, b.shape, dtype) as p:
+            p.force("skinny_n")
+            p.set_tc_variant(variant)
+            n = int(np.prod(p.output_shape))
+            buf = torch.full((n + 64,), float("nan"), dtype=A.dtype, device="cuda")
+            Y = buf[:n].view(p.output_shape)
+            p.execute_checked(A, B, Y)
+            torch.cuda.synchronize()
+            assert torch.isnan(buf[n:].float()).all()
+        y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+        compare(Y.cpu(), y_ref, s, dtype, exact=exact)
 
 
 TC_SKINNY_M_SHAPES = [
