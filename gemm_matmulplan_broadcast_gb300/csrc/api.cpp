@@ -740,7 +740,7 @@ olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant) {
     if (!plan) return OLC_ERR_NULL;
     if (variant < 0 || variant > 2) return OLC_ERR_INVALID;
     plan->tc_variant = variant;
-    return OLC_OK;
+    return prepare_algorithm(plan);   // the workspace depends on the kernel family
 }
 
 int olc_matmul_plan_launches(const olc_matmul_plan* plan) {
