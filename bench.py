@@ -272,7 +272,11 @@ def time_steps(items, steps, stream):
 
 def time_e2e(items, steps, stream):
     """End to end through olc_matmul_execute_host: pinned host inputs copied
-    in, kernels, result copied out, every step."""
+    in, kernels, result copied out, every step.  The products of a step are
+    independent, so each is issued on its own stream (a caller would do the
+    same); within a product the library pipelines copies and compute over
+    row chunks.  Timed by events on `stream`, which waits for every product
+    stream before the end event."""
     import torch
     host = []
     for it in items:
@@ -283,12 +287,20 @@ def time_e2e(items, steps, stream):
     h2d = sum(h[0].numel() * h[0].element_size() + h[1].numel() * h[1].element_size()
               for h in host)
     d2h = sum(h[2].numel() * h[2].element_size() for h in host)
+    streams = [torch.cuda.Stream() for _ in items]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
 
     def one_step():
-        for it, (ah, bh, yh) in zip(items, host):
-            it["plan"].execute_host(ah, bh, yh, it["A"], it["B"], it["Y"], stream=stream)
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for it, (ah, bh, yh), st in zip(items, host, streams):
+            st.wait_event(fork)
+            it["plan"].execute_host(ah, bh, yh, it["A"], it["B"], it["Y"], stream=st)
+        for st in streams:
+            done = torch.cuda.Event()
+            done.record(st)
+            stream.wait_event(done)
 
     one_step()
     stream.synchronize()

@@ -57,6 +57,12 @@ struct olc_matmul_plan {
     // fused epilogue: activation, and a residual in the output's layout
     int act;
     int residual;
+    // host-buffer pipeline: copy streams and per-chunk events (created at
+    // the first pipelined olc_matmul_execute_host)
+    cudaStream_t copy_in, copy_out;
+    cudaEvent_t ev_start, ev_b, ev_done;
+    cudaEvent_t ev_a[8], ev_y[8];
+    int pipe_ready;
     int device;                  // -1: planned without a device
     int sm_count;
     void* workspace;
@@ -523,6 +529,22 @@ olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const vo
 void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
     if (!plan) return;
     free_workspace(plan);
+    if (plan->pipe_ready) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (plan->device >= 0 && cur != plan->device) cudaSetDevice(plan->device);
+        cudaStreamDestroy(plan->copy_in);
+        cudaStreamDestroy(plan->copy_out);
+        cudaEventDestroy(plan->ev_start);
+        cudaEventDestroy(plan->ev_b);
+        cudaEventDestroy(plan->ev_done);
+        for (int i = 0; i < 8; ++i) {
+            cudaEventDestroy(plan->ev_a[i]);
+            cudaEventDestroy(plan->ev_y[i]);
+        }
+        if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
+        cudaGetLastError();
+    }
     if (plan->const_b) {
         int cur = -1;
         cudaGetDevice(&cur);
@@ -643,6 +665,39 @@ olc_status olc_matmul_execute_checked(const olc_matmul_plan* plan, const void* A
     return flags ? OLC_ERR_DEVICE_TIMEOUT : OLC_OK;
 }
 
+namespace {
+
+// Row chunks of a host-buffer product that can be pipelined (copy in, compute
+// and copy out of different chunks at once): one 2-D product (the batch, if
+// any, folded into rows), a workspace-free algorithm, no residual, and enough
+// rows for several tensor-core row tiles per chunk.  0 = not pipelined.
+int host_chunks(const olc_matmul_plan* p) {
+    if (p->items != 1 || p->K == 0 || p->residual) return 0;
+    if (p->algo != OLC_ALGO_GENERAL_TC && p->algo != OLC_ALGO_GENERAL_SIMT) return 0;
+    if (p->is_gemm && (p->trans_a || (p->c_rank >= 0 && p->c_rs != 0))) return 0;
+    const int64_t rows = p->rows;
+    if (rows < 4 * 1024) return 0;
+    return 4;
+}
+
+olc_status pipe_init(olc_matmul_plan* p) {
+    if (p->pipe_ready) return OLC_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&p->copy_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->copy_out, cudaStreamNonBlocking);
+    cudaEvent_t* evs[3] = {&p->ev_start, &p->ev_b, &p->ev_done};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+    for (int i = 0; i < 8 && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&p->ev_a[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_y[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    p->pipe_ready = 1;
+    return OLC_OK;
+}
+
+}  // namespace
+
 olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_host,
                                    const void* B_host, void* Y_host, void* A_dev, void* B_dev,
                                    void* Y_dev, void* stream) {
@@ -652,6 +707,61 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_ho
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t eb = elem_bytes(plan->dtype);
     if (!Y_host || !Y_dev) return OLC_ERR_NULL;
+    const int chunks = host_chunks(plan);
+    if (chunks > 0) {
+        if (!A_host || !B_host || !A_dev || !B_dev) return OLC_ERR_NULL;
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess) return from_cuda(cudaErrorNoDevice);
+        if (plan->device >= 0 && cur != plan->device) return OLC_ERR_WRONG_DEVICE;
+        olc_matmul_plan* mp = const_cast<olc_matmul_plan*>(plan);
+        if (mp->device < 0) mp->device = cur;
+        olc_status st = pipe_init(mp);
+        if (st != OLC_OK) return st;
+        // copy_in: B, then A in row chunks; the user stream computes chunk i
+        // once its rows have arrived; copy_out returns chunk i's rows of Y
+        // once they are computed; the user stream waits for the last copy.
+        const int64_t rows = plan->rows, K = plan->K, N = plan->N;
+        const int64_t step = (rows / chunks + 255) / 256 * 256;
+        const size_t b_bytes = (size_t)(numel(plan->b_shape, plan->b_rank) * eb);
+        cudaError_t e = cudaEventRecord(mp->ev_start, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(mp->copy_in, mp->ev_start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(mp->copy_out, mp->ev_start, 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, mp->copy_in);
+        if (e == cudaSuccess) e = cudaEventRecord(mp->ev_b, mp->copy_in);
+        int nc = 0;
+        for (int64_t r0 = 0; r0 < rows && e == cudaSuccess; r0 += step, ++nc) {
+            const int64_t rn = step < rows - r0 ? step : rows - r0;
+            e = cudaMemcpyAsync(static_cast<unsigned char*>(A_dev) + r0 * K * eb,
+                                static_cast<const unsigned char*>(A_host) + r0 * K * eb,
+                                (size_t)(rn * K * eb), cudaMemcpyHostToDevice, mp->copy_in);
+            if (e == cudaSuccess) e = cudaEventRecord(mp->ev_a[nc], mp->copy_in);
+        }
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, mp->ev_b, 0);
+        nc = 0;
+        for (int64_t r0 = 0; r0 < rows && e == cudaSuccess; r0 += step, ++nc) {
+            const int64_t rn = step < rows - r0 ? step : rows - r0;
+            e = cudaStreamWaitEvent(s, mp->ev_a[nc], 0);
+            if (e != cudaSuccess) break;
+            // chunk rows r0 .. r0 + rn of the same product (row-major A and Y)
+            olc_matmul_plan sub = *plan;
+            sub.rows = rn;
+            sub.M = rn;
+            const void* Ac = static_cast<const unsigned char*>(A_dev) + r0 * K * eb;
+            void* Yc = static_cast<unsigned char*>(Y_dev) + r0 * N * eb;
+            const void* Cc = nullptr;
+            st = run(&sub, Ac, B_dev, Yc, s, Cc);
+            if (st != OLC_OK) return st;
+            e = cudaEventRecord(mp->ev_y[nc], s);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(mp->copy_out, mp->ev_y[nc], 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(static_cast<unsigned char*>(Y_host) + r0 * N * eb,
+                                    static_cast<const unsigned char*>(Y_dev) + r0 * N * eb,
+                                    (size_t)(rn * N * eb), cudaMemcpyDeviceToHost, mp->copy_out);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(mp->ev_done, mp->copy_out);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, mp->ev_done, 0);
+        return from_cuda(e);
+    }
     if (plan->K > 0) {
         if (!A_host || !B_host || !A_dev || !B_dev) return OLC_ERR_NULL;
         cudaError_t e = cudaMemcpyAsync(A_dev, A_host, numel(plan->a_shape, plan->a_rank) * eb,

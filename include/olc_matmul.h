@@ -171,11 +171,21 @@ olc_status olc_matmul_execute_checked(const olc_matmul_plan* plan,
 
 /*
  * The same product from host buffers: copies A and B from host memory into
- * the caller's device buffers, runs the plan, and copies Y back, all enqueued
- * on `stream` (use pinned host memory for asynchronous copies).  Nothing is
- * allocated.  A_host/B_host/Y_host: host pointers; A_dev/B_dev/Y_dev: device
- * buffers of the same sizes.  Returns after enqueueing; synchronise `stream`
- * before reading Y_host.  Errors: as olc_matmul_execute.
+ * the caller's device buffers, runs the plan, and copies Y back, ordered on
+ * `stream` (use pinned host memory for asynchronous copies).  A_host/B_host/
+ * Y_host: host pointers; A_dev/B_dev/Y_dev: device buffers of the same sizes.
+ * Returns after enqueueing; synchronise `stream` before reading Y_host.
+ * A single 2-D product (a batch folded into rows) of at least 4096 rows on
+ * the general kernels, without a residual, runs as a pipeline over four row
+ * chunks: B and the A chunks are copied in on one internal stream, chunk i
+ * is computed on `stream` once its rows have arrived, and its rows of Y are
+ * copied out on a second internal stream while later chunks compute; the
+ * call's work still starts after earlier work on `stream` and later work on
+ * `stream` starts after the last copy.  The two streams and the events are
+ * created (and owned by the plan) at the first such call; nothing else is
+ * allocated.  Other products: the three steps in order on `stream`.  A plan
+ * must not run two host-buffer executes at once on different streams.
+ * Errors: as olc_matmul_execute.
  */
 olc_status olc_matmul_execute_host(const olc_matmul_plan* plan,
                                    const void* A_host, const void* B_host, void* Y_host,
