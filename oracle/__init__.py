@@ -407,3 +407,29 @@ def matmul_fused(a, b, dtype, residual=None, act="none"):
     """MatMul followed by the fused residual and activation.  Returns (Y, S)."""
     acc, s = matmul_acc(a, b, dtype)
     return fused_epilogue(acc, s, dtype, residual, act)
+
+
+# --------------------------------------------------------------------------
+# grouped products
+#
+# "Gemm and MatMul Performance Roadmap": the batch-fusion row of the
+# opportunity table (hundreds of tiny or irregular products, where one
+# dispatch per product costs more than the product) and the GroupedGemm
+# interface of its plan (small products scheduled together).  Reading where
+# the page is silent: a group is a list of independent rank-2 products
+# Y_i = A_i @ B_i with their own M_i, N_i, K_i, one element type for the
+# group, each computed exactly as MatMul computes a rank-2 product.
+
+
+def grouped(a_list, b_list, dtype):
+    """Independent rank-2 products.  Returns ([Y_i], [S_i])."""
+    if len(a_list) != len(b_list):
+        raise ShapeError("a group needs as many A as B operands")
+    ys, ss = [], []
+    for a, b in zip(a_list, b_list):
+        if np.ndim(a) != 2 or np.ndim(b) != 2:
+            raise ShapeError("grouped products are rank-2")
+        y, s = matmul(np.asarray(a), np.asarray(b), dtype)
+        ys.append(y)
+        ss.append(s)
+    return ys, ss
