@@ -576,6 +576,47 @@ def measure_fused(device, peaks, l2):
     return out
 
 
+def measure_grouped(device, peaks):
+    """Hundreds of small irregular products (the pages' batch-fusion case):
+    256 members with M, N, K drawn from {16, 32, ..., 256} (seed 7), timed
+    as one grouped launch and as one plan execute per member (all captured
+    in CUDA graphs, so launch gaps are the GPU's own, not Python's)."""
+    import numpy as np
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import GroupedPlan, Plan, synth
+    rng = np.random.default_rng(7)
+    shapes = [tuple(int(x) * 16 for x in rng.integers(1, 17, size=3)) for _ in range(256)]
+    flop = sum(2.0 * m * n * k for m, n, k in shapes)
+    out = []
+    stream = torch.cuda.Stream()
+    for dtype in ("float16", "float32"):
+        tdt = synth.TORCH_DTYPES[dtype]
+        As = [torch.randn(m, k, device=device).to(tdt) for m, n, k in shapes]
+        Bs = [(torch.randn(k, n, device=device) * 0.1).to(tdt) for m, n, k in shapes]
+        Ys = [torch.empty(m, n, dtype=tdt, device=device) for m, n, k in shapes]
+        g = GroupedPlan(shapes, dtype)
+        ptrs = g.pointer_arrays(As, Bs, Ys)
+        plans = [Plan((m, k), (k, n), dtype) for m, n, k in shapes]
+        t_group = statistics.median(graph_time(lambda i: g.execute_ptrs(*ptrs, stream=stream),
+                                               1, stream, reps=20, launches=4))
+
+        def each(i):
+            for p, a, b, y in zip(plans, As, Bs, Ys):
+                p.execute(a, b, y, stream=stream)
+
+        t_each = statistics.median(graph_time(each, 1, stream, reps=10, launches=2))
+        out.append({"dtype": dtype, "members": len(shapes), "flop": flop,
+                    "ms_grouped": t_group, "ms_per_member_launches": t_each,
+                    "tflops_grouped": flop / (t_group * 1e-3) / 1e12,
+                    "tflops_per_member_launches": flop / (t_each * 1e-3) / 1e12,
+                    "speedup": t_each / t_group, "gpu_launches_grouped": 1,
+                    "gpu_launches_per_member": len(shapes)})
+        g.close()
+        for p in plans:
+            p.close()
+    return out
+
+
 def run_ours(args):
     import torch
     from gemm_matmulplan_broadcast_gb300 import load, synth
@@ -641,6 +682,7 @@ def run_ours(args):
         for wname in names:
             secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)
+        secondary["grouped_small_products"] = measure_grouped(device, peaks)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -7,6 +7,6 @@ The library is loaded on first use; if it has not been built, that use
 raises (build with ``python -m gemm_matmulplan_broadcast_gb300.build``).
 """
 
-from .binding import ALGORITHMS, GemmPlan, OlcError, Plan, gemm, load, matmul  # noqa: F401
+from .binding import ALGORITHMS, GemmPlan, GroupedPlan, OlcError, Plan, gemm, load, matmul  # noqa: F401
 
-__all__ = ["Plan", "GemmPlan", "matmul", "gemm", "load", "OlcError", "ALGORITHMS"]
+__all__ = ["Plan", "GemmPlan", "GroupedPlan", "matmul", "gemm", "load", "OlcError", "ALGORITHMS"]

@@ -83,6 +83,12 @@ def load():
             "olc_matmul_plan_has_constant_b": ([vp], ctypes.c_int),
             "olc_matmul_execute_constant": ([vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_plan_set_epilogue": ([vp, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+            "olc_grouped_plan_create": ([ctypes.c_int, i64p, i64p, i64p, ctypes.c_int,
+                                         ctypes.POINTER(vp)], ctypes.c_int),
+            "olc_grouped_plan_destroy": ([vp], None),
+            "olc_grouped_plan_tiles": ([vp], ctypes.c_int64),
+            "olc_grouped_plan_count": ([vp], ctypes.c_int),
+            "olc_grouped_execute": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute_fused": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_gemm_execute_constant": ([vp, vp, vp, vp, vp], ctypes.c_int),
             "olc_matmul_execute": ([vp, vp, vp, vp, vp], ctypes.c_int),
@@ -381,6 +387,82 @@ class GemmPlan(Plan):
                                                 _stream_handle(stream))
         _check(st, "olc_gemm_execute_constant")
         return Y
+
+
+class GroupedPlan:
+    """A group of independent rank-2 products Y_i = A_i @ B_i with their own
+    shapes, run in one launch.  `shapes`: list of (m, n, k)."""
+
+    def __init__(self, shapes, dtype: str):
+        from .synth import ONNX_CODES
+        self.lib = load()
+        self.shapes = [tuple(int(x) for x in sh) for sh in shapes]
+        self.dtype = dtype
+        cnt = len(self.shapes)
+        arr = ctypes.c_int64 * max(cnt, 1)
+        m = arr(*[sh[0] for sh in self.shapes])
+        n = arr(*[sh[1] for sh in self.shapes])
+        k = arr(*[sh[2] for sh in self.shapes])
+        h = ctypes.c_void_p()
+        _check(self.lib.olc_grouped_plan_create(cnt, m, n, k, ONNX_CODES[dtype], ctypes.byref(h)),
+               "olc_grouped_plan_create")
+        self._h = h
+        self._keep = None
+
+    @property
+    def tiles(self) -> int:
+        return int(self.lib.olc_grouped_plan_tiles(self._h))
+
+    def execute(self, As, Bs, Ys, stream=None):
+        """As, Bs, Ys: lists of CUDA tensors (member i: [m, k], [k, n], [m, n])."""
+        import torch
+        from .synth import TORCH_DTYPES
+        if not (len(As) == len(Bs) == len(Ys) == len(self.shapes)):
+            raise ValueError("need one A, B and Y per member")
+        want = TORCH_DTYPES[self.dtype]
+        for (m, n, k), a, b, y in zip(self.shapes, As, Bs, Ys):
+            for name, t, shp in (("A", a, (m, k)), ("B", b, (k, n)), ("Y", y, (m, n))):
+                if tuple(t.shape) != shp or t.dtype != want:
+                    raise ValueError("%s of a member is %s %s, want %s %s" % (name, tuple(t.shape), t.dtype, shp, want))
+                if t.numel() > 0 and (not t.is_contiguous() or t.device.type != "cuda"):
+                    raise ValueError("%s must be a contiguous CUDA tensor" % name)
+        ptrs = self.pointer_arrays(As, Bs, Ys)
+        self.execute_ptrs(*ptrs, stream=stream)
+        self._keep = ptrs        # the kernel reads the pointer arrays asynchronously
+        return Ys
+
+    @staticmethod
+    def pointer_arrays(As, Bs, Ys):
+        """Device int64 arrays of the members' A, B and Y addresses (built
+        once, reusable while the tensors live; synchronous upload)."""
+        import torch
+        dev = next((t.device for t in list(As) + list(Ys) if t.numel() > 0), torch.device("cuda"))
+        return tuple(torch.tensor([_ptr(t) or 0 for t in ts], dtype=torch.int64, device=dev)
+                     for ts in (As, Bs, Ys))
+
+    def execute_ptrs(self, a_ptrs, b_ptrs, y_ptrs, stream=None):
+        """Run the group from prebuilt device pointer arrays (no host work
+        beyond the launch; capturable in a CUDA graph)."""
+        st = self.lib.olc_grouped_execute(self._h, a_ptrs.data_ptr(), b_ptrs.data_ptr(),
+                                          y_ptrs.data_ptr(), _stream_handle(stream))
+        _check(st, "olc_grouped_execute")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self.lib.olc_grouped_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def gemm(A, B, C=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=False, out=None, stream=None):

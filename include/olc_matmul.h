@@ -296,6 +296,43 @@ olc_status olc_matmul_plan_set_epilogue(olc_matmul_plan* plan, int activation, i
 olc_status olc_matmul_execute_fused(const olc_matmul_plan* plan, const void* A, const void* B,
                                     const void* C, const void* R, void* Y, void* stream);
 
+/* ---- grouped products ---------------------------------------------------- */
+
+/*
+ * Many independent rank-2 products in one launch ("Gemm and MatMul
+ * Performance Roadmap": the batch-fusion row of its opportunity table, for
+ * hundreds of tiny or irregular products, and the GroupedGemm interface of
+ * its plan).  Member i computes Y_i[m_i, n_i] = A_i[m_i, k_i] @ B_i[k_i, n_i],
+ * all row-major and dense, accumulated as MatMul accumulates (float32 for
+ * FLOAT16 / BFLOAT16 / FLOAT, float64 for DOUBLE) and narrowed once.
+ */
+typedef struct olc_grouped_plan olc_grouped_plan;
+
+/* m, n, k: host arrays of `count` dimensions (copied; the caller keeps
+ * ownership).  Errors: OLC_ERR_NULL, OLC_ERR_INVALID (count <= 0),
+ * OLC_ERR_NEGATIVE_DIM, OLC_ERR_DTYPE, OLC_ERR_OOM. */
+olc_status olc_grouped_plan_create(int count, const int64_t* m, const int64_t* n, const int64_t* k,
+                                   olc_dtype dtype, olc_grouped_plan** out);
+
+/* NULL is accepted. */
+void olc_grouped_plan_destroy(olc_grouped_plan* plan);
+
+/* Output tiles (64 x 64) of all members, and the member count; -1 for NULL. */
+int64_t olc_grouped_plan_tiles(const olc_grouped_plan* plan);
+int olc_grouped_plan_count(const olc_grouped_plan* plan);
+
+/*
+ * Run the group: A, B, Y are DEVICE arrays of `count` device pointers (member
+ * i's operands and output).  One launch on `stream`; returns after enqueueing.
+ * The first call on a device copies the plan's descriptor table there
+ * (cudaMalloc, freed with the plan); later calls allocate nothing.  Members
+ * with an empty output are skipped (their pointers may be NULL); K == 0
+ * members get zeros.  Errors: OLC_ERR_NULL, OLC_ERR_WRONG_DEVICE, OLC_ERR_OOM,
+ * OLC_ERR_CUDA.
+ */
+olc_status olc_grouped_execute(const olc_grouped_plan* plan, const void* const* A, const void* const* B,
+                               void* const* Y, void* stream);
+
 /* ---- queries ----------------------------------------------------------- */
 
 /* Output shape: writes up to `capacity` extents into shape[] and the rank

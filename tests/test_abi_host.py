@@ -250,3 +250,22 @@ def test_constant_b_host_rejections():
         st = lib.olc_matmul_plan_set_constant_b(p._h, None, 32 * 23, None)
         assert binding.STATUS[st] in ("OLC_ERR_BUFFER_TOO_SMALL", "OLC_ERR_NULL")
         assert not p.has_constant_b
+
+
+def test_grouped_plan_host_checks():
+    """No kernel runs: creation errors and the tile count of a group."""
+    lib = binding.load()
+    arr = ctypes.c_int64 * 3
+    h = ctypes.c_void_p()
+    m, n, k = arr(64, 65, 0), arr(64, 1, 5), arr(64, 8, 3)
+    assert binding.STATUS[lib.olc_grouped_plan_create(0, m, n, k, 1, ctypes.byref(h))] == "OLC_ERR_INVALID"
+    assert binding.STATUS[lib.olc_grouped_plan_create(3, None, n, k, 1, ctypes.byref(h))] == "OLC_ERR_NULL"
+    assert binding.STATUS[lib.olc_grouped_plan_create(3, m, n, k, 7, ctypes.byref(h))] == "OLC_ERR_DTYPE"
+    bad = arr(64, -1, 3)
+    assert binding.STATUS[lib.olc_grouped_plan_create(3, m, bad, k, 1, ctypes.byref(h))] == "OLC_ERR_NEGATIVE_DIM"
+    assert lib.olc_grouped_plan_create(3, m, n, k, 1, ctypes.byref(h)) == 0
+    assert lib.olc_grouped_plan_tiles(h) == 1 + 2 + 0      # a 0-row member owns no tiles
+    assert lib.olc_grouped_plan_count(h) == 3
+    lib.olc_grouped_plan_destroy(h)
+    lib.olc_grouped_plan_destroy(None)
+    assert lib.olc_grouped_plan_tiles(None) == -1
