@@ -27,12 +27,25 @@ TORCH_DTYPES = {
     "float64": torch.float64,
     "float16": torch.float16,
     "bfloat16": torch.bfloat16,
+    "float8_e4m3fn": torch.float8_e4m3fn,
+    "float8_e5m2": torch.float8_e5m2,
 }
 
 # ONNX TensorProto element type codes, as used by the C ABI.
-ONNX_CODES = {"float32": 1, "float16": 10, "float64": 11, "bfloat16": 16}
+ONNX_CODES = {"float32": 1, "float16": 10, "float64": 11, "bfloat16": 16,
+              "float8_e4m3fn": 17, "float8_e5m2": 19}
 
-ELEMENT_BYTES = {"float32": 4, "float64": 8, "float16": 2, "bfloat16": 2}
+ELEMENT_BYTES = {"float32": 4, "float64": 8, "float16": 2, "bfloat16": 2,
+                 "float8_e4m3fn": 1, "float8_e5m2": 1}
+
+FP8_DTYPES = ("float8_e4m3fn", "float8_e5m2")
+
+
+def output_dtype(dtype: str) -> str:
+    """Element type of a product's output: FLOAT for the 8-bit float
+    operand types (float32 accumulation, no narrowing), the operand type
+    otherwise."""
+    return "float32" if dtype in FP8_DTYPES else dtype
 
 
 @dataclass(frozen=True)
@@ -95,10 +108,13 @@ def chain_operands(shapes: List[Tuple[int, int]], dtype: str, dist: Dist,
 
 def to_numpy_storage(t: torch.Tensor):
     """A CPU tensor as the numpy array the oracle takes: float32 / float64
-    values, or uint16 bit patterns for the 16-bit types."""
+    values, uint16 bit patterns for the 16-bit types, uint8 bit patterns for
+    the 8-bit float types."""
     t = t.detach().cpu().contiguous()
     if t.dtype in (torch.float16, torch.bfloat16):
         return t.view(torch.int16).numpy().view("uint16")
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 
@@ -107,6 +123,9 @@ def from_numpy_storage(arr, dtype: str) -> torch.Tensor:
     import numpy as np
     if dtype in ("float16", "bfloat16"):
         return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16).copy()).view(
+            TORCH_DTYPES[dtype])
+    if dtype in FP8_DTYPES:
+        return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.uint8).copy()).view(
             TORCH_DTYPES[dtype])
     return torch.from_numpy(np.ascontiguousarray(arr).copy())
 

@@ -53,6 +53,7 @@ _lock = threading.Lock()
 _lib = None
 
 DTYPES = ("float32", "float64", "float16", "bfloat16")
+FP8_DTYPES = ("float8_e4m3fn", "float8_e5m2")
 
 
 def build(force: bool = False) -> str:
@@ -120,6 +121,37 @@ def encode(values: np.ndarray, dtype: str) -> np.ndarray:
     fn = _load().oracle_encode_f16 if dtype == "float16" else _load().oracle_encode_bf16
     fn(_ptr(values), _ptr(out), values.size)
     return out
+
+
+# --------------------------------------------------------------------------
+# 8-bit float operands
+#
+# "Gemm and MatMul Performance Roadmap", the Float8 packing-format item:
+# each one-byte pattern of a Float8 format is decoded exactly to float32 and
+# the float32 algorithm runs with float32 accumulation.  The two formats
+# built here are E4M3FN (1 sign, 4 exponent bits with bias 7, 3 mantissa
+# bits; no infinities; S.1111.111 is NaN) and E5M2 (1 sign, 5 exponent bits
+# with bias 15, 2 mantissa bits; IEEE-style infinities and NaNs).  Reading
+# where the page is silent: the output is FLOAT (the float32 sums are not
+# narrowed), and both operands have the same format.
+
+
+def decode_fp8(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """uint8 patterns of an 8-bit float format -> exact float32 values,
+    written from the format's fields."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    if dtype == "float8_e4m3fn":
+        e, m = (b >> 3) & 0xF, b & 0x7
+        mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+        mag = np.where((b & 0x7F) == 0x7F, np.nan, mag)
+    elif dtype == "float8_e5m2":
+        e, m = (b >> 2) & 0x1F, b & 0x3
+        mag = np.where(e == 0, m * 2.0 ** -16, (1.0 + m / 4.0) * np.exp2(e - 15.0))
+        mag = np.where(e == 31, np.where(m == 0, np.inf, np.nan), mag)
+    else:
+        raise ValueError("not an 8-bit float type: %r" % dtype)
+    return (sign * mag).astype(np.float32)
 
 
 # --------------------------------------------------------------------------
@@ -205,7 +237,10 @@ def gemm2d(a: np.ndarray, b: np.ndarray, dtype: str, rows=None):
 def matmul(a: np.ndarray, b: np.ndarray, dtype: str):
     """ONNX MatMul of two dense row-major arrays.  Returns (Y, S), both of the
     output shape; Y in the storage type of ``dtype``, S = sum |a||b| per
-    output element (float64)."""
+    output element (float64).  8-bit float operands (uint8 patterns) give a
+    float32 Y."""
+    if dtype in FP8_DTYPES:
+        return matmul(decode_fp8(a, dtype), decode_fp8(b, dtype), "float32")
     if dtype not in DTYPES:
         raise ValueError("unsupported dtype %r" % dtype)
     out_shape = output_shape(a.shape, b.shape)
@@ -230,7 +265,8 @@ def matmul(a: np.ndarray, b: np.ndarray, dtype: str):
 
 
 def to_float64(y: np.ndarray, dtype: str) -> np.ndarray:
-    """Values of a result array as float64 (16-bit patterns decoded)."""
+    """Values of a result array as float64 (16-bit patterns decoded; the
+    float32 results of 8-bit float operands as they are)."""
     if dtype in ("float16", "bfloat16"):
         return decode(y, dtype).astype(np.float64)
     return y.astype(np.float64)
@@ -384,6 +420,8 @@ def fused_epilogue(v, scale, dtype, residual=None, act="none"):
 def matmul_acc(a: np.ndarray, b: np.ndarray, dtype: str):
     """MatMul's accumulators before narrowing (float32, or float64 for
     DOUBLE), with the same shape rules and batch loop as ``matmul``."""
+    if dtype in FP8_DTYPES:
+        return matmul_acc(decode_fp8(a, dtype), decode_fp8(b, dtype), "float32")
     out_shape = output_shape(a.shape, b.shape)
     a2 = a.reshape((1,) + a.shape) if a.ndim == 1 else a
     b2 = b.reshape(b.shape + (1,)) if b.ndim == 1 else b
@@ -404,9 +442,10 @@ def matmul_acc(a: np.ndarray, b: np.ndarray, dtype: str):
 
 
 def matmul_fused(a, b, dtype, residual=None, act="none"):
-    """MatMul followed by the fused residual and activation.  Returns (Y, S)."""
+    """MatMul followed by the fused residual and activation.  Returns (Y, S).
+    With 8-bit float operands the output (and the residual) is float32."""
     acc, s = matmul_acc(a, b, dtype)
-    return fused_epilogue(acc, s, dtype, residual, act)
+    return fused_epilogue(acc, s, "float32" if dtype in FP8_DTYPES else dtype, residual, act)
 
 
 # --------------------------------------------------------------------------
