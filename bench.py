@@ -39,6 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dense tensor-core ratio of FP16 to BF16 (equal) and the FP32/FP64 SIMT
 # peaks derived from unit counts and the maximum SM clock
 SM_COUNT_GB300 = 152
+FP8_OVER_BF16 = 2.0          # dense FP8 / BF16 tensor rate on GB300 (4.5 / 2.25 PFLOP/s nominal)
 FP32_LANES_PER_SM = 128
 FP64_FLOPS_PER_SM_PER_CLK = 4.0   # ~1.25 TFLOP/s at 2.07 GHz over 152 SMs, FMA = 2 flops
 
@@ -66,13 +67,14 @@ def _out_shape(a_shape, b_shape):
 
 
 def work_of(a_shape, b_shape, dtype):
-    from gemm_matmulplan_broadcast_gb300.synth import ELEMENT_BYTES
+    from gemm_matmulplan_broadcast_gb300.synth import ELEMENT_BYTES, output_dtype
     import numpy as np
     batch, m, k, n = _out_shape(a_shape, b_shape)
     items = int(np.prod(batch, dtype=np.int64)) if len(batch) else 1
     eb = ELEMENT_BYTES[dtype]
     flop = 2.0 * m * n * k * items
-    byts = eb * (int(np.prod(a_shape)) + int(np.prod(b_shape)) + items * m * n)
+    byts = (eb * (int(np.prod(a_shape)) + int(np.prod(b_shape))) +
+            ELEMENT_BYTES[output_dtype(dtype)] * items * m * n)
     return flop, float(byts)
 
 
@@ -217,14 +219,15 @@ def committed_traffic(kernel_key: str):
 def build_inputs(workload, device):
     """Per product: (A, B, Y) device tensors and the plan."""
     import torch
-    from gemm_matmulplan_broadcast_gb300 import Plan
+    from gemm_matmulplan_broadcast_gb300 import Plan, synth
     items = []
     for prod in workload.products:
         a, b = prod.draw()
         plan = Plan(prod.a_shape, prod.b_shape, prod.dtype)
         A = a.to(device)
         B = b.to(device)
-        Y = torch.empty(plan.output_shape, dtype=a.dtype, device=device)
+        Y = torch.empty(plan.output_shape, device=device,
+                        dtype=synth.TORCH_DTYPES[synth.output_dtype(prod.dtype)])
         flop, byts = work_of(prod.a_shape, prod.b_shape, prod.dtype)
         items.append({"name": prod.name, "plan": plan, "A": A, "B": B, "Y": Y, "a": a, "b": b,
                       "flop": flop, "bytes": byts, "dtype": prod.dtype})
@@ -373,9 +376,11 @@ def roofline_for(item, ms_per_launch, peaks, long_region: bool):
         achieved = item["bytes"] / (ms_per_launch / 1e3) / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak}
-    if dt in ("bfloat16", "float16"):
+    if dt in ("bfloat16", "float16", "float8_e4m3fn", "float8_e5m2"):
         key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
         peak = peaks.get(key, FALLBACK_PEAKS[key])   # fp16 dense rate equals bf16
+        if dt.startswith("float8"):
+            peak *= FP8_OVER_BF16                    # nominal dense ratio, 4.5 / 2.25 PFLOP/s
         achieved = item["flop"] / (ms_per_launch / 1e3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
@@ -679,6 +684,7 @@ def run_ours(args):
         names = ["fp16_skinny_splitk", "float32_square_chain"]
         if args.full_secondary:
             names.append("float64_square_chain")
+        names.append("fp8_transformer_projection")
         for wname in names:
             secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)

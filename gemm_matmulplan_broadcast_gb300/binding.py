@@ -19,7 +19,8 @@ ROOT = os.path.dirname(PKG)
 LIB_PATH = os.path.join(PKG, "libolc_matmul.so")
 HEADER = os.path.join(ROOT, "include", "olc_matmul.h")
 
-DTYPE_CODES = {"float32": 1, "float16": 10, "float64": 11, "bfloat16": 16}
+DTYPE_CODES = {"float32": 1, "float16": 10, "float64": 11, "bfloat16": 16,
+               "float8_e4m3fn": 17, "float8_e5m2": 19}
 ALGORITHMS = {
     "auto": -1, "empty": 0, "zero_fill": 1, "direct": 2, "skinny_m": 3, "skinny_n": 4,
     "split_k": 5, "general_tc": 6, "general_simt": 7,
@@ -259,12 +260,12 @@ class Plan:
     # -- execution -------------------------------------------------------
     def _check_tensors(self, A, B, Y):
         import torch
-        from .synth import TORCH_DTYPES
-        want = TORCH_DTYPES[self.dtype]
+        from .synth import TORCH_DTYPES, output_dtype
         for name, t, shape in (("A", A, self.a_shape), ("B", B, self.b_shape),
                                ("Y", Y, self.output_shape)):
             if t is None:
                 continue
+            want = TORCH_DTYPES[output_dtype(self.dtype) if name == "Y" else self.dtype]
             if t.dtype != want:
                 raise TypeError("%s has dtype %s, plan is %s" % (name, t.dtype, self.dtype))
             if tuple(t.shape) != tuple(shape):

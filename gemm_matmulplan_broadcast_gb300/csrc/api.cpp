@@ -75,21 +75,29 @@ namespace {
 
 constexpr int kDefaultSmCount = 152;   // GB300; used only when no device is visible
 
+// bytes of one operand element
 int64_t elem_bytes(olc_dtype dt) {
     switch (dt) {
         case OLC_FLOAT: return 4;
         case OLC_DOUBLE: return 8;
         case OLC_FLOAT16:
         case OLC_BFLOAT16: return 2;
+        case OLC_FLOAT8E4M3FN:
+        case OLC_FLOAT8E5M2: return 1;
     }
     return 0;
 }
 
 bool valid_dtype(int dt) {
-    return dt == OLC_FLOAT || dt == OLC_DOUBLE || dt == OLC_FLOAT16 || dt == OLC_BFLOAT16;
+    return dt == OLC_FLOAT || dt == OLC_DOUBLE || dt == OLC_FLOAT16 || dt == OLC_BFLOAT16 ||
+           dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2;
 }
 
 bool is_half(olc_dtype dt) { return dt == OLC_FLOAT16 || dt == OLC_BFLOAT16; }
+bool is_fp8(olc_dtype dt) { return dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2; }
+
+// bytes of one output element: FLOAT for the 8-bit float operand types
+int64_t out_bytes(olc_dtype dt) { return is_fp8(dt) ? 4 : elem_bytes(dt); }
 
 int64_t out_numel(const olc_matmul_plan* p) {
     int64_t n = 1;
@@ -184,6 +192,19 @@ void collapse_and_fold(olc_matmul_plan* p) {
 bool feasible(const olc_matmul_plan* p, int algo) {
     const int64_t rows = p->rows, N = p->N, K = p->K;
     const int64_t n = out_numel(p);
+    if (is_fp8(p->dtype)) {
+        switch (algo) {
+            case OLC_ALGO_EMPTY: return n == 0;
+            case OLC_ALGO_ZERO_FILL: return n > 0 && K == 0;
+            case OLC_ALGO_DIRECT:
+            case OLC_ALGO_GENERAL_SIMT: return n > 0 && K > 0;
+            case OLC_ALGO_GENERAL_TC: {
+                Problem pr = make_problem(p, nullptr, nullptr, nullptr);
+                return n > 0 && K > 0 && fp8_tc_ok(pr);
+            }
+        }
+        return false;
+    }
     const bool trans = p->trans_a || p->trans_b;
     if (trans && (algo == OLC_ALGO_SKINNY_M || algo == OLC_ALGO_SKINNY_N || algo == OLC_ALGO_SPLIT_K))
         return false;   // transposed operands: general and direct kernels only
@@ -211,6 +232,11 @@ bool feasible(const olc_matmul_plan* p, int algo) {
 int choose_algorithm(const olc_matmul_plan* p) {
     if (out_numel(p) == 0) return OLC_ALGO_EMPTY;
     if (p->K == 0) return OLC_ALGO_ZERO_FILL;
+    if (is_fp8(p->dtype)) {
+        const double macs = (double)p->rows * (double)p->N * (double)p->K * (double)p->items;
+        if (macs >= 4.0 * 1024 * 1024 && feasible(p, OLC_ALGO_GENERAL_TC)) return OLC_ALGO_GENERAL_TC;
+        return macs < 4.0 * 1024 * 1024 ? OLC_ALGO_DIRECT : OLC_ALGO_GENERAL_SIMT;
+    }
     const int64_t rows = p->rows, N = p->N, K = p->K, items = p->items;
     const double macs = (double)rows * (double)N * (double)K * (double)items;
     if (rows <= skinny_m_max_rows() && N >= 256 && feasible(p, OLC_ALGO_SKINNY_M))
@@ -254,6 +280,8 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
     } else if (p->algo == OLC_ALGO_SKINNY_N) {
         p->partial_bytes = skinny_n_partial_bytes(dt, pr, p->sm_count);
         p->counter_count = skinny_n_counter_count(dt, pr, p->sm_count);
+    } else if (p->algo == OLC_ALGO_GENERAL_TC && is_fp8(dt)) {
+        p->partial_bytes = fp8_tc_workspace_bytes(pr);    // B transposed, [N, K] bytes
     } else if (p->algo == OLC_ALGO_SKINNY_M) {
         p->splits = skinny_m_pick_split(dt, pr, p->sm_count);
         if (p->splits > 1) {
@@ -310,7 +338,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     if (p->algo == OLC_ALGO_ZERO_FILL) {
         Problem zp = make_problem(p, A, B, Y, C, R);
         if (zp.epi.mode) return from_cuda(launch_epilogue_fill(p->dtype, zp, s));
-        return from_cuda(launch_zero_fill(Y, n * elem_bytes(p->dtype), s));
+        return from_cuda(launch_zero_fill(Y, n * out_bytes(p->dtype), s));
     }
     if (!A || !B) return OLC_ERR_NULL;
     int cur = -1;
@@ -332,6 +360,11 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     int algo = p->algo;
     if (!al && algo != OLC_ALGO_DIRECT && algo != OLC_ALGO_GENERAL_SIMT) algo = OLC_ALGO_DIRECT;
     cudaError_t e = cudaSuccess;
+    if (is_fp8(dt)) {
+        e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s)
+                                        : launch_fp8_simt(dt, pr, s);
+        return from_cuda(e);
+    }
     switch (algo) {
         case OLC_ALGO_DIRECT: e = launch_direct(dt, pr, s); break;
         case OLC_ALGO_GENERAL_SIMT: e = launch_general_simt(dt, pr, s); break;
@@ -456,7 +489,7 @@ olc_status olc_gemm_plan_create(const int64_t* a_shape, const int64_t* b_shape, 
     *out = nullptr;
     if (!a_shape || !b_shape || (c_rank > 0 && !c_shape)) return OLC_ERR_NULL;
     if (c_rank < -1 || c_rank > 2) return OLC_ERR_RANK;
-    if (!valid_dtype(dtype)) return OLC_ERR_DTYPE;
+    if (!valid_dtype(dtype) || is_fp8(dtype)) return OLC_ERR_DTYPE;   // Gemm: no 8-bit floats
     for (int i = 0; i < 2; ++i)
         if (a_shape[i] < 0 || b_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
     for (int i = 0; i < c_rank; ++i)
@@ -672,7 +705,7 @@ namespace {
 // any, folded into rows), a workspace-free algorithm, no residual, and enough
 // rows for several tensor-core row tiles per chunk.  0 = not pipelined.
 int host_chunks(const olc_matmul_plan* p) {
-    if (p->items != 1 || p->K == 0 || p->residual) return 0;
+    if (p->items != 1 || p->K == 0 || p->residual || is_fp8(p->dtype)) return 0;
     if (p->algo != OLC_ALGO_GENERAL_TC && p->algo != OLC_ALGO_GENERAL_SIMT) return 0;
     if (p->is_gemm && (p->trans_a || (p->c_rank >= 0 && p->c_rs != 0))) return 0;
     const int64_t rows = p->rows;
@@ -773,7 +806,7 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_ho
     }
     olc_status st = run(plan, A_dev, B_dev, Y_dev, s);
     if (st != OLC_OK) return st;
-    return from_cuda(cudaMemcpyAsync(Y_host, Y_dev, n * eb, cudaMemcpyDeviceToHost, s));
+    return from_cuda(cudaMemcpyAsync(Y_host, Y_dev, n * out_bytes(plan->dtype), cudaMemcpyDeviceToHost, s));
 }
 
 olc_status olc_matmul_plan_output_shape(const olc_matmul_plan* plan, int64_t* shape, int capacity,

@@ -110,6 +110,25 @@ __device__ __forceinline__ typename Num<T>::acc_t apply_epilogue(const Epilogue&
     }
 }
 
+// 8-bit float operands, decoded from the format fields (exact in float32).
+// E4M3FN: sign, 4 exponent bits (bias 7), 3 mantissa bits; S.1111.111 is
+// NaN, no infinities.  E5M2: sign, 5 exponent bits (bias 15), 2 mantissa
+// bits; exponent 31 holds infinities and NaNs.
+__device__ __forceinline__ float fp8_e4m3_to_f32(uint32_t b) {
+    const uint32_t sign = (b & 0x80u) << 24;
+    const uint32_t e = (b >> 3) & 0xFu, m = b & 0x7u;
+    if ((b & 0x7Fu) == 0x7Fu) return __uint_as_float(sign | 0x7FC00000u);
+    const float mag = e == 0 ? (float)m * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return __uint_as_float(__float_as_uint(mag) | sign);
+}
+__device__ __forceinline__ float fp8_e5m2_to_f32(uint32_t b) {
+    const uint32_t sign = (b & 0x80u) << 24;
+    const uint32_t e = (b >> 2) & 0x1Fu, m = b & 0x3u;
+    if (e == 31u) return __uint_as_float(sign | (m == 0 ? 0x7F800000u : 0x7FC00000u));
+    const float mag = e == 0 ? (float)m * 0x1p-16f : __uint_as_float(((e + 112u) << 23) | (m << 21));
+    return __uint_as_float(__float_as_uint(mag) | sign);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

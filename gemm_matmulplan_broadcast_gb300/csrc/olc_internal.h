@@ -112,6 +112,15 @@ cudaError_t launch_split_k_simt(olc_dtype dt, const Problem& p, int splits, cons
                                 cudaStream_t stream);
 int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count);
 
+// 8-bit float operands (FLOAT output): SIMT decode kernel for any shape and
+// batch; tcgen05 kind::f8f6f4 kernel for one item with K % 16 == 0 and
+// N % 4 == 0 (B transposed into the workspace first)
+cudaError_t launch_fp8_simt(olc_dtype dt, const Problem& p, cudaStream_t stream);
+bool fp8_tc_ok(const Problem& p);
+size_t fp8_tc_workspace_bytes(const Problem& p);
+cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
+                          cudaStream_t stream);
+
 // GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
 // variant: 0 automatic, 1 one CTA per 128 x 256 tile, 2 CTA pairs (cta_group::2)

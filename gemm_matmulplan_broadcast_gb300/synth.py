@@ -210,6 +210,20 @@ def _bf16_projection() -> Workload:
         ))
 
 
+def _fp8_projection() -> Workload:
+    a, w = normal(1.0), normal(0.5)
+    return Workload(
+        "fp8_transformer_projection",
+        "E4M3FN activations A ~ N(0,1) x weights B ~ N(0,0.5) (cast RNE), seed 2: "
+        "[8,2048,4096]x[4096,4096], [8,2048,4096]x[4096,14336], "
+        "[8,2048,14336]x[14336,4096]; float32 accumulation, FLOAT output",
+        products=(
+            Product("fp8_proj_4096x4096", (8, 2048, 4096), (4096, 4096), "float8_e4m3fn", a, w, 2),
+            Product("fp8_proj_4096x14336", (8, 2048, 4096), (4096, 14336), "float8_e4m3fn", a, w, 2),
+            Product("fp8_proj_14336x4096", (8, 2048, 14336), (14336, 4096), "float8_e4m3fn", a, w, 2),
+        ))
+
+
 def _fp16_corners() -> Workload:
     a, w = normal(1.0), normal(0.02)
     return Workload(
@@ -240,7 +254,7 @@ def _square_sweep(dtype: str) -> Workload:
 def workloads():
     """All named workloads, smallest first."""
     return [_fp32_small(), _fp32_broadcast(), _bf16_projection(), _fp16_corners(),
-            _square_sweep("float32"), _square_sweep("float64")]
+            _square_sweep("float32"), _square_sweep("float64"), _fp8_projection()]
 
 
 def workload(name: str) -> Workload:

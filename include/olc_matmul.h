@@ -38,12 +38,18 @@ extern "C" {
  * accumulate natively; FLOAT16 and BFLOAT16 accumulate in float32 and narrow
  * the result once with round-to-nearest-even ("Types and algorithm
  * selection"; "Gemm and MatMul Performance Roadmap", section "Scope and type
- * matrix"). */
+ * matrix").  The 8-bit float operand types ("Gemm and MatMul Performance
+ * Roadmap", the Float8 packing-format item) decode exactly to float32,
+ * accumulate in float32, and give a FLOAT output (4 bytes per element): A
+ * and B have the 8-bit type, Y (and a fused residual) is float32.  They are
+ * MatMul types only (Gemm plans reject them). */
 typedef enum {
     OLC_FLOAT = 1,
     OLC_FLOAT16 = 10,
     OLC_DOUBLE = 11,
-    OLC_BFLOAT16 = 16
+    OLC_BFLOAT16 = 16,
+    OLC_FLOAT8E4M3FN = 17,   /* 1-4-3, bias 7, no infinities, S.1111.111 NaN */
+    OLC_FLOAT8E5M2 = 19      /* 1-5-2, bias 15, IEEE-style infinities / NaNs */
 } olc_dtype;
 
 typedef enum {
@@ -414,6 +420,11 @@ int olc_version(void);
  * exported so a host test can check the bit layout.  Pure functions. */
 uint64_t olc_debug_tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout);
 uint32_t olc_debug_tc_instr_desc(int is_bf16, int m, int n, int a_mn_major, int b_mn_major);
+
+/* Testing hook: the tcgen05 kind::f8f6f4 instruction descriptor the FP8
+ * kernel uses (fmt 0 = E4M3, 1 = E5M2; both operands K-major; float32
+ * accumulator).  Host only, no device needed. */
+uint32_t olc_debug_f8_instr_desc(int fmt, int m, int n);
 
 /* Self-test of the bounded device-side wait the tensor-core kernel uses on
  * every mbarrier: one thread waits for an mbarrier phase that completes only

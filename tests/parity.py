@@ -14,7 +14,9 @@ import oracle
 from gemm_matmulplan_broadcast_gb300 import Plan
 from gemm_matmulplan_broadcast_gb300 import synth
 
-TOL = {"float32": 1e-5, "float64": 1e-12, "float16": 2e-3, "bfloat16": 1e-2}
+TOL = {"float32": 1e-5, "float64": 1e-12, "float16": 2e-3, "bfloat16": 1e-2,
+       # 8-bit float operands: exact products, float32 sums, float32 output
+       "float8_e4m3fn": 1e-5, "float8_e5m2": 1e-5}
 
 
 def gpu_matmul(a_cpu: torch.Tensor, b_cpu: torch.Tensor, dtype: str, algorithm=None,
@@ -29,7 +31,7 @@ def gpu_matmul(a_cpu: torch.Tensor, b_cpu: torch.Tensor, dtype: str, algorithm=N
             p.force(algorithm)
         shape = p.output_shape
         n = int(np.prod(shape, dtype=np.int64))
-        buf = torch.full((n + guard,), float("nan"), dtype=synth.TORCH_DTYPES[dtype], device="cuda")
+        buf = torch.full((n + guard,), float("nan"), dtype=synth.TORCH_DTYPES[synth.output_dtype(dtype)], device="cuda")
         Y = buf[:n].view(shape)
         if checked:
             p.execute_checked(A, B, Y)

@@ -1,0 +1,86 @@
+"""8-bit float operands (E4M3FN, E5M2) on the GPU against the oracle:
+the tcgen05 kind::f8f6f4 kernel (B transposed into the workspace) and the
+SIMT decode kernel, float32 output; ragged tiles, batches, integer inputs
+bit for bit, the fused epilogue, K == 0 and the rejections."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_matmulplan_broadcast_gb300 import GemmPlan, OlcError, Plan, synth
+from parity import check_product, compare
+
+pytestmark = pytest.mark.gpu
+
+FP8 = ["float8_e4m3fn", "float8_e5m2"]
+
+TC_SHAPES = [
+    ((128, 128), (128, 256)),          # one tile, one K block
+    ((300, 1040), (1040, 264)),        # M, N, K tails (K a multiple of 16, N of 4)
+    ((2, 512, 2048), (2048, 1024)),    # folded batch, several tiles and K blocks
+    ((64, 4096), (4096, 4096)),
+]
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes", TC_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_tensor_core(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 41)
+    y, algo = check_product(a, b, dtype, algorithm="general_tc")
+    assert algo == "general_tc" and y.dtype == torch.float32
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 42)
+    check_product(ai, bi, dtype, algorithm="general_tc", exact=True)
+
+
+SIMT_SHAPES = [
+    ((1, 8), (8, 16)),
+    ((37, 55), (55, 29)),              # no 16-byte rows at all
+    ((3, 2, 40, 24), (2, 24, 48)),     # broadcast batch with batched B
+    ((64,), (64, 48)),                 # rank-one A
+    ((300, 1040), (1040, 264)),
+]
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes", SIMT_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_simt(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.UNIFORM, synth.UNIFORM, 43)
+    check_product(a, b, dtype, algorithm="general_simt")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 44)
+    check_product(ai, bi, dtype, algorithm="direct", exact=True)
+
+
+@pytest.mark.parametrize("dtype", FP8)
+def test_fp8_fused_relu_residual_and_k_zero(dtype):
+    a, b = synth.operands((256, 512), (512, 256), dtype, synth.normal(1.0), synth.normal(0.5), 45)
+    r = torch.randn(256, 256)
+    with Plan(a.shape, b.shape, dtype) as p:
+        assert p.algorithm == "general_tc"
+        p.set_epilogue("relu", True)
+        Y = torch.empty(256, 256, device="cuda")
+        p.execute_fused(a.cuda(), b.cuda(), Y, R=r.cuda())
+        torch.cuda.synchronize()
+    ref, s = oracle.matmul_fused(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype,
+                                 r.numpy(), "relu")
+    compare(Y.cpu(), ref, s, dtype)
+    with Plan((5, 0), (0, 7), dtype) as p:
+        assert p.algorithm == "zero_fill"
+        Y = torch.full((5, 7), float("nan"), device="cuda")
+        p.execute(torch.empty(5, 0, dtype=a.dtype, device="cuda"),
+                  torch.empty(0, 7, dtype=a.dtype, device="cuda"), Y)
+        torch.cuda.synchronize()
+        assert torch.equal(Y.cpu(), torch.zeros(5, 7))
+
+
+def test_fp8_rejections():
+    with pytest.raises(OlcError) as ei:
+        GemmPlan((4, 8), (8, 4), "float8_e4m3fn")
+    assert ei.value.name == "OLC_ERR_DTYPE"
+    with Plan((64, 40), (40, 30), "float8_e5m2") as p:    # N not a multiple of 4
+        with pytest.raises(OlcError):
+            p.force("general_tc")
+        with pytest.raises(OlcError):
+            p.force("split_k")
