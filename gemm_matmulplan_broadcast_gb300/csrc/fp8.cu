@@ -445,6 +445,9 @@ cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Wo
                                                                p.K, p.N, ttn);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // CTA pairs (256 x 256 tiles, half of B per CTA) once the product holds
+    // a pair tile; 128 x 256 tiles of one CTA otherwise (or when asked)
+    if (p.M >= 256 && p.N >= 256 && p.variant != 1) return launch_pair_f8(dt, p, bt, sm_count, s);
     CUtensorMap ma, mb;
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);

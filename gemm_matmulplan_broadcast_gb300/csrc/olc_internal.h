@@ -120,6 +120,10 @@ bool fp8_tc_ok(const Problem& p);
 size_t fp8_tc_workspace_bytes(const Problem& p);
 cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
                           cudaStream_t stream);
+// the CTA-pair tensor-core kernel on 8-bit float operands: A [M, K] and the
+// transposed B [N, K] (bytes), float32 Y; one item, M and N >= 256
+cudaError_t launch_pair_f8(olc_dtype dt, const Problem& p, const void* bt, int sm_count,
+                           cudaStream_t stream);
 
 // GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);

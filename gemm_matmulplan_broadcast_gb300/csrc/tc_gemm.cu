@@ -114,6 +114,7 @@ struct Params {
     int stream;               // 1: stream-K shares (split instantiation only)
     int a_mn;                 // A stored [K, M] (Gemm transA): MN-major A operand
     int b_k;                  // B stored [N, K] (Gemm transB): K-major B operand
+    int f8_fmt;               // 8-bit float operands (pair kernel): 0 = E4M3, 1 = E5M2
     Epilogue epi;
     int64_t iterations;       // stream-K: total (tile, K block) iterations
     float* part1;             // [tiles][splits][BM][BN] float32 partial tiles
@@ -950,6 +951,24 @@ __device__ __forceinline__ void mma2_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+__device__ __forceinline__ void mma2_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// kind::f8f6f4 instruction descriptor: float32 accumulator (bits 4-5 = 1), A
+// and B formats in bits 7-9 / 10-12 (0 = E4M3, 1 = E5M2), both K-major, N >> 3
+// in bits 17-22, M >> 4 in bits 24-28
+__host__ __device__ constexpr uint32_t f8_desc(int fmt, int m, int n) {
+    return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
 // arrive on the barrier at this offset in both CTAs of the pair once the
 // MMAs issued so far have completed
 __device__ __forceinline__ void commit2_both(uint64_t* bar) {
@@ -967,6 +986,11 @@ __device__ __forceinline__ void commit2_local(uint64_t* bar) {
         : "memory");
 }
 
+// F8: 8-bit float operands, both K-major (B given as [N, K]), 128 elements
+// per 128-byte swizzle row and 32 per MMA (kind::f8f6f4), float32 output;
+// the byte geometry of the shared-memory stages is the same as for 16-bit
+// operands with K-major B.
+template <bool F8>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -1043,7 +1067,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         armed[stage] = true;
                         armed_parity[stage] = phase;
                     }
-                    const int k0 = (int)(kb * BK);
+                    const int k0 = (int)(kb * (F8 ? 128 : BK));
                     if (!p.a_mn) {
                         tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
                     } else {
@@ -1066,7 +1090,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc = instr_desc(p.is_bf16, 256, 256, p.a_mn, p.b_k ? 0 : 1);
+            const uint32_t idesc = F8 ? f8_desc(p.f8_fmt, 256, 256)
+                                      : instr_desc(p.is_bf16, 256, 256, p.a_mn, p.b_k ? 0 : 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t t = cluster_id(); t < total && ok; t += cluster_count()) {
@@ -1084,7 +1109,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                    : smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
                         const uint64_t bd = p.b_k ? smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u)
                                                   : smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
-                        mma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (F8) mma2_f8(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        else mma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     commit2_both(&s->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -1104,7 +1130,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int64_t t = cluster_id(); t < total; t += cluster_count()) {
             int64_t item, mb, nb;
             coords(t, item, mb, nb);
-            if (mb * 256 + rank * 128 + row_in_tile < p.M)
+            if (!F8 && mb * 256 + rank * 128 + row_in_tile < p.M)
                 prefetch_residual(p, item, mb * 256 + rank * 128 + row_in_tile, nb * 256,
                                   min64(256, p.N - nb * 256));
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
@@ -1112,6 +1138,39 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const int64_t row = mb * 256 + rank * 128 + row_in_tile;
             const bool row_ok = row < p.M;
             const uint32_t t_base = tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * 256;
+            if constexpr (F8) {
+                // float32 output rows; N is a multiple of 4: whole 16-byte groups
+                float* yrow = static_cast<float*>(p.Y) + (item * p.M + (row_ok ? row : 0)) * p.N;
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_base + c, r);
+                    const int64_t col = nb * 256 + c;
+                    if (row_ok && col < p.N) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                        if (p.epi.mode != 0) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col + i < p.N)
+                                    v[i] = apply_epilogue<float>(p.epi, v[i], row, col + i, yrow + col + i);
+                        }
+                        const int64_t left = (p.N - col) / 4;
+                        const int groups = (int)(left < 8 ? left : 8);
+                        float4* dst = reinterpret_cast<float4*>(yrow + col);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (q < groups)
+                                dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) remote_arrive(acc_empty_leader[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                continue;
+            }
             unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
                                   ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
 #pragma unroll 1
@@ -1652,7 +1711,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(pair::tc_pair_kernel,
+        attr_err = cudaFuncSetAttribute(pair::tc_pair_kernel<false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -1670,7 +1729,77 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel, ma, mb, p);
+    return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel<false>, ma, mb, p);
+}
+
+// rank-3 map over [1][rows][cols] bytes (cols innermost), box {box_cols,
+// box_rows, 1}, 128-byte swizzle
+static bool encode_u8(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                      uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, rows, 1};
+    cuuint64_t strides[2] = {cols, cols * rows};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 8-bit float operands on CTA pairs: A [M, K] and the transposed B [N, K]
+// (both bytes, K-major), float32 Y; one item
+static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const void* bt, int sm_count,
+                                       cudaStream_t s) {
+    if (pr.items != 1 || pr.K % 16 != 0 || pr.N % 4 != 0 || pr.M >= (1LL << 31) ||
+        pr.N >= (1LL << 31) || pr.K >= (1LL << 31))
+        return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof ma);
+    std::memset(&mb, 0, sizeof mb);
+    if (!encode_u8(&ma, pr.A, (uint64_t)pr.K, (uint64_t)pr.M, 128, 128) ||
+        !encode_u8(&mb, bt, (uint64_t)pr.K, (uint64_t)pr.N, 128, 128))
+        return cudaErrorInvalidValue;
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.M = pr.M;
+    p.N = pr.N;
+    p.K = pr.K;
+    p.items = 1;
+    p.k_blocks = ceil_div(pr.K, 128);
+    p.a_item_elems = pr.M * pr.K;
+    p.b_item_elems = pr.K * pr.N;
+    p.map = pr.map;
+    p.Y = pr.Y;
+    p.err = device_error_word();
+    p.f8_fmt = dt == OLC_FLOAT8E4M3FN ? 0 : 1;
+    p.a_mn = 0;
+    p.b_k = 1;
+    p.epi = pr.epi;
+    const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256);
+    if (pairs <= 0) return cudaSuccess;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(pair::tc_pair_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel<true>, ma, mb, p);
 }
 
 // Split-K plan and launch for tiny outputs: one slice per CTA, about one
@@ -1752,6 +1881,11 @@ bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K) {
     if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;
     // TMA needs 16-byte row strides; coordinates fit in int32
     return N % 8 == 0 && K % 8 == 0 && N < (1LL << 31) && K < (1LL << 31);
+}
+
+cudaError_t launch_pair_f8(olc_dtype dt, const Problem& pr, const void* bt, int sm_count,
+                           cudaStream_t s) {
+    return tc::launch_pair_f8_impl(dt, pr, bt, sm_count, s);
 }
 
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,

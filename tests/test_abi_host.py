@@ -269,3 +269,21 @@ def test_grouped_plan_host_checks():
     lib.olc_grouped_plan_destroy(h)
     lib.olc_grouped_plan_destroy(None)
     assert lib.olc_grouped_plan_tiles(None) == -1
+
+
+def test_f8_instruction_descriptor_layout():
+    """kind::f8f6f4 instruction descriptor fields, as the FP8 kernel builds
+    them: float32 accumulator (bits 4-5 = 1), A / B format (bits 7-9 /
+    10-12: 0 = E4M3, 1 = E5M2), K-major operands (bits 15, 16 clear),
+    N / 8 in bits 17-22, M / 16 in bits 24-28."""
+    lib = binding.load()
+    lib.olc_debug_f8_instr_desc.restype = ctypes.c_uint32
+    for fmt in (0, 1):
+        for m, n in ((128, 256), (128, 16), (64, 8)):
+            d = lib.olc_debug_f8_instr_desc(fmt, m, n)
+            assert (d >> 4) & 3 == 1
+            assert (d >> 7) & 7 == fmt and (d >> 10) & 7 == fmt
+            assert (d >> 15) & 3 == 0
+            assert (d >> 17) & 0x3F == n // 8
+            assert (d >> 24) & 0x1F == m // 16
+            assert d & 0b1111 == 0 and (d >> 13) & 3 == 0 and (d >> 23) & 1 == 0 and d >> 29 == 0

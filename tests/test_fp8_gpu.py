@@ -17,21 +17,40 @@ FP8 = ["float8_e4m3fn", "float8_e5m2"]
 
 TC_SHAPES = [
     ((128, 128), (128, 256)),          # one tile, one K block
+    ((256, 128), (128, 256)),          # one pair tile
+    ((260, 2064), (2064, 516)),        # pair tiles with the peer CTA's rows and columns ragged
     ((300, 1040), (1040, 264)),        # M, N, K tails (K a multiple of 16, N of 4)
     ((2, 512, 2048), (2048, 1024)),    # folded batch, several tiles and K blocks
     ((64, 4096), (4096, 4096)),
 ]
 
 
+def _tc(a, b, dtype, variant, exact):
+    A, B = a.cuda(), b.cuda()
+    with Plan(a.shape, b.shape, dtype) as p:
+        p.force("general_tc")
+        p.set_tc_variant(variant)
+        n = int(np.prod(p.output_shape))
+        buf = torch.full((n + 64,), float("nan"), device="cuda")
+        Y = buf[:n].view(p.output_shape)
+        p.execute_checked(A, B, Y)
+        torch.cuda.synchronize()
+        assert torch.isnan(buf[n:]).all()
+    ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+    compare(Y.cpu(), ref, s, dtype, exact=exact)
+
+
 @pytest.mark.parametrize("dtype", FP8)
 @pytest.mark.parametrize("shapes", TC_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
-def test_fp8_tensor_core(dtype, shapes):
+@pytest.mark.parametrize("variant", [0, 1], ids=["auto_pairs", "one_cta"])
+def test_fp8_tensor_core(dtype, shapes, variant):
+    """Automatic choice (CTA pairs with 256 x 256 tiles once M and N reach
+    256) and variant 1 (one CTA per 128 x 256 tile)."""
     a_shape, b_shape = shapes
     a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 41)
-    y, algo = check_product(a, b, dtype, algorithm="general_tc")
-    assert algo == "general_tc" and y.dtype == torch.float32
+    _tc(a, b, dtype, variant, exact=False)
     ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 42)
-    check_product(ai, bi, dtype, algorithm="general_tc", exact=True)
+    _tc(ai, bi, dtype, variant, exact=True)
 
 
 SIMT_SHAPES = [
