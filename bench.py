@@ -337,7 +337,10 @@ def cpu_oracle_sample(workload, target_seconds: float, items=None):
         # timing sample: A's rows (all batch items stacked) against one B matrix
         an = an.reshape((1, k) if an.ndim == 1 else (-1, k))
         bn = bn.reshape((k, 1)) if bn.ndim == 1 else bn.reshape((-1, k, n))[0]
-        prods.append((prod, an, np.ascontiguousarray(bn), n, k))
+        dt = prod.dtype
+        if dt in synth.FP8_DTYPES:       # the oracle decodes 8-bit floats, then runs in float32
+            an, bn, dt = oracle.decode_fp8(an, dt), oracle.decode_fp8(bn, dt), "float32"
+        prods.append((dt, an, np.ascontiguousarray(bn), n, k))
     # size the sample: grow the row count until one pass takes a quarter of
     # the target, then scale to the target
     rng = np.random.default_rng(0)
@@ -345,10 +348,10 @@ def cpu_oracle_sample(workload, target_seconds: float, items=None):
     def one_pass(rows):
         fl = 0.0
         t0 = time.perf_counter()
-        for prod, an, bn, n, k in prods:
+        for dt, an, bn, n, k in prods:
             r = min(rows, an.shape[0])
             sel = np.sort(rng.choice(an.shape[0], size=r, replace=False))
-            oracle.gemm2d(an, bn, prod.dtype, rows=sel)
+            oracle.gemm2d(an, bn, dt, rows=sel)
             fl += 2.0 * r * n * k
         return fl, time.perf_counter() - t0
 
@@ -698,7 +701,8 @@ def run_ours(args):
 
     launches = sum(it["plan"].launches for it in items) * args.steps
     dtypes = sorted({it["dtype"] for it in items})
-    short = {"bfloat16": "bf16", "float16": "f16", "float32": "f32", "float64": "f64"}
+    short = {"bfloat16": "bf16", "float16": "f16", "float32": "f32", "float64": "f64",
+             "float8_e4m3fn": "e4m3", "float8_e5m2": "e5m2"}
     line = {
         "metric": METRIC,
         "value": value,

@@ -873,7 +873,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // m0 + 128 r .. +127 and B columns n0 + 128 r .. +127 in its own shared
 // memory, the leader (rank 0) issues the MMAs that read both CTAs' halves,
 // and each CTA's TMEM receives its own 128 rows x 256 columns.  Per SM that
-// is 32 KB of operands per 64-deep K block instead of 48 KB, so 6 stages fit
+// is 32 KB of operands per 64-deep K block instead of 48 KB, so 7 stages fit
 // where the 1-CTA kernel has 4.
 //
 // Synchronisation: both CTAs' TMA loads complete on the leader's full[s]
@@ -885,7 +885,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 namespace pair {
 
-constexpr int STAGES = 6;
+constexpr int STAGES = 7;                           // 7 x 32 KiB: the most that fits
 constexpr int A_BYTES = 128 * BK * 2;               // this CTA's 128 rows of A
 constexpr int B_BYTES = 128 * BK * 2;               // this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 32 KiB
