@@ -565,9 +565,13 @@ def measure_fused(device, peaks, l2):
             else:
                 Y.copy_(F.gelu(Y))
 
-        t = {}
-        for label, fn in (("plain", run_plain), ("fused", run_fused), ("unfused", run_unfused)):
-            t[label] = statistics.median(graph_time(fn, nsets, stream))
+        # the three variants interleaved over rounds, so that clock and power
+        # drift under the power cap does not favour whichever runs first
+        samples = {"plain": [], "fused": [], "unfused": []}
+        for _ in range(3):
+            for label, fn in (("plain", run_plain), ("fused", run_fused), ("unfused", run_unfused)):
+                samples[label] += graph_time(fn, nsets, stream, reps=4)
+        t = {k: statistics.median(v) for k, v in samples.items()}
         out.append({
             "product": name, "a": list(a_shape), "b": list(b_shape),
             "epilogue": ("residual" if resid else act),
@@ -575,7 +579,7 @@ def measure_fused(device, peaks, l2):
             "tflops_fused": flop / (t["fused"] * 1e-3) / 1e12,
             "fused_cost_pct": 100.0 * (t["fused"] / t["plain"] - 1.0),
             "unfused_cost_pct": 100.0 * (t["unfused"] / t["plain"] - 1.0),
-            "timing": "cuda graph of %d launches x 10 replays, %d operand sets" % (max(4, nsets), nsets),
+            "timing": "cuda graph of %d launches x 4 replays x 3 interleaved rounds, %d operand sets" % (max(4, nsets), nsets),
         })
         plain.close()
         fused.close()
