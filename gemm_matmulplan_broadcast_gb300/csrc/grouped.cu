@@ -6,14 +6,16 @@
 // dispatch per product costs more than the product) and the GroupedGemm
 // interface of its plan (small products scheduled together).  The plan
 // numbers the 64 x 64 output tiles of all members consecutively (member i
-// owns tiles [tile_begin_i, tile_begin_{i+1})); persistent blocks walk the
-// tile numbers with a grid stride, find the member of a tile by binary search
-// in the descriptor table, and compute the tile.  Members with an empty
+// owns tiles [tile_begin_i, tile_begin_{i+1})) and keeps, next to the
+// descriptor table, the owning member of every tile; persistent blocks walk
+// the tile numbers with a grid stride, read the tile's member (one load),
+// and compute the tile.  Members with an empty
 // output own no tiles; K == 0 tiles are written as zeros.
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <type_traits>
 #include <vector>
 
 #include "common.cuh"
@@ -32,7 +34,7 @@ struct GDesc {
 
 template <typename T>
 __global__ void __launch_bounds__(kGThreads)
-grouped_kernel(const GDesc* __restrict__ desc, int count, int64_t total_tiles,
+grouped_kernel(const GDesc* __restrict__ desc, const int* __restrict__ owner, int64_t total_tiles,
                const void* const* __restrict__ Aptr, const void* const* __restrict__ Bptr,
                void* const* __restrict__ Yptr) {
     using acc_t = typename Num<T>::acc_t;
@@ -42,13 +44,7 @@ grouped_kernel(const GDesc* __restrict__ desc, int count, int64_t total_tiles,
     const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
 
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        // member of this tile: the last i with tile_begin_i <= tile
-        int lo = 0, hi = count - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (desc[mid].tile_begin <= tile) lo = mid;
-            else hi = mid - 1;
-        }
+        const int lo = owner[tile];                        // the member owning this tile
         const GDesc d = desc[lo];
         const int64_t local = tile - d.tile_begin;
         const int64_t m0 = (local / d.tiles_n) * kGBM, n0 = (local % d.tiles_n) * kGBN;
@@ -63,16 +59,22 @@ grouped_kernel(const GDesc* __restrict__ desc, int count, int64_t total_tiles,
 #pragma unroll
             for (int j = 0; j < kGTN; ++j) acc[i][j] = acc_t(0);
         for (int64_t k0 = 0; k0 < K; k0 += kGBK) {
-            __syncthreads();   // the previous step (or tile) is done with the tiles
-            for (int e = threadIdx.x; e < kGBM * kGBK; e += kGThreads) {
-                const int r = e / kGBK, c = e % kGBK;
-                const int64_t gm = m0 + r, gk = k0 + c;
-                As[c][r] = (gm < M && gk < K) ? Num<T>::to_acc(A[gm * K + gk]) : acc_t(0);
+            // all of a thread's loads of the step first, then the stores
+            constexpr int P = kGBM * kGBK / kGThreads;    // = kGBK * kGBN / kGThreads
+            acc_t va[P], vb[P];
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                const int e = threadIdx.x + q * kGThreads;
+                const int ra = e / kGBK, ca = e % kGBK, rb = e / kGBN, cb = e % kGBN;
+                va[q] = (m0 + ra < M && k0 + ca < K) ? Num<T>::to_acc(A[(m0 + ra) * K + k0 + ca]) : acc_t(0);
+                vb[q] = (k0 + rb < K && n0 + cb < N) ? Num<T>::to_acc(B[(k0 + rb) * N + n0 + cb]) : acc_t(0);
             }
-            for (int e = threadIdx.x; e < kGBK * kGBN; e += kGThreads) {
-                const int r = e / kGBN, c = e % kGBN;
-                const int64_t gk = k0 + r, gn = n0 + c;
-                Bs[r][c] = (gk < K && gn < N) ? Num<T>::to_acc(B[gk * N + gn]) : acc_t(0);
+            __syncthreads();   // the previous step (or tile) is done with the tiles
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                const int e = threadIdx.x + q * kGThreads;
+                As[e % kGBK][e / kGBK] = va[q];
+                Bs[e / kGBN][e % kGBN] = vb[q];
             }
             __syncthreads();
 #pragma unroll
@@ -101,6 +103,139 @@ grouped_kernel(const GDesc* __restrict__ desc, int count, int64_t total_tiles,
     }
 }
 
+// FLOAT16 / BFLOAT16 members: the same tiles on the tensor cores.  Four warps
+// per 64 x 64 tile, each a 32 x 32 quarter from 2 x 4 mma.sync.m16n8k16
+// products per 16-deep step (float32 accumulators).  The 64 x 32 A slice and
+// 32 x 64 B slice of a step are staged as 16-bit values (zero outside the
+// member), rows padded so that the ldmatrix row addresses of one 8 x 8
+// matrix fall in eight different bank groups; A fragments by ldmatrix, B
+// fragments by ldmatrix.trans from the row-major [k][n] slice.
+constexpr int kMK = 32;                 // K per staged slice
+constexpr int kALd = kMK + 8;           // A slice row: 40 halves (80 bytes)
+constexpr int kBLd = kGBN + 8;          // B slice row: 72 halves (144 bytes)
+
+__device__ __forceinline__ void g_ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void g_ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+template <bool BF16>
+__device__ __forceinline__ void g_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if (BF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128)
+grouped_mma_kernel(const GDesc* __restrict__ desc, const int* __restrict__ owner, int64_t total_tiles,
+                   const void* const* __restrict__ Aptr, const void* const* __restrict__ Bptr,
+                   void* const* __restrict__ Yptr) {
+    constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+    __shared__ __align__(16) unsigned short As[kGBM][kALd];
+    __shared__ __align__(16) unsigned short Bs[kMK][kBLd];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wm = (warp >> 1) * 32, wn = (warp & 1) * 32;    // this warp's quarter of the tile
+    const uint32_t as_base = static_cast<uint32_t>(__cvta_generic_to_shared(&As[0][0]));
+    const uint32_t bs_base = static_cast<uint32_t>(__cvta_generic_to_shared(&Bs[0][0]));
+
+    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const int lo = owner[tile];                        // the member owning this tile
+        const GDesc d = desc[lo];
+        const int64_t local = tile - d.tile_begin;
+        const int64_t m0 = (local / d.tiles_n) * kGBM, n0 = (local % d.tiles_n) * kGBN;
+        const int64_t M = d.m, N = d.n, K = d.k;
+        const unsigned short* __restrict__ A = static_cast<const unsigned short*>(Aptr[lo]);
+        const unsigned short* __restrict__ B = static_cast<const unsigned short*>(Bptr[lo]);
+        T* __restrict__ Y = static_cast<T*>(Yptr[lo]);
+
+        float acc[2][4][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
+        for (int64_t k0 = 0; k0 < K; k0 += kMK) {
+            // the slice's elements are all requested before any is stored, so
+            // the loads of a thread overlap instead of queueing one by one
+            constexpr int PA = kGBM * kMK / 128, PB = kMK * kGBN / 128;
+            unsigned short va[PA], vb[PB];
+#pragma unroll
+            for (int q = 0; q < PA; ++q) {
+                const int e = threadIdx.x + q * 128, r = e / kMK, c = e % kMK;
+                const int64_t gm = m0 + r, gk = k0 + c;
+                va[q] = (gm < M && gk < K) ? A[gm * K + gk] : (unsigned short)0;
+            }
+#pragma unroll
+            for (int q = 0; q < PB; ++q) {
+                const int e = threadIdx.x + q * 128, r = e / kGBN, c = e % kGBN;
+                const int64_t gk = k0 + r, gn = n0 + c;
+                vb[q] = (gk < K && gn < N) ? B[gk * N + gn] : (unsigned short)0;
+            }
+            __syncthreads();   // the previous slice (or tile) is no longer read
+#pragma unroll
+            for (int q = 0; q < PA; ++q) {
+                const int e = threadIdx.x + q * 128;
+                As[e / kMK][e % kMK] = va[q];
+            }
+#pragma unroll
+            for (int q = 0; q < PB; ++q) {
+                const int e = threadIdx.x + q * 128;
+                Bs[e / kGBN][e % kGBN] = vb[q];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < kMK; kk += 16) {
+                uint32_t a[2][4], b[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    // matrices: rows 0-7 / 8-15 at k, then at k + 8
+                    const int r = wm + 16 * i + (lane & 15), c = kk + (lane >> 4) * 8;
+                    g_ldsm_x4(as_base + (uint32_t)((r * kALd + c) * 2), a[i]);
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    // matrices: k 0-7 / 8-15 of columns n, then of columns n + 8
+                    const int r = kk + (lane & 15), c = wn + 16 * j + (lane >> 4) * 8;
+                    g_ldsm_x4_t(bs_base + (uint32_t)((r * kBLd + c) * 2), b[j]);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        g_mma<BF16>(acc[i][j], a[i], b[j >> 1][2 * (j & 1)], b[j >> 1][2 * (j & 1) + 1]);
+            }
+        }
+        // fragment (g, t): rows g and g + 8 of each 16-row block, columns 2t, 2t + 1
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t gm = m0 + wm + 16 * i + g + 8 * h;
+                    const int64_t gn = n0 + wn + 8 * j + 2 * t;
+                    if (gm >= M) continue;
+                    if (gn < N) Y[gm * N + gn] = Num<T>::from_acc(acc[i][j][2 * h]);
+                    if (gn + 1 < N) Y[gm * N + gn + 1] = Num<T>::from_acc(acc[i][j][2 * h + 1]);
+                }
+    }
+}
+
 }  // namespace
 }  // namespace olc
 
@@ -109,8 +244,9 @@ struct olc_grouped_plan {
     int count;
     std::vector<olc::GDesc> desc;
     int64_t total_tiles;
-    int device;                  // -1 until the descriptor table is on a device
+    int device;                  // -1 until the tables are on a device
     olc::GDesc* desc_dev;
+    int* owner_dev;              // member of every tile
     int sm_count;
 };
 
@@ -131,14 +267,24 @@ olc_status grouped_bind(olc_grouped_plan* p) {
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return grouped_from_cuda(cudaErrorNoDevice);
     if (p->device >= 0) return cur == p->device ? OLC_OK : OLC_ERR_WRONG_DEVICE;
+    // the descriptor table and, for every tile, the member that owns it
+    std::vector<int> owner((size_t)p->total_tiles);
+    for (int i = 0; i < p->count; ++i) {
+        const int64_t end = i + 1 < p->count ? p->desc[i + 1].tile_begin : p->total_tiles;
+        for (int64_t t = p->desc[i].tile_begin; t < end; ++t) owner[(size_t)t] = i;
+    }
     void* mem = nullptr;
     const size_t bytes = sizeof(olc::GDesc) * (size_t)p->count;
-    cudaError_t e = cudaMalloc(&mem, bytes);
+    const size_t obytes = sizeof(int) * owner.size();
+    cudaError_t e = cudaMalloc(&mem, bytes + obytes);
     if (e == cudaSuccess) e = cudaMemcpy(mem, p->desc.data(), bytes, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && obytes)
+        e = cudaMemcpy(static_cast<unsigned char*>(mem) + bytes, owner.data(), obytes, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         if (mem) cudaFree(mem);
         return grouped_from_cuda(e);
     }
+    p->owner_dev = reinterpret_cast<int*>(static_cast<unsigned char*>(mem) + bytes);
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, cur) != cudaSuccess || sms <= 0)
         sms = 152;
@@ -167,6 +313,7 @@ olc_status olc_grouped_plan_create(int count, const int64_t* m, const int64_t* n
     p->count = count;
     p->device = -1;
     p->desc_dev = nullptr;
+    p->owner_dev = nullptr;
     p->sm_count = 0;
     p->desc.resize((size_t)count);
     int64_t t = 0;
@@ -206,13 +353,25 @@ olc_status olc_grouped_execute(const olc_grouped_plan* plan, const void* const* 
     olc_status st = grouped_bind(p);
     if (st != OLC_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t grid = olc::min64(plan->total_tiles, (int64_t)plan->sm_count * 4);
-    cudaError_t e = olc::dispatch_dtype(plan->dtype, [&](auto tag) {
-        using T = decltype(tag);
-        olc::grouped_kernel<T><<<(unsigned)grid, olc::kGThreads, 0, s>>>(
-            p->desc_dev, p->count, p->total_tiles, A, B, Y);
-        return cudaGetLastError();
-    });
+    cudaError_t e;
+    if (plan->dtype == OLC_FLOAT16 || plan->dtype == OLC_BFLOAT16) {
+        const int64_t grid = olc::min64(plan->total_tiles, (int64_t)plan->sm_count * 8);
+        if (plan->dtype == OLC_FLOAT16)
+            olc::grouped_mma_kernel<__half><<<(unsigned)grid, 128, 0, s>>>(p->desc_dev, p->owner_dev,
+                                                                          p->total_tiles, A, B, Y);
+        else
+            olc::grouped_mma_kernel<__nv_bfloat16><<<(unsigned)grid, 128, 0, s>>>(
+                p->desc_dev, p->owner_dev, p->total_tiles, A, B, Y);
+        e = cudaGetLastError();
+    } else {
+        const int64_t grid = olc::min64(plan->total_tiles, (int64_t)plan->sm_count * 4);
+        e = olc::dispatch_dtype(plan->dtype, [&](auto tag) {
+            using T = decltype(tag);
+            olc::grouped_kernel<T><<<(unsigned)grid, olc::kGThreads, 0, s>>>(
+                p->desc_dev, p->owner_dev, p->total_tiles, A, B, Y);
+            return cudaGetLastError();
+        });
+    }
     return grouped_from_cuda(e);
 }
 
