@@ -247,6 +247,8 @@ __device__ __forceinline__ void fma_f2(unsigned long long& d, unsigned long long
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
+constexpr int SIMT_GROUP_M = 16;
+
 template <typename T, int BM, int BN, int BK, int TM, int TN, bool AT, bool BT>
 __global__ void __launch_bounds__(256, 2)
 simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
@@ -266,8 +268,15 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     const int64_t per_item = tiles_m * tiles_n;
     const int64_t item = blockIdx.x / per_item;
     const int64_t rem = blockIdx.x % per_item;
-    const int64_t m0 = (rem / tiles_n) * BM;
-    const int64_t n0 = (rem % tiles_n) * BN;
+    // tile raster in groups of SIMT_GROUP_M row blocks, column-major inside a
+    // group: the blocks resident at one time share a few A row strips and B
+    // column strips, so L2 serves most re-reads instead of DRAM
+    const int64_t span = (int64_t)SIMT_GROUP_M * tiles_n;
+    const int64_t first = (rem / span) * SIMT_GROUP_M;
+    const int64_t gm = min64(tiles_m - first, (int64_t)SIMT_GROUP_M);
+    const int64_t in = rem % span;
+    const int64_t m0 = (first + in % gm) * BM;
+    const int64_t n0 = (in / gm) * BN;
     int64_t a_off, b_off;
     batch_offsets(p.map, item, a_off, b_off);
     const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
