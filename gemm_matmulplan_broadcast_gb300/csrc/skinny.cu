@@ -257,8 +257,20 @@ static int skinny_m_blocks_per_sm(olc_dtype dt, int64_t M) {
 // wave fill, discounted by the extra partial-tile traffic it causes.
 // FLOAT16 / BFLOAT16 with 16-byte row strides: the tensor-core kernel with
 // swapped operands streams B through its TMA ring; the rest: the SIMT kernel.
+// FLOAT16 / BFLOAT16: the tensor cores (swapped operands) from 4 rows up,
+// and from 2 rows for a B of 256 MB or more; the SIMT kernel below that,
+// where one B vector feeds only one to three rows and the plain streaming
+// kernel is faster (measured on GB300: 6.8 against 5.8 TB/s for one row of
+// [8192, 28672], 5.2 against 2.0 TB/s for one row of [4096, 11008]).  The
+// kernel-family override forces the SIMT kernel (variant 1) or the tensor
+// cores (variant 2).
 static bool skinny_m_on_tc(olc_dtype dt, const Problem& p) {
-    return (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K) && p.M <= 16;
+    if (!(dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) || !tc_shape_ok(dt, p.N, p.K) || p.M > 16)
+        return false;
+    if (p.variant == 1) return false;
+    if (p.variant == 2) return true;
+    const double b_bytes = 2.0 * (double)p.K * (double)p.N * (double)p.items;
+    return p.M >= 4 || (p.M >= 2 && b_bytes >= 256.0 * 1024 * 1024);
 }
 
 static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count);

@@ -391,6 +391,10 @@ int olc_matmul_plan_splits(const olc_matmul_plan* plan);
  * FLOAT16 / BFLOAT16: 0 = automatic, 1 = the tcgen05 16-column kernel,
  * 2 = the register-streaming mma.sync kernel wherever it applies (one B for
  * all rows, K a multiple of 8, B^T within its shared-memory budget).
+ * SKINNY_M plans of FLOAT16 / BFLOAT16: 0 = automatic (tensor cores from 4
+ * rows, or from 2 rows with a B of 256 MB or more), 1 = the SIMT streaming
+ * kernel, 2 = the swapped-operand tcgen05 kernel.  GENERAL_TC plans of 8-bit
+ * floats: 1 = one CTA per 128 x 256 tile instead of CTA pairs.
  * Results are identical within the parity tolerance either way.  Errors:
  * OLC_ERR_NULL, OLC_ERR_INVALID. */
 olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant);

@@ -317,12 +317,26 @@ TC_SKINNY_M_SHAPES = [
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
 @pytest.mark.parametrize("shapes", TC_SKINNY_M_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
-def test_tc_skinny_m(dtype, shapes):
+@pytest.mark.parametrize("variant", [0, 1, 2], ids=["auto", "simt", "tcgen05"])
+def test_tc_skinny_m(dtype, shapes, variant):
+    """FLOAT16 / BFLOAT16 skinny-M: automatic choice, the SIMT streaming
+    kernel (variant 1) and the swapped-operand tcgen05 kernel (variant 2)."""
     a_shape, b_shape = shapes
-    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=14)
-    check_product(a, b, dtype, algorithm="skinny_m")
-    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=14)
-    check_product(ai, bi, dtype, algorithm="skinny_m", exact=True)
+    for dist_a, dist_b, exact in ((synth.normal(1.0), synth.normal(0.02), False),
+                                  (synth.SMALL_INT, synth.SMALL_INT, True)):
+        a, b = synth.operands(a_shape, b_shape, dtype, dist_a, dist_b, seed=14)
+        A, B = a.cuda(), b.cuda()
+        with Plan(a.shape, b.shape, dtype) as p:
+            p.force("skinny_m")
+            p.set_tc_variant(variant)
+            n = int(np.prod(p.output_shape))
+            buf = torch.full((n + 64,), float("nan"), dtype=A.dtype, device="cuda")
+            Y = buf[:n].view(p.output_shape)
+            p.execute_checked(A, B, Y)
+            torch.cuda.synchronize()
+            assert torch.isnan(buf[n:].float()).all()
+        y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+        compare(Y.cpu(), y_ref, s, dtype, exact=exact)
 
 
 def _pair_product(a, b, dtype, exact=False):
