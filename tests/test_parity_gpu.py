@@ -122,6 +122,7 @@ SMALL_SHAPES = [
     ((5, 1, 7, 40), (1, 3, 40, 16)),
     ((64,), (64, 48)),
     ((3, 80, 64), (64,)),
+    ((2, 1, 2, 1, 2, 1, 5, 24), (1, 2, 1, 2, 1, 2, 24, 16)),   # rank 8: 64 broadcast items
 ]
 
 
