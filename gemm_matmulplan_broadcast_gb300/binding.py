@@ -343,8 +343,10 @@ class Plan:
 
     def __call__(self, A, B, out=None, stream=None):
         import torch
+        from .synth import TORCH_DTYPES, output_dtype
         if out is None:
-            out = torch.empty(self.output_shape, dtype=A.dtype, device=A.device)
+            out = torch.empty(self.output_shape, dtype=TORCH_DTYPES[output_dtype(self.dtype)],
+                              device=A.device)
         return self.execute(A, B, out, stream)
 
 

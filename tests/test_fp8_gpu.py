@@ -103,3 +103,13 @@ def test_fp8_rejections():
             p.force("general_tc")
         with pytest.raises(OlcError):
             p.force("split_k")
+
+
+def test_fp8_convenience_call_returns_float32():
+    from gemm_matmulplan_broadcast_gb300 import matmul
+    a, b = synth.operands((64, 96), (96, 40), "float8_e5m2", synth.SMALL_INT, synth.SMALL_INT, 46)
+    y = matmul(a.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    assert y.dtype == torch.float32 and tuple(y.shape) == (64, 40)
+    ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "float8_e5m2")
+    compare(y.cpu(), ref, s, "float8_e5m2", exact=True)
