@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -1224,14 +1225,25 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 namespace tiny {
 
+// Split-K for outputs of at most 32 x 32: one K slice per CTA, CTAs in
+// clusters of CL.  Each CTA's 32 x 32 partial stays in its shared memory; CTA
+// r of a cluster sums rows [r * 32 / CL, (r + 1) * 32 / CL) of the CL partials
+// through distributed shared memory and writes that cluster sum; the last
+// cluster to deliver a row band sums the cluster sums in cluster order and
+// stores.  Every sum runs in a fixed order, so the result is the same run to
+// run.
 constexpr int ROWS = 32, COLS = 32;
 constexpr int A_CHUNK = ROWS * BK * 2;             // 4 KiB
 constexpr int B_CHUNK = BK * COLS * 2;             // 4 KiB
 constexpr int CHUNK = A_CHUNK + B_CHUNK;
 constexpr int STAGES = 24;
 constexpr int MMA_WARPS = 4;
+constexpr int MMA_THREADS = MMA_WARPS * 32;
 constexpr int THREADS_T = (MMA_WARPS + 1) * 32;    // + one producer warp
-constexpr int SMEM_BYTES = STAGES * CHUNK + MMA_WARPS * ROWS * (COLS + 1) * 4 + 1024 + 512;
+constexpr int RED_BYTES = MMA_WARPS * ROWS * (COLS + 1) * 4;
+constexpr int TILE_BYTES = ROWS * COLS * 4;        // this CTA's partial (float32)
+constexpr int SMEM_BYTES = STAGES * CHUNK + RED_BYTES + TILE_BYTES + 1024 + 512;
+constexpr int LOAD_BATCH = 8;                      // cluster sums loaded per round trip
 
 struct Bars {
     uint64_t full[STAGES];
@@ -1266,22 +1278,67 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+}
+// arrival count with release (this CTA's earlier writes, ordered before it by
+// a block barrier) and acquire (the other arrivals' writes) at GPU scope
+__device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* counter) {
+    unsigned int prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
+    return prev;
+}
+
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their writes are visible (a no-op without the launch
+// attribute), and let the next launch in the stream start its prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int CL>
 __global__ void __launch_bounds__(THREADS_T, 1)
 splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    static_assert(CL == 2 || CL == 4 || CL == 8, "cluster of 2, 4 or 8 CTAs");
+    constexpr int BAND_ROWS = ROWS / CL;                 // rows this CTA reduces
+    constexpr int BAND_F4 = BAND_ROWS * COLS / 4;        // float4s of one band
+    constexpr int PARTS = MMA_THREADS / BAND_F4;         // threads per float4 at level 2
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* red = reinterpret_cast<float*>(base + STAGES * CHUNK);      // [4][32][33]
-    Bars* s = reinterpret_cast<Bars*>(base + STAGES * CHUNK + MMA_WARPS * ROWS * (COLS + 1) * 4);
+    float* red = reinterpret_cast<float*>(base + STAGES * CHUNK);           // [4][32][33]
+    float* tile = reinterpret_cast<float*>(base + STAGES * CHUNK + RED_BYTES);   // [32][32]
+    Bars* s = reinterpret_cast<Bars*>(base + STAGES * CHUNK + RED_BYTES + TILE_BYTES);
     volatile int* abort_flag = &s->abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
     const int slice = blockIdx.x;
-    const int64_t kb0 = (int64_t)slice * p.kb_per_split;
-    const int64_t kb1 = min64(p.k_blocks, kb0 + p.kb_per_split);
-    const int nchunks = (int)(kb1 - kb0);
+    const int rank = (int)pair::cluster_rank();
+    const int cluster = slice / CL;
+    // K blocks split evenly: slice s takes [s * kb / S, (s + 1) * kb / S)
+    const int64_t kb0 = (int64_t)slice * p.k_blocks / p.splits;
+    const int64_t kb1 = (int64_t)(slice + 1) * p.k_blocks / p.splits;
+    const int nchunks = kb1 > kb0 ? (int)(kb1 - kb0) : 0;
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&s->full[i], 1);
             mbar_init(&s->empty[i], MMA_WARPS);
@@ -1292,6 +1349,9 @@ splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    // nothing global is read or written before the previous grid is done
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == MMA_WARPS) {
         // producer: one lane issues every chunk's two TMA loads
@@ -1317,6 +1377,7 @@ splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 for (int i = 0; i < STAGES; ++i)
                     if (armed[i]) mbar_wait_drain(&s->full[i], armed_parity[i]);
         }
+        __syncwarp();
     } else {
         // MMA warps: warp w takes the 16-deep step w of every chunk
         float acc[2][4][4];
@@ -1370,69 +1431,73 @@ splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 mine[(row + 8) * (COLS + 1) + col + 1] = acc[mb][nb][3];
             }
         epi_sync();
-        // slice sum in warp order -> part1[slice]
-        const int tid = threadIdx.x;                  // 0..127
-        float* P = p.part1 + (int64_t)slice * ROWS * COLS;
+        // the slice's partial: warp sums in warp order -> tile
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const int idx = tid + e * 128;
+            const int idx = tid + e * MMA_THREADS;
             const int row = idx / COLS, col = idx % COLS;
             float v = red[row * (COLS + 1) + col];
 #pragma unroll
             for (int w = 1; w < MMA_WARPS; ++w) v += red[w * ROWS * (COLS + 1) + row * (COLS + 1) + col];
-            P[idx] = v;
-        }
-        // two-level fixed-order reduction over the slices
-        const int g = slice / p.group;
-        const int gsize = min(p.group, p.splits - g * p.group);
-        const int64_t tile_floats = (int64_t)ROWS * COLS;
-        const int64_t e4 = tid, e4b = tid + 128;      // 256 float4s per partial
-        auto store_y = [&](int64_t e, float4 v) {
-            const int row = (int)((e * 4) / COLS), col = (int)((e * 4) % COLS);
-            if (row < p.M && col < p.N) store4(p, 0, row, col, v);
-        };
-        __threadfence();
-        epi_sync();
-        if (tid == 0) {
-            const unsigned int prev = atomicAdd(p.cnt1 + g, 1u);
-            s->last_flag = (prev == (unsigned int)gsize - 1) ? 1 : 0;
-        }
-        epi_sync();
-        const int last1 = s->last_flag;
-        epi_sync();
-        if (last1) {
-            __threadfence();
-            const float* first = p.part1 + (int64_t)g * p.group * tile_floats;
-            float4 v0, v1;
-            ordered_sum4x2(first, tile_floats, gsize, e4, e4b, v0, v1);
-            if (p.groups == 1) {
-                store_y(e4, v0);
-                store_y(e4b, v1);
-                if (tid == 0) p.cnt1[g] = 0u;
-            } else {
-                float* gsum = p.part2 + (int64_t)g * tile_floats;
-                reinterpret_cast<float4*>(gsum)[e4] = v0;
-                reinterpret_cast<float4*>(gsum)[e4b] = v1;
-                __threadfence();
-                epi_sync();
-                if (tid == 0) {
-                    p.cnt1[g] = 0u;
-                    const unsigned int prev = atomicAdd(p.cnt2, 1u);
-                    s->last_flag = (prev == (unsigned int)p.groups - 1) ? 1 : 0;
-                }
-                epi_sync();
-                const int last2 = s->last_flag;
-                epi_sync();
-                if (last2) {
-                    __threadfence();
-                    ordered_sum4x2(p.part2, tile_floats, p.groups, e4, e4b, v0, v1);
-                    store_y(e4, v0);
-                    store_y(e4b, v1);
-                    if (tid == 0) p.cnt2[0] = 0u;
-                }
-            }
+            tile[idx] = v;
         }
     }
+    // every CTA of the cluster holds its partial
+    cluster_arrive();
+    cluster_wait();
+
+    // level 1: this CTA's row band summed over the cluster's CTAs in rank
+    // order, through distributed shared memory
+    const int band0 = rank * BAND_ROWS * COLS;            // first float of the band
+    if (tid < BAND_F4) {
+        float4 x[CL];
+#pragma unroll
+        for (int r = 0; r < CL; ++r) x[r] = ld_cluster4(pair::map_to(tile + band0 + tid * 4, r));
+        float4 v = x[0];
+#pragma unroll
+        for (int r = 1; r < CL; ++r) add4(v, x[r]);
+        reinterpret_cast<float4*>(p.part1 + (int64_t)cluster * ROWS * COLS + band0)[tid] = v;
+    }
+    // done with the other CTAs' shared memory (waited for before exit)
+    cluster_arrive();
+
+    // level 2: the last cluster to deliver this band sums the cluster sums
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned int prev = arrive_acq_rel(p.cnt1 + rank);
+        s->last_flag = (prev == (unsigned int)p.groups - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s->last_flag && tid < MMA_THREADS) {
+        const int f = tid % BAND_F4, part = tid / BAND_F4;
+        const int c0 = part * p.groups / PARTS, c1 = (part + 1) * p.groups / PARTS;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4* src = reinterpret_cast<const float4*>(p.part1 + band0) + f;
+        for (int cb = c0; cb < c1; cb += LOAD_BATCH) {
+            float4 x[LOAD_BATCH];
+#pragma unroll
+            for (int j = 0; j < LOAD_BATCH; ++j)
+                if (cb + j < c1) x[j] = __ldcg(src + (int64_t)(cb + j) * (ROWS * COLS / 4));
+#pragma unroll
+            for (int j = 0; j < LOAD_BATCH; ++j)
+                if (cb + j < c1) add4(v, x[j]);
+        }
+        // the parts' sums in part order (red is free again)
+        float4* parts = reinterpret_cast<float4*>(red);
+        parts[part * BAND_F4 + f] = v;
+        epi_sync();
+        if (part == 0) {
+            float4 t = parts[f];
+#pragma unroll
+            for (int q2 = 1; q2 < PARTS; ++q2) add4(t, parts[q2 * BAND_F4 + f]);
+            const int e = band0 + f * 4;
+            const int row = e / COLS, col = e % COLS;
+            if (row < p.M && col < p.N) store4(p, 0, row, col, t);
+        }
+        if (tid == 0) p.cnt1[rank] = 0u;
+    }
+    // no CTA leaves while another may still read its partial
+    cluster_wait();
 }
 
 }  // namespace tiny
@@ -1802,33 +1867,113 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
     return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel<true>, ma, mb, p);
 }
 
-// Split-K plan and launch for tiny outputs: one slice per CTA, about one
-// CTA per SM, at most SUM_BATCH^2 slices, slices of at least 2 chunks.
+// Split-K for tiny outputs: one slice per CTA, clusters of CL CTAs, about one
+// CTA per SM (as many clusters as fit at once), slices of at least 2 chunks.
+template <int CL>
+static cudaError_t tiny_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(tiny::splitk_tiny_kernel<CL>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, tiny::SMEM_BYTES);
+    });
+    return err;
+}
+
+// Clusters of CL that the device runs at once (an estimate from the SM count
+// when the occupancy query is unavailable); cached per device.
+template <int CL>
+static int tiny_max_clusters(int sm_count) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cached[kMaxDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        dev = -1;
+    }
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (dev >= 0 && tiny_attr<CL>() == cudaSuccess) {
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3((unsigned)(CL * (sm_count / CL > 0 ? sm_count / CL : 1)), 1, 1);
+        cfg.blockDim = dim3(tiny::THREADS_T, 1, 1);
+        cfg.dynamicSmemBytes = tiny::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, tiny::splitk_tiny_kernel<CL>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+    }
+    if (n <= 0) return sm_count / CL > 0 ? sm_count / CL : 1;
+    if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+static int tiny_cluster_size(int64_t slices) { return slices >= 16 ? 8 : (slices >= 8 ? 4 : 2); }
+
 static SplitPlan tiny_plan(const Problem& pr, int sm_count) {
     SplitPlan sp;
     const int64_t kbs = ceil_div(pr.K, BK);
-    int64_t want = min64((int64_t)sm_count, (int64_t)SUM_BATCH * SUM_BATCH);
-    want = min64(want, max64(1, kbs / 2));
-    if (pr.split_hint > 0) want = min64(pr.split_hint, min64(kbs, (int64_t)SUM_BATCH * SUM_BATCH));
-    sp.kb_per_split = ceil_div(kbs, want);
-    sp.splits = (int)ceil_div(kbs, sp.kb_per_split);
-    int g = 1;
-    while ((int64_t)g * g < sp.splits) ++g;
-    sp.group = g < SUM_BATCH ? g : SUM_BATCH;
-    sp.groups = (int)ceil_div(sp.splits, sp.group);
+    int64_t want = max64(1, kbs / 2);
+    if (pr.split_hint > 0) want = min64(pr.split_hint, kbs);
+    const int cl = tiny_cluster_size(want);
+    int64_t clusters = max64(1, want / cl);
+    if (pr.split_hint <= 0) {
+        const int fit = cl == 8 ? tiny_max_clusters<8>(sm_count)
+                                : (cl == 4 ? tiny_max_clusters<4>(sm_count) : tiny_max_clusters<2>(sm_count));
+        clusters = max64(1, min64(clusters, fit));
+    }
+    sp.splits = (int)(clusters * cl);
+    sp.kb_per_split = ceil_div(kbs, sp.splits);
+    sp.group = cl;
+    sp.groups = (int)clusters;
     sp.tiles = 1;
-    const int64_t tile_bytes = (int64_t)tiny::ROWS * tiny::COLS * 4;
-    sp.part1_bytes = (size_t)(sp.splits * tile_bytes);
-    sp.part2_bytes = sp.groups > 1 ? (size_t)(sp.groups * tile_bytes) : 0;
-    sp.counters = (size_t)(sp.groups + 1);
+    sp.part1_bytes = (size_t)(clusters * tiny::TILE_BYTES);
+    sp.part2_bytes = 0;
+    sp.counters = (size_t)cl;
     return sp;
+}
+
+template <int CL>
+static cudaError_t launch_tiny_cl(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p,
+                                  int grid, cudaStream_t s) {
+    const cudaError_t e = tiny_attr<CL>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(tiny::THREADS_T, 1, 1);
+    cfg.dynamicSmemBytes = tiny::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // the prologue may overlap the tail of the previous kernel in the stream;
+    // the kernel waits for that kernel before touching global memory
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tiny::splitk_tiny_kernel<CL>, ma, mb, p);
 }
 
 static cudaError_t launch_tiny(olc_dtype dt, const Problem& pr, int sm_count, const Workspace& ws,
                                cudaStream_t s) {
     const SplitPlan sp = tiny_plan(pr, sm_count);
-    if (ws.partial_bytes < sp.part1_bytes + sp.part2_bytes || ws.counter_count < sp.counters ||
-        !ws.partials || !ws.counters)
+    if (ws.partial_bytes < sp.part1_bytes || ws.counter_count < sp.counters || !ws.partials ||
+        !ws.counters)
         return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
     std::memset(&ma, 0, sizeof ma);
@@ -1854,20 +1999,12 @@ static cudaError_t launch_tiny(olc_dtype dt, const Problem& pr, int sm_count, co
     p.groups = sp.groups;
     p.kb_per_split = sp.kb_per_split;
     p.part1 = static_cast<float*>(ws.partials);
-    p.part2 = sp.groups > 1
-                  ? reinterpret_cast<float*>(static_cast<char*>(ws.partials) + sp.part1_bytes)
-                  : nullptr;
     p.cnt1 = ws.counters;
-    p.cnt2 = ws.counters + sp.groups;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tiny::splitk_tiny_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tiny::SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    tiny::splitk_tiny_kernel<<<sp.splits, tiny::THREADS_T, tiny::SMEM_BYTES, s>>>(ma, mb, p);
-    return cudaGetLastError();
+    switch (sp.group) {
+        case 8: return launch_tiny_cl<8>(ma, mb, p, sp.splits, s);
+        case 4: return launch_tiny_cl<4>(ma, mb, p, sp.splits, s);
+        default: return launch_tiny_cl<2>(ma, mb, p, sp.splits, s);
+    }
 }
 
 static double operand_bytes(const Problem& pr) {

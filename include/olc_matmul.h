@@ -456,9 +456,10 @@ olc_status olc_debug_wait_selftest(uint64_t limit_ns, int arrive, void* stream);
  * partial tiles and arrival counters in one file-scope device array of
  * OLC_SPLIT_K_STATIC_SCRATCH_BYTES bytes inside the library.
  *
- * It runs the same split-K kernel as the plan path (partials per K slice,
- * summed by the last-arriving block in slice order) with the number of slices
- * capped so the partials fit the array.
+ * It runs the SIMT split-K kernel (the plan path's kernel for FLOAT and
+ * DOUBLE: partials per K slice, summed by the last-arriving block in slice
+ * order) for every type, with the number of slices capped so the partials
+ * fit the array; FLOAT16 / BFLOAT16 plans use a tensor-core kernel instead.
  *
  *  dtype: OLC_FLOAT, OLC_DOUBLE, OLC_FLOAT16 or OLC_BFLOAT16.
  *  A, B, Y: caller-owned device pointers (M*K, K*N and M*N elements).
