@@ -54,6 +54,8 @@ struct olc_matmul_plan {
     void* const_b;
     size_t const_b_bytes;
     int const_b_set;
+    void* const_bt;              // 8-bit float tensor-core plans: constant B as [N, K] bytes
+    size_t const_bt_bytes;
     // fused epilogue: activation, and a residual in the output's layout
     int act;
     int residual;
@@ -361,7 +363,9 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     if (!al && algo != OLC_ALGO_DIRECT && algo != OLC_ALGO_GENERAL_SIMT) algo = OLC_ALGO_DIRECT;
     cudaError_t e = cudaSuccess;
     if (is_fp8(dt)) {
-        e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s)
+        // the plan's constant B comes transposed already
+        const void* bt = (p->const_bt && B == p->const_b) ? p->const_bt : nullptr;
+        e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s, bt)
                                         : launch_fp8_simt(dt, pr, s);
         return from_cuda(e);
     }
@@ -578,11 +582,12 @@ void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
         if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
         cudaGetLastError();
     }
-    if (plan->const_b) {
+    if (plan->const_b || plan->const_bt) {
         int cur = -1;
         cudaGetDevice(&cur);
         if (plan->device >= 0 && cur != plan->device) cudaSetDevice(plan->device);
-        cudaFree(plan->const_b);
+        if (plan->const_b) cudaFree(plan->const_b);
+        if (plan->const_bt) cudaFree(plan->const_bt);
         if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
         cudaGetLastError();
     }
@@ -628,6 +633,31 @@ olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, 
         cudaError_t e = cudaMemcpyAsync(plan->const_b, B, bytes, cudaMemcpyDefault, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return from_cuda(e);
+    }
+    // 8-bit float tensor-core plans: keep B transposed as well ([N, K], the
+    // K-major operand the MMA reads), so executes with the constant B skip
+    // the per-call transpose
+    if (plan->const_bt) {
+        cudaFree(plan->const_bt);
+        plan->const_bt = nullptr;
+        plan->const_bt_bytes = 0;
+    }
+    if (bytes > 0 && is_fp8(plan->dtype) && plan->algo == OLC_ALGO_GENERAL_TC) {
+        Problem pr = make_problem(plan, nullptr, plan->const_b, nullptr);
+        void* mem = nullptr;
+        if (cudaMalloc(&mem, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return OLC_ERR_OOM;
+        }
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        cudaError_t e = launch_fp8_transpose(pr, mem, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) {
+            cudaFree(mem);
+            return from_cuda(e);
+        }
+        plan->const_bt = mem;
+        plan->const_bt_bytes = bytes;
     }
     plan->const_b_set = 1;
     return OLC_OK;

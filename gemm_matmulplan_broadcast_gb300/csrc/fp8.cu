@@ -122,6 +122,46 @@ __global__ void __launch_bounds__(256) transpose_kernel(const unsigned char* __r
     }
 }
 
+// Vector form for K % 16 == 0 and N % 16 == 0 (16-byte aligned rows): 128 x
+// 128 byte tiles, 16-byte loads along n and 16-byte stores along k.  Tile
+// row r keeps its 16-byte chunk c at chunk c ^ ((r >> 4) & 7), so the 32
+// lanes of a store warp (8 k-chunks x 4 n) read 32 different banks.
+constexpr int TT = 128;
+
+__global__ void __launch_bounds__(256) transpose16_kernel(const unsigned char* __restrict__ B,
+                                                          unsigned char* __restrict__ Bt, int64_t K,
+                                                          int64_t N, int64_t tiles_n) {
+    __shared__ __align__(16) unsigned char t[TT * TT];
+    const int64_t k0 = (blockIdx.x / tiles_n) * TT, n0 = (blockIdx.x % tiles_n) * TT;
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = tid + 256 * i;
+        const int r = e >> 3, c = e & 7;                  // r: k, c: 16-byte chunk along n
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (k0 + r < K && n0 + c * 16 < N)
+            v = __ldg(reinterpret_cast<const uint4*>(B + (k0 + r) * N + n0 + c * 16));
+        *reinterpret_cast<uint4*>(t + r * TT + ((c ^ ((r >> 4) & 7)) << 4)) = v;
+    }
+    __syncthreads();
+    const int lane = tid & 31, warp = tid >> 5;
+    const int kc = lane & 7;                              // 16-byte chunk along k
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int n = warp * 16 + i * 4 + (lane >> 3);    // tile column = output row
+        const int col = ((n >> 4) ^ kc) << 4 | (n & 15);  // rows kc*16.. share (r >> 4) = kc
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int r = kc * 16 + q * 4;
+            w[q] = (uint32_t)t[r * TT + col] | ((uint32_t)t[(r + 1) * TT + col] << 8) |
+                   ((uint32_t)t[(r + 2) * TT + col] << 16) | ((uint32_t)t[(r + 3) * TT + col] << 24);
+        }
+        if (n0 + n < N && k0 + kc * 16 < K)
+            *reinterpret_cast<uint4*>(Bt + (n0 + n) * K + k0 + kc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // tensor-core kernel
 
@@ -435,16 +475,33 @@ cudaError_t launch_fp8_simt(olc_dtype dt, const Problem& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_fp8_transpose(const Problem& p, void* bt, cudaStream_t s) {
+    const unsigned char* b = static_cast<const unsigned char*>(p.B);
+    unsigned char* out = static_cast<unsigned char*>(bt);
+    if (p.K <= 0 || p.N <= 0) return cudaSuccess;
+    if (p.N % 16 == 0 && p.K % 16 == 0 && reinterpret_cast<uintptr_t>(b) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(out) % 16 == 0) {
+        const int64_t ttn = ceil_div(p.N, f8::TT), ttk = ceil_div(p.K, f8::TT);
+        if (ttn * ttk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        f8::transpose16_kernel<<<(unsigned)(ttn * ttk), 256, 0, s>>>(b, out, p.K, p.N, ttn);
+    } else {
+        const int64_t ttn = ceil_div(p.N, 64), ttk = ceil_div(p.K, 64);
+        if (ttn * ttk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        f8::transpose_kernel<<<(unsigned)(ttn * ttk), 256, 0, s>>>(b, out, p.K, p.N, ttn);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
-                          cudaStream_t s) {
+                          cudaStream_t s, const void* bt_ready) {
     if (!fp8_tc_ok(p)) return cudaErrorInvalidValue;
-    if (!ws.partials || ws.partial_bytes < fp8_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
-    unsigned char* bt = static_cast<unsigned char*>(ws.partials);
-    const int64_t ttn = ceil_div(p.N, 64), ttk = ceil_div(p.K, 64);
-    f8::transpose_kernel<<<(unsigned)(ttn * ttk), 256, 0, s>>>(static_cast<const unsigned char*>(p.B), bt,
-                                                               p.K, p.N, ttn);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const unsigned char* bt = static_cast<const unsigned char*>(bt_ready);
+    if (!bt) {
+        if (!ws.partials || ws.partial_bytes < fp8_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
+        const cudaError_t e = launch_fp8_transpose(p, ws.partials, s);
+        if (e != cudaSuccess) return e;
+        bt = static_cast<const unsigned char*>(ws.partials);
+    }
     // CTA pairs (256 x 256 tiles, half of B per CTA) once the product holds
     // a pair tile; 128 x 256 tiles of one CTA otherwise (or when asked)
     if (p.M >= 256 && p.N >= 256 && p.variant != 1) return launch_pair_f8(dt, p, bt, sm_count, s);

@@ -118,8 +118,12 @@ int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count);
 cudaError_t launch_fp8_simt(olc_dtype dt, const Problem& p, cudaStream_t stream);
 bool fp8_tc_ok(const Problem& p);
 size_t fp8_tc_workspace_bytes(const Problem& p);
+// bt_ready: B already transposed ([N, K] bytes; a plan's constant B), else
+// the transpose runs into the workspace first
 cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const void* bt_ready = nullptr);
+// B [K, N] bytes -> bt [N, K] bytes
+cudaError_t launch_fp8_transpose(const Problem& p, void* bt, cudaStream_t stream);
 // the CTA-pair tensor-core kernel on 8-bit float operands: A [M, K] and the
 // transposed B [N, K] (bytes), float32 Y; one item, M and N >= 256
 cudaError_t launch_pair_f8(olc_dtype dt, const Problem& p, const void* bt, int sm_count,

@@ -245,9 +245,13 @@ olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const vo
  * copy is made on `stream` and has completed when the call returns, so the
  * caller may free or overwrite its buffer.  Device memory is allocated once
  * (cudaMalloc on the plan's device) and freed with the plan; calling again
- * replaces the contents.  No repacking is done: the kernels read B's layout
- * directly.  Errors: OLC_ERR_NULL, OLC_ERR_BUFFER_TOO_SMALL (b_numel is not
- * the planned size), OLC_ERR_WRONG_DEVICE, OLC_ERR_OOM, OLC_ERR_CUDA.
+ * replaces the contents.  The 16-bit and wider kernels read B's layout
+ * directly.  A plan with 8-bit float operands on the tensor cores also keeps
+ * B transposed ([N, K] bytes, the K-major operand the MMA reads; b_numel more
+ * bytes of device memory), so executes with the constant B skip the
+ * transpose that an execute with a caller's B runs first.  Errors:
+ * OLC_ERR_NULL, OLC_ERR_BUFFER_TOO_SMALL (b_numel is not the planned size),
+ * OLC_ERR_WRONG_DEVICE, OLC_ERR_OOM, OLC_ERR_CUDA.
  */
 olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, int64_t b_numel,
                                           void* stream);

@@ -113,3 +113,27 @@ def test_fp8_convenience_call_returns_float32():
     assert y.dtype == torch.float32 and tuple(y.shape) == (64, 40)
     ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "float8_e5m2")
     compare(y.cpu(), ref, s, "float8_e5m2", exact=True)
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes", [((260, 2064), (2064, 516)), ((512, 1024), (1024, 2048)),
+                                    ((96, 272), (272, 48)), ((37, 55), (55, 29))],
+                         ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_constant_b_prepacked(dtype, shapes):
+    """A constant B is kept transposed by the plan (tensor-core plans); the
+    executes without B give the per-call result bit for bit, also after the
+    source is overwritten."""
+    a, b = synth.operands(shapes[0], shapes[1], dtype, synth.normal(1.0), synth.normal(0.5), 43)
+    A = a.cuda()
+    with Plan(a.shape, b.shape, dtype) as p:
+        Y1 = torch.empty(p.output_shape, device="cuda")
+        Y2 = torch.empty_like(Y1)
+        p.execute(A, b.cuda(), Y1)
+        src = b.cuda()
+        p.set_constant_b(src)
+        src.view(torch.uint8).fill_(0x38)
+        p.execute_constant(A, Y2)
+        torch.cuda.synchronize()
+        assert torch.equal(Y1, Y2)
+    ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+    compare(Y2.cpu(), ref, s, dtype)
