@@ -230,6 +230,8 @@ TC_SPLIT_SHAPES = [
     ((40, 20000), (20000, 24)),        # 32-column tiles, N tail
     ((16, 9000), (9000, 16)),          # 16-column tiles
     ((8, 3000), (3000, 8)),
+    ((32, 1536), (1536, 32)),          # clusters of 4 CTAs
+    ((24, 640), (640, 16)),            # clusters of 2 CTAs
     ((300, 5000), (5000, 264)),        # 256-column tiles, several tiles
     ((2, 24, 2048), (2048, 40)),       # folded batch
     ((3, 24, 1024), (3, 1024, 32)),    # batched B
@@ -265,6 +267,30 @@ def test_tc_split_k(dtype, shapes):
     _split_product(a, b, dtype, 0, exact=False)
     ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=12)
     _split_product(ai, bi, dtype, 0, exact=True)
+
+
+@pytest.mark.parametrize("splits", [2, 5, 13, 24, 64, 200])
+def test_tiny_split_k_slice_counts(splits):
+    """The small-output split-K kernel with requested slice counts (clusters
+    of 2, 4 and 8 CTAs, more clusters than run at once): integer inputs bit
+    for bit, normal inputs within the bound, two runs identical."""
+    shapes = ((32, 16384), (16384, 32))
+    for dist_a, dist_b, exact in [(synth.SMALL_INT, synth.SMALL_INT, True),
+                                  (synth.normal(1.0), synth.normal(0.02), False)]:
+        a, b = synth.operands(shapes[0], shapes[1], "float16", dist_a, dist_b, seed=13)
+        A, B = a.cuda(), b.cuda()
+        with Plan(a.shape, b.shape, "float16") as p:
+            p.force("split_k")
+            p.set_splits(splits)
+            assert p.splits >= 2
+            Y = torch.empty(p.output_shape, dtype=A.dtype, device="cuda")
+            Y2 = torch.empty_like(Y)
+            p.execute_checked(A, B, Y)
+            p.execute_checked(A, B, Y2)
+            torch.cuda.synchronize()
+            assert torch.equal(Y, Y2)
+        y_ref, sabs = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "float16")
+        compare(Y.cpu(), y_ref, sabs, "float16", exact=exact)
 
 
 TC_SKINNY_N_SHAPES = [
