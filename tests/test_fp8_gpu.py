@@ -20,6 +20,7 @@ TC_SHAPES = [
     ((256, 128), (128, 256)),          # one pair tile
     ((260, 2064), (2064, 516)),        # pair tiles with the peer CTA's rows and columns ragged
     ((300, 1040), (1040, 264)),        # M, N, K tails (K a multiple of 16, N of 4)
+    ((200, 1040), (1040, 400)),        # 16-byte B transpose with ragged K and N tiles
     ((2, 512, 2048), (2048, 1024)),    # folded batch, several tiles and K blocks
     ((64, 4096), (4096, 4096)),
 ]
