@@ -5,6 +5,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "olc_internal.h"
 
@@ -183,5 +186,63 @@ inline int dispatch_int(olc_dtype dt, F&& f) {
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once
+// per (kernel, device): the attribute belongs to the device's context, so a
+// process that launches on several devices sets it on each of them.
+inline cudaError_t set_smem_limit(const void* kernel, int bytes) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, uint64_t>> done;   // kernel -> device mask
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < kMaxDevices ? (1ull << dev) : 0ull;
+    std::lock_guard<std::mutex> lock(mu);
+    uint64_t* mask = nullptr;
+    for (auto& d : done)
+        if (d.first == kernel) {
+            mask = &d.second;
+            break;
+        }
+    if (mask && bit && (*mask & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (!mask) {
+        done.emplace_back(kernel, 0ull);
+        mask = &done.back().second;
+    }
+    *mask |= bit;
+    return cudaSuccess;
+}
+
+// Programmatic dependent launch.  A kernel launched with launch_pdl may
+// start while the previous kernel in the stream is still finishing; it calls
+// grid_dependency_wait() before its first access to global memory (the wait
+// returns once that kernel has completed and its writes are visible; without
+// the launch attribute it returns at once) and grid_launch_dependents() to
+// let the next such launch start its own prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace olc

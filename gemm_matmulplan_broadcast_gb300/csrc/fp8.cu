@@ -524,12 +524,7 @@ cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Wo
     q.err = device_error_word();
     q.fmt = dt == OLC_FLOAT8E4M3FN ? 0 : 1;
     q.epi = p.epi;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(f8::tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    f8::SMEM_BYTES);
-    });
+    const cudaError_t attr = set_smem_limit(reinterpret_cast<const void*>(f8::tc_kernel), f8::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     const int64_t grid = min64(q.total_tiles, (int64_t)sm_count);
     f8::tc_kernel<<<(unsigned)grid, f8::THREADS, f8::SMEM_BYTES, s>>>(ma, mb, q);

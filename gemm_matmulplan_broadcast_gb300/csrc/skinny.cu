@@ -451,12 +451,8 @@ static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const size_t smem = sizeof(typename Num<T>::acc_t) * NC * Cfg::KC;
     if (smem > 48 * 1024) {
-        static std::once_flag once;
-        static cudaError_t attr = cudaSuccess;
-        std::call_once(once, [&] {
-            attr = cudaFuncSetAttribute(skinny_n_kernel<T, NC>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        });
+        const cudaError_t attr =
+            set_smem_limit(reinterpret_cast<const void*>(skinny_n_kernel<T, NC>), (int)smem);
         if (attr != cudaSuccess) return attr;
     }
     skinny_n_kernel<T, NC><<<(unsigned)blocks, 256, smem, s>>>(p, groups);
@@ -584,6 +580,8 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
     }
     if (threadIdx.x == 0) sh.abort = 0;
     __syncthreads();   // slot counters initialised before any warp arrives
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     // Each warp stages only the B rows of its own K range, so it never waits
     // for the others.  With N == 8 or 16 every 16-byte vector of B is one
@@ -749,18 +747,12 @@ static cudaError_t launch_skinny_n_mma_t(const Problem& p, int sm_count, cudaStr
     const int kw = (int)sn_k_per_warp(p.K);
     const int64_t rows = sn_rows(p.K);
     const size_t smem = (size_t)NB * rows * 16;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [&] {
-        attr = cudaFuncSetAttribute(skinny_n_mma_kernel<T, NB>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSnMaxBtBytes);
-    });
+    const cudaError_t attr = set_smem_limit(reinterpret_cast<const void*>(skinny_n_mma_kernel<T, NB>),
+                                            (int)kSnMaxBtBytes);
     if (attr != cudaSuccess) return attr;
     const int64_t grid = min64(units, (int64_t)sm_count);
-    skinny_n_mma_kernel<T, NB><<<(unsigned)grid, kSnWarps * 32, smem, s>>>(p, units, kw, rows,
-                                                                            device_error_word());
-    return cudaGetLastError();
+    return launch_pdl(skinny_n_mma_kernel<T, NB>, dim3((unsigned)grid), dim3(kSnWarps * 32), smem, s,
+                      p, units, kw, rows, device_error_word());
 }
 
 static cudaError_t launch_skinny_n_mma(olc_dtype dt, const Problem& p, int sm_count,

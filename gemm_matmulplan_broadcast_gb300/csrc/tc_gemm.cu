@@ -563,6 +563,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // while warp 1 allocates TMEM and hands the address to the epilogue warps
     // through named barrier 2 (warps 1..5)
     __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
     uint32_t tmem_base = 0;
     if (warp == 1) tmem_alloc(&s->tmem_base, C::TMEM_COLS);
     if (warp >= 1) {
@@ -1303,16 +1305,6 @@ __device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* counter) {
     return prev;
 }
 
-// Programmatic dependent launch: wait until the grids this launch depends on
-// have completed and their writes are visible (a no-op without the launch
-// attribute), and let the next launch in the stream start its prologue.
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 template <int CL>
 __global__ void __launch_bounds__(THREADS_T, 1)
 splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -1722,17 +1714,13 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
     }
     if (p.total_tiles <= 0) return cudaSuccess;
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, SPLIT, SWAP>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    });
+    const cudaError_t attr_err =
+        set_smem_limit(reinterpret_cast<const void*>(tc_gemm_kernel<BN, SPLIT, SWAP>), C::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t units = p.total_tiles * p.splits;
     const int64_t grid = p.stream ? sp->grid : min64(units, (int64_t)sm_count);
-    tc_gemm_kernel<BN, SPLIT, SWAP><<<(unsigned)grid, THREADS, C::SMEM_BYTES, s>>>(ma, mb, p);
-    return cudaGetLastError();
+    return launch_pdl(tc_gemm_kernel<BN, SPLIT, SWAP>, dim3((unsigned)grid), dim3(THREADS),
+                      (size_t)C::SMEM_BYTES, s, ma, mb, p);
 }
 
 static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
@@ -1773,12 +1761,8 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     p.epi = pr.epi;
     const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.items;
     if (pairs <= 0) return cudaSuccess;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(pair::tc_pair_kernel<false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
-    });
+    const cudaError_t attr_err =
+        set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<false>), pair::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
     cudaLaunchConfig_t cfg;
@@ -1843,12 +1827,8 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
     p.epi = pr.epi;
     const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256);
     if (pairs <= 0) return cudaSuccess;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(pair::tc_pair_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
-    });
+    const cudaError_t attr_err =
+        set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<true>), pair::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
     cudaLaunchConfig_t cfg;
@@ -1871,13 +1851,7 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
 // CTA per SM (as many clusters as fit at once), slices of at least 2 chunks.
 template <int CL>
 static cudaError_t tiny_attr() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tiny::splitk_tiny_kernel<CL>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, tiny::SMEM_BYTES);
-    });
-    return err;
+    return set_smem_limit(reinterpret_cast<const void*>(tiny::splitk_tiny_kernel<CL>), tiny::SMEM_BYTES);
 }
 
 // Clusters of CL that the device runs at once (an estimate from the SM count
