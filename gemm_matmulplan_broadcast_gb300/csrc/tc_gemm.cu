@@ -1030,6 +1030,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     cluster_sync();          // both CTAs' barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = s->tmem_base;
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     auto coords = [&](int64_t t, int64_t& item, int64_t& mb, int64_t& nb) {
         item = t / per_item;
@@ -1771,13 +1773,15 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel<false>, ma, mb, p);
 }
 
@@ -1837,13 +1841,15 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, pair::tc_pair_kernel<true>, ma, mb, p);
 }
 
