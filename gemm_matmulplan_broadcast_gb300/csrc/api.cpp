@@ -284,6 +284,12 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
         p->counter_count = skinny_n_counter_count(dt, pr, p->sm_count);
     } else if (p->algo == OLC_ALGO_GENERAL_TC && is_fp8(dt)) {
         p->partial_bytes = fp8_tc_workspace_bytes(pr);    // B transposed, [N, K] bytes
+    } else if (p->algo == OLC_ALGO_GENERAL_SIMT) {
+        p->splits = general_simt_pick_split(dt, pr, p->sm_count);
+        if (p->splits > 1) {
+            p->partial_bytes = general_simt_partial_bytes(dt, pr, p->splits);
+            p->counter_count = general_simt_counter_count(dt, pr, p->splits);
+        }
     } else if (p->algo == OLC_ALGO_SKINNY_M) {
         p->splits = skinny_m_pick_split(dt, pr, p->sm_count);
         if (p->splits > 1) {
@@ -371,7 +377,11 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     }
     switch (algo) {
         case OLC_ALGO_DIRECT: e = launch_direct(dt, pr, s); break;
-        case OLC_ALGO_GENERAL_SIMT: e = launch_general_simt(dt, pr, s); break;
+        case OLC_ALGO_GENERAL_SIMT: {
+            const Workspace ws = workspace_of(p);
+            e = launch_general_simt(dt, pr, s, p->splits, &ws);
+            break;
+        }
         case OLC_ALGO_SKINNY_M:
             e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
             break;
@@ -737,6 +747,7 @@ namespace {
 int host_chunks(const olc_matmul_plan* p) {
     if (p->items != 1 || p->K == 0 || p->residual || is_fp8(p->dtype)) return 0;
     if (p->algo != OLC_ALGO_GENERAL_TC && p->algo != OLC_ALGO_GENERAL_SIMT) return 0;
+    if (p->splits > 1) return 0;          // K-sliced plans use the workspace per launch
     if (p->is_gemm && (p->trans_a || (p->c_rank >= 0 && p->c_rs != 0))) return 0;
     const int64_t rows = p->rows;
     if (rows < 4 * 1024) return 0;

@@ -80,8 +80,14 @@ cudaError_t launch_epilogue_fill(olc_dtype dt, const Problem& p, cudaStream_t st
 cudaError_t launch_direct(olc_dtype dt, const Problem& p, cudaStream_t stream);
 
 // GENERAL_SIMT: FP32 FFMA / FP64 DFMA register-tiled kernel (any dtype works;
-// the plan routes FLOAT and DOUBLE here).
-cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t stream);
+// the plan routes FLOAT and DOUBLE here).  FLOAT products with fewer tiles
+// than SMs take `splits` > 1 K slices per tile (partial tiles in the
+// workspace, summed in slice order by the last slice to finish).
+cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t stream, int splits = 1,
+                                const Workspace* ws = nullptr);
+int general_simt_pick_split(olc_dtype dt, const Problem& p, int sm_count);
+size_t general_simt_partial_bytes(olc_dtype dt, const Problem& p, int splits);
+size_t general_simt_counter_count(olc_dtype dt, const Problem& p, int splits);
 bool general_simt_vectorizable(olc_dtype dt, int64_t N, int64_t K);
 
 // SKINNY_M: M <= 16.  `ksplit` slices of K, reduced in fixed order.

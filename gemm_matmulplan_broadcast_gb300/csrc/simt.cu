@@ -251,7 +251,8 @@ constexpr int SIMT_GROUP_M = 16;
 
 template <typename T, int BM, int BN, int BK, int TM, int TN, bool AT, bool BT>
 __global__ void __launch_bounds__(256, 2)
-simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
+simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n, int splits, int64_t k_slice,
+                 T* __restrict__ part, unsigned int* __restrict__ cnt) {
     using V = typename Vec<T>::type;
     constexpr int W = Vec<T>::W;
     constexpr int PAD = W;
@@ -265,9 +266,14 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     __shared__ __align__(16) T As[2][BK][BM + PAD];
     __shared__ __align__(16) T Bs[2][BK][BN];
 
+    // K slice (splits > 1: slice s covers [s * k_slice, (s + 1) * k_slice),
+    // k_slice a multiple of BK) and tile of this block
     const int64_t per_item = tiles_m * tiles_n;
-    const int64_t item = blockIdx.x / per_item;
-    const int64_t rem = blockIdx.x % per_item;
+    const int64_t all_tiles = per_item * p.items;
+    const int slice = (int)(blockIdx.x / all_tiles);
+    const int64_t tile_id = blockIdx.x % all_tiles;
+    const int64_t item = tile_id / per_item;
+    const int64_t rem = tile_id % per_item;
     // tile raster in groups of SIMT_GROUP_M row blocks, column-major inside a
     // group: the blocks resident at one time share a few A row strips and B
     // column strips, so L2 serves most re-reads instead of DRAM
@@ -283,6 +289,8 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
     T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
     const int64_t M = p.M, N = p.N, K = p.K;
+    const int64_t k_begin = splits > 1 ? (int64_t)slice * k_slice : 0;
+    const int64_t k_end = splits > 1 ? min64(K, k_begin + k_slice) : K;
 
     const int t = threadIdx.x;
     const int tx = t % 16, ty = t / 16;
@@ -364,13 +372,13 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     }
 
     V va[AV], vb[BV];
-    load_a(0, va);
-    load_b(0, vb);
+    load_a(k_begin, va);
+    load_b(k_begin, vb);
     store_stage(0, va, vb);
     __syncthreads();
     int buf = 0;
-    for (int64_t k0 = 0; k0 < K; k0 += BK) {
-        const bool more = k0 + BK < K;
+    for (int64_t k0 = k_begin; k0 < k_end; k0 += BK) {
+        const bool more = k0 + BK < k_end;
         if (more) {
             load_a(k0 + BK, va);
             load_b(k0 + BK, vb);
@@ -430,6 +438,51 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
             }
     }
 
+    if (splits > 1) {
+        // this slice's partial tile, in the thread's own register order
+        constexpr int F = TM * TN;
+        T* mine = part + ((int64_t)tile_id * splits + slice) * (256 * F) + (int64_t)t * F;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; j += W) {
+                V v;
+                T* e = reinterpret_cast<T*>(&v);
+#pragma unroll
+                for (int q = 0; q < W; ++q) e[q] = acc[i][j + q];
+                *reinterpret_cast<V*>(mine + i * TN + j) = v;
+            }
+        __threadfence();
+        __syncthreads();
+        __shared__ int last;
+        if (t == 0) {
+            const unsigned int prev = atomicAdd(cnt + tile_id, 1u);
+            last = prev == (unsigned int)splits - 1 ? 1 : 0;
+        }
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+        // the last slice to finish sums the slices in slice order
+        const T* first = part + (int64_t)tile_id * splits * (256 * F) + (int64_t)t * F;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = T(0);
+        for (int s2 = 0; s2 < splits; ++s2) {
+            const T* src = first + (int64_t)s2 * (256 * F);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; j += W) {
+                    const V v = __ldcg(reinterpret_cast<const V*>(src + i * TN + j));
+                    const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+                    for (int q = 0; q < W; ++q) acc[i][j + q] += e[q];
+                }
+        }
+        if (t == 0) cnt[tile_id] = 0u;
+    }
+
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int64_t gm = m0 + (i / HM) * (BM / 2) + ty * HM + (i % HM);
@@ -453,21 +506,50 @@ simt_fast_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
     }
 }
 
+// K slice length for `splits` slices: a multiple of BK, so that slice
+// boundaries fall on the kernel's BK-deep steps
+static int64_t simt_k_slice(int64_t K, int splits, int bk) {
+    return ceil_div(ceil_div(K, (int64_t)splits), (int64_t)bk) * bk;
+}
+
 template <typename T, int BM, int BN, int BK, int TM, int TN>
-static cudaError_t launch_fast(const Problem& p, cudaStream_t stream) {
+static cudaError_t launch_fast(const Problem& p, cudaStream_t stream, int splits, const Workspace* ws) {
     const int64_t tm = ceil_div(p.M, BM), tn = ceil_div(p.N, BN);
-    const int64_t blocks = tm * tn * p.items;
-    if (blocks <= 0) return cudaSuccess;
+    const int64_t tiles = tm * tn * p.items;
+    if (tiles <= 0) return cudaSuccess;
+    int64_t k_slice = p.K;
+    T* part = nullptr;
+    unsigned int* cnt = nullptr;
+    if (splits > 1) {
+        k_slice = simt_k_slice(p.K, splits, BK);
+        splits = (int)ceil_div(p.K, k_slice);          // non-empty slices
+    }
+    if (splits > 1) {
+        const size_t need = (size_t)tiles * splits * BM * BN * sizeof(T);
+        if (!ws || !ws->partials || ws->partial_bytes < need || !ws->counters ||
+            ws->counter_count < (size_t)tiles)
+            return cudaErrorInvalidValue;
+        part = static_cast<T*>(ws->partials);
+        cnt = ws->counters;
+    } else {
+        splits = 1;
+        k_slice = p.K;
+    }
+    const int64_t blocks = tiles * splits;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const unsigned g = (unsigned)blocks;
     if (!p.a_trans && !p.b_trans)
-        simt_fast_kernel<T, BM, BN, BK, TM, TN, false, false><<<g, 256, 0, stream>>>(p, tm, tn);
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, false, false>
+            <<<g, 256, 0, stream>>>(p, tm, tn, splits, k_slice, part, cnt);
     else if (p.a_trans && !p.b_trans)
-        simt_fast_kernel<T, BM, BN, BK, TM, TN, true, false><<<g, 256, 0, stream>>>(p, tm, tn);
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, true, false>
+            <<<g, 256, 0, stream>>>(p, tm, tn, splits, k_slice, part, cnt);
     else if (!p.a_trans && p.b_trans)
-        simt_fast_kernel<T, BM, BN, BK, TM, TN, false, true><<<g, 256, 0, stream>>>(p, tm, tn);
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, false, true>
+            <<<g, 256, 0, stream>>>(p, tm, tn, splits, k_slice, part, cnt);
     else
-        simt_fast_kernel<T, BM, BN, BK, TM, TN, true, true><<<g, 256, 0, stream>>>(p, tm, tn);
+        simt_fast_kernel<T, BM, BN, BK, TM, TN, true, true>
+            <<<g, 256, 0, stream>>>(p, tm, tn, splits, k_slice, part, cnt);
     return cudaGetLastError();
 }
 
@@ -491,11 +573,37 @@ static bool aligned_items(const Problem& p, int64_t elem) {
     return ((p.M * p.N) * elem) % 16 == 0;
 }
 
-cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream) {
+cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream, int splits,
+                                     const Workspace* ws) {
     if (!fast_shape_ok(dt, p)) return launch_general_simt_generic(dt, p, stream);
-    if (dt == OLC_FLOAT && aligned_items(p, 4)) return launch_fast<float, 128, 128, 16, 8, 8>(p, stream);
-    if (dt == OLC_DOUBLE && aligned_items(p, 8)) return launch_fast<double, 64, 64, 8, 4, 4>(p, stream);
+    if (dt == OLC_FLOAT && aligned_items(p, 4))
+        return launch_fast<float, 128, 128, 16, 8, 8>(p, stream, splits, ws);
+    if (dt == OLC_DOUBLE && aligned_items(p, 8))
+        return launch_fast<double, 64, 64, 8, 4, 4>(p, stream, 1, nullptr);
     return launch_general_simt_generic(dt, p, stream);
+}
+
+// FLOAT products whose 128 x 128 tiles leave SMs idle: enough K slices to
+// give each SM about two blocks, slices of at least 128 (8 steps of 16)
+int general_simt_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
+    if (dt != OLC_FLOAT || !fast_shape_ok(dt, p) || p.split_hint == 1) return 1;
+    const int64_t tiles = ceil_div(p.M, 128) * ceil_div(p.N, 128) * p.items;
+    if (tiles <= 0 || p.K <= 0) return 1;
+    int64_t s = p.split_hint > 1 ? p.split_hint : (tiles >= sm_count ? 1 : (2 * sm_count) / tiles);
+    s = min64(s, max64(1, p.K / 128));
+    s = min64(s, 16);
+    if (s < 2) return 1;
+    return (int)ceil_div(p.K, simt_k_slice(p.K, (int)s, 16));   // non-empty slices
+}
+
+size_t general_simt_partial_bytes(olc_dtype dt, const Problem& p, int splits) {
+    if (splits < 2 || dt != OLC_FLOAT) return 0;
+    return (size_t)(ceil_div(p.M, 128) * ceil_div(p.N, 128) * p.items) * splits * 128 * 128 * 4;
+}
+
+size_t general_simt_counter_count(olc_dtype dt, const Problem& p, int splits) {
+    if (splits < 2 || dt != OLC_FLOAT) return 0;
+    return (size_t)(ceil_div(p.M, 128) * ceil_div(p.N, 128) * p.items);
 }
 
 }  // namespace olc

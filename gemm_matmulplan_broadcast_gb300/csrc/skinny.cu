@@ -17,15 +17,17 @@
 namespace olc {
 
 cudaError_t launch_general_simt_generic(olc_dtype dt, const Problem& p, cudaStream_t stream);
-cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream);
+cudaError_t launch_general_simt_fast(olc_dtype dt, const Problem& p, cudaStream_t stream, int splits,
+                                     const Workspace* ws);
 bool general_simt_fast_ok(olc_dtype dt, int64_t N, int64_t K);
 
 bool general_simt_vectorizable(olc_dtype dt, int64_t N, int64_t K) {
     return general_simt_fast_ok(dt, N, K);
 }
 
-cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t stream) {
-    if (general_simt_fast_ok(dt, p.N, p.K)) return launch_general_simt_fast(dt, p, stream);
+cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t stream, int splits,
+                                const Workspace* ws) {
+    if (general_simt_fast_ok(dt, p.N, p.K)) return launch_general_simt_fast(dt, p, stream, splits, ws);
     return launch_general_simt_generic(dt, p, stream);
 }
 

@@ -380,9 +380,10 @@ int olc_matmul_plan_algorithm(const olc_matmul_plan* plan);
  * only themselves or AUTO. */
 olc_status olc_matmul_plan_force_algorithm(olc_matmul_plan* plan, int algo);
 
-/* Tuning override of the number of K slices of SPLIT_K and SKINNY_M plans
- * (0 = automatic choice from the SM count; values are clamped to what the
- * shape allows).  Re-sizes the workspace.  Errors: OLC_ERR_NULL,
+/* Tuning override of the number of K slices of SPLIT_K and SKINNY_M plans,
+ * and of FLOAT GENERAL_SIMT plans (which slice K when their 128 x 128 tiles
+ * are fewer than the SMs; 1 = never) (0 = automatic choice from the SM count;
+ * values are clamped to what the shape allows).  Re-sizes the workspace.  Errors: OLC_ERR_NULL,
  * OLC_ERR_INVALID (negative or above 4096), OLC_ERR_OOM, OLC_ERR_CUDA. */
 olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits);
 

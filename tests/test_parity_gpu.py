@@ -293,6 +293,49 @@ def test_tiny_split_k_slice_counts(splits):
         compare(Y.cpu(), y_ref, sabs, "float16", exact=exact)
 
 
+@pytest.mark.parametrize("splits", [0, 1, 2, 3, 7, 16])
+def test_fp32_simt_k_slices(splits):
+    """FLOAT products with fewer 128 x 128 tiles than SMs run K slices whose
+    partial tiles the last slice sums in slice order: integer inputs bit for
+    bit, normal inputs within the bound, two runs identical; 0 is the
+    automatic choice, 1 no slicing."""
+    shapes = ((2, 200, 2048), (2048, 392))
+    for dist, exact in [(synth.SMALL_INT, True), (synth.UNIFORM, False)]:
+        a, b = synth.operands(shapes[0], shapes[1], "float32", dist, dist, seed=14)
+        A, B = a.cuda(), b.cuda()
+        with Plan(a.shape, b.shape, "float32") as p:
+            p.force("general_simt")
+            p.set_splits(splits)
+            if splits == 1:
+                assert p.splits == 1
+            elif splits > 1:
+                assert p.splits > 1
+            Y = torch.empty(p.output_shape, dtype=A.dtype, device="cuda")
+            Y2 = torch.empty_like(Y)
+            p.execute_checked(A, B, Y)
+            p.execute_checked(A, B, Y2)
+            torch.cuda.synchronize()
+            assert torch.equal(Y, Y2)
+        y_ref, sabs = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "float32")
+        compare(Y.cpu(), y_ref, sabs, "float32", exact=exact)
+
+
+def test_fp32_square_1024_sampled():
+    """The 1024-cube FLOAT product (64 tiles: sliced over K automatically)
+    on sampled rows."""
+    a, b = synth.operands((1024, 1024), (1024, 1024), "float32", synth.UNIFORM, synth.UNIFORM, seed=4)
+    with Plan(a.shape, b.shape, "float32") as p:
+        assert p.algorithm == "general_simt"
+        assert p.splits > 1
+        A, B = a.cuda(), b.cuda()
+        Y = torch.empty(1024, 1024, device="cuda")
+        p.execute_checked(A, B, Y)
+    rows = sample_rows(1024, extra=64)
+    y_ref, sabs = oracle.gemm2d(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "float32",
+                                rows=rows)
+    compare(Y.cpu()[rows], y_ref, sabs, "float32")
+
+
 TC_SKINNY_N_SHAPES = [
     ((4096, 1024), (1024, 8)),         # 32 row tiles: stream-K shares over the SMs
     ((16384, 4096), (4096, 8)),        # the FP16 corner's skinny-N product
