@@ -29,16 +29,19 @@ TORCH_DTYPES = {
     "bfloat16": torch.bfloat16,
     "float8_e4m3fn": torch.float8_e4m3fn,
     "float8_e5m2": torch.float8_e5m2,
+    "float8_e4m3fnuz": torch.float8_e4m3fnuz,
+    "float8_e5m2fnuz": torch.float8_e5m2fnuz,
 }
 
 # ONNX TensorProto element type codes, as used by the C ABI.
 ONNX_CODES = {"float32": 1, "float16": 10, "float64": 11, "bfloat16": 16,
-              "float8_e4m3fn": 17, "float8_e5m2": 19}
+              "float8_e4m3fn": 17, "float8_e4m3fnuz": 18, "float8_e5m2": 19,
+              "float8_e5m2fnuz": 20}
 
 ELEMENT_BYTES = {"float32": 4, "float64": 8, "float16": 2, "bfloat16": 2,
-                 "float8_e4m3fn": 1, "float8_e5m2": 1}
+                 "float8_e4m3fn": 1, "float8_e5m2": 1, "float8_e4m3fnuz": 1, "float8_e5m2fnuz": 1}
 
-FP8_DTYPES = ("float8_e4m3fn", "float8_e5m2")
+FP8_DTYPES = ("float8_e4m3fn", "float8_e5m2", "float8_e4m3fnuz", "float8_e5m2fnuz")
 
 
 def output_dtype(dtype: str) -> str:
@@ -113,7 +116,8 @@ def to_numpy_storage(t: torch.Tensor):
     t = t.detach().cpu().contiguous()
     if t.dtype in (torch.float16, torch.bfloat16):
         return t.view(torch.int16).numpy().view("uint16")
-    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2, torch.float8_e4m3fnuz,
+                   torch.float8_e5m2fnuz):
         return t.view(torch.uint8).numpy()
     return t.numpy()
 

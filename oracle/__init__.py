@@ -53,7 +53,7 @@ _lock = threading.Lock()
 _lib = None
 
 DTYPES = ("float32", "float64", "float16", "bfloat16")
-FP8_DTYPES = ("float8_e4m3fn", "float8_e5m2")
+FP8_DTYPES = ("float8_e4m3fn", "float8_e5m2", "float8_e4m3fnuz", "float8_e5m2fnuz")
 
 
 def build(force: bool = False) -> str:
@@ -130,10 +130,13 @@ def encode(values: np.ndarray, dtype: str) -> np.ndarray:
 # each one-byte pattern of a Float8 format is decoded exactly to float32 and
 # the float32 algorithm runs with float32 accumulation.  The two formats
 # built here are E4M3FN (1 sign, 4 exponent bits with bias 7, 3 mantissa
-# bits; no infinities; S.1111.111 is NaN) and E5M2 (1 sign, 5 exponent bits
-# with bias 15, 2 mantissa bits; IEEE-style infinities and NaNs).  Reading
-# where the page is silent: the output is FLOAT (the float32 sums are not
-# narrowed), and both operands have the same format.
+# bits; no infinities; S.1111.111 is NaN), E5M2 (1 sign, 5 exponent bits
+# with bias 15, 2 mantissa bits; IEEE-style infinities and NaNs), and the two
+# "FNUZ" variants the roadmap lists beside them: E4M3FNUZ and E5M2FNUZ have
+# the same fields with the exponent bias one larger (8 and 16), no
+# infinities, no negative zero, and the one pattern 1.0000.000 (0x80) as NaN.
+# Reading where the page is silent: the output is FLOAT (the float32 sums are
+# not narrowed), and both operands have the same format.
 
 
 def decode_fp8(bits: np.ndarray, dtype: str) -> np.ndarray:
@@ -149,6 +152,16 @@ def decode_fp8(bits: np.ndarray, dtype: str) -> np.ndarray:
         e, m = (b >> 2) & 0x1F, b & 0x3
         mag = np.where(e == 0, m * 2.0 ** -16, (1.0 + m / 4.0) * np.exp2(e - 15.0))
         mag = np.where(e == 31, np.where(m == 0, np.inf, np.nan), mag)
+    elif dtype == "float8_e4m3fnuz":
+        e, m = (b >> 3) & 0xF, b & 0x7
+        mag = np.where(e == 0, m * 2.0 ** -10, (1.0 + m / 8.0) * np.exp2(e - 8.0))
+        mag = np.where(b == 0x80, np.nan, mag)
+        sign = np.where(b == 0x80, 1.0, sign)
+    elif dtype == "float8_e5m2fnuz":
+        e, m = (b >> 2) & 0x1F, b & 0x3
+        mag = np.where(e == 0, m * 2.0 ** -17, (1.0 + m / 4.0) * np.exp2(e - 16.0))
+        mag = np.where(b == 0x80, np.nan, mag)
+        sign = np.where(b == 0x80, 1.0, sign)
     else:
         raise ValueError("not an 8-bit float type: %r" % dtype)
     return (sign * mag).astype(np.float32)

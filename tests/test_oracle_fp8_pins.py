@@ -33,6 +33,21 @@ def test_decode_known_values():
     assert np.isinf(e5[3]) and np.isnan(e5[4])
 
 
+def test_decode_known_values_fnuz():
+    # exponent bias one larger than the FN formats, no infinities, no -0, 0x80 the only NaN
+    e4 = oracle.decode_fp8(np.array([0x7F, 0x01, 0x40, 0xC0, 0x80, 0x00], np.uint8), "float8_e4m3fnuz")
+    assert e4[0] == 240.0 and e4[1] == 2.0 ** -10 and e4[2] == 1.0 and e4[3] == -1.0
+    assert np.isnan(e4[4]) and e4[5] == 0.0 and not np.signbit(e4[5])
+    assert np.isnan(e4).sum() == 1
+    e5 = oracle.decode_fp8(np.array([0x7F, 0x01, 0x40, 0x7C, 0x80, 0xFF], np.uint8), "float8_e5m2fnuz")
+    assert e5[0] == 57344.0 and e5[1] == 2.0 ** -17 and e5[2] == 1.0 and e5[3] == 32768.0
+    assert np.isnan(e5[4]) and e5[5] == -57344.0
+    full4 = oracle.decode_fp8(np.arange(256, dtype=np.uint8), "float8_e4m3fnuz")
+    full5 = oracle.decode_fp8(np.arange(256, dtype=np.uint8), "float8_e5m2fnuz")
+    assert np.isnan(full4).sum() == 1 and np.isnan(full5).sum() == 1
+    assert not np.isinf(full4).any() and not np.isinf(full5).any()
+
+
 @pytest.mark.parametrize("dtype", oracle.FP8_DTYPES)
 def test_fp8_matmul_integer_exact(dtype):
     a, b = synth.operands((2, 5, 40), (40, 7), dtype, synth.SMALL_INT, synth.SMALL_INT, 3)
