@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(PKG, "libolc_matmul.so")
 HEADER = os.path.join(ROOT, "include", "olc_matmul.h")
 
 DTYPE_CODES = {"float32": 1, "float16": 10, "float64": 11, "bfloat16": 16,
-               "float8_e4m3fn": 17, "float8_e5m2": 19}
+               "float8_e4m3fn": 17, "float8_e4m3fnuz": 18, "float8_e5m2": 19,
+               "float8_e5m2fnuz": 20}
 ALGORITHMS = {
     "auto": -1, "empty": 0, "zero_fill": 1, "direct": 2, "skinny_m": 3, "skinny_n": 4,
     "split_k": 5, "general_tc": 6, "general_simt": 7,

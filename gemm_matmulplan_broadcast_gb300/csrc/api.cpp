@@ -85,18 +85,26 @@ int64_t elem_bytes(olc_dtype dt) {
         case OLC_FLOAT16:
         case OLC_BFLOAT16: return 2;
         case OLC_FLOAT8E4M3FN:
-        case OLC_FLOAT8E5M2: return 1;
+        case OLC_FLOAT8E4M3FNUZ:
+        case OLC_FLOAT8E5M2:
+        case OLC_FLOAT8E5M2FNUZ: return 1;
     }
     return 0;
 }
 
 bool valid_dtype(int dt) {
     return dt == OLC_FLOAT || dt == OLC_DOUBLE || dt == OLC_FLOAT16 || dt == OLC_BFLOAT16 ||
-           dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2;
+           dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2 || dt == OLC_FLOAT8E4M3FNUZ ||
+           dt == OLC_FLOAT8E5M2FNUZ;
 }
 
 bool is_half(olc_dtype dt) { return dt == OLC_FLOAT16 || dt == OLC_BFLOAT16; }
-bool is_fp8(olc_dtype dt) { return dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2; }
+bool is_fp8(olc_dtype dt) {
+    return dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2 || dt == OLC_FLOAT8E4M3FNUZ ||
+           dt == OLC_FLOAT8E5M2FNUZ;
+}
+// the 8-bit formats the tensor cores take (kind::f8f6f4 E4M3 / E5M2)
+bool is_fp8_tc_format(olc_dtype dt) { return dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2; }
 
 // bytes of one output element: FLOAT for the 8-bit float operand types
 int64_t out_bytes(olc_dtype dt) { return is_fp8(dt) ? 4 : elem_bytes(dt); }
@@ -202,7 +210,7 @@ bool feasible(const olc_matmul_plan* p, int algo) {
             case OLC_ALGO_GENERAL_SIMT: return n > 0 && K > 0;
             case OLC_ALGO_GENERAL_TC: {
                 Problem pr = make_problem(p, nullptr, nullptr, nullptr);
-                return n > 0 && K > 0 && fp8_tc_ok(pr);
+                return n > 0 && K > 0 && is_fp8_tc_format(p->dtype) && fp8_tc_ok(pr);
             }
         }
         return false;

@@ -132,6 +132,23 @@ __device__ __forceinline__ float fp8_e5m2_to_f32(uint32_t b) {
     return __uint_as_float(__float_as_uint(mag) | sign);
 }
 
+// FNUZ variants: exponent bias one larger (8 / 16), no infinities, no
+// negative zero, 0x80 the only NaN
+__device__ __forceinline__ float fp8_e4m3fnuz_to_f32(uint32_t b) {
+    if (b == 0x80u) return __uint_as_float(0x7FC00000u);
+    const uint32_t sign = (b & 0x80u) << 24;
+    const uint32_t e = (b >> 3) & 0xFu, m = b & 0x7u;
+    const float mag = e == 0 ? (float)m * 0x1p-10f : __uint_as_float(((e + 119u) << 23) | (m << 20));
+    return __uint_as_float(__float_as_uint(mag) | sign);
+}
+__device__ __forceinline__ float fp8_e5m2fnuz_to_f32(uint32_t b) {
+    if (b == 0x80u) return __uint_as_float(0x7FC00000u);
+    const uint32_t sign = (b & 0x80u) << 24;
+    const uint32_t e = (b >> 2) & 0x1Fu, m = b & 0x3u;
+    const float mag = e == 0 ? (float)m * 0x1p-17f : __uint_as_float(((e + 111u) << 23) | (m << 21));
+    return __uint_as_float(__float_as_uint(mag) | sign);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

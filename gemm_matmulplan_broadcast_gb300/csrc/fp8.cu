@@ -34,9 +34,13 @@ namespace f8 {
 // ---------------------------------------------------------------------------
 // decode
 
+// FMT: 0 E4M3FN, 1 E5M2, 2 E4M3FNUZ, 3 E5M2FNUZ
 template <int FMT>
 __device__ __forceinline__ float decode(uint32_t b) {
-    return FMT == 0 ? fp8_e4m3_to_f32(b) : fp8_e5m2_to_f32(b);
+    if constexpr (FMT == 0) return fp8_e4m3_to_f32(b);
+    else if constexpr (FMT == 1) return fp8_e5m2_to_f32(b);
+    else if constexpr (FMT == 2) return fp8_e4m3fnuz_to_f32(b);
+    else return fp8_e5m2fnuz_to_f32(b);
 }
 
 // ---------------------------------------------------------------------------
@@ -470,8 +474,13 @@ cudaError_t launch_fp8_simt(olc_dtype dt, const Problem& p, cudaStream_t s) {
     const int64_t blocks = tm * tn * p.items;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (dt == OLC_FLOAT8E4M3FN) f8::simt_kernel<0><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn);
-    else f8::simt_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn);
+    switch (dt) {
+        case OLC_FLOAT8E4M3FN: f8::simt_kernel<0><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn); break;
+        case OLC_FLOAT8E5M2: f8::simt_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn); break;
+        case OLC_FLOAT8E4M3FNUZ: f8::simt_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn); break;
+        case OLC_FLOAT8E5M2FNUZ: f8::simt_kernel<3><<<(unsigned)blocks, 256, 0, s>>>(p, tm, tn); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
@@ -494,7 +503,8 @@ cudaError_t launch_fp8_transpose(const Problem& p, void* bt, cudaStream_t s) {
 
 cudaError_t launch_fp8_tc(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
                           cudaStream_t s, const void* bt_ready) {
-    if (!fp8_tc_ok(p)) return cudaErrorInvalidValue;
+    // the tensor cores take E4M3 and E5M2 (not the FNUZ encodings)
+    if (!fp8_tc_ok(p) || (dt != OLC_FLOAT8E4M3FN && dt != OLC_FLOAT8E5M2)) return cudaErrorInvalidValue;
     const unsigned char* bt = static_cast<const unsigned char*>(bt_ready);
     if (!bt) {
         if (!ws.partials || ws.partial_bytes < fp8_tc_workspace_bytes(p)) return cudaErrorInvalidValue;

@@ -42,14 +42,19 @@ extern "C" {
  * Roadmap", the Float8 packing-format item) decode exactly to float32,
  * accumulate in float32, and give a FLOAT output (4 bytes per element): A
  * and B have the 8-bit type, Y (and a fused residual) is float32.  They are
- * MatMul types only (Gemm plans reject them). */
+ * MatMul types only (Gemm plans reject them).  E4M3FN and E5M2 run on the
+ * tensor cores (tcgen05 kind::f8f6f4) where the shape allows; the FNUZ
+ * variants, whose encodings the tensor cores do not take, always run on the
+ * SIMT decode kernel. */
 typedef enum {
     OLC_FLOAT = 1,
     OLC_FLOAT16 = 10,
     OLC_DOUBLE = 11,
     OLC_BFLOAT16 = 16,
     OLC_FLOAT8E4M3FN = 17,   /* 1-4-3, bias 7, no infinities, S.1111.111 NaN */
-    OLC_FLOAT8E5M2 = 19      /* 1-5-2, bias 15, IEEE-style infinities / NaNs */
+    OLC_FLOAT8E4M3FNUZ = 18, /* 1-4-3, bias 8, no infinities, no -0, 0x80 NaN */
+    OLC_FLOAT8E5M2 = 19,     /* 1-5-2, bias 15, IEEE-style infinities / NaNs */
+    OLC_FLOAT8E5M2FNUZ = 20  /* 1-5-2, bias 16, no infinities, no -0, 0x80 NaN */
 } olc_dtype;
 
 typedef enum {

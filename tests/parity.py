@@ -16,7 +16,8 @@ from gemm_matmulplan_broadcast_gb300 import synth
 
 TOL = {"float32": 1e-5, "float64": 1e-12, "float16": 2e-3, "bfloat16": 1e-2,
        # 8-bit float operands: exact products, float32 sums, float32 output
-       "float8_e4m3fn": 1e-5, "float8_e5m2": 1e-5}
+       "float8_e4m3fn": 1e-5, "float8_e5m2": 1e-5, "float8_e4m3fnuz": 1e-5,
+       "float8_e5m2fnuz": 1e-5}
 
 
 def gpu_matmul(a_cpu: torch.Tensor, b_cpu: torch.Tensor, dtype: str, algorithm=None,

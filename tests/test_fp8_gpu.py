@@ -63,7 +63,10 @@ SIMT_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", FP8)
+FNUZ = ["float8_e4m3fnuz", "float8_e5m2fnuz"]
+
+
+@pytest.mark.parametrize("dtype", FP8 + FNUZ)
 @pytest.mark.parametrize("shapes", SIMT_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
 def test_fp8_simt(dtype, shapes):
     a_shape, b_shape = shapes
@@ -138,3 +141,34 @@ def test_fp8_constant_b_prepacked(dtype, shapes):
         assert torch.equal(Y1, Y2)
     ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
     compare(Y2.cpu(), ref, s, dtype)
+
+
+@pytest.mark.parametrize("dtype", FNUZ)
+def test_fnuz_runs_on_the_decode_kernel(dtype):
+    """The FNUZ encodings are not tensor-core formats: the plan takes the SIMT
+    decode kernel, forcing the tensor cores is rejected; a large product and
+    the special patterns (0x80 is NaN, 0x7F and 0xFF the largest finite
+    values) against the oracle."""
+    a, b = synth.operands((512, 1024), (1024, 768), dtype, synth.normal(1.0), synth.normal(0.5), 47)
+    with Plan(a.shape, b.shape, dtype) as p:
+        assert p.algorithm == "general_simt"
+        with pytest.raises(OlcError):
+            p.force("general_tc")
+    check_product(a, b, dtype)
+    a8 = np.full((4, 16), 0x00, np.uint8)
+    b8 = np.full((16, 8), 0x00, np.uint8)
+    a8[0, 0] = 0x80            # NaN: row 0 of Y is NaN
+    a8[1, :2] = [0x7F, 0xFF]   # +max, -max
+    b8[:2, :] = 0x40           # 1.0
+    a8[2, 5] = 0x01            # the smallest subnormal
+    b8[5, :] = 0x01
+    ta, tb = synth.from_numpy_storage(a8, dtype), synth.from_numpy_storage(b8, dtype)
+    ref, s = oracle.matmul(a8, b8, dtype)
+    with Plan(ta.shape, tb.shape, dtype) as p:
+        Y = torch.empty(4, 8, device="cuda")
+        p.execute_checked(ta.cuda(), tb.cuda(), Y)
+        torch.cuda.synchronize()
+    y = Y.cpu().numpy()
+    assert np.isnan(y[0]).all() and np.isnan(ref[0]).all()
+    assert np.array_equal(y[1:], ref[1:])
+    assert y[1, 0] == 0.0 and y[2, 0] == ref[2, 0] and ref[2, 0] > 0
