@@ -208,6 +208,8 @@ bool feasible(const olc_matmul_plan* p, int algo) {
             case OLC_ALGO_ZERO_FILL: return n > 0 && K == 0;
             case OLC_ALGO_DIRECT:
             case OLC_ALGO_GENERAL_SIMT: return n > 0 && K > 0;
+            case OLC_ALGO_SKINNY_M:     // 16 one-byte B elements per vector
+                return n > 0 && K > 0 && rows <= skinny_m_max_rows() && N % 16 == 0;
             case OLC_ALGO_GENERAL_TC: {
                 Problem pr = make_problem(p, nullptr, nullptr, nullptr);
                 return n > 0 && K > 0 && is_fp8_tc_format(p->dtype) && fp8_tc_ok(pr);
@@ -244,6 +246,8 @@ int choose_algorithm(const olc_matmul_plan* p) {
     if (p->K == 0) return OLC_ALGO_ZERO_FILL;
     if (is_fp8(p->dtype)) {
         const double macs = (double)p->rows * (double)p->N * (double)p->K * (double)p->items;
+        if (p->rows <= skinny_m_max_rows() && p->N >= 256 && feasible(p, OLC_ALGO_SKINNY_M))
+            return OLC_ALGO_SKINNY_M;
         if (macs >= 4.0 * 1024 * 1024 && feasible(p, OLC_ALGO_GENERAL_TC)) return OLC_ALGO_GENERAL_TC;
         return macs < 4.0 * 1024 * 1024 ? OLC_ALGO_DIRECT : OLC_ALGO_GENERAL_SIMT;
     }
@@ -379,8 +383,11 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     if (is_fp8(dt)) {
         // the plan's constant B comes transposed already
         const void* bt = (p->const_bt && B == p->const_b) ? p->const_bt : nullptr;
-        e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s, bt)
-                                        : launch_fp8_simt(dt, pr, s);
+        if (algo == OLC_ALGO_SKINNY_M)
+            e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
+        else
+            e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s, bt)
+                                            : launch_fp8_simt(dt, pr, s);
         return from_cuda(e);
     }
     switch (algo) {

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
 #include <mutex>
 #include <utility>
@@ -21,24 +22,28 @@ struct Num;
 template <>
 struct Num<float> {
     using acc_t = float;
+    using out_t = float;
     static __device__ __forceinline__ float to_acc(float v) { return v; }
     static __device__ __forceinline__ float from_acc(float v) { return v; }
 };
 template <>
 struct Num<double> {
     using acc_t = double;
+    using out_t = double;
     static __device__ __forceinline__ double to_acc(double v) { return v; }
     static __device__ __forceinline__ double from_acc(double v) { return v; }
 };
 template <>
 struct Num<__half> {
     using acc_t = float;
+    using out_t = __half;
     static __device__ __forceinline__ float to_acc(__half v) { return __half2float(v); }
     static __device__ __forceinline__ __half from_acc(float v) { return __float2half_rn(v); }
 };
 template <>
 struct Num<__nv_bfloat16> {
     using acc_t = float;
+    using out_t = __nv_bfloat16;
     static __device__ __forceinline__ float to_acc(__nv_bfloat16 v) { return __bfloat162float(v); }
     static __device__ __forceinline__ __nv_bfloat16 from_acc(float v) { return __float2bfloat16_rn(v); }
 };
@@ -147,6 +152,66 @@ __device__ __forceinline__ float fp8_e5m2fnuz_to_f32(uint32_t b) {
     const uint32_t e = (b >> 2) & 0x1Fu, m = b & 0x3u;
     const float mag = e == 0 ? (float)m * 0x1p-17f : __uint_as_float(((e + 111u) << 23) | (m << 21));
     return __uint_as_float(__float_as_uint(mag) | sign);
+}
+
+// One 8-bit float operand element of format FMT (0 E4M3FN, 1 E5M2,
+// 2 E4M3FNUZ, 3 E5M2FNUZ): decoded exactly to float32, accumulated in
+// float32, and the output is float32 (no narrowing).
+template <int FMT>
+struct F8 {
+    static constexpr int kFormat = FMT;
+    unsigned char bits;
+};
+template <int FMT>
+__device__ __forceinline__ float fp8_decode(uint32_t b) {
+    if constexpr (FMT == 0) return fp8_e4m3_to_f32(b);
+    else if constexpr (FMT == 1) return fp8_e5m2_to_f32(b);
+    else if constexpr (FMT == 2) return fp8_e4m3fnuz_to_f32(b);
+    else return fp8_e5m2fnuz_to_f32(b);
+}
+template <int FMT>
+struct Num<F8<FMT>> {
+    using acc_t = float;
+    using out_t = float;
+    static __device__ __forceinline__ float to_acc(F8<FMT> v) { return fp8_decode<FMT>(v.bits); }
+    static __device__ __forceinline__ float from_acc(float v) { return v; }
+};
+
+// Sixteen 8-bit float elements (one 16-byte vector, element i in byte i) to
+// float32.  E4M3FN and E5M2 go through the hardware pair conversion to half
+// precision, which holds every value of both formats exactly, then to
+// float32; the FNUZ formats are decoded from their fields.
+template <int FMT>
+__device__ __forceinline__ void fp8_decode16(const uint4& raw, float (&out)[16]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if constexpr (FMT <= 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+                    (__nv_fp8x2_storage_t)((w[q] >> (16 * h)) & 0xFFFFu), FMT == 0 ? __NV_E4M3 : __NV_E5M2);
+                __half_raw lo, hi;
+                lo.x = r.x;
+                hi.x = r.y;
+                out[4 * q + 2 * h] = __half2float(__half(lo));
+                out[4 * q + 2 * h + 1] = __half2float(__half(hi));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) out[4 * q + i] = fp8_decode<FMT>((w[q] >> (8 * i)) & 0xFFu);
+        }
+    }
+}
+
+// one element through the read-only path (8-bit float elements as bytes)
+template <typename T>
+__device__ __forceinline__ T ldg_elem(const T* p) {
+    return __ldg(p);
+}
+template <int FMT>
+__device__ __forceinline__ F8<FMT> ldg_elem(const F8<FMT>* p) {
+    return F8<FMT>{__ldg(reinterpret_cast<const unsigned char*>(p))};
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

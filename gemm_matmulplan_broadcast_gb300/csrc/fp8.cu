@@ -37,10 +37,7 @@ namespace f8 {
 // FMT: 0 E4M3FN, 1 E5M2, 2 E4M3FNUZ, 3 E5M2FNUZ
 template <int FMT>
 __device__ __forceinline__ float decode(uint32_t b) {
-    if constexpr (FMT == 0) return fp8_e4m3_to_f32(b);
-    else if constexpr (FMT == 1) return fp8_e5m2_to_f32(b);
-    else if constexpr (FMT == 2) return fp8_e4m3fnuz_to_f32(b);
-    else return fp8_e5m2fnuz_to_f32(b);
+    return fp8_decode<FMT>(b);
 }
 
 // ---------------------------------------------------------------------------

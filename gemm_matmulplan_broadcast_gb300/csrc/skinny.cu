@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(SkinnyMConfig<MR>::KW * 32)
 skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws,
                 int a_vec_ok) {
     using acc_t = typename Num<T>::acc_t;
+    using out_t = typename Num<T>::out_t;    // float32 for 8-bit float operands
     constexpr int VEC = Vec16<T>::N;
     constexpr int KW = SkinnyMConfig<MR>::KW;
     constexpr int COLS = 32 * VEC;
@@ -82,7 +83,7 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
     batch_offsets(p.map, item, a_off, b_off);
     const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
     const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
-    T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
+    out_t* __restrict__ Y = static_cast<out_t*>(p.Y) + item * p.M * p.N;
     const int64_t M = p.M, N = p.N, K = p.K;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -115,16 +116,24 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
             for (int i = 0; i < MR; ++i) {
                 if (i < M) {
                     if (a_vec_ok) {
-                        uint4 av[AV];
+                        if constexpr (sizeof(T) == 1) {
+                            // 8 one-byte elements: one 8-byte load (k is a multiple of 8)
+                            const uint2 av = __ldg(reinterpret_cast<const uint2*>(A + i * K + k));
+                            const T* ae = reinterpret_cast<const T*>(&av);
 #pragma unroll
-                        for (int q = 0; q < AV; ++q)
-                            av[q] = __ldg(reinterpret_cast<const uint4*>(A + i * K + k) + q);
-                        const T* ae = reinterpret_cast<const T*>(av);
+                            for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ae[u]);
+                        } else {
+                            uint4 av[AV];
 #pragma unroll
-                        for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ae[u]);
+                            for (int q = 0; q < AV; ++q)
+                                av[q] = __ldg(reinterpret_cast<const uint4*>(A + i * K + k) + q);
+                            const T* ae = reinterpret_cast<const T*>(av);
+#pragma unroll
+                            for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ae[u]);
+                        }
                     } else {
 #pragma unroll
-                        for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(__ldg(A + i * K + k + u));
+                        for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ldg_elem(A + i * K + k + u));
                     }
                 } else {
 #pragma unroll
@@ -135,8 +144,12 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
             for (int u = 0; u < KU; ++u) {
                 const T* be = reinterpret_cast<const T*>(&bv[u]);
                 acc_t b[VEC];
+                if constexpr (sizeof(T) == 1) {
+                    fp8_decode16<T::kFormat>(bv[u], b);
+                } else {
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) b[v] = Num<T>::to_acc(be[v]);
+                    for (int v = 0; v < VEC; ++v) b[v] = Num<T>::to_acc(be[v]);
+                }
 #pragma unroll
                 for (int i = 0; i < MR; ++i)
 #pragma unroll
@@ -148,7 +161,7 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
             const T* be = reinterpret_cast<const T*>(&bv);
 #pragma unroll
             for (int i = 0; i < MR; ++i) {
-                const acc_t a = i < M ? Num<T>::to_acc(__ldg(A + i * K + k)) : acc_t(0);
+                const acc_t a = i < M ? Num<T>::to_acc(ldg_elem(A + i * K + k)) : acc_t(0);
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a, Num<T>::to_acc(be[v]), acc[i][v]);
             }
@@ -185,7 +198,8 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
             if (e >= ENTRIES) continue;
             const int i = e / COLS, c = e % COLS;
             const int64_t col = cg * COLS + c;
-            if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(apply_epilogue<T>(p.epi, part[q], i, col, Y + i * N + col));
+            if (i < M && col < N)
+                Y[i * N + col] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, part[q], i, col, Y + i * N + col));
         }
         return;
     }
@@ -214,7 +228,8 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
         for (int t = 1; t < ksplit; ++t) s += __ldcg(all + (int64_t)t * ENTRIES + e);
         const int i = e / COLS, c = e % COLS;
         const int64_t col = cg * COLS + c;
-        if (i < M && col < N) Y[i * N + col] = Num<T>::from_acc(apply_epilogue<T>(p.epi, s, i, col, Y + i * N + col));
+        if (i < M && col < N)
+            Y[i * N + col] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, s, i, col, Y + i * N + col));
     }
     if (threadIdx.x == 0) ws.counters[tile] = 0u;   // ready for the next launch
 }
@@ -223,9 +238,31 @@ static int round_rows(int64_t m) {
     return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
 }
 
+// bytes of one operand element (8-bit float types: 1)
+static int64_t operand_bytes(olc_dtype dt) {
+    return dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) ? 2 : 1;
+}
+
 static int64_t skinny_m_col_groups(olc_dtype dt, int64_t N) {
-    const int64_t vec = 16 / (dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2);
+    const int64_t vec = 16 / operand_bytes(dt);
     return ceil_div(N, 32 * vec);
+}
+
+// the SIMT skinny-M kernel's element types: the four MatMul types and the
+// 8-bit float formats (F8<FMT>, float32 output); `other` for any other type
+template <typename R, typename F>
+static R dispatch_skinny_m(olc_dtype dt, R other, F&& f) {
+    switch (dt) {
+        case OLC_FLOAT: return f(float{});
+        case OLC_DOUBLE: return f(double{});
+        case OLC_FLOAT16: return f(__half{});
+        case OLC_BFLOAT16: return f(__nv_bfloat16{});
+        case OLC_FLOAT8E4M3FN: return f(F8<0>{});
+        case OLC_FLOAT8E5M2: return f(F8<1>{});
+        case OLC_FLOAT8E4M3FNUZ: return f(F8<2>{});
+        case OLC_FLOAT8E5M2FNUZ: return f(F8<3>{});
+    }
+    return other;
 }
 
 template <typename T, int MR>
@@ -241,7 +278,7 @@ static int skinny_m_occupancy() {
 
 static int skinny_m_blocks_per_sm(olc_dtype dt, int64_t M) {
     const int mr = round_rows(M);
-    return dispatch_int(dt, [&](auto tag) {
+    return dispatch_skinny_m(dt, 4, [&](auto tag) -> int {
         using T = decltype(tag);
         switch (mr) {
             case 1: return skinny_m_occupancy<T, 1>();
@@ -286,7 +323,7 @@ static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
     if (p.split_hint > 0) return (int)min64(p.split_hint, max64(1, p.K / 8));
     const int64_t groups = skinny_m_col_groups(dt, p.N) * p.items;
     const int64_t slots = (int64_t)sm_count * skinny_m_blocks_per_sm(dt, p.M);
-    const int64_t eb = dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2;
+    const int64_t eb = operand_bytes(dt);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
     const double stream_bytes = (double)p.K * p.N * eb * p.items;
     const int64_t smax = min64(64, max64(1, p.K / 256));
@@ -308,7 +345,7 @@ static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
 
 size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_partial_bytes(p, sm_count);
-    const int64_t vec = 16 / (dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : 2);
+    const int64_t vec = 16 / operand_bytes(dt);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
     const int64_t entries = round_rows(p.M) * 32 * vec;
     return (size_t)(skinny_m_col_groups(dt, p.N) * p.items * ksplit * entries * acc);
@@ -329,11 +366,13 @@ static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspa
     const int64_t blocks = groups * ksplit * p.items;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (ksplit > 1 && (!ws.partials || !ws.counters)) return cudaErrorInvalidValue;
-    // 16-byte A loads need every A row (and each operand item) 16-byte aligned
-    bool a_vec_ok = (p.K * (int64_t)sizeof(T)) % 16 == 0 &&
-                    (reinterpret_cast<uintptr_t>(p.A) & 15) == 0;
+    // vector A loads (16 bytes; 8 for one-byte elements) need every A row
+    // (and each operand item) aligned to the load
+    const int64_t a_align = sizeof(T) == 1 ? 8 : 16;
+    bool a_vec_ok = (p.K * (int64_t)sizeof(T)) % a_align == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.A) % a_align) == 0;
     for (int d = 0; d < p.map.rank; ++d)
-        if ((p.map.a_stride[d] * (int64_t)sizeof(T)) % 16 != 0) a_vec_ok = false;
+        if ((p.map.a_stride[d] * (int64_t)sizeof(T)) % a_align != 0) a_vec_ok = false;
     skinny_m_kernel<T, MR><<<(unsigned)blocks, SkinnyMConfig<MR>::KW * 32, 0, s>>>(
         p, groups, ksplit, kslice, ws, a_vec_ok ? 1 : 0);
     return cudaGetLastError();
@@ -343,7 +382,7 @@ cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_c
                             const Workspace& ws, cudaStream_t s) {
     if (skinny_m_on_tc(dt, p)) return launch_tc_skinny_m(dt, p, sm_count, ws, s);
     const int mr = round_rows(p.M);
-    return dispatch_dtype(dt, [&](auto tag) {
+    return dispatch_skinny_m(dt, cudaErrorInvalidValue, [&](auto tag) -> cudaError_t {
         using T = decltype(tag);
         switch (mr) {
             case 1: return launch_skinny_m_t<T, 1>(p, ksplit, ws, s);

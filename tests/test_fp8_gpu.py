@@ -172,3 +172,56 @@ def test_fnuz_runs_on_the_decode_kernel(dtype):
     assert np.isnan(y[0]).all() and np.isnan(ref[0]).all()
     assert np.array_equal(y[1:], ref[1:])
     assert y[1, 0] == 0.0 and y[2, 0] == ref[2, 0] and ref[2, 0] > 0
+
+
+SKINNY_SHAPES = [
+    ((4, 8192), (8192, 2048)),         # K sliced across blocks
+    ((1, 4096), (4096, 4096)),
+    ((16, 1024), (1024, 512)),
+    ((3, 2, 64), (64, 256)),           # batch folded into 6 rows
+    ((5, 1000), (1000, 272)),          # K tail, partial column group
+    ((64,), (64, 512)),                # rank-one A
+]
+
+
+@pytest.mark.parametrize("dtype", FP8 + FNUZ)
+@pytest.mark.parametrize("shapes", SKINNY_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_skinny_m(dtype, shapes):
+    """Up to 16 rows: the SIMT streaming kernel (16 one-byte B elements per
+    16-byte load, decoded to float32), chosen automatically from N >= 256."""
+    a_shape, b_shape = shapes
+    with Plan(a_shape, b_shape, dtype) as p:
+        if b_shape[-1] >= 256:
+            assert p.algorithm == "skinny_m"
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 48)
+    check_product(a, b, dtype, algorithm="skinny_m")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 49)
+    check_product(ai, bi, dtype, algorithm="skinny_m", exact=True)
+
+
+ONE = {"float8_e4m3fn": 0x38, "float8_e5m2": 0x3C, "float8_e4m3fnuz": 0x40, "float8_e5m2fnuz": 0x40}
+
+
+@pytest.mark.parametrize("dtype", FP8 + FNUZ)
+def test_fp8_skinny_m_decodes_every_pattern(dtype):
+    """Every one of the 256 patterns through the skinny kernel's 16-byte
+    vector decode (element i of a vector in byte i): Y row 0 = 1.0 x B row 0
+    (patterns 0..255), Y row 1 = 1.0 x B row 8 (255..0), all other terms 0."""
+    a8 = np.zeros((2, 16), np.uint8)
+    a8[0, 0] = ONE[dtype]
+    a8[1, 8] = ONE[dtype]
+    b8 = np.zeros((16, 256), np.uint8)
+    b8[0] = np.arange(256)
+    b8[8] = np.arange(255, -1, -1)
+    assert oracle.decode_fp8(np.array([ONE[dtype]], np.uint8), dtype)[0] == 1.0
+    ref, _ = oracle.matmul(a8, b8, dtype)
+    ta, tb = synth.from_numpy_storage(a8, dtype), synth.from_numpy_storage(b8, dtype)
+    with Plan(ta.shape, tb.shape, dtype) as p:
+        p.force("skinny_m")
+        Y = torch.empty(2, 256, device="cuda")
+        p.execute_checked(ta.cuda(), tb.cuda(), Y)
+        torch.cuda.synchronize()
+    y = Y.cpu().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(y), nan)
+    assert np.array_equal(y[~nan], ref[~nan])
