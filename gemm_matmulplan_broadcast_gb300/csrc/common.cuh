@@ -177,15 +177,14 @@ struct Num<F8<FMT>> {
     static __device__ __forceinline__ float from_acc(float v) { return v; }
 };
 
-// Sixteen 8-bit float elements (one 16-byte vector, element i in byte i) to
-// float32.  E4M3FN and E5M2 go through the hardware pair conversion to half
+// 8-bit float elements packed in WORDS 32-bit words (element i in byte i of
+// the little-endian sequence) to float32.  E4M3FN and E5M2 go through the hardware pair conversion to half
 // precision, which holds every value of both formats exactly, then to
 // float32; the FNUZ formats are decoded from their fields.
-template <int FMT>
-__device__ __forceinline__ void fp8_decode16(const uint4& raw, float (&out)[16]) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+template <int FMT, int WORDS>
+__device__ __forceinline__ void fp8_decode_words(const uint32_t (&w)[WORDS], float (&out)[4 * WORDS]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < WORDS; ++q) {
         if constexpr (FMT <= 1) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -202,6 +201,20 @@ __device__ __forceinline__ void fp8_decode16(const uint4& raw, float (&out)[16])
             for (int i = 0; i < 4; ++i) out[4 * q + i] = fp8_decode<FMT>((w[q] >> (8 * i)) & 0xFFu);
         }
     }
+}
+// Paired FP32 multiply-add (Blackwell fma.rn.f32x2): d = a * b + d on two
+// lanes of packed floats, one issue slot for two FMAs.
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f2(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void fma_f2(unsigned long long& d, unsigned long long a,
+                                       unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
 // one element through the read-only path (8-bit float elements as bytes)

@@ -232,21 +232,6 @@ struct Vec<double> {
     static constexpr int W = 2;
 };
 
-// Paired FP32 multiply-add (Blackwell fma.rn.f32x2): d = a * b + d on two
-// lanes of packed floats, one issue slot for two FMAs.
-__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack_f2(unsigned long long v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ void fma_f2(unsigned long long& d, unsigned long long a,
-                                       unsigned long long b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
-
 constexpr int SIMT_GROUP_M = 16;
 
 template <typename T, int BM, int BN, int BK, int TM, int TN, bool AT, bool BT>

@@ -35,11 +35,13 @@ cudaError_t launch_general_simt(olc_dtype dt, const Problem& p, cudaStream_t str
 // SKINNY_M
 //
 // Block = KW warps.  Lane l of every warp owns VEC consecutive output columns
-// (one 16-byte vector of each B row); the block covers 32 * VEC columns.  The
-// KW warps split the block's K range; within its range a warp walks k in
-// ascending order, loading B[k][cols] as one 16-byte vector per lane and the
-// MR values A[i][k] (the same address for all lanes, so one broadcast load),
-// and keeps an MR x VEC accumulator tile in registers.  The warps' tiles are
+// (one 16-byte vector of each B row; 8 or 4 bytes for one-byte elements with
+// 4 or more rows); the block covers 32 * VEC columns.  The KW warps split the
+// block's K range; within its range a warp walks k in ascending order,
+// loading B[k][cols] as one vector per lane and the MR rows' next 8 values
+// of A (the same addresses for all lanes, so broadcast loads, kept packed and
+// widened two k positions at a time), and keeps an MR x VEC accumulator tile
+// in registers (float accumulators as packed pairs for fma.rn.f32x2).  The warps' tiles are
 // summed in shared memory in warp order.  With ksplit > 1 the grid also
 // splits K across blocks: each block writes its partial tile to the
 // workspace, and the last block to arrive for a column group (counted with an
@@ -50,27 +52,184 @@ constexpr int kSkinnyMMax = 16;
 
 int skinny_m_max_rows() { return kSkinnyMMax; }
 
-template <typename T>
-struct Vec16 {
-    static constexpr int N = 16 / sizeof(T);
+// Columns per lane: one 16-byte B vector, except for one-byte elements with
+// four or more rows, where 16 columns per lane would hold 16 * MR float
+// accumulators: 8 columns (8-byte loads) for 4 rows, 4 columns (4-byte
+// loads) from 8 rows on.
+template <typename T, int MR>
+struct SkinnyMVec {
+    static constexpr int N = sizeof(T) != 1 ? 16 / (int)sizeof(T) : (MR <= 2 ? 16 : MR == 4 ? 8 : 4);
+    static constexpr int WORDS = N * (int)sizeof(T) / 4;   // 32-bit words per lane per B row
 };
 
-template <int MR>
+// WORDS consecutive 32-bit words through the read-only path, in one load
+template <int WORDS>
+__device__ __forceinline__ void ldg_words(const void* ptr, uint32_t (&w)[WORDS]) {
+    if constexpr (WORDS == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(ptr));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (WORDS == 2) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(ptr));
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        static_assert(WORDS == 1, "1, 2 or 4 words");
+        w[0] = __ldg(reinterpret_cast<const unsigned int*>(ptr));
+    }
+}
+
+// One output row's VEC accumulators of a lane.  Float accumulators are kept
+// as packed column pairs and updated with fma.rn.f32x2 (two round-to-nearest
+// FMAs per issue slot, per element the same arithmetic as fmaf); double
+// accumulators use DFMA.
+template <typename A, int VEC>
+struct AccRow {
+    A v[VEC];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) v[c] = A(0);
+    }
+    __device__ __forceinline__ void fma_row(A a, const A (&b)[VEC]) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) v[c] = fma(a, b[c], v[c]);
+    }
+    __device__ __forceinline__ A get(int c) const { return v[c]; }
+};
+template <int VEC>
+struct AccRow<float, VEC> {
+    static_assert(VEC % 2 == 0, "column pairs");
+    unsigned long long v[VEC / 2];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int c = 0; c < VEC / 2; ++c) v[c] = 0ull;
+    }
+    __device__ __forceinline__ void fma_row(float a, const unsigned long long (&b2)[VEC / 2]) {
+        const unsigned long long a2 = pack_f2(a, a);
+#pragma unroll
+        for (int c = 0; c < VEC / 2; ++c) fma_f2(v[c], a2, b2[c]);
+    }
+    __device__ __forceinline__ float get(int c) const {
+        float lo, hi;
+        unpack_f2(v[c / 2], lo, hi);
+        return (c & 1) ? hi : lo;
+    }
+};
+
+// B operand row as the accumulator row consumes it: packed pairs for float
+template <typename A, int VEC>
+struct BRow {
+    A b[VEC];
+    __device__ __forceinline__ void set(const A (&x)[VEC]) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) b[c] = x[c];
+    }
+    __device__ __forceinline__ const A (&operand() const)[VEC] { return b; }
+};
+template <int VEC>
+struct BRow<float, VEC> {
+    unsigned long long b2[VEC / 2];
+    __device__ __forceinline__ void set(const float (&x)[VEC]) {
+#pragma unroll
+        for (int c = 0; c < VEC / 2; ++c) b2[c] = pack_f2(x[2 * c], x[2 * c + 1]);
+    }
+    __device__ __forceinline__ const unsigned long long (&operand() const)[VEC / 2] { return b2; }
+};
+
+// Bits of one element and back, for A rows kept as raw 32-bit words
+// (elements packed little-endian, 8-byte elements over two words).
+template <typename T>
+struct ElemBits;
+template <>
+struct ElemBits<float> {
+    static __device__ __forceinline__ uint32_t bits(float v) { return __float_as_uint(v); }
+};
+template <>
+struct ElemBits<__half> {
+    static __device__ __forceinline__ uint32_t bits(__half v) { return __half_as_ushort(v); }
+};
+template <>
+struct ElemBits<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t bits(__nv_bfloat16 v) { return __bfloat16_as_ushort(v); }
+};
+template <int FMT>
+struct ElemBits<F8<FMT>> {
+    static __device__ __forceinline__ uint32_t bits(F8<FMT> v) { return v.bits; }
+};
+
+// element u of a raw row, stored into the words
+template <typename T, int AW>
+__device__ __forceinline__ void put_elem(uint32_t (&w)[AW], int u, T v) {
+    if constexpr (sizeof(T) == 8) {
+        const unsigned long long b = (unsigned long long)__double_as_longlong(v);
+        w[2 * u] = (uint32_t)b;
+        w[2 * u + 1] = (uint32_t)(b >> 32);
+    } else {
+        constexpr int PER = 4 / (int)sizeof(T);
+        const uint32_t b = ElemBits<T>::bits(v) << (8 * (int)sizeof(T) * (u % PER));
+        w[u / PER] = (u % PER == 0) ? b : (w[u / PER] | b);
+    }
+}
+
+// elements u0 and u0 + 1 (UP = 2: one- and two-byte types) or u0 alone
+// (UP = 1) of a raw row, in the accumulator type
+template <typename T, int AW, int UP>
+__device__ __forceinline__ void get_elems(const uint32_t (&w)[AW], int u0,
+                                          typename Num<T>::acc_t (&out)[UP]) {
+    if constexpr (sizeof(T) == 8) {
+        out[0] = __hiloint2double((int)w[2 * u0 + 1], (int)w[2 * u0]);
+    } else if constexpr (sizeof(T) == 4) {
+        out[0] = __uint_as_float(w[u0]);
+    } else if constexpr (sizeof(T) == 2) {
+        const uint32_t x = w[u0 / 2];
+        if constexpr (std::is_same<T, __half>::value) {
+            out[0] = __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu)));
+            out[1] = __half2float(__ushort_as_half((unsigned short)(x >> 16)));
+        } else {
+            out[0] = __bfloat162float(__ushort_as_bfloat16((unsigned short)(x & 0xFFFFu)));
+            out[1] = __bfloat162float(__ushort_as_bfloat16((unsigned short)(x >> 16)));
+        }
+    } else {
+        const uint32_t x = (w[u0 / 4] >> (8 * (u0 % 4))) & 0xFFFFu;
+        const uint32_t pair[1] = {x};
+        float four[4];
+        fp8_decode_words<T::kFormat, 1>(pair, four);   // bytes 2 and 3 are zero
+        out[0] = four[0];
+        out[1] = four[1];
+    }
+}
+
+// the accumulator-type values of the elements packed in `w`
+template <typename T, int WORDS>
+__device__ __forceinline__ void widen_words(const uint32_t (&w)[WORDS],
+                                            typename Num<T>::acc_t (&out)[WORDS * 4 / sizeof(T)]) {
+    if constexpr (sizeof(T) == 1) {
+        fp8_decode_words<T::kFormat, WORDS>(w, out);
+    } else {
+        const T* e = reinterpret_cast<const T*>(w);
+#pragma unroll
+        for (int v = 0; v < (int)(WORDS * 4 / sizeof(T)); ++v) out[v] = Num<T>::to_acc(e[v]);
+    }
+}
+
+// warps splitting K in a block; one-byte operands, whose lanes hold fewer
+// columns from 4 rows on, keep more warps (and more loads in flight)
+template <typename T, int MR>
 struct SkinnyMConfig {
-    static constexpr int KW = MR <= 4 ? 8 : (MR <= 8 ? 4 : 2);   // warps splitting K
+    static constexpr int KW = sizeof(T) == 1 ? (MR <= 8 ? 8 : 4) : (MR <= 4 ? 8 : (MR <= 8 ? 4 : 2));
 };
 
 template <typename T, int MR>
-__global__ void __launch_bounds__(SkinnyMConfig<MR>::KW * 32)
+__global__ void __launch_bounds__(SkinnyMConfig<T, MR>::KW * 32)
 skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws,
                 int a_vec_ok) {
     using acc_t = typename Num<T>::acc_t;
     using out_t = typename Num<T>::out_t;    // float32 for 8-bit float operands
-    constexpr int VEC = Vec16<T>::N;
-    constexpr int KW = SkinnyMConfig<MR>::KW;
+    constexpr int VEC = SkinnyMVec<T, MR>::N;
+    constexpr int WORDS = SkinnyMVec<T, MR>::WORDS;
+    constexpr int KW = SkinnyMConfig<T, MR>::KW;
     constexpr int COLS = 32 * VEC;
     constexpr int KU = 8;                    // k rows per step: 8 B vectors in flight per lane
-    constexpr int AV = (KU * (int)sizeof(T) + 15) / 16;   // 16-byte A vectors per row per step
+    constexpr int AW = KU * (int)sizeof(T) / 4;           // 32-bit words of A per row per step
+    constexpr int UP = sizeof(T) <= 2 ? 2 : 1;             // k rows decoded together from A
     __shared__ acc_t red[KW][MR][COLS];
     __shared__ unsigned int am_last;
 
@@ -97,80 +256,79 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
     const int64_t k0 = min64(kb1, kb0 + warp * wlen);
     const int64_t k1 = min64(kb1, k0 + wlen);
 
-    acc_t acc[MR][VEC];
+    AccRow<acc_t, VEC> acc[MR];
 #pragma unroll
-    for (int i = 0; i < MR; ++i)
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[i][v] = acc_t(0);
+    for (int i = 0; i < MR; ++i) acc[i].zero();
 
     if (col_ok) {
         const T* bp = B + col0;
         int64_t k = k0;
         for (; k + KU <= k1; k += KU) {
-            uint4 bv[KU];
+            uint32_t bw[KU][WORDS];
 #pragma unroll
-            for (int u = 0; u < KU; ++u)
-                bv[u] = __ldg(reinterpret_cast<const uint4*>(bp + (k + u) * N));
-            acc_t a[MR][KU];
+            for (int u = 0; u < KU; ++u) ldg_words<WORDS>(bp + (k + u) * N, bw[u]);
+            // A rows kept as raw words, decoded a k pair at a time: MR x KU
+            // decoded values would take most of the registers at 8-16 rows
+            uint32_t araw[MR][AW];
 #pragma unroll
             for (int i = 0; i < MR; ++i) {
                 if (i < M) {
                     if (a_vec_ok) {
-                        if constexpr (sizeof(T) == 1) {
-                            // 8 one-byte elements: one 8-byte load (k is a multiple of 8)
+                        if constexpr (AW == 2) {
                             const uint2 av = __ldg(reinterpret_cast<const uint2*>(A + i * K + k));
-                            const T* ae = reinterpret_cast<const T*>(&av);
-#pragma unroll
-                            for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ae[u]);
+                            araw[i][0] = av.x;
+                            araw[i][1] = av.y;
                         } else {
-                            uint4 av[AV];
 #pragma unroll
-                            for (int q = 0; q < AV; ++q)
-                                av[q] = __ldg(reinterpret_cast<const uint4*>(A + i * K + k) + q);
-                            const T* ae = reinterpret_cast<const T*>(av);
-#pragma unroll
-                            for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ae[u]);
+                            for (int q = 0; q < AW / 4; ++q) {
+                                const uint4 av = __ldg(reinterpret_cast<const uint4*>(A + i * K + k) + q);
+                                araw[i][4 * q] = av.x;
+                                araw[i][4 * q + 1] = av.y;
+                                araw[i][4 * q + 2] = av.z;
+                                araw[i][4 * q + 3] = av.w;
+                            }
                         }
                     } else {
 #pragma unroll
-                        for (int u = 0; u < KU; ++u) a[i][u] = Num<T>::to_acc(ldg_elem(A + i * K + k + u));
+                        for (int u = 0; u < KU; ++u) put_elem<T, AW>(araw[i], u, ldg_elem(A + i * K + k + u));
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < KU; ++u) a[i][u] = acc_t(0);
+                    for (int q = 0; q < AW; ++q) araw[i][q] = 0u;
                 }
             }
 #pragma unroll
-            for (int u = 0; u < KU; ++u) {
-                const T* be = reinterpret_cast<const T*>(&bv[u]);
-                acc_t b[VEC];
-                if constexpr (sizeof(T) == 1) {
-                    fp8_decode16<T::kFormat>(bv[u], b);
-                } else {
+            for (int u0 = 0; u0 < KU; u0 += UP) {
+                acc_t a[MR][UP];
 #pragma unroll
-                    for (int v = 0; v < VEC; ++v) b[v] = Num<T>::to_acc(be[v]);
+                for (int i = 0; i < MR; ++i) get_elems<T, AW, UP>(araw[i], u0, a[i]);
+#pragma unroll
+                for (int uu = 0; uu < UP; ++uu) {
+                    acc_t b[VEC];
+                    widen_words<T, WORDS>(bw[u0 + uu], b);
+                    BRow<acc_t, VEC> br;
+                    br.set(b);
+#pragma unroll
+                    for (int i = 0; i < MR; ++i) acc[i].fma_row(a[i][uu], br.operand());
                 }
-#pragma unroll
-                for (int i = 0; i < MR; ++i)
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a[i][u], b[v], acc[i][v]);
             }
         }
         for (; k < k1; ++k) {
-            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bp + k * N));
-            const T* be = reinterpret_cast<const T*>(&bv);
+            uint32_t bw[WORDS];
+            ldg_words<WORDS>(bp + k * N, bw);
+            acc_t b[VEC];
+            widen_words<T, WORDS>(bw, b);
+            BRow<acc_t, VEC> br;
+            br.set(b);
 #pragma unroll
-            for (int i = 0; i < MR; ++i) {
-                const acc_t a = i < M ? Num<T>::to_acc(ldg_elem(A + i * K + k)) : acc_t(0);
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) acc[i][v] = fma(a, Num<T>::to_acc(be[v]), acc[i][v]);
-            }
+            for (int i = 0; i < MR; ++i)
+                acc[i].fma_row(i < M ? Num<T>::to_acc(ldg_elem(A + i * K + k)) : acc_t(0), br.operand());
         }
     }
 #pragma unroll
     for (int i = 0; i < MR; ++i)
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) red[warp][i][lane * VEC + v] = acc[i][v];
+        for (int v = 0; v < VEC; ++v) red[warp][i][lane * VEC + v] = acc[i].get(v);
     __syncthreads();
 
     // sum the warps' tiles in warp order: thread t owns entries t, t + NT, ...
@@ -243,9 +401,15 @@ static int64_t operand_bytes(olc_dtype dt) {
     return dt == OLC_DOUBLE ? 8 : dt == OLC_FLOAT ? 4 : (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) ? 2 : 1;
 }
 
-static int64_t skinny_m_col_groups(olc_dtype dt, int64_t N) {
-    const int64_t vec = 16 / operand_bytes(dt);
-    return ceil_div(N, 32 * vec);
+// columns per lane of the SIMT skinny-M kernel (SkinnyMVec on the device)
+static int64_t skinny_m_vec(olc_dtype dt, int64_t M) {
+    const int64_t eb = operand_bytes(dt);
+    const int mr = round_rows(M);
+    return eb != 1 ? 16 / eb : (mr <= 2 ? 16 : mr == 4 ? 8 : 4);
+}
+
+static int64_t skinny_m_col_groups(olc_dtype dt, int64_t M, int64_t N) {
+    return ceil_div(N, 32 * skinny_m_vec(dt, M));
 }
 
 // the SIMT skinny-M kernel's element types: the four MatMul types and the
@@ -269,7 +433,7 @@ template <typename T, int MR>
 static int skinny_m_occupancy() {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, skinny_m_kernel<T, MR>,
-                                                      SkinnyMConfig<MR>::KW * 32, 0) != cudaSuccess) {
+                                                      SkinnyMConfig<T, MR>::KW * 32, 0) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -321,7 +485,7 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
 
 static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
     if (p.split_hint > 0) return (int)min64(p.split_hint, max64(1, p.K / 8));
-    const int64_t groups = skinny_m_col_groups(dt, p.N) * p.items;
+    const int64_t groups = skinny_m_col_groups(dt, p.M, p.N) * p.items;
     const int64_t slots = (int64_t)sm_count * skinny_m_blocks_per_sm(dt, p.M);
     const int64_t eb = operand_bytes(dt);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
@@ -345,22 +509,21 @@ static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
 
 size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_partial_bytes(p, sm_count);
-    const int64_t vec = 16 / operand_bytes(dt);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
-    const int64_t entries = round_rows(p.M) * 32 * vec;
-    return (size_t)(skinny_m_col_groups(dt, p.N) * p.items * ksplit * entries * acc);
+    const int64_t entries = round_rows(p.M) * 32 * skinny_m_vec(dt, p.M);
+    return (size_t)(skinny_m_col_groups(dt, p.M, p.N) * p.items * ksplit * entries * acc);
 }
 
 size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
     (void)ksplit;
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_counter_count(p, sm_count);
-    return (size_t)(skinny_m_col_groups(dt, p.N) * p.items);
+    return (size_t)(skinny_m_col_groups(dt, p.M, p.N) * p.items);
 }
 
 template <typename T, int MR>
 static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspace& ws,
                                      cudaStream_t s) {
-    constexpr int VEC = Vec16<T>::N;
+    constexpr int VEC = SkinnyMVec<T, MR>::N;
     const int64_t groups = ceil_div(p.N, 32 * VEC);
     const int64_t kslice = ceil_div(ceil_div(p.K, ksplit), 8) * 8;
     const int64_t blocks = groups * ksplit * p.items;
@@ -373,7 +536,7 @@ static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspa
                     (reinterpret_cast<uintptr_t>(p.A) % a_align) == 0;
     for (int d = 0; d < p.map.rank; ++d)
         if ((p.map.a_stride[d] * (int64_t)sizeof(T)) % a_align != 0) a_vec_ok = false;
-    skinny_m_kernel<T, MR><<<(unsigned)blocks, SkinnyMConfig<MR>::KW * 32, 0, s>>>(
+    skinny_m_kernel<T, MR><<<(unsigned)blocks, SkinnyMConfig<T, MR>::KW * 32, 0, s>>>(
         p, groups, ksplit, kslice, ws, a_vec_ok ? 1 : 0);
     return cudaGetLastError();
 }

@@ -181,14 +181,19 @@ SKINNY_SHAPES = [
     ((3, 2, 64), (64, 256)),           # batch folded into 6 rows
     ((5, 1000), (1000, 272)),          # K tail, partial column group
     ((64,), (64, 512)),                # rank-one A
+    ((4, 2048), (2048, 4096)),         # 4 rows: 8 columns per lane
+    ((16, 4096), (4096, 1024)),        # 16 rows: 4 columns per lane
+    ((6, 1001), (1001, 256)),          # A rows not 8-byte aligned: element loads
+    ((12, 999), (999, 512)),           # the same with 16 rows
 ]
 
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
 @pytest.mark.parametrize("shapes", SKINNY_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
 def test_fp8_skinny_m(dtype, shapes):
-    """Up to 16 rows: the SIMT streaming kernel (16 one-byte B elements per
-    16-byte load, decoded to float32), chosen automatically from N >= 256."""
+    """Up to 16 rows: the SIMT streaming kernel (16, 8 or 4 one-byte B
+    elements per lane load, decoded to float32), chosen automatically from
+    N >= 256; A rows that are not 8-byte aligned take element loads."""
     a_shape, b_shape = shapes
     with Plan(a_shape, b_shape, dtype) as p:
         if b_shape[-1] >= 256:
@@ -203,11 +208,13 @@ ONE = {"float8_e4m3fn": 0x38, "float8_e5m2": 0x3C, "float8_e4m3fnuz": 0x40, "flo
 
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
-def test_fp8_skinny_m_decodes_every_pattern(dtype):
-    """Every one of the 256 patterns through the skinny kernel's 16-byte
-    vector decode (element i of a vector in byte i): Y row 0 = 1.0 x B row 0
-    (patterns 0..255), Y row 1 = 1.0 x B row 8 (255..0), all other terms 0."""
-    a8 = np.zeros((2, 16), np.uint8)
+@pytest.mark.parametrize("m", [2, 4, 16])
+def test_fp8_skinny_m_decodes_every_pattern(dtype, m):
+    """Every one of the 256 patterns through the skinny kernel's B decode
+    (16, 8 or 4 one-byte columns per lane for 2, 4 or 16 rows; element i of a
+    vector in byte i): Y row 0 = 1.0 x B row 0 (patterns 0..255), Y row 1 =
+    1.0 x B row 8 (255..0), all other terms 0."""
+    a8 = np.zeros((m, 16), np.uint8)
     a8[0, 0] = ONE[dtype]
     a8[1, 8] = ONE[dtype]
     b8 = np.zeros((16, 256), np.uint8)
@@ -218,7 +225,34 @@ def test_fp8_skinny_m_decodes_every_pattern(dtype):
     ta, tb = synth.from_numpy_storage(a8, dtype), synth.from_numpy_storage(b8, dtype)
     with Plan(ta.shape, tb.shape, dtype) as p:
         p.force("skinny_m")
-        Y = torch.empty(2, 256, device="cuda")
+        Y = torch.empty(m, 256, device="cuda")
+        p.execute_checked(ta.cuda(), tb.cuda(), Y)
+        torch.cuda.synchronize()
+    y = Y.cpu().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(y), nan)
+    assert np.array_equal(y[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("dtype", FP8 + FNUZ)
+def test_fp8_skinny_m_decodes_every_a_pattern(dtype):
+    """Every pattern through the skinny kernel's A decode (A rows kept as
+    packed bytes, decoded two k positions at a time): A[i, k] = 16 i + k for
+    16 rows and K = 16, B[k, j] = 1.0 where j == k < 16, else 0.  Y[i, j] =
+    A[i, j] exactly, except in rows holding a NaN or an infinity, where every
+    other term is NaN x 0 or inf x 0 and the oracle's row is NaN too."""
+    a8 = np.arange(256, dtype=np.uint8).reshape(16, 16)
+    b8 = np.zeros((16, 256), np.uint8)
+    b8[np.arange(16), np.arange(16)] = ONE[dtype]
+    ref, _ = oracle.matmul(a8, b8, dtype)
+    dec = oracle.decode_fp8(a8.reshape(-1), dtype).reshape(16, 16)
+    clean = ~np.isnan(ref).any(axis=1)
+    assert clean.sum() >= 14
+    assert np.array_equal(ref[clean][:, :16], dec[clean])
+    ta, tb = synth.from_numpy_storage(a8, dtype), synth.from_numpy_storage(b8, dtype)
+    with Plan(ta.shape, tb.shape, dtype) as p:
+        p.force("skinny_m")
+        Y = torch.empty(16, 256, device="cuda")
         p.execute_checked(ta.cuda(), tb.cuda(), Y)
         torch.cuda.synchronize()
     y = Y.cpu().numpy()
