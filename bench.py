@@ -37,7 +37,8 @@ if ROOT not in sys.path:
 METRIC = "MatMul TFLOP/s (BF16/FP16/FP32/FP64) and skinny GB/s, % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dense tensor-core ratio of FP16 to BF16 (equal) and the FP32/FP64 SIMT
-# peaks derived from unit counts and the maximum SM clock
+# peaks derived from unit counts and the maximum SM clock: 152 SMs x 128 FP32
+# lanes x 2 flop x 2.07 GHz, and 152 SMs x 4 FP64 flop per clock x 2.07 GHz
 SM_COUNT_GB300 = 152
 FP8_OVER_BF16 = 2.0          # dense FP8 / BF16 tensor rate on GB300 (4.5 / 2.25 PFLOP/s nominal)
 FP32_LANES_PER_SM = 128
@@ -719,7 +720,7 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "+".join(short[d] for d in dtypes),
-        "data": "synthetic (seeded torch CPU generator, cast RNE; see DESIGN.md input recipe)",
+        "data": "synthetic (seeded torch CPU generator per product, A drawn before B in float32, cast to the storage type with RNE)",
         "config": {
             "workload": workload.name,
             "description": workload.description,

@@ -25,7 +25,7 @@ MatMul Performance Roadmap, section "Phase 4: complete MatMul"):
    (extent 1) is 0;
 4. an output with no elements is returned without reading the inputs.
 
-Readings where the pages are silent (each is listed in the design doc): rank-0
+Readings where the pages are silent: rank-0
 operands are rejected; broadcasting an extent 0 against 1 gives 0 and against
 n > 1 is an error; K == 0 with a non-empty output gives zeros; two rank-one
 operands give a rank-0 (one element) output.
