@@ -217,6 +217,82 @@ struct SkinnyMConfig {
     static constexpr int KW = sizeof(T) == 1 ? (MR <= 8 ? 8 : 4) : (MR <= 4 ? 8 : (MR <= 8 ? 4 : 2));
 };
 
+// End of a skinny-M block: sum the KW warps' MR x COLS tiles (red) in warp
+// order; with ksplit == 1 store them through the epilogue, otherwise file the
+// block's partial tile in the workspace and let the last block of the column
+// group to arrive (an atomic count) add the partials in split order
+// 0..ksplit-1 -- the same order whichever block arrives last, so results are
+// reproducible run to run.  Every thread of the block calls it.
+template <typename T, int MR, int COLS, int KW>
+__device__ __forceinline__ void skinny_m_finish(const Problem& p,
+                                                const typename Num<T>::acc_t (&red)[KW][MR][COLS],
+                                                unsigned int& am_last, int64_t item, int64_t cg, int split,
+                                                int ksplit, int64_t col_groups, const Workspace& ws,
+                                                typename Num<T>::out_t* __restrict__ Y) {
+    using acc_t = typename Num<T>::acc_t;
+    using out_t = typename Num<T>::out_t;
+    const int64_t M = p.M, N = p.N;
+    // thread t owns entries t, t + NT, ...
+    constexpr int NT = KW * 32;
+    constexpr int ENTRIES = MR * COLS;
+    constexpr int Q = (ENTRIES + NT - 1) / NT;
+    acc_t part[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int e = threadIdx.x + q * NT;
+        acc_t s = acc_t(0);
+        if (e < ENTRIES) {
+            const int i = e / COLS, c = e % COLS;
+            s = red[0][i][c];
+#pragma unroll
+            for (int w = 1; w < KW; ++w) s += red[w][i][c];
+        }
+        part[q] = s;
+    }
+
+    if (ksplit == 1) {
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const int e = threadIdx.x + q * NT;
+            if (e >= ENTRIES) continue;
+            const int i = e / COLS, c = e % COLS;
+            const int64_t col = cg * COLS + c;
+            if (i < M && col < N)
+                Y[i * N + col] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, part[q], i, col, Y + i * N + col));
+        }
+        return;
+    }
+
+    // cross-block split: partial tile -> workspace, last arrival reduces
+    acc_t* P = static_cast<acc_t*>(ws.partials);
+    const int64_t tile = item * col_groups + cg;
+    acc_t* mine = P + (tile * ksplit + split) * ENTRIES;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int e = threadIdx.x + q * NT;
+        if (e < ENTRIES) mine[e] = part[q];
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int prev = atomicAdd(ws.counters + tile, 1u);
+        am_last = (prev == (unsigned int)ksplit - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+    const acc_t* all = P + tile * ksplit * ENTRIES;
+    for (int e = threadIdx.x; e < ENTRIES; e += NT) {
+        acc_t s = __ldcg(all + e);
+        for (int t = 1; t < ksplit; ++t) s += __ldcg(all + (int64_t)t * ENTRIES + e);
+        const int i = e / COLS, c = e % COLS;
+        const int64_t col = cg * COLS + c;
+        if (i < M && col < N)
+            Y[i * N + col] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, s, i, col, Y + i * N + col));
+    }
+    if (threadIdx.x == 0) ws.counters[tile] = 0u;   // ready for the next launch
+}
+
 template <typename T, int MR>
 __global__ void __launch_bounds__(SkinnyMConfig<T, MR>::KW * 32)
 skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws,
@@ -331,65 +407,174 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
         for (int v = 0; v < VEC; ++v) red[warp][i][lane * VEC + v] = acc[i].get(v);
     __syncthreads();
 
-    // sum the warps' tiles in warp order: thread t owns entries t, t + NT, ...
-    constexpr int NT = KW * 32;
-    constexpr int ENTRIES = MR * COLS;
-    constexpr int Q = (ENTRIES + NT - 1) / NT;
-    acc_t part[Q];
+    skinny_m_finish<T, MR, COLS, KW>(p, red, am_last, item, cg, split, ksplit, col_groups, ws, Y);
+}
+
+// ===========================================================================
+// SKINNY_M for E4M3FN / E5M2 operands on the warp-level MMA
+//
+// mma.sync.aligned.m16n8k32.row.col.f32.{e4m3,e5m2}: D[16 x 8] += A[16 x 32]
+// * B[32 x 8] with float32 accumulation.  The MMA's 16 rows are the
+// product's rows of A (at most 16, the rest zeros); its 32 K positions a
+// 32-row chunk of B.  Lane (g, t) = (lane / 4, lane % 4) loads 8 bytes --
+// columns 8 g .. 8 g + 7 of the warp's 64-column group -- from the chunk's B
+// rows 4 t .. 4 t + 3 and 16 + 4 t .. 16 + 4 t + 3, the K positions its B
+// fragment registers hold, and transposes each 4 x 4 byte block with byte
+// permutes: register p of the result holds column 8 g + p at those four K
+// positions, i.e. the B fragment of MMA p (p = 0..7), whose column n stands
+// for product column 8 n + p.  The eight MMAs of a chunk cover the 64
+// columns and share one A fragment (rows g and g + 8 at the lane's K
+// positions, one 4-byte load each).  So B is read once, in the layout it is
+// stored in.  Each lane keeps F8_RING chunks of loads (B and A) in a
+// register ring, issuing chunk c + F8_RING - 1 before the MMAs of chunk c:
+// at HBM rates a load takes microseconds to return, and the bytes in flight
+// per SM set the bandwidth.  Blocks of kF8MmaWarps warps split K as the SIMT
+// kernel's do and end the same way (skinny_m_finish).
+
+constexpr int kF8MmaWarps = 4;
+constexpr int kF8MmaCols = 64;
+constexpr int F8_RING = 4;
+
+template <int FMT>
+__device__ __forceinline__ void mma_f8_m16n8k32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1) {
+    if constexpr (FMT == 0) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        static_assert(FMT == 1, "E4M3FN or E5M2");
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.f32.e5m2.e5m2.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// 4 x 4 byte transpose: out[q] = byte q of r0, r1, r2, r3 (in that order)
+__device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
+                                                   uint32_t (&out)[4]) {
+    const uint32_t x = __byte_perm(r0, r1, 0x5140), y = __byte_perm(r2, r3, 0x5140);
+    const uint32_t x2 = __byte_perm(r0, r1, 0x7362), y2 = __byte_perm(r2, r3, 0x7362);
+    out[0] = __byte_perm(x, y, 0x5410);
+    out[1] = __byte_perm(x, y, 0x7632);
+    out[2] = __byte_perm(x2, y2, 0x5410);
+    out[3] = __byte_perm(x2, y2, 0x7632);
+}
+
+// one chunk's operands in a lane: 8 B rows of 8 bytes, the A fragment
+struct F8Chunk {
+    uint2 b[8];
+    uint32_t a[4];
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kF8MmaWarps * 32, 3)
+skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws,
+                       int a_vec_ok) {
+    using T = F8<FMT>;
+    constexpr int KW = kF8MmaWarps;
+    constexpr int COLS = kF8MmaCols;
+    constexpr int MR = 16;
+    constexpr int R = F8_RING;
+    __shared__ float red[KW][MR][COLS];
+    __shared__ unsigned int am_last;
+
+    const int64_t per_item = col_groups * ksplit;
+    const int64_t item = blockIdx.x / per_item;
+    const int64_t rem = blockIdx.x % per_item;
+    const int split = (int)(rem / col_groups);
+    const int64_t cg = rem % col_groups;
+    int64_t a_off, b_off;
+    batch_offsets(p.map, item, a_off, b_off);
+    const unsigned char* __restrict__ A = static_cast<const unsigned char*>(p.A) + a_off;
+    const unsigned char* __restrict__ B = static_cast<const unsigned char*>(p.B) + b_off;
+    float* __restrict__ Y = static_cast<float*>(p.Y) + item * p.M * p.N;
+    const int64_t M = p.M, N = p.N, K = p.K;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t col0 = cg * COLS + 8 * g;    // this lane's 8 columns
+    const bool col_ok = col0 < N;             // N is a multiple of 16
+    // this block's K range (kslice is a multiple of 32), then this warp's
+    // share of it, also a multiple of 32
+    const int64_t kb0 = (int64_t)split * kslice;
+    const int64_t kb1 = min64(K, kb0 + kslice);
+    const int64_t wlen = ceil_div(ceil_div(max64(kb1 - kb0, 0), KW), 32) * 32;
+    const int64_t k0 = min64(kb1, kb0 + warp * wlen);
+    const int64_t k1 = min64(kb1, k0 + wlen);
+
+    // A[row][kk .. kk + 3] packed little-endian; zero past k1 and past M
+    auto a_word = [&](int row, int64_t kk) -> uint32_t {
+        if (row >= M) return 0u;
+        const unsigned char* ar = A + row * K;
+        if (a_vec_ok && kk + 4 <= k1) return __ldg(reinterpret_cast<const unsigned int*>(ar + kk));
+        uint32_t w = 0u;
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int e = threadIdx.x + q * NT;
-        acc_t s = acc_t(0);
-        if (e < ENTRIES) {
-            const int i = e / COLS, c = e % COLS;
-            s = red[0][i][c];
+        for (int i = 0; i < 4; ++i)
+            if (kk + i < k1) w |= (uint32_t)__ldg(ar + kk + i) << (8 * i);
+        return w;
+    };
+    // B rows kc + 4t + j (j < 4) and kc + 16 + 4t + j of the lane's columns,
+    // and the A fragment; rows at or past k1 (another warp's range, or past
+    // K) read as zeros
+    auto load_chunk = [&](int64_t kc, F8Chunk& c) {
 #pragma unroll
-            for (int w = 1; w < KW; ++w) s += red[w][i][c];
+        for (int j = 0; j < 8; ++j) {
+            const int64_t r = kc + (j < 4 ? 4 * t + j : 16 + 4 * t + (j - 4));
+            c.b[j] = (col_ok && r < k1) ? __ldg(reinterpret_cast<const uint2*>(B + r * N + col0))
+                                        : make_uint2(0u, 0u);
         }
-        part[q] = s;
+        if (kc < k1) {
+            c.a[0] = a_word(g, kc + 4 * t);
+            c.a[1] = a_word(g + 8, kc + 4 * t);
+            c.a[2] = a_word(g, kc + 16 + 4 * t);
+            c.a[3] = a_word(g + 8, kc + 16 + 4 * t);
+        }
+    };
+
+    float d[8][4];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[q][i] = 0.0f;
+
+    F8Chunk ring[R];
+#pragma unroll
+    for (int r = 0; r < R - 1; ++r) load_chunk(k0 + 32 * r, ring[r]);
+    for (int64_t kc = k0; kc < k1; kc += 32 * R) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t kcur = kc + 32 * r;
+            load_chunk(kcur + 32 * (R - 1), ring[(r + R - 1) % R]);
+            if (kcur < k1) {
+                const F8Chunk& c = ring[r];
+                // lo: K positions 4t..4t+3, hi: 16+4t..; [0]: columns 0-3, [1]: 4-7
+                uint32_t lo[2][4], hi[2][4];
+                transpose4x4_bytes(c.b[0].x, c.b[1].x, c.b[2].x, c.b[3].x, lo[0]);
+                transpose4x4_bytes(c.b[0].y, c.b[1].y, c.b[2].y, c.b[3].y, lo[1]);
+                transpose4x4_bytes(c.b[4].x, c.b[5].x, c.b[6].x, c.b[7].x, hi[0]);
+                transpose4x4_bytes(c.b[4].y, c.b[5].y, c.b[6].y, c.b[7].y, hi[1]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mma_f8_m16n8k32<FMT>(d[q], c.a, lo[q / 4][q % 4], hi[q / 4][q % 4]);
+            }
+        }
     }
 
-    if (ksplit == 1) {
+    // MMA q's accumulator: rows g and g + 8, MMA columns 2t and 2t + 1, i.e.
+    // columns 8 (2t) + q and 8 (2t + 1) + q of the group
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int e = threadIdx.x + q * NT;
-            if (e >= ENTRIES) continue;
-            const int i = e / COLS, c = e % COLS;
-            const int64_t col = cg * COLS + c;
-            if (i < M && col < N)
-                Y[i * N + col] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, part[q], i, col, Y + i * N + col));
-        }
-        return;
-    }
-
-    // cross-block split: partial tile -> workspace, last arrival reduces
-    acc_t* P = static_cast<acc_t*>(ws.partials);
-    const int64_t tile = item * col_groups + cg;
-    acc_t* mine = P + (tile * ksplit + split) * ENTRIES;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int e = threadIdx.x + q * NT;
-        if (e < ENTRIES) mine[e] = part[q];
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned int prev = atomicAdd(ws.counters + tile, 1u);
-        am_last = (prev == (unsigned int)ksplit - 1) ? 1u : 0u;
+    for (int q = 0; q < 8; ++q) {
+        red[warp][g][16 * t + q] = d[q][0];
+        red[warp][g][16 * t + 8 + q] = d[q][1];
+        red[warp][g + 8][16 * t + q] = d[q][2];
+        red[warp][g + 8][16 * t + 8 + q] = d[q][3];
     }
     __syncthreads();
-    if (!am_last) return;
-    __threadfence();
-    const acc_t* all = P + tile * ksplit * ENTRIES;
-    for (int e = threadIdx.x; e < ENTRIES; e += NT) {
-        acc_t s = __ldcg(all + e);
-        for (int t = 1; t < ksplit; ++t) s += __ldcg(all + (int64_t)t * ENTRIES + e);
-        const int i = e / COLS, c = e % COLS;
-        const int64_t col = cg * COLS + c;
-        if (i < M && col < N)
-            Y[i * N + col] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, s, i, col, Y + i * N + col));
-    }
-    if (threadIdx.x == 0) ws.counters[tile] = 0u;   // ready for the next launch
+    skinny_m_finish<T, MR, COLS, KW>(p, red, am_last, item, cg, split, ksplit, col_groups, ws, Y);
 }
 
 static int round_rows(int64_t m) {
@@ -476,6 +661,28 @@ static bool skinny_m_on_tc(olc_dtype dt, const Problem& p) {
     return p.M >= 4 || (p.M >= 2 && b_bytes >= 256.0 * 1024 * 1024);
 }
 
+// E4M3FN / E5M2: the warp-MMA kernel from 4 rows, the SIMT kernel below
+// (measured on GB300 for one [8192, 28672] B, TB/s, SIMT against MMA: 1 row
+// 5.8 / 3.5, 2 rows 4.1 / 3.5, 4 rows 2.9 / 3.5, 16 rows 0.8 / 3.5); variant
+// 1 forces the SIMT kernel, variant 2 the MMA kernel.
+static bool skinny_m_on_f8_mma(olc_dtype dt, const Problem& p) {
+    if (!(dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2) || p.M > 16 || p.N % 16 != 0) return false;
+    if (p.variant == 1) return false;
+    if (p.variant == 2) return true;
+    return p.M >= 4;
+}
+
+template <int FMT>
+static int f8_mma_occupancy() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, skinny_m_f8_mma_kernel<FMT>, kF8MmaWarps * 32, 0) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    return n > 0 ? n : 4;   // no device visible: assume four resident blocks
+}
+
 static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count);
 
 int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
@@ -485,10 +692,15 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
 
 static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
     if (p.split_hint > 0) return (int)min64(p.split_hint, max64(1, p.K / 8));
-    const int64_t groups = skinny_m_col_groups(dt, p.M, p.N) * p.items;
-    const int64_t slots = (int64_t)sm_count * skinny_m_blocks_per_sm(dt, p.M);
+    const bool mma = skinny_m_on_f8_mma(dt, p);
+    const int64_t cols = mma ? kF8MmaCols : 32 * skinny_m_vec(dt, p.M);
+    const int64_t groups = ceil_div(p.N, cols) * p.items;
+    const int64_t slots = (int64_t)sm_count *
+                          (mma ? (dt == OLC_FLOAT8E4M3FN ? f8_mma_occupancy<0>() : f8_mma_occupancy<1>())
+                               : skinny_m_blocks_per_sm(dt, p.M));
     const int64_t eb = operand_bytes(dt);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
+    const int64_t rows = mma ? 16 : round_rows(p.M);
     const double stream_bytes = (double)p.K * p.N * eb * p.items;
     const int64_t smax = min64(64, max64(1, p.K / 256));
     int best = 1;
@@ -497,7 +709,7 @@ static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
         const int64_t blocks = groups * s;
         const int64_t waves = ceil_div(blocks, slots);
         const double fill = (double)blocks / (double)(waves * slots);
-        const double extra = s > 1 ? 2.0 * (double)s * round_rows(p.M) * p.N * acc * p.items : 0.0;
+        const double extra = s > 1 ? 2.0 * (double)s * rows * p.N * acc * p.items : 0.0;
         const double score = fill * stream_bytes / (stream_bytes + extra);
         if (score > best_score + 1e-9) {
             best_score = score;
@@ -509,6 +721,8 @@ static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
 
 size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_partial_bytes(p, sm_count);
+    if (skinny_m_on_f8_mma(dt, p))
+        return (size_t)(ceil_div(p.N, kF8MmaCols) * p.items * ksplit * 16 * kF8MmaCols * 4);
     const int64_t acc = dt == OLC_DOUBLE ? 8 : 4;
     const int64_t entries = round_rows(p.M) * 32 * skinny_m_vec(dt, p.M);
     return (size_t)(skinny_m_col_groups(dt, p.M, p.N) * p.items * ksplit * entries * acc);
@@ -517,6 +731,7 @@ size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm
 size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
     (void)ksplit;
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_counter_count(p, sm_count);
+    if (skinny_m_on_f8_mma(dt, p)) return (size_t)(ceil_div(p.N, kF8MmaCols) * p.items);
     return (size_t)(skinny_m_col_groups(dt, p.M, p.N) * p.items);
 }
 
@@ -541,9 +756,28 @@ static cudaError_t launch_skinny_m_t(const Problem& p, int ksplit, const Workspa
     return cudaGetLastError();
 }
 
+template <int FMT>
+static cudaError_t launch_skinny_m_f8_mma(const Problem& p, int ksplit, const Workspace& ws, cudaStream_t s) {
+    const int64_t groups = ceil_div(p.N, kF8MmaCols);
+    const int64_t kslice = ceil_div(ceil_div(p.K, ksplit), 32) * 32;
+    const int64_t blocks = groups * ksplit * p.items;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (ksplit > 1 && (!ws.partials || !ws.counters)) return cudaErrorInvalidValue;
+    // 4-byte A loads need every A row (and each operand item) 4-byte aligned
+    bool a_vec_ok = p.K % 4 == 0 && (reinterpret_cast<uintptr_t>(p.A) % 4) == 0;
+    for (int d = 0; d < p.map.rank; ++d)
+        if (p.map.a_stride[d] % 4 != 0) a_vec_ok = false;
+    skinny_m_f8_mma_kernel<FMT><<<(unsigned)blocks, kF8MmaWarps * 32, 0, s>>>(p, groups, ksplit, kslice, ws,
+                                                                             a_vec_ok ? 1 : 0);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_count,
                             const Workspace& ws, cudaStream_t s) {
     if (skinny_m_on_tc(dt, p)) return launch_tc_skinny_m(dt, p, sm_count, ws, s);
+    if (skinny_m_on_f8_mma(dt, p))
+        return dt == OLC_FLOAT8E4M3FN ? launch_skinny_m_f8_mma<0>(p, ksplit, ws, s)
+                                      : launch_skinny_m_f8_mma<1>(p, ksplit, ws, s);
     const int mr = round_rows(p.M);
     return dispatch_skinny_m(dt, cudaErrorInvalidValue, [&](auto tag) -> cudaError_t {
         using T = decltype(tag);

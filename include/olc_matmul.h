@@ -403,8 +403,11 @@ int olc_matmul_plan_splits(const olc_matmul_plan* plan);
  * all rows, K a multiple of 8, B^T within its shared-memory budget).
  * SKINNY_M plans of FLOAT16 / BFLOAT16: 0 = automatic (tensor cores from 4
  * rows, or from 2 rows with a B of 256 MB or more), 1 = the SIMT streaming
- * kernel, 2 = the swapped-operand tcgen05 kernel.  GENERAL_TC plans of 8-bit
- * floats: 1 = one CTA per 128 x 256 tile instead of CTA pairs.
+ * kernel, 2 = the swapped-operand tcgen05 kernel.  SKINNY_M plans of
+ * FLOAT8E4M3FN / FLOAT8E5M2: 0 = automatic (the warp-level MMA kernel from 4
+ * rows), 1 = the SIMT streaming kernel, 2 = the warp-level MMA kernel
+ * (mma.sync m16n8k32 on B fragments transposed in registers).  GENERAL_TC
+ * plans of 8-bit floats: 1 = one CTA per 128 x 256 tile instead of CTA pairs.
  * Results are identical within the parity tolerance either way.  Errors:
  * OLC_ERR_NULL, OLC_ERR_INVALID. */
 olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant);

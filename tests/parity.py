@@ -21,15 +21,17 @@ TOL = {"float32": 1e-5, "float64": 1e-12, "float16": 2e-3, "bfloat16": 1e-2,
 
 
 def gpu_matmul(a_cpu: torch.Tensor, b_cpu: torch.Tensor, dtype: str, algorithm=None,
-               checked=True, guard=64):
-    """Y = MatMul(A, B) through the library; Y is allocated with `guard`
-    trailing canary elements that must stay untouched.  Returns (Y on CPU,
-    plan algorithm)."""
+               checked=True, guard=64, variant=None):
+    """Y = MatMul(A, B) through the library (kernel-family override `variant`
+    if given); Y is allocated with `guard` trailing canary elements that must
+    stay untouched.  Returns (Y on CPU, plan algorithm)."""
     A = a_cpu.cuda()
     B = b_cpu.cuda()
     with Plan(a_cpu.shape, b_cpu.shape, dtype) as p:
         if algorithm is not None:
             p.force(algorithm)
+        if variant is not None:
+            p.set_tc_variant(variant)
         shape = p.output_shape
         n = int(np.prod(shape, dtype=np.int64))
         buf = torch.full((n + guard,), float("nan"), dtype=synth.TORCH_DTYPES[synth.output_dtype(dtype)], device="cuda")
@@ -67,8 +69,8 @@ def compare(y_gpu: torch.Tensor, y_ref: np.ndarray, s: np.ndarray, dtype: str, e
     return float(r.max()) if r.size else 0.0
 
 
-def check_product(a_cpu, b_cpu, dtype, algorithm=None, exact=False):
-    y, algo = gpu_matmul(a_cpu, b_cpu, dtype, algorithm)
+def check_product(a_cpu, b_cpu, dtype, algorithm=None, exact=False, variant=None):
+    y, algo = gpu_matmul(a_cpu, b_cpu, dtype, algorithm, variant=variant)
     y_ref, s = oracle.matmul(synth.to_numpy_storage(a_cpu), synth.to_numpy_storage(b_cpu), dtype)
     compare(y, y_ref, s, dtype, exact=exact)
     return y, algo

@@ -188,20 +188,28 @@ SKINNY_SHAPES = [
 ]
 
 
+SKINNY_VARIANTS = {"auto": 0, "simt": 1, "mma": 2}
+
+
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
 @pytest.mark.parametrize("shapes", SKINNY_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
-def test_fp8_skinny_m(dtype, shapes):
-    """Up to 16 rows: the SIMT streaming kernel (16, 8 or 4 one-byte B
-    elements per lane load, decoded to float32), chosen automatically from
-    N >= 256; A rows that are not 8-byte aligned take element loads."""
+@pytest.mark.parametrize("variant", list(SKINNY_VARIANTS), ids=list(SKINNY_VARIANTS))
+def test_fp8_skinny_m(dtype, shapes, variant):
+    """Up to 16 rows, chosen automatically from N >= 256: the SIMT streaming
+    kernel (16, 8 or 4 one-byte B elements per lane load, decoded to float32;
+    A rows that are not 8-byte aligned take element loads) and, for E4M3FN
+    and E5M2, the warp-level MMA kernel (m16n8k32, B fragments transposed in
+    registers; automatic from 4 rows).  The FNUZ formats take the SIMT kernel
+    whatever the variant."""
     a_shape, b_shape = shapes
     with Plan(a_shape, b_shape, dtype) as p:
         if b_shape[-1] >= 256:
             assert p.algorithm == "skinny_m"
+    v = SKINNY_VARIANTS[variant]
     a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 48)
-    check_product(a, b, dtype, algorithm="skinny_m")
+    check_product(a, b, dtype, algorithm="skinny_m", variant=v)
     ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 49)
-    check_product(ai, bi, dtype, algorithm="skinny_m", exact=True)
+    check_product(ai, bi, dtype, algorithm="skinny_m", exact=True, variant=v)
 
 
 ONE = {"float8_e4m3fn": 0x38, "float8_e5m2": 0x3C, "float8_e4m3fnuz": 0x40, "float8_e5m2fnuz": 0x40}
@@ -209,7 +217,8 @@ ONE = {"float8_e4m3fn": 0x38, "float8_e5m2": 0x3C, "float8_e4m3fnuz": 0x40, "flo
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
 @pytest.mark.parametrize("m", [2, 4, 16])
-def test_fp8_skinny_m_decodes_every_pattern(dtype, m):
+@pytest.mark.parametrize("variant", [1, 2], ids=["simt", "mma"])
+def test_fp8_skinny_m_decodes_every_pattern(dtype, m, variant):
     """Every one of the 256 patterns through the skinny kernel's B decode
     (16, 8 or 4 one-byte columns per lane for 2, 4 or 16 rows; element i of a
     vector in byte i): Y row 0 = 1.0 x B row 0 (patterns 0..255), Y row 1 =
@@ -225,6 +234,7 @@ def test_fp8_skinny_m_decodes_every_pattern(dtype, m):
     ta, tb = synth.from_numpy_storage(a8, dtype), synth.from_numpy_storage(b8, dtype)
     with Plan(ta.shape, tb.shape, dtype) as p:
         p.force("skinny_m")
+        p.set_tc_variant(variant)
         Y = torch.empty(m, 256, device="cuda")
         p.execute_checked(ta.cuda(), tb.cuda(), Y)
         torch.cuda.synchronize()
@@ -235,7 +245,8 @@ def test_fp8_skinny_m_decodes_every_pattern(dtype, m):
 
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
-def test_fp8_skinny_m_decodes_every_a_pattern(dtype):
+@pytest.mark.parametrize("variant", [1, 2], ids=["simt", "mma"])
+def test_fp8_skinny_m_decodes_every_a_pattern(dtype, variant):
     """Every pattern through the skinny kernel's A decode (A rows kept as
     packed bytes, decoded two k positions at a time): A[i, k] = 16 i + k for
     16 rows and K = 16, B[k, j] = 1.0 where j == k < 16, else 0.  Y[i, j] =
@@ -252,6 +263,7 @@ def test_fp8_skinny_m_decodes_every_a_pattern(dtype):
     ta, tb = synth.from_numpy_storage(a8, dtype), synth.from_numpy_storage(b8, dtype)
     with Plan(ta.shape, tb.shape, dtype) as p:
         p.force("skinny_m")
+        p.set_tc_variant(variant)
         Y = torch.empty(16, 256, device="cuda")
         p.execute_checked(ta.cuda(), tb.cuda(), Y)
         torch.cuda.synchronize()
