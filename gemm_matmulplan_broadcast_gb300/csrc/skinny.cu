@@ -521,11 +521,14 @@ skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice
     // B rows kc + 4t + j (j < 4) and kc + 16 + 4t + j of the lane's columns,
     // and the A fragment; rows at or past k1 (another warp's range, or past
     // K) read as zeros
+    const unsigned char* __restrict__ Bl = B + (int64_t)(4 * t) * N + col0;   // row 4t, lane's columns
     auto load_chunk = [&](int64_t kc, F8Chunk& c) {
+        const unsigned char* bk = Bl + kc * N;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int64_t r = kc + (j < 4 ? 4 * t + j : 16 + 4 * t + (j - 4));
-            c.b[j] = (col_ok && r < k1) ? __ldg(reinterpret_cast<const uint2*>(B + r * N + col0))
+            const int dr = j < 4 ? j : 16 + (j - 4);
+            const int64_t r = kc + 4 * t + dr;
+            c.b[j] = (col_ok && r < k1) ? __ldg(reinterpret_cast<const uint2*>(bk + (int64_t)dr * N))
                                         : make_uint2(0u, 0u);
         }
         if (kc < k1) {
@@ -663,7 +666,7 @@ static bool skinny_m_on_tc(olc_dtype dt, const Problem& p) {
 
 // E4M3FN / E5M2: the warp-MMA kernel from 4 rows, the SIMT kernel below
 // (measured on GB300 for one [8192, 28672] B, TB/s, SIMT against MMA: 1 row
-// 5.8 / 3.5, 2 rows 4.1 / 3.5, 4 rows 2.9 / 3.5, 16 rows 0.8 / 3.5); variant
+// 5.8 / 3.7, 2 rows 4.1 / 3.7, 4 rows 2.9 / 3.7, 16 rows 0.8 / 3.6); variant
 // 1 forces the SIMT kernel, variant 2 the MMA kernel.
 static bool skinny_m_on_f8_mma(olc_dtype dt, const Problem& p) {
     if (!(dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2) || p.M > 16 || p.N % 16 != 0) return false;

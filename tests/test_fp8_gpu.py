@@ -185,6 +185,8 @@ SKINNY_SHAPES = [
     ((16, 4096), (4096, 1024)),        # 16 rows: 4 columns per lane
     ((6, 1001), (1001, 256)),          # A rows not 8-byte aligned: element loads
     ((12, 999), (999, 512)),           # the same with 16 rows
+    ((2, 5, 256), (2, 256, 512)),      # batched B: 2 items of 5 rows
+    ((3, 1, 12, 64), (1, 2, 64, 256)), # broadcast on both sides: 6 items of 12 rows
 ]
 
 
