@@ -121,6 +121,21 @@ int64_t numel(const int64_t* s, int r) {
     return n;
 }
 
+// Largest tensor the plans accept, in bytes: 2^62, so that every element and
+// byte offset the kernels form (and sums of two of them) fits in int64.
+constexpr int64_t kMaxTensorBytes = int64_t(1) << 62;
+
+// true when the tensor of these extents, `elem` bytes per element, stays
+// within kMaxTensorBytes (an extent of 0 makes it empty, which always fits)
+bool tensor_fits(const int64_t* s, int r, int64_t elem) {
+    for (int i = 0; i < r; ++i)
+        if (s[i] == 0) return true;
+    int64_t n = elem;
+    for (int i = 0; i < r; ++i)
+        if (__builtin_mul_overflow(n, s[i], &n) || n > kMaxTensorBytes) return false;
+    return true;
+}
+
 Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, void* Y,
                      const void* C = nullptr, const void* R = nullptr) {
     Problem pr;
@@ -429,6 +444,8 @@ olc_status olc_matmul_plan_create(const int64_t* a_shape, int a_rank, const int6
         if (a_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
     for (int i = 0; i < b_rank; ++i)
         if (b_shape[i] < 0) return OLC_ERR_NEGATIVE_DIM;
+    if (!tensor_fits(a_shape, a_rank, elem_bytes(dtype)) || !tensor_fits(b_shape, b_rank, elem_bytes(dtype)))
+        return OLC_ERR_INVALID;
 
     olc_matmul_plan* p = new (std::nothrow) olc_matmul_plan;
     if (!p) return OLC_ERR_OOM;
@@ -487,6 +504,7 @@ olc_status olc_matmul_plan_create(const int64_t* a_shape, int a_rank, const int6
     if (a_rank > 1) p->out_shape[p->out_rank++] = p->M;
     if (b_rank > 1) p->out_shape[p->out_rank++] = p->N;
     if (p->out_rank > OLC_MAX_RANK) { delete p; return OLC_ERR_RANK; }
+    if (!tensor_fits(p->out_shape, p->out_rank, out_bytes(dtype))) { delete p; return OLC_ERR_INVALID; }
 
     // 4. collapse and fold the batch, then choose the algorithm
     collapse_and_fold(p);
@@ -533,6 +551,10 @@ olc_status olc_gemm_plan_create(const int64_t* a_shape, const int64_t* b_shape, 
     if (c_rank == 2) c2[0] = c_shape[0];
     if (c_rank >= 0 && (!(c2[0] == 1 || c2[0] == M) || !(c2[1] == 1 || c2[1] == N)))
         return OLC_ERR_BATCH_MISMATCH;   // C does not broadcast to [M, N]
+    const int64_t y_shape[2] = {M, N};
+    if (!tensor_fits(a_shape, 2, elem_bytes(dtype)) || !tensor_fits(b_shape, 2, elem_bytes(dtype)) ||
+        !tensor_fits(y_shape, 2, elem_bytes(dtype)))
+        return OLC_ERR_INVALID;
 
     olc_matmul_plan* p = new (std::nothrow) olc_matmul_plan;
     if (!p) return OLC_ERR_OOM;

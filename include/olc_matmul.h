@@ -127,8 +127,10 @@ typedef struct olc_matmul_plan olc_matmul_plan;
  *      olc_matmul_plan_destroy).  Set to NULL on error.
  *
  * Errors: OLC_ERR_NULL, OLC_ERR_RANK, OLC_ERR_NEGATIVE_DIM, OLC_ERR_K_MISMATCH,
- * OLC_ERR_BATCH_MISMATCH, OLC_ERR_DTYPE, OLC_ERR_OOM (host or workspace
- * allocation), OLC_ERR_CUDA.  If a CUDA device is present and the chosen
+ * OLC_ERR_BATCH_MISMATCH, OLC_ERR_DTYPE, OLC_ERR_INVALID (A, B or Y would
+ * hold more than 2^62 bytes, so that element offsets could overflow int64),
+ * OLC_ERR_OOM (host or workspace allocation), OLC_ERR_CUDA.  If a CUDA
+ * device is present and the chosen
  * algorithm needs a split reduction workspace, it is allocated here
  * (cudaMalloc on the current device) and owned by the plan.
  */
@@ -222,7 +224,8 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan,
  * epilogue in float32 and narrow once.  With K == 0, Y = beta * C.
  * Errors: OLC_ERR_NULL, OLC_ERR_RANK (c_rank outside -1..2),
  * OLC_ERR_NEGATIVE_DIM, OLC_ERR_K_MISMATCH, OLC_ERR_BATCH_MISMATCH (C does
- * not broadcast to [M, N]), OLC_ERR_DTYPE, OLC_ERR_OOM, OLC_ERR_CUDA.
+ * not broadcast to [M, N]), OLC_ERR_DTYPE, OLC_ERR_INVALID (A, B or Y would
+ * hold more than 2^62 bytes), OLC_ERR_OOM, OLC_ERR_CUDA.
  * Free with olc_matmul_plan_destroy; the query functions below apply.
  */
 olc_status olc_gemm_plan_create(const int64_t* a_shape, const int64_t* b_shape, int trans_a,

@@ -12,6 +12,7 @@ import pytest
 import oracle
 from gemm_matmulplan_broadcast_gb300 import Plan, binding
 from gemm_matmulplan_broadcast_gb300.binding import OlcError
+from gemm_matmulplan_broadcast_gb300 import GemmPlan
 
 from test_oracle_pins import _golden_shapes
 
@@ -120,6 +121,28 @@ def test_create_errors(bad, status):
     with pytest.raises(OlcError) as ei:
         Plan(bad[0], bad[1], "float32")
     assert ei.value.name == status
+
+
+def test_create_rejects_sizes_whose_offsets_overflow():
+    """Operands or outputs of more than 2^62 bytes are refused before any
+    allocation (their element offsets could overflow int64); a zero extent
+    makes a tensor empty whatever its other extents."""
+    big = 1 << 31
+    for a, b in [((big, big), (big, 4)),                 # A: 2^62 elements x 4 bytes
+                 ((4, 8), (8, big, big)),               # B batch dims
+                 ((big, 2), (2, big))]:                 # Y only
+        with pytest.raises(OlcError) as ei:
+            Plan(a, b, "float32")
+        assert ei.value.name == "OLC_ERR_INVALID"
+    with pytest.raises(OlcError) as ei:
+        GemmPlan((big, big), (big, 2), "float16")
+    assert ei.value.name == "OLC_ERR_INVALID"
+    # 2^61 bytes of FP16 output: accepted (nothing is allocated for Y)
+    with Plan((1 << 30, 2), (2, 1 << 30), "float16") as p:
+        assert p.output_shape == (1 << 30, 1 << 30)
+    # empty: a zero extent next to huge ones
+    with Plan((0, big, big), (big, 4), "float32") as p:
+        assert p.algorithm == "empty"
 
 
 def test_create_rejects_rank0_null_and_bad_dtype():
