@@ -268,7 +268,12 @@ olc_status grouped_bind(olc_grouped_plan* p) {
     if (cudaGetDevice(&cur) != cudaSuccess) return grouped_from_cuda(cudaErrorNoDevice);
     if (p->device >= 0) return cur == p->device ? OLC_OK : OLC_ERR_WRONG_DEVICE;
     // the descriptor table and, for every tile, the member that owns it
-    std::vector<int> owner((size_t)p->total_tiles);
+    std::vector<int> owner;
+    try {
+        owner.resize((size_t)p->total_tiles);
+    } catch (const std::bad_alloc&) {
+        return OLC_ERR_OOM;
+    }
     for (int i = 0; i < p->count; ++i) {
         const int64_t end = i + 1 < p->count ? p->desc[i + 1].tile_begin : p->total_tiles;
         for (int64_t t = p->desc[i].tile_begin; t < end; ++t) owner[(size_t)t] = i;
@@ -307,6 +312,22 @@ olc_status olc_grouped_plan_create(int count, const int64_t* m, const int64_t* n
     if (!grouped_dtype_ok(dtype)) return OLC_ERR_DTYPE;
     for (int i = 0; i < count; ++i)
         if (m[i] < 0 || n[i] < 0 || k[i] < 0) return OLC_ERR_NEGATIVE_DIM;
+    // every member's A, B and Y within 2^62 bytes (element offsets stay in
+    // int64), and all members' tiles numbered in an int owner table
+    const int64_t eb = (dtype == OLC_DOUBLE) ? 8 : (dtype == OLC_FLOAT) ? 4 : 2;
+    int64_t t = 0;
+    for (int i = 0; i < count; ++i) {
+        const int64_t pairs[3][2] = {{m[i], k[i]}, {k[i], n[i]}, {m[i], n[i]}};
+        for (const auto& d : pairs) {
+            int64_t bytes = 0;
+            if (d[0] != 0 && d[1] != 0 &&
+                (__builtin_mul_overflow(d[0], d[1], &bytes) || __builtin_mul_overflow(bytes, eb, &bytes) ||
+                 bytes > (int64_t(1) << 62)))
+                return OLC_ERR_INVALID;
+        }
+        t += olc::ceil_div(m[i], olc::kGBM) * olc::ceil_div(n[i], olc::kGBN);
+        if (t > 0x7fffffffLL) return OLC_ERR_INVALID;
+    }
     olc_grouped_plan* p = new (std::nothrow) olc_grouped_plan;
     if (!p) return OLC_ERR_OOM;
     p->dtype = dtype;
@@ -315,8 +336,13 @@ olc_status olc_grouped_plan_create(int count, const int64_t* m, const int64_t* n
     p->desc_dev = nullptr;
     p->owner_dev = nullptr;
     p->sm_count = 0;
-    p->desc.resize((size_t)count);
-    int64_t t = 0;
+    try {
+        p->desc.resize((size_t)count);
+    } catch (const std::bad_alloc&) {
+        delete p;
+        return OLC_ERR_OOM;
+    }
+    t = 0;
     for (int i = 0; i < count; ++i) {
         const int64_t tm = olc::ceil_div(m[i], olc::kGBM), tn = olc::ceil_div(n[i], olc::kGBN);
         p->desc[i] = olc::GDesc{m[i], n[i], k[i], t, tn > 0 ? tn : 1};

@@ -327,8 +327,9 @@ olc_status olc_matmul_execute_fused(const olc_matmul_plan* plan, const void* A, 
 typedef struct olc_grouped_plan olc_grouped_plan;
 
 /* m, n, k: host arrays of `count` dimensions (copied; the caller keeps
- * ownership).  Errors: OLC_ERR_NULL, OLC_ERR_INVALID (count <= 0),
- * OLC_ERR_NEGATIVE_DIM, OLC_ERR_DTYPE, OLC_ERR_OOM. */
+ * ownership).  Errors: OLC_ERR_NULL, OLC_ERR_INVALID (count <= 0, a
+ * member's A, B or Y above 2^62 bytes, or more than 2^31 - 1 output tiles of
+ * 64 x 64 in all), OLC_ERR_NEGATIVE_DIM, OLC_ERR_DTYPE, OLC_ERR_OOM. */
 olc_status olc_grouped_plan_create(int count, const int64_t* m, const int64_t* n, const int64_t* k,
                                    olc_dtype dtype, olc_grouped_plan** out);
 

@@ -286,6 +286,13 @@ def test_grouped_plan_host_checks():
     assert binding.STATUS[lib.olc_grouped_plan_create(3, m, n, k, 7, ctypes.byref(h))] == "OLC_ERR_DTYPE"
     bad = arr(64, -1, 3)
     assert binding.STATUS[lib.olc_grouped_plan_create(3, m, bad, k, 1, ctypes.byref(h))] == "OLC_ERR_NEGATIVE_DIM"
+    # a member above 2^62 bytes, or more than 2^31 - 1 tiles in all
+    big = arr(1 << 31, 1, 1)
+    assert binding.STATUS[lib.olc_grouped_plan_create(3, big, arr(1 << 31, 1, 1), k, 1,
+                                                      ctypes.byref(h))] == "OLC_ERR_INVALID"
+    assert binding.STATUS[lib.olc_grouped_plan_create(3, arr(1 << 22, 1, 1), arr(1 << 22, 1, 1), k, 10,
+                                                      ctypes.byref(h))] == "OLC_ERR_INVALID"
+    assert h.value is None
     assert lib.olc_grouped_plan_create(3, m, n, k, 1, ctypes.byref(h)) == 0
     assert lib.olc_grouped_plan_tiles(h) == 1 + 2 + 0      # a 0-row member owns no tiles
     assert lib.olc_grouped_plan_count(h) == 3
