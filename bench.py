@@ -693,6 +693,7 @@ def run_ours(args):
         if args.full_secondary:
             names.append("float64_square_chain")
         names.append("fp8_transformer_projection")
+        names.append("fp8_skinny_decode")
         for wname in names:
             secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)

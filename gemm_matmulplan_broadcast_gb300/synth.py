@@ -242,6 +242,18 @@ def _fp16_corners() -> Workload:
         ))
 
 
+def _fp8_decode() -> Workload:
+    a, w = normal(1.0), normal(0.5)
+    return Workload(
+        "fp8_skinny_decode",
+        "E4M3FN few-row products against one large weight, A ~ N(0,1) x B ~ N(0,0.5) "
+        "(cast RNE), seed 3: [1,8192], [4,8192] and [16,8192] x [8192,28672]; "
+        "float32 accumulation, FLOAT output",
+        products=tuple(
+            Product("fp8_rows_%d" % m, (m, 8192), (8192, 28672), "float8_e4m3fn", a, w, 3)
+            for m in (1, 4, 16)))
+
+
 def _square_sweep(dtype: str) -> Workload:
     u = UNIFORM
     return Workload(
@@ -258,7 +270,7 @@ def _square_sweep(dtype: str) -> Workload:
 def workloads():
     """All named workloads, smallest first."""
     return [_fp32_small(), _fp32_broadcast(), _bf16_projection(), _fp16_corners(),
-            _square_sweep("float32"), _square_sweep("float64"), _fp8_projection()]
+            _square_sweep("float32"), _square_sweep("float64"), _fp8_projection(), _fp8_decode()]
 
 
 def workload(name: str) -> Workload:

@@ -141,7 +141,15 @@ def encode(values: np.ndarray, dtype: str) -> np.ndarray:
 
 def decode_fp8(bits: np.ndarray, dtype: str) -> np.ndarray:
     """uint8 patterns of an 8-bit float format -> exact float32 values,
-    written from the format's fields."""
+    written from the format's fields (decode_fp8_fields), looked up from
+    the 256 decoded patterns so that large operands cost one gather."""
+    table = decode_fp8_fields(np.arange(256, dtype=np.uint8), dtype)
+    return table[np.asarray(bits, dtype=np.uint8)]
+
+
+def decode_fp8_fields(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """uint8 patterns of an 8-bit float format -> exact float32 values,
+    decoded element by element from the sign, exponent and mantissa fields."""
     b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
     sign = np.where(b & 0x80, -1.0, 1.0)
     if dtype == "float8_e4m3fn":

@@ -273,3 +273,13 @@ def test_fp8_skinny_m_decodes_every_a_pattern(dtype, variant):
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(y), nan)
     assert np.array_equal(y[~nan], ref[~nan])
+
+
+def test_fp8_skinny_decode_workload_full():
+    """The named FP8 few-row workload at full size ([1|4|16, 8192] x [8192,
+    28672]): SKINNY_M chosen, every element against the oracle."""
+    w = synth.workload("fp8_skinny_decode")
+    for prod in w.products:
+        a, b = prod.draw()
+        y, algo = check_product(a, b, prod.dtype)
+        assert algo == "skinny_m"

@@ -58,3 +58,15 @@ def test_fp8_matmul_integer_exact(dtype):
         want = np.array(_brute(an[z], bn), dtype=np.float64)
         assert np.array_equal(y[z].astype(np.float64), want)
         assert np.all(s[z] >= np.abs(want))
+
+
+@pytest.mark.parametrize("dtype", oracle.FP8_DTYPES)
+def test_lookup_decode_equals_field_decode(dtype):
+    """The oracle decodes large operands by looking up the 256 patterns that
+    the field decode produces; both give the same values (NaN where NaN) in
+    the input's shape."""
+    bits = np.random.default_rng(11).integers(0, 256, (37, 129), dtype=np.uint8)
+    got = oracle.decode_fp8(bits, dtype)
+    want = oracle.decode_fp8_fields(bits, dtype)
+    assert got.shape == bits.shape and got.dtype == np.float32
+    assert np.array_equal(got, want, equal_nan=True)
