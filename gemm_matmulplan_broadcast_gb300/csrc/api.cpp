@@ -225,6 +225,10 @@ bool feasible(const olc_matmul_plan* p, int algo) {
             case OLC_ALGO_GENERAL_SIMT: return n > 0 && K > 0;
             case OLC_ALGO_SKINNY_M:     // 16 one-byte B elements per vector
                 return n > 0 && K > 0 && rows <= skinny_m_max_rows() && N % 16 == 0;
+            case OLC_ALGO_SPLIT_K: {    // warp-MMA split-K: small outputs
+                Problem pr = make_problem(p, nullptr, nullptr, nullptr);
+                return n > 0 && f8_split_k_ok(p->dtype, pr);
+            }
             case OLC_ALGO_GENERAL_TC: {
                 Problem pr = make_problem(p, nullptr, nullptr, nullptr);
                 return n > 0 && K > 0 && is_fp8_tc_format(p->dtype) && fp8_tc_ok(pr);
@@ -263,6 +267,11 @@ int choose_algorithm(const olc_matmul_plan* p) {
         const double macs = (double)p->rows * (double)p->N * (double)p->K * (double)p->items;
         if (p->rows <= skinny_m_max_rows() && p->N >= 256 && feasible(p, OLC_ALGO_SKINNY_M))
             return OLC_ALGO_SKINNY_M;
+        // the split-K corner, as for the other types: too few output tiles to
+        // fill half the SMs, and a long K
+        const int64_t tiles = ((p->rows + 127) / 128) * ((p->N + 127) / 128) * p->items;
+        if (tiles * 2 <= p->sm_count && p->K >= 8 * 1024 && feasible(p, OLC_ALGO_SPLIT_K))
+            return OLC_ALGO_SPLIT_K;
         if (macs >= 4.0 * 1024 * 1024 && feasible(p, OLC_ALGO_GENERAL_TC)) return OLC_ALGO_GENERAL_TC;
         return macs < 4.0 * 1024 * 1024 ? OLC_ALGO_DIRECT : OLC_ALGO_GENERAL_SIMT;
     }
@@ -400,6 +409,8 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         const void* bt = (p->const_bt && B == p->const_b) ? p->const_bt : nullptr;
         if (algo == OLC_ALGO_SKINNY_M)
             e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
+        else if (algo == OLC_ALGO_SPLIT_K)
+            e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
         else
             e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s, bt)
                                             : launch_fp8_simt(dt, pr, s);

@@ -118,6 +118,15 @@ cudaError_t launch_split_k_simt(olc_dtype dt, const Problem& p, int splits, cons
                                 cudaStream_t stream);
 int split_k_simt_pick(olc_dtype dt, const Problem& p, int sm_count);
 
+// SPLIT_K for E4M3FN / E5M2 with at most 32 rows and 128 columns (N a
+// multiple of 16): warp-level MMA over K slices, two fixed-order levels.
+bool f8_split_k_ok(olc_dtype dt, const Problem& p);
+int f8_split_k_pick(const Problem& p, int sm_count);
+size_t f8_split_k_partial_bytes(const Problem& p, int splits);
+size_t f8_split_k_counter_count(const Problem& p, int splits);
+cudaError_t launch_f8_split_k(olc_dtype dt, const Problem& p, int splits, const Workspace& ws,
+                              cudaStream_t stream);
+
 // 8-bit float operands (FLOAT output): SIMT decode kernel for any shape and
 // batch; tcgen05 kind::f8f6f4 kernel for one item with K % 16 == 0 and
 // N % 4 == 0 (B transposed into the workspace first)

@@ -465,20 +465,125 @@ __device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uin
     out[3] = __byte_perm(x2, y2, 0x7632);
 }
 
-// one chunk's operands in a lane: 8 B rows of 8 bytes, the A fragment
+// one chunk's operands in a lane: 8 B rows of 8 bytes, the A fragments of
+// MT 16-row tiles
+template <int MT>
 struct F8Chunk {
     uint2 b[8];
-    uint32_t a[4];
+    uint32_t a[MT][4];
 };
 
-template <int FMT>
-__global__ void __launch_bounds__(kF8MmaWarps * 32, 3)
-skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Workspace ws,
+// acc[q] = sum over slices t = 0..n-1 (ascending) of src[t * stride + q * NT]
+// for this thread's entries (ok[q]; others give 0); the loads of UNR slices
+// are issued together, so a sum over many slices costs n / UNR round trips
+// to L2 instead of n.
+template <int Q, int NT, int UNR = 4>
+__device__ __forceinline__ void sum_slices(float (&acc)[Q], const float* __restrict__ src, int n, int64_t stride,
+                                           const bool (&ok)[Q]) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) acc[q] = ok[q] ? __ldcg(src + q * NT) : 0.0f;
+    int t = 1;
+    for (; t + UNR <= n; t += UNR) {
+        float x[UNR][Q];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+#pragma unroll
+            for (int q = 0; q < Q; ++q) x[u][q] = ok[q] ? __ldcg(src + (int64_t)(t + u) * stride + q * NT) : 0.0f;
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+#pragma unroll
+            for (int q = 0; q < Q; ++q) acc[q] += x[u][q];
+    }
+    for (; t < n; ++t)
+#pragma unroll
+        for (int q = 0; q < Q; ++q) acc[q] += ok[q] ? __ldcg(src + (int64_t)t * stride + q * NT) : 0.0f;
+}
+
+// Two-level end of a split over K (sgroup > 0): each block files its partial
+// tile; the last block of each group of sgroup consecutive slices (an atomic
+// count) adds the group's partials in slice order into a group sum; the last
+// group to finish adds the group sums in group order and stores through the
+// epilogue.  Fixed orders at both levels, so results are reproducible run to
+// run; one level would leave a single block reading every slice's partial.
+// Workspace: partials [tiles][ksplit][ENTRIES], then group sums
+// [tiles][groups][ENTRIES]; counters [tiles][groups + 1], zero between
+// launches (the last arrivals reset them).  Only columns below N are filed
+// and summed.
+template <typename T, int MR, int COLS, int KW>
+__device__ __forceinline__ void skinny_m_finish_grouped(const Problem& p, const float (&red)[KW][MR][COLS],
+                                                        unsigned int& am_last, int64_t item, int64_t cg,
+                                                        int split, int ksplit, int sgroup, int64_t col_groups,
+                                                        const Workspace& ws, float* __restrict__ Y) {
+    constexpr int NT = KW * 32;
+    constexpr int ENTRIES = MR * COLS;
+    static_assert(ENTRIES % NT == 0, "whole entries per thread");
+    constexpr int Q = ENTRIES / NT;
+    const int64_t M = p.M, N = p.N;
+    const int ncols = (int)min64(COLS, N - cg * COLS);
+    const int64_t tile = item * col_groups + cg;
+    const int64_t tiles = col_groups * p.items;
+    const int groups = (ksplit + sgroup - 1) / sgroup;
+    float* P = static_cast<float*>(ws.partials);
+    float* G = P + tiles * ksplit * ENTRIES;
+    unsigned int* cnt = ws.counters + tile * (groups + 1);
+
+    bool ok[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) ok[q] = (threadIdx.x + q * NT) % COLS < ncols;
+    float* mine = P + (tile * ksplit + split) * ENTRIES;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int e = threadIdx.x + q * NT;
+        if (!ok[q]) continue;
+        const int i = e / COLS, c = e % COLS;
+        float v = red[0][i][c];
+#pragma unroll
+        for (int w = 1; w < KW; ++w) v += red[w][i][c];
+        mine[e] = v;
+    }
+    __threadfence();
+    __syncthreads();
+    const int grp = split / sgroup;
+    const int s0 = grp * sgroup, sn = min(sgroup, ksplit - s0);
+    if (threadIdx.x == 0) am_last = (atomicAdd(cnt + grp, 1u) == (unsigned int)sn - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+    float acc[Q];
+    sum_slices<Q, NT>(acc, P + (tile * ksplit + s0) * ENTRIES + threadIdx.x, sn, ENTRIES, ok);
+    float* gsum = G + (tile * groups + grp) * ENTRIES;
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+        if (ok[q]) gsum[threadIdx.x + q * NT] = acc[q];
+    if (threadIdx.x == 0) cnt[grp] = 0u;   // ready for the next launch
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) am_last = (atomicAdd(cnt + groups, 1u) == (unsigned int)groups - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!am_last) return;
+    __threadfence();
+#pragma unroll
+    for (int q = 0; q < Q; ++q) ok[q] = ok[q] && (threadIdx.x + q * NT) / COLS < M;
+    sum_slices<Q, NT>(acc, G + tile * groups * ENTRIES + threadIdx.x, groups, ENTRIES, ok);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        if (!ok[q]) continue;
+        const int e = threadIdx.x + q * NT;
+        const int i = e / COLS;
+        const int64_t col = cg * COLS + e % COLS;
+        Y[i * N + col] = apply_epilogue<float>(p.epi, acc[q], i, col, Y + i * N + col);
+    }
+    if (threadIdx.x == 0) cnt[groups] = 0u;
+}
+
+template <int FMT, int MT>
+__global__ void __launch_bounds__(kF8MmaWarps * 32, MT == 1 ? 3 : 2)
+skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, int sgroup, Workspace ws,
                        int a_vec_ok) {
     using T = F8<FMT>;
     constexpr int KW = kF8MmaWarps;
     constexpr int COLS = kF8MmaCols;
-    constexpr int MR = 16;
+    constexpr int MR = 16 * MT;
     constexpr int R = F8_RING;
     __shared__ float red[KW][MR][COLS];
     __shared__ unsigned int am_last;
@@ -522,7 +627,7 @@ skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice
     // and the A fragment; rows at or past k1 (another warp's range, or past
     // K) read as zeros
     const unsigned char* __restrict__ Bl = B + (int64_t)(4 * t) * N + col0;   // row 4t, lane's columns
-    auto load_chunk = [&](int64_t kc, F8Chunk& c) {
+    auto load_chunk = [&](int64_t kc, F8Chunk<MT>& c) {
         const unsigned char* bk = Bl + kc * N;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -532,20 +637,25 @@ skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice
                                         : make_uint2(0u, 0u);
         }
         if (kc < k1) {
-            c.a[0] = a_word(g, kc + 4 * t);
-            c.a[1] = a_word(g + 8, kc + 4 * t);
-            c.a[2] = a_word(g, kc + 16 + 4 * t);
-            c.a[3] = a_word(g + 8, kc + 16 + 4 * t);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                c.a[mt][0] = a_word(16 * mt + g, kc + 4 * t);
+                c.a[mt][1] = a_word(16 * mt + g + 8, kc + 4 * t);
+                c.a[mt][2] = a_word(16 * mt + g, kc + 16 + 4 * t);
+                c.a[mt][3] = a_word(16 * mt + g + 8, kc + 16 + 4 * t);
+            }
         }
     };
 
-    float d[8][4];
+    float d[MT][8][4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[q][i] = 0.0f;
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[mt][q][i] = 0.0f;
 
-    F8Chunk ring[R];
+    F8Chunk<MT> ring[R];
 #pragma unroll
     for (int r = 0; r < R - 1; ++r) load_chunk(k0 + 32 * r, ring[r]);
     for (int64_t kc = k0; kc < k1; kc += 32 * R) {
@@ -554,7 +664,7 @@ skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice
             const int64_t kcur = kc + 32 * r;
             load_chunk(kcur + 32 * (R - 1), ring[(r + R - 1) % R]);
             if (kcur < k1) {
-                const F8Chunk& c = ring[r];
+                const F8Chunk<MT>& c = ring[r];
                 // lo: K positions 4t..4t+3, hi: 16+4t..; [0]: columns 0-3, [1]: 4-7
                 uint32_t lo[2][4], hi[2][4];
                 transpose4x4_bytes(c.b[0].x, c.b[1].x, c.b[2].x, c.b[3].x, lo[0]);
@@ -562,22 +672,32 @@ skinny_m_f8_mma_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice
                 transpose4x4_bytes(c.b[4].x, c.b[5].x, c.b[6].x, c.b[7].x, hi[0]);
                 transpose4x4_bytes(c.b[4].y, c.b[5].y, c.b[6].y, c.b[7].y, hi[1]);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) mma_f8_m16n8k32<FMT>(d[q], c.a, lo[q / 4][q % 4], hi[q / 4][q % 4]);
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        mma_f8_m16n8k32<FMT>(d[mt][q], c.a[mt], lo[q / 4][q % 4], hi[q / 4][q % 4]);
             }
         }
     }
 
-    // MMA q's accumulator: rows g and g + 8, MMA columns 2t and 2t + 1, i.e.
-    // columns 8 (2t) + q and 8 (2t + 1) + q of the group
+    // MMA q's accumulator of tile mt: rows 16 mt + g and 16 mt + g + 8, MMA
+    // columns 2t and 2t + 1, i.e. columns 8 (2t) + q and 8 (2t + 1) + q of
+    // the group
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        red[warp][g][16 * t + q] = d[q][0];
-        red[warp][g][16 * t + 8 + q] = d[q][1];
-        red[warp][g + 8][16 * t + q] = d[q][2];
-        red[warp][g + 8][16 * t + 8 + q] = d[q][3];
-    }
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            red[warp][16 * mt + g][16 * t + q] = d[mt][q][0];
+            red[warp][16 * mt + g][16 * t + 8 + q] = d[mt][q][1];
+            red[warp][16 * mt + g + 8][16 * t + q] = d[mt][q][2];
+            red[warp][16 * mt + g + 8][16 * t + 8 + q] = d[mt][q][3];
+        }
     __syncthreads();
-    skinny_m_finish<T, MR, COLS, KW>(p, red, am_last, item, cg, split, ksplit, col_groups, ws, Y);
+    if (sgroup > 0 && ksplit > 1)
+        skinny_m_finish_grouped<T, MR, COLS, KW>(p, red, am_last, item, cg, split, ksplit, sgroup, col_groups, ws,
+                                                 Y);
+    else
+        skinny_m_finish<T, MR, COLS, KW>(p, red, am_last, item, cg, split, ksplit, col_groups, ws, Y);
 }
 
 static int round_rows(int64_t m) {
@@ -678,7 +798,7 @@ static bool skinny_m_on_f8_mma(olc_dtype dt, const Problem& p) {
 template <int FMT>
 static int f8_mma_occupancy() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, skinny_m_f8_mma_kernel<FMT>, kF8MmaWarps * 32, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, skinny_m_f8_mma_kernel<FMT, 1>, kF8MmaWarps * 32, 0) !=
         cudaSuccess) {
         cudaGetLastError();
         n = 0;
@@ -770,9 +890,64 @@ static cudaError_t launch_skinny_m_f8_mma(const Problem& p, int ksplit, const Wo
     bool a_vec_ok = p.K % 4 == 0 && (reinterpret_cast<uintptr_t>(p.A) % 4) == 0;
     for (int d = 0; d < p.map.rank; ++d)
         if (p.map.a_stride[d] % 4 != 0) a_vec_ok = false;
-    skinny_m_f8_mma_kernel<FMT><<<(unsigned)blocks, kF8MmaWarps * 32, 0, s>>>(p, groups, ksplit, kslice, ws,
+    skinny_m_f8_mma_kernel<FMT, 1><<<(unsigned)blocks, kF8MmaWarps * 32, 0, s>>>(p, groups, ksplit, kslice, 0, ws,
                                                                              a_vec_ok ? 1 : 0);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// SPLIT_K for E4M3FN / E5M2 products with small outputs (at most 32 rows and
+// 128 columns, N a multiple of 16): the warp-MMA kernel above with one or two
+// 16-row tiles, K cut into about one slice per SM, the partials summed in
+// two fixed-order levels (skinny_m_finish_grouped).
+
+constexpr int kF8SplitGroup = 16;   // slices per first-level group
+
+bool f8_split_k_ok(olc_dtype dt, const Problem& p) {
+    return (dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2) && p.M <= 32 && p.N % 16 == 0 && p.N <= 128 &&
+           p.K > 0;
+}
+
+int f8_split_k_pick(const Problem& p, int sm_count) {
+    const int64_t tiles = ceil_div(p.N, kF8MmaCols) * p.items;
+    int64_t s = p.split_hint > 0 ? p.split_hint : ceil_div(sm_count, tiles);
+    s = max64(1, min64(s, ceil_div(p.K, 32)));   // at least one 32-row chunk per slice
+    const int64_t kslice = ceil_div(ceil_div(p.K, s), 32) * 32;
+    return (int)ceil_div(p.K, kslice);           // no empty slices
+}
+
+size_t f8_split_k_partial_bytes(const Problem& p, int splits) {
+    const int64_t tiles = ceil_div(p.N, kF8MmaCols) * p.items;
+    return (size_t)(tiles * (splits + ceil_div(splits, kF8SplitGroup)) * 32 * kF8MmaCols * 4);
+}
+
+size_t f8_split_k_counter_count(const Problem& p, int splits) {
+    const int64_t tiles = ceil_div(p.N, kF8MmaCols) * p.items;
+    return (size_t)(tiles * (ceil_div(splits, kF8SplitGroup) + 1));
+}
+
+template <int FMT, int MT>
+static cudaError_t launch_f8_split_t(const Problem& p, int splits, const Workspace& ws, cudaStream_t s) {
+    const int64_t groups = ceil_div(p.N, kF8MmaCols);
+    const int64_t kslice = ceil_div(ceil_div(p.K, splits), 32) * 32;
+    const int64_t blocks = groups * splits * p.items;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (splits > 1 && (!ws.partials || !ws.counters || ws.partial_bytes < f8_split_k_partial_bytes(p, splits) ||
+                       ws.counter_count < f8_split_k_counter_count(p, splits)))
+        return cudaErrorInvalidValue;
+    bool a_vec_ok = p.K % 4 == 0 && (reinterpret_cast<uintptr_t>(p.A) % 4) == 0;
+    for (int d = 0; d < p.map.rank; ++d)
+        if (p.map.a_stride[d] % 4 != 0) a_vec_ok = false;
+    skinny_m_f8_mma_kernel<FMT, MT><<<(unsigned)blocks, kF8MmaWarps * 32, 0, s>>>(
+        p, groups, splits, kslice, kF8SplitGroup, ws, a_vec_ok ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f8_split_k(olc_dtype dt, const Problem& p, int splits, const Workspace& ws, cudaStream_t s) {
+    if (!f8_split_k_ok(dt, p)) return cudaErrorInvalidValue;
+    if (dt == OLC_FLOAT8E4M3FN)
+        return p.M <= 16 ? launch_f8_split_t<0, 1>(p, splits, ws, s) : launch_f8_split_t<0, 2>(p, splits, ws, s);
+    return p.M <= 16 ? launch_f8_split_t<1, 1>(p, splits, ws, s) : launch_f8_split_t<1, 2>(p, splits, ws, s);
 }
 
 cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_count,

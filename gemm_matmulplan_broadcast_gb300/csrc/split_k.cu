@@ -157,22 +157,31 @@ static bool split_on_tc(olc_dtype dt, const Problem& p) {
     return (dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) && tc_shape_ok(dt, p.N, p.K);
 }
 
+// 8-bit float operands: the warp-MMA split-K (E4M3FN / E5M2, small outputs)
+static bool is_f8(olc_dtype dt) {
+    return dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2 || dt == OLC_FLOAT8E4M3FNUZ ||
+           dt == OLC_FLOAT8E5M2FNUZ;
+}
+
 int split_k_pick(olc_dtype dt, const Problem& p, int sm_count) {
+    if (is_f8(dt)) return f8_split_k_pick(p, sm_count);
     return split_on_tc(dt, p) ? tc_split_pick(p, sm_count) : split_k_simt_pick(dt, p, sm_count);
 }
 
 size_t split_k_partial_bytes(olc_dtype dt, const Problem& p, int splits, int sm_count) {
+    if (is_f8(dt)) return splits > 1 ? f8_split_k_partial_bytes(p, splits) : 0;
     return split_on_tc(dt, p) ? tc_split_partial_bytes(p, sm_count)
                               : simt_partial_bytes(dt, p, splits);
 }
 
 size_t split_k_counter_count(olc_dtype dt, const Problem& p, int splits, int sm_count) {
-    (void)splits;
+    if (is_f8(dt)) return splits > 1 ? f8_split_k_counter_count(p, splits) : 0;
     return split_on_tc(dt, p) ? tc_split_counter_count(p, sm_count) : simt_counter_count(p);
 }
 
 cudaError_t launch_split_k(olc_dtype dt, const Problem& p, int splits, int sm_count,
                            const Workspace& ws, cudaStream_t s) {
+    if (is_f8(dt)) return launch_f8_split_k(dt, p, splits, ws, s);
     if (split_on_tc(dt, p)) return launch_tc_split(dt, p, sm_count, ws, s);
     return launch_split_k_simt(dt, p, splits, ws, s);
 }

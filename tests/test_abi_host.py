@@ -145,6 +145,26 @@ def test_create_rejects_sizes_whose_offsets_overflow():
         assert p.algorithm == "empty"
 
 
+def test_fp8_split_k_choice_and_workspace():
+    """FP8 products with small outputs and long K plan the warp-MMA split-K
+    (about one slice per SM, a workspace for both reduction levels); the
+    FNUZ formats, columns not a multiple of 16 and more than 32 rows do not
+    take it."""
+    with Plan((32, 131072), (131072, 32), "float8_e4m3fn") as p:
+        assert p.algorithm == "split_k"
+        s = p.splits
+        assert 16 < s <= 152
+        groups = -(-s // 16)
+        assert p.workspace_bytes >= (s + groups) * 32 * 64 * 4 + (groups + 1) * 4
+    for a, b, dt in [((32, 131072), (131072, 32), "float8_e4m3fnuz"),
+                     ((32, 131072), (131072, 24), "float8_e4m3fn"),
+                     ((40, 131072), (131072, 32), "float8_e5m2")]:
+        with Plan(a, b, dt) as p:
+            assert p.algorithm != "split_k"
+            with pytest.raises(OlcError):
+                p.force("split_k")
+
+
 def test_create_rejects_rank0_null_and_bad_dtype():
     lib = binding.load()
     h = ctypes.c_void_p()

@@ -283,3 +283,52 @@ def test_fp8_skinny_decode_workload_full():
         a, b = prod.draw()
         y, algo = check_product(a, b, prod.dtype)
         assert algo == "skinny_m"
+
+
+F8_SPLIT_SHAPES = [
+    ((32, 131072), (131072, 32)),          # the tiny-output long-K corner: two 16-row tiles
+    ((16, 40000), (40000, 48)),            # one tile, K tail inside a chunk
+    ((20, 9000), (9000, 128)),             # two column groups
+    ((3, 2, 8, 3000), (2, 3000, 16)),      # six batch items, batched B
+    ((17, 10001), (10001, 32)),            # A rows not 4-byte aligned: byte loads
+]
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes", F8_SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_split_k(dtype, shapes):
+    """Small outputs over long K: the warp-MMA split-K (about one K slice
+    per SM, partials summed in slice order within groups of 16, then in
+    group order); normal inputs within the float32 bar, integers exact."""
+    a_shape, b_shape = shapes
+    with Plan(a_shape, b_shape, dtype) as p:
+        if a_shape == (32, 131072):
+            assert p.algorithm == "split_k" and p.splits > 16
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 50)
+    check_product(a, b, dtype, algorithm="split_k")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 51)
+    check_product(ai, bi, dtype, algorithm="split_k", exact=True)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16, 17, 40])
+def test_fp8_split_k_slice_counts_and_reproducibility(splits):
+    """Requested slice counts: one level (1..16 slices) and two levels (17:
+    groups of 16 and 1; 40: 16, 16, 8); the same inputs give bit-identical
+    results on every run."""
+    dtype = "float8_e4m3fn"
+    a, b = synth.operands((24, 20000), (20000, 64), dtype, synth.normal(1.0), synth.normal(0.5), 52)
+    ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+    A, B = a.cuda(), b.cuda()
+    with Plan(a.shape, b.shape, dtype) as p:
+        p.force("split_k")
+        p.set_splits(splits)
+        assert p.splits == splits
+        outs = []
+        for _ in range(3):
+            Y = torch.full((24, 64), float("nan"), device="cuda")
+            p.execute_checked(A, B, Y)
+            torch.cuda.synchronize()
+            outs.append(Y.cpu())
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+    compare(outs[0], ref, s, dtype)
