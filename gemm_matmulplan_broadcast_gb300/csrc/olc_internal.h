@@ -100,6 +100,9 @@ int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count);
 
 // SKINNY_N: N <= 16.
 int skinny_n_max_cols();
+// E4M3FN / E5M2 products the register-streaming warp-MMA kernel takes (one
+// B, K a multiple of 16, B within its shared-memory budget)
+bool skinny_n_f8_ok(olc_dtype dt, const Problem& p);
 cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, const Workspace& ws,
                             cudaStream_t stream);
 size_t skinny_n_partial_bytes(olc_dtype dt, const Problem& p, int sm_count);

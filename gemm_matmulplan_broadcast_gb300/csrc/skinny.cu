@@ -1108,6 +1108,17 @@ static cudaError_t launch_skinny_n_t(const Problem& p, cudaStream_t s) {
 // registers of the two products.  Rows are placed with an XOR swizzle (row
 // k at 16-byte slot k ^ (((k >> 3) & 3) << 1)) so that the eight rows of
 // each matrix fall in eight different bank groups.
+//
+// E4M3FN / E5M2 operands use the same streaming and the same register
+// assignment with mma.sync.m16n8k32 (8-bit operands, float32 accumulation,
+// FLOAT output): a chunk is 64 K positions (the same 64 bytes of each row),
+// thread t's 16 bytes hold k0 + 16t .. 16t + 15, and the first product takes
+// 16t + {0..3} and 16t + {4..7} for its logical K positions 4t + {0..3} and
+// 16 + 4t + {0..3}, the second 16t + {8..15}.  B is staged transposed, one
+// row of K bytes per column (rows padded to 64 bytes past a multiple of 128,
+// so that the two columns a quarter-warp reads fall in different banks), and
+// a thread's two B fragments of an 8-column block are one 16-byte shared
+// load at its column and k0 + 16t.
 
 constexpr int kSnWarps = 16;
 constexpr int kSnSlots = 4;
@@ -1140,10 +1151,15 @@ __device__ __forceinline__ uint4 ldmatrix_x4_trans(uint32_t addr) {
 // 16-byte slot of B row k in its plane
 __device__ __forceinline__ int64_t sn_slot(int64_t k) { return k ^ (((k >> 3) & 3) << 1); }
 
-// K per warp (whole 32-wide chunks) and the rows of a B plane (every warp's
-// range; rows at or past K hold zeros).
-static int64_t sn_k_per_warp(int64_t K) { return ceil_div(ceil_div(K, kSnWarps), 32) * 32; }
-static int64_t sn_rows(int64_t K) { return sn_k_per_warp(K) * kSnWarps; }
+// K per warp (whole chunks of ck elements, 64 bytes of a row) and the rows
+// of a B plane (every warp's range; rows at or past K hold zeros).
+static int64_t sn_k_per_warp(int64_t K, int ck) { return ceil_div(ceil_div(K, kSnWarps), ck) * ck; }
+static int64_t sn_rows(int64_t K, int ck) { return sn_k_per_warp(K, ck) * kSnWarps; }
+// shared-memory bytes of B: 16-byte rows per 8-column plane (16-bit types),
+// or one transposed row of K bytes (+ 64 bytes) per column (8-bit types)
+static int64_t sn_b_bytes(int eb, int nb, int64_t K) {
+    return eb == 1 ? (int64_t)nb * 8 * (sn_rows(K, 64) + 64) : (int64_t)nb * sn_rows(K, 32) * 16;
+}
 
 template <int NB>
 struct SnShared {
@@ -1157,8 +1173,13 @@ template <typename T, int NB>
 __global__ void __launch_bounds__(kSnWarps * 32, 1)
 skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int* err) {
     constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr bool F8 = sizeof(T) == 1;
+    using out_t = typename Num<T>::out_t;
+    constexpr int EB = (int)sizeof(T);
+    constexpr int CK = 64 / EB;                            // K positions per chunk
     constexpr int R = 8;                                   // K chunks in flight per thread
-    extern __shared__ __align__(16) uint4 bs[];            // [NB planes][rows] 16-byte B rows
+    // 16-bit types: [NB planes][rows] 16-byte B rows; 8-bit: [NB * 8 columns][rows + 64] bytes
+    extern __shared__ __align__(16) uint4 bs[];
     __shared__ SnShared<NB> sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -1168,13 +1189,13 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
     // the same ones (the partials are still summed in K-range order)
     const int krange = (warp + (int)(blockIdx.x % kSnWarps)) % kSnWarps;
     const int64_t kbeg = (int64_t)krange * kw;
-    const unsigned short* A = static_cast<const unsigned short*>(p.A);
+    const unsigned char* A = static_cast<const unsigned char*>(p.A);
 
     // This warp's work is one sequence of 32-wide K chunks: chunk c of its K
     // range for each of the block's units in turn.  A ring of R register
     // slots keeps R chunks (2 x 16 bytes per thread each) in flight: chunk
     // i + R is requested as soon as chunk i has been multiplied.
-    const int cpu = kw / 32;                               // chunks per unit
+    const int cpu = kw / CK;                               // chunks per unit
     const int my_units = (int)((units - blockIdx.x + gridDim.x - 1) / gridDim.x);
     // the next chunk to request: unit index (within this block) and chunk
     int lu = 0, lc = 0;
@@ -1183,10 +1204,11 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
         vb = va;
         if (lu < my_units) {
             const int64_t r0 = (blockIdx.x + (int64_t)lu * gridDim.x) * 16;
-            const int64_t k = kbeg + lc * 32 + 8 * t;      // K is a multiple of 8
+            // K is a multiple of 16 bytes: a 16-byte piece starting below K is whole
+            const int64_t k = kbeg + lc * CK + (CK / 4) * t;
             const int64_t ra = r0 + g, rb = r0 + g + 8;
-            if (k < K && ra < M) va = __ldcs(reinterpret_cast<const uint4*>(A + ra * K + k));
-            if (k < K && rb < M) vb = __ldcs(reinterpret_cast<const uint4*>(A + rb * K + k));
+            if (k < K && ra < M) va = __ldcs(reinterpret_cast<const uint4*>(A + (ra * K + k) * EB));
+            if (k < K && rb < M) vb = __ldcs(reinterpret_cast<const uint4*>(A + (rb * K + k) * EB));
         }
         if (++lc == cpu) { lc = 0; ++lu; }
     };
@@ -1203,9 +1225,18 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
     // for the others.  With N == 8 or 16 every 16-byte vector of B is one
     // row of one plane and is stored as it is; other N are padded to 8
     // columns element by element.  Rows at or past K are zero.
+    const int64_t rstride = rows + 64;                    // 8-bit types: bytes per transposed row
     {
         const int64_t kend = min64(K, kbeg + kw);
-        if (N == 8 * NB) {
+        if constexpr (F8) {
+            const unsigned char* B = static_cast<const unsigned char*>(p.B);
+            unsigned char* bt = reinterpret_cast<unsigned char*>(bs);
+            for (int v = lane; v < kw * NB * 8; v += 32) {
+                const int n = v % (NB * 8);
+                const int64_t k = kbeg + v / (NB * 8);
+                bt[n * rstride + k] = (k < kend && n < N) ? __ldg(B + k * N + n) : (unsigned char)0;
+            }
+        } else if (N == 8 * NB) {
             const uint4* B4 = static_cast<const uint4*>(p.B);
             for (int v0 = lane; v0 < kw * NB; v0 += 4 * 32) {
                 uint4 w[4];
@@ -1249,7 +1280,7 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
     const int koff = 8 * (mr >> 1) + 2 * mi + (mr & 1);
     const uint32_t bs_base = static_cast<uint32_t>(__cvta_generic_to_shared(bs));
 
-    T* Y = static_cast<T*>(p.Y);
+    out_t* Y = static_cast<out_t*>(p.Y);
     volatile int* uses = sh.uses;
     volatile int* abort_flag = &sh.abort;
     // two accumulator chains per n-block (the two MMAs of a chunk), summed
@@ -1305,7 +1336,7 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
                 float v = sh.red[slot][0][r][c];
 #pragma unroll
                 for (int w = 1; w < kSnWarps; ++w) v += sh.red[slot][w][r][c];
-                Y[row * N + c] = Num<T>::from_acc(apply_epilogue<T>(p.epi, v, row, c, Y + row * N + c));
+                Y[row * N + c] = Num<T>::from_acc(apply_epilogue<out_t>(p.epi, v, row, c, Y + row * N + c));
             }
             __syncwarp();
             if (lane == 0) {
@@ -1323,12 +1354,25 @@ skinny_n_mma_kernel(Problem p, int64_t units, int kw, int64_t rows, unsigned int
 #pragma unroll
         for (int q = 0; q < R; ++q) {
             if (cu >= my_units) break;
-            const int64_t krow = sn_slot(kbeg + cc * 32 + koff);
+            if constexpr (F8) {
+                const uint32_t kb = (uint32_t)(kbeg + cc * CK + 16 * t);
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                const uint4 b = ldmatrix_x4_trans(bs_base + (uint32_t)((j * rows + krow) * 16));
-                mma_16816(d0[j], va[q].x, vb[q].x, va[q].y, vb[q].y, b.x, b.y, BF16);
-                mma_16816(d1[j], va[q].z, vb[q].z, va[q].w, vb[q].w, b.z, b.w, BF16);
+                for (int j = 0; j < NB; ++j) {
+                    const uint4 b = *reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const unsigned char*>(bs) + (j * 8 + g) * rstride + kb);
+                    const uint32_t a0[4] = {va[q].x, vb[q].x, va[q].y, vb[q].y};
+                    const uint32_t a1[4] = {va[q].z, vb[q].z, va[q].w, vb[q].w};
+                    mma_f8_m16n8k32<T::kFormat>(d0[j], a0, b.x, b.y);
+                    mma_f8_m16n8k32<T::kFormat>(d1[j], a1, b.z, b.w);
+                }
+            } else {
+                const int64_t krow = sn_slot(kbeg + cc * 32 + koff);
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const uint4 b = ldmatrix_x4_trans(bs_base + (uint32_t)((j * rows + krow) * 16));
+                    mma_16816(d0[j], va[q].x, vb[q].x, va[q].y, vb[q].y, b.x, b.y, BF16);
+                    mma_16816(d1[j], va[q].z, vb[q].z, va[q].w, vb[q].w, b.z, b.w, BF16);
+                }
             }
             load(va[q], vb[q]);
             if (++cc == cpu) {
@@ -1346,23 +1390,31 @@ constexpr int64_t kSnMaxBtBytes = 150 * 1024;
 static_assert(kSnMaxBtBytes + sizeof(SnShared<2>) <= 227 * 1024, "shared memory of one block");
 
 bool skinny_n_mma_ok(olc_dtype dt, const Problem& p) {
-    if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;
-    if (p.N > 16 || (p.K % 8) != 0) return false;
+    const bool f8 = dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2;
+    if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16 && !f8) return false;
+    // 16-byte pieces of A rows: K a multiple of 8 (16-bit) or 16 (8-bit)
+    if (p.N > 16 || (p.K % (f8 ? 16 : 8)) != 0) return false;
     // one B for every unit: a single item, or items folded into rows
     if (p.items != 1) return false;
-    // above 8 columns the tcgen05 16-column kernel is faster (two mma.sync
-    // per 8 columns cost more than one 128 x 16 tcgen05 MMA)
-    if (p.N > 8 && p.variant != 2) return false;
+    // above 8 columns the tcgen05 16-column kernel is faster for 16-bit
+    // types (two mma.sync per 8 columns cost more than one 128 x 16 tcgen05
+    // MMA); 8-bit types have no such kernel
+    if (!f8 && p.N > 8 && p.variant != 2) return false;
     const int nb = p.N <= 8 ? 1 : 2;                       // 8-column planes
-    return (int64_t)nb * sn_rows(p.K) * 16 <= kSnMaxBtBytes;
+    return sn_b_bytes(f8 ? 1 : 2, nb, p.K) <= kSnMaxBtBytes;
+}
+
+bool skinny_n_f8_ok(olc_dtype dt, const Problem& p) {
+    return (dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2) && skinny_n_mma_ok(dt, p);
 }
 
 template <typename T, int NB>
 static cudaError_t launch_skinny_n_mma_t(const Problem& p, int sm_count, cudaStream_t s) {
+    constexpr int CK = 64 / (int)sizeof(T);
     const int64_t units = ceil_div(p.M, 16);
-    const int kw = (int)sn_k_per_warp(p.K);
-    const int64_t rows = sn_rows(p.K);
-    const size_t smem = (size_t)NB * rows * 16;
+    const int kw = (int)sn_k_per_warp(p.K, CK);
+    const int64_t rows = sn_rows(p.K, CK);
+    const size_t smem = (size_t)sn_b_bytes((int)sizeof(T), NB, p.K);
     const cudaError_t attr = set_smem_limit(reinterpret_cast<const void*>(skinny_n_mma_kernel<T, NB>),
                                             (int)kSnMaxBtBytes);
     if (attr != cudaSuccess) return attr;
@@ -1373,6 +1425,12 @@ static cudaError_t launch_skinny_n_mma_t(const Problem& p, int sm_count, cudaStr
 
 static cudaError_t launch_skinny_n_mma(olc_dtype dt, const Problem& p, int sm_count,
                                        cudaStream_t s) {
+    if (dt == OLC_FLOAT8E4M3FN)
+        return p.N <= 8 ? launch_skinny_n_mma_t<F8<0>, 1>(p, sm_count, s)
+                        : launch_skinny_n_mma_t<F8<0>, 2>(p, sm_count, s);
+    if (dt == OLC_FLOAT8E5M2)
+        return p.N <= 8 ? launch_skinny_n_mma_t<F8<1>, 1>(p, sm_count, s)
+                        : launch_skinny_n_mma_t<F8<1>, 2>(p, sm_count, s);
     if (dt == OLC_FLOAT16)
         return p.N <= 8 ? launch_skinny_n_mma_t<__half, 1>(p, sm_count, s)
                         : launch_skinny_n_mma_t<__half, 2>(p, sm_count, s);
@@ -1397,6 +1455,7 @@ cudaError_t launch_skinny_n(olc_dtype dt, const Problem& p, int sm_count, const 
     // FLOAT16 / BFLOAT16 with 16-byte row strides: stream A through the
     // tensor cores with 16-column tiles (8 FMAs per A element would need most
     // of the SIMT FMA rate at full HBM bandwidth)
+    if (skinny_n_f8_ok(dt, p)) return launch_skinny_n_mma(dt, p, sm_count, s);   // 8-bit: the only kernel
     if (p.variant != 1 && skinny_n_mma_ok(dt, p)) return launch_skinny_n_mma(dt, p, sm_count, s);
     if (skinny_n_on_tc(dt, p)) return launch_skinny_n_tc(dt, p, sm_count, ws, s);
     return dispatch_dtype(dt, [&](auto tag) {

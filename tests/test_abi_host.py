@@ -165,6 +165,25 @@ def test_fp8_split_k_choice_and_workspace():
                 p.force("split_k")
 
 
+def test_fp8_skinny_n_choice():
+    """FP8 products with at most 8 columns and one B stream A through the
+    warp-MMA skinny-N kernel (up to 16 when forced); the FNUZ formats and K
+    not a multiple of 16 do not take it."""
+    for a, b in [((16384, 4096), (4096, 8)), ((2, 3, 100, 2048), (2048, 5))]:
+        with Plan(a, b, "float8_e5m2") as p:
+            assert p.algorithm == "skinny_n"
+    # 9-16 columns: the tensor-core tile kernel by default, this one on request
+    with Plan((1000, 4096), (4096, 16), "float8_e4m3fn") as p:
+        assert p.algorithm == "general_tc"
+        p.force("skinny_n")
+    for a, b, dt in [((16384, 4096), (4096, 8), "float8_e4m3fnuz"),
+                     ((16384, 4104), (4104, 8), "float8_e4m3fn")]:
+        with Plan(a, b, dt) as p:
+            assert p.algorithm != "skinny_n"
+            with pytest.raises(OlcError):
+                p.force("skinny_n")
+
+
 def test_create_rejects_rank0_null_and_bad_dtype():
     lib = binding.load()
     h = ctypes.c_void_p()

@@ -332,3 +332,28 @@ def test_fp8_split_k_slice_counts_and_reproducibility(splits):
     for y in outs[1:]:
         assert torch.equal(y, outs[0])
     compare(outs[0], ref, s, dtype)
+
+
+F8_SKINNY_N_SHAPES = [
+    ((16384, 4096), (4096, 8)),            # the skinny-N corner shape
+    ((1000, 4096), (4096, 16)),            # two 8-column blocks, rows not a multiple of 16
+    ((300, 1040), (1040, 5)),              # N padded to 8 columns, K tail of a warp's range
+    ((2, 3, 100, 2048), (2048, 12)),       # batch folded into 600 rows
+    ((513, 64), (64, 3)),                  # K shorter than the sixteen warps' ranges
+]
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes", F8_SKINNY_N_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_skinny_n(dtype, shapes):
+    """Few columns: the register-streaming kernel of FLOAT16 skinny-N on
+    mma.sync.m16n8k32 (A rows streamed in 16-byte pieces, B transposed in
+    shared memory), chosen up to 8 columns and forced up to 16; normal
+    inputs within the float32 bar, integers exact."""
+    a_shape, b_shape = shapes
+    with Plan(a_shape, b_shape, dtype) as p:
+        assert (p.algorithm == "skinny_n") == (b_shape[-1] <= 8)
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 53)
+    check_product(a, b, dtype, algorithm="skinny_n")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 54)
+    check_product(ai, bi, dtype, algorithm="skinny_n", exact=True)
