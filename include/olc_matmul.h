@@ -43,9 +43,11 @@ extern "C" {
  * accumulate in float32, and give a FLOAT output (4 bytes per element): A
  * and B have the 8-bit type, Y (and a fused residual) is float32.  They are
  * MatMul types only (Gemm plans reject them).  E4M3FN and E5M2 run on the
- * tensor cores (tcgen05 kind::f8f6f4) where the shape allows; the FNUZ
- * variants, whose encodings the tensor cores do not take, always run on the
- * SIMT decode kernel. */
+ * tensor cores: tcgen05 kind::f8f6f4 tiles for general shapes, and the
+ * warp-level mma.sync m16n8k32 for few rows (SKINNY_M from 4 rows), few
+ * columns (SKINNY_N up to 8) and small outputs over a long K (SPLIT_K); the
+ * FNUZ variants, whose encodings the tensor cores do not take, always run on
+ * SIMT decode kernels (SKINNY_M, GENERAL_SIMT, DIRECT). */
 typedef enum {
     OLC_FLOAT = 1,
     OLC_FLOAT16 = 10,
