@@ -263,6 +263,7 @@ inline cudaError_t dispatch_dtype(olc_dtype dt, F&& f) {
         case OLC_DOUBLE: return f(double{});
         case OLC_FLOAT16: return f(__half{});
         case OLC_BFLOAT16: return f(__nv_bfloat16{});
+        default: break;   // 8-bit float types have kernels of their own
     }
     return cudaErrorInvalidValue;
 }
@@ -274,6 +275,7 @@ inline int dispatch_int(olc_dtype dt, F&& f) {
         case OLC_DOUBLE: return f(double{});
         case OLC_FLOAT16: return f(__half{});
         case OLC_BFLOAT16: return f(__nv_bfloat16{});
+        default: break;
     }
     return 0;
 }

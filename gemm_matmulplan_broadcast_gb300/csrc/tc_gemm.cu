@@ -1767,8 +1767,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
         set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<false>), pair::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::SMEM_BYTES;
@@ -1835,8 +1834,7 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
         set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<true>), pair::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::SMEM_BYTES;
@@ -1877,8 +1875,7 @@ static int tiny_max_clusters(int sm_count) {
     }
     int n = 0;
     if (dev >= 0 && tiny_attr<CL>() == cudaSuccess) {
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
+        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(CL * (sm_count / CL > 0 ? sm_count / CL : 1)), 1, 1);
         cfg.blockDim = dim3(tiny::THREADS_T, 1, 1);
         cfg.dynamicSmemBytes = tiny::SMEM_BYTES;
@@ -1929,8 +1926,7 @@ static cudaError_t launch_tiny_cl(const CUtensorMap& ma, const CUtensorMap& mb, 
                                   int grid, cudaStream_t s) {
     const cudaError_t e = tiny_attr<CL>();
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(tiny::THREADS_T, 1, 1);
     cfg.dynamicSmemBytes = tiny::SMEM_BYTES;
