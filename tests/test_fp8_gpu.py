@@ -357,3 +357,37 @@ def test_fp8_skinny_n(dtype, shapes):
     check_product(a, b, dtype, algorithm="skinny_n")
     ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, 54)
     check_product(ai, bi, dtype, algorithm="skinny_n", exact=True)
+
+
+FP8_FUSED_CASES = [
+    ("skinny_m", 1, (4, 2048), (2048, 512)),       # SIMT skinny-M
+    ("skinny_m", 2, (12, 2048), (2048, 512)),      # warp-MMA skinny-M
+    ("split_k", None, (24, 20000), (20000, 64)),   # warp-MMA split-K, two reduction levels
+    ("skinny_n", None, (1000, 1024), (1024, 8)),   # warp-MMA skinny-N
+    ("general_simt", None, (100, 300), (300, 200)),
+    ("direct", None, (7, 33), (33, 9)),
+]
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+@pytest.mark.parametrize("case", FP8_FUSED_CASES, ids=lambda c: "%s-%s" % (c[0], c[1]))
+def test_fp8_fused_epilogue_every_kernel(dtype, act, case):
+    """Residual and activation fused into the store of every FP8 kernel,
+    against the oracle's float64 activation of the float32 sum plus the
+    residual."""
+    algo, variant, a_shape, b_shape = case
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.5), 55)
+    M, N = a_shape[0], b_shape[1]
+    r = torch.randn(M, N, generator=torch.Generator().manual_seed(56))
+    with Plan(a.shape, b.shape, dtype) as p:
+        p.force(algo)
+        if variant is not None:
+            p.set_tc_variant(variant)
+        p.set_epilogue(act, True)
+        Y = torch.full((M, N), float("nan"), device="cuda")
+        p.execute_fused(a.cuda(), b.cuda(), Y, R=r.cuda())
+        torch.cuda.synchronize()
+    ref, s = oracle.matmul_fused(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype,
+                                 r.numpy(), act)
+    compare(Y.cpu(), ref, s, dtype)
