@@ -429,7 +429,9 @@ skinny_m_kernel(Problem p, int64_t col_groups, int ksplit, int64_t kslice, Works
 // register ring, issuing chunk c + F8_RING - 1 before the MMAs of chunk c:
 // at HBM rates a load takes microseconds to return, and the bytes in flight
 // per SM set the bandwidth.  Blocks of kF8MmaWarps warps split K as the SIMT
-// kernel's do and end the same way (skinny_m_finish).
+// kernel's do and end the same way (skinny_m_finish), or, as the split-K of
+// small outputs (MT = 2 tiles for up to 32 rows, about one K slice per SM),
+// with two reduction levels (skinny_m_finish_grouped).
 
 constexpr int kF8MmaWarps = 4;
 constexpr int kF8MmaCols = 64;
