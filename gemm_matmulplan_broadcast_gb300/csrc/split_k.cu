@@ -266,6 +266,16 @@ extern "C" olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, 
         cudaGetLastError();
         return OLC_ERR_CUDA;
     }
+    // the array's address and the SM count are the current device's: a
+    // stream of another device would get an address of the wrong context
+    if (s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return OLC_ERR_CUDA;
+        }
+        if (sdev != dev) return OLC_ERR_WRONG_DEVICE;
+    }
     int splits = split_k_simt_pick(dtype, p, sms);
     const int64_t fit = (int64_t)kStaticPartialBytes / (tiles * tile_bytes);
     if (splits > fit) splits = (int)fit;

@@ -3,7 +3,13 @@ compute the oracle on the same seeded inputs, compare element by element.
 
 Tolerances: |y_gpu - y_oracle| <= tol * sum_k |a||b| per element, with tol =
 1e-5 (FLOAT), 1e-12 (DOUBLE), 2e-3 (FLOAT16), 1e-2 (BFLOAT16).  Integer-valued
-inputs whose sums are exact in the accumulator must match bit for bit."""
+inputs whose sums are exact in the accumulator must match bit for bit.
+
+Special values follow the oracle exactly: an output is NaN where, and only
+where, the oracle's is NaN, and an infinite output must be the oracle's
+infinity with its sign ("MatMul Kernel Design", section "Types and algorithm
+selection": float32 accumulation, then one narrowing; NaN stays NaN and a sum
+beyond the output type's range becomes an infinity)."""
 
 from __future__ import annotations
 
@@ -21,10 +27,13 @@ TOL = {"float32": 1e-5, "float64": 1e-12, "float16": 2e-3, "bfloat16": 1e-2,
 
 
 def gpu_matmul(a_cpu: torch.Tensor, b_cpu: torch.Tensor, dtype: str, algorithm=None,
-               checked=True, guard=64, variant=None):
+               checked=True, guard=64, variant=None, fill=float("nan")):
     """Y = MatMul(A, B) through the library (kernel-family override `variant`
-    if given); Y is allocated with `guard` trailing canary elements that must
-    stay untouched.  Returns (Y on CPU, plan algorithm)."""
+    if given); Y is allocated filled with `fill`, with `guard` trailing canary
+    elements of that value that must stay untouched.  Products whose correct
+    output holds NaNs pass a finite `fill` that no correct output takes, so
+    that an unwritten element still shows.  Returns (Y on CPU, plan
+    algorithm)."""
     A = a_cpu.cuda()
     B = b_cpu.cuda()
     with Plan(a_cpu.shape, b_cpu.shape, dtype) as p:
@@ -34,29 +43,48 @@ def gpu_matmul(a_cpu: torch.Tensor, b_cpu: torch.Tensor, dtype: str, algorithm=N
             p.set_tc_variant(variant)
         shape = p.output_shape
         n = int(np.prod(shape, dtype=np.int64))
-        buf = torch.full((n + guard,), float("nan"), dtype=synth.TORCH_DTYPES[synth.output_dtype(dtype)], device="cuda")
+        buf = torch.full((n + guard,), fill, dtype=synth.TORCH_DTYPES[synth.output_dtype(dtype)], device="cuda")
         Y = buf[:n].view(shape)
         if checked:
             p.execute_checked(A, B, Y)
         else:
             p.execute(A, B, Y)
         torch.cuda.synchronize()
-        tail = buf[n:].float().cpu()
-        assert torch.isnan(tail).all(), "kernel wrote past the end of Y"
+        tail = buf[n:].double().cpu()
+        if np.isnan(fill):
+            assert torch.isnan(tail).all(), "kernel wrote past the end of Y"
+        else:
+            want = torch.tensor(fill, dtype=buf.dtype).double()
+            assert bool((tail == want).all()), "kernel wrote past the end of Y"
         return Y.cpu(), p.algorithm
 
 
 def compare(y_gpu: torch.Tensor, y_ref: np.ndarray, s: np.ndarray, dtype: str, exact=False):
-    """Element-by-element comparison; returns the largest error / (tol * S)."""
+    """Element-by-element comparison; returns the largest error / (tol * S).
+    NaN must appear exactly where the oracle has NaN (with the usual NaN
+    fill of gpu_matmul an unwritten element therefore fails), an infinity
+    must equal the oracle's, and finite outputs must be within tol * S (equal
+    with `exact`)."""
     yg = oracle.to_float64(synth.to_numpy_storage(y_gpu), dtype).reshape(y_ref.shape)
     yr = oracle.to_float64(y_ref, dtype)
     assert yg.shape == yr.shape
-    assert not np.isnan(yg).any(), "unwritten (NaN) outputs"
+    nan_g, nan_r = np.isnan(yg), np.isnan(yr)
+    if (nan_g != nan_r).any():
+        i = tuple(np.argwhere(nan_g != nan_r)[0])
+        raise AssertionError("NaN pattern differs (unwritten or wrong) at %s: gpu %r oracle %r" % (
+            i, yg[i], yr[i]))
+    inf = ~nan_r & (np.isinf(yg) | np.isinf(yr))
+    if inf.any() and (yg[inf] != yr[inf]).any():
+        i = tuple(np.argwhere(inf & (yg != yr))[0])
+        raise AssertionError("infinity differs at %s: gpu %r oracle %r" % (i, yg[i], yr[i]))
+    fin = ~nan_r & ~inf
     if exact:
-        bad = np.argwhere(yg != yr)
+        bad = np.argwhere(fin & (yg != yr))
         assert bad.size == 0, "first mismatch at %s: gpu %r oracle %r" % (
             tuple(bad[0]), yg[tuple(bad[0])], yr[tuple(bad[0])])
         return 0.0
+    yg, yr = np.where(fin, yg, 0.0), np.where(fin, yr, 0.0)
+    s = np.where(fin, s, 0.0)
     err = np.abs(yg - yr)
     bound = TOL[dtype] * s
     ok = err <= bound

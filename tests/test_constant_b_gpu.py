@@ -1,14 +1,18 @@
-"""Plan-owned constant B: executes without B equal executes with it bit for
-bit (the same kernels read the owned copy), the copy outlives the source
-buffer, the size must be the planned one, and the B-less execute is rejected
-when the plan owns no B."""
+"""Plan-owned constant B: executes without B compute the planned product
+(checked against the oracle) and equal executes with it bit for bit (the
+same kernels read the owned copy), the copy outlives the source buffer, the
+size must be the planned one, and the B-less execute is rejected when the
+plan owns no B."""
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from gemm_matmulplan_broadcast_gb300 import GemmPlan, OlcError, Plan, binding, synth
+from parity import compare, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +37,22 @@ def test_constant_b_matches_per_call_b(dtype, shapes, source):
         p.execute_constant(A, Y2)
         torch.cuda.synchronize()
         assert torch.equal(Y1, Y2)
+    _check_against_oracle(a, b, Y2.cpu(), dtype)
+
+
+def _check_against_oracle(a, b, y, dtype):
+    """The constant-B result against the oracle: on sampled rows of the
+    folded product when B is one matrix, in full otherwise."""
+    an, bn = synth.to_numpy_storage(a), synth.to_numpy_storage(b)
+    if b.dim() == 2 and an.size // an.shape[-1] > 512:
+        k = an.shape[-1]
+        a2 = an.reshape(-1, k)
+        rows = sample_rows(a2.shape[0], extra=64)
+        y_ref, s = oracle.gemm2d(a2, bn, dtype, rows=rows)
+        compare(y.reshape(-1, bn.shape[-1])[rows], y_ref, s, dtype)
+    else:
+        y_ref, s = oracle.matmul(an, bn, dtype)
+        compare(y, y_ref, s, dtype)
 
 
 def test_constant_b_rejections():
@@ -61,3 +81,7 @@ def test_gemm_constant_b_with_bias():
         p.execute_constant(A, Y2, C=C)
         torch.cuda.synchronize()
         assert torch.equal(Y1, Y2)
+    y_ref, s = oracle.gemm_op(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "bfloat16",
+                              c=synth.to_numpy_storage(c), alpha=0.5, beta=2.0, trans_a=False,
+                              trans_b=True)
+    compare(Y2.cpu(), y_ref, s, "bfloat16")

@@ -9,7 +9,9 @@ import os
 import pytest
 import torch
 
+import oracle
 from gemm_matmulplan_broadcast_gb300 import Plan, binding, synth
+from parity import compare
 
 
 def _selftest():
@@ -31,8 +33,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     with Plan(a.shape, b.shape, "bfloat16") as p:
         y = torch.empty(p.output_shape, dtype=torch.bfloat16, device="cuda")
         p.execute_checked(a.cuda(), b.cuda(), y)
-    ref = (a.double() @ b.double()).to(torch.bfloat16)
-    assert torch.equal(y.cpu(), ref)
+    y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), "bfloat16")
+    compare(y.cpu(), y_ref, s, "bfloat16", exact=True)
 
 
 def test_host_errors_come_back_before_any_launch():
