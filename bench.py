@@ -471,6 +471,10 @@ def measure_secondary(workload, device, peaks, l2):
     _, probe = time_steps(items, 1, stream)
     res = []
     for i, it in enumerate(items):
+        if it["plan"].launches == 0:
+            res.append({"product": it["name"], "algorithm": it["plan"].algorithm,
+                        "gpu_launches": 0, "note": "empty output: nothing launched"})
+            continue
         if probe[i][0] < 2.0:
             per = graph_time_per_launch(it, stream)
             how = "cuda graph of %d launches x %d replays" % (max(4, len(it["sets"])), len(per))
@@ -630,6 +634,153 @@ def measure_grouped(device, peaks):
     return out
 
 
+def measure_alu(stream):
+    """The FMA pipes' delivered rate (library probe: independent FMA chains
+    on every SM, no memory traffic), beside the peaks derived from unit
+    counts and the maximum clock that the FLOAT / DOUBLE rooflines use."""
+    from gemm_matmulplan_broadcast_gb300 import binding
+    # iterations for about 25-50 ms per launch at the derived peaks
+    kinds = [("fp32_ffma2", 0, 800000), ("fp32_ffma", 1, 800000), ("fp64_dfma", 2, 24000),
+             ("fp64_dmma", 3, 6000)]
+    out = {}
+    for name, kind, iters in kinds:
+        rates = [binding.alu_rate(kind, iters, stream) for _ in range(3)]
+        out[name] = {"tflops": max(rates) / 1e12, "runs": 3, "iters": iters}
+    return out
+
+
+def measure_split_k_curve(device, peaks, l2):
+    """The FP16 small-output split-K product [32, K] x [K, 32] as K grows
+    (131072 is the named corner): GB/s against K gives the kernel's fixed
+    cost per launch (intercept) and its streaming rate (slope)."""
+    from gemm_matmulplan_broadcast_gb300 import synth
+    prods = tuple(synth.Product("split_k_%d" % k, (32, k), (k, 32), "float16", synth.normal(1.0),
+                                synth.normal(0.02), 3) for k in (131072, 262144, 524288, 1048576))
+    w = synth.Workload("fp16_split_k_curve", "FP16 [32,K]x[K,32], K = 2^17..2^20, seed 3", prods)
+    res = measure_secondary(w, device, peaks, l2)
+    # least-squares line t = t0 + bytes / rate over the sizes
+    import numpy as np
+    x = np.array([2.0 * 32 * int(r["product"].split("_")[-1]) * 2 + 32 * 32 * 2 for r in res])
+    t = np.array([r["ms_per_launch"] * 1e-3 for r in res])
+    slope, t0 = np.polyfit(x, t, 1)
+    return {"points": res, "fit_fixed_us": t0 * 1e6, "fit_stream_gbs": 1.0 / slope / 1e9}
+
+
+def measure_split_k_static(device, l2):
+    """The allocation-free split-K entry point (SIMT split kernel, scratch in
+    a fixed device array) on the FP16 corner [32, 131072] x [131072, 32],
+    against the plan path's split-K on the same operands: events around 20
+    back-to-back calls of each, after warm-up."""
+    import ctypes
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import Plan, binding, synth
+    m, k, n = 32, 131072, 32
+    a, b = synth.operands((m, k), (k, n), "float16", synth.normal(1.0), synth.normal(0.02), 3)
+    A, B = a.to(device), b.to(device)
+    Y = torch.empty(m, n, dtype=torch.float16, device=device)
+    fn = binding.load().olc_matmul_split_k_static
+    vp = ctypes.c_void_p
+    fn.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp]
+    fn.restype = ctypes.c_int
+    stream = torch.cuda.Stream()
+    plan = Plan((m, k), (k, n), "float16")
+
+    def static_call():
+        st = fn(10, A.data_ptr(), B.data_ptr(), Y.data_ptr(), m, n, k, stream.cuda_stream)
+        assert st == 0, st
+
+    def plan_call():
+        plan.execute(A, B, Y, stream=stream)
+
+    out = {}
+    for label, call in (("static", static_call), ("plan", plan_call)):
+        for _ in range(5):
+            call()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            call()
+        e1.record(stream)
+        e1.synchronize()
+        out["ms_" + label] = e0.elapsed_time(e1) / 20
+    plan.close()
+    byts = 2.0 * (m * k + k * n + m * n)
+    out["gbs_static"] = byts / (out["ms_static"] * 1e-3) / 1e9
+    out["gbs_plan"] = byts / (out["ms_plan"] * 1e-3) / 1e9
+    out["timing"] = "events around 20 back-to-back calls (operands L2-resident)"
+    return out
+
+
+def oracle_single_thread(names):
+    """The oracle on one host core over the small named workloads, in full."""
+    import oracle
+    from gemm_matmulplan_broadcast_gb300 import synth
+    n0 = oracle.threads()
+    oracle.set_threads(1)
+    out = {}
+    try:
+        for wname in names:
+            w = synth.workload(wname)
+            fl, secs = 0.0, 0.0
+            for prod in w.products:
+                a, b = prod.draw()
+                an, bn = synth.to_numpy_storage(a), synth.to_numpy_storage(b)
+                flop, _ = work_of(prod.a_shape, prod.b_shape, prod.dtype)
+                reps = 0
+                t0 = time.perf_counter()
+                while True:
+                    oracle.matmul(an, bn, prod.dtype)
+                    reps += 1
+                    if time.perf_counter() - t0 > 0.2:
+                        break
+                secs += (time.perf_counter() - t0) / reps
+                fl += flop
+            out[wname] = {"gflops": fl / secs / 1e9, "ms_per_pass": secs * 1e3, "threads": 1}
+    finally:
+        oracle.set_threads(n0)
+    return out
+
+
+def _short(x):
+    return float("%.3g" % x)
+
+
+def compact_summary(breakdown, secondary):
+    """One short entry per named configuration (and the extra workloads):
+    per product its time and achieved rate with the roofline fraction."""
+    def rows(lst):
+        d = {}
+        for r in lst:
+            if "achieved" not in r:
+                d[r["product"]] = "empty: 0 launches"
+                continue
+            d[r["product"]] = "%s us %s %s (%s)" % (_short(r["ms_per_launch"] * 1e3), _short(r["achieved"]),
+                                                    r["unit"], _short(r["frac"]))
+        return d
+    out = {"C3_bf16_projection": rows(breakdown)}
+    names = [("C1_fp32_64x128x96", "fp32_64x128x96"), ("C2_fp32_broadcast", "fp32_broadcast_batch"),
+             ("C4_fp16_corners", "fp16_skinny_splitk"), ("C5_fp32", "float32_square_chain"),
+             ("C5_fp64", "float64_square_chain"), ("fp8_proj", "fp8_transformer_projection"),
+             ("fp8_rows", "fp8_skinny_decode")]
+    for key, wname in names:
+        if wname in secondary:
+            out[key] = rows(secondary[wname])
+    if "split_k_curve" in secondary:
+        c = secondary["split_k_curve"]
+        out["split_k_curve"] = {"fixed_us": _short(c["fit_fixed_us"]),
+                                "stream_gbs": _short(c["fit_stream_gbs"]),
+                                "gbs_by_K": {r["product"].split("_")[-1]: _short(r["achieved"])
+                                             for r in c["points"]}}
+    if "split_k_static" in secondary:
+        st = secondary["split_k_static"]
+        out["split_k_static_us"] = {"static": _short(st["ms_static"] * 1e3),
+                                    "plan": _short(st["ms_plan"] * 1e3)}
+    if "alu_rates" in secondary:
+        out["alu_tflops"] = {k: _short(v["tflops"]) for k, v in secondary["alu_rates"].items()}
+    return out
+
+
 def run_ours(args):
     import torch
     from gemm_matmulplan_broadcast_gb300 import load, synth
@@ -689,21 +840,27 @@ def run_ours(args):
 
     secondary = {}
     if not args.no_secondary and args.workload == "bf16_transformer_projection":
-        names = ["fp16_skinny_splitk", "float32_square_chain"]
-        if args.full_secondary:
+        names = ["fp32_64x128x96", "fp32_broadcast_batch", "fp16_skinny_splitk",
+                 "float32_square_chain"]
+        if not args.no_fp64:
             names.append("float64_square_chain")
         names.append("fp8_transformer_projection")
         names.append("fp8_skinny_decode")
         for wname in names:
             secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
+        secondary["split_k_curve"] = measure_split_k_curve(device, peaks, l2)
+        secondary["split_k_static"] = measure_split_k_static(device, l2)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)
         secondary["grouped_small_products"] = measure_grouped(device, peaks)
+        secondary["alu_rates"] = measure_alu(stream)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         fl, cs, cores, desc = cpu_oracle_sample(workload, args.cpu_seconds, items)
         cpu = {"value": fl / cs / (1e12 if not bw_bound else 1.0), "unit": unit if not bw_bound else "flop/s",
                "cores": cores, "kind": "oracle", "sample": desc, "seconds": cs}
+        if not args.no_secondary:
+            cpu["single_thread"] = oracle_single_thread(["fp32_64x128x96", "fp32_broadcast_batch"])
 
     launches = sum(it["plan"].launches for it in items) * args.steps
     dtypes = sorted({it["dtype"] for it in items})
@@ -740,6 +897,8 @@ def run_ours(args):
         "clocks": clocks,
         "host_enqueue_s": host_enqueue_s,
         "gpu": props.name,
+        # last, so that a reader keeping only the end of the line keeps it
+        "summary": compact_summary(breakdown, secondary),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -801,8 +960,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="bf16_transformer_projection")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--full-secondary", action="store_true",
-                    help="also time the FP64 square/chain workload (slow)")
+    ap.add_argument("--no-fp64", action="store_true",
+                    help="skip the FP64 square/chain workload (about 10 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)

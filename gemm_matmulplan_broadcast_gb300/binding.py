@@ -115,6 +115,10 @@ def load():
             "olc_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "olc_algorithm_name": ([ctypes.c_int], ctypes.c_char_p),
             "olc_version": ([], ctypes.c_int),
+            "olc_matmul_plan_algorithm_for": ([vp, vp, vp, vp, vp], ctypes.c_int),
+            "olc_matmul_plan_staging_copies": ([vp, vp, vp, vp, vp], ctypes.c_int),
+            "olc_debug_alu_rate": ([ctypes.c_int, ctypes.c_int64, vp, ctypes.POINTER(ctypes.c_double)],
+                                   ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -224,6 +228,15 @@ class Plan:
     @property
     def algorithm(self) -> str:
         return ALGORITHM_NAMES[self.lib.olc_matmul_plan_algorithm(self._h)]
+
+    def algorithm_for(self, A, B, Y, R=None) -> str:
+        """The algorithm an execute with these tensors runs (host query)."""
+        a = self.lib.olc_matmul_plan_algorithm_for(self._h, _ptr(A), _ptr(B), _ptr(Y), _ptr(R))
+        return ALGORITHM_NAMES.get(a, str(a))
+
+    def staging_copies(self, A, B, Y, R=None) -> int:
+        """Staging copies an execute with these tensors makes (host query)."""
+        return int(self.lib.olc_matmul_plan_staging_copies(self._h, _ptr(A), _ptr(B), _ptr(Y), _ptr(R)))
 
     def force(self, algorithm: str):
         _check(self.lib.olc_matmul_plan_force_algorithm(self._h, ALGORITHMS[algorithm]),
@@ -467,6 +480,15 @@ class GroupedPlan:
             self.close()
         except Exception:
             pass
+
+
+def alu_rate(kind: int, iters: int, stream=None) -> float:
+    """flop/s of the library's FMA-pipe probe (olc_debug_alu_rate): kind 0
+    paired FP32 FMA, 1 FP32 FMA, 2 FP64 FMA, 3 FP64 tensor-core MMA."""
+    out = ctypes.c_double(0.0)
+    st = load().olc_debug_alu_rate(int(kind), int(iters), _stream_handle(stream), ctypes.byref(out))
+    _check(st, "olc_debug_alu_rate")
+    return float(out.value)
 
 
 def gemm(A, B, C=None, alpha=1.0, beta=1.0, trans_a=False, trans_b=False, out=None, stream=None):

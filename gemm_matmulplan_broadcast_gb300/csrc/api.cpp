@@ -56,6 +56,13 @@ struct olc_matmul_plan {
     int const_b_set;
     void* const_bt;              // 8-bit float tensor-core plans: constant B as [N, K] bytes
     size_t const_bt_bytes;
+    void* const_b_pad;           // 16-bit plans with N % 8 != 0: constant B, rows padded to 16 bytes
+    size_t const_b_pad_bytes;
+    // staging copies of operands the tensor-core kernels cannot read in
+    // place (rows not a multiple of 16 bytes, or a pointer off a 16-byte
+    // boundary): A's copy, then B's, 256-byte aligned
+    void* stage;
+    size_t stage_bytes;
     // fused epilogue: activation, and a residual in the output's layout
     int act;
     int residual;
@@ -259,9 +266,85 @@ bool feasible(const olc_matmul_plan* p, int algo) {
         case OLC_ALGO_SPLIT_K:
             return n > 0 && K > 0 && (K * elem_bytes(p->dtype)) % 16 == 0 &&
                    (N * elem_bytes(p->dtype)) % 16 == 0;
-        case OLC_ALGO_GENERAL_TC: return n > 0 && K > 0 && is_half(p->dtype) && tc_shape_ok(p->dtype, N, K);
+        case OLC_ALGO_GENERAL_TC:
+            // operands whose rows are not 16-byte multiples are staged into
+            // padded rows first (A as [M, K], B as [K, N]); transposed
+            // operands are read in place and need 16-byte rows
+            return n > 0 && K > 0 && is_half(p->dtype) && rows < (1LL << 31) && N < (1LL << 31) &&
+                   K < (1LL << 31) && (!p->trans_b || K % 8 == 0);
     }
     return false;
+}
+
+// ---- staging copies for the tensor-core kernels --------------------------
+
+// An operand as stored: `rows` rows of `cols` 16-bit elements.
+struct StoredRows {
+    int64_t rows, cols;
+};
+StoredRows stored_a(const olc_matmul_plan* p) {
+    const int64_t cols = p->trans_a ? p->M : p->K;
+    const int64_t total = numel(p->a_shape, p->a_rank);
+    return {cols > 0 ? total / cols : 0, cols};
+}
+StoredRows stored_b(const olc_matmul_plan* p) {
+    const int64_t cols = p->trans_b ? p->K : p->N;
+    const int64_t total = numel(p->b_shape, p->b_rank);
+    return {cols > 0 ? total / cols : 0, cols};
+}
+int64_t pad8(int64_t n) { return (n + 7) / 8 * 8; }
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Staging copies an execute needs (16-bit plans on the tensor-core, skinny
+// and split-K kernels, which read A and B with TMA or 16-byte vectors).  An
+// operand is copied when its pointer is off a 16-byte boundary or, for the
+// general tensor-core tiles (`tc`), when its stored rows are not a multiple
+// of 16 bytes.  The general tiles take the copy with rows padded to 8
+// elements (read through a row pitch); the other kernels take a dense copy.
+struct StageNeed {
+    bool a, b;
+    size_t a_bytes, b_bytes;
+};
+StageNeed stage_need(const olc_matmul_plan* p, const void* A, const void* B, bool tc,
+                     bool b_padded) {
+    StageNeed n{false, false, 0, 0};
+    const StoredRows ra = stored_a(p), rb = stored_b(p);
+    n.a = (reinterpret_cast<uintptr_t>(A) & 15) != 0 || (tc && ra.cols % 8 != 0);
+    n.b = !b_padded && ((reinterpret_cast<uintptr_t>(B) & 15) != 0 || (tc && rb.cols % 8 != 0));
+    auto bytes = [&](const StoredRows& r) {
+        return round256((size_t)(tc ? r.rows * pad8(r.cols) : pad8(r.rows * r.cols)) * 2);
+    };
+    if (n.a) n.a_bytes = bytes(ra);
+    if (n.b) n.b_bytes = bytes(rb);
+    return n;
+}
+
+void free_stage(olc_matmul_plan* p) {
+    if (p->stage) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (p->device >= 0 && cur != p->device) cudaSetDevice(p->device);
+        cudaFree(p->stage);
+        if (p->device >= 0 && cur >= 0 && cur != p->device) cudaSetDevice(cur);
+        cudaGetLastError();
+    }
+    p->stage = nullptr;
+    p->stage_bytes = 0;
+}
+
+// Grow the staging buffer to `bytes` (cudaMalloc on the plan's device; the
+// previous buffer is freed first, which waits for work using it).
+olc_status ensure_stage(olc_matmul_plan* p, size_t bytes) {
+    if (bytes <= p->stage_bytes) return OLC_OK;
+    free_stage(p);
+    void* mem = nullptr;
+    if (cudaMalloc(&mem, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return OLC_ERR_OOM;
+    }
+    p->stage = mem;
+    p->stage_bytes = bytes;
+    return OLC_OK;
 }
 
 int choose_algorithm(const olc_matmul_plan* p) {
@@ -343,6 +426,16 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
             p->counter_count = skinny_m_counter_count(dt, pr, p->splits, p->sm_count);
         }
     }
+    // 16-bit tensor-core plans whose operand rows are not 16-byte multiples
+    // stage those operands at every execute: the copy buffer belongs to the
+    // plan from here on (pointer misalignment alone is only known at execute)
+    if (p->algo == OLC_ALGO_GENERAL_TC && is_half(dt) && p->device >= 0) {
+        const StageNeed need = stage_need(p, nullptr, nullptr, true, p->const_b_pad != nullptr);
+        if (need.a_bytes + need.b_bytes > 0) {
+            const olc_status st = ensure_stage(p, need.a_bytes + need.b_bytes);
+            if (st != OLC_OK) return st;
+        }
+    }
     if (p->partial_bytes == 0 && p->counter_count == 0) return OLC_OK;
     const size_t counters_off = (p->partial_bytes + 255) / 256 * 256;
     p->ws_bytes = counters_off + p->counter_count * sizeof(unsigned int);
@@ -382,6 +475,48 @@ olc_status from_cuda(cudaError_t e) {
     return e == cudaErrorMemoryAllocation ? OLC_ERR_OOM : OLC_ERR_CUDA;
 }
 
+// The kernels an execute with these pointers runs.  FLOAT16 / BFLOAT16 stay
+// on the tensor cores whatever the alignment: operands the kernels cannot
+// read in place are copied first (stage_need), and the general kernels store
+// a Y of any alignment; the skinny and split-K kernels store with 16-byte
+// vectors, so a misaligned Y (or residual) moves their products to the
+// general kernels.  Other types: a misaligned pointer sends the product to
+// the DIRECT kernel.
+struct Route {
+    int algo;
+    bool tc;            // general tensor-core tiles
+    bool b_padded;      // B is the plan's constant B, already in padded rows
+    bool y_unaligned;   // Y stored by alignment
+    StageNeed need;
+};
+Route route_of(const olc_matmul_plan* p, const void* A, const void* B, const void* Y, const void* R) {
+    Route r;
+    r.algo = p->algo;
+    r.tc = false;
+    r.b_padded = false;
+    r.y_unaligned = false;
+    r.need = StageNeed{false, false, 0, 0};
+    const int a = p->algo;
+    if (a == OLC_ALGO_EMPTY || a == OLC_ALGO_ZERO_FILL || a == OLC_ALGO_DIRECT ||
+        a == OLC_ALGO_GENERAL_SIMT)
+        return r;
+    if (is_half(p->dtype)) {
+        const bool yr_off = !aligned16(Y) || (R && !aligned16(R));
+        if (yr_off && a != OLC_ALGO_GENERAL_TC)
+            r.algo = feasible(p, OLC_ALGO_GENERAL_TC) ? OLC_ALGO_GENERAL_TC : OLC_ALGO_DIRECT;
+        if (r.algo == OLC_ALGO_DIRECT) return r;
+        r.tc = r.algo == OLC_ALGO_GENERAL_TC;
+        r.b_padded = r.tc && p->const_b_pad && B == p->const_b;
+        r.need = stage_need(p, A, B, r.tc, r.b_padded);
+        r.y_unaligned = r.tc && (yr_off || p->N % 8 != 0);
+        return r;
+    }
+    // the residual is read with the same vector widths as Y is written
+    const bool al = aligned16(A) && aligned16(B) && aligned16(Y) && (!R || aligned16(R));
+    if (!al) r.algo = OLC_ALGO_DIRECT;
+    return r;
+}
+
 olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, cudaStream_t s,
                const void* C = nullptr, const void* R = nullptr) {
     const int64_t n = out_numel(p);
@@ -395,6 +530,15 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         return from_cuda(launch_zero_fill(Y, n * out_bytes(p->dtype), s));
     }
     if (!A || !B) return OLC_ERR_NULL;
+    // every pointer must be aligned to its element size (the kernels load
+    // and store whole elements)
+    {
+        const uintptr_t ein = (uintptr_t)elem_bytes(p->dtype) - 1, eout = (uintptr_t)out_bytes(p->dtype) - 1;
+        if ((reinterpret_cast<uintptr_t>(A) & ein) || (reinterpret_cast<uintptr_t>(B) & ein) ||
+            (reinterpret_cast<uintptr_t>(Y) & eout) || (reinterpret_cast<uintptr_t>(C) & ein) ||
+            (reinterpret_cast<uintptr_t>(R) & eout))
+            return OLC_ERR_INVALID;
+    }
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return from_cuda(cudaErrorNoDevice);
     if (p->device >= 0 && cur != p->device) return OLC_ERR_WRONG_DEVICE;
@@ -409,11 +553,39 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     }
     Problem pr = make_problem(p, A, B, Y, C, R);
     const olc_dtype dt = p->dtype;
-    // the residual is read with the same vector widths as Y is written
-    const bool al = aligned16(A) && aligned16(B) && aligned16(Y) && (!R || aligned16(R));
-    int algo = p->algo;
-    if (!al && algo != OLC_ALGO_DIRECT && algo != OLC_ALGO_GENERAL_SIMT) algo = OLC_ALGO_DIRECT;
+    const Route rt = route_of(p, A, B, Y, R);
+    const int algo = rt.algo;
     cudaError_t e = cudaSuccess;
+    if (rt.need.a || rt.need.b) {
+        const olc_status st = ensure_stage(mp, rt.need.a_bytes + rt.need.b_bytes);
+        if (st != OLC_OK) return st;
+        unsigned char* base = static_cast<unsigned char*>(p->stage);
+        // copy one operand: padded rows for the general tiles, one dense run
+        // otherwise; `ld` receives the row pitch the kernels read (0: dense)
+        auto stage = [&](const void* src, void* dst, const StoredRows& r, int64_t& ld) {
+            if (rt.tc) {
+                ld = pad8(r.cols) != r.cols ? pad8(r.cols) : 0;
+                return launch_pad_rows16(src, dst, r.rows, r.cols, pad8(r.cols), s);
+            }
+            ld = 0;
+            return launch_pad_rows16(src, dst, 1, r.rows * r.cols, pad8(r.rows * r.cols), s);
+        };
+        if (rt.need.a) {
+            e = stage(A, base, stored_a(p), pr.a_ld);
+            if (e != cudaSuccess) return from_cuda(e);
+            pr.A = base;
+        }
+        if (rt.need.b) {
+            e = stage(B, base + rt.need.a_bytes, stored_b(p), pr.b_ld);
+            if (e != cudaSuccess) return from_cuda(e);
+            pr.B = base + rt.need.a_bytes;
+        }
+    }
+    if (rt.b_padded) {
+        pr.B = p->const_b_pad;
+        pr.b_ld = pad8(stored_b(p).cols);
+    }
+    pr.y_unaligned = rt.y_unaligned ? 1 : 0;
     if (is_fp8(dt)) {
         // the plan's constant B comes transposed already
         const void* bt = (p->const_bt && B == p->const_b) ? p->const_bt : nullptr;
@@ -636,6 +808,7 @@ olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const vo
 void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
     if (!plan) return;
     free_workspace(plan);
+    free_stage(plan);
     if (plan->pipe_ready) {
         int cur = -1;
         cudaGetDevice(&cur);
@@ -652,12 +825,13 @@ void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
         if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
         cudaGetLastError();
     }
-    if (plan->const_b || plan->const_bt) {
+    if (plan->const_b || plan->const_bt || plan->const_b_pad) {
         int cur = -1;
         cudaGetDevice(&cur);
         if (plan->device >= 0 && cur != plan->device) cudaSetDevice(plan->device);
         if (plan->const_b) cudaFree(plan->const_b);
         if (plan->const_bt) cudaFree(plan->const_bt);
+        if (plan->const_b_pad) cudaFree(plan->const_b_pad);
         if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
         cudaGetLastError();
     }
@@ -728,6 +902,32 @@ olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, 
         }
         plan->const_bt = mem;
         plan->const_bt_bytes = bytes;
+    }
+    // 16-bit tensor-core plans whose B rows are not 16-byte multiples: keep
+    // B with padded rows as well, the copy every execute would make
+    if (plan->const_b_pad) {
+        cudaFree(plan->const_b_pad);
+        plan->const_b_pad = nullptr;
+        plan->const_b_pad_bytes = 0;
+    }
+    const StoredRows rb = stored_b(plan);
+    if (bytes > 0 && is_half(plan->dtype) && plan->algo == OLC_ALGO_GENERAL_TC && !plan->trans_b &&
+        rb.cols % 8 != 0) {
+        const size_t pbytes = (size_t)(rb.rows * pad8(rb.cols) * 2);
+        void* mem = nullptr;
+        if (cudaMalloc(&mem, pbytes) != cudaSuccess) {
+            cudaGetLastError();
+            return OLC_ERR_OOM;
+        }
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        cudaError_t e = launch_pad_rows16(plan->const_b, mem, rb.rows, rb.cols, pad8(rb.cols), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) {
+            cudaFree(mem);
+            return from_cuda(e);
+        }
+        plan->const_b_pad = mem;
+        plan->const_b_pad_bytes = pbytes;
     }
     plan->const_b_set = 1;
     return OLC_OK;
@@ -806,6 +1006,8 @@ namespace {
 // rows for several tensor-core row tiles per chunk.  0 = not pipelined.
 int host_chunks(const olc_matmul_plan* p) {
     if (p->items != 1 || p->K == 0 || p->residual || is_fp8(p->dtype)) return 0;
+    // chunks read A and write Y in place: rows must be 16-byte multiples
+    if (is_half(p->dtype) && (p->K % 8 != 0 || p->N % 8 != 0)) return 0;
     if (p->algo != OLC_ALGO_GENERAL_TC && p->algo != OLC_ALGO_GENERAL_SIMT) return 0;
     if (p->splits > 1) return 0;          // K-sliced plans use the workspace per launch
     if (p->is_gemm && (p->trans_a || (p->c_rank >= 0 && p->c_rs != 0))) return 0;
@@ -841,7 +1043,7 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_ho
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t eb = elem_bytes(plan->dtype);
     if (!Y_host || !Y_dev) return OLC_ERR_NULL;
-    const int chunks = host_chunks(plan);
+    const int chunks = aligned16(A_dev) && aligned16(B_dev) && aligned16(Y_dev) ? host_chunks(plan) : 0;
     if (chunks > 0) {
         if (!A_host || !B_host || !A_dev || !B_dev) return OLC_ERR_NULL;
         int cur = -1;
@@ -971,6 +1173,19 @@ olc_status olc_matmul_plan_force_algorithm(olc_matmul_plan* plan, int algo) {
     return prepare_algorithm(plan);
 }
 
+int olc_matmul_plan_algorithm_for(const olc_matmul_plan* plan, const void* A, const void* B,
+                                  const void* Y, const void* R) {
+    if (!plan) return -1;
+    return route_of(plan, A, B, Y, R).algo;
+}
+
+int olc_matmul_plan_staging_copies(const olc_matmul_plan* plan, const void* A, const void* B,
+                                   const void* Y, const void* R) {
+    if (!plan) return -1;
+    const Route r = route_of(plan, A, B, Y, R);
+    return (r.need.a ? 1 : 0) + (r.need.b ? 1 : 0);
+}
+
 olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits) {
     if (!plan) return OLC_ERR_NULL;
     if (splits < 0 || splits > 4096) return OLC_ERR_INVALID;
@@ -989,10 +1204,15 @@ olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant) {
 
 int olc_matmul_plan_launches(const olc_matmul_plan* plan) {
     if (!plan) return -1;
-    switch (plan->algo) {
-        case OLC_ALGO_EMPTY: return 0;
-        default: return 1;
+    if (plan->algo == OLC_ALGO_EMPTY) return 0;
+    int n = 1;
+    if (plan->algo == OLC_ALGO_GENERAL_TC && is_half(plan->dtype)) {
+        // staging copies of rows that are not 16-byte multiples
+        const StageNeed need = stage_need(plan, nullptr, nullptr, true, plan->const_b_pad != nullptr);
+        n += (need.a ? 1 : 0) + (need.b ? 1 : 0);
     }
+    if (plan->algo == OLC_ALGO_GENERAL_TC && is_fp8(plan->dtype) && !plan->const_bt) ++n;   // B transpose
+    return n;
 }
 
 size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan) {

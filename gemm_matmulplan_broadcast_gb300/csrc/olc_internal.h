@@ -53,6 +53,14 @@ struct Problem {
     int variant;      // kernel-family override (0: automatic; see olc_matmul_plan_set_tc_variant)
     int a_trans, b_trans;
     Epilogue epi;
+    // Row pitches in elements of A and B as the general tensor-core kernels
+    // read them (0: dense, K for A and N for B).  A pitch above the row
+    // length is a staged copy whose rows were padded to 16-byte multiples.
+    int64_t a_ld, b_ld;
+    // Y (or the residual) is not 16-byte aligned or N is not a multiple of
+    // 8: the general tensor-core kernels store with 2-, 4- and 16-byte
+    // accesses as each row's alignment allows.
+    int y_unaligned;
 };
 
 // Workspace handed to the split reductions: `partials` holds fp32/fp64
@@ -148,7 +156,13 @@ cudaError_t launch_pair_f8(olc_dtype dt, const Problem& p, const void* bt, int s
                            cudaStream_t stream);
 
 // GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
+// tc_shape_ok: the dense operands are TMA-readable as given (16-byte rows).
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
+// Copy `rows` rows of `cols` 16-bit elements (src rows dense, any 2-byte
+// alignment) into dst rows `pitch` elements apart (dst 16-byte aligned,
+// pitch a multiple of 8 >= cols); the pitch's extra elements are zeroed.
+cudaError_t launch_pad_rows16(const void* src, void* dst, int64_t rows, int64_t cols,
+                              int64_t pitch, cudaStream_t stream);
 // variant: 0 automatic, 1 one CTA per 128 x 256 tile, 2 CTA pairs (cta_group::2)
 // with 256 x 256 tiles
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream,

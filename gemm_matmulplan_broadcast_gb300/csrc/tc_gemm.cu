@@ -115,6 +115,7 @@ struct Params {
     int stream;               // 1: stream-K shares (split instantiation only)
     int a_mn;                 // A stored [K, M] (Gemm transA): MN-major A operand
     int b_k;                  // B stored [N, K] (Gemm transB): K-major B operand
+    int y_unaligned;          // Y rows not 16-byte aligned: stores by alignment (general kernels)
     int f8_fmt;               // 8-bit float operands (pair kernel): 0 = E4M3, 1 = E5M2
     Epilogue epi;
     int64_t iterations;       // stream-K: total (tile, K block) iterations
@@ -427,7 +428,7 @@ __device__ __forceinline__ void epi_run(const Params& p, const uint32_t* r, int6
             for (int i = 0; i < 2 * NP; ++i)
                 v[i] = __fadd_rn(v[i], __fmul_rn(beta, widen16(__ldg(c + (col + i) * p.epi.c_cs), p.is_bf16)));
         }
-        if (p.epi.R) {
+        if (p.epi.R && !p.y_unaligned) {
             const uint4* src = reinterpret_cast<const uint4*>(dst + p.epi.r_delta);
             uint32_t rr[NP];
 #pragma unroll
@@ -439,6 +440,13 @@ __device__ __forceinline__ void epi_run(const Params& p, const uint32_t* r, int6
 #pragma unroll
             for (int i = 0; i < 2 * NP; ++i)
                 v[i] = __fadd_rn(v[i], widen16(rr[i >> 1] >> (16 * (i & 1)), p.is_bf16));
+        } else if (p.epi.R) {
+            // unaligned rows: the residual element by element (`groups` is
+            // then the number of valid columns of the run)
+            const unsigned short* src = reinterpret_cast<const unsigned short*>(dst + p.epi.r_delta);
+#pragma unroll
+            for (int i = 0; i < 2 * NP; ++i)
+                if (i < groups) v[i] = __fadd_rn(v[i], widen16(__ldg(src + i), p.is_bf16));
         }
         if (p.epi.act == OLC_ACT_RELU) {
 #pragma unroll
@@ -458,7 +466,7 @@ __device__ __forceinline__ void epi_run(const Params& p, const uint32_t* r, int6
 // (N is a multiple of 8 on the tensor-core path).
 __device__ __forceinline__ void prefetch_residual(const Params& p, int64_t item, int64_t row,
                                                   int64_t col0, int64_t cols) {
-    if (!p.epi.R || cols <= 0) return;
+    if (!p.epi.R || cols <= 0 || p.y_unaligned) return;
     const unsigned char* src = static_cast<const unsigned char*>(p.epi.R) +
                                ((item * p.M + row) * p.N + col0) * 2;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)(cols * 2))
@@ -494,6 +502,70 @@ __device__ __noinline__ void ordered_sum4x2(const float* base, int64_t stride, i
     }
     r0 = a0;
     r1 = a1;
+}
+
+// ---------------------------------------------------------------------------
+// Stores of one 32-column run of 16-bit outputs (element i of the run in half
+// i & 1 of packed[i >> 1]) to a row of Y that need not be 16-byte aligned:
+// the general kernels with an odd N, or a Y pointer off a 16-byte boundary.
+// A full run takes H single elements up to the next 16-byte boundary (pairs
+// as 32-bit stores where the address allows), 16-byte stores of the shifted
+// elements, then the rest; H is the run's start in elements modulo 8, so each
+// of the 8 cases is unrolled with static register indices.
+
+__device__ __forceinline__ uint32_t run_pair(const uint32_t (&pk)[16], int e) {
+    // elements e and e + 1 packed (e static after unrolling)
+    return (e & 1) ? __funnelshift_r(pk[e >> 1], pk[(e >> 1) + 1], 16) : pk[e >> 1];
+}
+__device__ __forceinline__ unsigned short run_elem(const uint32_t (&pk)[16], int e) {
+    return (unsigned short)(pk[e >> 1] >> (16 * (e & 1)));
+}
+
+template <int H>
+__device__ __forceinline__ void store_run_shifted(unsigned short* dst, const uint32_t (&pk)[16]) {
+    constexpr int G = (32 - H) / 8;              // whole 16-byte groups after the head
+    // head: elements 0..H-1 (dst + H is 16-byte aligned)
+    if constexpr (H & 1) {
+        dst[0] = run_elem(pk, 0);
+#pragma unroll
+        for (int e = 1; e < H; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = run_pair(pk, e);
+    } else {
+#pragma unroll
+        for (int e = 0; e < H; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = run_pair(pk, e);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int e = H + 8 * g;
+        *reinterpret_cast<uint4*>(dst + e) =
+            make_uint4(run_pair(pk, e), run_pair(pk, e + 2), run_pair(pk, e + 4), run_pair(pk, e + 6));
+    }
+    // tail: elements H + 8 G .. 31, starting on a 16-byte boundary
+#pragma unroll
+    for (int e = H + 8 * G; e + 1 < 32; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = run_pair(pk, e);
+    if constexpr (((32 - H - 8 * G) & 1) != 0) dst[31] = run_elem(pk, 31);
+}
+
+// `valid` (1..32) elements of the run to dst (2-byte aligned).
+__device__ __forceinline__ void store_run_unaligned(unsigned char* dst_bytes, const uint32_t (&pk)[16],
+                                                    int valid) {
+    unsigned short* dst = reinterpret_cast<unsigned short*>(dst_bytes);
+    if (valid < 32) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            if (e < valid) dst[e] = run_elem(pk, e);
+        return;
+    }
+    const int h = (int)((8 - ((reinterpret_cast<uintptr_t>(dst) >> 1) & 7)) & 7);
+    switch (h) {
+        case 0: store_run_shifted<0>(dst, pk); break;
+        case 1: store_run_shifted<1>(dst, pk); break;
+        case 2: store_run_shifted<2>(dst, pk); break;
+        case 3: store_run_shifted<3>(dst, pk); break;
+        case 4: store_run_shifted<4>(dst, pk); break;
+        case 5: store_run_shifted<5>(dst, pk); break;
+        case 6: store_run_shifted<6>(dst, pk); break;
+        default: store_run_shifted<7>(dst, pk); break;
+    }
 }
 
 // Narrow four float32 sums and store them at output row r, column col of
@@ -750,6 +822,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         if (CH == 32) tmem_ld_32x32b_x32(t_base + c, r);
                         else tmem_ld_32x32b_x16(t_base + c, r);
                         const int64_t col = nb * BN + c;
+                        if constexpr (CH == 32 && !SPLIT) {
+                            if (row_ok && col < p.N && p.y_unaligned) {
+                                const int valid = (int)min64(32, p.N - col);
+                                uint32_t packed[16];
+                                epi_run<16>(p, r, row, col, yrow + col * 2, valid, packed);
+                                store_run_unaligned(yrow + col * 2, packed, valid);
+                                continue;
+                            }
+                        }
                         if (row_ok && col < p.N) {
                             uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                             // N is a multiple of 8: whole 16-byte groups only
@@ -1183,7 +1264,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_base + c, r);
                 const int64_t col = nb * 256 + c;
-                if (row_ok && col < p.N) {
+                if (row_ok && col < p.N && p.y_unaligned) {
+                    const int valid = (int)min64(32, p.N - col);
+                    uint32_t packed[16];
+                    epi_run<16>(p, r, row, col, yrow + col * 2, valid, packed);
+                    store_run_unaligned(yrow + col * 2, packed, valid);
+                } else if (row_ok && col < p.N) {
                     uint4* dst = reinterpret_cast<uint4*>(yrow + col * 2);
                     const int64_t left = (p.N - col) / 8;
                     const int groups = (int)(left < 4 ? left : 4);
@@ -1515,14 +1601,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // rank-3 map over [items][rows][cols] (cols innermost), 16-bit elements,
-// box {box_cols, box_rows, 1} with the given swizzle
+// rows `ld` elements apart (0: dense, ld = cols), box {box_cols, box_rows, 1}
+// with the given swizzle
 static bool encode_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t cols,
                       uint64_t rows, uint64_t items, uint32_t box_cols, uint32_t box_rows,
-                      CUtensorMapSwizzle swizzle) {
+                      CUtensorMapSwizzle swizzle, uint64_t ld = 0) {
     auto fn = encode_fn();
     if (!fn) return false;
+    if (ld == 0) ld = cols;
     cuuint64_t dims[3] = {cols, rows, items};
-    cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+    cuuint64_t strides[2] = {ld * 2, ld * rows * 2};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -1537,6 +1625,21 @@ static CUtensorMapSwizzle b_swizzle() {
     return Cfg<BN>::SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                               : (Cfg<BN>::SW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                    : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// The general tiles' operand requirements: 16-bit types, coordinates in
+// int32, 16-byte aligned A and B with 16-byte row pitches (TMA), and a dense
+// or aligned Y unless the launch stores Y by alignment (y_unaligned).
+static bool tc_operands_ok(olc_dtype dt, const Problem& pr, int64_t a_ld, int64_t b_ld) {
+    if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;
+    if (pr.M >= (1LL << 31) || pr.N >= (1LL << 31) || pr.K >= (1LL << 31)) return false;
+    if ((reinterpret_cast<uintptr_t>(pr.A) & 15) || (reinterpret_cast<uintptr_t>(pr.B) & 15))
+        return false;
+    // stored row lengths: A [M, K] or [K, M] (transA), B [K, N] or [N, K] (transB)
+    if (pr.a_trans ? (pr.M % 8 != 0 || pr.a_ld) : (a_ld % 8 != 0 || a_ld < pr.K)) return false;
+    if (pr.b_trans ? (pr.K % 8 != 0 || pr.b_ld) : (b_ld % 8 != 0 || b_ld < pr.N)) return false;
+    if (!pr.y_unaligned && ((reinterpret_cast<uintptr_t>(pr.Y) & 15) || pr.N % 8 != 0)) return false;
+    return true;
 }
 
 // Shape of a split-K launch: slices, group size, workspace layout.
@@ -1628,7 +1731,15 @@ template <int BN, bool SPLIT, bool SWAP>
 static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
                              const SplitPlan* sp, const Workspace* ws) {
     using C = Cfg<BN>;
-    if (!tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31)) return cudaErrorInvalidValue;
+    const int64_t a_ld = pr.a_ld ? pr.a_ld : pr.K, b_ld = pr.b_ld ? pr.b_ld : pr.N;
+    if (!(SPLIT || SWAP) && BN == 256) {
+        // the general tiles read A and B through row pitches (16-byte rows)
+        // and store Y at any alignment
+        if (!tc_operands_ok(dt, pr, a_ld, b_ld)) return cudaErrorInvalidValue;
+    } else if (!tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31) || pr.a_ld || pr.b_ld ||
+               pr.y_unaligned) {
+        return cudaErrorInvalidValue;
+    }
     if (SWAP && pr.M > BN) return cudaErrorInvalidValue;
     // the operands' batch extents: every item offset is a multiple of the
     // matrix size (dense operands), so offset / size is the TMA batch index
@@ -1652,14 +1763,15 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
             if (!encode_3d(&ma, pr.A, bf, pr.M, pr.K, a_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B))
                 return cudaErrorInvalidValue;
         } else if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, a_box_rows,
-                              CU_TENSOR_MAP_SWIZZLE_128B)) {
+                              CU_TENSOR_MAP_SWIZZLE_128B, a_ld)) {
             return cudaErrorInvalidValue;
         }
         if (pr.b_trans) {
             if (BN != 256) return cudaErrorInvalidValue;
             if (!encode_3d(&mb, pr.B, bf, pr.K, pr.N, b_items, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
                 return cudaErrorInvalidValue;
-        } else if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>())) {
+        } else if (!encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, C::BLK_COLS, BK, b_swizzle<BN>(),
+                              b_ld)) {
             return cudaErrorInvalidValue;
         }
     } else {
@@ -1696,6 +1808,7 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
                             : (uint32_t)((pr.a_trans ? BM : a_box_rows) * BK * 2 + C::B_STAGE_BYTES);
     p.a_mn = pr.a_trans;
     p.b_k = pr.b_trans;
+    p.y_unaligned = pr.y_unaligned;
     p.epi = pr.epi;
     if ((pr.a_trans || pr.b_trans) && (SWAP || SPLIT)) return cudaErrorInvalidValue;
     if (SPLIT) {
@@ -1726,7 +1839,8 @@ static cudaError_t launch_tc(olc_dtype dt, const Problem& pr, int sm_count, cuda
 }
 
 static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s) {
-    if (!tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31)) return cudaErrorInvalidValue;
+    const int64_t a_ld = pr.a_ld ? pr.a_ld : pr.K, b_ld = pr.b_ld ? pr.b_ld : pr.N;
+    if (!tc_operands_ok(dt, pr, a_ld, b_ld)) return cudaErrorInvalidValue;
     int64_t a_items = 1, b_items = 1;
     for (int d = 0; d < pr.map.rank; ++d) {
         if (pr.map.a_stride[d])
@@ -1740,10 +1854,12 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     const int bf = dt == OLC_BFLOAT16;
     const bool at = pr.a_trans != 0, bt = pr.b_trans != 0;
     if (!(at ? encode_3d(&ma, pr.A, bf, pr.M, pr.K, a_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)
-             : encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
+             : encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                         a_ld)))
         return cudaErrorInvalidValue;
     if (!(bt ? encode_3d(&mb, pr.B, bf, pr.K, pr.N, b_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
-             : encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)))
+             : encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                         b_ld)))
         return cudaErrorInvalidValue;
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -1760,6 +1876,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     p.is_bf16 = bf;
     p.a_mn = at;
     p.b_k = bt;
+    p.y_unaligned = pr.y_unaligned;
     p.epi = pr.epi;
     const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.items;
     if (pairs <= 0) return cudaSuccess;
@@ -1989,6 +2106,53 @@ static double operand_bytes(const Problem& pr) {
 }
 
 }  // namespace tc
+
+// Row-pitch staging copy for operands the TMA cannot read in place: each
+// thread writes one 16-byte group of a destination row, loading its source
+// elements with the widest accesses the source address allows (the source
+// rows are dense with any 2-byte alignment).
+__global__ void pad_rows16_kernel(const unsigned short* __restrict__ src, uint4* __restrict__ dst,
+                                  int64_t rows, int64_t cols, int64_t pitch) {
+    const int64_t groups_per_row = pitch / 8;
+    const int64_t total = rows * groups_per_row;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = g / groups_per_row;
+        const int64_t c0 = (g - r * groups_per_row) * 8;
+        const unsigned short* s = src + r * cols + c0;
+        uint32_t w[4];
+        if (c0 + 8 <= cols && (reinterpret_cast<uintptr_t>(s) & 3) == 0) {
+            const uint32_t* s4 = reinterpret_cast<const uint32_t*>(s);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = __ldg(s4 + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo = c0 + 2 * j < cols ? __ldg(s + 2 * j) : 0u;
+                const uint32_t hi = c0 + 2 * j + 1 < cols ? __ldg(s + 2 * j + 1) : 0u;
+                w[j] = lo | (hi << 16);
+            }
+        }
+        dst[g] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+cudaError_t launch_pad_rows16(const void* src, void* dst, int64_t rows, int64_t cols, int64_t pitch,
+                              cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (pitch % 8 != 0 || pitch < cols || (reinterpret_cast<uintptr_t>(dst) & 15) ||
+        (reinterpret_cast<uintptr_t>(src) & 1))
+        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t total = rows * (pitch / 8);
+    const int64_t blocks = min64(ceil_div(total, 256), (int64_t)sms * 8);
+    pad_rows16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const unsigned short*>(src),
+                                                            static_cast<uint4*>(dst), rows, cols, pitch);
+    return cudaGetLastError();
+}
 
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K) {
     if (dt != OLC_FLOAT16 && dt != OLC_BFLOAT16) return false;

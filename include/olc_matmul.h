@@ -74,7 +74,7 @@ typedef enum {
     OLC_ERR_DEVICE_TIMEOUT = 11,  /* a bounded device-side wait ran out            */
     OLC_ERR_OOM = 12,             /* workspace allocation failed                   */
     OLC_ERR_INVALID = 13,         /* an argument is out of its documented range    */
-    OLC_ERR_WRONG_DEVICE = 14,    /* current device differs from the plan's        */
+    OLC_ERR_WRONG_DEVICE = 14,    /* current device differs from the plan or stream */
     OLC_ERR_SCRATCH_LIMIT = 15,   /* needs more than the static scratch array      */
     OLC_ERR_NEEDS_RESIDUAL = 16   /* the plan fuses a residual: use the fused call */
 } olc_status;
@@ -158,11 +158,24 @@ void olc_matmul_plan_destroy(olc_matmul_plan* plan);
  *  An output with no elements returns OLC_OK without launching anything and
  *     without reading A, B or Y (they may be NULL).  With K == 0 and a
  *     non-empty output, Y is filled with zeros and A and B are not read.
- *  The tensor-core, skinny and split-K paths need 16-byte aligned A, B and Y;
- *     with pointers that are not, the execute runs the DIRECT kernel instead.
+ *  Alignment: FLOAT16 / BFLOAT16 products stay on the tensor cores for any
+ *     2-byte aligned pointers and any N and K.  An operand the kernels
+ *     cannot read in place (pointer off a 16-byte boundary; on the general
+ *     tiles, stored rows that are not a multiple of 16 bytes) is first
+ *     copied by a kernel of this library into a staging buffer the plan
+ *     owns: allocated (cudaMalloc) at olc_matmul_plan_create when the shape
+ *     alone needs it, otherwise at the first execute that does -- make that
+ *     first call before any stream capture.  The general tiles store a Y of
+ *     any alignment; skinny and split-K products with a misaligned Y (or
+ *     residual) run on the general tiles.  FLOAT, DOUBLE and the 8-bit
+ *     types need 16-byte aligned A, B and Y on their skinny, split-K and
+ *     tensor-core paths and run the DIRECT kernel otherwise.
+ *     olc_matmul_plan_algorithm_for / _staging_copies report the route.
  *
  * Errors: OLC_ERR_NULL (plan, or a data pointer of a non-empty product),
- * OLC_ERR_WRONG_DEVICE, OLC_ERR_CUDA (a launch failed), OLC_ERR_OOM.
+ * OLC_ERR_INVALID (a pointer not aligned to its element size),
+ * OLC_ERR_WRONG_DEVICE, OLC_ERR_CUDA (a launch failed), OLC_ERR_OOM (a
+ * staging buffer could not be allocated).
  * Device-side failures are not seen here; use olc_matmul_execute_checked.
  */
 olc_status olc_matmul_execute(const olc_matmul_plan* plan, const void* A, const void* B,
@@ -259,7 +272,11 @@ olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const vo
  * directly.  A plan with 8-bit float operands on the tensor cores also keeps
  * B transposed ([N, K] bytes, the K-major operand the MMA reads; b_numel more
  * bytes of device memory), so executes with the constant B skip the
- * transpose that an execute with a caller's B runs first.  Errors:
+ * transpose that an execute with a caller's B runs first.  Likewise a
+ * FLOAT16 / BFLOAT16 plan on the general tensor-core tiles whose B rows are
+ * not a multiple of 16 bytes (N not a multiple of 8) keeps B with rows
+ * padded to 8 elements, so executes with the constant B copy nothing.
+ * Errors:
  * OLC_ERR_NULL, OLC_ERR_BUFFER_TOO_SMALL (b_numel is not the planned size),
  * OLC_ERR_WRONG_DEVICE, OLC_ERR_OOM, OLC_ERR_CUDA.
  */
@@ -384,6 +401,25 @@ olc_status olc_matmul_plan_launch_shape(const olc_matmul_plan* plan, int64_t* ro
 /* Selected algorithm (an olc_algorithm value), or -1 for a NULL plan. */
 int olc_matmul_plan_algorithm(const olc_matmul_plan* plan);
 
+/* The algorithm an execute with these pointers runs (R: the fused
+ * residual, or NULL), or -1 for a NULL plan.  It differs from the plan's
+ * algorithm only for pointers off a 16-byte boundary: FLOAT16 / BFLOAT16
+ * skinny and split-K products whose Y (or R) is misaligned run on the
+ * general tensor-core tiles, and other types' products with any misaligned
+ * pointer run on DIRECT.  Host only; nothing is launched. */
+int olc_matmul_plan_algorithm_for(const olc_matmul_plan* plan, const void* A, const void* B,
+                                  const void* Y, const void* R);
+
+/* Staging copies (0, 1 or 2) an execute with these pointers makes before its
+ * product kernel, or -1 for a NULL plan.  FLOAT16 / BFLOAT16 products on the
+ * tensor cores copy an operand the kernels cannot read in place: one whose
+ * pointer is off a 16-byte boundary, and, on the general tiles, one whose
+ * stored rows are not a multiple of 16 bytes (K or N not a multiple of 8) --
+ * into rows padded to 8 elements that the tiles read through a row pitch.
+ * Host only; nothing is launched. */
+int olc_matmul_plan_staging_copies(const olc_matmul_plan* plan, const void* A, const void* B,
+                                   const void* Y, const void* R);
+
 /* Force an algorithm (testing and tuning sweeps); OLC_ALGO_AUTO restores the
  * automatic choice.  Errors: OLC_ERR_NULL, OLC_ERR_INVALID (unknown value),
  * OLC_ERR_ALIGNMENT (the algorithm cannot take this shape or type),
@@ -418,10 +454,15 @@ int olc_matmul_plan_splits(const olc_matmul_plan* plan);
  * OLC_ERR_NULL, OLC_ERR_INVALID. */
 olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant);
 
-/* Kernel launches one execute of this plan makes (0 for EMPTY). */
+/* Kernel launches one execute of this plan makes with 16-byte aligned
+ * pointers (0 for EMPTY): the product kernel, plus the staging copies its
+ * shape needs (FLOAT16 / BFLOAT16 on the general tiles with K or N not a
+ * multiple of 8; none for a B kept padded with the plan's constant B), plus
+ * the B transpose of 8-bit tensor-core plans without a constant B. */
 int olc_matmul_plan_launches(const olc_matmul_plan* plan);
 
-/* Bytes of device workspace the plan owns (split reductions), 0 if none. */
+/* Bytes of device workspace the plan owns for split reductions (and the
+ * FP8 B transpose), 0 if none; staging buffers are not included. */
 size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan);
 
 /* One-line description of the plan (algorithm, tile, grid, splits) written
@@ -457,6 +498,17 @@ uint32_t olc_debug_f8_instr_desc(int fmt, int m, int n);
  * is read and cleared); the CUDA context stays usable either way. */
 olc_status olc_debug_wait_selftest(uint64_t limit_ns, int arrive, void* stream);
 
+/* Measurement hook: the arithmetic rate the FP32 / FP64 pipes deliver on the
+ * current device (the FLOAT and DOUBLE kernels keep native precision, so
+ * their roofline is the FMA pipes, not the tensor cores or memory).  Runs
+ * SM count x 4 blocks of 256 threads, each thread `iters` iterations of
+ * independent FMA chains with no memory traffic, timed with CUDA events on
+ * `stream` (synchronised); *flops receives flop/s (an FMA counts 2).
+ * kind: 0 = paired FP32 FMA (fma.rn.f32x2), 1 = FP32 FMA, 2 = FP64 FMA,
+ * 3 = FP64 tensor-core MMA (mma.sync m8n8k4 .f64).  Errors: OLC_ERR_NULL,
+ * OLC_ERR_INVALID (kind outside 0..3, iters outside 1..2^40), OLC_ERR_CUDA. */
+olc_status olc_debug_alu_rate(int kind, int64_t iters, void* stream, double* flops);
+
 /* ---- allocation-free split-K ------------------------------------------- */
 
 /* Size of the device array behind olc_matmul_split_k_static: 4 MiB, held by
@@ -486,9 +538,19 @@ olc_status olc_debug_wait_selftest(uint64_t limit_ns, int arrive, void* stream);
  *  fills Y with zeros.
  *  stream: cudaStream_t as void* (NULL = legacy default stream).
  *
+ * `stream` must belong to the current device (OLC_ERR_WRONG_DEVICE
+ * otherwise): the array's address and the SM count are the current
+ * device's.
+ *
  * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture on that device.  Every call clears the arrival counters
+ * device (cudaGetSymbolAddress) and caches it.  Under CUDA's default lazy
+ * module loading that lookup (or any earlier split-K launch of this
+ * library) is also what loads the library's split-K module onto the device,
+ * and with it the array: so the first call itself commits the 4 MiB of
+ * device memory, and fails with OLC_ERR_CUDA if nothing is left.  Make that
+ * first call at set-up time -- before a memory pool takes the rest of the
+ * device, and before any stream capture on that device; later calls
+ * allocate nothing.  Every call clears the arrival counters
  * with cudaMemsetAsync on `stream` before its kernel, so a call never depends
  * on what the previous one left in the array; but all calls share the one
  * array, so calls whose executions overlap on the GPU (other streams, other
@@ -501,7 +563,9 @@ olc_status olc_debug_wait_selftest(uint64_t limit_ns, int arrive, void* stream);
  *
  * Errors: OLC_ERR_DTYPE, OLC_ERR_NULL (a pointer of a non-empty product),
  * OLC_ERR_NEGATIVE_DIM, OLC_ERR_SCRATCH_LIMIT (more output tiles than the
- * limits above), OLC_ERR_CUDA (the address lookup, memset or launch failed).
+ * limits above), OLC_ERR_WRONG_DEVICE (`stream` belongs to another device
+ * than the current one), OLC_ERR_CUDA (the address lookup, memset or
+ * launch failed).
  * Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 olc_status olc_matmul_split_k_static(olc_dtype dtype, const void* A, const void* B, void* Y,

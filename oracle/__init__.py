@@ -89,6 +89,8 @@ def _load():
             fn.restype = None
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = None
         _lib = lib
         return lib
 
@@ -96,6 +98,12 @@ def _load():
 def threads() -> int:
     """Host threads the oracle's parallel loops use."""
     return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Use `n` host threads from now on (1: a single-core timing).  Results
+    do not depend on it: each output row is one thread's k-ordered sum."""
+    _load().oracle_set_threads(int(n))
 
 
 def _ptr(a: np.ndarray):

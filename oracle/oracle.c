@@ -51,6 +51,17 @@ int oracle_threads(void) {
 #endif
 }
 
+/* Set the number of host threads (n >= 1) for the following calls; used
+ * to time the oracle on one core.  The results do not depend on it: every
+ * output row is computed by one thread in the same k order. */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* IEEE 754 binary16 -> binary32 (exact).  Fields: 1 sign bit, 5 exponent bits
  * (bias 15), 10 fraction bits.  exponent 0 = zero / subnormal (value =
