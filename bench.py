@@ -712,6 +712,64 @@ def measure_split_k_static(device, l2):
     return out
 
 
+def measure_unaligned(device, peaks, l2):
+    """FLOAT16 / BFLOAT16 products the TMA cannot read in place, on the
+    tensor cores: the output projection [16384, 4096] x [4096, 50257] BF16
+    (N odd: B is staged into padded rows every call, or once with a
+    plan-owned constant B; Y stored by alignment), and the up projection
+    [16384, 4096] x [4096, 14336] with A one element into its buffer (A
+    staged every call) beside the same product aligned.  CUDA graphs of
+    back-to-back launches; the operands exceed L2."""
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import Plan, synth
+    stream = torch.cuda.Stream()
+    out = []
+    # the vocabulary projection
+    a, b = synth.operands((16384, 4096), (4096, 50257), "bfloat16", synth.normal(1.0),
+                          synth.normal(0.02), 2)
+    flop, byts = work_of((16384, 4096), (4096, 50257), "bfloat16")
+    A, B = a.to(device), b.to(device)
+    Y = torch.empty(16384, 50257, dtype=torch.bfloat16, device=device)
+    p = Plan((16384, 4096), (4096, 50257), "bfloat16")
+    pc = Plan((16384, 4096), (4096, 50257), "bfloat16")
+    pc.set_constant_b(B)
+    for label, fn, plan in (("vocab_50257_per_call_b", lambda i: p.execute(A, B, Y, stream=stream), p),
+                            ("vocab_50257_constant_b", lambda i: pc.execute_constant(A, Y, stream=stream), pc)):
+        ms = statistics.median(graph_time(fn, 1, stream, reps=5, launches=2))
+        out.append({"product": label, "a": [16384, 4096], "b": [4096, 50257],
+                    "algorithm": plan.algorithm, "launches": plan.launches,
+                    "ms_per_launch": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+                    "frac": flop / (ms * 1e-3) / 1e12 / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])})
+    p.close()
+    pc.close()
+    del A, B, Y
+    torch.cuda.empty_cache()
+    # the up projection, aligned and with A one element off
+    a, b = synth.operands((8, 2048, 4096), (4096, 14336), "bfloat16", synth.normal(1.0),
+                          synth.normal(0.02), 2)
+    flop, _ = work_of((8, 2048, 4096), (4096, 14336), "bfloat16")
+    abuf = torch.empty(a.numel() + 8, dtype=torch.bfloat16, device=device)
+    A_al = abuf[:a.numel()].view(a.shape)
+    A_al.copy_(a.to(device))
+    abuf2 = torch.empty(a.numel() + 8, dtype=torch.bfloat16, device=device)
+    A_off = abuf2[1:1 + a.numel()].view(a.shape)
+    A_off.copy_(a.to(device))
+    B = b.to(device)
+    Y = torch.empty(8, 2048, 14336, dtype=torch.bfloat16, device=device)
+    p = Plan((8, 2048, 4096), (4096, 14336), "bfloat16")
+    for label, AA in (("up_proj_aligned", A_al), ("up_proj_a_offset_1", A_off)):
+        ms = statistics.median(graph_time(lambda i: p.execute(AA, B, Y, stream=stream), 1, stream,
+                                          reps=5, launches=2))
+        out.append({"product": label, "a": [8, 2048, 4096], "b": [4096, 14336],
+                    "algorithm": p.algorithm_for(AA, B, Y), "staging_copies": p.staging_copies(AA, B, Y),
+                    "ms_per_launch": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+                    "frac": flop / (ms * 1e-3) / 1e12 / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])})
+    p.close()
+    del abuf, abuf2, B, Y
+    torch.cuda.empty_cache()
+    return out
+
+
 def oracle_single_thread(names):
     """The oracle on one host core over the small named workloads, in full."""
     import oracle
@@ -776,6 +834,10 @@ def compact_summary(breakdown, secondary):
         st = secondary["split_k_static"]
         out["split_k_static_us"] = {"static": _short(st["ms_static"] * 1e3),
                                     "plan": _short(st["ms_plan"] * 1e3)}
+    if "unaligned_tc" in secondary:
+        out["unaligned_tc"] = {r["product"]: "%s us %s TFLOP/s (%s)" % (
+            _short(r["ms_per_launch"] * 1e3), _short(r["tflops"]), _short(r["frac"]))
+            for r in secondary["unaligned_tc"]}
     if "alu_rates" in secondary:
         out["alu_tflops"] = {k: _short(v["tflops"]) for k, v in secondary["alu_rates"].items()}
     return out
@@ -850,6 +912,7 @@ def run_ours(args):
             secondary[wname] = measure_secondary(synth.workload(wname), device, peaks, l2)
         secondary["split_k_curve"] = measure_split_k_curve(device, peaks, l2)
         secondary["split_k_static"] = measure_split_k_static(device, l2)
+        secondary["unaligned_tc"] = measure_unaligned(device, peaks, l2)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)
         secondary["grouped_small_products"] = measure_grouped(device, peaks)
         secondary["alu_rates"] = measure_alu(stream)
