@@ -250,27 +250,39 @@ def rotate_sets(items, min_total_bytes, device):
         it["sets"] = sets
 
 
-def time_steps(items, steps, stream):
+def time_steps(items, steps, stream, chunk=5):
     """Run `steps` steps; returns (total seconds by the outer events,
-    per-product list of per-launch milliseconds)."""
+    per-product list of per-launch milliseconds, one sample per chunk).
+
+    The steps run in chunks of `chunk`: each product's launches of a chunk
+    go back to back (rotating over its operand sets), products in turn, with
+    CUDA events only around each product's run of launches.  An event
+    between two launches would end the programmatic dependent launch that
+    lets a kernel's prologue overlap its predecessor's tail (6-12 us per
+    launch on the projections), so events sit only at chunk boundaries;
+    taking the products in turn chunk by chunk spreads the clock drift of a
+    long run evenly over them."""
     import torch
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    bounds = [(s0, min(steps, s0 + chunk)) for s0 in range(0, steps, chunk)]
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(steps)] for _ in items]
+            for _ in bounds] for _ in items]
     with torch.cuda.stream(stream):
         start.record(stream)
-        for s in range(steps):
+        for c, (s0, s1) in enumerate(bounds):
             for i, it in enumerate(items):
-                A, B, Y = it["sets"][s % len(it["sets"])]
-                e0, e1 = evs[i][s]
+                e0, e1 = evs[i][c]
                 e0.record(stream)
-                it["plan"].execute(A, B, Y, stream=stream)
+                for s in range(s0, s1):
+                    A, B, Y = it["sets"][s % len(it["sets"])]
+                    it["plan"].execute(A, B, Y, stream=stream)
                 e1.record(stream)
         end.record(stream)
     end.synchronize()
     total = start.elapsed_time(end) / 1e3
-    per = [[e0.elapsed_time(e1) for (e0, e1) in evs[i]] for i in range(len(items))]
+    per = [[evs[i][c][0].elapsed_time(evs[i][c][1]) / (s1 - s0) for c, (s0, s1) in enumerate(bounds)]
+           for i in range(len(items))]
     return total, per
 
 

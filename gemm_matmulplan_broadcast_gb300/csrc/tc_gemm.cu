@@ -116,6 +116,8 @@ struct Params {
     int a_mn;                 // A stored [K, M] (Gemm transA): MN-major A operand
     int b_k;                  // B stored [N, K] (Gemm transB): K-major B operand
     int y_unaligned;          // Y rows not 16-byte aligned: stores by alignment (general kernels)
+    int64_t pair_half_tiles;  // CTA pairs: the last tiles, run as two 256 x 128 halves each (a
+                              // last partial wave of at most half the clusters); 0: none
     int f8_fmt;               // 8-bit float operands (pair kernel): 0 = E4M3, 1 = E5M2
     Epilogue epi;
     int64_t iterations;       // stream-K: total (tile, K block) iterations
@@ -1091,6 +1093,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int64_t ptm = ceil_div(p.M, 256), ptn = ceil_div(p.N, 256);
     const int64_t per_item = ptm * ptn;
     const int64_t total = per_item * p.items;
+    // work units: tiles [0, pair_full) whole, then each later tile as two
+    // halves of 128 columns, so that a last partial wave of r tiles keeps
+    // 2r clusters busy for half as long
+    const int64_t full = total - (p.pair_half_tiles < total ? p.pair_half_tiles : total);
+    const int64_t units = full + 2 * (total - full);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -1114,6 +1121,16 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     grid_dependency_wait();
     grid_launch_dependents();
 
+    // unit u -> tile and half (-1: the whole 256 columns; 0 / 1: columns
+    // 0..127 / 128..255 of the tile)
+    auto unit_tile = [&](int64_t u, int& half) -> int64_t {
+        if (u < full) {
+            half = -1;
+            return u;
+        }
+        half = (int)((u - full) & 1);
+        return full + (u - full) / 2;
+    };
     auto coords = [&](int64_t t, int64_t& item, int64_t& mb, int64_t& nb) {
         item = t / per_item;
         const int64_t r = t % per_item;
@@ -1135,21 +1152,27 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             bool armed[STAGES];
             for (int i = 0; i < STAGES; ++i) armed[i] = false;
             bool ok = true;
-            for (int64_t t = cluster_id(); t < total && ok; t += cluster_count()) {
+            for (int64_t u = cluster_id(); u < units && ok; u += cluster_count()) {
+                int half;
+                const int64_t t = unit_tile(u, half);
                 int64_t item, mb, nb;
                 coords(t, item, mb, nb);
                 int64_t a_off, b_off;
                 batch_offsets(p.map, item, a_off, b_off);
                 const int a_item = (int)(a_off / p.a_item_elems);
                 const int b_item = (int)(b_off / p.b_item_elems);
-                const int m0 = (int)(mb * 256 + rank * 128), n0 = (int)(nb * 256 + rank * 128);
+                // each CTA stages its half of the unit's B columns: 128 of a
+                // whole tile, 64 of a half tile
+                const int m0 = (int)(mb * 256 + rank * 128);
+                const int n0 = half < 0 ? (int)(nb * 256 + rank * 128) : (int)(nb * 256 + half * 128 + rank * 64);
+                const uint32_t tx = half < 0 ? 2u * STAGE_BYTES : 2u * (A_BYTES + B_BYTES / 2);
                 for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     unsigned char* sa = base + stage * STAGE_BYTES;
                     unsigned char* sb = sa + A_BYTES;
                     const uint32_t full_leader = map_to(&s->full[stage], 0);
                     if (leader) {
-                        mbar_arrive_expect_tx(&s->full[stage], 2 * STAGE_BYTES);
+                        mbar_arrive_expect_tx(&s->full[stage], tx);
                         armed[stage] = true;
                         armed_parity[stage] = phase;
                     }
@@ -1162,7 +1185,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     if (!p.b_k) {
                         tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
-                        tma_load_3d_pair(sb + 64 * BK * 2, &tmap_b, full_leader, n0 + 64, k0, b_item);
+                        if (half < 0)
+                            tma_load_3d_pair(sb + 64 * BK * 2, &tmap_b, full_leader, n0 + 64, k0, b_item);
                     } else {
                         tma_load_3d_pair(sb, &tmap_b, full_leader, k0, n0, b_item);
                     }
@@ -1178,9 +1202,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (lane == 0 && leader) {
             const uint32_t idesc = F8 ? f8_desc(p.f8_fmt, 256, 256)
                                       : instr_desc(p.is_bf16, 256, 256, p.a_mn, p.b_k ? 0 : 1);
+            const uint32_t idesc_half = F8 ? idesc : instr_desc(p.is_bf16, 256, 128, p.a_mn, p.b_k ? 0 : 1);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int64_t t = cluster_id(); t < total && ok; t += cluster_count()) {
+            for (int64_t u = cluster_id(); u < units && ok; u += cluster_count()) {
+                int half;
+                unit_tile(u, half);
+                const uint32_t id = half < 0 ? idesc : idesc_half;
                 if (!mbar_wait(&s->acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * 256;
@@ -1195,8 +1223,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                    : smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
                         const uint64_t bd = p.b_k ? smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u)
                                                   : smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
-                        if constexpr (F8) mma2_f8(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                        else mma2_f16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (F8) mma2_f8(d_tmem, ad, bd, id, (kb > 0 || kk > 0) ? 1u : 0u);
+                        else mma2_f16(d_tmem, ad, bd, id, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     commit2_both(&s->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -1213,12 +1241,17 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int row_in_tile = lane_group * 32 + lane;
         const uint32_t acc_empty_leader[2] = {map_to(&s->acc_empty[0], 0), map_to(&s->acc_empty[1], 0)};
         uint32_t acc = 0, acc_phase = 0;
-        for (int64_t t = cluster_id(); t < total; t += cluster_count()) {
+        for (int64_t u = cluster_id(); u < units; u += cluster_count()) {
+            int half;
+            const int64_t t = unit_tile(u, half);
             int64_t item, mb, nb;
             coords(t, item, mb, nb);
+            // the unit's columns: [cbase, cbase + width) of the output
+            const int64_t cbase = nb * 256 + (half < 0 ? 0 : half * 128);
+            const int width = half < 0 ? 256 : 128;
             if (!F8 && mb * 256 + rank * 128 + row_in_tile < p.M)
-                prefetch_residual(p, item, mb * 256 + rank * 128 + row_in_tile, nb * 256,
-                                  min64(256, p.N - nb * 256));
+                prefetch_residual(p, item, mb * 256 + rank * 128 + row_in_tile, cbase,
+                                  min64(width, p.N - cbase));
             if (!mbar_wait(&s->acc_full[acc], acc_phase, abort_flag, p.err)) break;
             tc_fence_after();
             const int64_t row = mb * 256 + rank * 128 + row_in_tile;
@@ -1260,10 +1293,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
                                   ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
 #pragma unroll 1
-            for (int c = 0; c < 256; c += 32) {
+            for (int c = 0; c < width; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_base + c, r);
-                const int64_t col = nb * 256 + c;
+                const int64_t col = cbase + c;
                 if (row_ok && col < p.N && p.y_unaligned) {
                     const int valid = (int)min64(32, p.N - col);
                     uint32_t packed[16];
@@ -1883,7 +1916,15 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     const cudaError_t attr_err =
         set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<false>), pair::SMEM_BYTES);
     if (attr_err != cudaSuccess) return attr_err;
-    const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
+    // a last partial wave of r tiles on at most half the clusters runs as 2r
+    // half tiles (256 x 128): the same work on twice the SMs, so the wave
+    // takes about half as long (the 4096 x 4096 projection: 1024 tiles, 13
+    // whole waves of 76 and 36 tiles left -> 72 halves)
+    const int64_t per_wave = sm_count / 2;
+    const int64_t tail = per_wave > 0 ? pairs % per_wave : 0;
+    if (!bt && tail > 0 && 2 * tail <= per_wave) p.pair_half_tiles = tail;
+    const int64_t units = pairs + p.pair_half_tiles;
+    const int64_t clusters = min64(units, per_wave);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);

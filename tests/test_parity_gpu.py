@@ -437,6 +437,12 @@ TC_PAIR_SHAPES = [
     ((130, 64), (64, 136)),            # the peer CTA's rows and columns out of range
     ((3, 1, 260, 64), (1, 2, 64, 264)),
     ((1024, 2048), (2048, 1024)),      # several pair tiles per cluster
+    # a last partial wave of at most half the clusters runs as 256 x 128
+    # half tiles (on 76 clusters): 77 tiles -> 76 whole and one split; 256
+    # tiles -> 228 whole and 28 split; 10 tiles -> all split
+    ((1792, 512), (512, 2816)),
+    ((4096, 256), (256, 4096)),
+    ((3, 1, 500, 128), (1, 2, 128, 600)),
 ]
 
 
