@@ -380,6 +380,18 @@ int choose_algorithm(const olc_matmul_plan* p) {
     const int64_t tiles = ((rows + 127) / 128) * ((N + 127) / 128) * items;
     if (tiles * 2 <= p->sm_count && K >= 8 * 1024 && feasible(p, OLC_ALGO_SPLIT_K))
         return OLC_ALGO_SPLIT_K;
+    // Short-K FLOAT / DOUBLE products that leave the register-tile kernel
+    // few tiles per SM: DIRECT's whole-K 32 x 32 tiles (one global round
+    // trip per tile, four times as many blocks) are faster.  Measured on
+    // GB300 (us, whole-K against register tiles): FLOAT 512x256x512 14 / 26,
+    // 1024x256x64 9 / 25, 256x256x2048 25 / 26, but 1024x256x1024 43 / 27;
+    // DOUBLE 1024x128x1024 227 / 260, 2048x64x512 115 / 132.
+    if (!is_half(p->dtype)) {
+        const Problem pr = make_problem(p, nullptr, nullptr, nullptr);
+        const int64_t tiles64 = ((rows + 63) / 64) * ((N + 63) / 64) * items;
+        const bool few = p->dtype == OLC_FLOAT ? tiles * 4 <= p->sm_count : tiles64 <= 4 * p->sm_count;
+        if (few && direct_wholek_ok(p->dtype, pr)) return OLC_ALGO_DIRECT;
+    }
     if (is_half(p->dtype) && feasible(p, OLC_ALGO_GENERAL_TC)) return OLC_ALGO_GENERAL_TC;
     return is_half(p->dtype) ? OLC_ALGO_DIRECT : OLC_ALGO_GENERAL_SIMT;
 }

@@ -84,8 +84,11 @@ cudaError_t launch_zero_fill(void* Y, int64_t bytes, cudaStream_t stream);
 // K == 0 with a Gemm epilogue: Y = beta * C (the product term is empty)
 cudaError_t launch_epilogue_fill(olc_dtype dt, const Problem& p, cudaStream_t stream);
 
-// DIRECT: small tiles, scalar loads, any shape and alignment.
+// DIRECT: small tiles, scalar loads, any shape and alignment.  FLOAT /
+// DOUBLE products with K <= 256 / 128 (operands as given) fetch the whole K
+// range of a tile at once (direct_wholek_ok).
 cudaError_t launch_direct(olc_dtype dt, const Problem& p, cudaStream_t stream);
+bool direct_wholek_ok(olc_dtype dt, const Problem& p);
 
 // GENERAL_SIMT: FP32 FFMA / FP64 DFMA register-tiled kernel (any dtype works;
 // the plan routes FLOAT and DOUBLE here).  FLOAT products with fewer tiles

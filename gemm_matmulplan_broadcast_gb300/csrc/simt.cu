@@ -186,7 +186,119 @@ static cudaError_t launch_tile(const Problem& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// DIRECT for small FLOAT / DOUBLE products: the whole K range at once.
+//
+// Small products are latency-bound: the slice loop above pays one global
+// round trip per 16-deep slice.  Here a block issues every element copy of
+// its 32 x K strip of A and K x 32 strip of B at once (cp.async, one element
+// each, so any alignment and any K), waits once, and then multiplies from
+// shared memory; each thread sums its 2 x 2 outputs over k ascending with
+// fused multiply-adds, as the slice kernel does.  K is bounded so that both
+// strips fit in 64 KiB of shared memory (K <= 256 for FLOAT, 128 for
+// DOUBLE); operands stored as given (no Gemm transposes).
+
+template <typename T>
+constexpr int wholek_max_k() { return sizeof(T) == 4 ? 256 : 128; }
+
+__device__ __forceinline__ void cp_async_elem(void* smem, const void* gmem, int bytes) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    if (bytes == 4)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) wholek_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
+    extern __shared__ __align__(16) unsigned char wk_smem[];
+    const int64_t K = p.K;
+    const int ks = (int)K + 1;                 // A row stride: odd, so the two rows a warp reads differ in bank
+    T* As = reinterpret_cast<T*>(wk_smem);     // [32][ks]
+    T* Bs = As + 32 * ks;                      // [K][32]
+
+    const int64_t per_item = tiles_m * tiles_n;
+    const int64_t item = blockIdx.x / per_item;
+    const int64_t rem = blockIdx.x % per_item;
+    const int64_t m0 = (rem / tiles_n) * 32;
+    const int64_t n0 = (rem % tiles_n) * 32;
+    int64_t a_off, b_off;
+    batch_offsets(p.map, item, a_off, b_off);
+    const T* __restrict__ A = static_cast<const T*>(p.A) + a_off;
+    const T* __restrict__ B = static_cast<const T*>(p.B) + b_off;
+    T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
+    const int64_t M = p.M, N = p.N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // A rows m0 + r (r = warp, warp + 8, ...), lanes along k; B rows k
+    // (k = warp, warp + 8, ...), lanes along n.  Outside the product: zeros.
+    for (int r = warp; r < 32; r += 8) {
+        const bool ok = m0 + r < M;
+        const T* src = A + (m0 + r) * K;
+        for (int k = lane; k < (int)K; k += 32) {
+            if (ok) cp_async_elem(As + r * ks + k, src + k, (int)sizeof(T));
+            else As[r * ks + k] = T(0);
+        }
+    }
+    const bool col_ok = n0 + lane < N;
+    for (int k = warp; k < (int)K; k += 8) {
+        if (col_ok) cp_async_elem(Bs + k * 32 + lane, B + (int64_t)k * N + n0 + lane, (int)sizeof(T));
+        else Bs[k * 32 + lane] = T(0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    T c00 = T(0), c01 = T(0), c10 = T(0), c11 = T(0);
+    const T* a0p = As + ty * ks;
+    const T* a1p = As + (ty + 16) * ks;
+#pragma unroll 4
+    for (int k = 0; k < (int)K; ++k) {
+        const T a0 = a0p[k], a1 = a1p[k];
+        const T b0 = Bs[k * 32 + tx], b1 = Bs[k * 32 + tx + 16];
+        c00 = fma(a0, b0, c00);
+        c01 = fma(a0, b1, c01);
+        c10 = fma(a1, b0, c10);
+        c11 = fma(a1, b1, c11);
+    }
+    const T c[2][2] = {{c00, c01}, {c10, c11}};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int64_t gm = m0 + ty + 16 * i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t gn = n0 + tx + 16 * j;
+            if (gn < N) Y[gm * N + gn] = apply_epilogue<T>(p.epi, c[i][j], gm, gn, Y + gm * N + gn);
+        }
+    }
+}
+
+bool direct_wholek_ok(olc_dtype dt, const Problem& p) {
+    if (p.a_trans || p.b_trans || p.K < 1) return false;
+    if (dt == OLC_FLOAT) return p.K <= wholek_max_k<float>();
+    if (dt == OLC_DOUBLE) return p.K <= wholek_max_k<double>();
+    return false;
+}
+
+template <typename T>
+static cudaError_t launch_wholek(const Problem& p, cudaStream_t stream) {
+    const int64_t tm = ceil_div(p.M, 32), tn = ceil_div(p.N, 32);
+    const int64_t blocks = tm * tn * p.items;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)(32 * (p.K + 1) + p.K * 32) * sizeof(T);
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(wholek_kernel<T>),
+                                         (int)((32 * (wholek_max_k<T>() + 1) + wholek_max_k<T>() * 32) * sizeof(T)));
+    if (e != cudaSuccess) return e;
+    wholek_kernel<T><<<(unsigned)blocks, 256, smem, stream>>>(p, tm, tn);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_direct(olc_dtype dt, const Problem& p, cudaStream_t stream) {
+    if (direct_wholek_ok(dt, p))
+        return dt == OLC_FLOAT ? launch_wholek<float>(p, stream) : launch_wholek<double>(p, stream);
     return dispatch_dtype(dt, [&](auto tag) {
         using T = decltype(tag);
         return launch_tile<T, 32, 32, 16, 2, 2>(p, stream);

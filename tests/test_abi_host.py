@@ -200,7 +200,10 @@ def test_create_rejects_rank0_null_and_bad_dtype():
 def test_algorithm_choice_for_named_shapes():
     cases = [
         ((64, 128), (128, 96), "float32", "direct"),
-        ((8, 1, 128, 256), (1, 4, 256, 64), "float32", "general_simt"),
+        # 32 items of one 128 x 128 tile each (fewer than half the SMs), K =
+        # 256: latency-bound, DIRECT's whole-K tiles
+        ((8, 1, 128, 256), (1, 4, 256, 64), "float32", "direct"),
+        ((8, 1, 128, 512), (1, 4, 512, 64), "float32", "general_simt"),   # K past the whole-K bound
         ((0, 16, 32), (32, 8), "float32", "empty"),
         ((5, 0), (0, 7), "float32", "zero_fill"),
         ((4, 8192), (8192, 28672), "float16", "skinny_m"),
