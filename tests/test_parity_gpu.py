@@ -320,6 +320,25 @@ def test_fp32_simt_k_slices(splits):
         compare(Y.cpu(), y_ref, sabs, "float32", exact=exact)
 
 
+FP32_SIMT_SHAPES = [
+    ((128, 16), (16, 128)),            # one tile, one slice
+    ((300, 1000), (1000, 260)),        # M, N, K tails (K, N multiples of 4)
+    ((3, 1, 130, 68), (1, 2, 68, 132)),   # broadcast batch through 3-D tensor maps
+    ((8, 2048, 256), (256, 512)),      # folded batch, many tiles
+    ((64,), (64, 48)),                 # rank-one A
+]
+
+
+@pytest.mark.parametrize("shapes", FP32_SIMT_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp32_simt_register_tiles(shapes):
+    """The FLOAT register-tile kernel on tails, batches and a rank-one A:
+    integer inputs bit for bit, uniform inputs within the bound."""
+    a_shape, b_shape = shapes
+    for dist, exact in [(synth.SMALL_INT, True), (synth.UNIFORM, False)]:
+        a, b = synth.operands(a_shape, b_shape, "float32", dist, dist, seed=16)
+        check_product(a, b, "float32", algorithm="general_simt", exact=exact)
+
+
 def test_fp32_square_1024_sampled():
     """The 1024-cube FLOAT product (64 tiles: sliced over K automatically)
     on sampled rows."""
