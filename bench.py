@@ -782,6 +782,35 @@ def measure_unaligned(device, peaks, l2):
     return out
 
 
+def measure_fp8_decode_constant_b(device, peaks):
+    """The FP8 few-row products of the decode workload ([1|4|16, 8192] x
+    [8192, 28672], E4M3FN) with B owned by the plan (resident weights, set
+    once): the tcgen05 few-row kernel streams the plan's transposed copy.
+    CUDA graphs of back-to-back launches; two A / Y sets, B 235 MB."""
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import Plan, synth
+    stream = torch.cuda.Stream()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out = []
+    for m in (1, 4, 16):
+        a, b = synth.operands((m, 8192), (8192, 28672), "float8_e4m3fn", synth.normal(1.0),
+                              synth.normal(0.5), 3)
+        p = Plan((m, 8192), (8192, 28672), "float8_e4m3fn")
+        p.set_constant_b(b)
+        sets = [(a.to(device), torch.empty(m, 28672, device=device)) for _ in range(2)]
+        byts = m * 8192 + 8192 * 28672 + 4 * m * 28672
+        ms = statistics.median(graph_time(lambda i: p.execute_constant(*sets[i], stream=stream), 2,
+                                          stream, reps=10, launches=8))
+        gbs = byts / (ms * 1e-3) / 1e9
+        out.append({"product": "fp8_rows_%d_constant_b" % m, "algorithm": p.algorithm,
+                    "ms_per_launch": ms, "achieved": gbs, "unit": "GB/s", "frac": gbs / hbm,
+                    "bound": "hbm", "peak": hbm})
+        p.close()
+        del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def oracle_single_thread(names):
     """The oracle on one host core over the small named workloads, in full."""
     import oracle
@@ -832,7 +861,7 @@ def compact_summary(breakdown, secondary):
     names = [("C1_fp32_64x128x96", "fp32_64x128x96"), ("C2_fp32_broadcast", "fp32_broadcast_batch"),
              ("C4_fp16_corners", "fp16_skinny_splitk"), ("C5_fp32", "float32_square_chain"),
              ("C5_fp64", "float64_square_chain"), ("fp8_proj", "fp8_transformer_projection"),
-             ("fp8_rows", "fp8_skinny_decode")]
+             ("fp8_rows", "fp8_skinny_decode"), ("fp8_rows_constant_b", "fp8_rows_constant_b")]
     for key, wname in names:
         if wname in secondary:
             out[key] = rows(secondary[wname])
@@ -925,6 +954,7 @@ def run_ours(args):
         secondary["split_k_curve"] = measure_split_k_curve(device, peaks, l2)
         secondary["split_k_static"] = measure_split_k_static(device, l2)
         secondary["unaligned_tc"] = measure_unaligned(device, peaks, l2)
+        secondary["fp8_rows_constant_b"] = measure_fp8_decode_constant_b(device, peaks)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)
         secondary["grouped_small_products"] = measure_grouped(device, peaks)
         secondary["alu_rates"] = measure_alu(stream)

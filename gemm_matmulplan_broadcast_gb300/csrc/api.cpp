@@ -56,6 +56,7 @@ struct olc_matmul_plan {
     int const_b_set;
     void* const_bt;              // 8-bit float tensor-core plans: constant B as [N, K] bytes
     size_t const_bt_bytes;
+    int f8_const_tc;             // 8-bit few-row plan moved to the tcgen05 kernel by its constant B
     void* const_b_pad;           // 16-bit plans with N % 8 != 0: constant B, rows padded to 16 bytes
     size_t const_b_pad_bytes;
     // staging copies of operands the tensor-core kernels cannot read in
@@ -156,7 +157,9 @@ Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, voi
     pr.items = p->items;
     pr.map = p->map;
     pr.split_hint = p->split_hint;
-    pr.variant = p->tc_variant;
+    // an 8-bit few-row plan with a constant B runs the tcgen05 kernel
+    // (variant 3) unless a kernel family was asked for
+    pr.variant = (p->f8_const_tc && (p->tc_variant == 0 || p->tc_variant == 3)) ? 3 : p->tc_variant;
     pr.a_trans = p->trans_a;
     pr.b_trans = p->trans_b;
     // Gemm: alpha * acc + beta * C, then the fused residual and activation;
@@ -602,7 +605,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         // the plan's constant B comes transposed already
         const void* bt = (p->const_bt && B == p->const_b) ? p->const_bt : nullptr;
         if (algo == OLC_ALGO_SKINNY_M)
-            e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
+            e = launch_skinny_m(dt, pr, p->splits, p->sm_count, workspace_of(p), s, bt);
         else if (algo == OLC_ALGO_SPLIT_K)
             e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
         else if (algo == OLC_ALGO_SKINNY_N)
@@ -898,7 +901,23 @@ olc_status olc_matmul_plan_set_constant_b(olc_matmul_plan* plan, const void* B, 
         plan->const_bt = nullptr;
         plan->const_bt_bytes = 0;
     }
-    if (bytes > 0 && is_fp8(plan->dtype) && plan->algo == OLC_ALGO_GENERAL_TC) {
+    // 8-bit few-row plans (automatic kernel family): with a constant B the
+    // tcgen05 kernel reads the transposed copy as loaded, streaming B at the
+    // rate of the 16-bit swapped kernel, so the plan moves to it
+    // (from 2 rows: one row streams faster on the SIMT kernel, 40.9 against
+    // 42.5 us for [1, 8192] x [8192, 28672])
+    plan->f8_const_tc = 0;
+    if (bytes > 0 && is_fp8_tc_format(plan->dtype) && plan->algo == OLC_ALGO_SKINNY_M &&
+        (plan->tc_variant == 3 || (plan->tc_variant == 0 && plan->rows >= 2))) {
+        plan->f8_const_tc = 1;
+        const Problem pr = make_problem(plan, nullptr, plan->const_b, nullptr);
+        if (!f8_skinny_tc_ok(plan->dtype, pr)) plan->f8_const_tc = 0;
+    }
+    {
+        const olc_status st = prepare_algorithm(plan);   // the kernel family sizes the workspace
+        if (st != OLC_OK) return st;
+    }
+    if (bytes > 0 && is_fp8(plan->dtype) && (plan->algo == OLC_ALGO_GENERAL_TC || plan->f8_const_tc)) {
         Problem pr = make_problem(plan, nullptr, plan->const_b, nullptr);
         void* mem = nullptr;
         if (cudaMalloc(&mem, bytes) != cudaSuccess) {
@@ -1209,7 +1228,7 @@ int olc_matmul_plan_splits(const olc_matmul_plan* plan) { return plan ? plan->sp
 
 olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant) {
     if (!plan) return OLC_ERR_NULL;
-    if (variant < 0 || variant > 2) return OLC_ERR_INVALID;
+    if (variant < 0 || variant > 3) return OLC_ERR_INVALID;
     plan->tc_variant = variant;
     return prepare_algorithm(plan);   // the workspace depends on the kernel family
 }

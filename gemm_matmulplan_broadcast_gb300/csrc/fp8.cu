@@ -457,7 +457,419 @@ bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t ro
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------------------
+// Few rows (M <= 16), E4M3FN / E5M2, B read in its stored layout: the
+// tensor cores with swapped operands, Y^T = B^T A^T.  One unit is 128 output
+// columns over one K slice; the MMA is kind::f8f6f4 with M = 128 (columns
+// n), N = 16 (rows of A, zero-padded), K = 32, float32 accumulators in TMEM.
+// The MMA wants both operands K-major, while B is stored [K, N] (n
+// contiguous), so B is transposed inside shared memory on the way:
+//   warp 0    one lane streams 128 x 128-byte boxes of B (128 K-rows of 128
+//             columns, 128-byte swizzle) and 16 x 128-byte boxes of A into
+//             an 8-deep ring (full[], empty[]);
+//   warps 2-5 transpose each B box into a 2-deep ring of K-major tiles (128
+//             rows n of 128 K-bytes, the 128-byte-swizzle layout TMA would
+//             write): per 16 x 16-byte block one ldmatrix.x2.trans of byte
+//             pairs (its two 8 x 8 matrices take the K rows 4j, 4j + 1 and
+//             4j + 2, 4j + 3, so each lane holds two K pairs of two columns),
+//             two byte permutes that make four consecutive K bytes of one
+//             column, and one stmatrix.x2 (even and odd columns); then they
+//             run the epilogue of each unit;
+//   warp 1    one lane issues the MMAs (4 per 128-deep block) and owns TMEM
+//             (two 16-column accumulators, so a unit's epilogue overlaps the
+//             next unit's MMAs).
+// K slices: the last slice of a tile to finish sums the tiles' slices in
+// slice order (float32 partials in the workspace), so results are the same
+// run to run.
+
+namespace sk {
+
+constexpr int TN = 128;                       // output columns per unit (MMA M)
+constexpr int KB = 128;                       // K bytes per stage: one swizzle row
+constexpr int MR = 16;                        // A rows per MMA (MMA N)
+constexpr int RAW_BYTES = KB * TN;            // 16 KiB: B as stored, K rows of 128 columns
+constexpr int A_BYTES = MR * KB;              // 2 KiB: A, K-major
+constexpr int BT_BYTES = TN * KB;             // 16 KiB: B^T, K-major
+constexpr int RING = 8;                       // B / A stages in flight
+constexpr int BT_RING = 2;                    // transposed tiles
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 32;                 // two 16-column accumulators
+constexpr int SMEM_BYTES = RING * (RAW_BYTES + A_BYTES) + BT_RING * BT_BYTES + 1024 + 512;
+
+struct Bars {
+    uint64_t full[RING], empty[RING];
+    uint64_t bt_full[BT_RING], bt_empty[BT_RING];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct SkParams {
+    int64_t M, N, K;
+    int64_t tiles_n, units, kslice;           // kslice: a multiple of KB
+    int ksplit;
+    float* Y;
+    float* part;                              // [tiles_n][ksplit][MR][TN] float32 (ksplit > 1)
+    unsigned int* cnt;                        // [tiles_n][4] arrivals per 32-column group, zero between launches
+    unsigned int* err;
+    int fmt;
+    int pre_t;                                // B given transposed ([N, K] bytes): no transposition
+    Epilogue epi;
+};
+
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void stsm_x2(uint32_t addr, uint32_t r0, uint32_t r1) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x2.shared.b16 [%0], {%1, %2};" ::"r"(addr), "r"(r0), "r"(r1)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// unit u -> column tile and K slice (consecutive units: consecutive tiles)
+__device__ __forceinline__ void unit_of(const SkParams& p, int64_t u, int64_t& tile, int& slice,
+                                        int64_t& kb0, int64_t& kb1) {
+    tile = u % p.tiles_n;
+    slice = (int)(u / p.tiles_n);
+    const int64_t k0 = (int64_t)slice * p.kslice;
+    const int64_t k1 = min64(p.K, k0 + p.kslice);
+    kb0 = k0 / KB;
+    kb1 = ceil_div(k1, (int64_t)KB);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+skinny_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
+                 const SkParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* raw = base;                                    // RING x RAW_BYTES
+    unsigned char* bt = base + RING * RAW_BYTES;                  // BT_RING x BT_BYTES
+    unsigned char* as = bt + BT_RING * BT_BYTES;                  // RING x A_BYTES
+    Bars* s = reinterpret_cast<Bars*>(as + RING * A_BYTES);
+    volatile int* abort_flag = &s->abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RING; ++i) {
+            bar_init(&s->full[i], 1);
+            // four transposer warps and the MMA's commit (the MMA's alone when
+            // B comes transposed)
+            bar_init(&s->empty[i], p.pre_t ? 1 : 5);
+        }
+        for (int i = 0; i < BT_RING; ++i) {
+            bar_init(&s->bt_full[i], 4);
+            bar_init(&s->bt_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            bar_init(&s->acc_full[i], 1);
+            bar_init(&s->acc_empty[i], 4);
+        }
+        bar_init(&s->drain, 1);
+        s->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&s->tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = s->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            uint32_t st = 0, ph = 0;
+            bool armed[RING];
+            uint32_t armed_parity[RING];
+            for (int i = 0; i < RING; ++i) armed[i] = false;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                int64_t tile, kb0, kb1;
+                int slice;
+                unit_of(p, u, tile, slice, kb0, kb1);
+                for (int64_t kb = kb0; kb < kb1; ++kb) {
+                    if (!bar_wait(&s->empty[st], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    bar_expect(&s->full[st], RAW_BYTES + A_BYTES);
+                    armed[st] = true;
+                    armed_parity[st] = ph;
+                    if (p.pre_t)   // B^T: 128 rows n of 128 K-bytes, the MMA's layout already
+                        tma_2d(raw + st * RAW_BYTES, &tmap_b, &s->full[st], (int)(kb * KB), (int)(tile * TN));
+                    else
+                        tma_2d(raw + st * RAW_BYTES, &tmap_b, &s->full[st], (int)(tile * TN), (int)(kb * KB));
+                    tma_2d(as + st * A_BYTES, &tmap_a, &s->full[st], (int)(kb * KB), 0);
+                    if (++st == RING) { st = 0; ph ^= 1; }
+                }
+            }
+            if (*abort_flag)
+                for (int i = 0; i < RING; ++i)
+                    if (armed[i]) bar_drain(&s->full[i], armed_parity[i]);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = f8_instr_desc(p.fmt, TN, MR);
+            uint32_t st = 0, ph = 0, tb = 0, tph = 0, acc = 0, acc_ph = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                int64_t tile, kb0, kb1;
+                int slice;
+                unit_of(p, u, tile, slice, kb0, kb1);
+                if (!bar_wait(&s->acc_empty[acc], acc_ph ^ 1, abort_flag, p.err)) break;
+                fence_after();
+                const uint32_t d = tmem_base + acc * MR;
+                for (int64_t kb = kb0; kb < kb1; ++kb) {
+                    if ((!p.pre_t && !bar_wait(&s->bt_full[tb], tph, abort_flag, p.err)) ||
+                        !bar_wait(&s->full[st], ph, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    // MMA A: B^T, 128 x 128 K-bytes (transposed here, or as loaded)
+                    const uint32_t a_addr = p.pre_t ? su32(raw + st * RAW_BYTES) : su32(bt + tb * BT_BYTES);
+                    const uint32_t b_addr = su32(as + st * A_BYTES);      // MMA B: A, 16 x 128 K-bytes
+#pragma unroll
+                    for (int kk = 0; kk < KB / UMMA_K; ++kk)
+                        mma_f8(d, kmajor_desc(a_addr + kk * UMMA_K), kmajor_desc(b_addr + kk * UMMA_K), idesc,
+                               (kb > kb0 || kk > 0) ? 1u : 0u);
+                    if (!p.pre_t) commit(&s->bt_empty[tb]);
+                    commit(&s->empty[st]);
+                    if (++st == RING) { st = 0; ph ^= 1; }
+                    if (++tb == BT_RING) { tb = 0; tph ^= 1; }
+                }
+                if (!ok) break;
+                commit(&s->acc_full[acc]);
+                if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+            }
+            commit(&s->drain);
+            bar_drain(&s->drain, 0);
+        }
+    } else {
+        // ---------------------------------------------------- transpose + epilogue
+        const int tw = warp - 2;                  // 0..3
+        const int lane_group = warp & 3;          // the TMEM lanes this warp may read
+        uint32_t st = 0, ph = 0, tb = 0, tph = 0, acc = 0, acc_ph = 0;
+        bool ok = true;
+        // this lane's ldmatrix row: matrix (lane >> 3) & 1, row lane & 7 -> K row
+        // 4 (row >> 1) + (row & 1) + 2 matrix of a 16-row block
+        const int lrow = lane & 7, lmat = (lane >> 3) & 1;
+        const int k_in = 4 * (lrow >> 1) + (lrow & 1) + 2 * lmat;    // 0..15
+        // stmatrix row: matrix (lane >> 3) & 1 (even / odd column), row lane & 7
+        const int n_in = 2 * lrow + lmat;                            // 0..15
+        for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            int64_t tile, kb0, kb1;
+            int slice;
+            unit_of(p, u, tile, slice, kb0, kb1);
+            for (int64_t kb = kb0; kb < kb1 && !p.pre_t; ++kb) {
+                if (!bar_wait(&s->full[st], ph, abort_flag, p.err) ||
+                    !bar_wait(&s->bt_empty[tb], tph ^ 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = su32(raw + st * RAW_BYTES);
+                const uint32_t dst = su32(bt + tb * BT_BYTES);
+                // 64 blocks of 16 K-rows x 16 columns, 16 per warp
+#pragma unroll 4
+                for (int b = tw; b < 64; b += 4) {
+                    const int kb16 = b >> 3, nb16 = b & 7;
+                    // source: K row k, 16-byte chunk nb16 at position nb16 ^ (k & 7)
+                    const int k = 16 * kb16 + k_in;
+                    uint32_t r0, r1;
+                    ldsm_x2_t(src + k * 128 + ((nb16 ^ (k & 7)) << 4), r0, r1);
+                    // r0: K rows ka, ka + 1 of columns 2q, 2q + 1; r1: ka + 2, ka + 3
+                    // (ka = 4 (lane & 3), q = lane >> 2): four K bytes per column
+                    const uint32_t even = __byte_perm(r0, r1, 0x6420);
+                    const uint32_t odd = __byte_perm(r0, r1, 0x7531);
+                    // destination: row n, 16-byte chunk kb16 at position kb16 ^ (n & 7)
+                    const int n = 16 * nb16 + n_in;
+                    stsm_x2(dst + n * 128 + ((kb16 ^ (n & 7)) << 4), even, odd);
+                }
+                // generic-proxy writes, read next by the tensor core
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    bar_arrive(&s->bt_full[tb]);
+                    bar_arrive(&s->empty[st]);
+                }
+                if (++st == RING) { st = 0; ph ^= 1; }
+                if (++tb == BT_RING) { tb = 0; tph ^= 1; }
+            }
+            if (!ok) break;
+            // epilogue of the unit: TMEM lane = output column, column = row of A
+            if (!bar_wait(&s->acc_full[acc], acc_ph, abort_flag, p.err)) break;
+            fence_after();
+            uint32_t r[16];
+            tmem_ld16(tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * MR, r);
+            fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&s->acc_empty[acc]);
+            if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+            const int64_t n = tile * TN + lane_group * 32 + lane;
+            const int rows = (int)min64(p.M, MR);
+            if (p.ksplit == 1) {
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MR; ++m)
+                        if (m < rows)
+                            p.Y[m * p.N + n] =
+                                apply_epilogue<float>(p.epi, __uint_as_float(r[m]), m, n, p.Y + m * p.N + n);
+                }
+                continue;
+            }
+            // K slices: each warp files its 32 columns of this slice's partial
+            // tile and arrives on the counter of its column group; the last of
+            // the group's ksplit arrivals sums the slices in slice order.
+            // Warps coordinate only through the counters, so no warp can be
+            // left waiting for another that gave up.
+            const int64_t col = lane_group * 32 + lane;
+            float* mine = p.part + ((tile * p.ksplit + slice) * MR) * (int64_t)TN + col;
+#pragma unroll
+            for (int m = 0; m < MR; ++m)
+                if (m < rows) mine[m * TN] = __uint_as_float(r[m]);
+            __threadfence();
+            __syncwarp();
+            unsigned int* c = p.cnt + tile * 4 + lane_group;
+            unsigned int last = 0;
+            if (lane == 0) last = atomicAdd(c, 1u) == (unsigned int)p.ksplit - 1u ? 1u : 0u;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last) continue;
+            __threadfence();
+            const float* first = p.part + (tile * p.ksplit * MR) * (int64_t)TN + col;
+            float v[MR];
+#pragma unroll
+            for (int m = 0; m < MR; ++m) v[m] = 0.f;
+            for (int sl = 0; sl < p.ksplit; ++sl) {
+                // one slice's rows loaded together: one L2 round trip per slice
+                float t[MR];
+#pragma unroll
+                for (int m = 0; m < MR; ++m)
+                    t[m] = m < rows ? __ldcg(first + ((int64_t)sl * MR + m) * TN) : 0.f;
+#pragma unroll
+                for (int m = 0; m < MR; ++m) v[m] += t[m];
+            }
+            if (n < p.N) {
+#pragma unroll
+                for (int m = 0; m < MR; ++m)
+                    if (m < rows) p.Y[m * p.N + n] = apply_epilogue<float>(p.epi, v[m], m, n, p.Y + m * p.N + n);
+            }
+            if (lane == 0) *c = 0u;   // ready for the next launch
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+}
+
+}  // namespace sk
+
 }  // namespace f8
+
+// E4M3FN / E5M2 few-row products the swapped tensor-core kernel takes: one
+// item, N and K multiples of 16, 16-byte aligned A and B
+bool f8_skinny_tc_ok(olc_dtype dt, const Problem& p) {
+    return (dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2) && p.items == 1 && p.M >= 1 && p.M <= 16 &&
+           p.N % 16 == 0 && p.K % 16 == 0 && p.N < (1LL << 31) && p.K < (1LL << 31);
+}
+
+// K slices: whole waves of one unit per SM, discounted by the partial
+// traffic (the same rule as the other skinny kernels)
+int f8_skinny_tc_pick(const Problem& p, int sm_count) {
+    if (p.split_hint > 0) return (int)min64(p.split_hint, max64(1, p.K / f8::sk::KB));
+    const int64_t tiles = ceil_div(p.N, (int64_t)f8::sk::TN);
+    const double stream = (double)p.K * (double)p.N;
+    const int64_t smax = min64(32, max64(1, p.K / 1024));
+    int best = 1;
+    double best_score = -1.0;
+    for (int64_t sp = 1; sp <= smax; ++sp) {
+        const int64_t units = tiles * sp;
+        const int64_t waves = ceil_div(units, (int64_t)sm_count);
+        const double fill = (double)units / (double)(waves * sm_count);
+        const double extra = sp > 1 ? 2.0 * (double)sp * 16.0 * (double)p.N * 4.0 : 0.0;
+        const double score = fill * stream / (stream + extra);
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = (int)sp;
+        }
+    }
+    return best;
+}
+
+size_t f8_skinny_tc_partial_bytes(const Problem& p, int ksplit) {
+    if (ksplit <= 1) return 0;
+    return (size_t)(ceil_div(p.N, (int64_t)f8::sk::TN) * ksplit * f8::sk::MR * f8::sk::TN * 4);
+}
+
+size_t f8_skinny_tc_counter_count(const Problem& p, int ksplit) {
+    return ksplit > 1 ? (size_t)ceil_div(p.N, (int64_t)f8::sk::TN) * 4 : 0;
+}
+
+cudaError_t launch_f8_skinny_tc(olc_dtype dt, const Problem& p, int ksplit, int sm_count, const Workspace& ws,
+                                cudaStream_t s, const void* bt_ready) {
+    using namespace f8::sk;
+    const void* bsrc = bt_ready ? bt_ready : p.B;
+    if (!f8_skinny_tc_ok(dt, p) || (reinterpret_cast<uintptr_t>(p.A) & 15) || (reinterpret_cast<uintptr_t>(bsrc) & 15))
+        return cudaErrorInvalidValue;
+    if (ksplit < 1) ksplit = 1;
+    const int64_t kslice = ceil_div(ceil_div(p.K, (int64_t)ksplit), (int64_t)KB) * KB;
+    ksplit = (int)ceil_div(p.K, kslice);                   // non-empty slices
+    SkParams q;
+    std::memset(&q, 0, sizeof q);
+    q.M = p.M;
+    q.N = p.N;
+    q.K = p.K;
+    q.tiles_n = ceil_div(p.N, (int64_t)TN);
+    q.ksplit = ksplit;
+    q.kslice = kslice;
+    q.units = q.tiles_n * ksplit;
+    q.Y = static_cast<float*>(p.Y);
+    q.err = device_error_word();
+    q.fmt = dt == OLC_FLOAT8E4M3FN ? 0 : 1;
+    q.pre_t = bt_ready ? 1 : 0;
+    q.epi = p.epi;
+    if (ksplit > 1) {
+        if (!ws.partials || ws.partial_bytes < f8_skinny_tc_partial_bytes(p, ksplit) || !ws.counters ||
+            ws.counter_count < (size_t)q.tiles_n * 4)
+            return cudaErrorInvalidValue;
+        q.part = static_cast<float*>(ws.partials);
+        q.cnt = ws.counters;
+    }
+    CUtensorMap mb, ma;
+    std::memset(&mb, 0, sizeof mb);
+    std::memset(&ma, 0, sizeof ma);
+    // B as stored: [K rows][N bytes], boxes of 128 columns x 128 K-rows (or
+    // B^T: [N rows][K bytes], boxes of 128 K-bytes x 128 rows); A: [M rows]
+    // [K bytes], boxes of 128 K-bytes x 16 rows (rows past M read 0)
+    const bool mb_ok = bt_ready ? f8::encode_u8_2d(&mb, bsrc, (uint64_t)p.K, (uint64_t)p.N, KB, TN)
+                                : f8::encode_u8_2d(&mb, bsrc, (uint64_t)p.N, (uint64_t)p.K, TN, KB);
+    if (!mb_ok || !f8::encode_u8_2d(&ma, p.A, (uint64_t)p.K, (uint64_t)p.M, KB, MR)) return cudaErrorInvalidValue;
+    const cudaError_t attr = set_smem_limit(reinterpret_cast<const void*>(skinny_tc_kernel), SMEM_BYTES);
+    if (attr != cudaSuccess) return attr;
+    const int64_t grid = min64(q.units, (int64_t)sm_count);
+    skinny_tc_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, s>>>(mb, ma, q);
+    return cudaGetLastError();
+}
 
 bool fp8_tc_ok(const Problem& p) {
     return p.items == 1 && p.K % 16 == 0 && p.N % 4 == 0 && p.M < (1LL << 31) && p.N < (1LL << 31) &&

@@ -104,10 +104,21 @@ bool general_simt_vectorizable(olc_dtype dt, int64_t N, int64_t K);
 // SKINNY_M: M <= 16.  `ksplit` slices of K, reduced in fixed order.
 int skinny_m_max_rows();
 cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_count,
-                            const Workspace& ws, cudaStream_t stream);
+                            const Workspace& ws, cudaStream_t stream, const void* bt_ready = nullptr);
 size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count);
 size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit, int sm_count);
 int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count);
+
+// SKINNY_M for E4M3FN / E5M2 on the tensor cores (fp8.cu): swapped operands,
+// B transposed in shared memory on the way, K slices summed in slice order
+bool f8_skinny_tc_ok(olc_dtype dt, const Problem& p);
+int f8_skinny_tc_pick(const Problem& p, int sm_count);
+size_t f8_skinny_tc_partial_bytes(const Problem& p, int ksplit);
+size_t f8_skinny_tc_counter_count(const Problem& p, int ksplit);
+// bt_ready: B already transposed ([N, K] bytes, a plan's constant B): the
+// tiles go to the MMA as loaded, without the shared-memory transposition
+cudaError_t launch_f8_skinny_tc(olc_dtype dt, const Problem& p, int ksplit, int sm_count, const Workspace& ws,
+                                cudaStream_t stream, const void* bt_ready = nullptr);
 
 // SKINNY_N: N <= 16.
 int skinny_n_max_cols();

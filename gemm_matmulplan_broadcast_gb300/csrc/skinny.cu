@@ -790,8 +790,15 @@ static bool skinny_m_on_tc(olc_dtype dt, const Problem& p) {
 // (measured on GB300 for one [8192, 28672] B, TB/s, SIMT against MMA: 1 row
 // 5.8 / 3.7, 2 rows 4.1 / 3.7, 4 rows 2.9 / 3.7, 16 rows 0.8 / 3.6); variant
 // 1 forces the SIMT kernel, variant 2 the MMA kernel.
+// E4M3FN / E5M2 on the tensor cores (variant 3): tcgen05 kind::f8f6f4 with
+// swapped operands, B transposed in shared memory (fp8.cu)
+static bool skinny_m_on_f8_tc(olc_dtype dt, const Problem& p) {
+    return p.variant == 3 && f8_skinny_tc_ok(dt, p);
+}
+
 static bool skinny_m_on_f8_mma(olc_dtype dt, const Problem& p) {
     if (!(dt == OLC_FLOAT8E4M3FN || dt == OLC_FLOAT8E5M2) || p.M > 16 || p.N % 16 != 0) return false;
+    if (skinny_m_on_f8_tc(dt, p)) return false;
     if (p.variant == 1) return false;
     if (p.variant == 2) return true;
     return p.M >= 4;
@@ -811,6 +818,7 @@ static int f8_mma_occupancy() {
 static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count);
 
 int skinny_m_pick_split(olc_dtype dt, const Problem& p, int sm_count) {
+    if (skinny_m_on_f8_tc(dt, p)) return f8_skinny_tc_pick(p, sm_count);
     return skinny_m_on_tc(dt, p) ? tc_skinny_m_pick(p, sm_count)
                                  : skinny_m_simt_split(dt, p, sm_count);
 }
@@ -845,6 +853,7 @@ static int skinny_m_simt_split(olc_dtype dt, const Problem& p, int sm_count) {
 }
 
 size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
+    if (skinny_m_on_f8_tc(dt, p)) return f8_skinny_tc_partial_bytes(p, ksplit);
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_partial_bytes(p, sm_count);
     if (skinny_m_on_f8_mma(dt, p))
         return (size_t)(ceil_div(p.N, kF8MmaCols) * p.items * ksplit * 16 * kF8MmaCols * 4);
@@ -854,7 +863,7 @@ size_t skinny_m_partial_bytes(olc_dtype dt, const Problem& p, int ksplit, int sm
 }
 
 size_t skinny_m_counter_count(olc_dtype dt, const Problem& p, int ksplit, int sm_count) {
-    (void)ksplit;
+    if (skinny_m_on_f8_tc(dt, p)) return f8_skinny_tc_counter_count(p, ksplit);
     if (skinny_m_on_tc(dt, p)) return tc_skinny_m_counter_count(p, sm_count);
     if (skinny_m_on_f8_mma(dt, p)) return (size_t)(ceil_div(p.N, kF8MmaCols) * p.items);
     return (size_t)(skinny_m_col_groups(dt, p.M, p.N) * p.items);
@@ -953,8 +962,9 @@ cudaError_t launch_f8_split_k(olc_dtype dt, const Problem& p, int splits, const 
 }
 
 cudaError_t launch_skinny_m(olc_dtype dt, const Problem& p, int ksplit, int sm_count,
-                            const Workspace& ws, cudaStream_t s) {
+                            const Workspace& ws, cudaStream_t s, const void* bt_ready) {
     if (skinny_m_on_tc(dt, p)) return launch_tc_skinny_m(dt, p, sm_count, ws, s);
+    if (skinny_m_on_f8_tc(dt, p)) return launch_f8_skinny_tc(dt, p, ksplit, sm_count, ws, s, bt_ready);
     if (skinny_m_on_f8_mma(dt, p))
         return dt == OLC_FLOAT8E4M3FN ? launch_skinny_m_f8_mma<0>(p, ksplit, ws, s)
                                       : launch_skinny_m_f8_mma<1>(p, ksplit, ws, s);

@@ -272,7 +272,12 @@ olc_status olc_gemm_execute(const olc_matmul_plan* plan, const void* A, const vo
  * directly.  A plan with 8-bit float operands on the tensor cores also keeps
  * B transposed ([N, K] bytes, the K-major operand the MMA reads; b_numel more
  * bytes of device memory), so executes with the constant B skip the
- * transpose that an execute with a caller's B runs first.  Likewise a
+ * transpose that an execute with a caller's B runs first.  An 8-bit few-row
+ * plan (SKINNY_M, E4M3FN / E5M2, 2 to 16 rows, one item, N and K multiples
+ * of 16, kernel family automatic or 3) keeps the transposed B as well and from then on runs the
+ * tcgen05 few-row kernel, which streams that copy straight to the MMA
+ * (executes with a caller's B on such a plan run the same kernel, which then
+ * transposes B in shared memory on the way).  Likewise a
  * FLOAT16 / BFLOAT16 plan on the general tensor-core tiles whose B rows are
  * not a multiple of 16 bytes (N not a multiple of 8) keeps B with rows
  * padded to 8 elements, so executes with the constant B copy nothing.
@@ -448,7 +453,11 @@ int olc_matmul_plan_splits(const olc_matmul_plan* plan);
  * kernel, 2 = the swapped-operand tcgen05 kernel.  SKINNY_M plans of
  * FLOAT8E4M3FN / FLOAT8E5M2: 0 = automatic (the warp-level MMA kernel from 4
  * rows), 1 = the SIMT streaming kernel, 2 = the warp-level MMA kernel
- * (mma.sync m16n8k32 on B fragments transposed in registers).  GENERAL_TC
+ * (mma.sync m16n8k32 on B fragments transposed in registers), 3 = the
+ * tcgen05 kernel with swapped operands (kind::f8f6f4, 128 output columns per
+ * MMA; B transposed in shared memory, or read transposed from the plan's
+ * constant B; one item, N and K multiples of 16, else the warp-level MMA
+ * kernel).  GENERAL_TC
  * plans of 8-bit floats: 1 = one CTA per 128 x 256 tile instead of CTA pairs.
  * Results are identical within the parity tolerance either way.  Errors:
  * OLC_ERR_NULL, OLC_ERR_INVALID. */

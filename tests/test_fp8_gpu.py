@@ -190,7 +190,7 @@ SKINNY_SHAPES = [
 ]
 
 
-SKINNY_VARIANTS = {"auto": 0, "simt": 1, "mma": 2}
+SKINNY_VARIANTS = {"auto": 0, "simt": 1, "mma": 2, "tcgen05": 3}
 
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
@@ -201,8 +201,10 @@ def test_fp8_skinny_m(dtype, shapes, variant):
     kernel (16, 8 or 4 one-byte B elements per lane load, decoded to float32;
     A rows that are not 8-byte aligned take element loads) and, for E4M3FN
     and E5M2, the warp-level MMA kernel (m16n8k32, B fragments transposed in
-    registers; automatic from 4 rows).  The FNUZ formats take the SIMT kernel
-    whatever the variant."""
+    registers; automatic from 4 rows) and the tcgen05 kernel with swapped
+    operands and B transposed in shared memory (variant 3; one item, N and K
+    multiples of 16, else the warp-level MMA kernel).  The FNUZ formats take
+    the SIMT kernel whatever the variant."""
     a_shape, b_shape = shapes
     with Plan(a_shape, b_shape, dtype) as p:
         if b_shape[-1] >= 256:
@@ -219,7 +221,7 @@ ONE = {"float8_e4m3fn": 0x38, "float8_e5m2": 0x3C, "float8_e4m3fnuz": 0x40, "flo
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
 @pytest.mark.parametrize("m", [2, 4, 16])
-@pytest.mark.parametrize("variant", [1, 2], ids=["simt", "mma"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["simt", "mma", "tcgen05"])
 def test_fp8_skinny_m_decodes_every_pattern(dtype, m, variant):
     """Every one of the 256 patterns through the skinny kernel's B decode
     (16, 8 or 4 one-byte columns per lane for 2, 4 or 16 rows; element i of a
@@ -247,7 +249,7 @@ def test_fp8_skinny_m_decodes_every_pattern(dtype, m, variant):
 
 
 @pytest.mark.parametrize("dtype", FP8 + FNUZ)
-@pytest.mark.parametrize("variant", [1, 2], ids=["simt", "mma"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["simt", "mma", "tcgen05"])
 def test_fp8_skinny_m_decodes_every_a_pattern(dtype, variant):
     """Every pattern through the skinny kernel's A decode (A rows kept as
     packed bytes, decoded two k positions at a time): A[i, k] = 16 i + k for
@@ -273,6 +275,67 @@ def test_fp8_skinny_m_decodes_every_a_pattern(dtype, variant):
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(y), nan)
     assert np.array_equal(y[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes,splits", [
+    (((4, 8192), (8192, 28672)), 0),     # the named few-row workload's product, automatic slices
+    (((16, 8192), (8192, 2048)), 5),     # several K slices summed in slice order
+    (((1, 300), (300, 4112)), 1),        # one row, K and N tails of the boxes
+    (((7, 4096), (4096, 512)), 32),      # many slices
+])
+def test_fp8_skinny_m_tcgen05(dtype, shapes, splits):
+    """The tcgen05 few-row kernel (variant 3): normal inputs within the
+    bound, integer inputs bit for bit, two runs identical (fixed-order
+    reduction of the K slices)."""
+    a_shape, b_shape = shapes
+    for dist, exact in [(synth.normal(1.0), False), (synth.SMALL_INT, True)]:
+        a, b = synth.operands(a_shape, b_shape, dtype, dist, dist if exact else synth.normal(0.5), 50)
+        A, B = a.cuda(), b.cuda()
+        with Plan(a_shape, b_shape, dtype) as p:
+            p.force("skinny_m")
+            p.set_tc_variant(3)
+            if splits:
+                p.set_splits(splits)
+            Y = torch.full(p.output_shape, float("nan"), device="cuda")
+            Y2 = torch.empty_like(Y)
+            p.execute_checked(A, B, Y)
+            p.execute_checked(A, B, Y2)
+            torch.cuda.synchronize()
+            assert torch.equal(Y, Y2)
+        y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+        compare(Y.cpu(), y_ref, s, dtype, exact=exact)
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("shapes", [((4, 8192), (8192, 2048)), ((16, 1024), (1024, 512)),
+                                    ((2, 300), (300, 4112)), ((1, 512), (512, 1024))],
+                         ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_fp8_skinny_m_constant_b(dtype, shapes):
+    """An 8-bit few-row plan of 2 or more rows given a constant B keeps it
+    transposed and runs the tcgen05 kernel on that copy (no shared-memory
+    transposition; one row stays on the SIMT kernel): against
+    the oracle (integer inputs bit for bit), two executes identical; an
+    execute with a caller's B on the same plan (the same kernel, transposing
+    in shared memory) too."""
+    a_shape, b_shape = shapes
+    for dist, exact in [(synth.normal(1.0), False), (synth.SMALL_INT, True)]:
+        a, b = synth.operands(a_shape, b_shape, dtype, dist, dist if exact else synth.normal(0.5), 51)
+        A = a.cuda()
+        with Plan(a_shape, b_shape, dtype) as p:
+            assert p.algorithm == "skinny_m"
+            p.set_constant_b(b)
+            Y = torch.full(p.output_shape, float("nan"), device="cuda")
+            Y2 = torch.empty_like(Y)
+            Y3 = torch.full(p.output_shape, float("nan"), device="cuda")
+            p.execute_constant(A, Y)
+            p.execute_constant(A, Y2)
+            p.execute(A, b.cuda(), Y3)
+            torch.cuda.synchronize()
+            assert torch.equal(Y, Y2)
+        y_ref, s = oracle.matmul(synth.to_numpy_storage(a), synth.to_numpy_storage(b), dtype)
+        compare(Y.cpu(), y_ref, s, dtype, exact=exact)
+        compare(Y3.cpu(), y_ref, s, dtype, exact=exact)
 
 
 def test_fp8_skinny_decode_workload_full():
