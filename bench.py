@@ -731,7 +731,8 @@ def measure_unaligned(device, peaks, l2):
     plan-owned constant B; Y stored by alignment), and the up projection
     [16384, 4096] x [4096, 14336] with A one element into its buffer (A
     staged every call) beside the same product aligned.  CUDA graphs of
-    back-to-back launches; the operands exceed L2."""
+    back-to-back launches, the two variants of each pair interleaved over
+    three rounds; the operands exceed L2."""
     import torch
     from gemm_matmulplan_broadcast_gb300 import Plan, synth
     stream = torch.cuda.Stream()
@@ -745,9 +746,15 @@ def measure_unaligned(device, peaks, l2):
     p = Plan((16384, 4096), (4096, 50257), "bfloat16")
     pc = Plan((16384, 4096), (4096, 50257), "bfloat16")
     pc.set_constant_b(B)
-    for label, fn, plan in (("vocab_50257_per_call_b", lambda i: p.execute(A, B, Y, stream=stream), p),
-                            ("vocab_50257_constant_b", lambda i: pc.execute_constant(A, Y, stream=stream), pc)):
-        ms = statistics.median(graph_time(fn, 1, stream, reps=5, launches=2))
+    # the two variants interleaved over rounds (clock drift under load)
+    cases = (("vocab_50257_per_call_b", lambda i: p.execute(A, B, Y, stream=stream), p),
+             ("vocab_50257_constant_b", lambda i: pc.execute_constant(A, Y, stream=stream), pc))
+    samples = {c[0]: [] for c in cases}
+    for _ in range(3):
+        for label, fn, _plan in cases:
+            samples[label] += graph_time(fn, 1, stream, reps=2, launches=2)
+    for label, fn, plan in cases:
+        ms = statistics.median(samples[label])
         out.append({"product": label, "a": [16384, 4096], "b": [4096, 50257],
                     "algorithm": plan.algorithm, "launches": plan.launches,
                     "ms_per_launch": ms, "tflops": flop / (ms * 1e-3) / 1e12,
@@ -769,9 +776,13 @@ def measure_unaligned(device, peaks, l2):
     B = b.to(device)
     Y = torch.empty(8, 2048, 14336, dtype=torch.bfloat16, device=device)
     p = Plan((8, 2048, 4096), (4096, 14336), "bfloat16")
+    samples = {"up_proj_aligned": [], "up_proj_a_offset_1": []}
+    for _ in range(3):
+        for label, AA in (("up_proj_aligned", A_al), ("up_proj_a_offset_1", A_off)):
+            samples[label] += graph_time(lambda i: p.execute(AA, B, Y, stream=stream), 1, stream,
+                                         reps=2, launches=2)
     for label, AA in (("up_proj_aligned", A_al), ("up_proj_a_offset_1", A_off)):
-        ms = statistics.median(graph_time(lambda i: p.execute(AA, B, Y, stream=stream), 1, stream,
-                                          reps=5, launches=2))
+        ms = statistics.median(samples[label])
         out.append({"product": label, "a": [8, 2048, 4096], "b": [4096, 14336],
                     "algorithm": p.algorithm_for(AA, B, Y), "staging_copies": p.staging_copies(AA, B, Y),
                     "ms_per_launch": ms, "tflops": flop / (ms * 1e-3) / 1e12,
@@ -842,45 +853,53 @@ def oracle_single_thread(names):
 
 
 def _short(x):
-    return float("%.3g" % x)
+    v = float("%.3g" % x)
+    return int(v) if abs(v) >= 100 and v == int(v) else v
 
 
 def compact_summary(breakdown, secondary):
-    """One short entry per named configuration (and the extra workloads):
-    per product its time and achieved rate with the roofline fraction."""
+    """One short entry per named configuration (and the extra workloads),
+    kept small so that the end of the JSON line alone carries every figure:
+    per product [microseconds per launch, achieved rate, roofline fraction],
+    with the rate's unit once per configuration."""
+    def short_name(name):
+        for pre in ("fp8_proj_", "proj_", "fp8_rows_", "square_"):
+            if name.startswith(pre):
+                name = name[len(pre):]
+        return name.replace("_constant_b", "")
+
     def rows(lst):
         d = {}
         for r in lst:
             if "achieved" not in r:
-                d[r["product"]] = "empty: 0 launches"
+                d[short_name(r["product"])] = "empty"
                 continue
-            d[r["product"]] = "%s us %s %s (%s)" % (_short(r["ms_per_launch"] * 1e3), _short(r["achieved"]),
-                                                    r["unit"], _short(r["frac"]))
+            d.setdefault("unit", r["unit"])
+            d[short_name(r["product"])] = [_short(r["ms_per_launch"] * 1e3), _short(r["achieved"]),
+                                           _short(r["frac"])]
         return d
-    out = {"C3_bf16_projection": rows(breakdown)}
-    names = [("C1_fp32_64x128x96", "fp32_64x128x96"), ("C2_fp32_broadcast", "fp32_broadcast_batch"),
-             ("C4_fp16_corners", "fp16_skinny_splitk"), ("C5_fp32", "float32_square_chain"),
+    out = {"fmt": "us/launch,rate,roofline frac", "C3_bf16": rows(breakdown)}
+    names = [("C1_fp32", "fp32_64x128x96"), ("C2_fp32", "fp32_broadcast_batch"),
+             ("C4_fp16", "fp16_skinny_splitk"), ("C5_fp32", "float32_square_chain"),
              ("C5_fp64", "float64_square_chain"), ("fp8_proj", "fp8_transformer_projection"),
-             ("fp8_rows", "fp8_skinny_decode"), ("fp8_rows_constant_b", "fp8_rows_constant_b")]
+             ("fp8_rows", "fp8_skinny_decode"), ("fp8_rows_const_b", "fp8_rows_constant_b")]
     for key, wname in names:
         if wname in secondary:
             out[key] = rows(secondary[wname])
     if "split_k_curve" in secondary:
         c = secondary["split_k_curve"]
-        out["split_k_curve"] = {"fixed_us": _short(c["fit_fixed_us"]),
-                                "stream_gbs": _short(c["fit_stream_gbs"]),
-                                "gbs_by_K": {r["product"].split("_")[-1]: _short(r["achieved"])
-                                             for r in c["points"]}}
+        out["split_k_curve"] = {"fixed_us": _short(c["fit_fixed_us"]), "stream_gbs": _short(c["fit_stream_gbs"]),
+                                "gbs": [_short(r["achieved"]) for r in c["points"]]}
     if "split_k_static" in secondary:
         st = secondary["split_k_static"]
-        out["split_k_static_us"] = {"static": _short(st["ms_static"] * 1e3),
-                                    "plan": _short(st["ms_plan"] * 1e3)}
+        out["split_k_static_us"] = [_short(st["ms_static"] * 1e3), _short(st["ms_plan"] * 1e3)]
     if "unaligned_tc" in secondary:
-        out["unaligned_tc"] = {r["product"]: "%s us %s TFLOP/s (%s)" % (
-            _short(r["ms_per_launch"] * 1e3), _short(r["tflops"]), _short(r["frac"]))
-            for r in secondary["unaligned_tc"]}
+        out["unaligned_tc"] = {"unit": "TFLOP/s"}
+        for r in secondary["unaligned_tc"]:
+            out["unaligned_tc"][r["product"].replace("vocab_50257_", "vocab_")] = [
+                _short(r["ms_per_launch"] * 1e3), _short(r["tflops"]), _short(r["frac"])]
     if "alu_rates" in secondary:
-        out["alu_tflops"] = {k: _short(v["tflops"]) for k, v in secondary["alu_rates"].items()}
+        out["alu_tflops"] = [_short(v["tflops"]) for v in secondary["alu_rates"].values()]
     return out
 
 
@@ -1006,7 +1025,7 @@ def run_ours(args):
         "summary": compact_summary(breakdown, secondary),
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     for it in items:
         it["plan"].close()
     if world > 1:
