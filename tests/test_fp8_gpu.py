@@ -425,6 +425,7 @@ def test_fp8_skinny_n(dtype, shapes):
 FP8_FUSED_CASES = [
     ("skinny_m", 1, (4, 2048), (2048, 512)),       # SIMT skinny-M
     ("skinny_m", 2, (12, 2048), (2048, 512)),      # warp-MMA skinny-M
+    ("skinny_m", 3, (12, 8192), (8192, 512)),      # tcgen05 skinny-M, K slices
     ("split_k", None, (24, 20000), (20000, 64)),   # warp-MMA split-K, two reduction levels
     ("skinny_n", None, (1000, 1024), (1024, 8)),   # warp-MMA skinny-N
     ("general_simt", None, (100, 300), (300, 200)),
