@@ -359,3 +359,44 @@ def test_f8_instruction_descriptor_layout():
             assert (d >> 17) & 0x3F == n // 8
             assert (d >> 24) & 0x1F == m // 16
             assert d & 0b1111 == 0 and (d >> 13) & 3 == 0 and (d >> 23) & 1 == 0 and d >> 29 == 0
+
+
+def test_route_for_misaligned_pointers_and_odd_rows():
+    """The host-side route an execute takes (no device needed): FP16 / BF16
+    stay on their tensor-core kernels with staging copies for operands the
+    TMA cannot read in place; a misaligned Y moves skinny and split-K
+    products to the general tiles; other types fall back to DIRECT."""
+    lib = binding.load()
+    al, off = 1 << 20, (1 << 20) + 2          # 16-byte aligned, and two bytes off
+    with Plan((300, 520), (520, 264), "bfloat16") as p:
+        assert p.algorithm == "general_tc"
+        h = p.handle
+        assert lib.olc_matmul_plan_algorithm_for(h, al, al, al, None) == 6
+        assert lib.olc_matmul_plan_staging_copies(h, al, al, al, None) == 0
+        assert lib.olc_matmul_plan_staging_copies(h, off, al, al, None) == 1
+        assert lib.olc_matmul_plan_staging_copies(h, off, off, off, None) == 2
+        assert lib.olc_matmul_plan_algorithm_for(h, off, off, off, None) == 6
+    with Plan((300, 515), (515, 263), "float16") as p:       # odd K and N: both staged
+        assert p.algorithm == "general_tc" and p.launches == 3
+        assert lib.olc_matmul_plan_staging_copies(p.handle, al, al, al, None) == 2
+    with Plan((4, 8192), (8192, 512), "float16") as p:       # skinny-M
+        h = p.handle
+        assert p.algorithm == "skinny_m"
+        assert lib.olc_matmul_plan_algorithm_for(h, off, al, al, None) == 3   # A copied densely
+        assert lib.olc_matmul_plan_staging_copies(h, off, al, al, None) == 1
+        assert lib.olc_matmul_plan_algorithm_for(h, al, al, off, None) == 6   # Y off: general tiles
+    with Plan((64, 128), (128, 96), "float32") as p:
+        h = p.handle
+        assert lib.olc_matmul_plan_algorithm_for(h, al, al, al, None) == 2
+    with Plan((1024, 1024), (1024, 1024), "float32") as p:
+        h = p.handle
+        assert p.algorithm == "general_simt"
+        # the FFMA register tiles load element by element: any alignment
+        assert lib.olc_matmul_plan_algorithm_for(h, al + 4, al, al, None) == 7
+        assert lib.olc_matmul_plan_staging_copies(h, al + 4, al, al, None) == 0
+    with Plan((4, 8192), (8192, 512), "float32") as p:
+        h = p.handle
+        assert p.algorithm == "skinny_m"
+        assert lib.olc_matmul_plan_algorithm_for(h, al, al, al, None) == 3
+        assert lib.olc_matmul_plan_algorithm_for(h, al + 4, al, al, None) == 2   # vector loads: DIRECT
+    assert lib.olc_matmul_plan_algorithm_for(None, al, al, al, None) == -1
