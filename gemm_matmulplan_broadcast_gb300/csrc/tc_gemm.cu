@@ -1009,11 +1009,11 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_addr) {
 }
 // TMA load into this CTA's shared memory, completing on an mbarrier that may
 // be in the peer CTA (shared::cluster address)
-__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster,
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
                                                  int c0, int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
@@ -1147,10 +1147,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
-            uint32_t stage = 0, phase = 0;
-            uint32_t armed_parity[STAGES];
-            bool armed[STAGES];
-            for (int i = 0; i < STAGES; ++i) armed[i] = false;
+            // the issue loop is on the critical path (one K block every 512
+            // MMA cycles): shared and cluster addresses advance by adds, and
+            // the stages armed for the abort drain are bits in registers
+            const uint32_t stage0 = smem_u32(base);
+            const uint32_t full0_leader = map_to(&s->full[0], 0);
+            const uint32_t a_tma_bytes = p.a_mn ? 64 * BK * 2 : 0;     // second A box, if any
+            uint32_t stage = 0, phase = 0, armed_bits = 0, parity_bits = 0;
             bool ok = true;
             for (int64_t u = cluster_id(); u < units && ok; u += cluster_count()) {
                 int half;
@@ -1166,22 +1169,23 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const int m0 = (int)(mb * 256 + rank * 128);
                 const int n0 = half < 0 ? (int)(nb * 256 + rank * 128) : (int)(nb * 256 + half * 128 + rank * 64);
                 const uint32_t tx = half < 0 ? 2u * STAGE_BYTES : 2u * (A_BYTES + B_BYTES / 2);
-                for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
+                const int k_step = F8 ? 128 : BK;
+                int k0 = 0;
+                for (int64_t kb = 0; kb < p.k_blocks; ++kb, k0 += k_step) {
                     if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    unsigned char* sa = base + stage * STAGE_BYTES;
-                    unsigned char* sb = sa + A_BYTES;
-                    const uint32_t full_leader = map_to(&s->full[stage], 0);
+                    const uint32_t sa = stage0 + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t full_leader = full0_leader + stage * (uint32_t)sizeof(uint64_t);
                     if (leader) {
                         mbar_arrive_expect_tx(&s->full[stage], tx);
-                        armed[stage] = true;
-                        armed_parity[stage] = phase;
+                        armed_bits |= 1u << stage;
+                        parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
                     }
-                    const int k0 = (int)(kb * (F8 ? 128 : BK));
-                    if (!p.a_mn) {
+                    if (!a_tma_bytes) {
                         tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
                     } else {
                         tma_load_3d_pair(sa, &tmap_a, full_leader, m0, k0, a_item);
-                        tma_load_3d_pair(sa + 64 * BK * 2, &tmap_a, full_leader, m0 + 64, k0, a_item);
+                        tma_load_3d_pair(sa + a_tma_bytes, &tmap_a, full_leader, m0 + 64, k0, a_item);
                     }
                     if (!p.b_k) {
                         tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
@@ -1195,7 +1199,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             if (*abort_flag && leader) {
                 for (int i = 0; i < STAGES; ++i)
-                    if (armed[i]) mbar_wait_drain(&s->full[i], armed_parity[i]);
+                    if ((armed_bits >> i) & 1u) mbar_wait_drain(&s->full[i], (parity_bits >> i) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -1203,6 +1207,18 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const uint32_t idesc = F8 ? f8_desc(p.f8_fmt, 256, 256)
                                       : instr_desc(p.is_bf16, 256, 256, p.a_mn, p.b_k ? 0 : 1);
             const uint32_t idesc_half = F8 ? idesc : instr_desc(p.is_bf16, 256, 128, p.a_mn, p.b_k ? 0 : 1);
+            // descriptors of stage 0, built once: a later stage and each
+            // 16-deep step add their byte offset >> 4 to the start-address
+            // field (bits 0-13), which no shared-memory address overflows.
+            // Issuing one K block must take well under the 512 cycles its
+            // four MMAs run for.
+            const uint32_t stage0 = smem_u32(base);
+            const uint64_t a_desc0 = p.a_mn ? smem_desc(stage0, 64 * BK * 2, 1024, 2u)
+                                            : smem_desc(stage0, 16, 1024, 2u);
+            const uint64_t b_desc0 = p.b_k ? smem_desc(stage0 + A_BYTES, 16, 1024, 2u)
+                                           : smem_desc(stage0 + A_BYTES, 64 * BK * 2, 1024, 2u);
+            const uint64_t a_step = p.a_mn ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+            const uint64_t b_step = p.b_k ? (UMMA_K * 2) >> 4 : (UMMA_K * 128) >> 4;
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t u = cluster_id(); u < units && ok; u += cluster_count()) {
@@ -1212,20 +1228,18 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (!mbar_wait(&s->acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * 256;
+                uint32_t first = 0u;      // 0 for the unit's first MMA: overwrite the accumulator
                 for (int64_t kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(base + stage * STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + A_BYTES;
+                    const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
+                    const uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = p.a_mn ? smem_desc(a_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u)
-                                                   : smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
-                        const uint64_t bd = p.b_k ? smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u)
-                                                  : smem_desc(b_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
-                        if constexpr (F8) mma2_f8(d_tmem, ad, bd, id, (kb > 0 || kk > 0) ? 1u : 0u);
-                        else mma2_f16(d_tmem, ad, bd, id, (kb > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (F8) mma2_f8(d_tmem, ad + kk * a_step, bd + kk * b_step, id, kk > 0 ? 1u : first);
+                        else mma2_f16(d_tmem, ad + kk * a_step, bd + kk * b_step, id, kk > 0 ? 1u : first);
                     }
+                    first = 1u;
                     commit2_both(&s->empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
