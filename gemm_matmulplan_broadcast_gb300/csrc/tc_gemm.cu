@@ -192,6 +192,14 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     }
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2) {
     asm volatile(
@@ -664,10 +672,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
-            uint32_t stage = 0, phase = 0;
-            uint32_t armed_parity[STAGES];
-            bool armed[STAGES];
-            for (int i = 0; i < STAGES; ++i) armed[i] = false;
+            // running shared addresses and register bitmasks keep the issue
+            // loop short (see the pair kernel's producer)
+            const uint32_t stage0 = smem_u32(base);
+            const uint32_t full0 = smem_u32(&s->full[0]);
+            uint32_t stage = 0, phase = 0, armed_bits = 0, parity_bits = 0;
             bool ok = true;
             Cursor cur = cursor_begin(p);
             int64_t tile, kb0, kb1;
@@ -680,38 +689,39 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const int a_item = (int)(a_off / p.a_item_elems);
                 const int b_item = (int)(b_off / p.b_item_elems);
                 const int m0 = (int)(mb * BM), n0 = (int)(nb * BN);
-                for (int64_t kb = kb0; kb < kb1; ++kb) {
+                int k0 = (int)(kb0 * BK);
+                for (int64_t kb = kb0; kb < kb1; ++kb, k0 += BK) {
                     if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    unsigned char* sa = base + stage * C::STAGE_BYTES;
-                    unsigned char* sb = sa + A_STAGE_BYTES;
+                    const uint32_t sa = stage0 + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint32_t fb = full0 + stage * (uint32_t)sizeof(uint64_t);
                     mbar_arrive_expect_tx(&s->full[stage], p.stage_tx_bytes);
-                    armed[stage] = true;
-                    armed_parity[stage] = phase;
-                    const int k0 = (int)(kb * BK);
+                    armed_bits |= 1u << stage;
+                    parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
                     if constexpr (!SWAP) {
                         if (!p.a_mn) {
-                            tma_load_3d(sa, &tmap_a, &s->full[stage], k0, m0, a_item);
+                            tma_load_3d(sa, &tmap_a, fb, k0, m0, a_item);
                         } else {
                             // A stored [K, M]: two MN-major 64-row boxes
-                            tma_load_3d(sa, &tmap_a, &s->full[stage], m0, k0, a_item);
-                            tma_load_3d(sa + 64 * BK * 2, &tmap_a, &s->full[stage], m0 + 64, k0, a_item);
+                            tma_load_3d(sa, &tmap_a, fb, m0, k0, a_item);
+                            tma_load_3d(sa + 64 * BK * 2, &tmap_a, fb, m0 + 64, k0, a_item);
                         }
                         if (!p.b_k) {
 #pragma unroll
                             for (int j = 0; j < C::NBLK; ++j)
-                                tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, &s->full[stage],
-                                            n0 + C::BLK_COLS * j, k0, b_item);
+                                tma_load_3d(sb + j * C::B_BLK_BYTES, &tmap_b, fb, n0 + C::BLK_COLS * j, k0,
+                                            b_item);
                         } else {
                             // B stored [N, K]: one K-major box of BN rows
-                            tma_load_3d(sb, &tmap_b, &s->full[stage], k0, n0, b_item);
+                            tma_load_3d(sb, &tmap_b, fb, k0, n0, b_item);
                         }
                     } else {
                         // MMA operand A = 128 columns of the problem's B (two
                         // 64-column MN-major boxes); operand B = the problem's
                         // A rows (K-major, rows past M read as zeros)
-                        tma_load_3d(sa, &tmap_a, &s->full[stage], m0, k0, b_item);
-                        tma_load_3d(sa + 64 * BK * 2, &tmap_a, &s->full[stage], m0 + 64, k0, b_item);
-                        tma_load_3d(sb, &tmap_b, &s->full[stage], k0, 0, a_item);
+                        tma_load_3d(sa, &tmap_a, fb, m0, k0, b_item);
+                        tma_load_3d(sa + 64 * BK * 2, &tmap_a, fb, m0 + 64, k0, b_item);
+                        tma_load_3d(sb, &tmap_b, fb, k0, 0, a_item);
                         (void)n0;
                     }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -720,7 +730,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if (*abort_flag) {
                 // let this CTA's own loads land before the CTA goes away
                 for (int i = 0; i < STAGES; ++i)
-                    if (armed[i]) mbar_wait_drain(&s->full[i], armed_parity[i]);
+                    if ((armed_bits >> i) & 1u) mbar_wait_drain(&s->full[i], (parity_bits >> i) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -728,6 +738,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (lane == 0) {
             const uint32_t idesc = SWAP ? instr_desc(p.is_bf16, BM, BN, 1, 0)
                                         : instr_desc(p.is_bf16, BM, BN, p.a_mn, p.b_k ? 0 : 1);
+            // descriptors of stage 0, advanced by adds to the start-address
+            // field (see the pair kernel's MMA issuer).
+            // Not swapped: A K-major (128-byte swizzle, 16 elements = 32
+            // bytes per step) or MN-major (16 K-rows of 128 bytes per step,
+            // the two 64-row boxes 8192 bytes apart); B MN-major (16 K-rows
+            // of SW bytes per step, boxes of BLK_COLS columns B_BLK_BYTES
+            // apart, 8-row groups 8 * SW apart) or K-major (transB: rows of
+            // 64 K-elements).  Swapped: A = the problem's B, MN-major; B =
+            // the problem's A rows, K-major.
+            const uint32_t stage0 = smem_u32(base);
+            uint64_t a_desc0, b_desc0, a_step, b_step;
+            if constexpr (!SWAP) {
+                a_desc0 = p.a_mn ? smem_desc(stage0, 64 * BK * 2, 1024, 2u) : smem_desc(stage0, 16, 1024, 2u);
+                a_step = p.a_mn ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+                b_desc0 = p.b_k ? smem_desc(stage0 + A_STAGE_BYTES, 16, 1024, 2u)
+                                : smem_desc(stage0 + A_STAGE_BYTES, C::B_BLK_BYTES, 8 * C::SW, C::LAYOUT);
+                b_step = p.b_k ? (UMMA_K * 2) >> 4 : (UMMA_K * C::SW) >> 4;
+            } else {
+                a_desc0 = smem_desc(stage0, 64 * BK * 2, 1024, 2u);
+                a_step = (UMMA_K * 128) >> 4;
+                b_desc0 = smem_desc(stage0 + A_STAGE_BYTES, 16, 1024, 2u);
+                b_step = (UMMA_K * 2) >> 4;
+            }
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             Cursor cur = cursor_begin(p);
@@ -737,35 +770,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (!mbar_wait(&s->acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+                uint32_t first = 0u;      // 0 for the tile's first MMA: overwrite the accumulator
                 for (int64_t kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(base + stage * C::STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+                    const uint64_t so = (uint64_t)((stage * C::STAGE_BYTES) >> 4);
+                    const uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // A: K-major, 128-byte swizzle; advance 16 elements = 32
-                        // bytes inside the swizzle row; 8-row groups 1024 apart
-                        uint64_t ad, bd;
-                        if constexpr (!SWAP) {
-                            ad = p.a_mn ? smem_desc(a_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u)
-                                        : smem_desc(a_addr + kk * UMMA_K * 2, 16, 1024, 2u);
-                            // B: MN-major; advance 16 K-rows of SW bytes; boxes of
-                            // BLK_COLS columns B_BLK_BYTES apart (LBO), 8-row
-                            // groups 8 * SW apart (SBO).  K-major (transB): rows
-                            // of 64 K-elements, 128-byte swizzle
-                            bd = p.b_k ? smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u)
-                                       : smem_desc(b_addr + kk * UMMA_K * C::SW, C::B_BLK_BYTES,
-                                                   8 * C::SW, C::LAYOUT);
-                        } else {
-                            // A: MN-major, 128-byte swizzle; advance 16 K-rows of
-                            // 128 bytes; the two 64-column boxes 8192 bytes apart
-                            ad = smem_desc(a_addr + kk * UMMA_K * 128, 64 * BK * 2, 1024, 2u);
-                            // B: K-major, 128-byte swizzle, rows of 64 K-elements
-                            bd = smem_desc(b_addr + kk * UMMA_K * 2, 16, 1024, 2u);
-                        }
-                        mma_f16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        mma_f16(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, kk > 0 ? 1u : first);
+                    first = 1u;
                     mma_commit(&s->empty[stage]);   // stage free once these MMAs finish
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
