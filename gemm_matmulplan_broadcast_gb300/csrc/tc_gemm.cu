@@ -985,11 +985,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 namespace pair {
 
-constexpr int STAGES = 7;                           // 7 x 32 KiB: the most that fits
 constexpr int A_BYTES = 128 * BK * 2;               // this CTA's 128 rows of A
 constexpr int B_BYTES = 128 * BK * 2;               // this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 32 KiB
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
+// 16-bit operands: 7 x 32 KiB, the most that fits.  FP8: 6 stages and an
+// epilogue staging area where each epilogue warp turns its 32 rows x 32
+// float32 columns into runs of whole rows (32 + 4 floats per row, so that
+// both the row-wise writes and the column-wise reads are free of bank
+// conflicts)
+constexpr int STAGE_PITCH = 36;                     // floats per staged row
+constexpr int STAGING_BYTES = 4 * 32 * STAGE_PITCH * 4;   // 4 warps: 18 KiB
+template <bool F8>
+constexpr int stages() { return F8 ? 6 : 7; }
+template <bool F8>
+constexpr int smem_bytes() {
+    return stages<F8>() * STAGE_BYTES + (F8 ? STAGING_BYTES : 0) + 1024 + 512;
+}
 constexpr int TMEM_COLS = 512;                       // two 256-column accumulators
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -1094,10 +1105,12 @@ template <bool F8>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    constexpr int STAGES = stages<F8>();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem* s = reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+    float* staging = reinterpret_cast<float*>(base + STAGES * STAGE_BYTES);
+    Smem* s = reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES + (F8 ? STAGING_BYTES : 0));
     volatile int* abort_flag = &s->abort_flag;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
@@ -1286,31 +1299,44 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const bool row_ok = row < p.M;
             const uint32_t t_base = tmem_base + ((uint32_t)(lane_group * 32) << 16) + acc * 256;
             if constexpr (F8) {
-                // float32 output rows; N is a multiple of 4: whole 16-byte groups
+                // float32 output rows; N is a multiple of 4: whole 16-byte
+                // groups.  Each 32-column run goes through this warp's
+                // staging rows, so that a warp store writes 4 rows x 128
+                // bytes instead of 16 bytes in each of 32 rows
                 float* yrow = static_cast<float*>(p.Y) + (item * p.M + (row_ok ? row : 0)) * p.N;
+                float* stage_rows = staging + lane_group * 32 * STAGE_PITCH;
+                const int64_t row0 = mb * 256 + rank * 128 + lane_group * 32;   // the warp's first row
+                const int cq = lane & 7;                  // 16-byte group this lane writes back
 #pragma unroll 1
                 for (int c = 0; c < 256; c += 32) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(t_base + c, r);
                     const int64_t col = nb * 256 + c;
-                    if (row_ok && col < p.N) {
-                        float v[32];
+                    if (col >= p.N) continue;             // warp-uniform: the whole run is past N
+                    float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        if (p.epi.mode != 0) {
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    if (p.epi.mode != 0 && row_ok) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col + i < p.N)
-                                    v[i] = apply_epilogue<float>(p.epi, v[i], row, col + i, yrow + col + i);
-                        }
-                        const int64_t left = (p.N - col) / 4;
-                        const int groups = (int)(left < 8 ? left : 8);
-                        float4* dst = reinterpret_cast<float4*>(yrow + col);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            if (q < groups)
-                                dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        for (int i = 0; i < 32; ++i)
+                            if (col + i < p.N)
+                                v[i] = apply_epilogue<float>(p.epi, v[i], row, col + i, yrow + col + i);
                     }
+                    float4* mine = reinterpret_cast<float4*>(stage_rows + lane * STAGE_PITCH);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        mine[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    __syncwarp();
+                    const int64_t gcol = col + cq * 4;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = (lane >> 3) + 4 * j;
+                        const int64_t grow = row0 + rr;
+                        const float4 w = *reinterpret_cast<const float4*>(stage_rows + rr * STAGE_PITCH + cq * 4);
+                        if (grow < p.M && gcol < p.N)
+                            *reinterpret_cast<float4*>(static_cast<float*>(p.Y) + (item * p.M + grow) * p.N + gcol) = w;
+                    }
+                    __syncwarp();                          // the rows are rewritten by the next run
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1942,7 +1968,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.items;
     if (pairs <= 0) return cudaSuccess;
     const cudaError_t attr_err =
-        set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<false>), pair::SMEM_BYTES);
+        set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<false>), pair::smem_bytes<false>());
     if (attr_err != cudaSuccess) return attr_err;
     // a last partial wave of r tiles on at most half the clusters runs as 2r
     // half tiles (256 x 128): the same work on twice the SMs, so the wave
@@ -1956,7 +1982,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.dynamicSmemBytes = pair::smem_bytes<false>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -2017,13 +2043,13 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
     const int64_t pairs = ceil_div(pr.M, 256) * ceil_div(pr.N, 256);
     if (pairs <= 0) return cudaSuccess;
     const cudaError_t attr_err =
-        set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<true>), pair::SMEM_BYTES);
+        set_smem_limit(reinterpret_cast<const void*>(pair::tc_pair_kernel<true>), pair::smem_bytes<true>());
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.dynamicSmemBytes = pair::smem_bytes<true>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
