@@ -116,6 +116,8 @@ struct Params {
     int a_mn;                 // A stored [K, M] (Gemm transA): MN-major A operand
     int b_k;                  // B stored [N, K] (Gemm transB): K-major B operand
     int y_unaligned;          // Y rows not 16-byte aligned: stores by alignment (general kernels)
+    int b_blocks;             // CTA pairs, MN-major B with N a multiple of 64: tmap_b is the 4-D
+                              // view [items][N/64][K][64] and one load brings both 64-column blocks
     int64_t pair_half_tiles;  // CTA pairs: the last tiles, run as two 256 x 128 halves each (a
                               // last partial wave of at most half the clusters); 0: none
     int f8_fmt;               // 8-bit float operands (pair kernel): 0 = E4M3, 1 = E5M2
@@ -1042,6 +1044,14 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc2(uint32_t* dst_smem, uint32_t cols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(dst_smem)),
@@ -1195,7 +1205,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 // whole tile, 64 of a half tile
                 const int m0 = (int)(mb * 256 + rank * 128);
                 const int n0 = half < 0 ? (int)(nb * 256 + rank * 128) : (int)(nb * 256 + half * 128 + rank * 64);
-                const uint32_t tx = half < 0 ? 2u * STAGE_BYTES : 2u * (A_BYTES + B_BYTES / 2);
+                // bytes landing on the leader's full barrier from both CTAs;
+                // the 4-D B load brings two 64-column blocks for half tiles
+                // too (the second one unused)
+                const uint32_t tx = (half < 0 || p.b_blocks) ? 2u * STAGE_BYTES : 2u * (A_BYTES + B_BYTES / 2);
                 const int k_step = F8 ? 128 : BK;
                 int k0 = 0;
                 for (int64_t kb = 0; kb < p.k_blocks; ++kb, k0 += k_step) {
@@ -1214,7 +1227,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         tma_load_3d_pair(sa, &tmap_a, full_leader, m0, k0, a_item);
                         tma_load_3d_pair(sa + a_tma_bytes, &tmap_a, full_leader, m0 + 64, k0, a_item);
                     }
-                    if (!p.b_k) {
+                    if (p.b_blocks) {
+                        tma_load_4d_pair(sb, &tmap_b, full_leader, 0, k0, n0 >> 6, b_item);
+                    } else if (!p.b_k) {
                         tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
                         if (half < 0)
                             tma_load_3d_pair(sb + 64 * BK * 2, &tmap_b, full_leader, n0 + 64, k0, b_item);
@@ -1707,6 +1722,25 @@ static bool encode_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+// rank-4 view of a row-major [items][K][N] 16-bit B (rows `ld` elements
+// apart, N a multiple of 64) as [items][N / 64][K][64]: a box {64, BK, 2, 1}
+// is two 64-column MN-major blocks of BK rows, one after the other in shared
+// memory (the layout of two 3-D boxes at n0 and n0 + 64), in one TMA load
+static bool encode_b_blocks(CUtensorMap* map, const void* base, int is_bf16, uint64_t n, uint64_t k,
+                            uint64_t items, uint64_t ld) {
+    auto fn = encode_fn();
+    if (!fn || n % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, k, n / 64, items};
+    cuuint64_t strides[3] = {ld * 2, 128, ld * k * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)BK, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BN>
 static CUtensorMapSwizzle b_swizzle() {
     return Cfg<BN>::SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -1944,7 +1978,11 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
              : encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B,
                          a_ld)))
         return cudaErrorInvalidValue;
-    if (!(bt ? encode_3d(&mb, pr.B, bf, pr.K, pr.N, b_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+    // MN-major B with whole 64-column blocks: one 4-D load per K block
+    // instead of two 3-D ones (the producer lane issues every load)
+    const bool b_blocks = !bt && pr.N % 64 == 0 && encode_b_blocks(&mb, pr.B, bf, pr.N, pr.K, b_items, b_ld);
+    if (!b_blocks &&
+        !(bt ? encode_3d(&mb, pr.B, bf, pr.K, pr.N, b_items, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
              : encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
                          b_ld)))
         return cudaErrorInvalidValue;
@@ -1958,6 +1996,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     p.a_item_elems = pr.M * pr.K;
     p.b_item_elems = pr.K * pr.N;
     p.map = pr.map;
+    p.b_blocks = b_blocks ? 1 : 0;
     p.Y = pr.Y;
     p.err = device_error_word();
     p.is_bf16 = bf;
