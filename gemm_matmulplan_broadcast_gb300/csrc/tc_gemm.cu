@@ -996,6 +996,9 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 32 KiB
 // both the row-wise writes and the column-wise reads are free of bank
 // conflicts)
 constexpr int STAGE_PITCH = 36;                     // floats per staged row
+// warps: 0 loads A, 1 issues the MMAs, 2-5 run the epilogue, 6 loads B (one
+// TMA load per K block and lane keeps each issue loop short)
+constexpr int PAIR_THREADS = 224;
 constexpr int STAGING_BYTES = 4 * 32 * STAGE_PITCH * 4;   // 4 warps: 18 KiB
 template <bool F8>
 constexpr int stages() { return F8 ? 6 : 7; }
@@ -1112,7 +1115,7 @@ __device__ __forceinline__ void commit2_local(uint64_t* bar) {
 // the byte geometry of the shared-memory stages is the same as for 16-bit
 // operands with K-major B.
 template <bool F8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
     constexpr int STAGES = stages<F8>();
@@ -1138,7 +1141,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&s->full[i], 1);
+            mbar_init(&s->full[i], 2);        // the leader's A and B loaders arm it
             mbar_init(&s->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1180,13 +1183,19 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         nb = in / gm;
     };
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 6) {
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
-            // the issue loop is on the critical path (one K block every 512
-            // MMA cycles): shared and cluster addresses advance by adds, and
-            // the stages armed for the abort drain are bits in registers
+            // warp 0 loads A, warp 6 loads B, each waiting for the same free
+            // stages; the leader's two loaders each arm the leader's full
+            // barrier with their operand's bytes from both CTAs.  The issue
+            // loop is on the critical path (one K block every 512 MMA
+            // cycles): shared and cluster addresses advance by adds, and the
+            // stages armed for the abort drain are bits in registers
+            const bool load_a = warp == 0;
+            if (load_a)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            else
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
             const uint32_t stage0 = smem_u32(base);
             const uint32_t full0_leader = map_to(&s->full[0], 0);
             const uint32_t a_tma_bytes = p.a_mn ? 64 * BK * 2 : 0;     // second A box, if any
@@ -1205,10 +1214,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 // whole tile, 64 of a half tile
                 const int m0 = (int)(mb * 256 + rank * 128);
                 const int n0 = half < 0 ? (int)(nb * 256 + rank * 128) : (int)(nb * 256 + half * 128 + rank * 64);
-                // bytes landing on the leader's full barrier from both CTAs;
-                // the 4-D B load brings two 64-column blocks for half tiles
-                // too (the second one unused)
-                const uint32_t tx = (half < 0 || p.b_blocks) ? 2u * STAGE_BYTES : 2u * (A_BYTES + B_BYTES / 2);
+                // this loader's bytes landing on the leader's full barrier
+                // from both CTAs; the 4-D B load brings two 64-column blocks
+                // for half tiles too (the second one unused)
+                const uint32_t tx = load_a ? 2u * A_BYTES : ((half < 0 || p.b_blocks) ? 2u * B_BYTES : B_BYTES);
                 const int k_step = F8 ? 128 : BK;
                 int k0 = 0;
                 for (int64_t kb = 0; kb < p.k_blocks; ++kb, k0 += k_step) {
@@ -1221,13 +1230,14 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         armed_bits |= 1u << stage;
                         parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
                     }
-                    if (!a_tma_bytes) {
-                        tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
-                    } else {
-                        tma_load_3d_pair(sa, &tmap_a, full_leader, m0, k0, a_item);
-                        tma_load_3d_pair(sa + a_tma_bytes, &tmap_a, full_leader, m0 + 64, k0, a_item);
-                    }
-                    if (p.b_blocks) {
+                    if (load_a) {
+                        if (!a_tma_bytes) {
+                            tma_load_3d_pair(sa, &tmap_a, full_leader, k0, m0, a_item);
+                        } else {
+                            tma_load_3d_pair(sa, &tmap_a, full_leader, m0, k0, a_item);
+                            tma_load_3d_pair(sa + a_tma_bytes, &tmap_a, full_leader, m0 + 64, k0, a_item);
+                        }
+                    } else if (p.b_blocks) {
                         tma_load_4d_pair(sb, &tmap_b, full_leader, 0, k0, n0 >> 6, b_item);
                     } else if (!p.b_k) {
                         tma_load_3d_pair(sb, &tmap_b, full_leader, n0, k0, b_item);
@@ -2020,7 +2030,7 @@ static cudaError_t launch_pair(olc_dtype dt, const Problem& pr, int sm_count, cu
     const int64_t clusters = min64(units, per_wave);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(pair::PAIR_THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::smem_bytes<false>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -2087,7 +2097,7 @@ static cudaError_t launch_pair_f8_impl(olc_dtype dt, const Problem& pr, const vo
     const int64_t clusters = min64(pairs, (int64_t)(sm_count / 2));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(pair::PAIR_THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::smem_bytes<true>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
