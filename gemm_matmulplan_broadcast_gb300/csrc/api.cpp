@@ -79,6 +79,11 @@ struct olc_matmul_plan {
     size_t ws_bytes;
     size_t partial_bytes;
     size_t counter_count;
+    // the last execute that used the workspace or the staging buffer:
+    // an execute on another stream waits for it (created at first use)
+    cudaEvent_t state_ev;
+    cudaStream_t state_stream;
+    int state_ev_live;           // state_ev marks the last such execute
 };
 
 namespace {
@@ -532,6 +537,44 @@ Route route_of(const olc_matmul_plan* p, const void* A, const void* B, const voi
     return r;
 }
 
+cudaError_t launch_route(const olc_matmul_plan* p, const Problem& pr, olc_dtype dt, int algo,
+                         const void* B, cudaStream_t s);
+
+// Executes that use the plan's workspace (split partials and counters, the
+// per-call FP8 transpose of B) or its staging buffer must not overlap on
+// the GPU.  An execute on another stream than the last such one waits for
+// it (cudaStreamWaitEvent), so calls from several streams are serialised
+// on that state instead of racing; on one stream, stream order does it.
+// Nothing is recorded or waited for while `s` is capturing a graph:
+// ordering captured work is the graph's.
+cudaError_t order_after_state_use(olc_matmul_plan* p, cudaStream_t s) {
+    if (!p->state_ev_live || p->state_stream == s) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
+    return cudaStreamWaitEvent(s, p->state_ev, 0);
+}
+
+cudaError_t note_state_use(olc_matmul_plan* p, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) {
+        p->state_ev_live = 0;        // a captured use is ordered by its graph
+        return cudaSuccess;
+    }
+    if (!p->state_ev) {
+        e = cudaEventCreateWithFlags(&p->state_ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaEventRecord(p->state_ev, s);
+    if (e != cudaSuccess) return e;
+    p->state_stream = s;
+    p->state_ev_live = 1;
+    return cudaSuccess;
+}
+
 olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, cudaStream_t s,
                const void* C = nullptr, const void* R = nullptr) {
     const int64_t n = out_numel(p);
@@ -571,6 +614,11 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
     const Route rt = route_of(p, A, B, Y, R);
     const int algo = rt.algo;
     cudaError_t e = cudaSuccess;
+    const bool uses_state = p->workspace != nullptr || rt.need.a || rt.need.b;
+    if (uses_state) {
+        e = order_after_state_use(mp, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     if (rt.need.a || rt.need.b) {
         const olc_status st = ensure_stage(mp, rt.need.a_bytes + rt.need.b_bytes);
         if (st != OLC_OK) return st;
@@ -601,6 +649,15 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         pr.b_ld = pad8(stored_b(p).cols);
     }
     pr.y_unaligned = rt.y_unaligned ? 1 : 0;
+    if (algo < OLC_ALGO_DIRECT || algo > OLC_ALGO_GENERAL_SIMT) return OLC_ERR_INVALID;
+    e = launch_route(p, pr, dt, algo, B, s);
+    if (e == cudaSuccess && uses_state) e = note_state_use(mp, s);
+    return from_cuda(e);
+}
+
+cudaError_t launch_route(const olc_matmul_plan* p, const Problem& pr, olc_dtype dt, int algo,
+                         const void* B, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
     if (is_fp8(dt)) {
         // the plan's constant B comes transposed already
         const void* bt = (p->const_bt && B == p->const_b) ? p->const_bt : nullptr;
@@ -613,7 +670,7 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
         else
             e = algo == OLC_ALGO_GENERAL_TC ? launch_fp8_tc(dt, pr, p->sm_count, workspace_of(p), s, bt)
                                             : launch_fp8_simt(dt, pr, s);
-        return from_cuda(e);
+        return e;
     }
     switch (algo) {
         case OLC_ALGO_DIRECT: e = launch_direct(dt, pr, s); break;
@@ -630,9 +687,9 @@ olc_status run(const olc_matmul_plan* p, const void* A, const void* B, void* Y, 
             e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
             break;
         case OLC_ALGO_GENERAL_TC: e = launch_general_tc(dt, pr, p->sm_count, s, p->tc_variant); break;
-        default: return OLC_ERR_INVALID;
+        default: return cudaErrorInvalidValue;
     }
-    return from_cuda(e);
+    return e;
 }
 
 }  // namespace
@@ -824,6 +881,14 @@ void olc_matmul_plan_destroy(olc_matmul_plan* plan) {
     if (!plan) return;
     free_workspace(plan);
     free_stage(plan);
+    if (plan->state_ev) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (plan->device >= 0 && cur != plan->device) cudaSetDevice(plan->device);
+        cudaEventDestroy(plan->state_ev);
+        if (plan->device >= 0 && cur >= 0 && cur != plan->device) cudaSetDevice(cur);
+        cudaGetLastError();
+    }
     if (plan->pipe_ready) {
         int cur = -1;
         cudaGetDevice(&cur);

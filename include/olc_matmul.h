@@ -20,9 +20,17 @@
  *    dimensions fail before compute).
  *  - Functions returning olc_status never abort the process.
  *  - A plan is bound to the CUDA device that was current when it was created.
- *    It may be executed on any stream of that device, but not concurrently
- *    from two host threads or on two streams at once when it holds a split
- *    reduction workspace (olc_matmul_plan_workspace_bytes > 0).
+ *    It may be executed on any stream of that device; its calls must not run
+ *    concurrently from two host threads.  Executes that use the plan's own
+ *    device state -- its workspace (olc_matmul_plan_workspace_bytes > 0:
+ *    split reductions, the per-call transpose of an 8-bit B) or its staging
+ *    buffer (olc_matmul_plan_staging_copies > 0) -- are ordered across
+ *    streams by the plan: such an execute on another stream than the
+ *    previous one waits, on the GPU, for that previous one to finish
+ *    (cudaStreamWaitEvent on an event the plan records; one event, created
+ *    at the first such execute).  While a stream is capturing a graph the
+ *    plan records and waits for nothing: ordering captured launches against
+ *    other uses of the plan is the caller's.
  */
 #ifndef OLC_MATMUL_H
 #define OLC_MATMUL_H
