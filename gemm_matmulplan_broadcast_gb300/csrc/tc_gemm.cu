@@ -990,21 +990,20 @@ namespace pair {
 constexpr int A_BYTES = 128 * BK * 2;               // this CTA's 128 rows of A
 constexpr int B_BYTES = 128 * BK * 2;               // this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 32 KiB
-// 16-bit operands: 7 x 32 KiB, the most that fits.  FP8: 6 stages and an
-// epilogue staging area where each epilogue warp turns its 32 rows x 32
-// float32 columns into runs of whole rows (32 + 4 floats per row, so that
-// both the row-wise writes and the column-wise reads are free of bank
-// conflicts)
-constexpr int STAGE_PITCH = 36;                     // floats per staged row
 // warps: 0 loads A, 1 issues the MMAs, 2-5 run the epilogue, 6 loads B (one
 // TMA load per K block and lane keeps each issue loop short)
 constexpr int PAIR_THREADS = 224;
+// 6 stages and an epilogue staging area where each epilogue warp turns its
+// 32 rows x 128 bytes (32 float32 columns, or 64 16-bit ones) into runs of
+// whole rows (36 words per row, so that both the row-wise writes and the
+// column-wise reads are free of bank conflicts)
+constexpr int STAGE_PITCH = 36;                     // 32-bit words per staged row
 constexpr int STAGING_BYTES = 4 * 32 * STAGE_PITCH * 4;   // 4 warps: 18 KiB
 template <bool F8>
-constexpr int stages() { return F8 ? 6 : 7; }
+constexpr int stages() { return 6; }
 template <bool F8>
 constexpr int smem_bytes() {
-    return stages<F8>() * STAGE_BYTES + (F8 ? STAGING_BYTES : 0) + 1024 + 512;
+    return stages<F8>() * STAGE_BYTES + STAGING_BYTES + 1024 + 512;
 }
 constexpr int TMEM_COLS = 512;                       // two 256-column accumulators
 
@@ -1123,7 +1122,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* staging = reinterpret_cast<float*>(base + STAGES * STAGE_BYTES);
-    Smem* s = reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES + (F8 ? STAGING_BYTES : 0));
+    Smem* s = reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES + STAGING_BYTES);
     volatile int* abort_flag = &s->abort_flag;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
@@ -1371,6 +1370,55 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             unsigned char* yrow = static_cast<unsigned char*>(p.Y) +
                                   ((item * p.M + (row_ok ? row : 0)) * p.N) * 2;
+            if (!p.y_unaligned) {
+                // 64-column runs (two TMEM loads) through this warp's staging
+                // rows, so that a warp store writes 4 rows x 128 bytes; Y's
+                // rows are 16-byte multiples here (N % 8 == 0)
+                uint32_t* stage_rows = reinterpret_cast<uint32_t*>(staging) + lane_group * 32 * STAGE_PITCH;
+                const int64_t row0 = mb * 256 + rank * 128 + lane_group * 32;   // the warp's first row
+                const int cq = lane & 7;                  // 16-byte group this lane writes back
+#pragma unroll 1
+                for (int c = 0; c < width; c += 64) {
+                    uint32_t packed[32];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_base + c + hh * 32, r);
+                        const int64_t col = cbase + c + hh * 32;
+                        if (row_ok && col < p.N) {
+                            const int64_t left = (p.N - col) / 8;
+                            const int groups = (int)(left < 4 ? left : 4);
+                            epi_run<16>(p, r, row, col, yrow + col * 2, groups, packed + hh * 16);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) packed[hh * 16 + i] = 0u;   // never stored
+                        }
+                    }
+                    const int64_t col0 = cbase + c;
+                    if (col0 >= p.N) continue;            // warp-uniform: the whole run is past N
+                    uint4* mine = reinterpret_cast<uint4*>(stage_rows + lane * STAGE_PITCH);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        mine[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    __syncwarp();
+                    const int64_t gcol = col0 + cq * 8;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = (lane >> 3) + 4 * j;
+                        const int64_t grow = row0 + rr;
+                        const uint4 w = *reinterpret_cast<const uint4*>(stage_rows + rr * STAGE_PITCH + cq * 4);
+                        if (grow < p.M && gcol < p.N)
+                            *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.Y) +
+                                                      ((item * p.M + grow) * p.N + gcol) * 2) = w;
+                    }
+                    __syncwarp();                          // the rows are rewritten by the next run
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) remote_arrive(acc_empty_leader[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < width; c += 32) {
                 uint32_t r[32];
