@@ -68,6 +68,7 @@ KERNEL_CASES = [
     ((3, 1, 260, 64), (1, 2, 64, 264), ["bfloat16"], "general_tc", 1),
     ((300, 520), (520, 264), ["bfloat16", "float16"], "general_tc", 2),       # CTA pairs
     ((1024, 2048), (2048, 1024), ["bfloat16"], "general_tc", 2),
+    ((300, 200), (200, 320), ["bfloat16", "float16"], "general_tc", 2),   # 4-D B loads, blocks past N
 ]
 CASES = [(a, b, dt, al, v) for a, b, dts, al, v in KERNEL_CASES for dt in dts]
 

@@ -462,6 +462,12 @@ TC_PAIR_SHAPES = [
     ((1792, 512), (512, 2816)),
     ((4096, 256), (256, 4096)),
     ((3, 1, 500, 128), (1, 2, 128, 600)),
+    # N a multiple of 64: B's two 64-column blocks come in one 4-D load, and
+    # blocks past N (the peer CTA's, or the second of a pair) read as zeros
+    ((300, 200), (200, 320)),
+    ((512, 64), (64, 448)),
+    ((3, 1, 260, 96), (1, 2, 96, 384)),   # broadcast batch through the 4-D map
+    ((1792, 128), (128, 2880)),           # 84 tiles: 8 run as halves, the last column tile partial
 ]
 
 
