@@ -127,6 +127,12 @@ tile_gemm_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
 
     const int tx = threadIdx.x % TX;
     const int ty = threadIdx.x / TX;
+    // launched with programmatic dependent launch: wait for the previous
+    // kernel in the stream before touching global memory; the next launch
+    // is released once this block's products are done (released at the
+    // start, the next kernel's blocks would hold SM resources through all
+    // of this one)
+    grid_dependency_wait();
     acc_t acc[TM][TN];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
@@ -163,6 +169,7 @@ tile_gemm_kernel(Problem p, int64_t tiles_m, int64_t tiles_n) {
         }
         __syncthreads();
     }
+    grid_launch_dependents();
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int64_t gm = m0 + ty + i * TY;
@@ -181,9 +188,8 @@ static cudaError_t launch_tile(const Problem& p, cudaStream_t stream) {
     const int64_t blocks = tm * tn * p.items;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    tile_gemm_kernel<T, BM, BN, BK, TM, TN>
-        <<<(unsigned)blocks, (BM / TM) * (BN / TN), 0, stream>>>(p, tm, tn);
-    return cudaGetLastError();
+    return launch_pdl(tile_gemm_kernel<T, BM, BN, BK, TM, TN>, dim3((unsigned)blocks),
+                      dim3((BM / TM) * (BN / TN)), 0, stream, p, tm, tn);
 }
 
 // ---------------------------------------------------------------------------
@@ -229,6 +235,7 @@ __global__ void __launch_bounds__(256) wholek_kernel(Problem p, int64_t tiles_m,
     T* __restrict__ Y = static_cast<T*>(p.Y) + item * p.M * p.N;
     const int64_t M = p.M, N = p.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dependency_wait();                    // programmatic dependent launch, as above
 
     // A rows m0 + r (r = warp, warp + 8, ...), lanes along k; B rows k
     // (k = warp, warp + 8, ...), lanes along n.  Outside the product: zeros.
@@ -262,6 +269,7 @@ __global__ void __launch_bounds__(256) wholek_kernel(Problem p, int64_t tiles_m,
         c10 = fma(a1, b0, c10);
         c11 = fma(a1, b1, c11);
     }
+    grid_launch_dependents();
     const T c[2][2] = {{c00, c01}, {c10, c11}};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -292,8 +300,7 @@ static cudaError_t launch_wholek(const Problem& p, cudaStream_t stream) {
     const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(wholek_kernel<T>),
                                          (int)((32 * (wholek_max_k<T>() + 1) + wholek_max_k<T>() * 32) * sizeof(T)));
     if (e != cudaSuccess) return e;
-    wholek_kernel<T><<<(unsigned)blocks, 256, smem, stream>>>(p, tm, tn);
-    return cudaGetLastError();
+    return launch_pdl(wholek_kernel<T>, dim3((unsigned)blocks), dim3(256), smem, stream, p, tm, tn);
 }
 
 cudaError_t launch_direct(olc_dtype dt, const Problem& p, cudaStream_t stream) {
