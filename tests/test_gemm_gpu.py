@@ -79,8 +79,11 @@ def test_gemm_small_all_algorithms(dtype, ta, tb, c_shape):
 @pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
 @pytest.mark.parametrize("ta,tb", [(False, False), (True, False), (False, True), (True, True)])
 @pytest.mark.parametrize("variant", [1, 2])
-def test_gemm_tensor_cores_large(dtype, ta, tb, variant):
-    m, n, k = 520, 776, 264
+# N = 832 = 13 x 64: the CTA pairs load MN-major B as 4-D boxes of two 64-column
+# blocks, the last one past N
+@pytest.mark.parametrize("n", [776, 832])
+def test_gemm_tensor_cores_large(dtype, ta, tb, variant, n):
+    m, k = 520, 264
     a, b, c = _operands(m, n, k, ta, tb, (n,), dtype, synth.normal(1.0), seed=4)
     algo = _check(a, b, c, dtype, ta, tb, 0.5, 2.0, variant=variant)
     assert algo == "general_tc"
