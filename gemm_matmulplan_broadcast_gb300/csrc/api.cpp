@@ -84,6 +84,9 @@ struct olc_matmul_plan {
     cudaEvent_t state_ev;
     cudaStream_t state_stream;
     int state_ev_live;           // state_ev marks the last such execute
+    // row chunks of a host-buffer pipeline: the whole product's cluster
+    // split-K choice (0 on every plan; set on the chunk copies only)
+    int chunk_tc_ways;
 };
 
 namespace {
@@ -165,6 +168,7 @@ Problem make_problem(const olc_matmul_plan* p, const void* A, const void* B, voi
     // an 8-bit few-row plan with a constant B runs the tcgen05 kernel
     // (variant 3) unless a kernel family was asked for
     pr.variant = (p->f8_const_tc && (p->tc_variant == 0 || p->tc_variant == 3)) ? 3 : p->tc_variant;
+    pr.tc_ways = p->chunk_tc_ways;
     pr.a_trans = p->trans_a;
     pr.b_trans = p->trans_b;
     // Gemm: alpha * acc + beta * C, then the fused residual and activation;
@@ -386,8 +390,17 @@ int choose_algorithm(const olc_matmul_plan* p) {
     // Split-K only for the guarded corner: too few output tiles (counting the
     // batch, which takes priority) to fill half the SMs, and a long K.
     const int64_t tiles = ((rows + 127) / 128) * ((N + 127) / 128) * items;
-    if (tiles * 2 <= p->sm_count && K >= 8 * 1024 && feasible(p, OLC_ALGO_SPLIT_K))
-        return OLC_ALGO_SPLIT_K;
+    if (tiles * 2 <= p->sm_count && K >= 8 * 1024 && feasible(p, OLC_ALGO_SPLIT_K)) {
+        // FLOAT16 / BFLOAT16 outputs above 32 x 32 whose general tiles take
+        // the cluster split-K (slices summed through distributed shared
+        // memory) stay there: faster than the global two-level reduction
+        // (BF16 [64, 8192] x [8192, 512]: 14.9 against 38.8 us; [128, 16384]
+        // x [16384, 1024]: 24.9 against 71.8 us)
+        const bool tiny_out = rows <= 32 && N <= 32 && items == 1;
+        if (!(is_half(p->dtype) && !tiny_out && feasible(p, OLC_ALGO_GENERAL_TC) &&
+              tc_general_csplit_ways(p->dtype, make_problem(p, nullptr, nullptr, nullptr), p->sm_count) >= 2))
+            return OLC_ALGO_SPLIT_K;
+    }
     // Short-K FLOAT / DOUBLE products that leave the register-tile kernel
     // few tiles per SM: DIRECT's whole-K 32 x 32 tiles (one global round
     // trip per tile, four times as many blocks) are faster.  Measured on
@@ -1154,6 +1167,11 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_ho
         // once they are computed; the user stream waits for the last copy.
         const int64_t rows = plan->rows, K = plan->K, N = plan->N;
         const int64_t step = (rows / chunks + 255) / 256 * 256;
+        int whole_ways = 0;
+        if (plan->algo == OLC_ALGO_GENERAL_TC && plan->tc_variant == 0) {
+            const Problem whole = make_problem(plan, A_dev, B_dev, Y_dev);
+            whole_ways = tc_general_csplit_ways(plan->dtype, whole, plan->sm_count);
+        }
         const size_t b_bytes = (size_t)(numel(plan->b_shape, plan->b_rank) * eb);
         cudaError_t e = cudaEventRecord(mp->ev_start, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(mp->copy_in, mp->ev_start, 0);
@@ -1178,6 +1196,9 @@ olc_status olc_matmul_execute_host(const olc_matmul_plan* plan, const void* A_ho
             olc_matmul_plan sub = *plan;
             sub.rows = rn;
             sub.M = rn;
+            // the chunks sum every element as the whole product would: the
+            // same cluster split-K slices, or none
+            sub.chunk_tc_ways = whole_ways >= 2 ? whole_ways : 1;
             const void* Ac = static_cast<const unsigned char*>(A_dev) + r0 * K * eb;
             void* Yc = static_cast<unsigned char*>(Y_dev) + r0 * N * eb;
             const void* Cc = nullptr;

@@ -61,6 +61,11 @@ struct Problem {
     // 8: the general tensor-core kernels store with 2-, 4- and 16-byte
     // accesses as each row's alignment allows.
     int y_unaligned;
+    // General FP16/BF16 tiles: K slices per tile of the cluster split-K (0:
+    // chosen from this problem's shape; 1: none; k >= 2: k).  Row chunks of
+    // a larger product carry the whole product's choice, so that every
+    // output element is summed in the same order as without chunks.
+    int tc_ways;
 };
 
 // Workspace handed to the split reductions: `partials` holds fp32/fp64
@@ -172,6 +177,9 @@ cudaError_t launch_pair_f8(olc_dtype dt, const Problem& p, const void* bt, int s
 // GENERAL_TC: tcgen05 tensor-core GEMM for FLOAT16 / BFLOAT16.
 // tc_shape_ok: the dense operands are TMA-readable as given (16-byte rows).
 bool tc_shape_ok(olc_dtype dt, int64_t N, int64_t K);
+// cluster split-K slices the general FP16/BF16 tiles would use for this
+// problem (0: none)
+int tc_general_csplit_ways(olc_dtype dt, const Problem& p, int sm_count);
 // Copy `rows` rows of `cols` 16-bit elements (src rows dense, any 2-byte
 // alignment) into dst rows `pitch` elements apart (dst 16-byte aligned,
 // pitch a multiple of 8 >= cols); the pitch's extra elements are zeroed.

@@ -1743,6 +1743,215 @@ splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
 }  // namespace tiny
 
 // ---------------------------------------------------------------------------
+// Cluster split-K for general FP16/BF16 products whose 128 x 256 tiles leave
+// most SMs idle (a few hundred rows, or a narrow N): the K blocks of each
+// tile are cut into `ways` slices, one per CTA of a thread-block cluster.
+// Each CTA streams its slice of A and B through a 4-stage TMA ring into a
+// 128 x 256 TMEM accumulator, moves the accumulator into a float32 partial
+// tile in its own shared memory (the ring, idle by then), and after a
+// cluster barrier sums its share of the tile's 8-column runs over the
+// cluster's partials through distributed shared memory, in slice order (so
+// the result does not depend on timing), runs the epilogue and stores.  No
+// global workspace, no atomics; a second cluster barrier keeps every CTA's
+// shared memory alive until the others have read it.
+
+namespace csplit {
+
+constexpr int BN = 256;
+constexpr int A_BYTES = BM * BK * 2;               // 16 KiB (rows past M: stale, never stored)
+constexpr int B_BYTES = BK * BN * 2;               // 32 KiB: four 64-column MN-major blocks
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KiB
+constexpr int STAGES = 4;
+constexpr int PART_PITCH = BN + 4;                 // floats per partial row: float4 rows 16 B apart in banks
+constexpr int PART_BYTES = BM * PART_PITCH * 4;    // 133,120 bytes, inside the idle ring
+static_assert(PART_BYTES <= STAGES * STAGE_BYTES, "the partial tile fits in the ring");
+constexpr int THREADS_CS = 192;                    // producer, MMA issuer, 4 epilogue warps
+constexpr int TMEM_COLS = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int MAX_WAYS = 8;
+
+struct Bars {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full;
+    int abort_flag;
+    uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(THREADS_CS, 1)
+csplit_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+              const Params p, int ways, int64_t kb_per) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars* s = reinterpret_cast<Bars*>(base + STAGES * STAGE_BYTES);
+    float* part = reinterpret_cast<float*>(base);          // after the main loop
+    volatile int* abort_flag = &s->abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = (int)pair::cluster_rank();            // this CTA's K slice
+    const int64_t tile = pair::cluster_id();
+    const int64_t item = tile / p.tiles_per_item;
+    const int64_t r_in = tile % p.tiles_per_item;
+    const int64_t mb = r_in / p.tiles_n, nb = r_in % p.tiles_n;
+    const int64_t kb0 = rank * kb_per;
+    const int64_t kb1 = min64(p.k_blocks, kb0 + kb_per);   // the host leaves no slice empty
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&s->full[i], 1);
+            mbar_init(&s->empty[i], 1);
+        }
+        mbar_init(&s->acc_full, 1);
+        s->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(&s->tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s->tmem_base;
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+        int64_t a_off, b_off;
+        batch_offsets(p.map, item, a_off, b_off);
+        const int a_item = (int)(a_off / p.a_item_elems);
+        const int b_item = (int)(b_off / p.b_item_elems);
+        const int m0 = (int)(mb * BM), n0 = (int)(nb * BN);
+        const uint32_t stage0 = smem_u32(base);
+        const uint32_t full0 = smem_u32(&s->full[0]);
+        uint32_t stage = 0, phase = 0, armed_bits = 0, parity_bits = 0;
+        int k0 = (int)(kb0 * BK);
+        for (int64_t kb = kb0; kb < kb1; ++kb, k0 += BK) {
+            if (!mbar_wait(&s->empty[stage], phase ^ 1, abort_flag, p.err)) break;
+            const uint32_t sa = stage0 + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+            const uint32_t fb = full0 + stage * (uint32_t)sizeof(uint64_t);
+            mbar_arrive_expect_tx(&s->full[stage], p.stage_tx_bytes);
+            armed_bits |= 1u << stage;
+            parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+            tma_load_3d(sa, &tmap_a, fb, k0, m0, a_item);
+            if (p.b_blocks) {
+                asm volatile(
+                    "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(sb),
+                    "l"(reinterpret_cast<uint64_t>(&tmap_b)), "r"(fb), "r"(0), "r"(k0), "r"(n0 >> 6),
+                    "r"(b_item)
+                    : "memory");
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tma_load_3d(sb + j * (BK * 128), &tmap_b, fb, n0 + 64 * j, k0, b_item);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (*abort_flag) {
+            for (int i = 0; i < STAGES; ++i)
+                if ((armed_bits >> i) & 1u) mbar_wait_drain(&s->full[i], (parity_bits >> i) & 1u);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer: A K-major (128-byte swizzle, 32 bytes per 16-deep
+        // step), B MN-major (64-column blocks 8 KiB apart, 16 K-rows of 128
+        // bytes per step); descriptors advanced by adds
+        const uint32_t idesc = instr_desc(p.is_bf16, BM, BN, 0, 1);
+        const uint32_t stage0 = smem_u32(base);
+        const uint64_t a_desc0 = smem_desc(stage0, 16, 1024, 2u);
+        const uint64_t b_desc0 = smem_desc(stage0 + A_BYTES, BK * 128, 1024, 2u);
+        uint32_t stage = 0, phase = 0, first = 0u;
+        bool ok = true;
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                mma_f16(tmem_base, a_desc0 + so + kk * 2, b_desc0 + so + kk * 128, idesc, kk > 0 ? 1u : first);
+            first = 1u;
+            mma_commit(&s->empty[stage]);
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        (void)ok;
+        mma_commit(&s->acc_full);      // every MMA issued above has completed once it flips
+    } else if (warp >= 2) {
+        // ---- accumulator -> this CTA's float32 partial tile (all 128 rows;
+        // the rows past M are never read back)
+        const int lane_group = warp & 3;
+        const int row_in_tile = lane_group * 32 + lane;
+        if (mbar_wait(&s->acc_full, 0, abort_flag, p.err)) {
+            tc_fence_after();
+            const uint32_t t_base = tmem_base + ((uint32_t)(lane_group * 32) << 16);
+            float4* prow = reinterpret_cast<float4*>(part + row_in_tile * PART_PITCH);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + c, r);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    prow[c / 4 + q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                  __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    pair::cluster_sync();              // every CTA's partial tile is written
+
+    // ---- this CTA's share of the tile: a contiguous band of its 8-column
+    // runs (runs [rank * runs / ways, (rank + 1) * runs / ways)) over the
+    // valid rows, summed over the slices in slice order.  The threads of a
+    // 16-byte load phase read 2 rows x 4 runs: distinct banks
+    {
+        const int64_t rows_valid = min64(BM, p.M - mb * BM);
+        const int64_t cols_valid = min64(BN, p.N - nb * BN);
+        const int runs = (int)ceil_div(cols_valid, 8);
+        const int run0 = rank * runs / ways, run1 = (rank + 1) * runs / ways;
+        const int my_runs = run1 - run0;
+        const int64_t items = my_runs > 0 ? rows_valid * my_runs : 0;
+        for (int64_t e = threadIdx.x; e < items; e += THREADS_CS) {
+            const int row = (int)(e / my_runs);
+            const int run = run0 + (int)(e % my_runs);
+            const float* src = part + row * PART_PITCH + run * 8;
+            float4 x0[MAX_WAYS], x1[MAX_WAYS];
+#pragma unroll
+            for (int j = 0; j < MAX_WAYS; ++j) {
+                if (j < ways) {
+                    x0[j] = tiny::ld_cluster4(pair::map_to(src, j));
+                    x1[j] = tiny::ld_cluster4(pair::map_to(src + 4, j));
+                }
+            }
+            float4 a0 = x0[0], a1 = x1[0];
+#pragma unroll
+            for (int j = 1; j < MAX_WAYS; ++j) {
+                if (j < ways) {
+                    a0.x += x0[j].x; a0.y += x0[j].y; a0.z += x0[j].z; a0.w += x0[j].w;
+                    a1.x += x1[j].x; a1.y += x1[j].y; a1.z += x1[j].z; a1.w += x1[j].w;
+                }
+            }
+            const int64_t grow = mb * BM + row;
+            const int64_t gcol = nb * BN + run * 8;
+            unsigned char* dst = static_cast<unsigned char*>(p.Y) + ((item * p.M + grow) * p.N + gcol) * 2;
+            const uint32_t r8[8] = {__float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a0.z),
+                                    __float_as_uint(a0.w), __float_as_uint(a1.x), __float_as_uint(a1.y),
+                                    __float_as_uint(a1.z), __float_as_uint(a1.w)};
+            uint32_t packed[4];
+            epi_run<4>(p, r8, grow, gcol, dst, 1, packed);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+    pair::cluster_sync();              // no CTA leaves while its partial may still be read
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace csplit
+
+// ---------------------------------------------------------------------------
 // host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1781,16 +1990,17 @@ static bool encode_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t 
 }
 
 // rank-4 view of a row-major [items][K][N] 16-bit B (rows `ld` elements
-// apart, N a multiple of 64) as [items][N / 64][K][64]: a box {64, BK, 2, 1}
-// is two 64-column MN-major blocks of BK rows, one after the other in shared
-// memory (the layout of two 3-D boxes at n0 and n0 + 64), in one TMA load
+// apart, N a multiple of 64) as [items][N / 64][K][64]: a box {64, BK,
+// blocks, 1} is `blocks` 64-column MN-major blocks of BK rows, one after the
+// other in shared memory (the layout of 3-D boxes at n0, n0 + 64, ...), in
+// one TMA load
 static bool encode_b_blocks(CUtensorMap* map, const void* base, int is_bf16, uint64_t n, uint64_t k,
-                            uint64_t items, uint64_t ld) {
+                            uint64_t items, uint64_t ld, uint32_t blocks = 2) {
     auto fn = encode_fn();
     if (!fn || n % 64 != 0) return false;
     cuuint64_t dims[4] = {64, k, n / 64, items};
     cuuint64_t strides[3] = {ld * 2, 128, ld * k * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)BK, 2, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)BK, blocks, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     4, const_cast<void*>(base), dims, strides, box, estr,
@@ -2297,6 +2507,130 @@ static double operand_bytes(const Problem& pr) {
     return 2.0 * (double)(pr.M * pr.K + pr.K * pr.N) * (double)pr.items;
 }
 
+// Cluster split-K for general products with few 128 x 256 tiles: K slices
+// per tile (one CTA each, clusters of `ways`), 0 when the tiles already
+// fill half the SMs or K is too short to split (at least 2 K blocks per
+// slice, at most 8 slices); no slice is left empty.
+// clusters of `ways` CTAs of the cluster split-K kernel that fit on the GPU
+// at once (one CTA per SM; a cluster takes its SMs from one GPC, so fewer
+// fit than the SM count suggests); queried once per size and device
+static int csplit_max_clusters(int ways, int sm_count) {
+    static std::mutex mu;
+    static int cached[64][csplit::MAX_WAYS + 1];
+    static bool done[64][csplit::MAX_WAYS + 1];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return sm_count / ways / 2;                 // no device: a conservative guess
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev][ways]) {
+        int n = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ways, 1, 1);
+        cfg.blockDim = dim3(csplit::THREADS_CS, 1, 1);
+        cfg.dynamicSmemBytes = csplit::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)ways;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (set_smem_limit(reinterpret_cast<const void*>(csplit::csplit_kernel), csplit::SMEM_BYTES) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, csplit::csplit_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = sm_count / ways / 2;
+        }
+        cached[dev][ways] = n;
+        done[dev][ways] = true;
+    }
+    return cached[dev][ways];
+}
+
+// K slices per tile: the most (at most 8, at least 2 K blocks each, no
+// slice empty) whose tiles x slices CTAs fit the SMs and whose clusters all
+// run in one wave
+static int csplit_ways(olc_dtype dt, const Problem& pr, int sm_count) {
+    if (!(dt == OLC_FLOAT16 || dt == OLC_BFLOAT16) || pr.a_trans || pr.b_trans || pr.a_ld || pr.b_ld ||
+        pr.y_unaligned || !tc_shape_ok(dt, pr.N, pr.K) || pr.M >= (1LL << 31))
+        return 0;
+    const int64_t tiles = ceil_div(pr.M, BM) * ceil_div(pr.N, csplit::BN) * pr.items;
+    const int64_t kbs = ceil_div(pr.K, BK);
+    if (tiles <= 0 || 2 * tiles > (int64_t)sm_count) return 0;
+    const int64_t wmax = min64(min64((int64_t)sm_count / tiles, (int64_t)csplit::MAX_WAYS), kbs / 2);
+    for (int64_t w = wmax; w >= 2; --w) {
+        const int64_t ways = ceil_div(kbs, ceil_div(kbs, w));     // no empty slice
+        if (ways < 2) break;
+        if (tiles <= csplit_max_clusters((int)ways, sm_count)) return (int)ways;
+    }
+    return 0;
+}
+
+static cudaError_t launch_csplit(olc_dtype dt, const Problem& pr, int ways, cudaStream_t s) {
+    int64_t a_items = 1, b_items = 1;
+    for (int d = 0; d < pr.map.rank; ++d) {
+        if (pr.map.a_stride[d])
+            a_items = max64(a_items, pr.map.a_stride[d] / (pr.M * pr.K) * pr.map.dims[d]);
+        if (pr.map.b_stride[d])
+            b_items = max64(b_items, pr.map.b_stride[d] / (pr.K * pr.N) * pr.map.dims[d]);
+    }
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof ma);
+    std::memset(&mb, 0, sizeof mb);
+    const int bf = dt == OLC_BFLOAT16;
+    // A with fewer rows than one tile: only its rows are loaded (rounded up
+    // to a whole 8-row swizzle group); the stage's other rows feed only
+    // output rows that are never stored
+    const uint32_t a_box_rows = pr.M < BM ? (uint32_t)ceil_div(pr.M, 8) * 8 : BM;
+    if (!encode_3d(&ma, pr.A, bf, pr.K, pr.M, a_items, BK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const bool b_blocks = pr.N % 64 == 0 && encode_b_blocks(&mb, pr.B, bf, pr.N, pr.K, b_items, pr.N, 4);
+    if (!b_blocks && !encode_3d(&mb, pr.B, bf, pr.N, pr.K, b_items, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.M = pr.M;
+    p.N = pr.N;
+    p.K = pr.K;
+    p.items = pr.items;
+    p.tiles_m = ceil_div(pr.M, BM);
+    p.tiles_n = ceil_div(pr.N, csplit::BN);
+    p.tiles_per_item = p.tiles_m * p.tiles_n;
+    p.total_tiles = p.tiles_per_item * pr.items;
+    p.k_blocks = ceil_div(pr.K, BK);
+    p.a_item_elems = pr.M * pr.K;
+    p.b_item_elems = pr.K * pr.N;
+    p.map = pr.map;
+    p.b_blocks = b_blocks ? 1 : 0;
+    p.Y = pr.Y;
+    p.err = device_error_word();
+    p.is_bf16 = bf;
+    p.stage_tx_bytes = a_box_rows * BK * 2 + csplit::B_BYTES;
+    p.epi = pr.epi;
+    if (p.total_tiles <= 0) return cudaSuccess;
+    const int64_t kb_per = ceil_div(p.k_blocks, (int64_t)ways);
+    if (ceil_div(p.k_blocks, kb_per) != ways || p.total_tiles * ways > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(csplit::csplit_kernel), csplit::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.total_tiles * ways), 1, 1);
+    cfg.blockDim = dim3(csplit::THREADS_CS, 1, 1);
+    cfg.dynamicSmemBytes = csplit::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ways;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, csplit::csplit_kernel, ma, mb, p, ways, kb_per);
+}
+
 }  // namespace tc
 
 // Row-pitch staging copy for operands the TMA cannot read in place: each
@@ -2357,11 +2691,22 @@ cudaError_t launch_pair_f8(olc_dtype dt, const Problem& pr, const void* bt, int 
     return tc::launch_pair_f8_impl(dt, pr, bt, sm_count, s);
 }
 
+int tc_general_csplit_ways(olc_dtype dt, const Problem& p, int sm_count) {
+    return tc::csplit_ways(dt, p, sm_count);
+}
+
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
                               int variant) {
     // variant 2: CTA pairs with 256 x 256 tiles; 1: one CTA per 128 x 256
     // tile; 0 (automatic): pairs when the product holds a full pair tile
-    const bool pair = variant == 2 || (variant == 0 && pr.M >= 256 && pr.N >= 256);
+    if (variant == 0) {
+        const int ways = pr.tc_ways == 0 ? tc::csplit_ways(dt, pr, sm_count) : (pr.tc_ways >= 2 ? pr.tc_ways : 0);
+        if (ways >= 2) return tc::launch_csplit(dt, pr, ways, s);
+    }
+    // CTA pairs once a product has more rows than one 128-row tile (a pair
+    // tile's spare rows cost less than a second row of 1-CTA tiles: BF16
+    // [255, 4096] x [4096, 4096] 23.0 against 28.7 us)
+    const bool pair = variant == 2 || (variant == 0 && pr.M > 128 && pr.N >= 256);
     if (pair && sm_count >= 2) return tc::launch_pair(dt, pr, sm_count, s);
     return tc::launch_tc<256, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
 }

@@ -69,6 +69,7 @@ KERNEL_CASES = [
     ((300, 520), (520, 264), ["bfloat16", "float16"], "general_tc", 2),       # CTA pairs
     ((1024, 2048), (2048, 1024), ["bfloat16"], "general_tc", 2),
     ((300, 200), (200, 320), ["bfloat16", "float16"], "general_tc", 2),   # 4-D B loads, blocks past N
+    ((100, 2048), (2048, 520), ["bfloat16", "float16"], "general_tc", None),  # cluster split-K
 ]
 CASES = [(a, b, dt, al, v) for a, b, dts, al, v in KERNEL_CASES for dt in dts]
 

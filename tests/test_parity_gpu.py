@@ -588,3 +588,44 @@ def test_plan_reuse_across_streams_and_inputs():
             s.synchronize()
             y_ref, sm = oracle.matmul(a.numpy(), b.numpy(), "float32")
             compare(Y.cpu(), y_ref, sm, "float32")
+
+
+# --------------------------------------------------------------------------
+# cluster split-K: general FP16/BF16 products whose 128 x 256 tiles fill at
+# most half the SMs run each tile's K slices on the CTAs of a cluster and sum
+# them through distributed shared memory
+
+CSPLIT_SHAPES = [
+    ((17, 4096), (4096, 1024)),          # few rows, B in 4-D loads, 8 slices
+    ((100, 2056), (2056, 264)),          # N not a multiple of 64: 3-D loads, a partial last run
+    ((129, 4104), (4104, 520)),          # two row tiles, K tail
+    ((300, 1024), (1024, 320)),          # three row tiles, blocks past N
+    ((2, 3, 40, 512), (3, 512, 256)),    # broadcast batch through the 3-D / 4-D maps
+]
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("shapes", CSPLIT_SHAPES, ids=lambda s: "x".join(map(str, s[0] + s[1])))
+def test_cluster_split_k_shapes(dtype, shapes):
+    a_shape, b_shape = shapes
+    a, b = synth.operands(a_shape, b_shape, dtype, synth.normal(1.0), synth.normal(0.02), seed=61)
+    check_product(a, b, dtype, algorithm="general_tc")
+    ai, bi = synth.operands(a_shape, b_shape, dtype, synth.SMALL_INT, synth.SMALL_INT, seed=61)
+    check_product(ai, bi, dtype, algorithm="general_tc", exact=True)
+
+
+def test_cluster_split_k_is_reproducible():
+    """The slices are summed in slice order, whatever order the CTAs finish
+    in: repeated executes give the same bits."""
+    a, b = synth.operands((64, 8192), (8192, 512), "bfloat16", synth.normal(1.0), synth.normal(0.02), 62)
+    A, B = a.cuda(), b.cuda()
+    with Plan(a.shape, b.shape, "bfloat16") as p:
+        p.force("general_tc")
+        ys = []
+        for _ in range(3):
+            Y = torch.empty(p.output_shape, dtype=A.dtype, device="cuda")
+            p.execute(A, B, Y)
+            ys.append(Y)
+        torch.cuda.synchronize()
+        for y in ys[1:]:
+            assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
