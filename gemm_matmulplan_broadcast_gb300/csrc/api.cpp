@@ -446,6 +446,9 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
         p->counter_count = skinny_n_counter_count(dt, pr, p->sm_count);
     } else if (p->algo == OLC_ALGO_GENERAL_TC && is_fp8(dt)) {
         p->partial_bytes = fp8_tc_workspace_bytes(pr);    // B transposed, [N, K] bytes
+    } else if (p->algo == OLC_ALGO_GENERAL_TC && is_half(dt) && p->tc_variant == 0) {
+        // few tiles: the cluster split-K's float32 partial tiles
+        p->partial_bytes = tc_general_partial_bytes(dt, pr, p->sm_count);
     } else if (p->algo == OLC_ALGO_GENERAL_SIMT) {
         p->splits = general_simt_pick_split(dt, pr, p->sm_count);
         if (p->splits > 1) {
@@ -699,7 +702,11 @@ cudaError_t launch_route(const olc_matmul_plan* p, const Problem& pr, olc_dtype 
         case OLC_ALGO_SPLIT_K:
             e = launch_split_k(dt, pr, p->splits, p->sm_count, workspace_of(p), s);
             break;
-        case OLC_ALGO_GENERAL_TC: e = launch_general_tc(dt, pr, p->sm_count, s, p->tc_variant); break;
+        case OLC_ALGO_GENERAL_TC: {
+            const Workspace ws = workspace_of(p);
+            e = launch_general_tc(dt, pr, p->sm_count, s, p->tc_variant, &ws);
+            break;
+        }
         default: return cudaErrorInvalidValue;
     }
     return e;

@@ -186,9 +186,13 @@ int tc_general_csplit_ways(olc_dtype dt, const Problem& p, int sm_count);
 cudaError_t launch_pad_rows16(const void* src, void* dst, int64_t rows, int64_t cols,
                               int64_t pitch, cudaStream_t stream);
 // variant: 0 automatic, 1 one CTA per 128 x 256 tile, 2 CTA pairs (cta_group::2)
-// with 256 x 256 tiles
+// with 256 x 256 tiles.  `ws` (may be null) holds the cluster split-K's
+// partial tiles (tc_general_partial_bytes); without it those products run
+// the plain tiles.
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& p, int sm_count, cudaStream_t stream,
-                              int variant);
+                              int variant, const Workspace* ws);
+// workspace of the cluster split-K for this problem (0: it does not apply)
+size_t tc_general_partial_bytes(olc_dtype dt, const Problem& p, int sm_count);
 // the same kernel with 16-column tiles (N <= 16): the tensor-core skinny-N,
 // in stream-K shares when the row tiles alone leave SMs idle
 size_t tc_skinny_n_partial_bytes(const Problem& p, int sm_count);

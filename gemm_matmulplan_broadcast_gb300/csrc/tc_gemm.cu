@@ -1900,29 +1900,37 @@ csplit_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    pair::cluster_sync();              // every CTA's partial tile is written
+    // the valid rows of the partial tile to the plan's workspace (rows of
+    // 256 floats; consecutive threads write consecutive 16-byte groups)
+    const int64_t rows_valid = min64(BM, p.M - mb * BM);
+    float* mine = p.part1 + (tile * ways + rank) * (int64_t)(BM * BN);
+    for (int64_t e = threadIdx.x; e < rows_valid * (BN / 4); e += THREADS_CS) {
+        const int row = (int)(e / (BN / 4)), c4 = (int)(e % (BN / 4));
+        reinterpret_cast<float4*>(mine + (int64_t)row * BN)[c4] =
+            reinterpret_cast<const float4*>(part + row * PART_PITCH)[c4];
+    }
+    pair::cluster_sync();              // every CTA's partial tile is in the workspace (cluster scope)
 
     // ---- this CTA's share of the tile: a contiguous band of its 8-column
     // runs (runs [rank * runs / ways, (rank + 1) * runs / ways)) over the
-    // valid rows, summed over the slices in slice order.  The threads of a
-    // 16-byte load phase read 2 rows x 4 runs: distinct banks
+    // valid rows, summed over the slices in slice order from L2
     {
-        const int64_t rows_valid = min64(BM, p.M - mb * BM);
         const int64_t cols_valid = min64(BN, p.N - nb * BN);
         const int runs = (int)ceil_div(cols_valid, 8);
         const int run0 = rank * runs / ways, run1 = (rank + 1) * runs / ways;
         const int my_runs = run1 - run0;
         const int64_t items = my_runs > 0 ? rows_valid * my_runs : 0;
+        const float* first = p.part1 + tile * ways * (int64_t)(BM * BN);
         for (int64_t e = threadIdx.x; e < items; e += THREADS_CS) {
             const int row = (int)(e / my_runs);
             const int run = run0 + (int)(e % my_runs);
-            const float* src = part + row * PART_PITCH + run * 8;
+            const float* src = first + (int64_t)row * BN + run * 8;
             float4 x0[MAX_WAYS], x1[MAX_WAYS];
 #pragma unroll
             for (int j = 0; j < MAX_WAYS; ++j) {
                 if (j < ways) {
-                    x0[j] = tiny::ld_cluster4(pair::map_to(src, j));
-                    x1[j] = tiny::ld_cluster4(pair::map_to(src + 4, j));
+                    x0[j] = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)j * BM * BN));
+                    x1[j] = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)j * BM * BN + 4));
                 }
             }
             float4 a0 = x0[0], a1 = x1[0];
@@ -1944,7 +1952,6 @@ csplit_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
             *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
     }
-    pair::cluster_sync();              // no CTA leaves while its partial may still be read
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -2562,12 +2569,18 @@ static int csplit_ways(olc_dtype dt, const Problem& pr, int sm_count) {
     for (int64_t w = wmax; w >= 2; --w) {
         const int64_t ways = ceil_div(kbs, ceil_div(kbs, w));     // no empty slice
         if (ways < 2) break;
-        if (tiles <= csplit_max_clusters((int)ways, sm_count)) return (int)ways;
+        if (tiles > csplit_max_clusters((int)ways, sm_count)) continue;
+        // two slices double the streaming CTAs but add the partial tiles'
+        // traffic to an already HBM-bound B stream: worth it only for few
+        // rows (BF16 [128, 4096] x [4096, 14336]: 31.6 us against 28.1 on
+        // CTA pairs; [17, ...]: 23.5 against 26.7)
+        if (ways == 2 && pr.M > 64) return 0;
+        return (int)ways;
     }
     return 0;
 }
 
-static cudaError_t launch_csplit(olc_dtype dt, const Problem& pr, int ways, cudaStream_t s) {
+static cudaError_t launch_csplit(olc_dtype dt, const Problem& pr, int ways, float* partials, cudaStream_t s) {
     int64_t a_items = 1, b_items = 1;
     for (int d = 0; d < pr.map.rank; ++d) {
         if (pr.map.a_stride[d])
@@ -2608,6 +2621,7 @@ static cudaError_t launch_csplit(olc_dtype dt, const Problem& pr, int ways, cuda
     p.is_bf16 = bf;
     p.stage_tx_bytes = a_box_rows * BK * 2 + csplit::B_BYTES;
     p.epi = pr.epi;
+    p.part1 = partials;
     if (p.total_tiles <= 0) return cudaSuccess;
     const int64_t kb_per = ceil_div(p.k_blocks, (int64_t)ways);
     if (ceil_div(p.k_blocks, kb_per) != ways || p.total_tiles * ways > 0x7fffffffLL)
@@ -2695,18 +2709,29 @@ int tc_general_csplit_ways(olc_dtype dt, const Problem& p, int sm_count) {
     return tc::csplit_ways(dt, p, sm_count);
 }
 
+size_t tc_general_partial_bytes(olc_dtype dt, const Problem& p, int sm_count) {
+    const int ways = tc::csplit_ways(dt, p, sm_count);
+    if (ways < 2) return 0;
+    const int64_t tiles = ceil_div(p.M, tc::BM) * ceil_div(p.N, tc::csplit::BN) * p.items;
+    return (size_t)(tiles * ways) * tc::BM * tc::csplit::BN * sizeof(float);
+}
+
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
-                              int variant) {
+                              int variant, const Workspace* ws) {
     // variant 2: CTA pairs with 256 x 256 tiles; 1: one CTA per 128 x 256
     // tile; 0 (automatic): pairs when the product holds a full pair tile
     if (variant == 0) {
         const int ways = pr.tc_ways == 0 ? tc::csplit_ways(dt, pr, sm_count) : (pr.tc_ways >= 2 ? pr.tc_ways : 0);
-        if (ways >= 2) return tc::launch_csplit(dt, pr, ways, s);
+        const int64_t tiles = ceil_div(pr.M, tc::BM) * ceil_div(pr.N, tc::csplit::BN) * pr.items;
+        const size_t need = (size_t)(tiles * (ways > 0 ? ways : 0)) * tc::BM * tc::csplit::BN * sizeof(float);
+        if (ways >= 2 && ws && ws->partials && ws->partial_bytes >= need)
+            return tc::launch_csplit(dt, pr, ways, static_cast<float*>(ws->partials), s);
     }
-    // CTA pairs once a product has more rows than one 128-row tile (a pair
-    // tile's spare rows cost less than a second row of 1-CTA tiles: BF16
-    // [255, 4096] x [4096, 4096] 23.0 against 28.7 us)
-    const bool pair = variant == 2 || (variant == 0 && pr.M > 128 && pr.N >= 256);
+    // CTA pairs whenever N holds a pair tile: the spare rows of a 256-row
+    // pair tile cost less than leaving half the SMs of a 128-row band idle
+    // (BF16 x [4096, 14336], us, pairs / one CTA per 128 x 256 tile: 17
+    // rows 26.8 / 30.3, 128 rows 27.9 / 32.9, 255 rows 28.8 / 33.7)
+    const bool pair = variant == 2 || (variant == 0 && pr.N >= 256);
     if (pair && sm_count >= 2) return tc::launch_pair(dt, pr, sm_count, s);
     return tc::launch_tc<256, false, false>(dt, pr, sm_count, s, nullptr, nullptr);
 }
