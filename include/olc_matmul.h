@@ -450,9 +450,14 @@ olc_status olc_matmul_plan_set_splits(olc_matmul_plan* plan, int splits);
 /* K slices the plan currently uses (1 when it does not split). */
 int olc_matmul_plan_splits(const olc_matmul_plan* plan);
 
-/* Tuning override of the kernel family.  GENERAL_TC plans: 0 = automatic,
- * 1 = one CTA per 128 x 256 output tile, 2 = pairs of CTAs on one TPC
- * sharing a 256 x 256 tile (tcgen05 cta_group::2).  SKINNY_N plans of
+/* Tuning override of the kernel family.  GENERAL_TC plans: 0 = automatic
+ * (FLOAT16 / BFLOAT16: when the 128 x 256 tiles would fill at most half the
+ * SMs, the cluster split-K -- the K blocks of each tile cut into slices run
+ * by the CTAs of one thread-block cluster, whose float32 partial tiles meet
+ * in the plan's workspace and are summed in slice order, so the result does
+ * not depend on timing; otherwise CTA pairs whenever N >= 256), 1 = one CTA
+ * per 128 x 256 output tile, 2 = pairs of CTAs on one TPC sharing a 256 x
+ * 256 tile (tcgen05 cta_group::2).  SKINNY_N plans of
  * FLOAT16 / BFLOAT16: 0 = automatic, 1 = the tcgen05 16-column kernel,
  * 2 = the register-streaming mma.sync kernel wherever it applies (one B for
  * all rows, K a multiple of 8, B^T within its shared-memory budget).
@@ -467,7 +472,8 @@ int olc_matmul_plan_splits(const olc_matmul_plan* plan);
  * constant B; one item, N and K multiples of 16, else the warp-level MMA
  * kernel).  GENERAL_TC
  * plans of 8-bit floats: 1 = one CTA per 128 x 256 tile instead of CTA pairs.
- * Results are identical within the parity tolerance either way.  Errors:
+ * Results are identical within the parity tolerance either way (the
+ * variants sum K in different orders only where one splits it).  Errors:
  * OLC_ERR_NULL, OLC_ERR_INVALID. */
 olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant);
 
@@ -478,8 +484,10 @@ olc_status olc_matmul_plan_set_tc_variant(olc_matmul_plan* plan, int variant);
  * the B transpose of 8-bit tensor-core plans without a constant B. */
 int olc_matmul_plan_launches(const olc_matmul_plan* plan);
 
-/* Bytes of device workspace the plan owns for split reductions (and the
- * FP8 B transpose), 0 if none; staging buffers are not included. */
+/* Bytes of device workspace the plan owns for split reductions (SPLIT_K,
+ * SKINNY_M and SKINNY_N slices, the FLOAT register tiles' K slices, the
+ * general FP16 / BF16 tiles' cluster split-K) and the FP8 B transpose, 0 if
+ * none; staging buffers are not included. */
 size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan);
 
 /* One-line description of the plan (algorithm, tile, grid, splits) written
