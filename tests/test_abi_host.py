@@ -400,3 +400,26 @@ def test_route_for_misaligned_pointers_and_odd_rows():
         assert lib.olc_matmul_plan_algorithm_for(h, al, al, al, None) == 3
         assert lib.olc_matmul_plan_algorithm_for(h, al + 4, al, al, None) == 2   # vector loads: DIRECT
     assert lib.olc_matmul_plan_algorithm_for(None, al, al, al, None) == -1
+
+
+def test_few_tile_half_products_take_the_cluster_split_k():
+    """FLOAT16 / BFLOAT16 products whose 128 x 256 tiles fill at most half the
+    SMs stay on the general tiles, which then own a workspace of whole
+    128 x 256 float32 partial tiles (tiles x K slices); the tiny-output
+    corner (at most 32 x 32) and other types keep SPLIT_K, and products with
+    many tiles own no workspace."""
+    tile_bytes = 128 * 256 * 4
+    for dt in ("bfloat16", "float16"):
+        with Plan((64, 8192), (8192, 512), dt) as p:
+            assert p.algorithm == "general_tc"
+            ws = p.workspace_bytes
+            assert ws > 0 and ws % (2 * tile_bytes) == 0 and 2 * 2 <= ws // tile_bytes <= 2 * 8
+        with Plan((32, 131072), (131072, 32), dt) as p:
+            assert p.algorithm == "split_k"
+        with Plan((8, 2048, 4096), (4096, 14336), dt) as p:
+            assert p.algorithm == "general_tc" and p.workspace_bytes == 0
+    with Plan((64, 8192), (8192, 512), "float32") as p:
+        assert p.algorithm == "split_k"
+    with Plan((64, 8192), (8192, 512), "bfloat16") as p:
+        p.set_tc_variant(2)                  # forced pairs: no split, no workspace
+        assert p.workspace_bytes == 0
