@@ -724,6 +724,37 @@ def measure_split_k_static(device, l2):
     return out
 
 
+def measure_few_tiles(device, peaks):
+    """BF16 products whose 128 x 256 tiles would leave most SMs idle, which
+    the general tensor-core path runs as a cluster split-K: [17 | 128, 4096]
+    x [4096, 4096] and the long-K small output [64, 8192] x [8192, 512].
+    CUDA graphs of back-to-back launches over B copies that exceed L2
+    together; the rate is HBM bytes (A + B + Y once) per second against the
+    measured copy rate, the bound of these B-streaming products."""
+    import torch
+    from gemm_matmulplan_broadcast_gb300 import Plan
+    stream = torch.cuda.Stream()
+    out = []
+    g = torch.Generator(device="cpu").manual_seed(3)
+    for (m, k, n) in ((17, 4096, 4096), (128, 4096, 4096), (64, 8192, 512)):
+        nb = max(2, (300 << 20) // (k * n * 2))
+        Bs = [(torch.randn(k, n, generator=g) * 0.02).to(torch.bfloat16).to(device) for _ in range(nb)]
+        A = torch.randn(m, k, generator=g).to(torch.bfloat16).to(device)
+        Y = torch.empty(m, n, dtype=torch.bfloat16, device=device)
+        p = Plan((m, k), (k, n), "bfloat16")
+        ms = statistics.median(graph_time(lambda i: p.execute(A, Bs[i % nb], Y, stream=stream), nb, stream,
+                                          reps=5, launches=2 * nb))
+        byts = (m * k + k * n + m * n) * 2
+        out.append({"product": "%dx%dx%d" % (m, k, n), "algorithm": p.algorithm,
+                    "workspace_bytes": p.workspace_bytes, "ms_per_launch": ms,
+                    "gbs": byts / (ms * 1e-3) / 1e9,
+                    "frac": byts / (ms * 1e-3) / 1e9 / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])})
+        p.close()
+        del Bs, A, Y
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_unaligned(device, peaks, l2):
     """FLOAT16 / BFLOAT16 products the TMA cannot read in place, on the
     tensor cores: the output projection [16384, 4096] x [4096, 50257] BF16
@@ -898,6 +929,11 @@ def compact_summary(breakdown, secondary):
         for r in secondary["unaligned_tc"]:
             out["unaligned_tc"][r["product"].replace("vocab_50257_", "vocab_")] = [
                 _short(r["ms_per_launch"] * 1e3), _short(r["tflops"]), _short(r["frac"])]
+    if "few_tiles_bf16" in secondary:
+        out["few_tiles_bf16"] = {"unit": "GB/s"}
+        for r in secondary["few_tiles_bf16"]:
+            out["few_tiles_bf16"][r["product"]] = [_short(r["ms_per_launch"] * 1e3), _short(r["gbs"]),
+                                                  _short(r["frac"])]
     if "alu_rates" in secondary:
         out["alu_tflops"] = [_short(v["tflops"]) for v in secondary["alu_rates"].values()]
     return out
@@ -973,6 +1009,7 @@ def run_ours(args):
         secondary["split_k_curve"] = measure_split_k_curve(device, peaks, l2)
         secondary["split_k_static"] = measure_split_k_static(device, l2)
         secondary["unaligned_tc"] = measure_unaligned(device, peaks, l2)
+        secondary["few_tiles_bf16"] = measure_few_tiles(device, peaks)
         secondary["fp8_rows_constant_b"] = measure_fp8_decode_constant_b(device, peaks)
         secondary["fused_epilogue"] = measure_fused(device, peaks, l2)
         secondary["grouped_small_products"] = measure_grouped(device, peaks)
