@@ -1747,13 +1747,13 @@ splitk_tiny_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // most SMs idle (a few hundred rows, or a narrow N): the K blocks of each
 // tile are cut into `ways` slices, one per CTA of a thread-block cluster.
 // Each CTA streams its slice of A and B through a 4-stage TMA ring into a
-// 128 x 256 TMEM accumulator, moves the accumulator into a float32 partial
-// tile in its own shared memory (the ring, idle by then), and after a
-// cluster barrier sums its share of the tile's 8-column runs over the
-// cluster's partials through distributed shared memory, in slice order (so
-// the result does not depend on timing), runs the epilogue and stores.  No
-// global workspace, no atomics; a second cluster barrier keeps every CTA's
-// shared memory alive until the others have read it.
+// 128 x 256 TMEM accumulator, stages the accumulator as a float32 partial
+// tile in its own shared memory (the ring, idle by then) and copies its
+// valid rows, in coalesced 16-byte groups, to its slot of a plan-owned
+// workspace (L2-resident).  After one cluster barrier each CTA sums a
+// contiguous band of the tile's 8-column runs over the cluster's partials,
+// read from L2 in slice order (so the result does not depend on timing),
+// runs the epilogue and stores.  No atomics.
 
 namespace csplit {
 
@@ -2514,11 +2514,7 @@ static double operand_bytes(const Problem& pr) {
     return 2.0 * (double)(pr.M * pr.K + pr.K * pr.N) * (double)pr.items;
 }
 
-// Cluster split-K for general products with few 128 x 256 tiles: K slices
-// per tile (one CTA each, clusters of `ways`), 0 when the tiles already
-// fill half the SMs or K is too short to split (at least 2 K blocks per
-// slice, at most 8 slices); no slice is left empty.
-// clusters of `ways` CTAs of the cluster split-K kernel that fit on the GPU
+// Clusters of `ways` CTAs of the cluster split-K kernel that fit on the GPU
 // at once (one CTA per SM; a cluster takes its SMs from one GPC, so fewer
 // fit than the SM count suggests); queried once per size and device
 static int csplit_max_clusters(int ways, int sm_count) {
