@@ -392,10 +392,10 @@ int choose_algorithm(const olc_matmul_plan* p) {
     const int64_t tiles = ((rows + 127) / 128) * ((N + 127) / 128) * items;
     if (tiles * 2 <= p->sm_count && K >= 8 * 1024 && feasible(p, OLC_ALGO_SPLIT_K)) {
         // FLOAT16 / BFLOAT16 outputs above 32 x 32 whose general tiles take
-        // the cluster split-K (slices summed through distributed shared
-        // memory) stay there: faster than the global two-level reduction
-        // (BF16 [64, 8192] x [8192, 512]: 14.9 against 38.8 us; [128, 16384]
-        // x [16384, 1024]: 24.9 against 71.8 us)
+        // the cluster split-K (slices summed from L2 in slice order within
+        // one cluster) stay there: faster than the global two-level
+        // reduction (BF16 [64, 8192] x [8192, 512]: 12.2 against 38.4 us;
+        // [128, 16384] x [16384, 1024]: 20.1 against 71.8 us)
         const bool tiny_out = rows <= 32 && N <= 32 && items == 1;
         if (!(is_half(p->dtype) && !tiny_out && feasible(p, OLC_ALGO_GENERAL_TC) &&
               tc_general_csplit_ways(p->dtype, make_problem(p, nullptr, nullptr, nullptr), p->sm_count) >= 2))

@@ -975,11 +975,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // m0 + 128 r .. +127 and B columns n0 + 128 r .. +127 in its own shared
 // memory, the leader (rank 0) issues the MMAs that read both CTAs' halves,
 // and each CTA's TMEM receives its own 128 rows x 256 columns.  Per SM that
-// is 32 KB of operands per 64-deep K block instead of 48 KB, so 7 stages fit
-// where the 1-CTA kernel has 4.
+// is 32 KB of operands per 64-deep K block instead of 48 KB, so 6 stages and
+// an epilogue staging area fit where the 1-CTA kernel has 4 stages.
 //
 // Synchronisation: both CTAs' TMA loads complete on the leader's full[s]
-// barrier (armed once by the leader with both CTAs' bytes); the leader's MMA
+// barrier (two arrivals: the leader's A loader and B loader each arm it with
+// both CTAs' bytes of their operand); the leader's MMA
 // commits multicast to empty[s] and acc_full[b] in both CTAs; both CTAs'
 // epilogue warps arrive on the leader's acc_empty[b] (8 arrivals).  Both
 // CTAs allocate and free TMEM with .cta_group::2, and meet at a cluster
@@ -2715,7 +2716,8 @@ size_t tc_general_partial_bytes(olc_dtype dt, const Problem& p, int sm_count) {
 cudaError_t launch_general_tc(olc_dtype dt, const Problem& pr, int sm_count, cudaStream_t s,
                               int variant, const Workspace* ws) {
     // variant 2: CTA pairs with 256 x 256 tiles; 1: one CTA per 128 x 256
-    // tile; 0 (automatic): pairs when the product holds a full pair tile
+    // tile; 0 (automatic): the cluster split-K when its slices apply and the
+    // workspace holds their partial tiles, else pairs when N >= 256
     if (variant == 0) {
         const int ways = pr.tc_ways == 0 ? tc::csplit_ways(dt, pr, sm_count) : (pr.tc_ways >= 2 ? pr.tc_ways : 0);
         const int64_t tiles = ceil_div(pr.M, tc::BM) * ceil_div(pr.N, tc::csplit::BN) * pr.items;
