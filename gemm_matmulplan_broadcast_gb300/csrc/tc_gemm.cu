@@ -1865,9 +1865,8 @@ csplit_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
         const uint64_t a_desc0 = smem_desc(stage0, 16, 1024, 2u);
         const uint64_t b_desc0 = smem_desc(stage0 + A_BYTES, BK * 128, 1024, 2u);
         uint32_t stage = 0, phase = 0, first = 0u;
-        bool ok = true;
         for (int64_t kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+            if (!mbar_wait(&s->full[stage], phase, abort_flag, p.err)) break;
             tc_fence_after();
             const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
 #pragma unroll
@@ -1877,7 +1876,6 @@ csplit_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
             mma_commit(&s->empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        (void)ok;
         mma_commit(&s->acc_full);      // every MMA issued above has completed once it flips
     } else if (warp >= 2) {
         // ---- accumulator -> this CTA's float32 partial tile (all 128 rows;
