@@ -43,6 +43,7 @@ struct olc_matmul_plan {
     int splits;                  // SPLIT_K slices or SKINNY_M K-slices
     int split_hint;              // tuning override of the slice count (0 = automatic)
     int tc_variant;              // tuning override of the tensor-core tiling (0 = automatic)
+    int cluster_slices;          // GENERAL_TC FLOAT16 / BFLOAT16: K slices of the cluster split-K (1: none)
     // Gemm operator (rank-2, transA / transB, alpha, beta, broadcast C)
     int is_gemm;
     int trans_a, trans_b;
@@ -435,6 +436,7 @@ void free_workspace(olc_matmul_plan* p) {
 olc_status prepare_algorithm(olc_matmul_plan* p) {
     free_workspace(p);
     p->splits = 1;
+    p->cluster_slices = 1;
     Problem pr = make_problem(p, nullptr, nullptr, nullptr);
     const olc_dtype dt = p->dtype;
     if (p->algo == OLC_ALGO_SPLIT_K) {
@@ -449,6 +451,7 @@ olc_status prepare_algorithm(olc_matmul_plan* p) {
     } else if (p->algo == OLC_ALGO_GENERAL_TC && is_half(dt) && p->tc_variant == 0) {
         // few tiles: the cluster split-K's float32 partial tiles
         p->partial_bytes = tc_general_partial_bytes(dt, pr, p->sm_count);
+        if (p->partial_bytes > 0) p->cluster_slices = tc_general_csplit_ways(dt, pr, p->sm_count);
     } else if (p->algo == OLC_ALGO_GENERAL_SIMT) {
         p->splits = general_simt_pick_split(dt, pr, p->sm_count);
         if (p->splits > 1) {
@@ -1346,13 +1349,16 @@ size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan) {
 int olc_matmul_plan_describe(const olc_matmul_plan* plan, char* buf, size_t cap) {
     if (!plan) return -1;
     char tmp[512];
+    char slices[48] = "";
+    if (plan->cluster_slices > 1)
+        std::snprintf(slices, sizeof slices, " cluster_slices=%d", plan->cluster_slices);
     int n = std::snprintf(tmp, sizeof tmp,
                           "algo=%s dtype=%d M=%lld N=%lld K=%lld batch=%lld rows=%lld items=%lld "
-                          "collapsed_rank=%d splits=%d ws=%zu sms=%d%s",
+                          "collapsed_rank=%d splits=%d%s ws=%zu sms=%d%s",
                           olc_algorithm_name(plan->algo), (int)plan->dtype, (long long)plan->M,
                           (long long)plan->N, (long long)plan->K, (long long)plan->batch,
                           (long long)plan->rows, (long long)plan->items, plan->map.rank,
-                          plan->splits, plan->ws_bytes, plan->sm_count,
+                          plan->splits, slices, plan->ws_bytes, plan->sm_count,
                           plan->forced ? " forced" : "");
     if (buf && cap > 0) {
         std::strncpy(buf, tmp, cap - 1);

@@ -490,8 +490,10 @@ int olc_matmul_plan_launches(const olc_matmul_plan* plan);
  * none; staging buffers are not included. */
 size_t olc_matmul_plan_workspace_bytes(const olc_matmul_plan* plan);
 
-/* One-line description of the plan (algorithm, tile, grid, splits) written
- * into buf (NUL-terminated, truncated to cap).  Returns the full length. */
+/* One-line description of the plan (algorithm, type, shape after batch
+ * collapse and fold, K slices, the cluster split-K's slices where the general
+ * FP16 / BF16 tiles use it, workspace bytes, SM count) written into buf
+ * (NUL-terminated, truncated to cap).  Returns the full length. */
 int olc_matmul_plan_describe(const olc_matmul_plan* plan, char* buf, size_t cap);
 
 /* Static strings; never NULL. */

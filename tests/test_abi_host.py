@@ -414,10 +414,13 @@ def test_few_tile_half_products_take_the_cluster_split_k():
             assert p.algorithm == "general_tc"
             ws = p.workspace_bytes
             assert ws > 0 and ws % (2 * tile_bytes) == 0 and 2 * 2 <= ws // tile_bytes <= 2 * 8
+            # two tiles, each cut into the slices the description names
+            assert " cluster_slices=%d " % (ws // (2 * tile_bytes)) in p.describe()
         with Plan((32, 131072), (131072, 32), dt) as p:
             assert p.algorithm == "split_k"
         with Plan((8, 2048, 4096), (4096, 14336), dt) as p:
             assert p.algorithm == "general_tc" and p.workspace_bytes == 0
+            assert "cluster_slices" not in p.describe()
     with Plan((64, 8192), (8192, 512), "float32") as p:
         assert p.algorithm == "split_k"
     with Plan((64, 8192), (8192, 512), "bfloat16") as p:
