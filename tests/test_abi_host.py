@@ -88,6 +88,63 @@ def test_batch_strides_match_numpy_broadcast_views(a_shape, b_shape):
         assert nb == int(np.prod(batch, dtype=np.int64))
 
 
+def _random_shape_pair(rng):
+    """Shapes of rank 1-5 with small extents (0 included), K matched most of
+    the time and batch extents drawn so that broadcasts, matches and
+    mismatches all occur."""
+    ra, rb = int(rng.integers(1, 6)), int(rng.integers(1, 6))
+    k = int(rng.integers(0, 4))
+    a = [int(x) for x in rng.integers(0, 4, size=ra)]
+    b = [int(x) for x in rng.integers(0, 4, size=rb)]
+    if rng.random() < 0.85:
+        a[-1] = k
+        b[0 if rb == 1 else -2] = k
+    ba, bb = a[:-2], b[:-2]
+    for i in range(1, min(len(ba), len(bb)) + 1):
+        r = rng.random()
+        if r < 0.4:
+            bb[-i] = ba[-i]
+        elif r < 0.6:
+            bb[-i] = 1
+        elif r < 0.8:
+            ba[-i] = 1
+    return tuple(ba + a[len(ba):]), tuple(bb + b[len(bb):])
+
+
+def test_random_shapes_agree_with_numpy_matmul():
+    """A seeded sweep of 3,000 shape pairs: the plan accepts exactly the
+    pairs numpy.matmul accepts, with numpy's output shape; its batch strides
+    are numpy's broadcast-view strides (where the batch is not empty), and
+    collapse / fold keep every row (launch rows x items = M x batch)."""
+    rng = np.random.default_rng(20261202)
+    accepted = rejected = 0
+    for _ in range(3000):
+        a_shape, b_shape = _random_shape_pair(rng)
+        try:
+            want = np.matmul(np.zeros(a_shape, np.float32), np.zeros(b_shape, np.float32)).shape
+        except ValueError:
+            want = None
+        if want is None:
+            with pytest.raises(OlcError):
+                Plan(a_shape, b_shape, "float32")
+            rejected += 1
+            continue
+        accepted += 1
+        with Plan(a_shape, b_shape, "float32") as p:
+            assert p.output_shape == tuple(want), (a_shape, b_shape)
+            batch, sa_ref, sb_ref = _numpy_batch_strides(a_shape, b_shape)
+            shape, sa, sb = p.batch()
+            assert shape == tuple(batch)
+            m, n, k, nb = p.dims()
+            for d, e in enumerate(batch):
+                if e > 1 and nb > 0:    # an empty batch addresses no item
+                    assert sa[d] == sa_ref[d] and sb[d] == sb_ref[d], (a_shape, b_shape)
+            if m * n * nb > 0:
+                rows, items, _ = p.launch_shape()
+                assert rows * items == m * nb, (a_shape, b_shape)
+    assert accepted > 1000 and rejected > 300
+
+
 def test_batch_collapse_and_fold():
     # B shared by every item and A's items consecutive: folded into rows
     with Plan((8, 2048, 64), (64, 32), "float32") as p:
