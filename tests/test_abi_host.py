@@ -112,8 +112,9 @@ def _random_shape_pair(rng):
 
 
 def test_random_shapes_agree_with_numpy_matmul():
-    """A seeded sweep of 3,000 shape pairs: the plan accepts exactly the
-    pairs numpy.matmul accepts, with numpy's output shape; its batch strides
+    """A seeded sweep of 3,000 shape pairs: the plan (and the oracle's shape
+    rule) accept exactly the pairs numpy.matmul accepts, with numpy's output
+    shape; its batch strides
     are numpy's broadcast-view strides (where the batch is not empty), and
     collapse / fold keep every row (launch rows x items = M x batch)."""
     rng = np.random.default_rng(20261202)
@@ -127,9 +128,12 @@ def test_random_shapes_agree_with_numpy_matmul():
         if want is None:
             with pytest.raises(OlcError):
                 Plan(a_shape, b_shape, "float32")
+            with pytest.raises(oracle.ShapeError):
+                oracle.output_shape(a_shape, b_shape)
             rejected += 1
             continue
         accepted += 1
+        assert oracle.output_shape(a_shape, b_shape) == tuple(want), (a_shape, b_shape)
         with Plan(a_shape, b_shape, "float32") as p:
             assert p.output_shape == tuple(want), (a_shape, b_shape)
             batch, sa_ref, sb_ref = _numpy_batch_strides(a_shape, b_shape)
