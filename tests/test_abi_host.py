@@ -149,6 +149,45 @@ def test_random_shapes_agree_with_numpy_matmul():
     assert accepted > 1000 and rejected > 300
 
 
+def test_random_gemm_shapes_agree_with_numpy():
+    """A seeded sweep of 2,000 Gemm shape sets (transA / transB, C of rank
+    0-3): the plan and the oracle's shape rule accept exactly the sets whose
+    A' B' numpy can multiply and whose C numpy.broadcast_to takes to [M, N]
+    (ONNX's unidirectional broadcast), and the plan's output is [M, N]."""
+    rng = np.random.default_rng(20261203)
+    accepted = rejected = 0
+    for _ in range(2000):
+        m, n, k = (int(x) for x in rng.integers(0, 4, size=3))
+        ta, tb = bool(rng.integers(0, 2)), bool(rng.integers(0, 2))
+        kb = k if rng.random() < 0.85 else int(rng.integers(0, 4))
+        a_shape = (k, m) if ta else (m, k)
+        b_shape = (n, kb) if tb else (kb, n)
+        c_shape = None
+        if rng.random() < 0.8:
+            rank = int(rng.integers(0, 4))
+            c_shape = tuple(int(rng.choice([1, m, n, int(rng.integers(0, 4))])) for _ in range(rank))
+        try:
+            a = np.zeros(a_shape, np.float32)
+            b = np.zeros(b_shape, np.float32)
+            want = ((a.T if ta else a) @ (b.T if tb else b)).shape
+            if c_shape is not None:
+                np.broadcast_to(np.zeros(c_shape, np.float32), want)
+        except ValueError:
+            want = None
+        if want is None:
+            with pytest.raises(OlcError):
+                GemmPlan(a_shape, b_shape, "float32", ta, tb, 1.0, 1.0, c_shape)
+            with pytest.raises(oracle.ShapeError):
+                oracle.gemm_output_shape(a_shape, b_shape, ta, tb, c_shape)
+            rejected += 1
+            continue
+        accepted += 1
+        assert oracle.gemm_output_shape(a_shape, b_shape, ta, tb, c_shape)[:2] == want
+        with GemmPlan(a_shape, b_shape, "float32", ta, tb, 1.0, 1.0, c_shape) as p:
+            assert p.output_shape == want, (a_shape, b_shape, ta, tb, c_shape)
+    assert accepted > 1000 and rejected > 200
+
+
 def test_batch_collapse_and_fold():
     # B shared by every item and A's items consecutive: folded into rows
     with Plan((8, 2048, 64), (64, 32), "float32") as p:
