@@ -188,6 +188,40 @@ def test_random_gemm_shapes_agree_with_numpy():
     assert accepted > 1000 and rejected > 200
 
 
+def test_random_plans_choose_a_feasible_algorithm():
+    """A seeded sweep over shapes from tiny to projection-sized and every
+    element type: EMPTY exactly for empty outputs, ZERO_FILL exactly for
+    K = 0 with a non-empty output, the chosen algorithm can be forced again
+    (it is feasible) and stays chosen, plans that launch no product own no
+    workspace, and the description names the choice."""
+    rng = np.random.default_rng(20261204)
+    dtypes = ["float32", "float64", "float16", "bfloat16", "float8_e4m3fn", "float8_e5m2",
+              "float8_e4m3fnuz"]
+    ms = [0, 1, 2, 4, 16, 17, 64, 128, 300, 4096, 16384]
+    ks = [0, 8, 64, 520, 4096, 131072]
+    ns = [1, 8, 16, 24, 32, 64, 256, 4096, 14336]
+    seen = set()
+    for _ in range(600):
+        m, k, n = (int(rng.choice(v)) for v in (ms, ks, ns))
+        batch = [int(x) for x in rng.choice([1, 2, 3, 8], size=int(rng.integers(0, 3)))]
+        a_shape = tuple(batch + [m, k])
+        b_shape = (k, n) if rng.random() < 0.5 else tuple(batch + [k, n])
+        dt = str(rng.choice(dtypes))
+        with Plan(a_shape, b_shape, dt) as p:
+            algo = p.algorithm
+            seen.add(algo)
+            empty = int(np.prod(p.output_shape, dtype=np.int64)) == 0
+            assert (algo == "empty") == empty, (a_shape, b_shape, dt, algo)
+            assert (algo == "zero_fill") == (not empty and k == 0), (a_shape, b_shape, dt, algo)
+            assert p.describe().startswith("algo=%s " % algo)
+            if algo in ("empty", "zero_fill", "direct"):
+                assert p.workspace_bytes == 0
+            p.force(algo)
+            assert p.algorithm == algo
+    assert {"empty", "zero_fill", "direct", "skinny_m", "skinny_n", "split_k", "general_tc",
+            "general_simt"} <= seen
+
+
 def test_batch_collapse_and_fold():
     # B shared by every item and A's items consecutive: folded into rows
     with Plan((8, 2048, 64), (64, 32), "float32") as p:
