@@ -557,7 +557,9 @@ olc_status olc_debug_alu_rate(int kind, int64_t iters, void* stream, double* flo
  * It runs the SIMT split-K kernel (the plan path's kernel for FLOAT and
  * DOUBLE: partials per K slice, summed by the last-arriving block in slice
  * order) for every type, with the number of slices capped so the partials
- * fit the array; FLOAT16 / BFLOAT16 plans use a tensor-core kernel instead.
+ * fit the array (the plan path, by contrast, runs FLOAT16 / BFLOAT16 split-K
+ * products on the tensor cores; on [32, 131072] x [131072, 32] FLOAT16 this
+ * entry point takes about ten times as long).
  *
  *  dtype: OLC_FLOAT, OLC_DOUBLE, OLC_FLOAT16 or OLC_BFLOAT16.
  *  A, B, Y: caller-owned device pointers (M*K, K*N and M*N elements).
